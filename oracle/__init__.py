@@ -1,0 +1,170 @@
+"""CPU oracle for paged-KV attention (fp64, plain C) -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package.  The product library never does, and the two
+share no code.  ``build()`` compiles ``pkv_oracle.c`` with gcc (OpenMP over
+(request, head) pairs; each reduction stays sequential, so results do not
+depend on the thread count).
+
+All functions take numpy arrays; bf16 tensors are passed as their uint16 bit
+patterns.  Each mirrors a function of ``pkv_oracle.c``, whose comments cite the
+passages they follow.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pkv_oracle.c")
+_LIB = os.path.join(_HERE, "libpkv_oracle.so")
+
+OK, ERR_RANGE, ERR_CONTIG, ERR_CAPACITY, ERR_ARG = 0, 1, 2, 3, 4
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle shared library (portable flags: runs on x86 and Arm)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        P, I32, I64, D = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+        lib.pkvo_build_indices.argtypes = [P, I64, I64, I64, P, P, P, I32, I32, I64, P, P, I64, P, P, I32]
+        lib.pkvo_build_indices.restype = ctypes.c_int
+        lib.pkvo_store.argtypes = [P, I64, I64, I64, P, I64, P, I32]
+        lib.pkvo_store.restype = ctypes.c_int
+        lib.pkvo_decode.argtypes = [P, I32, I32, I32, I32, I32, P, I64, P, I64, I64,
+                                    P, I64, I64, I64, P, P, P, D, I32, I32, P, P, P, I32]
+        lib.pkvo_decode.restype = ctypes.c_int
+        lib.pkvo_lse_merge.argtypes = [I32, I64, I32, P, P, P, P]
+        lib.pkvo_lse_merge.restype = None
+        lib.pkvo_ragged_gather.argtypes = [P, P, I64, I64, I64, P, I64, I64, I64, P, P, P, I32,
+                                           P, P, I64, P]
+        lib.pkvo_ragged_gather.restype = ctypes.c_int
+        lib.pkvo_max_threads.argtypes = []
+        lib.pkvo_max_threads.restype = ctypes.c_int32
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _i32(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.int32)
+
+
+def max_threads() -> int:
+    return int(_load().pkvo_max_threads())
+
+
+def build_indices(req_to_token, req_pool_idx, seq_lens, page_size, num_pool_pages, kv_start=None,
+                  kv_indices_cap=None, bt_width=None):
+    """Returns (status, kv_indptr, kv_indices, kv_last_page_len, block_table)."""
+    r2t = _i32(req_to_token)
+    rpi, sl, ks = _i32(req_pool_idx), _i32(seq_lens), _i32(kv_start)
+    B = len(sl)
+    npages = -(-sl.astype(np.int64) // page_size)
+    cap = int(npages.sum()) if kv_indices_cap is None else int(kv_indices_cap)
+    width = int(npages.max()) if (bt_width is None and B) else int(bt_width or 0)
+    indptr = np.zeros(B + 1, dtype=np.int32)
+    indices = np.zeros(max(cap, 1), dtype=np.int32)
+    last = np.zeros(B, dtype=np.int32)
+    bt = np.zeros((B, max(width, 1)), dtype=np.int32)
+    st = _load().pkvo_build_indices(_ptr(r2t), r2t.shape[0], r2t.shape[1], r2t.shape[1], _ptr(rpi),
+                                    _ptr(sl), _ptr(ks), B, page_size, num_pool_pages, _ptr(indptr),
+                                    _ptr(indices), cap, _ptr(last), _ptr(bt), width)
+    return st, indptr, indices[:cap], last, bt[:, :width]
+
+
+def store(pool: np.ndarray, new_rows: np.ndarray, slot_mapping) -> int:
+    """In-place bitwise row store ``pool[slot_mapping[i]] = new_rows[i]`` (any dtype)."""
+    sm = _i32(slot_mapping)
+    assert pool.flags["C_CONTIGUOUS"] and new_rows.flags["C_CONTIGUOUS"]
+    row_bytes = new_rows[0].nbytes if len(new_rows) else 0
+    pool_row = pool.strides[0]
+    assert row_bytes <= pool_row
+    return _load().pkvo_store(_ptr(pool), pool.shape[0], pool_row, row_bytes, _ptr(new_rows),
+                              new_rows.strides[0] if len(new_rows) else 0, _ptr(sm), len(sm))
+
+
+def decode(q, k_pool, v_pool, req_to_token, req_pool_idx, seq_lens, scale, kv_start=None,
+           head_dim_v=None, t_begin=0, t_end=-1, req_mask=None, num_threads=0):
+    """fp64 decode attention.  q [B, Hq, Dqk] uint16 (bf16 bits); k_pool [slots, Hkv, Dqk]
+    (or [slots, Dqk] latent); v_pool [slots, Hkv, Dv] (or the latent pool again with
+    ``head_dim_v`` set).  Returns (status, out [B, Hq, Dv] float64, lse [B, Hq])."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k = np.ascontiguousarray(k_pool, dtype=np.uint16)
+    v = np.ascontiguousarray(v_pool, dtype=np.uint16)
+    B, hq, dqk = q.shape
+    if k.ndim == 2:       # latent pool: one kv head
+        hkv = 1
+        k_row = k.shape[1]
+    else:
+        hkv = k.shape[1]
+        k_row = k.shape[1] * k.shape[2]
+        assert k.shape[2] == dqk
+    if v.ndim == 2:
+        v_row = v.shape[1]
+        dv = int(head_dim_v) if head_dim_v is not None else v.shape[1]
+    else:
+        v_row = v.shape[1] * v.shape[2]
+        dv = v.shape[2]
+    r2t = _i32(req_to_token)
+    rpi, sl, ks = _i32(req_pool_idx), _i32(seq_lens), _i32(kv_start)
+    mask = None if req_mask is None else np.ascontiguousarray(req_mask, dtype=np.uint8)
+    out = np.zeros((B, hq, dv), dtype=np.float64)
+    lse = np.zeros((B, hq), dtype=np.float64)
+    st = _load().pkvo_decode(_ptr(q), B, hq, hkv, dqk, dv, _ptr(k), k_row, _ptr(v), v_row, k.shape[0],
+                             _ptr(r2t), r2t.shape[0], r2t.shape[1], r2t.shape[1], _ptr(rpi), _ptr(ks),
+                             _ptr(sl), float(scale), int(t_begin), int(t_end), _ptr(mask), _ptr(out),
+                             _ptr(lse), int(num_threads))
+    return st, out, lse
+
+
+def lse_merge(o_parts: np.ndarray, lse_parts: np.ndarray):
+    """o_parts [n, rows, dv], lse_parts [n, rows] (float64) -> (out [rows, dv], lse [rows])."""
+    o = np.ascontiguousarray(o_parts, dtype=np.float64)
+    l = np.ascontiguousarray(lse_parts, dtype=np.float64)
+    n, rows, dv = o.shape
+    out = np.zeros((rows, dv), dtype=np.float64)
+    lse = np.zeros(rows, dtype=np.float64)
+    _load().pkvo_lse_merge(n, rows, dv, _ptr(o), _ptr(l), _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def ragged_gather(k_pool: np.ndarray, v_pool: Optional[np.ndarray], req_to_token, req_pool_idx,
+                  seq_lens, kv_start=None, out_rows_cap=None):
+    """Returns (status, k_out, v_out, cu_seqlens); rows keep the pool's trailing shape."""
+    k = np.ascontiguousarray(k_pool)
+    v = None if v_pool is None else np.ascontiguousarray(v_pool)
+    r2t = _i32(req_to_token)
+    rpi, sl, ks = _i32(req_pool_idx), _i32(seq_lens), _i32(kv_start)
+    B = len(sl)
+    cap = int(sl.astype(np.int64).sum()) if out_rows_cap is None else int(out_rows_cap)
+    k_out = np.zeros((max(cap, 1),) + k.shape[1:], dtype=k.dtype)
+    v_out = None if v is None else np.zeros((max(cap, 1),) + v.shape[1:], dtype=v.dtype)
+    cu = np.zeros(B + 1, dtype=np.int32)
+    st = _load().pkvo_ragged_gather(_ptr(k), _ptr(v), k.shape[0], k.strides[0], k[0].nbytes,
+                                    _ptr(r2t), r2t.shape[0], r2t.shape[1], r2t.shape[1], _ptr(rpi),
+                                    _ptr(ks), _ptr(sl), B, _ptr(k_out), _ptr(v_out), cap, _ptr(cu))
+    return st, k_out[:cap], (None if v_out is None else v_out[:cap]), cu
