@@ -1,0 +1,428 @@
+"""Benchmark: paged decode attention over a paged KV cache on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one decode layer step of the whole hot path over one batch of the
+workload: pkv_build_indices (req_to_token -> page lists), pkv_store (one new
+K/V row per request), pkv_decode (split-KV attention + log-sum-exp merge); the
+encoder-decoder workload adds its cross-attention (page-aligned, or
+pkv_ragged_gather + varlen decode with --cross-mode gather).
+
+Prints ONE JSON line.  ``value`` is the step's algorithmic bytes (unique KV
+bytes read, q/out, page-table reads, stored rows; a shared prefix page counts
+once) per second of device time, with every input resident in HBM;
+``decode_steps_per_s`` the matching step rate.  ``roofline`` reports the decode
+launch (split kernel + merge) against the measured HBM copy bandwidth,
+``e2e`` the same metric through the host-buffer API (pinned h2d of the step
+inputs and d2h of the outputs inside the timed region), ``cpu_baseline`` the
+fp64 CPU oracle timed on a bounded sample of the same workload on this host.
+
+With N > 1 (torchrun), every rank runs its own replica of the workload on its
+own GPU: requests are independent, so the work shards with no collective on
+the data path (weak scaling); the barrier and max-over-ranks timing use
+torch.distributed only for timing.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention KV-read GB/s (frac of HBM peak) and decode steps/s"
+DEFAULT_WORKLOAD = "llama3_8b"
+L2_BYTES = 129 * 10**6
+WORKLOAD_TEXT = {
+    "tiny_gqa": "tiny GQA decode: 4 requests, cached lengths {17,64,100,255}, 16 q / 8 kv heads x 128, page_size 1",
+    "qwen3_0p6b": "Qwen3-0.6B-shaped decode: batch 32, cached lengths U[1,4096], 16 q / 8 kv heads x 128, page_size 16, 200k-token pool",
+    "llama3_8b": "Llama-3-8B-shaped large-batch decode: batch 256, cached lengths log-U[128,32768], 32 q / 8 kv heads x 128, page_size 64, groups of 16 share a 2048-token prefix",
+    "whisper_encdec": "Whisper-large-shaped encoder-decoder step: batch 64, decoder lengths U[1,448] + cross-attention over 1500 encoder tokens, 20 heads x 64, page_size 16",
+    "deepseek_v3_mla": "DeepSeek-V3-shaped MLA decode: batch 128, cached lengths U[512,16384], 128 q heads over a 512+64 latent, page_size 64",
+}
+
+
+# ---------------------------------------------------------------- accounting
+def step_bytes(wl, cross_mode="paged"):
+    """Algorithmic bytes of one step and of its decode launches (unique slots once)."""
+    r2t = wl.req_to_token.numpy()
+    rpi = wl.req_pool_idx.numpy().astype(np.int64)
+    if wl.kind == "mla":
+        kv_row = wl.head_dim_qk * 2                     # one latent row serves K and V
+        store_row = kv_row
+    else:
+        kv_row = 2 * wl.num_kv_heads * wl.head_dim_qk * 2
+        store_row = kv_row
+    total = 0
+    decode = 0
+    for p in wl.problems:
+        lens = p.seq_lens.numpy().astype(np.int64)
+        starts = p.kv_start.numpy().astype(np.int64)
+        slots = np.concatenate([r2t[rpi[b], starts[b]:starts[b] + lens[b]] for b in range(wl.batch)]) \
+            if wl.batch else np.zeros(0, np.int64)
+        uniq = np.unique(slots).size
+        q_out = wl.batch * wl.num_q_heads * (wl.head_dim_qk + wl.head_dim_v) * 2
+        pages = int((-(-lens // wl.page_size)).sum())
+        dec = uniq * kv_row + q_out + pages * 4
+        decode += dec
+        if p.name == "cross" and cross_mode == "gather":
+            total += dec + 2 * int(lens.sum()) * kv_row + int(lens.sum()) * 4
+        else:
+            total += dec + int(lens.sum()) * 4 + pages * 4        # table read + page-list write
+        if p.stores:
+            total += 2 * wl.batch * store_row                   # read new rows + write pool rows
+    return total, decode
+
+
+def unique_keys(wl):
+    r2t = wl.req_to_token.numpy()
+    rpi = wl.req_pool_idx.numpy().astype(np.int64)
+    out = {}
+    for p in wl.problems:
+        lens = p.seq_lens.numpy().astype(np.int64)
+        starts = p.kv_start.numpy().astype(np.int64)
+        slots = np.concatenate([r2t[rpi[b], starts[b]:starts[b] + lens[b]] for b in range(wl.batch)])
+        out[p.name] = (int(lens.sum()), int(np.unique(slots).size))
+    return out
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1961.1)), float(d.get("bf16_tflops_sustained", 1733.8)), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def decode_traffic(workload):
+    """Per-launch DRAM bytes of the decode launch from a committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    src = os.path.join(ROOT, "paged_kv_cache_req_gb300", "csrc", d.get("source", "decode_gqa.cu"))
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    ent = d.get("workloads", {}).get(workload)
+    if not ent or ent.get("source_sha") != h:
+        return None
+    return ent.get("bytes_per_launch")
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        rows = []
+        with open(self.tmp.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                    rows.append(parts)
+        os.unlink(self.tmp.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())
+                if any(r[3].replace(".", "").isdigit() for r in rows) else None}
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+def oracle_sample_run(wl, budget_key_heads, seed=0, num_threads=0):
+    """Times the fp64 oracle (store + decode) on a sample of the workload's requests.
+
+    The sampled requests keep the recipe's lengths and page layout; their slots
+    are relabelled into a compact host pool whose values are drawn on the CPU.
+    Returns (seconds, algorithmic bytes of the sample, description, threads).
+    """
+    import oracle
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(wl.batch)
+    r2t = wl.req_to_token.numpy()
+    rpi = wl.req_pool_idx.numpy().astype(np.int64)
+    per_req = np.zeros(wl.batch, dtype=np.int64)
+    for p in wl.problems:
+        per_req += p.seq_lens.numpy().astype(np.int64) * wl.num_q_heads
+    sample, acc = [], 0
+    for b in order:
+        sample.append(int(b))
+        acc += int(per_req[b])
+        if acc >= budget_key_heads:
+            break
+    sample.sort()
+    gen = torch.Generator().manual_seed(7 + seed)
+    secs = 0.0
+    nbytes = 0
+    kv_row = (wl.head_dim_qk * 2) if wl.kind == "mla" else 2 * wl.num_kv_heads * wl.head_dim_qk * 2
+    for p in wl.problems:
+        lens = p.seq_lens.numpy().astype(np.int64)[sample]
+        starts = p.kv_start.numpy().astype(np.int64)[sample]
+        rows = [r2t[rpi[b], s:s + L].astype(np.int64) for b, s, L in zip(sample, starts, lens)]
+        allslots = np.unique(np.concatenate(rows))
+        table = np.zeros((len(sample) + 1, max(int(lens.max()), 1)), dtype=np.int32)
+        for i, r in enumerate(rows):
+            table[i + 1, :len(r)] = np.searchsorted(allslots, r)
+        shape = (len(allslots), wl.head_dim_qk) if wl.kind == "mla" else (len(allslots), wl.num_kv_heads, wl.head_dim_qk)
+        k = torch.randn(shape, generator=gen).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        v = k if wl.kind == "mla" else torch.randn(shape, generator=gen).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        q = torch.randn((len(sample), wl.num_q_heads, wl.head_dim_qk), generator=gen).to(torch.bfloat16) \
+            .view(torch.int16).numpy().view(np.uint16)
+        rpi_c = np.arange(1, len(sample) + 1, dtype=np.int32)
+        t0 = time.perf_counter()
+        if p.stores:
+            new_rows = k[:len(sample)].copy()
+            oracle.store(k, new_rows, np.searchsorted(allslots, [r[-1] for r in rows]).astype(np.int32))
+        st, out, lse = oracle.decode(q, k, v, table, rpi_c, lens, wl.sm_scale,
+                                     head_dim_v=wl.head_dim_v if wl.kind == "mla" else None,
+                                     num_threads=num_threads)
+        secs += time.perf_counter() - t0
+        nbytes += len(allslots) * kv_row + len(sample) * wl.num_q_heads * (wl.head_dim_qk + wl.head_dim_v) * 2
+    desc = "%d of %d requests (%d key x q-head pairs), compact host pool" % (len(sample), wl.batch, int(per_req[sample].sum()))
+    return secs, nbytes, desc, oracle.max_threads() if num_threads <= 0 else num_threads
+
+
+# ---------------------------------------------------------------- arms
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from paged_kv_cache_req_gb300.workloads import make_workload
+    wl = make_workload(args.workload)
+    import oracle
+    oracle.build()
+    budget = args.ref_key_heads
+    for _ in range(args.warmup):
+        oracle_sample_run(wl, budget // 4, seed=0)
+    times, total_bytes, desc, threads = [], 0, "", 0
+    for i in range(args.steps):
+        secs, nb, desc, threads = oracle_sample_run(wl, budget, seed=i)
+        times.append(secs)
+        total_bytes += nb
+    value = total_bytes / sum(times) / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * sum(times) / len(times), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": "each step: " + desc},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from paged_kv_cache_req_gb300 import build
+    if rank == 0 or world == 1:
+        build.build()
+    if dist is not None:
+        dist.barrier()
+    from paged_kv_cache_req_gb300.engine import DecodeStep
+    from paged_kv_cache_req_gb300.workloads import make_workload
+
+    wl = make_workload(args.workload, seed=args.seed)
+    step = DecodeStep(wl, device="cuda", cross_mode=args.cross_mode, kv_chunk=args.kv_chunk, seed=args.seed)
+    total_bytes, decode_bytes = step_bytes(wl, args.cross_mode)
+    flush = total_bytes < 4 * L2_BYTES
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda") if flush else None
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    if step.check_errors():
+        raise SystemExit("device error flags raised: %d" % step.check_errors())
+
+    # ---- device-timed steps (inputs resident) ----
+    n_dec = len([p for p in step.problems.values()])
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    dev_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_dec)]
+              for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        if flush:
+            flush_buf.zero_()
+        ev[i][0].record(stream)
+        for j, (name, pb) in enumerate(step.problems.items()):
+            if pb.gather:
+                step.gather(name)
+            else:
+                step.build_indices(name)
+            if pb.spec.stores:
+                step.store(name)
+            dev_ev[i][j][0].record(stream)
+            step.decode(name)
+            dev_ev[i][j][1].record(stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    if dist is not None:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    dec_ms = [sum(a.elapsed_time(b) for a, b in row) for row in dev_ev]
+    tot_ms = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([tot_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_ms = float(t.item())
+    ms_per_step = tot_ms / args.steps
+    value = world * total_bytes * args.steps / (tot_ms / 1e3) / 1e9
+    if step.check_errors():
+        raise SystemExit("device error flags raised: %d" % step.check_errors())
+
+    # ---- end to end through the host-buffer API ----
+    h_in, h_out = step.host_step_tensors()
+    h2d = DecodeStep.bytes_of(h_in)
+    d2h = DecodeStep.bytes_of(h_out)
+    for _ in range(2):
+        step.run_from_host(h_in, h_out)
+    torch.cuda.synchronize()
+    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        if flush:
+            flush_buf.zero_()
+        e_ev[i][0].record(stream)
+        step.run_from_host(h_in, h_out)
+        e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e_ms = sum(a.elapsed_time(b) for a, b in e_ev)
+    if dist is not None:
+        t = torch.tensor([e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e_ms = float(t.item())
+    e2e_value = world * total_bytes * args.steps / (e_ms / 1e3) / 1e9
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    hbm, _, _, peak_kind = measured_peaks()
+    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    achieved = decode_bytes / (dec_avg_ms / 1e3) / 1e9
+    traffic = decode_traffic(args.workload)
+    launches = step.launches_per_step() * args.steps
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        secs, nb, desc, threads = oracle_sample_run(wl, args.cpu_key_heads, seed=0)
+        cpu = {"value": round(nb / secs / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": desc + "; %.1f s of fp64 store+decode on %d host threads" % (secs, threads),
+               "host_cpus": os.cpu_count()}
+
+    keys = unique_keys(wl)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "accumulate": "fp32", "data": "synthetic",
+        "decode_steps_per_s": round(world * 1e3 / ms_per_step, 2),
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "batch": wl.batch,
+                   "cross_mode": args.cross_mode if wl.kind == "gqa" and len(wl.problems) > 1 else None,
+                   "keys_per_step": {k: v[0] for k, v in keys.items()},
+                   "unique_keys_per_step": {k: v[1] for k, v in keys.items()},
+                   "algorithmic_bytes_per_step": total_bytes,
+                   "l2": "flushed between steps (2x L2 write)" if flush else "inputs larger than L2",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": "pkv_decode (split kernel + merge)",
+                     "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "peak_kind": peak_kind,
+                     "frac_of_8TBs": round(achieved / 8000.0, 4),
+                     "algorithmic_bytes_per_launch": decode_bytes, "avg_launch_ms": round(dec_avg_ms, 4),
+                     "traffic": traffic},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e_ms / args.steps, 4)},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--cross-mode", default="paged", choices=["paged", "gather"])
+    ap.add_argument("--kv-chunk", type=int, default=0)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-key-heads", type=int, default=12_000_000,
+                    help="size of the CPU-oracle sample in (key, query head) pairs")
+    ap.add_argument("--ref-key-heads", type=int, default=4_000_000,
+                    help="per-step sample of the reference arm in (key, query head) pairs")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,235 @@
+/*
+ * pkv.h -- C ABI of libpkv: attention over a paged KV cache on one GB300 GPU (sm_103a).
+ *
+ * The KV cache of every in-flight request lives in one preallocated pool of
+ * fixed-size pages; a request's token positions map to pool slots through the
+ * token-granular table req_to_token[row, position] ("Enabling Encoder-Decoder
+ * Models on Intel XPU in SGLang: A KV-Cache Story", section "How SGLang stores
+ * the KV cache: two pools and a page size").  The library offers the four
+ * steps of a decode layer over that cache:
+ *
+ *   pkv_build_indices  req_to_token -> per-request page lists (CSR and/or a -1 padded table)
+ *   pkv_store          scatter this step's new K/V rows into their pool slots
+ *   pkv_decode         one query token per request attending through the page table
+ *                      (GQA/MHA, or MLA over a latent pool), split-KV + log-sum-exp merge
+ *   pkv_ragged_gather  pack a request's token-granular K/V into a contiguous varlen buffer
+ *
+ * Conventions shared by every call
+ *   - Every pointer is caller-owned DEVICE memory unless stated otherwise.  The
+ *     library allocates nothing and keeps no state between calls except a
+ *     per-device cache of the SM count.
+ *   - Every call is asynchronous on the caller's stream and never synchronizes.
+ *   - Tensors are row-major with the last dimension contiguous.  K/V/q/out are
+ *     bf16; tables are int32; lse is fp32.
+ *   - Errors the host can see (null pointers, bad sizes, unsupported shapes,
+ *     misalignment) return a status before anything is launched;
+ *     pkv_last_error() then gives a one-line reason (thread-local).
+ *   - Errors only the device can see (a slot or page outside the pool, a page
+ *     whose tokens are not contiguous, an output too small) are OR-ed into the
+ *     caller's int32 *err_flags on the device as PKV_DEVERR_* bits.  The kernel
+ *     never reads or writes outside the buffers it was given: the offending
+ *     row or page is skipped (reads of it return zeros) and nothing traps.
+ *     The outputs of a request that raised a flag are unspecified.
+ *     err_flags is never cleared by the library.
+ *   - A request with no keys (L = 0) produces out = 0 and lse = -inf rather
+ *     than a launch failure (the guard of "Approach 2: gather and go ragged").
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *pkv_stream_t;
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1, /* null pointer, negative size, inconsistent shapes, misaligned buffer */
+    PKV_ERR_UNSUPPORTED = 2, /* a shape the kernels are not built for (see each call) */
+    PKV_ERR_CAPACITY = 3,    /* a buffer the host can size is too small (workspace) */
+    PKV_ERR_CUDA = 4         /* a CUDA runtime call or launch failed */
+} pkv_status;
+
+/* Device-side error bits OR-ed into *err_flags. */
+#define PKV_DEVERR_RANGE 1    /* slot, page, row or position outside its pool or table */
+#define PKV_DEVERR_CONTIG 2   /* a page's tokens are not page-aligned and contiguous */
+#define PKV_DEVERR_CAPACITY 4 /* an output had too little room; the excess was not written */
+
+#define PKV_ABI_VERSION 1
+
+/*
+ * pkv_build_indices -- page lists from the token-granular table.
+ *
+ * Defined by "From slots to a page table: how attention reads the cache" (the
+ * page of position t is req_to_token[row, t - t % ps] / ps, valid because the
+ * paged allocator keeps a request's tokens contiguous inside each page) and by
+ * the AttentionBackend notes, sections "kv_indptr and kv_indices" (CSR) and
+ * "init_forward_metadata" (the FlashMLA table [B, cdiv(max L, ps)] filled with
+ * -1 past each request's last page).
+ *
+ * For request b (row r = req_pool_idx[b], start s = kv_start ? kv_start[b] : 0,
+ * L = seq_lens[b] keys, n = ceil(L / ps) pages):
+ *   kv_indptr[b+1]              = kv_indptr[b] + n,   kv_indptr[0] = 0
+ *   kv_indices[kv_indptr[b]+p]  = req_to_token[r, s + p*ps] / ps          (p < n)
+ *   kv_last_page_len[b]         = L - (n-1)*ps, or 0 when L = 0
+ *   block_table[b, p]           = the same page for p < n, -1 for n <= p < block_table_width
+ * Every position is checked: each page's first slot must be a multiple of ps,
+ * the following ones must continue it (PKV_DEVERR_CONTIG otherwise) and every
+ * page must lie in [0, num_pool_pages) (PKV_DEVERR_RANGE).  A row or region
+ * outside the table raises PKV_DEVERR_RANGE and the request gets n = 0.  Pages
+ * beyond kv_indices_cap or block_table_width raise PKV_DEVERR_CAPACITY and are
+ * not written.
+ *
+ * req_to_token  int32 [r2t_rows, r2t_row_stride], r2t_width valid columns per row
+ * req_pool_idx, seq_lens  int32 [batch];  kv_start  int32 [batch] or NULL
+ * page_size     >= 1 (any value)
+ * Outputs (each group nullable, not both): kv_indptr [batch+1], kv_indices
+ * [kv_indices_cap], kv_last_page_len [batch]; block_table [batch, block_table_width].
+ * err_flags     int32 on the device, required.
+ */
+pkv_status pkv_build_indices(const int32_t *req_to_token, int64_t r2t_rows, int64_t r2t_row_stride,
+                             int64_t r2t_width, const int32_t *req_pool_idx, const int32_t *seq_lens,
+                             const int32_t *kv_start, int32_t batch, int32_t page_size,
+                             int64_t num_pool_pages, int32_t *kv_indptr, int32_t *kv_indices,
+                             int64_t kv_indices_cap, int32_t *kv_last_page_len, int32_t *block_table,
+                             int32_t block_table_width, int32_t *err_flags, pkv_stream_t stream);
+
+/*
+ * pkv_store -- write this step's new K/V rows into their pool slots.
+ *
+ * Defined by the mini-sglang handbook, "The KV pool" (store_kv / store_cache:
+ * k_cache[out_loc[i]] = k[i], the same for v; pure indexed movement, one warp
+ * per token and 16 bytes per move).  The copy is bitwise.
+ *
+ * k_pool        bf16 rows of kv_heads*head_dim_k elements, k_row_stride elements apart,
+ *               num_slots rows (an MLA latent pool: kv_heads = 1, head_dim_k = 576)
+ * v_pool        bf16 rows of kv_heads*head_dim_v elements, v_row_stride apart; NULL for
+ *               a latent pool (then v_new must be NULL too)
+ * k_new, v_new  bf16 [n_tokens, kv_heads, head_dim] contiguous
+ * slot_mapping  int32 [n_tokens]; a negative entry is a padded token and is skipped;
+ *               an entry >= num_slots raises PKV_DEVERR_RANGE and is skipped.
+ * Duplicate slots in one call give an unspecified winner.
+ */
+pkv_status pkv_store(void *k_pool, void *v_pool, int64_t num_slots, int64_t k_row_stride,
+                     int64_t v_row_stride, int32_t kv_heads, int32_t head_dim_k, int32_t head_dim_v,
+                     const void *k_new, const void *v_new, const int32_t *slot_mapping,
+                     int32_t n_tokens, int32_t *err_flags, pkv_stream_t stream);
+
+/* pkv_decode: which attention and which page-table form. */
+typedef enum pkv_kind {
+    PKV_KIND_GQA = 0, /* Hq query heads over Hkv kv heads; kv head of query head h is h / (Hq/Hkv) */
+    PKV_KIND_MLA = 1  /* one latent kv head: K = the whole latent row, V = its first head_dim_v entries */
+} pkv_kind;
+
+typedef enum pkv_layout {
+    PKV_LAYOUT_CSR = 0,         /* kv_indptr / kv_indices / kv_last_page_len */
+    PKV_LAYOUT_BLOCK_TABLE = 1, /* block_table [B, block_table_width] + seq_lens */
+    PKV_LAYOUT_VARLEN = 2       /* contiguous rows: keys of b are rows cu_seqlens[b] .. cu_seqlens[b+1]-1 */
+} pkv_layout;
+
+typedef struct pkv_decode_args {
+    int32_t kind;              /* pkv_kind */
+    int32_t layout;            /* pkv_layout */
+    int32_t batch;             /* B >= 0 */
+    int32_t num_q_heads;       /* Hq */
+    int32_t num_kv_heads;      /* Hkv (must be 1 for MLA) */
+    int32_t head_dim_qk;       /* GQA: 64 or 128; MLA: 576 */
+    int32_t head_dim_v;        /* GQA: equal to head_dim_qk; MLA: 512 */
+    int32_t page_size;         /* power of two, 1..1024 (CSR / block table); ignored for VARLEN */
+    float sm_scale;            /* softmax scale, e.g. 1/sqrt(head_dim) */
+    int32_t max_seq_len;       /* host upper bound on every request's key count; sizes the split plan */
+    int32_t kv_chunk;          /* keys per split, a multiple of 64; 0 lets the library choose */
+    int32_t block_table_width; /* columns of block_table (BLOCK_TABLE) */
+    int64_t num_slots;         /* rows of the pool(s) (VARLEN: rows of the contiguous buffer) */
+    int64_t k_row_stride;      /* elements between consecutive rows of k_pool */
+    int64_t v_row_stride;      /* elements between consecutive rows of v_pool (ignored for MLA) */
+    int64_t kv_indices_len;    /* CSR: entries of kv_indices (a kv_indptr value beyond it is an error) */
+    const void *q;             /* bf16 [B, Hq, head_dim_qk] contiguous */
+    const void *k_pool;        /* bf16 rows [Hkv, head_dim_qk] (MLA: the latent row) */
+    const void *v_pool;        /* bf16 rows [Hkv, head_dim_v]; NULL for MLA */
+    const int32_t *kv_indptr;        /* CSR [B+1] */
+    const int32_t *kv_indices;       /* CSR pages */
+    const int32_t *kv_last_page_len; /* CSR [B] */
+    const int32_t *block_table;      /* BLOCK_TABLE [B, block_table_width], -1 padded */
+    const int32_t *seq_lens;         /* BLOCK_TABLE [B] */
+    const int32_t *cu_seqlens;       /* VARLEN [B+1] */
+    void *out;                 /* bf16 [B, Hq, head_dim_v] */
+    float *lse;                /* fp32 [B, Hq], natural log of the softmax denominator; nullable */
+} pkv_decode_args;
+
+/*
+ * pkv_decode -- decode attention through the page table.
+ *
+ * For each request b with L keys (CSR: (n-1)*ps + kv_last_page_len[b] for n
+ * pages, BLOCK_TABLE: seq_lens[b], VARLEN: cu_seqlens[b+1]-cu_seqlens[b]) and
+ * query head h, key t lives at slot page_table[b][t / ps] * ps + t % ps
+ * ("From slots to a page table: how attention reads the cache"; AttentionBackend
+ * notes, "kv_indptr and kv_indices": base = page_id * page_size, address = base
+ * + offset) and
+ *     out[b,h,:] = softmax_t(sm_scale * q[b,h,:] . K[slot_t, kh, :]) V[slot_t, kh, :]
+ *     lse[b,h]   = ln sum_t exp(sm_scale * q[b,h,:] . K[slot_t, kh, :])
+ * with kh = h / (Hq/Hkv) for GQA and kh = 0 for MLA.  L = 0 gives out = 0,
+ * lse = -inf.  Long requests are cut into splits of kv_chunk keys whose
+ * partial results are combined by a log-sum-exp merge (the num_splits of the
+ * FlashMLA metadata, AttentionBackend notes, "init_forward_metadata").
+ * Arithmetic: bf16 inputs, fp32 accumulation and softmax, bf16 output rounded
+ * to nearest even.
+ *
+ * workspace     device scratch of at least pkv_decode_workspace_size(args) bytes,
+ *               256-byte aligned; its contents need no initialisation.
+ * Supported:    GQA head_dim 64 or 128 with Hq/Hkv in {1,2,4,8,16};
+ *               MLA head_dim_qk 576, head_dim_v 512, Hq a multiple of 64.
+ * A page id outside the pool or a -1 inside a request's page range raises
+ * PKV_DEVERR_RANGE; that key reads as zeros.  A kv_indptr range outside
+ * [0, kv_indices_len], a kv_last_page_len outside [1, page_size] or a negative
+ * length raises PKV_DEVERR_RANGE and the request is treated as empty.  A
+ * request longer than max_seq_len raises PKV_DEVERR_CAPACITY and only its
+ * first keys (up to the split plan's reach) are attended.
+ */
+pkv_status pkv_decode(const pkv_decode_args *args, void *workspace, size_t workspace_bytes,
+                      int32_t *err_flags, pkv_stream_t stream);
+
+/* Workspace bytes pkv_decode needs for these arguments (0 on invalid arguments). */
+size_t pkv_decode_workspace_size(const pkv_decode_args *args);
+
+/*
+ * pkv_ragged_gather -- pack token-granular K/V into contiguous varlen buffers.
+ *
+ * Defined by "Approach 2: gather and go ragged (variable-length
+ * FlashAttention)": the valid columns of each row (t < L_b), in request order,
+ * give the flat slot list; the K and V rows at those slots are copied into
+ * contiguous buffers addressed by cumulative lengths.
+ *   cu_seqlens[0] = 0,  cu_seqlens[b+1] = cu_seqlens[b] + seq_lens[b]
+ *   k_out[cu_seqlens[b] + t] = k_pool[req_to_token[req_pool_idx[b], s_b + t]]   (t < seq_lens[b])
+ * and the same for v.  Rows are row_elems bf16 elements (Hkv * head_dim),
+ * pool rows pool_row_stride elements apart, output rows packed.  Rows beyond
+ * out_rows_cap raise PKV_DEVERR_CAPACITY and are not written.  max_seq_len is
+ * a host upper bound on seq_lens (grid sizing only; longer requests are still
+ * copied whole).  v_pool / v_out may both be NULL (latent pool).
+ */
+pkv_status pkv_ragged_gather(const void *k_pool, const void *v_pool, int64_t num_slots,
+                             int64_t pool_row_stride, int64_t row_elems, const int32_t *req_to_token,
+                             int64_t r2t_rows, int64_t r2t_row_stride, int64_t r2t_width,
+                             const int32_t *req_pool_idx, const int32_t *kv_start,
+                             const int32_t *seq_lens, int32_t batch, int32_t max_seq_len, void *k_out,
+                             void *v_out, int64_t out_rows_cap, int32_t *cu_seqlens,
+                             int32_t *err_flags, pkv_stream_t stream);
+
+/* Static description of a status code. */
+const char *pkv_status_string(pkv_status status);
+
+/* One-line reason for the last non-OK status returned on this host thread ("" if none). */
+const char *pkv_last_error(void);
+
+/* PKV_ABI_VERSION of the loaded library. */
+int32_t pkv_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PKV_H_ */

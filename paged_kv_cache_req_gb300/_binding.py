@@ -1,0 +1,194 @@
+"""Thin ctypes binding over libpkv.so: argument marshalling only.
+
+Every function has the name of the C entry point it calls (see include/pkv.h),
+takes torch tensors that already live on the GPU, passes their data pointers,
+sizes and the current CUDA stream, and raises :class:`PkvError` on a non-OK
+status.  No step of the computation runs here: there is no CPU fallback, and a
+missing or unloadable libpkv.so raises at import time.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpkv.so")
+
+PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CAPACITY, PKV_ERR_CUDA = range(5)
+PKV_DEVERR_RANGE, PKV_DEVERR_CONTIG, PKV_DEVERR_CAPACITY = 1, 2, 4
+PKV_KIND_GQA, PKV_KIND_MLA = 0, 1
+PKV_LAYOUT_CSR, PKV_LAYOUT_BLOCK_TABLE, PKV_LAYOUT_VARLEN = 0, 1, 2
+
+EXPORTED_SYMBOLS = ("pkv_build_indices", "pkv_store", "pkv_decode", "pkv_decode_workspace_size",
+                    "pkv_ragged_gather", "pkv_status_string", "pkv_last_error", "pkv_abi_version")
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        super().__init__("%s failed: %s (%s)" % (where, _status_name(status), detail))
+        self.status = status
+
+
+def _status_name(st: int) -> str:
+    return {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "buffer too small",
+            4: "CUDA error"}.get(st, "status %d" % st)
+
+
+class DecodeArgs(ctypes.Structure):
+    """Mirror of ``pkv_decode_args`` (field order and types must match include/pkv.h)."""
+    _fields_ = [
+        ("kind", ctypes.c_int32), ("layout", ctypes.c_int32), ("batch", ctypes.c_int32),
+        ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+        ("head_dim_qk", ctypes.c_int32), ("head_dim_v", ctypes.c_int32), ("page_size", ctypes.c_int32),
+        ("sm_scale", ctypes.c_float), ("max_seq_len", ctypes.c_int32), ("kv_chunk", ctypes.c_int32),
+        ("block_table_width", ctypes.c_int32), ("num_slots", ctypes.c_int64),
+        ("k_row_stride", ctypes.c_int64), ("v_row_stride", ctypes.c_int64),
+        ("kv_indices_len", ctypes.c_int64),
+        ("q", ctypes.c_void_p), ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+        ("kv_indptr", ctypes.c_void_p), ("kv_indices", ctypes.c_void_p),
+        ("kv_last_page_len", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
+        ("seq_lens", ctypes.c_void_p), ("cu_seqlens", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+    ]
+
+
+def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError("libpkv.so is not built (%s); run `python -m paged_kv_cache_req_gb300.build`" % path)
+    lib = ctypes.CDLL(path)
+    P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    lib.pkv_build_indices.argtypes = [P, I64, I64, I64, P, P, P, I32, I32, I64, P, P, I64, P, P, I32, P, P]
+    lib.pkv_store.argtypes = [P, P, I64, I64, I64, I32, I32, I32, P, P, P, I32, P, P]
+    lib.pkv_decode.argtypes = [ctypes.POINTER(DecodeArgs), P, SZ, P, P]
+    lib.pkv_decode_workspace_size.argtypes = [ctypes.POINTER(DecodeArgs)]
+    lib.pkv_decode_workspace_size.restype = SZ
+    lib.pkv_ragged_gather.argtypes = [P, P, I64, I64, I64, P, I64, I64, I64, P, P, P, I32, I32, P, P, I64, P, P, P]
+    for f in ("pkv_build_indices", "pkv_store", "pkv_decode", "pkv_ragged_gather"):
+        getattr(lib, f).restype = ctypes.c_int
+    lib.pkv_status_string.argtypes = [ctypes.c_int]
+    lib.pkv_status_string.restype = ctypes.c_char_p
+    lib.pkv_last_error.argtypes = []
+    lib.pkv_last_error.restype = ctypes.c_char_p
+    lib.pkv_abi_version.argtypes = []
+    lib.pkv_abi_version.restype = ctypes.c_int32
+    return lib
+
+
+_lib = load_library()
+
+
+def _check(st: int, where: str):
+    if st != PKV_OK:
+        raise PkvError(st, where, _lib.pkv_last_error().decode())
+
+
+def _p(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libpkv takes device tensors only (got a %s tensor)" % t.device)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _i32(t: Optional[torch.Tensor], name: str):
+    if t is not None and (t.dtype != torch.int32 or not t.is_contiguous()):
+        raise ValueError("%s must be a contiguous int32 tensor" % name)
+    return t
+
+
+def pkv_build_indices(req_to_token, req_pool_idx, seq_lens, page_size, num_pool_pages, err_flags,
+                      kv_start=None, kv_indptr=None, kv_indices=None, kv_last_page_len=None,
+                      block_table=None, stream=None):
+    _i32(req_to_token, "req_to_token")
+    B = seq_lens.numel()
+    cap = kv_indices.numel() if kv_indices is not None else 0
+    bt_w = block_table.shape[1] if block_table is not None else 0
+    st = _lib.pkv_build_indices(_p(req_to_token), req_to_token.shape[0], req_to_token.stride(0),
+                                req_to_token.shape[1], _p(_i32(req_pool_idx, "req_pool_idx")),
+                                _p(_i32(seq_lens, "seq_lens")), _p(_i32(kv_start, "kv_start")), B,
+                                int(page_size), int(num_pool_pages), _p(kv_indptr), _p(kv_indices), cap,
+                                _p(kv_last_page_len), _p(block_table), bt_w, _p(err_flags), _stream(stream))
+    _check(st, "pkv_build_indices")
+
+
+def pkv_store(k_pool, v_pool, k_new, v_new, slot_mapping, err_flags, stream=None):
+    """k_pool [slots, Hkv, D] (or latent [slots, Dl]); k_new [n, Hkv, D] (or [n, Dl])."""
+    n = slot_mapping.numel()
+    if k_pool.dim() == 2:
+        hkv, dk = 1, k_pool.shape[1]
+    else:
+        hkv, dk = k_pool.shape[1], k_pool.shape[2]
+    dv = v_pool.shape[-1] if v_pool is not None else 0
+    st = _lib.pkv_store(_p(k_pool), _p(v_pool), k_pool.shape[0], k_pool.stride(0),
+                        v_pool.stride(0) if v_pool is not None else 0, hkv, dk, dv, _p(k_new.contiguous()),
+                        _p(v_new.contiguous() if v_new is not None else None),
+                        _p(_i32(slot_mapping, "slot_mapping")), n, _p(err_flags), _stream(stream))
+    _check(st, "pkv_store")
+
+
+def make_decode_args(kind, layout, q, k_pool, v_pool, out, *, page_size=1, sm_scale, max_seq_len,
+                     num_kv_heads=None, head_dim_v=None, kv_indptr=None, kv_indices=None,
+                     kv_last_page_len=None, block_table=None, seq_lens=None, cu_seqlens=None, lse=None,
+                     kv_chunk=0) -> DecodeArgs:
+    B, hq, dqk = q.shape
+    if kind == PKV_KIND_MLA:
+        hkv = 1
+        dv = int(head_dim_v)
+        v_stride = k_pool.stride(0)
+    else:
+        hkv = int(num_kv_heads if num_kv_heads is not None else k_pool.shape[1])
+        dv = v_pool.shape[-1]
+        v_stride = v_pool.stride(0)
+    a = DecodeArgs()
+    a.kind, a.layout, a.batch = kind, layout, B
+    a.num_q_heads, a.num_kv_heads, a.head_dim_qk, a.head_dim_v = hq, hkv, dqk, dv
+    a.page_size, a.sm_scale, a.max_seq_len, a.kv_chunk = int(page_size), float(sm_scale), int(max_seq_len), int(kv_chunk)
+    a.block_table_width = block_table.shape[1] if block_table is not None else 0
+    a.num_slots = k_pool.shape[0]
+    a.k_row_stride, a.v_row_stride = k_pool.stride(0), v_stride
+    a.kv_indices_len = kv_indices.numel() if kv_indices is not None else 0
+    for name, t in (("q", q), ("k_pool", k_pool), ("v_pool", v_pool), ("kv_indptr", kv_indptr),
+                    ("kv_indices", kv_indices), ("kv_last_page_len", kv_last_page_len),
+                    ("block_table", block_table), ("seq_lens", seq_lens), ("cu_seqlens", cu_seqlens),
+                    ("out", out), ("lse", lse)):
+        setattr(a, name, None if t is None else _p(t).value)
+    return a
+
+
+def pkv_decode_workspace_size(args: DecodeArgs) -> int:
+    return int(_lib.pkv_decode_workspace_size(ctypes.byref(args)))
+
+
+def pkv_decode(args: DecodeArgs, workspace: Optional[torch.Tensor], err_flags, stream=None):
+    ws_ptr = _p(workspace) if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = _lib.pkv_decode(ctypes.byref(args), ws_ptr, ws_bytes, _p(err_flags), _stream(stream))
+    _check(st, "pkv_decode")
+
+
+def pkv_ragged_gather(k_pool, v_pool, req_to_token, req_pool_idx, seq_lens, max_seq_len, k_out, v_out,
+                      cu_seqlens, err_flags, kv_start=None, stream=None):
+    row_elems = k_pool[0].numel()
+    st = _lib.pkv_ragged_gather(_p(k_pool), _p(v_pool), k_pool.shape[0], k_pool.stride(0), row_elems,
+                                _p(_i32(req_to_token, "req_to_token")), req_to_token.shape[0],
+                                req_to_token.stride(0), req_to_token.shape[1],
+                                _p(_i32(req_pool_idx, "req_pool_idx")), _p(_i32(kv_start, "kv_start")),
+                                _p(_i32(seq_lens, "seq_lens")), seq_lens.numel(), int(max_seq_len), _p(k_out),
+                                _p(v_out), k_out.shape[0], _p(_i32(cu_seqlens, "cu_seqlens")), _p(err_flags),
+                                _stream(stream))
+    _check(st, "pkv_ragged_gather")
+
+
+def pkv_status_string(status: int) -> str:
+    return _lib.pkv_status_string(status).decode()
+
+
+def pkv_abi_version() -> int:
+    return int(_lib.pkv_abi_version())

@@ -1,0 +1,62 @@
+// Status plumbing and device queries shared by the libpkv entry points.
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <vector>
+
+#include "pkv_internal.cuh"
+
+namespace pkv {
+
+static thread_local char g_last_error[512] = "";
+
+pkv_status fail(pkv_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+pkv_status ok() {
+    g_last_error[0] = '\0';
+    return PKV_OK;
+}
+
+pkv_status check_launch(const char *what) {
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    return ok();
+}
+
+int sm_count() {
+    static std::mutex mu;
+    static std::vector<int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= static_cast<int>(cache.size())) cache.resize(dev + 1, 0);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+}  // namespace pkv
+
+extern "C" const char *pkv_status_string(pkv_status status) {
+    switch (status) {
+        case PKV_OK: return "ok";
+        case PKV_ERR_INVALID_ARG: return "invalid argument";
+        case PKV_ERR_UNSUPPORTED: return "unsupported shape";
+        case PKV_ERR_CAPACITY: return "buffer too small";
+        case PKV_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+extern "C" const char *pkv_last_error(void) { return pkv::g_last_error; }
+
+extern "C" int32_t pkv_abi_version(void) { return PKV_ABI_VERSION; }

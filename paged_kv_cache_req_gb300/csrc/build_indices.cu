@@ -1,0 +1,115 @@
+// pkv_build_indices: per-request page lists from the token-granular req_to_token table.
+//
+// One CTA per request.  The CTA finds its kv_indptr offset by summing the page
+// counts of the requests before it (B is small: a few hundred ints from L2),
+// then reads its row once with coalesced loads.  Each position t compares its
+// slot with the slot of its page's first position (a broadcast load), which
+// checks page alignment and contiguity ("From slots to a page table": the
+// stride-and-divide derivation relies on tokens being contiguous inside a
+// page); the thread owning a page's first position writes the page id.
+#include "pkv_internal.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads)
+build_indices_kernel(const int32_t *__restrict__ r2t, int64_t r2t_rows, int64_t row_stride, int64_t width,
+                     const int32_t *__restrict__ req_pool_idx, const int32_t *__restrict__ seq_lens,
+                     const int32_t *__restrict__ kv_start, int32_t batch, int32_t ps, int64_t num_pool_pages,
+                     int32_t *__restrict__ kv_indptr, int32_t *__restrict__ kv_indices, int64_t cap,
+                     int32_t *__restrict__ last_page_len, int32_t *__restrict__ block_table, int32_t bt_width,
+                     int32_t *__restrict__ err) {
+    __shared__ long long scratch[32];
+    const int b = blockIdx.x;
+    if (b >= batch) {  // batch == 0: the single CTA only writes kv_indptr[0]
+        if (threadIdx.x == 0 && kv_indptr) kv_indptr[0] = 0;
+        return;
+    }
+
+    // A request whose row/region lies outside the table contributes no pages.
+    auto pages_of = [&](int j, bool &valid) -> long long {
+        const int64_t row = req_pool_idx[j];
+        const int64_t s = kv_start ? kv_start[j] : 0;
+        const int64_t L = seq_lens[j];
+        valid = row >= 0 && row < r2t_rows && s >= 0 && L >= 0 && s + L <= width;
+        return valid ? (L + ps - 1) / ps : 0;
+    };
+
+    long long before = 0;
+    for (int j = threadIdx.x; j < b; j += kThreads) {
+        bool v;
+        before += pages_of(j, v);
+    }
+    before = block_sum(before, scratch);
+
+    bool valid;
+    const long long n = pages_of(b, valid);
+    const int64_t L = valid ? seq_lens[b] : 0;
+    if (threadIdx.x == 0) {
+        if (!valid) raise_flag(err, PKV_DEVERR_RANGE);
+        if (kv_indptr) {
+            if (b == 0) kv_indptr[0] = 0;
+            kv_indptr[b + 1] = static_cast<int32_t>(before + n);
+        }
+        if (last_page_len) last_page_len[b] = L > 0 ? static_cast<int32_t>(L - (n - 1) * ps) : 0;
+        if (kv_indices && before + n > cap) raise_flag(err, PKV_DEVERR_CAPACITY);
+        if (block_table && n > bt_width) raise_flag(err, PKV_DEVERR_CAPACITY);
+    }
+
+    const int32_t *row = r2t + (valid ? req_pool_idx[b] * row_stride + (kv_start ? kv_start[b] : 0) : 0);
+    const int64_t pool_slots = num_pool_pages * ps;
+    int bad = 0;
+    for (int64_t t = threadIdx.x; t < L; t += kThreads) {
+        const int64_t off = t % ps;
+        const int64_t head = __ldg(row + (t - off));   // slot of this page's first position
+        const int64_t slot = off ? __ldg(row + t) : head;
+        if (off == 0) {
+            if (head < 0 || head >= pool_slots) {
+                bad |= PKV_DEVERR_RANGE;
+                continue;
+            }
+            if (head % ps != 0) bad |= PKV_DEVERR_CONTIG;
+            const int32_t page = static_cast<int32_t>(head / ps);
+            const long long p = t / ps;
+            if (kv_indices && before + p < cap) kv_indices[before + p] = page;
+            if (block_table && p < bt_width) block_table[static_cast<int64_t>(b) * bt_width + p] = page;
+        } else if (slot != head + off) {
+            bad |= PKV_DEVERR_CONTIG;
+        }
+    }
+    if (block_table)
+        for (int64_t p = n + threadIdx.x; p < bt_width; p += kThreads)
+            block_table[static_cast<int64_t>(b) * bt_width + p] = -1;
+    if (bad) raise_flag(err, bad);
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" pkv_status pkv_build_indices(const int32_t *req_to_token, int64_t r2t_rows, int64_t r2t_row_stride,
+                                        int64_t r2t_width, const int32_t *req_pool_idx, const int32_t *seq_lens,
+                                        const int32_t *kv_start, int32_t batch, int32_t page_size,
+                                        int64_t num_pool_pages, int32_t *kv_indptr, int32_t *kv_indices,
+                                        int64_t kv_indices_cap, int32_t *kv_last_page_len, int32_t *block_table,
+                                        int32_t block_table_width, int32_t *err_flags, pkv_stream_t stream) {
+    using namespace pkv;
+    if (batch < 0 || page_size < 1 || r2t_rows < 0 || r2t_width < 0 || r2t_row_stride < r2t_width ||
+        num_pool_pages < 0 || kv_indices_cap < 0 || block_table_width < 0)
+        return fail(PKV_ERR_INVALID_ARG, "pkv_build_indices: negative or inconsistent size");
+    if (!err_flags) return fail(PKV_ERR_INVALID_ARG, "pkv_build_indices: err_flags is required");
+    const bool csr = kv_indptr || kv_indices || kv_last_page_len;
+    if (csr && !(kv_indptr && kv_indices && kv_last_page_len))
+        return fail(PKV_ERR_INVALID_ARG, "pkv_build_indices: kv_indptr, kv_indices, kv_last_page_len go together");
+    if (!csr && !block_table) return fail(PKV_ERR_INVALID_ARG, "pkv_build_indices: no output requested");
+    if (batch > 0 && (!req_to_token || !req_pool_idx || !seq_lens))
+        return fail(PKV_ERR_INVALID_ARG, "pkv_build_indices: null input table");
+    if (num_pool_pages > INT32_MAX) return fail(PKV_ERR_UNSUPPORTED, "pkv_build_indices: more than 2^31 pages");
+    const int grid = batch > 0 ? batch : 1;
+    build_indices_kernel<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        req_to_token, r2t_rows, r2t_row_stride, r2t_width, req_pool_idx, seq_lens, kv_start, batch, page_size,
+        num_pool_pages, kv_indptr, kv_indices, kv_indices_cap, kv_last_page_len, block_table, block_table_width,
+        err_flags);
+    return check_launch("pkv_build_indices");
+}

@@ -1,0 +1,175 @@
+// Row movement: pkv_store (scatter new K/V rows into pool slots) and
+// pkv_ragged_gather (pack token-granular K/V rows into contiguous varlen buffers).
+//
+// Both are pure indexed copies of whole rows.  One warp moves one row with
+// 16-byte vector accesses (the mini-sglang store kernel's "one warp per token,
+// 16 bytes per move"); every row start is checked to be 16-byte aligned on the
+// host, otherwise a 2-byte element path is used.
+#include "pkv_internal.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kStoreThreads = 256;
+constexpr int kGatherThreads = 256;
+
+// Copies `elems` bf16 elements from src to dst with one warp.
+template <bool kVec>
+__device__ __forceinline__ void warp_copy_row(uint16_t *__restrict__ dst, const uint16_t *__restrict__ src,
+                                              int64_t elems, int lane) {
+    if (kVec) {
+        const int64_t n16 = elems / 8;
+        const uint4 *s = reinterpret_cast<const uint4 *>(src);
+        uint4 *d = reinterpret_cast<uint4 *>(dst);
+        for (int64_t i = lane; i < n16; i += 32) st_stream_16(d + i, ld_stream_16(s + i));
+    } else {
+        for (int64_t i = lane; i < elems; i += 32) dst[i] = src[i];
+    }
+}
+
+template <bool kVec>
+__global__ void __launch_bounds__(kStoreThreads)
+store_kernel(uint16_t *__restrict__ k_pool, uint16_t *__restrict__ v_pool, int64_t num_slots, int64_t k_stride,
+             int64_t v_stride, int64_t k_elems, int64_t v_elems, const uint16_t *__restrict__ k_new,
+             const uint16_t *__restrict__ v_new, const int32_t *__restrict__ slot_mapping, int32_t n,
+             int32_t *__restrict__ err) {
+    const int warp = (blockIdx.x * kStoreThreads + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const int rows_per_token = v_pool ? 2 : 1;
+    if (warp >= n * rows_per_token) return;
+    const int i = warp / rows_per_token;
+    const bool is_v = (warp % rows_per_token) == 1;
+    const int64_t slot = slot_mapping[i];
+    if (slot < 0) return;  // padded token
+    if (slot >= num_slots) {
+        if (lane == 0 && !is_v) raise_flag(err, PKV_DEVERR_RANGE);
+        return;
+    }
+    if (is_v)
+        warp_copy_row<kVec>(v_pool + slot * v_stride, v_new + i * v_elems, v_elems, lane);
+    else
+        warp_copy_row<kVec>(k_pool + slot * k_stride, k_new + i * k_elems, k_elems, lane);
+}
+
+// Grid (batch, splits).  CTA (b, s) finds cu_seqlens[b] by summing earlier
+// lengths, then its warps copy rows t = s*W + w, s*W + w + splits*W, ... of request b.
+template <bool kVec>
+__global__ void __launch_bounds__(kGatherThreads)
+ragged_gather_kernel(const uint16_t *__restrict__ k_pool, const uint16_t *__restrict__ v_pool, int64_t num_slots,
+                     int64_t pool_stride, int64_t row_elems, const int32_t *__restrict__ r2t, int64_t r2t_rows,
+                     int64_t row_stride, int64_t width, const int32_t *__restrict__ req_pool_idx,
+                     const int32_t *__restrict__ kv_start, const int32_t *__restrict__ seq_lens, int32_t batch,
+                     uint16_t *__restrict__ k_out, uint16_t *__restrict__ v_out, int64_t cap,
+                     int32_t *__restrict__ cu_seqlens, int32_t *__restrict__ err) {
+    __shared__ long long scratch[32];
+    const int b = blockIdx.x;
+    if (b >= batch) {
+        if (threadIdx.x == 0 && blockIdx.y == 0) cu_seqlens[0] = 0;
+        return;
+    }
+    long long before = 0;
+    for (int j = threadIdx.x; j < b; j += kGatherThreads) before += max(seq_lens[j], 0);
+    before = block_sum(before, scratch);
+
+    const int64_t row = req_pool_idx[b];
+    const int64_t s = kv_start ? kv_start[b] : 0;
+    int64_t L = max(seq_lens[b], 0);
+    if (threadIdx.x == 0 && blockIdx.y == 0) {
+        if (b == 0) cu_seqlens[0] = 0;
+        cu_seqlens[b + 1] = static_cast<int32_t>(before + L);
+        if (before + L > cap) raise_flag(err, PKV_DEVERR_CAPACITY);
+    }
+    if (row < 0 || row >= r2t_rows || s < 0 || s + L > width || seq_lens[b] < 0) {
+        if (threadIdx.x == 0 && blockIdx.y == 0) raise_flag(err, PKV_DEVERR_RANGE);
+        return;
+    }
+    if (before + L > cap) L = cap > before ? cap - before : 0;
+    const int32_t *rrow = r2t + row * row_stride + s;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int W = kGatherThreads / 32;
+    for (int64_t t = static_cast<int64_t>(blockIdx.y) * W + warp; t < L; t += static_cast<int64_t>(gridDim.y) * W) {
+        const int64_t slot = __ldg(rrow + t);
+        if (slot < 0 || slot >= num_slots) {
+            if (lane == 0) raise_flag(err, PKV_DEVERR_RANGE);
+            continue;
+        }
+        const int64_t o = before + t;
+        warp_copy_row<kVec>(k_out + o * row_elems, k_pool + slot * pool_stride, row_elems, lane);
+        if (v_pool) warp_copy_row<kVec>(v_out + o * row_elems, v_pool + slot * pool_stride, row_elems, lane);
+    }
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" pkv_status pkv_store(void *k_pool, void *v_pool, int64_t num_slots, int64_t k_row_stride,
+                                int64_t v_row_stride, int32_t kv_heads, int32_t head_dim_k, int32_t head_dim_v,
+                                const void *k_new, const void *v_new, const int32_t *slot_mapping,
+                                int32_t n_tokens, int32_t *err_flags, pkv_stream_t stream) {
+    using namespace pkv;
+    if (n_tokens < 0 || num_slots < 0 || kv_heads < 1 || head_dim_k < 1 || (v_pool && head_dim_v < 1))
+        return fail(PKV_ERR_INVALID_ARG, "pkv_store: bad sizes");
+    if (!err_flags) return fail(PKV_ERR_INVALID_ARG, "pkv_store: err_flags is required");
+    if (n_tokens == 0) return ok();
+    if (!k_pool || !k_new || !slot_mapping) return fail(PKV_ERR_INVALID_ARG, "pkv_store: null pointer");
+    if ((v_pool == nullptr) != (v_new == nullptr))
+        return fail(PKV_ERR_INVALID_ARG, "pkv_store: v_pool and v_new must both be set or both be NULL");
+    const int64_t k_elems = static_cast<int64_t>(kv_heads) * head_dim_k;
+    const int64_t v_elems = v_pool ? static_cast<int64_t>(kv_heads) * head_dim_v : 0;
+    if (k_row_stride < k_elems || (v_pool && v_row_stride < v_elems))
+        return fail(PKV_ERR_INVALID_ARG, "pkv_store: row stride smaller than a row");
+    const bool vec = aligned(k_pool, 16) && aligned(k_new, 16) && k_elems % 8 == 0 && k_row_stride % 8 == 0 &&
+                     (!v_pool || (aligned(v_pool, 16) && aligned(v_new, 16) && v_elems % 8 == 0 &&
+                                  v_row_stride % 8 == 0));
+    const int64_t warps = static_cast<int64_t>(n_tokens) * (v_pool ? 2 : 1);
+    const int64_t blocks = (warps * 32 + kStoreThreads - 1) / kStoreThreads;
+    auto s = reinterpret_cast<cudaStream_t>(stream);
+    auto kp = static_cast<uint16_t *>(k_pool), vp = static_cast<uint16_t *>(v_pool);
+    auto kn = static_cast<const uint16_t *>(k_new), vn = static_cast<const uint16_t *>(v_new);
+    if (vec)
+        store_kernel<true><<<blocks, kStoreThreads, 0, s>>>(kp, vp, num_slots, k_row_stride, v_row_stride, k_elems,
+                                                            v_elems, kn, vn, slot_mapping, n_tokens, err_flags);
+    else
+        store_kernel<false><<<blocks, kStoreThreads, 0, s>>>(kp, vp, num_slots, k_row_stride, v_row_stride, k_elems,
+                                                             v_elems, kn, vn, slot_mapping, n_tokens, err_flags);
+    return check_launch("pkv_store");
+}
+
+extern "C" pkv_status pkv_ragged_gather(const void *k_pool, const void *v_pool, int64_t num_slots,
+                                        int64_t pool_row_stride, int64_t row_elems, const int32_t *req_to_token,
+                                        int64_t r2t_rows, int64_t r2t_row_stride, int64_t r2t_width,
+                                        const int32_t *req_pool_idx, const int32_t *kv_start,
+                                        const int32_t *seq_lens, int32_t batch, int32_t max_seq_len, void *k_out,
+                                        void *v_out, int64_t out_rows_cap, int32_t *cu_seqlens,
+                                        int32_t *err_flags, pkv_stream_t stream) {
+    using namespace pkv;
+    if (batch < 0 || num_slots < 0 || row_elems < 1 || pool_row_stride < row_elems || r2t_rows < 0 ||
+        r2t_width < 0 || r2t_row_stride < r2t_width || out_rows_cap < 0 || max_seq_len < 0)
+        return fail(PKV_ERR_INVALID_ARG, "pkv_ragged_gather: bad sizes");
+    if (!err_flags || !cu_seqlens) return fail(PKV_ERR_INVALID_ARG, "pkv_ragged_gather: null err_flags/cu_seqlens");
+    if (batch > 0 && (!k_pool || !k_out || !req_to_token || !req_pool_idx || !seq_lens))
+        return fail(PKV_ERR_INVALID_ARG, "pkv_ragged_gather: null pointer");
+    if ((v_pool == nullptr) != (v_out == nullptr))
+        return fail(PKV_ERR_INVALID_ARG, "pkv_ragged_gather: v_pool and v_out must both be set or both be NULL");
+    const bool vec = aligned(k_pool, 16) && aligned(k_out, 16) && row_elems % 8 == 0 && pool_row_stride % 8 == 0 &&
+                     (!v_pool || (aligned(v_pool, 16) && aligned(v_out, 16)));
+    // Enough CTAs to cover ~2 waves of the device even for a handful of long requests.
+    const int warps_per_cta = kGatherThreads / 32;
+    int64_t splits = (static_cast<int64_t>(max_seq_len) + warps_per_cta * 4 - 1) / (warps_per_cta * 4);
+    const int64_t want = 2ll * sm_count() * (2048 / kGatherThreads);
+    if (batch > 0) splits = std::min<int64_t>(splits, std::max<int64_t>(1, (want + batch - 1) / batch));
+    splits = std::max<int64_t>(1, std::min<int64_t>(splits, 65535));
+    dim3 grid(batch > 0 ? batch : 1, static_cast<unsigned>(splits));
+    auto s = reinterpret_cast<cudaStream_t>(stream);
+    auto kp = static_cast<const uint16_t *>(k_pool), vp = static_cast<const uint16_t *>(v_pool);
+    auto ko = static_cast<uint16_t *>(k_out), vo = static_cast<uint16_t *>(v_out);
+    if (vec)
+        ragged_gather_kernel<true><<<grid, kGatherThreads, 0, s>>>(
+            kp, vp, num_slots, pool_row_stride, row_elems, req_to_token, r2t_rows, r2t_row_stride, r2t_width,
+            req_pool_idx, kv_start, seq_lens, batch, ko, vo, out_rows_cap, cu_seqlens, err_flags);
+    else
+        ragged_gather_kernel<false><<<grid, kGatherThreads, 0, s>>>(
+            kp, vp, num_slots, pool_row_stride, row_elems, req_to_token, r2t_rows, r2t_row_stride, r2t_width,
+            req_pool_idx, kv_start, seq_lens, batch, ko, vo, out_rows_cap, cu_seqlens, err_flags);
+    return check_launch("pkv_ragged_gather");
+}

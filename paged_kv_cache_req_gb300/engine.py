@@ -1,0 +1,180 @@
+"""Decode step over a paged KV cache: the library's public, per-step API.
+
+``DecodeStep`` keeps a workload's req_to_token table, pools and step buffers
+resident on one GPU and runs one decode layer step as a sequence of libpkv
+calls on the current stream:
+
+    pkv_build_indices   req_to_token -> kv_indptr / kv_indices (or the -1 padded table)
+    pkv_store           this step's new K/V rows -> their pool slots
+    pkv_decode          attention of every request's new token over its pages
+
+For an encoder-decoder workload the cross-attention over the encoder region
+runs either through its own page list ("paged": the page-aligned encoder of
+"Approach 1") or through pkv_ragged_gather into a contiguous varlen buffer
+followed by a varlen decode ("gather": "Approach 2").
+
+Nothing here computes: every step runs in libpkv's kernels.
+"""
+from __future__ import annotations
+
+from typing import Dict, Optional
+
+import torch
+
+from . import _binding as B
+from .workloads import Workload, fill_pool, make_values
+
+__all__ = ["DecodeStep"]
+
+
+class _ProblemBuffers:
+    pass
+
+
+class DecodeStep:
+    def __init__(self, wl: Workload, device="cuda", cross_mode: str = "paged", kv_chunk: int = 0,
+                 pools=None, values: Optional[Dict[str, torch.Tensor]] = None, seed: Optional[int] = None):
+        if cross_mode not in ("paged", "gather"):
+            raise ValueError(cross_mode)
+        self.wl = wl
+        self.device = torch.device(device)
+        self.cross_mode = cross_mode
+        self.kv_chunk = int(kv_chunk)
+        dev = self.device
+        ps = wl.page_size
+        self.r2t = wl.req_to_token.to(dev)
+        self.req_pool_idx = wl.req_pool_idx.to(dev)
+        if pools is None:
+            pools = fill_pool(wl, device=dev, seed=seed)
+        self.k_pool, self.v_pool = pools
+        vals = make_values(wl, seed=seed) if values is None else values
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        Bn = wl.batch
+        self.k_new = vals["k_new"].to(dev)
+        self.v_new = vals["v_new"].to(dev) if vals["v_new"] is not None else None
+        self.problems: Dict[str, _ProblemBuffers] = {}
+        for p in wl.problems:
+            pb = _ProblemBuffers()
+            pb.spec = p
+            pb.seq_lens = p.seq_lens.to(dev)
+            pb.kv_start = p.kv_start.to(dev)
+            pb.slot_mapping = p.slot_mapping.to(dev) if p.stores else None
+            pb.max_len = int(p.seq_lens.max()) if Bn else 0
+            pb.q = vals["q_" + p.name].to(dev)
+            pb.out = torch.empty((Bn, wl.num_q_heads, wl.head_dim_v), dtype=torch.bfloat16, device=dev)
+            pb.lse = torch.empty((Bn, wl.num_q_heads), dtype=torch.float32, device=dev)
+            max_pages = -(-pb.max_len // ps) if pb.max_len else 0
+            pb.gather = (p.name == "cross" and cross_mode == "gather")
+            if pb.gather:
+                rows = int(p.seq_lens.sum())
+                pb.k_rag = torch.empty((max(rows, 1),) + tuple(self.k_pool.shape[1:]), dtype=torch.bfloat16, device=dev)
+                pb.v_rag = torch.empty_like(pb.k_rag)
+                pb.cu = torch.empty(Bn + 1, dtype=torch.int32, device=dev)
+                layout = B.PKV_LAYOUT_VARLEN
+                pb.args = B.make_decode_args(B.PKV_KIND_GQA, layout, pb.q, pb.k_rag, pb.v_rag, pb.out,
+                                             sm_scale=wl.sm_scale, max_seq_len=pb.max_len,
+                                             cu_seqlens=pb.cu, lse=pb.lse, kv_chunk=self.kv_chunk)
+            elif wl.kind == "mla":
+                pb.block_table = torch.empty((Bn, max(max_pages, 1)), dtype=torch.int32, device=dev)
+                pb.args = B.make_decode_args(B.PKV_KIND_MLA, B.PKV_LAYOUT_BLOCK_TABLE, pb.q, self.k_pool, None,
+                                             pb.out, page_size=ps, sm_scale=wl.sm_scale, max_seq_len=pb.max_len,
+                                             head_dim_v=wl.head_dim_v, block_table=pb.block_table,
+                                             seq_lens=pb.seq_lens, lse=pb.lse, kv_chunk=self.kv_chunk)
+            else:
+                pb.kv_indptr = torch.empty(Bn + 1, dtype=torch.int32, device=dev)
+                pb.kv_indices = torch.empty(max(Bn * max_pages, 1), dtype=torch.int32, device=dev)
+                pb.kv_last = torch.empty(Bn, dtype=torch.int32, device=dev)
+                pb.args = B.make_decode_args(B.PKV_KIND_GQA, B.PKV_LAYOUT_CSR, pb.q, self.k_pool, self.v_pool,
+                                             pb.out, page_size=ps, sm_scale=wl.sm_scale, max_seq_len=pb.max_len,
+                                             kv_indptr=pb.kv_indptr, kv_indices=pb.kv_indices,
+                                             kv_last_page_len=pb.kv_last, lse=pb.lse, kv_chunk=self.kv_chunk)
+            nbytes = B.pkv_decode_workspace_size(pb.args)
+            pb.ws_bytes = nbytes
+            pb.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+            self.problems[p.name] = pb
+
+    # ------------------------------------------------------------------ steps
+    def build_indices(self, name: str):
+        pb = self.problems[name]
+        wl = self.wl
+        if pb.gather:
+            return
+        if wl.kind == "mla":
+            B.pkv_build_indices(self.r2t, self.req_pool_idx, pb.seq_lens, wl.page_size, wl.num_pool_pages,
+                                self.err, kv_start=pb.kv_start, block_table=pb.block_table)
+        else:
+            B.pkv_build_indices(self.r2t, self.req_pool_idx, pb.seq_lens, wl.page_size, wl.num_pool_pages,
+                                self.err, kv_start=pb.kv_start, kv_indptr=pb.kv_indptr, kv_indices=pb.kv_indices,
+                                kv_last_page_len=pb.kv_last)
+
+    def store(self, name: str = "self"):
+        pb = self.problems[name]
+        B.pkv_store(self.k_pool, self.v_pool, self.k_new, self.v_new, pb.slot_mapping, self.err)
+
+    def gather(self, name: str):
+        pb = self.problems[name]
+        B.pkv_ragged_gather(self.k_pool, self.v_pool, self.r2t, self.req_pool_idx, pb.seq_lens, pb.max_len,
+                            pb.k_rag, pb.v_rag, pb.cu, self.err, kv_start=pb.kv_start)
+
+    def decode(self, name: str):
+        pb = self.problems[name]
+        B.pkv_decode(pb.args, pb.workspace, self.err)
+
+    def run(self):
+        """One decode step: for each problem, page lists, (store), (gather), attention."""
+        for name, pb in self.problems.items():
+            if pb.gather:
+                self.gather(name)
+            else:
+                self.build_indices(name)
+            if pb.spec.stores:
+                self.store(name)
+            self.decode(name)
+
+    def launches_per_step(self) -> int:
+        """libpkv kernel launches one ``run()`` issues."""
+        n = 0
+        for pb in self.problems.values():
+            n += 1                                   # gather or build_indices
+            n += 1 if pb.spec.stores else 0          # store
+            n += 1 + (1 if pb.ws_bytes > 0 else 0)   # split kernel (+ merge when requests can split)
+        return n
+
+    def check_errors(self) -> int:
+        """Synchronises and returns the device error bits raised so far."""
+        return int(self.err.item())
+
+    # ------------------------------------------------------------------ host I/O
+    def host_step_tensors(self):
+        """Pinned host copies of the per-step inputs and outputs (for end-to-end timing)."""
+        h_in = {"k_new": self.k_new.cpu().pin_memory()}
+        if self.v_new is not None:
+            h_in["v_new"] = self.v_new.cpu().pin_memory()
+        h_out = {}
+        for name, pb in self.problems.items():
+            h_in["q_" + name] = pb.q.cpu().pin_memory()
+            h_in["seq_lens_" + name] = pb.seq_lens.cpu().pin_memory()
+            if pb.slot_mapping is not None:
+                h_in["slot_mapping_" + name] = pb.slot_mapping.cpu().pin_memory()
+            h_out[name] = torch.empty_like(pb.out, device="cpu").pin_memory()
+        h_in["req_pool_idx"] = self.req_pool_idx.cpu().pin_memory()
+        return h_in, h_out
+
+    def run_from_host(self, h_in, h_out):
+        """Copies this step's inputs from pinned host memory, runs the step, copies outputs back."""
+        self.k_new.copy_(h_in["k_new"], non_blocking=True)
+        if self.v_new is not None:
+            self.v_new.copy_(h_in["v_new"], non_blocking=True)
+        self.req_pool_idx.copy_(h_in["req_pool_idx"], non_blocking=True)
+        for name, pb in self.problems.items():
+            pb.q.copy_(h_in["q_" + name], non_blocking=True)
+            pb.seq_lens.copy_(h_in["seq_lens_" + name], non_blocking=True)
+            if pb.slot_mapping is not None:
+                pb.slot_mapping.copy_(h_in["slot_mapping_" + name], non_blocking=True)
+        self.run()
+        for name, pb in self.problems.items():
+            h_out[name].copy_(pb.out, non_blocking=True)
+
+    @staticmethod
+    def bytes_of(tensors) -> int:
+        return int(sum(t.numel() * t.element_size() for t in tensors.values()))

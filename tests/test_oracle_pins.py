@@ -20,6 +20,7 @@ import pytest
 import torch
 
 import oracle
+from _harness import paged_table
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -35,25 +36,6 @@ def bf16_bits(t: torch.Tensor) -> np.ndarray:
 
 def bits_to_f64(a: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(torch.float64)
-
-
-def paged_table(rng, lens, ps, num_pages, kv_start=None, width=None, rows=None):
-    """Tiny paged layout: shuffled whole pages per request; returns (r2t, rpi)."""
-    B = len(lens)
-    starts = np.zeros(B, dtype=np.int64) if kv_start is None else np.asarray(kv_start)
-    width = width or int((starts + np.asarray(lens)).max()) + 3
-    rows = rows or B + 1
-    r2t = np.zeros((rows, width), dtype=np.int32)
-    rpi = (rng.permutation(rows - 1)[:B] + 1).astype(np.int32)
-    free = list(rng.permutation(np.arange(1, num_pages)))
-    for b, L in enumerate(lens):
-        s = int(starts[b])
-        assert s % ps == 0
-        n = -(-L // ps)
-        pages, free = free[:n], free[n:]
-        slots = (np.asarray(pages, dtype=np.int64)[:, None] * ps + np.arange(ps)).reshape(-1)[:L]
-        r2t[rpi[b], s:s + L] = slots
-    return r2t, rpi
 
 
 # ---------------------------------------------------------------- index building
