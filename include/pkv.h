@@ -198,6 +198,34 @@ pkv_status pkv_decode(const pkv_decode_args *args, void *workspace, size_t works
 size_t pkv_decode_workspace_size(const pkv_decode_args *args);
 
 /*
+ * pkv_decode_no_alloc -- pkv_decode for GQA/MHA without a caller workspace.
+ *
+ * The pages describe no counterpart of this call; it exists for callers that
+ * cannot call cudaMalloc: a plug-in inside a process whose device memory is
+ * all owned by another allocator (for instance a serving engine that reserved
+ * the rest of HBM for its KV pool at start-up), or a latency-critical loop in
+ * which an allocation could block.  It computes exactly what pkv_decode
+ * computes (same split plan, same kernels, bitwise the same outputs) but keeps
+ * the split partials in a 32 MiB array compiled into the library, which every
+ * GPU that loads the library holds until the process exits.  The library
+ * still allocates nothing; q, the pools, the page table, out and lse stay
+ * caller-owned as for pkv_decode.
+ *
+ * - Only PKV_KIND_GQA is accepted (PKV_ERR_UNSUPPORTED otherwise).
+ * - A split plan needing more than 32 MiB of scratch (pkv_decode_workspace_size
+ *   of the same arguments) returns PKV_ERR_CAPACITY before launching; a larger
+ *   kv_chunk or a smaller batch brings it under the limit.
+ * - The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ * - All calls share the one array and it keeps the last call's contents.  No
+ *   part of it needs to start at zero (every partial is written before it is
+ *   read), but calls whose kernels overlap on the GPU (other streams, other
+ *   host threads) race on it: serialise them.
+ */
+pkv_status pkv_decode_no_alloc(const pkv_decode_args *args, int32_t *err_flags, pkv_stream_t stream);
+
+/*
  * pkv_ragged_gather -- pack token-granular K/V into contiguous varlen buffers.
  *
  * Defined by "Approach 2: gather and go ragged (variable-length

@@ -22,7 +22,8 @@ PKV_KIND_GQA, PKV_KIND_MLA = 0, 1
 PKV_LAYOUT_CSR, PKV_LAYOUT_BLOCK_TABLE, PKV_LAYOUT_VARLEN = 0, 1, 2
 
 EXPORTED_SYMBOLS = ("pkv_build_indices", "pkv_store", "pkv_decode", "pkv_decode_workspace_size",
-                    "pkv_ragged_gather", "pkv_status_string", "pkv_last_error", "pkv_abi_version")
+                    "pkv_decode_no_alloc", "pkv_ragged_gather", "pkv_status_string", "pkv_last_error",
+                    "pkv_abi_version")
 
 
 class PkvError(RuntimeError):
@@ -62,10 +63,11 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
     lib.pkv_build_indices.argtypes = [P, I64, I64, I64, P, P, P, I32, I32, I64, P, P, I64, P, P, I32, P, P]
     lib.pkv_store.argtypes = [P, P, I64, I64, I64, I32, I32, I32, P, P, P, I32, P, P]
     lib.pkv_decode.argtypes = [ctypes.POINTER(DecodeArgs), P, SZ, P, P]
+    lib.pkv_decode_no_alloc.argtypes = [ctypes.POINTER(DecodeArgs), P, P]
     lib.pkv_decode_workspace_size.argtypes = [ctypes.POINTER(DecodeArgs)]
     lib.pkv_decode_workspace_size.restype = SZ
     lib.pkv_ragged_gather.argtypes = [P, P, I64, I64, I64, P, I64, I64, I64, P, P, P, I32, I32, P, P, I64, P, P, P]
-    for f in ("pkv_build_indices", "pkv_store", "pkv_decode", "pkv_ragged_gather"):
+    for f in ("pkv_build_indices", "pkv_store", "pkv_decode", "pkv_decode_no_alloc", "pkv_ragged_gather"):
         getattr(lib, f).restype = ctypes.c_int
     lib.pkv_status_string.argtypes = [ctypes.c_int]
     lib.pkv_status_string.restype = ctypes.c_char_p
@@ -171,6 +173,12 @@ def pkv_decode(args: DecodeArgs, workspace: Optional[torch.Tensor], err_flags, s
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = _lib.pkv_decode(ctypes.byref(args), ws_ptr, ws_bytes, _p(err_flags), _stream(stream))
     _check(st, "pkv_decode")
+
+
+def pkv_decode_no_alloc(args: DecodeArgs, err_flags, stream=None):
+    """pkv_decode with the library's built-in scratch array instead of a caller workspace."""
+    st = _lib.pkv_decode_no_alloc(ctypes.byref(args), _p(err_flags), _stream(stream))
+    _check(st, "pkv_decode_no_alloc")
 
 
 def pkv_ragged_gather(k_pool, v_pool, req_to_token, req_pool_idx, seq_lens, max_seq_len, k_out, v_out,

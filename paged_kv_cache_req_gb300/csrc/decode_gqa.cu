@@ -21,6 +21,8 @@
 // log-sum-exp, combined by merge_kernel.
 #include <algorithm>
 #include <cmath>
+#include <mutex>
+#include <vector>
 
 #include "pkv_internal.cuh"
 
@@ -636,4 +638,66 @@ extern "C" pkv_status pkv_decode(const pkv_decode_args *args, void *workspace, s
     if (st != PKV_OK) return st;
     if (args->batch == 0) return ok();
     return gqa::launch(args, workspace, workspace_bytes, err_flags, s);
+}
+
+// ---------------------------------------------------------------------------
+// pkv_decode_no_alloc: GQA/MHA decode whose split-KV scratch is a fixed
+// device array inside this library instead of a caller-provided workspace.
+//
+// Some callers cannot call cudaMalloc at all: code loaded into a host
+// process whose device memory is entirely owned by another allocator (for
+// example a serving engine that reserved the rest of HBM for its KV pool at
+// start-up), or a latency-critical loop where a first-touch allocation could
+// block.  For them the partial outputs and log-sum-exp values of the split
+// plan live in g_no_alloc_scratch below.  Every GPU that loads this library
+// holds the array until the process exits.
+namespace pkv {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB
+__device__ __align__(256) unsigned char g_no_alloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the array, resolved once per device.  In host code the
+// symbol is only a host-side stand-in, so the kernel must receive this address.
+pkv_status no_alloc_scratch_address(void **out) {
+    static std::mutex mu;
+    static std::vector<void *> by_device;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(PKV_ERR_CUDA, "pkv_decode_no_alloc: cudaGetDevice: %s", cudaGetErrorString(e));
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= static_cast<int>(by_device.size())) by_device.resize(dev + 1, nullptr);
+    if (!by_device[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_no_alloc_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(PKV_ERR_CUDA, "pkv_decode_no_alloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+        by_device[dev] = p;
+    }
+    *out = by_device[dev];
+    return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" pkv_status pkv_decode_no_alloc(const pkv_decode_args *args, int32_t *err_flags, pkv_stream_t stream) {
+    using namespace pkv;
+    if (!args) return fail(PKV_ERR_INVALID_ARG, "pkv_decode_no_alloc: null args");
+    if (!err_flags) return fail(PKV_ERR_INVALID_ARG, "pkv_decode_no_alloc: err_flags is required");
+    if (args->kind != PKV_KIND_GQA)
+        return fail(PKV_ERR_UNSUPPORTED, "pkv_decode_no_alloc: only GQA/MHA decode has a built-in scratch");
+    pkv_status st = gqa::validate(args, true);
+    if (st != PKV_OK) return st;
+    if (args->batch == 0) return ok();
+    const size_t need = gqa::workspace_size(args);
+    if (need > kNoAllocScratchBytes)
+        return fail(PKV_ERR_CAPACITY,
+                    "pkv_decode_no_alloc: split plan needs %zu bytes of scratch, the built-in array holds %zu "
+                    "(use pkv_decode with a caller workspace, or a larger kv_chunk / smaller batch)",
+                    need, kNoAllocScratchBytes);
+    void *scratch = nullptr;
+    st = no_alloc_scratch_address(&scratch);
+    if (st != PKV_OK) return st;
+    return gqa::launch(args, scratch, kNoAllocScratchBytes, err_flags, reinterpret_cast<cudaStream_t>(stream));
 }
