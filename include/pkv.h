@@ -59,6 +59,7 @@ typedef enum pkv_status {
 #define PKV_DEVERR_RANGE 1    /* slot, page, row or position outside its pool or table */
 #define PKV_DEVERR_CONTIG 2   /* a page's tokens are not page-aligned and contiguous */
 #define PKV_DEVERR_CAPACITY 4 /* an output had too little room; the excess was not written */
+#define PKV_DEVERR_TIMEOUT 8  /* a device-side wait gave up after ~2 s; outputs of the launch unspecified */
 
 #define PKV_ABI_VERSION 1
 

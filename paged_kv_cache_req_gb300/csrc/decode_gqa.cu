@@ -33,7 +33,7 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTile = 64;   // keys per pipeline stage
 constexpr int kStages = 3;
-constexpr int kMaxGc = 4;   // query heads per CTA
+constexpr int kMaxRows = 16; // query heads per CTA (tensor-core path); the CUDA-core path takes <= 4
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kLog2e = 1.44269504088896341f;
 
@@ -45,6 +45,7 @@ struct Params {
     int32_t chunk, n_chunks_max;
     int32_t bt_width;
     int64_t num_slots, num_pages, k_stride, v_stride, kv_indices_len;
+    int32_t box_rows;   // TMA box height (keys per box)
     const uint16_t *q, *k_pool, *v_pool;
     const int32_t *kv_indptr, *kv_indices, *kv_last, *block_table, *seq_lens, *cu_seqlens;
     uint16_t *out;
@@ -103,19 +104,439 @@ __device__ __forceinline__ int64_t slot_of(const Params &p, int64_t base, int t)
     return (static_cast<int64_t>(page) << p.ps_shift) + (t & p.ps_mask);
 }
 
+// Tile layout in shared memory: a 64-key tile of one kv head is D/64 slabs of
+// [64 keys x 128 B]; 16-byte chunk c of key row r sits at chunk (c ^ (r & 7))
+// of its 128-byte row (the TMA 128-byte swizzle).  The eight rows an ldmatrix
+// reads, or the eight lanes of a SIMT read, land in eight bank groups.
 template <int D>
-struct Smem {
-    static constexpr int kRowElems = D;                         // one kv head of one key
-    static constexpr int kTileElems = kTile * D;
-    static constexpr int kStageBytes = 2 * kTileElems * 2;       // K + V
-    static constexpr int kRedOBytes = kWarps * kMaxGc * D * 4;
-    static constexpr int kFixedBytes = kStages * kStageBytes + kRedOBytes + 2 * kWarps * kMaxGc * 4;
+__device__ __forceinline__ int toff(int key, int c) {
+    return (c >> 3) * (kTile * 64) + key * 64 + (((c & 7) ^ (key & 7)) << 3);
+}
+
+template <int D>
+struct Tile {
+    static constexpr int kElems = kTile * D;          // one K (or V) tile
+    static constexpr int kBytes = kElems * 2;
+    static constexpr int kSlabs = D / 64;
+    static constexpr int kStageBytes = 2 * kBytes;    // K + V
 };
 
-// Issue the cp.async copies of one 64-key tile (K and V) of kv head kh.
+// ---------------------------------------------------------------- item table
+// off[b] = first work item of request b (exclusive scan of its item count),
+// off[B] = total.  Every CTA builds the same table from the lengths, with
+// `nthreads` threads (a multiple of 32) and one barrier id.
+__device__ __forceinline__ void build_item_table(const Params &p, int *off, int *scratch, int nthreads) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int B = p.batch;
+    const int per_chunk = p.hkv * p.hsplit;
+    const int seg = (B + nthreads - 1) / nthreads;
+    const int lo = min(B, tid * seg), hi = min(B, lo + seg);
+    int local = 0;
+    for (int b = lo; b < hi; ++b) {
+        int64_t base;
+        const int L = key_count(p, b, base, false);
+        local += max(1, (L + p.chunk - 1) / p.chunk) * per_chunk;
+    }
+    int incl = local;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) scratch[warp] = incl;
+    __syncthreads();
+    int wbase = 0;
+    for (int w = 0; w < warp; ++w) wbase += scratch[w];
+    int run = wbase + incl - local;
+    for (int b = lo; b < hi; ++b) {
+        off[b] = run;
+        int64_t base;
+        const int L = key_count(p, b, base, false);
+        run += max(1, (L + p.chunk - 1) / p.chunk) * per_chunk;
+    }
+    if (tid == nthreads - 1) off[B] = wbase + incl;
+    __syncthreads();
+}
+
+struct Item {
+    int b, c, kh, hs, L, n_chunks, head0, t_begin, t_end;
+    int64_t base;
+};
+
+template <int GC>
+__device__ __forceinline__ Item locate(const Params &p, const int *off, int w, bool report) {
+    Item it;
+    int lo = 0, hi = p.batch;  // off[lo] <= w < off[lo + 1]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (off[mid] <= w) lo = mid; else hi = mid;
+    }
+    it.b = lo;
+    int rem = w - off[lo];
+    it.hs = rem % p.hsplit;
+    rem /= p.hsplit;
+    it.kh = rem % p.hkv;
+    it.c = rem / p.hkv;
+    it.L = key_count(p, it.b, it.base, report && it.c == 0 && it.kh == 0 && it.hs == 0);
+    it.n_chunks = max(1, (it.L + p.chunk - 1) / p.chunk);
+    it.head0 = it.kh * p.g + it.hs * GC;
+    it.t_begin = it.c * p.chunk;
+    it.t_end = min(it.L, it.t_begin + p.chunk);
+    return it;
+}
+
+template <int D, int GC>
+__device__ __forceinline__ void write_empty(const Params &p, const Item &it) {
+    for (int i = threadIdx.x; i < GC * D; i += kThreads) {
+        const int h = i / D, d = i % D;
+        p.out[(static_cast<int64_t>(it.b) * p.hq + it.head0 + h) * D + d] = 0;
+        if (d == 0 && p.lse) p.lse[static_cast<int64_t>(it.b) * p.hq + it.head0 + h] = -INFINITY;
+    }
+}
+
+// Combines the per-warp states left in red_* (base-2 running max m, sum l,
+// unnormalised o; rows GC apart per warp) and writes the item's output or
+// split partial.  Run by the kThreads math threads.
+template <int D, int GC>
+__device__ __forceinline__ void finish_item(const Params &p, const Item &it, const float *red_o, const float *red_m,
+                                            const float *red_l) {
+    const int64_t pidx = ((static_cast<int64_t>(it.b) * p.hkv + it.kh) * p.hsplit + it.hs) * p.n_chunks_max + it.c;
+    for (int i = threadIdx.x; i < GC * D; i += kThreads) {
+        const int h = i / D, d = i % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, red_m[ww * GC + h]);
+        float num = 0.f, den = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < kWarps; ++ww) {
+            const float mw = red_m[ww * GC + h];
+            const float sc = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+            num = fmaf(red_o[(ww * GC + h) * D + d], sc, num);
+            den = fmaf(red_l[ww * GC + h], sc, den);
+        }
+        const float val = num / den;
+        if (it.n_chunks == 1) {
+            p.out[(static_cast<int64_t>(it.b) * p.hq + it.head0 + h) * D + d] =
+                __bfloat16_as_ushort(__float2bfloat16_rn(val));
+            if (d == 0 && p.lse) p.lse[static_cast<int64_t>(it.b) * p.hq + it.head0 + h] = (M + log2f(den)) * kLn2;
+        } else {
+            p.part_o[(pidx * GC + h) * D + d] = val;
+            if (d == 0) p.part_lse[pidx * GC + h] = M + log2f(den);
+        }
+    }
+}
+
+template <int D, int GC>
+struct RedLayout {
+    static constexpr int kBytes = kWarps * GC * D * 4 + 2 * kWarps * GC * 4;
+};
+
+// ---------------------------------------------------------------- tensor-core math (GQA groups)
+// Per 64-key tile each warp owns 16 keys.  S = Q K^T is an m16n8k16 bf16 MMA
+// with the group's query heads as the 16 rows (rows past the group are zero),
+// the warp's keys as columns (two n8 tiles) and head_dim as the reduction;
+// K comes from the swizzled tile with ldmatrix.  The fp32 scores go through a
+// per-warp online softmax (base 2; the running max is raised only when a row
+// grows by more than 2^8, so rescales are rare and p <= 256), are rounded to
+// bf16 in registers and reused directly as the A operand of O += P V (V read
+// with ldmatrix.trans).
+template <int D, int GC>
+struct MmaState {
+    static constexpr int KS = D / 16;
+    static constexpr int NT = D / 8;
+    static constexpr bool kRows8 = GC > 8;
+    uint32_t qa[KS][4];
+    float o[NT][4];
+    float m0, m1, l0, l1;
+};
+
+template <int D, int GC>
+__device__ __forceinline__ void mma_begin(MmaState<D, GC> &st, const Params &p, const Item &it) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
+    const uint32_t *q0 =
+        reinterpret_cast<const uint32_t *>(p.q + (static_cast<int64_t>(it.b) * p.hq + it.head0 + g) * D);
+    const uint32_t *q8 =
+        reinterpret_cast<const uint32_t *>(p.q + (static_cast<int64_t>(it.b) * p.hq + it.head0 + g + 8) * D);
+#pragma unroll
+    for (int ks = 0; ks < MmaState<D, GC>::KS; ++ks) {
+        st.qa[ks][0] = g < GC ? __ldg(q0 + ks * 8 + tig) : 0u;
+        st.qa[ks][2] = g < GC ? __ldg(q0 + ks * 8 + 4 + tig) : 0u;
+        st.qa[ks][1] = (MmaState<D, GC>::kRows8 && g + 8 < GC) ? __ldg(q8 + ks * 8 + tig) : 0u;
+        st.qa[ks][3] = (MmaState<D, GC>::kRows8 && g + 8 < GC) ? __ldg(q8 + ks * 8 + 4 + tig) : 0u;
+    }
+#pragma unroll
+    for (int nt = 0; nt < MmaState<D, GC>::NT; ++nt) st.o[nt][0] = st.o[nt][1] = st.o[nt][2] = st.o[nt][3] = 0.f;
+    st.m0 = st.m1 = -INFINITY;
+    st.l0 = st.l1 = 0.f;
+}
+
+template <int D, int GC>
+__device__ __forceinline__ void mma_tile(MmaState<D, GC> &st, const uint16_t *kt, const uint16_t *vt, int n_valid,
+                                         float scale_log2) {
+    constexpr bool kRows8 = MmaState<D, GC>::kRows8;
+    constexpr float kLazy = 8.f;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tig = lane & 3;
+    const int key0 = warp * 16;
+    float sc[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+        const int key = key0 + j * 8 + (lane & 7);
+#pragma unroll
+        for (int kk = 0; kk < D / 32; ++kk) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(b0, b1, b2, b3, kt + toff<D>(key, kk * 4 + (lane >> 3)));
+            mma_bf16_16816(sc[j], st.qa[2 * kk], b0, b1);
+            mma_bf16_16816(sc[j], st.qa[2 * kk + 1], b2, b3);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int key = key0 + j * 8 + tig * 2 + (e & 1);
+            sc[j][e] = key < n_valid ? sc[j][e] * scale_log2 : -INFINITY;
+        }
+    float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    if (mx0 > st.m0 + kLazy || (st.m0 == -INFINITY && mx0 != -INFINITY)) {
+        const float corr = ex2(st.m0 - mx0);
+        st.l0 *= corr;
+#pragma unroll
+        for (int nt = 0; nt < MmaState<D, GC>::NT; ++nt) { st.o[nt][0] *= corr; st.o[nt][1] *= corr; }
+        st.m0 = mx0;
+    }
+    if (kRows8) {
+        float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        if (mx1 > st.m1 + kLazy || (st.m1 == -INFINITY && mx1 != -INFINITY)) {
+            const float corr = ex2(st.m1 - mx1);
+            st.l1 *= corr;
+#pragma unroll
+            for (int nt = 0; nt < MmaState<D, GC>::NT; ++nt) { st.o[nt][2] *= corr; st.o[nt][3] *= corr; }
+            st.m1 = mx1;
+        }
+    }
+    uint32_t pa[4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const float p0 = st.m0 == -INFINITY ? 0.f : ex2(sc[j][0] - st.m0);
+        const float p1 = st.m0 == -INFINITY ? 0.f : ex2(sc[j][1] - st.m0);
+        const float p2 = (!kRows8 || st.m1 == -INFINITY) ? 0.f : ex2(sc[j][2] - st.m1);
+        const float p3 = (!kRows8 || st.m1 == -INFINITY) ? 0.f : ex2(sc[j][3] - st.m1);
+        st.l0 += p0 + p1;
+        st.l1 += p2 + p3;
+        pa[2 * j] = pack_bf16x2(p0, p1);
+        pa[2 * j + 1] = pack_bf16x2(p2, p3);
+    }
+#pragma unroll
+    for (int nn = 0; nn < D / 16; ++nn) {
+        const int mi = lane >> 3;
+        const int key = key0 + (mi & 1) * 8 + (lane & 7);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_trans(b0, b1, b2, b3, vt + toff<D>(key, nn * 2 + (mi >> 1)));
+        mma_bf16_16816(st.o[2 * nn], pa, b0, b1);
+        mma_bf16_16816(st.o[2 * nn + 1], pa, b2, b3);
+    }
+}
+
+template <int D, int GC>
+__device__ __forceinline__ void mma_store(MmaState<D, GC> &st, float *red_o, float *red_m, float *red_l) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
+    st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, 1);
+    st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, 2);
+    st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, 1);
+    st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, 2);
+    if (g < GC) {
+#pragma unroll
+        for (int nt = 0; nt < MmaState<D, GC>::NT; ++nt)
+            *reinterpret_cast<float2 *>(&red_o[(warp * GC + g) * D + nt * 8 + tig * 2]) =
+                make_float2(st.o[nt][0], st.o[nt][1]);
+        if (tig == 0) {
+            red_m[warp * GC + g] = st.m0;
+            red_l[warp * GC + g] = st.l0;
+        }
+    }
+    if (MmaState<D, GC>::kRows8 && g + 8 < GC) {
+#pragma unroll
+        for (int nt = 0; nt < MmaState<D, GC>::NT; ++nt)
+            *reinterpret_cast<float2 *>(&red_o[(warp * GC + g + 8) * D + nt * 8 + tig * 2]) =
+                make_float2(st.o[nt][2], st.o[nt][3]);
+        if (tig == 0) {
+            red_m[warp * GC + g + 8] = st.m1;
+            red_l[warp * GC + g + 8] = st.l1;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- CUDA-core math (one head per kv head)
+// Each warp takes 16 keys of a tile; 8 lanes share a key (each lane owns D/8
+// dims), reduce q.k with three xor-shuffles, and keep their own online-softmax
+// state (base 2, scale * log2 e folded into q).
+template <int D, int GC>
+struct SimtState {
+    static constexpr int NC = D / 64;
+    float q[GC][NC][8];
+    float o[GC][NC][8];
+    float m[GC], l[GC];
+};
+
+template <int D, int GC>
+__device__ __forceinline__ void simt_begin(SimtState<D, GC> &st, const Params &p, const Item &it) {
+    const int part = threadIdx.x & 7;
+#pragma unroll
+    for (int h = 0; h < GC; ++h)
+#pragma unroll
+        for (int ci = 0; ci < SimtState<D, GC>::NC; ++ci) {
+            const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
+                p.q + (static_cast<int64_t>(it.b) * p.hq + it.head0 + h) * D + (part + 8 * ci) * 8));
+            widen8(raw, st.q[h][ci]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                st.q[h][ci][e] *= p.scale_log2;
+                st.o[h][ci][e] = 0.f;
+            }
+        }
+#pragma unroll
+    for (int h = 0; h < GC; ++h) {
+        st.m[h] = -INFINITY;
+        st.l[h] = 0.f;
+    }
+}
+
+template <int D, int GC>
+__device__ __forceinline__ void simt_tile(SimtState<D, GC> &st, const uint16_t *kt, const uint16_t *vt, int n_valid) {
+    constexpr int NC = SimtState<D, GC>::NC;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, grp = lane >> 3, part = lane & 7;
+    float s[4][GC];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int key = warp * 16 + j * 4 + grp;
+#pragma unroll
+        for (int h = 0; h < GC; ++h) s[j][h] = 0.f;
+#pragma unroll
+        for (int ci = 0; ci < NC; ++ci) {
+            const uint4 raw = *reinterpret_cast<const uint4 *>(kt + toff<D>(key, part + 8 * ci));
+            float kf[8];
+            widen8(raw, kf);
+#pragma unroll
+            for (int h = 0; h < GC; ++h)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s[j][h] = fmaf(st.q[h][ci][e], kf[e], s[j][h]);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int h = 0; h < GC; ++h) {
+            float v = s[j][h];
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            s[j][h] = (warp * 16 + j * 4 + grp < n_valid) ? v : -INFINITY;
+        }
+#pragma unroll
+    for (int h = 0; h < GC; ++h) {
+        const float mt = fmaxf(fmaxf(s[0][h], s[1][h]), fmaxf(s[2][h], s[3][h]));
+        if (mt > st.m[h]) {
+            const float corr = ex2(st.m[h] - mt);  // m = -inf gives 0
+            st.l[h] *= corr;
+#pragma unroll
+            for (int ci = 0; ci < NC; ++ci)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) st.o[h][ci][e] *= corr;
+            st.m[h] = mt;
+        }
+        const bool live = st.m[h] != -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            s[j][h] = live ? ex2(s[j][h] - st.m[h]) : 0.f;
+            st.l[h] += s[j][h];
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int key = warp * 16 + j * 4 + grp;
+#pragma unroll
+        for (int ci = 0; ci < NC; ++ci) {
+            const uint4 raw = *reinterpret_cast<const uint4 *>(vt + toff<D>(key, part + 8 * ci));
+            float vf[8];
+            widen8(raw, vf);
+#pragma unroll
+            for (int h = 0; h < GC; ++h)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) st.o[h][ci][e] = fmaf(s[j][h], vf[e], st.o[h][ci][e]);
+        }
+    }
+}
+
+template <int D, int GC>
+__device__ __forceinline__ void simt_store(SimtState<D, GC> &st, float *red_o, float *red_m, float *red_l) {
+    constexpr int NC = SimtState<D, GC>::NC;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, grp = lane >> 3, part = lane & 7;
+#pragma unroll
+    for (int h = 0; h < GC; ++h) {
+        float mw = fmaxf(st.m[h], __shfl_xor_sync(0xffffffffu, st.m[h], 8));
+        mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 16));
+        const float corr = (st.m[h] == -INFINITY) ? 0.f : ex2(st.m[h] - mw);
+        float lw = st.l[h] * corr;
+        lw += __shfl_xor_sync(0xffffffffu, lw, 8);
+        lw += __shfl_xor_sync(0xffffffffu, lw, 16);
+#pragma unroll
+        for (int ci = 0; ci < NC; ++ci)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                float v = st.o[h][ci][e] * corr;
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 16);
+                st.o[h][ci][e] = v;
+            }
+        st.m[h] = mw;
+        st.l[h] = lw;
+    }
+    if (grp == 0) {
+#pragma unroll
+        for (int h = 0; h < GC; ++h) {
+#pragma unroll
+            for (int ci = 0; ci < NC; ++ci)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) red_o[(warp * GC + h) * D + (part + 8 * ci) * 8 + e] = st.o[h][ci][e];
+            if (part == 0) {
+                red_m[warp * GC + h] = st.m[h];
+                red_l[warp * GC + h] = st.l[h];
+            }
+        }
+    }
+}
+
+template <int D, int GC, bool MMA>
+struct Math;
+template <int D, int GC>
+struct Math<D, GC, true> {
+    using State = MmaState<D, GC>;
+    static __device__ __forceinline__ void begin(State &s, const Params &p, const Item &it) { mma_begin<D, GC>(s, p, it); }
+    static __device__ __forceinline__ void tile(State &s, const uint16_t *k, const uint16_t *v, int n, float sc) {
+        mma_tile<D, GC>(s, k, v, n, sc);
+    }
+    static __device__ __forceinline__ void store(State &s, float *o, float *m, float *l) { mma_store<D, GC>(s, o, m, l); }
+};
+template <int D, int GC>
+struct Math<D, GC, false> {
+    using State = SimtState<D, GC>;
+    static __device__ __forceinline__ void begin(State &s, const Params &p, const Item &it) { simt_begin<D, GC>(s, p, it); }
+    static __device__ __forceinline__ void tile(State &s, const uint16_t *k, const uint16_t *v, int n, float) {
+        simt_tile<D, GC>(s, k, v, n);
+    }
+    static __device__ __forceinline__ void store(State &s, float *o, float *m, float *l) { simt_store<D, GC>(s, o, m, l); }
+};
+
+// ---------------------------------------------------------------- cp.async kernel (page_size < 8)
+// Issue the cp.async copies of one 64-key tile (K and V) of kv head kh; keys
+// past t1, and keys whose page is outside the pool, are zero-filled.
 template <int D>
-__device__ __forceinline__ void load_tile(const Params &p, uint16_t *ks, uint16_t *vs, int64_t base, int t0, int t1,
-                                          int kh) {
+__device__ __forceinline__ void load_tile_cp_async(const Params &p, uint16_t *ks, uint16_t *vs, int64_t base, int t0,
+                                                   int t1, int kh) {
     constexpr int CPR = D / 8;              // 16-byte chunks per row
     constexpr int RPP = kThreads / CPR;     // rows per pass
     const int chunk = threadIdx.x % CPR;
@@ -132,263 +553,249 @@ __device__ __forceinline__ void load_tile(const Params &p, uint16_t *ks, uint16_
         const bool ok = slot >= 0;
         const uint16_t *ksrc = ok ? p.k_pool + slot * p.k_stride + kh * D + chunk * 8 : p.k_pool;
         const uint16_t *vsrc = ok ? p.v_pool + slot * p.v_stride + kh * D + chunk * 8 : p.v_pool;
-        cp_async_16(ks + key * D + chunk * 8, ksrc, ok ? 16 : 0);
-        cp_async_16(vs + key * D + chunk * 8, vsrc, ok ? 16 : 0);
+        const int dst = toff<D>(key, chunk);
+        cp_async_16(ks + dst, ksrc, ok ? 16 : 0);
+        cp_async_16(vs + dst, vsrc, ok ? 16 : 0);
     }
 }
 
-template <int D, int GC>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const Params p) {
-    constexpr int NC = D / 64;  // 16-byte chunks per lane: chunk index part + 8*ci
-    using S = Smem<D>;
+template <int D, int GC, bool MMA>
+__global__ void __launch_bounds__(kThreads, 2) decode_cp_async_kernel(const Params p) {
+    using T = Tile<D>;
+    using M = Math<D, GC, MMA>;
     extern __shared__ __align__(128) unsigned char smem[];
     uint16_t *tiles = reinterpret_cast<uint16_t *>(smem);
-    float *red_o = reinterpret_cast<float *>(smem + kStages * S::kStageBytes);
-    float *red_m = red_o + kWarps * kMaxGc * D;
-    float *red_l = red_m + kWarps * kMaxGc;
-    int *off = reinterpret_cast<int *>(red_l + kWarps * kMaxGc);
+    float *red_o = reinterpret_cast<float *>(smem + kStages * T::kStageBytes);
+    float *red_m = red_o + kWarps * GC * D;
+    float *red_l = red_m + kWarps * GC;
+    int *off = reinterpret_cast<int *>(smem + kStages * T::kStageBytes + RedLayout<D, GC>::kBytes);
+    __shared__ int scan_scratch[kWarps];
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int grp = lane >> 3, part = lane & 7;
-    const int per_chunk = p.hkv * p.hsplit;
-
-    // ---- prologue: item offsets off[b] = sum_{j<b} items(j) (exclusive scan) ----
-    {
-        const int B = p.batch;
-        const int seg = (B + kThreads - 1) / kThreads;
-        const int lo = min(B, tid * seg), hi = min(B, lo + seg);
-        int local = 0;
-        for (int b = lo; b < hi; ++b) {
-            int64_t base;
-            const int L = key_count(p, b, base, false);
-            local += max(1, (L + p.chunk - 1) / p.chunk) * per_chunk;
-        }
-        int incl = local;
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        if (lane == 31) red_m[warp] = __int_as_float(incl);
-        __syncthreads();
-        int wbase = 0;
-        for (int w = 0; w < warp; ++w) wbase += __float_as_int(red_m[w]);
-        int run = wbase + incl - local;
-        for (int b = lo; b < hi; ++b) {
-            off[b] = run;
-            int64_t base;
-            const int L = key_count(p, b, base, false);
-            run += max(1, (L + p.chunk - 1) / p.chunk) * per_chunk;
-        }
-        if (tid == kThreads - 1) off[B] = wbase + incl;
-        __syncthreads();
-    }
+    build_item_table(p, off, scan_scratch, kThreads);
     const int total = off[p.batch];
 
     for (int w = blockIdx.x; w < total; w += gridDim.x) {
-        // ---- locate the item ----
-        int lo = 0, hi = p.batch;  // find b with off[b] <= w < off[b+1]
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (off[mid] <= w) lo = mid; else hi = mid;
-        }
-        const int b = lo;
-        int rem = w - off[b];
-        const int hs = rem % p.hsplit;
-        rem /= p.hsplit;
-        const int kh = rem % p.hkv;
-        const int c = rem / p.hkv;
-        int64_t base;
-        const int L = key_count(p, b, base, tid == 0 && c == 0 && kh == 0 && hs == 0);
-        const int n_chunks = max(1, (L + p.chunk - 1) / p.chunk);
-        const int head0 = kh * p.g + hs * GC;
-        const int t_begin = c * p.chunk;
-        const int t_end = min(L, t_begin + p.chunk);
-
-        if (t_end <= t_begin) {  // empty request: zero output, lse = -inf
-            for (int i = tid; i < GC * D; i += kThreads) {
-                const int h = i / D, d = i % D;
-                p.out[(static_cast<int64_t>(b) * p.hq + head0 + h) * D + d] = 0;
-                if (d == 0 && p.lse) p.lse[static_cast<int64_t>(b) * p.hq + head0 + h] = -INFINITY;
-            }
+        const Item it = locate<GC>(p, off, w, threadIdx.x == 0);
+        if (it.t_end <= it.t_begin) {
+            write_empty<D, GC>(p, it);
             continue;
         }
-
-        // ---- q slice in registers, pre-scaled into the base-2 domain ----
-        float qr[GC][NC][8];
-#pragma unroll
-        for (int h = 0; h < GC; ++h)
-#pragma unroll
-            for (int ci = 0; ci < NC; ++ci) {
-                const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
-                    p.q + (static_cast<int64_t>(b) * p.hq + head0 + h) * D + (part + 8 * ci) * 8));
-                widen8(raw, qr[h][ci]);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) qr[h][ci][e] *= p.scale_log2;
-            }
-        float o[GC][NC][8];
-        float m[GC], l[GC];
-#pragma unroll
-        for (int h = 0; h < GC; ++h) {
-            m[h] = -INFINITY;
-            l[h] = 0.f;
-#pragma unroll
-            for (int ci = 0; ci < NC; ++ci)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[h][ci][e] = 0.f;
-        }
-
-        // ---- pipelined tile loop ----
-        const int n_tiles = (t_end - t_begin + kTile - 1) / kTile;
+        typename M::State st;
+        M::begin(st, p, it);
+        const int n_tiles = (it.t_end - it.t_begin + kTile - 1) / kTile;
 #pragma unroll
         for (int s = 0; s < kStages - 1; ++s) {
             if (s < n_tiles) {
-                uint16_t *ks = tiles + s * 2 * S::kTileElems;
-                load_tile<D>(p, ks, ks + S::kTileElems, base, t_begin + s * kTile, t_end, kh);
+                uint16_t *kst = tiles + s * 2 * T::kElems;
+                load_tile_cp_async<D>(p, kst, kst + T::kElems, it.base, it.t_begin + s * kTile, it.t_end, it.kh);
             }
             cp_async_commit();
         }
-        for (int it = 0; it < n_tiles; ++it) {
+        for (int ti = 0; ti < n_tiles; ++ti) {
             cp_async_wait<kStages - 2>();
             __syncthreads();
             {
-                const int nt = it + kStages - 1;
-                if (nt < n_tiles) {
-                    uint16_t *ks = tiles + (nt % kStages) * 2 * S::kTileElems;
-                    load_tile<D>(p, ks, ks + S::kTileElems, base, t_begin + nt * kTile, t_end, kh);
+                const int nt_ = ti + kStages - 1;
+                if (nt_ < n_tiles) {
+                    uint16_t *kst = tiles + (nt_ % kStages) * 2 * T::kElems;
+                    load_tile_cp_async<D>(p, kst, kst + T::kElems, it.base, it.t_begin + nt_ * kTile, it.t_end,
+                                          it.kh);
                 }
                 cp_async_commit();
             }
-            const uint16_t *ks = tiles + (it % kStages) * 2 * S::kTileElems;
-            const uint16_t *vs = ks + S::kTileElems;
-            const int n_valid = t_end - (t_begin + it * kTile);
-
-            float s[4][GC];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int key = warp * 16 + j * 4 + grp;
-#pragma unroll
-                for (int h = 0; h < GC; ++h) s[j][h] = 0.f;
-#pragma unroll
-                for (int ci = 0; ci < NC; ++ci) {
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(ks + key * D + (part + 8 * ci) * 8);
-                    float kf[8];
-                    widen8(raw, kf);
-#pragma unroll
-                    for (int h = 0; h < GC; ++h)
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) s[j][h] = fmaf(qr[h][ci][e], kf[e], s[j][h]);
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-#pragma unroll
-                for (int h = 0; h < GC; ++h) {
-                    float v = s[j][h];
-                    v += __shfl_xor_sync(0xffffffffu, v, 1);
-                    v += __shfl_xor_sync(0xffffffffu, v, 2);
-                    v += __shfl_xor_sync(0xffffffffu, v, 4);
-                    s[j][h] = (warp * 16 + j * 4 + grp < n_valid) ? v : -INFINITY;
-                }
-#pragma unroll
-            for (int h = 0; h < GC; ++h) {
-                const float mt = fmaxf(fmaxf(s[0][h], s[1][h]), fmaxf(s[2][h], s[3][h]));
-                if (mt > m[h]) {
-                    const float corr = ex2(m[h] - mt);  // m = -inf gives 0
-                    l[h] *= corr;
-#pragma unroll
-                    for (int ci = 0; ci < NC; ++ci)
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) o[h][ci][e] *= corr;
-                    m[h] = mt;
-                }
-                const bool live = m[h] != -INFINITY;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    s[j][h] = live ? ex2(s[j][h] - m[h]) : 0.f;
-                    l[h] += s[j][h];
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int key = warp * 16 + j * 4 + grp;
-#pragma unroll
-                for (int ci = 0; ci < NC; ++ci) {
-                    const uint4 raw = *reinterpret_cast<const uint4 *>(vs + key * D + (part + 8 * ci) * 8);
-                    float vf[8];
-                    widen8(raw, vf);
-#pragma unroll
-                    for (int h = 0; h < GC; ++h)
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) o[h][ci][e] = fmaf(s[j][h], vf[e], o[h][ci][e]);
-                }
-            }
+            const uint16_t *kt = tiles + (ti % kStages) * 2 * T::kElems;
+            M::tile(st, kt, kt + T::kElems, it.t_end - (it.t_begin + ti * kTile), p.scale_log2);
         }
         cp_async_wait<0>();
-
-        // ---- combine the four lane groups of each warp ----
-#pragma unroll
-        for (int h = 0; h < GC; ++h) {
-            float mw = fmaxf(m[h], __shfl_xor_sync(0xffffffffu, m[h], 8));
-            mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 16));
-            const float corr = (m[h] == -INFINITY) ? 0.f : ex2(m[h] - mw);
-            float lw = l[h] * corr;
-            lw += __shfl_xor_sync(0xffffffffu, lw, 8);
-            lw += __shfl_xor_sync(0xffffffffu, lw, 16);
-#pragma unroll
-            for (int ci = 0; ci < NC; ++ci)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    float v = o[h][ci][e] * corr;
-                    v += __shfl_xor_sync(0xffffffffu, v, 8);
-                    v += __shfl_xor_sync(0xffffffffu, v, 16);
-                    o[h][ci][e] = v;
-                }
-            m[h] = mw;
-            l[h] = lw;
-        }
-        if (grp == 0) {
-#pragma unroll
-            for (int h = 0; h < GC; ++h) {
-#pragma unroll
-                for (int ci = 0; ci < NC; ++ci)
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) red_o[(warp * kMaxGc + h) * D + (part + 8 * ci) * 8 + e] = o[h][ci][e];
-                if (part == 0) {
-                    red_m[warp * kMaxGc + h] = m[h];
-                    red_l[warp * kMaxGc + h] = l[h];
-                }
-            }
-        }
+        M::store(st, red_o, red_m, red_l);
         __syncthreads();
-
-        // ---- combine warps and write ----
-        const int64_t pidx = ((static_cast<int64_t>(b) * p.hkv + kh) * p.hsplit + hs) * p.n_chunks_max + c;
-        for (int i = tid; i < GC * D; i += kThreads) {
-            const int h = i / D, d = i % D;
-            float M = -INFINITY;
-#pragma unroll
-            for (int ww = 0; ww < kWarps; ++ww) M = fmaxf(M, red_m[ww * kMaxGc + h]);
-            float num = 0.f, den = 0.f;
-#pragma unroll
-            for (int ww = 0; ww < kWarps; ++ww) {
-                const float mw = red_m[ww * kMaxGc + h];
-                const float sc = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-                num = fmaf(red_o[(ww * kMaxGc + h) * D + d], sc, num);
-                den = fmaf(red_l[ww * kMaxGc + h], sc, den);
-            }
-            const float val = num / den;
-            if (n_chunks == 1) {
-                p.out[(static_cast<int64_t>(b) * p.hq + head0 + h) * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(val));
-                if (d == 0 && p.lse) p.lse[static_cast<int64_t>(b) * p.hq + head0 + h] = (M + log2f(den)) * kLn2;
-            } else {
-                p.part_o[(pidx * GC + h) * D + d] = val;
-                if (d == 0) p.part_lse[pidx * GC + h] = M + log2f(den);
-            }
-        }
+        finish_item<D, GC>(p, it, red_o, red_m, red_l);
         __syncthreads();
     }
 }
 
+// ---------------------------------------------------------------- TMA kernel (page_size >= 8, varlen)
+// Warp-specialised: warps 0-3 do the math, warp 4 (one lane) is the producer.
+// The producer walks the same item sequence as the math warps and, for every
+// 64-key tile, issues one TMA box per page (box = min(ps, 64) keys x 64 dims,
+// 128-byte swizzle; D = 128 takes two boxes per page) into a free stage, with
+// completion counted in bytes on that stage's full barrier.  It runs up to
+// kTmaStages tiles ahead, across item boundaries, so the next item's K/V is in
+// flight while the math warps reduce and write the current one.  Math warps
+// release a stage through its empty barrier.  Key rows past the item's end
+// (and rows of pages that do not exist) may hold stale data: K is masked by
+// the scores' select, V rows are zeroed by the warp that reads them.
+// Bounded mbarrier wait shared by the producer and the math warps: gives up
+// when another warp already gave up (abort flag) or after ~2 s, raising
+// PKV_DEVERR_TIMEOUT once; afterwards no warp of the CTA waits again.
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int32_t *err) {
+    if (*abort_flag) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63) == 0) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > 2000000000ull) {
+                *abort_flag = 1;
+                raise_flag(err, PKV_DEVERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+template <int D>
+struct TmaCfg {
+    static constexpr int kStagesN = D == 128 ? 3 : 5;
+};
+
+template <int D, int GC, bool MMA>
+__global__ void __launch_bounds__(kThreads + 32, 1)
+decode_tma_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+    using T = Tile<D>;
+    using M = Math<D, GC, MMA>;
+    constexpr int S = TmaCfg<D>::kStagesN;
+    extern __shared__ unsigned char smem_raw[];
+    // 1024-byte alignment for the 128-byte swizzle atoms
+    unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    uint16_t *tiles = reinterpret_cast<uint16_t *>(smem);
+    float *red_o = reinterpret_cast<float *>(smem + S * T::kStageBytes);
+    float *red_m = red_o + kWarps * GC * D;
+    float *red_l = red_m + kWarps * GC;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + S * T::kStageBytes + RedLayout<D, GC>::kBytes);
+    uint64_t *empty = full + S;
+    int *scan = reinterpret_cast<int *>(empty + S);
+    volatile int *abort_flag = scan + 7;
+    int *off = scan + 8;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        *abort_flag = 0;
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kWarps);
+        }
+        mbar_init_fence();
+    }
+    if (warp == kWarps && lane == 0) {
+        prefetch_tmap(&tmk);
+        prefetch_tmap(&tmv);
+    }
+    build_item_table(p, off, scan, kThreads + 32);
+    const int total = off[p.batch];
+
+    if (warp == kWarps) {
+        // ---------------- producer ----------------
+        // Lane j owns box j of every tile (kTile / box <= 8 boxes).  The page ids
+        // of tile n+1 are loaded before tile n is issued, so the table lookups
+        // overlap the wait for a free stage.
+        const int box = p.box_rows;
+        const int nbox = kTile / box;
+        const uint32_t box_bytes = static_cast<uint32_t>(box) * 128u;
+        const bool own = lane < nbox;
+        // cursor over (item, tile), skipping empty items
+        int w = blockIdx.x, ti = 0;
+        Item it{};
+        bool have = false;
+        auto next_item = [&]() {
+            while (w < total) {
+                it = locate<GC>(p, off, w, false);
+                if (it.t_end > it.t_begin) return true;
+                w += gridDim.x;
+            }
+            return false;
+        };
+        have = next_item();
+        // row of this lane's box for the cursor's tile (-1: no box, -2: bad page)
+        auto lookup = [&]() -> int {
+            if (!have || !own) return -1;
+            const int tb = it.t_begin + ti * kTile + lane * box;
+            if (tb >= it.t_end) return -1;
+            if (p.layout == PKV_LAYOUT_VARLEN) return static_cast<int>(it.base + tb);
+            const int32_t *tab = p.layout == PKV_LAYOUT_CSR ? p.kv_indices : p.block_table;
+            const int page = __ldg(tab + it.base + (tb >> p.ps_shift));
+            if (page < 0 || page >= p.num_pages) return -2;
+            return static_cast<int>((static_cast<int64_t>(page) << p.ps_shift) + (tb & p.ps_mask));
+        };
+        int row = lookup();
+        for (uint32_t n = 0; have; ++n) {
+            const int kh = it.kh;
+            // advance the cursor and start the next tile's lookups
+            const int n_tiles = (it.t_end - it.t_begin + kTile - 1) / kTile;
+            if (++ti >= n_tiles) {
+                ti = 0;
+                w += gridDim.x;
+                have = next_item();
+            }
+            const int next_row = lookup();
+            const int s = n % S;
+            bool ok = true;
+            if (lane == 0) ok = wait_or_abort(&empty[s], ((n / S) & 1) ^ 1, abort_flag, p.err);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) return;
+            if (row == -2) raise_flag(p.err, PKV_DEVERR_RANGE);
+            const uint32_t valid = __ballot_sync(0xffffffffu, row >= 0);
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], __popc(valid) * box_bytes * T::kSlabs * 2u);
+            __syncwarp();
+            if (row >= 0) {
+                unsigned char *kst = smem + s * T::kStageBytes;
+                unsigned char *vst = kst + T::kBytes;
+#pragma unroll
+                for (int h = 0; h < T::kSlabs; ++h) {
+                    tma_load_3d(kst + h * (kTile * 128) + lane * box_bytes, &tmk, h * 64, kh, row, &full[s]);
+                    tma_load_3d(vst + h * (kTile * 128) + lane * box_bytes, &tmv, h * 64, kh, row, &full[s]);
+                }
+            }
+            row = next_row;
+        }
+        return;
+    }
+
+    // ---------------- math warps ----------------
+    uint32_t n = 0;
+    for (int w = blockIdx.x; w < total; w += gridDim.x) {
+        const Item it = locate<GC>(p, off, w, tid == 0);
+        if (it.t_end <= it.t_begin) {
+            write_empty<D, GC>(p, it);
+            continue;
+        }
+        typename M::State st;
+        M::begin(st, p, it);
+        const int n_tiles = (it.t_end - it.t_begin + kTile - 1) / kTile;
+        for (int ti = 0; ti < n_tiles; ++ti, ++n) {
+            const int s = n % S;
+            if (!wait_or_abort(&full[s], (n / S) & 1, abort_flag, p.err)) {
+                // abandoned launch: keep releasing stages and reaching barriers, compute nothing
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+                continue;
+            }
+            uint16_t *kt = tiles + s * 2 * T::kElems;
+            uint16_t *vt = kt + T::kElems;
+            const int n_valid = it.t_end - (it.t_begin + ti * kTile);
+            if (n_valid < kTile) {
+                // zero the V rows of this warp's keys past the end (stale or never loaded)
+                for (int i = lane; i < 16 * (D / 8); i += 32) {
+                    const int key = warp * 16 + i / (D / 8);
+                    if (key >= n_valid)
+                        *reinterpret_cast<uint4 *>(vt + toff<D>(key, i % (D / 8))) = make_uint4(0, 0, 0, 0);
+                }
+                __syncwarp();
+            }
+            M::tile(st, kt, vt, n_valid, p.scale_log2);
+            if (n_valid < kTile) fence_proxy_async_smem();  // generic writes before the next TMA into this stage
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        M::store(st, red_o, red_m, red_l);
+        named_bar_sync(1, kThreads);
+        finish_item<D, GC>(p, it, red_o, red_m, red_l);
+        named_bar_sync(1, kThreads);
+    }
+}
+
+// ---------------------------------------------------------------- merge
 // Log-sum-exp merge of a request's chunk partials (base-2 lse inside the workspace).
 template <int D, int GC>
 __global__ void __launch_bounds__(kThreads) merge_kernel(const Params p) {
@@ -402,7 +809,7 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const Params p) {
     const int n = (L + p.chunk - 1) / p.chunk;
     if (n <= 1) return;
     const int64_t pbase = ((static_cast<int64_t>(b) * p.hkv + kh) * p.hsplit + hs) * p.n_chunks_max;
-    __shared__ float den_s[kMaxGc], mx_s[kMaxGc];
+    __shared__ float den_s[kMaxRows], mx_s[kMaxRows];
     for (int i = threadIdx.x; i < GC * n; i += kThreads) {
         const int h = i / n, c = i % n;
         wsm[h * p.n_chunks_max + c] = p.part_lse[(pbase + c) * GC + h];
@@ -426,7 +833,8 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const Params p) {
     for (int i = threadIdx.x; i < GC * D; i += kThreads) {
         const int h = i / D, d = i % D;
         float acc = 0.f;
-        for (int c = 0; c < n; ++c) acc = fmaf(wsm[h * p.n_chunks_max + c], p.part_o[((pbase + c) * GC + h) * D + d], acc);
+        for (int c = 0; c < n; ++c)
+            acc = fmaf(wsm[h * p.n_chunks_max + c], p.part_o[((pbase + c) * GC + h) * D + d], acc);
         acc /= den_s[h];
         p.out[(static_cast<int64_t>(b) * p.hq + head0 + h) * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
         if (d == 0 && p.lse) p.lse[static_cast<int64_t>(b) * p.hq + head0 + h] = (mx_s[h] + log2f(den_s[h])) * kLn2;
@@ -435,6 +843,7 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const Params p) {
 
 // ------------------------------------------------------------------ host side
 struct Plan {
+    bool mma;
     int gc, hsplit, chunk, n_chunks_max;
     size_t part_o_bytes, part_lse_bytes;
 };
@@ -453,7 +862,10 @@ static int choose_chunk(const pkv_decode_args *a, int units) {
 
 static pkv_status make_plan(const pkv_decode_args *a, Plan &pl) {
     const int g = a->num_q_heads / a->num_kv_heads;
-    pl.gc = std::min(g, kMaxGc);
+    // GQA groups go to the tensor-core kernel (up to 16 heads as MMA rows);
+    // a single head per kv head (MHA) stays on CUDA cores.
+    pl.mma = g >= 2;
+    pl.gc = pl.mma ? std::min(g, kMaxRows) : 1;
     pl.hsplit = g / pl.gc;
     pl.chunk = a->kv_chunk > 0 ? a->kv_chunk : choose_chunk(a, a->num_kv_heads * pl.hsplit);
     pl.n_chunks_max = std::max(1, (a->max_seq_len + pl.chunk - 1) / pl.chunk);
@@ -514,36 +926,87 @@ size_t workspace_size(const pkv_decode_args *a) {
     return pl.part_o_bytes + pl.part_lse_bytes;
 }
 
-template <int D, int GC>
-static pkv_status launch_t(const Params &p, cudaStream_t s) {
-    using S = Smem<D>;
-    const size_t smem = S::kFixedBytes + (static_cast<size_t>(p.batch) + 1) * 4;
-    static int configured_smem = 0;
-    if (configured_smem < 227 * 1024) {
-        if (cudaFuncSetAttribute(decode_kernel<D, GC>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
-            cudaSuccess)
-            return fail(PKV_ERR_CUDA, "pkv_decode: cannot raise the shared-memory limit");
-        configured_smem = 227 * 1024;
-    }
-    if (smem > 227 * 1024) return fail(PKV_ERR_UNSUPPORTED, "pkv_decode: batch too large for the on-chip item table");
+// Opt-in dynamic shared memory of a kernel (device limit minus its static part), set once.
+template <typename K>
+static pkv_status smem_limit(K kernel, size_t &lim) {
+    int optin = 0, dev = 0;
+    cudaFuncAttributes fa{};
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaFuncGetAttributes(&fa, kernel) != cudaSuccess)
+        return fail(PKV_ERR_CUDA, "pkv_decode: cannot query shared-memory limits");
+    lim = static_cast<size_t>(optin) - fa.sharedSizeBytes;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(lim)) != cudaSuccess)
+        return fail(PKV_ERR_CUDA, "pkv_decode: cannot raise the shared-memory limit to %zu bytes", lim);
+    return PKV_OK;
+}
+
+template <typename K>
+static int persistent_grid(K kernel, int threads, size_t smem, const Params &p) {
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, decode_kernel<D, GC>, kThreads, smem) != cudaSuccess ||
-        occ < 1)
-        occ = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, smem) != cudaSuccess || occ < 1) occ = 1;
     const int64_t upper = static_cast<int64_t>(p.batch) * p.hkv * p.hsplit * p.n_chunks_max;
-    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(upper, static_cast<int64_t>(sm_count()) * occ)));
-    decode_kernel<D, GC><<<grid, kThreads, smem, s>>>(p);
-    pkv_status st = check_launch("pkv_decode(GQA split kernel)");
-    if (st != PKV_OK || p.n_chunks_max == 1) return st;
+    return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(upper, static_cast<int64_t>(sm_count()) * occ)));
+}
+
+template <int D, int GC>
+static pkv_status launch_merge(const Params &p, cudaStream_t s) {
+    if (p.n_chunks_max == 1) return PKV_OK;
     const size_t msmem = static_cast<size_t>(GC) * p.n_chunks_max * 4;
     if (msmem > 200 * 1024) return fail(PKV_ERR_UNSUPPORTED, "pkv_decode: too many splits for the merge");
     if (msmem > 48 * 1024) {
         if (cudaFuncSetAttribute(merge_kernel<D, GC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(std::min<size_t>(msmem, 227 * 1024))) != cudaSuccess)
+                                 static_cast<int>(msmem)) != cudaSuccess)
             return fail(PKV_ERR_CUDA, "pkv_decode: cannot raise the merge shared-memory limit");
     }
     merge_kernel<D, GC><<<p.batch * p.hkv * p.hsplit, kThreads, msmem, s>>>(p);
     return check_launch("pkv_decode(GQA merge kernel)");
+}
+
+template <int D, int GC, bool MMA>
+static pkv_status launch_t(const Params &p, const pkv_decode_args *a, bool tma, cudaStream_t s) {
+    using T = Tile<D>;
+    pkv_status st;
+    if (tma) {
+        const auto kernel = decode_tma_kernel<D, GC, MMA>;
+        static size_t lim = 0;
+        if (!lim && (st = smem_limit(kernel, lim)) != PKV_OK) return st;
+        const size_t smem = 1024 + TmaCfg<D>::kStagesN * T::kStageBytes + RedLayout<D, GC>::kBytes +
+                            2 * TmaCfg<D>::kStagesN * 8 + 32 + (static_cast<size_t>(p.batch) + 1) * 4;
+        if (smem > lim) return fail(PKV_ERR_UNSUPPORTED, "pkv_decode: batch too large for the on-chip item table");
+        CUtensorMap tmk, tmv;
+        const uint64_t rows = static_cast<uint64_t>(a->num_slots);
+        const uint64_t dk[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(p.hkv), rows};
+        const uint64_t sk[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(p.k_stride) * 2};
+        const uint64_t sv[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(p.v_stride) * 2};
+        const uint32_t box[3] = {64, 1, static_cast<uint32_t>(p.box_rows)};
+        if (!encode_tmap_bf16(&tmk, a->k_pool, 3, dk, sk, box) || !encode_tmap_bf16(&tmv, a->v_pool, 3, dk, sv, box))
+            return fail(PKV_ERR_CUDA, "pkv_decode: cuTensorMapEncodeTiled rejected the pool layout");
+        const int grid = persistent_grid(kernel, kThreads + 32, smem, p);
+        kernel<<<grid, kThreads + 32, smem, s>>>(p, tmk, tmv);
+    } else {
+        const auto kernel = decode_cp_async_kernel<D, GC, MMA>;
+        static size_t lim = 0;
+        if (!lim && (st = smem_limit(kernel, lim)) != PKV_OK) return st;
+        const size_t smem = kStages * T::kStageBytes + RedLayout<D, GC>::kBytes + (static_cast<size_t>(p.batch) + 1) * 4;
+        if (smem > lim) return fail(PKV_ERR_UNSUPPORTED, "pkv_decode: batch too large for the on-chip item table");
+        const int grid = persistent_grid(kernel, kThreads, smem, p);
+        kernel<<<grid, kThreads, smem, s>>>(p);
+    }
+    st = check_launch("pkv_decode(GQA split kernel)");
+    if (st != PKV_OK) return st;
+    return launch_merge<D, GC>(p, s);
+}
+
+template <int D>
+static pkv_status launch_d(const Plan &pl, const Params &p, const pkv_decode_args *a, bool tma, cudaStream_t s) {
+    if (!pl.mma) return launch_t<D, 1, false>(p, a, tma, s);
+    switch (pl.gc) {
+        case 2: return launch_t<D, 2, true>(p, a, tma, s);
+        case 4: return launch_t<D, 4, true>(p, a, tma, s);
+        case 8: return launch_t<D, 8, true>(p, a, tma, s);
+        default: return launch_t<D, 16, true>(p, a, tma, s);
+    }
 }
 
 pkv_status launch(const pkv_decode_args *a, void *ws, size_t ws_bytes, int32_t *err, cudaStream_t s) {
@@ -590,15 +1053,11 @@ pkv_status launch(const pkv_decode_args *a, void *ws, size_t ws_bytes, int32_t *
     p.part_o = static_cast<float *>(ws);
     p.part_lse = reinterpret_cast<float *>(static_cast<char *>(ws) + pl.part_o_bytes);
     p.err = err;
-    const int D = a->head_dim_qk;
-    if (D == 128) {
-        if (pl.gc == 1) return launch_t<128, 1>(p, s);
-        if (pl.gc == 2) return launch_t<128, 2>(p, s);
-        return launch_t<128, 4>(p, s);
-    }
-    if (pl.gc == 1) return launch_t<64, 1>(p, s);
-    if (pl.gc == 2) return launch_t<64, 2>(p, s);
-    return launch_t<64, 4>(p, s);
+    // Whole pages of >= 8 keys (or contiguous rows) stream in as TMA boxes; smaller
+    // pages are gathered row by row with cp.async.
+    const bool tma = (a->layout == PKV_LAYOUT_VARLEN || a->page_size >= 8) && a->num_slots <= INT32_MAX;
+    p.box_rows = a->layout == PKV_LAYOUT_VARLEN ? kTile : std::min(a->page_size, kTile);
+    return a->head_dim_qk == 128 ? launch_d<128>(pl, p, a, tma, s) : launch_d<64>(pl, p, a, tma, s);
 }
 
 }  // namespace gqa
