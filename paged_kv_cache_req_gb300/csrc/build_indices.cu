@@ -60,22 +60,24 @@ build_indices_kernel(const int32_t *__restrict__ r2t, int64_t r2t_rows, int64_t 
 
     const int32_t *row = r2t + (valid ? req_pool_idx[b] * row_stride + (kv_start ? kv_start[b] : 0) : 0);
     const int64_t pool_slots = num_pool_pages * ps;
+    const bool pow2 = (ps & (ps - 1)) == 0;
+    const int shift = __ffs(ps) - 1;
+    const int Li = static_cast<int>(L);
     int bad = 0;
-    for (int64_t t = threadIdx.x; t < L; t += kThreads) {
-        const int64_t off = t % ps;
+    for (int t = threadIdx.x; t < Li; t += kThreads) {
+        const int off = pow2 ? (t & (ps - 1)) : (t % ps);
+        const int pg = pow2 ? (t >> shift) : (t / ps);
         const int64_t head = __ldg(row + (t - off));   // slot of this page's first position
-        const int64_t slot = off ? __ldg(row + t) : head;
         if (off == 0) {
             if (head < 0 || head >= pool_slots) {
                 bad |= PKV_DEVERR_RANGE;
                 continue;
             }
-            if (head % ps != 0) bad |= PKV_DEVERR_CONTIG;
-            const int32_t page = static_cast<int32_t>(head / ps);
-            const long long p = t / ps;
-            if (kv_indices && before + p < cap) kv_indices[before + p] = page;
-            if (block_table && p < bt_width) block_table[static_cast<int64_t>(b) * bt_width + p] = page;
-        } else if (slot != head + off) {
+            if ((pow2 ? (head & (ps - 1)) : (head % ps)) != 0) bad |= PKV_DEVERR_CONTIG;
+            const int32_t page = static_cast<int32_t>(pow2 ? (head >> shift) : (head / ps));
+            if (kv_indices && before + pg < cap) kv_indices[before + pg] = page;
+            if (block_table && pg < bt_width) block_table[static_cast<int64_t>(b) * bt_width + pg] = page;
+        } else if (__ldg(row + t) != head + off) {
             bad |= PKV_DEVERR_CONTIG;
         }
     }

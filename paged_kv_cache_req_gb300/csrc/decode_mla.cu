@@ -1,23 +1,790 @@
-// pkv_decode for MLA (latent attention over a single latent kv head).
+// pkv_decode for MLA: 128 query heads per item attending over one latent KV
+// head through a page table, on the 5th-generation tensor cores.
+//
+// Each latent row holds kv_lora_rank + rope dims (512 + 64); keys are the whole
+// row, values its first 512 entries (AttentionBackend notes: FlashMLA metadata
+// with num_kv_heads 1, kv_lora_rank and qk_rope_head_dim; block table padded
+// with -1, page_size 64).  For a decode token the work per key is
+// 128 x (576 + 512) x 2 flops on 1152 bytes, close to the HBM/tensor ridge.
+//
+// The fp32 output accumulator of 128 heads x 512 dims fills all of an SM's
+// tensor memory, so a 2-CTA cluster shares each work item (request, key chunk,
+// 128-head group):
+//   CTA 0 owns latent dims [0, 256): it computes the partial scores over them
+//          and accumulates output dims [0, 256);
+//   CTA 1 owns dims [256, 576): partial scores over them, output dims [256, 512).
+// The two partial score tiles (128 heads x 64 keys, fp32) are swapped through
+// distributed shared memory, so both CTAs hold identical full scores and run
+// the same softmax; nothing is loaded or multiplied twice.
+//
+// Per CTA: warp 4 is the TMA producer (the item's Q once, then one 64-key tile
+// per stage, one box per page per 64-dim slab, 128-byte swizzle), warp 5 issues
+// tcgen05 MMAs from one thread (S = Q K^T into a double-buffered TMEM tile,
+// O += P V into 256 TMEM columns, V read as an MN-major operand of the same
+// slabs), warps 0-3 own one head per TMEM lane: read S, exchange, online
+// softmax (base 2, running max raised only past 2^8 headroom so O rescales in
+// TMEM are rare), write P to shared memory, and finally normalise O.
+// Every wait is bounded (~2 s) and an abort flag lets the CTA drain instead of
+// hanging.
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
 #include "pkv_internal.cuh"
+#include "tc05.cuh"
 
 namespace pkv {
 namespace mla {
 
+constexpr int kDqk = 576, kDv = 512, kHeads = 128, kTile = 64;
+constexpr int kVSlabs = 4;                 // 256 value dims per CTA
+constexpr int kMaxSlabs = 5;               // q.k slabs of the wider CTA
+constexpr int kStages = 2;
+constexpr int kThreads = 192;              // warps 0-3 softmax, 4 producer, 5 MMA
+constexpr int kProducerWarp = 4, kMmaWarp = 5;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;              // two 64-column score tiles
+constexpr uint32_t kColO = 128;            // 256-column output accumulator
+constexpr float kLn2 = 0.69314718055994531f;
+constexpr float kLog2e = 1.44269504088896341f;
+constexpr float kLazy = 8.f;
+
+// shared-memory carve-up (bytes from a 1024-aligned base)
+constexpr int kQBytes = kMaxSlabs * kHeads * 128;           // 80 KB
+constexpr int kSlabBytes = kTile * 128;                     // 8 KB: 64 keys x 64 dims
+constexpr int kStageBytes = kMaxSlabs * kSlabBytes;         // 40 KB
+constexpr int kOffQ = 0;
+constexpr int kOffKV = kOffQ + kQBytes;
+constexpr int kOffP = kOffKV + kStages * kStageBytes;       // P: 128 heads x 64 keys bf16, SW128
+constexpr int kOffX = kOffP + kHeads * 128;                 // peer partial scores, fp32 [128][64]
+constexpr int kOffBar = kOffX + kHeads * kTile * 4;
+constexpr int kNumBars = 20;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;            // tmem slot, abort flag, scan scratch
+constexpr int kOffTable = kOffMisc + 64;
+constexpr int kFixedSmem = kOffTable + 1024;                // + item table + alignment slack
+
+struct Params {
+    int32_t layout;
+    int32_t batch, hq, hgroups;
+    int32_t ps_shift, ps_mask;
+    float scale_log2;
+    int32_t chunk, n_chunks_max;
+    int32_t bt_width;
+    int32_t box_rows;
+    int64_t num_slots, num_pages, kv_indices_len;
+    const int32_t *kv_indptr, *kv_indices, *kv_last, *block_table, *seq_lens, *cu_seqlens;
+    uint16_t *out;
+    float *lse;
+    float *part_o, *part_lse;
+    int32_t *err;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ int key_count(const Params &p, int b, int64_t &base, bool report) {
+    int64_t L, cap;
+    if (p.layout == PKV_LAYOUT_CSR) {
+        const int64_t lo = p.kv_indptr[b], hi = p.kv_indptr[b + 1];
+        const int64_t n = hi - lo;
+        const int last = n > 0 ? p.kv_last[b] : 0;
+        base = lo;
+        if (lo < 0 || n < 0 || hi > p.kv_indices_len || (n > 0 && (last < 1 || last > (1 << p.ps_shift)))) {
+            if (report) raise_flag(p.err, PKV_DEVERR_RANGE);
+            base = 0;
+            return 0;
+        }
+        L = n > 0 ? ((n - 1) << p.ps_shift) + last : 0;
+        cap = L;
+    } else if (p.layout == PKV_LAYOUT_BLOCK_TABLE) {
+        base = static_cast<int64_t>(b) * p.bt_width;
+        L = p.seq_lens[b];
+        cap = static_cast<int64_t>(p.bt_width) << p.ps_shift;
+    } else {
+        base = p.cu_seqlens[b];
+        L = static_cast<int64_t>(p.cu_seqlens[b + 1]) - base;
+        cap = L;
+    }
+    const int64_t limit = min(cap, static_cast<int64_t>(p.chunk) * p.n_chunks_max);
+    if (L < 0 || L > limit) {
+        if (report) raise_flag(p.err, L < 0 ? PKV_DEVERR_RANGE : PKV_DEVERR_CAPACITY);
+        L = L < 0 ? 0 : limit;
+    }
+    return static_cast<int>(L);
+}
+
+struct Item {
+    int b, c, hg, L, n_chunks, t_begin, t_end, n_tiles;
+    int64_t base;
+};
+
+__device__ __forceinline__ Item locate(const Params &p, const int *off, int w, bool report) {
+    Item it;
+    int lo = 0, hi = p.batch;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (off[mid] <= w) lo = mid; else hi = mid;
+    }
+    it.b = lo;
+    const int rem = w - off[lo];
+    it.hg = rem % p.hgroups;
+    it.c = rem / p.hgroups;
+    it.L = key_count(p, it.b, it.base, report && it.c == 0 && it.hg == 0);
+    it.n_chunks = max(1, (it.L + p.chunk - 1) / p.chunk);
+    it.t_begin = it.c * p.chunk;
+    it.t_end = min(it.L, it.t_begin + p.chunk);
+    it.n_tiles = it.t_end > it.t_begin ? (it.t_end - it.t_begin + kTile - 1) / kTile : 0;
+    return it;
+}
+
+// Item table shared by every CTA (same construction as the GQA kernels).
+__device__ __forceinline__ void build_item_table(const Params &p, int *off, int *scratch) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int B = p.batch;
+    const int seg = (B + kThreads - 1) / kThreads;
+    const int lo = min(B, tid * seg), hi = min(B, lo + seg);
+    int local = 0;
+    for (int b = lo; b < hi; ++b) {
+        int64_t base;
+        const int L = key_count(p, b, base, false);
+        local += max(1, (L + p.chunk - 1) / p.chunk) * p.hgroups;
+    }
+    int incl = local;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) scratch[warp] = incl;
+    __syncthreads();
+    int wbase = 0;
+    for (int w = 0; w < warp; ++w) wbase += scratch[w];
+    int run = wbase + incl - local;
+    for (int b = lo; b < hi; ++b) {
+        off[b] = run;
+        int64_t base;
+        const int L = key_count(p, b, base, false);
+        run += max(1, (L + p.chunk - 1) / p.chunk) * p.hgroups;
+    }
+    if (tid == kThreads - 1) off[B] = wbase + incl;
+    __syncthreads();
+}
+
+// Bounded wait (local or cluster-scope acquire) with the CTA-wide abort flag.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int32_t *err,
+                                         bool cluster_scope = false) {
+    auto poll = [&]() { return cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (*abort_flag) return false;
+    if (poll()) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (poll()) return true;
+        if ((i & 63) == 0) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > 2000000000ull) {
+                *abort_flag = 1;
+                raise_flag(err, PKV_DEVERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag: used only to drain work this CTA
+// itself started (MMAs, TMA copies) before its TMEM and shared memory go away.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait(bar, parity)) return;
+        if ((i & 63) == 63 && global_ns() - t0 > 2000000000ull) return;
+    }
+}
+
+enum Bar {
+    kQFull = 0, kQEmpty, kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kSFull0, kSFull1, kSFree0, kSFree1,
+    kPFull, kPFree, kXFull, kXEmpty, kODone, kOFree, kFinal
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmkv) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    unsigned char *sQ = smem + kOffQ;
+    unsigned char *sKV = smem + kOffKV;
+    unsigned char *sP = smem + kOffP;
+    float *sX = reinterpret_cast<float *>(smem + kOffX);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
+    int *scan = reinterpret_cast<int *>(smem + kOffMisc + 16);
+    int *off = reinterpret_cast<int *>(smem + kOffTable);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_rank();
+    const uint32_t peer = rank ^ 1u;
+    const int nslab = rank == 0 ? 4 : 5;        // q.k slabs owned by this CTA
+    const int slab0 = rank == 0 ? 0 : 4;        // first 64-dim slab of the latent row
+
+    if (tid == 0) {
+        *abort_flag = 0;
+        mbar_init(&bars[kQFull], 1);
+        mbar_init(&bars[kQEmpty], 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bars[kKvFull0 + s], 1);
+            mbar_init(&bars[kKvEmpty0 + s], 1);
+            mbar_init(&bars[kSFull0 + s], 1);
+            mbar_init(&bars[kSFree0 + s], 4);
+        }
+        mbar_init(&bars[kPFull], 4);
+        mbar_init(&bars[kPFree], 1);
+        mbar_init(&bars[kXFull], 128);   // the peer's 128 softmax threads
+        mbar_init(&bars[kXEmpty], 128);
+        mbar_init(&bars[kODone], 1);
+        mbar_init(&bars[kOFree], 4);
+        mbar_init(&bars[kFinal], 1);
+        mbar_init_fence();
+    }
+    if (warp == kMmaWarp) {
+        tc05::tmem_alloc(tslot, kTmemCols);
+        tc05::tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        prefetch_tmap(&tmq);
+        prefetch_tmap(&tmkv);
+    }
+    build_item_table(p, off, scan);   // contains __syncthreads
+    tc05::fence_before_sync();
+    __syncthreads();
+    tc05::fence_after_sync();
+    cluster_sync_all();                // the peer's barriers exist before any remote arrive
+    const uint32_t tbase = *tslot;
+    const int total = off[p.batch];
+    const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ producer
+        const int box = p.box_rows;
+        const int nbox = kTile / box;
+        const uint32_t box_bytes = static_cast<uint32_t>(box) * 128u;
+        uint32_t n = 0, ic = 0;
+        bool ok = true;
+        for (int w = pair; w < total && ok; w += npairs) {
+            const Item it = locate(p, off, w, false);
+            if (it.n_tiles == 0) continue;
+            if (lane == 0) {
+                ok = wait_bar(&bars[kQEmpty], (ic & 1) ^ 1, abort_flag, p.err);
+                if (ok) {
+                    mbar_arrive_expect_tx(&bars[kQFull], static_cast<uint32_t>(nslab) * kHeads * 128u);
+                    const int qrow = it.b * p.hq + it.hg * kHeads;
+                    for (int s = 0; s < nslab; ++s)
+                        tma_load_2d(sQ + s * kHeads * 128, &tmq, (slab0 + s) * 64, qrow, &bars[kQFull]);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            ++ic;
+            for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
+                int row = -1;
+                if (lane < nbox) {
+                    const int tb = it.t_begin + ti * kTile + lane * box;
+                    if (tb < it.t_end) {
+                        if (p.layout == PKV_LAYOUT_VARLEN) {
+                            row = static_cast<int>(it.base + tb);
+                        } else {
+                            const int32_t *tab = p.layout == PKV_LAYOUT_CSR ? p.kv_indices : p.block_table;
+                            const int page = __ldg(tab + it.base + (tb >> p.ps_shift));
+                            if (page < 0 || page >= p.num_pages) {
+                                raise_flag(p.err, PKV_DEVERR_RANGE);
+                                row = -2;
+                            } else {
+                                row = static_cast<int>((static_cast<int64_t>(page) << p.ps_shift) + (tb & p.ps_mask));
+                            }
+                        }
+                    }
+                }
+                const int s = n % kStages;
+                if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
+                const uint32_t valid = __ballot_sync(0xffffffffu, row >= 0);
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&bars[kKvFull0 + s], __popc(valid) * box_bytes * static_cast<uint32_t>(nslab));
+                __syncwarp();
+                if (row >= 0) {
+                    unsigned char *st = sKV + s * kStageBytes;
+                    for (int sl = 0; sl < nslab; ++sl)
+                        tma_load_2d(st + sl * kSlabBytes + lane * box_bytes, &tmkv, (slab0 + sl) * 64, row,
+                                    &bars[kKvFull0 + s]);
+                }
+            }
+        }
+        // drain: the copies this warp issued have landed before shared memory is released
+        if (lane == 0) {
+            if (ic > 0) drain_wait(&bars[kQFull], (ic - 1) & 1);
+            for (uint32_t k = n > kStages ? n - kStages : 0; k < n; ++k)
+                drain_wait(&bars[kKvFull0 + k % kStages], (k / kStages) & 1);
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issue
+        const uint32_t id_qk = tc05::idesc_bf16_f32(kHeads, kTile, false, false);
+        const uint32_t id_pv = tc05::idesc_bf16_f32(kHeads, 256, false, true);
+        uint32_t n = 0, ic = 0;
+        bool ok = true;
+        // O += P V for tile m (the item's tile index tim), after softmax wrote P.
+        auto pv = [&](uint32_t m, int tim, const Item &it) {
+            ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kPFull], m & 1, abort_flag, p.err));
+            if (!ok) return;
+            unsigned char *st = sKV + (m % kStages) * kStageBytes;
+            const int n_valid = it.t_end - (it.t_begin + tim * kTile);
+            if (n_valid < kTile) {
+                // key rows past the end hold stale data: zero their value dims
+                for (int i = lane; i < (kTile - n_valid) * kVSlabs * 8; i += 32) {
+                    const int key = n_valid + i / (kVSlabs * 8);
+                    const int sl = (i / 8) % kVSlabs, c = i % 8;
+                    *reinterpret_cast<uint4 *>(st + sl * kSlabBytes + key * 128 + (c << 4)) = make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            if (tim == 0) ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kOFree], (ic & 1) ^ 1, abort_flag, p.err));
+            if (!ok) return;
+            tc05::fence_after_sync();
+            if (lane == 0) {
+#pragma unroll
+                for (int k = 0; k < kTile / 16; ++k) {
+                    const uint64_t a = tc05::smem_desc(sP + k * 32, 16, 1024);
+                    const uint64_t b = tc05::smem_desc(st + k * 2048, kSlabBytes, 1024);
+                    tc05::mma_ss(tbase + kColO, a, b, id_pv, (tim == 0 && k == 0) ? 0u : 1u);
+                }
+                tc05::commit(&bars[kPFree]);
+                tc05::commit(&bars[kKvEmpty0 + m % kStages]);
+            }
+            __syncwarp();
+        };
+        for (int w = pair; w < total && ok; w += npairs) {
+            const Item it = locate(p, off, w, false);
+            if (it.n_tiles == 0) continue;
+            ok = __all_sync(0xffffffffu, wait_bar(&bars[kQFull], ic & 1, abort_flag, p.err));
+            for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
+                const int s = n % kStages;
+                ok = __all_sync(0xffffffffu, wait_bar(&bars[kKvFull0 + s], (n / kStages) & 1, abort_flag, p.err) &&
+                                                 wait_bar(&bars[kSFree0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err));
+                if (!ok) break;
+                tc05::fence_after_sync();
+                if (lane == 0) {
+                    unsigned char *st = sKV + s * kStageBytes;
+                    for (int sl = 0; sl < nslab; ++sl)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint64_t a = tc05::smem_desc(sQ + sl * kHeads * 128 + k * 32, 16, 1024);
+                            const uint64_t b = tc05::smem_desc(st + sl * kSlabBytes + k * 32, 16, 1024);
+                            tc05::mma_ss(tbase + kColS + s * 64, a, b, id_qk, (sl | k) ? 1u : 0u);
+                        }
+                    tc05::commit(&bars[kSFull0 + s]);
+                    if (ti == it.n_tiles - 1) tc05::commit(&bars[kQEmpty]);
+                }
+                __syncwarp();
+                if (ti > 0) pv(n - 1, ti - 1, it);
+            }
+            if (ok) pv(n - 1, it.n_tiles - 1, it);
+            if (ok && lane == 0) tc05::commit(&bars[kODone]);
+            __syncwarp();
+            ++ic;
+        }
+        // drain: every MMA this warp issued has completed before TMEM is freed
+        if (lane == 0) {
+            tc05::commit(&bars[kFinal]);
+            drain_wait(&bars[kFinal], 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax warps (one head per thread)
+        const int row = warp * 32 + lane;
+        const uint32_t x_peer = mapa(smem_u32(sX), peer);
+        const uint32_t xf_peer = mapa(smem_u32(&bars[kXFull]), peer);
+        const uint32_t xe_peer = mapa(smem_u32(&bars[kXEmpty]), peer);
+        const uint32_t trow = tc05::taddr(tbase, warp * 32, 0);
+        uint32_t n = 0, ic = 0;
+        bool ok = true;
+        for (int w = pair; w < total; w += npairs) {
+            const Item it = locate(p, off, w, tid == 0 && rank == 0);
+            const int head = it.hg * kHeads + row;
+            const int64_t orow = static_cast<int64_t>(it.b) * p.hq + head;
+            if (it.n_tiles == 0) {
+                uint4 *o = reinterpret_cast<uint4 *>(p.out + orow * kDv + rank * 256);
+                for (int i = 0; i < 32; ++i) o[i] = make_uint4(0, 0, 0, 0);
+                if (rank == 0 && p.lse) p.lse[orow] = -INFINITY;
+                continue;
+            }
+            float m = -INFINITY, l = 0.f;
+            bool p_free_seen = false;
+            for (int ti = 0; ti < it.n_tiles; ++ti, ++n) {
+                const int s = n % kStages;
+                float sv[64];
+                ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kSFull0 + s], (n / kStages) & 1, abort_flag, p.err));
+                if (ok) {
+                    tc05::fence_after_sync();
+                    tc05::ld_x64(trow + kColS + s * 64, sv);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) sv[j] = 0.f;
+                }
+                tc05::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kSFree0 + s]);
+                // ---- swap partial scores with the peer CTA ----
+                ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kXEmpty], (n & 1) ^ 1, abort_flag, p.err, true));
+                if (ok) {
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        st_cluster_v4(x_peer + (row * 64 + 4 * c) * 4, sv[4 * c], sv[4 * c + 1], sv[4 * c + 2],
+                                      sv[4 * c + 3]);
+                    mbar_arrive_cluster(xf_peer);
+                }
+                ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kXFull], n & 1, abort_flag, p.err, true));
+                if (ok) {
+                    const float4 *xr = reinterpret_cast<const float4 *>(sX + row * 64);
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const float4 x = xr[c];
+                        sv[4 * c] += x.x;
+                        sv[4 * c + 1] += x.y;
+                        sv[4 * c + 2] += x.z;
+                        sv[4 * c + 3] += x.w;
+                    }
+                    mbar_arrive_cluster(xe_peer);
+                }
+                // ---- online softmax over this tile's keys ----
+                const int n_valid = it.t_end - (it.t_begin + ti * kTile);
+                float mx = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    sv[j] = j < n_valid ? sv[j] * p.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, sv[j]);
+                }
+                const bool raise = mx > m + kLazy || (m == -INFINITY && mx != -INFINITY);
+                const float corr = raise ? ex2(m - mx) : 1.f;
+                // O rescale in TMEM (warp-collective; rows whose max did not move use corr = 1)
+                if (__any_sync(0xffffffffu, raise && l > 0.f)) {
+                    // O must be final for the previous tile before it is rescaled
+                    ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kPFree], (n & 1) ^ 1, abort_flag, p.err));
+                    p_free_seen = true;
+                    if (ok) {
+                        tc05::fence_after_sync();
+#pragma unroll 1
+                        for (int cc = 0; cc < 16; ++cc) {
+                            float ov[16];
+                            tc05::ld_x16(trow + kColO + cc * 16, ov);
+                            tc05::wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) ov[e] *= corr;
+                            tc05::st_x16(trow + kColO + cc * 16, ov);
+                        }
+                        tc05::wait_st();
+                    }
+                }
+                if (raise) {
+                    l *= corr;
+                    m = mx;
+                }
+                uint32_t pk[32];
+                float lsum = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float p0 = m == -INFINITY ? 0.f : ex2(sv[2 * j] - m);
+                    const float p1 = m == -INFINITY ? 0.f : ex2(sv[2 * j + 1] - m);
+                    lsum += p0 + p1;
+                    pk[j] = pack_bf16x2(p0, p1);
+                }
+                l += lsum;
+                if (!p_free_seen) ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kPFree], (n & 1) ^ 1, abort_flag, p.err));
+                p_free_seen = false;
+                // P row (64 keys, 128 bytes) in the 128-byte-swizzled K-major layout
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<uint4 *>(sP + row * 128 + ((c ^ (row & 7)) << 4)) =
+                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                fence_proxy_async_smem();
+                tc05::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kPFull]);
+            }
+            // ---- epilogue: normalise O and write the output (or the split partial) ----
+            ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kODone], ic & 1, abort_flag, p.err));
+            tc05::fence_after_sync();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const bool single = it.n_chunks == 1;
+            const int64_t prow = (static_cast<int64_t>(it.b) * p.n_chunks_max + it.c) * p.hq + head;
+#pragma unroll 1
+            for (int cc = 0; cc < 16; ++cc) {
+                float ov[16];
+                if (ok) {
+                    tc05::ld_x16(trow + kColO + cc * 16, ov);
+                    tc05::wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) ov[e] = 0.f;
+                }
+                const int col = rank * 256 + cc * 16;
+                if (single) {
+                    uint32_t h[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) h[e] = pack_bf16x2(ov[2 * e] * inv, ov[2 * e + 1] * inv);
+                    uint4 *o = reinterpret_cast<uint4 *>(p.out + orow * kDv + col);
+                    o[0] = make_uint4(h[0], h[1], h[2], h[3]);
+                    o[1] = make_uint4(h[4], h[5], h[6], h[7]);
+                } else {
+                    float4 *o = reinterpret_cast<float4 *>(p.part_o + prow * kDv + col);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        o[e] = make_float4(ov[4 * e] * inv, ov[4 * e + 1] * inv, ov[4 * e + 2] * inv, ov[4 * e + 3] * inv);
+                }
+            }
+            if (rank == 0) {
+                const float lse2 = m + log2f(l);
+                if (single) {
+                    if (p.lse) p.lse[orow] = lse2 * kLn2;
+                } else {
+                    p.part_lse[prow] = lse2;
+                }
+            }
+            tc05::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kOFree]);
+            ++ic;
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc05::fence_before_sync();
+    __syncthreads();
+    cluster_sync_all();   // the peer no longer touches this CTA's shared memory
+    if (warp == kMmaWarp) {
+        tc05::fence_after_sync();
+        tc05::tmem_dealloc(tbase, kTmemCols);
+    }
+}
+
+// Log-sum-exp merge of the chunk partials of MLA requests: one CTA per
+// (request, 16 heads); base-2 lse in the workspace.
+__global__ void __launch_bounds__(256) mla_merge_kernel(const Params p) {
+    extern __shared__ float wsm[];  // [16][n_chunks_max]
+    __shared__ float den_s[16], mx_s[16];
+    const int b = blockIdx.x, h0 = blockIdx.y * 16;
+    int64_t base;
+    const int L = key_count(p, b, base, false);
+    const int n = (L + p.chunk - 1) / p.chunk;
+    if (n <= 1) return;
+    const int64_t rb = static_cast<int64_t>(b) * p.n_chunks_max;
+    for (int i = threadIdx.x; i < 16 * n; i += blockDim.x) {
+        const int h = i / n, c = i % n;
+        wsm[h * p.n_chunks_max + c] = p.part_lse[(rb + c) * p.hq + h0 + h];
+    }
+    __syncthreads();
+    if (threadIdx.x < 16) {
+        const int h = threadIdx.x;
+        float M = -INFINITY;
+        for (int c = 0; c < n; ++c) M = fmaxf(M, wsm[h * p.n_chunks_max + c]);
+        float den = 0.f;
+        for (int c = 0; c < n; ++c) {
+            const float wgt = ex2(wsm[h * p.n_chunks_max + c] - M);
+            wsm[h * p.n_chunks_max + c] = wgt;
+            den += wgt;
+        }
+        den_s[h] = den;
+        mx_s[h] = M;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 16 * (kDv / 4); i += blockDim.x) {
+        const int h = i / (kDv / 4), d4 = i % (kDv / 4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = 0; c < n; ++c) {
+            const float wgt = wsm[h * p.n_chunks_max + c];
+            const float4 v = reinterpret_cast<const float4 *>(p.part_o + ((rb + c) * p.hq + h0 + h) * kDv)[d4];
+            acc.x = fmaf(wgt, v.x, acc.x);
+            acc.y = fmaf(wgt, v.y, acc.y);
+            acc.z = fmaf(wgt, v.z, acc.z);
+            acc.w = fmaf(wgt, v.w, acc.w);
+        }
+        const float inv = 1.f / den_s[h];
+        uint2 o;
+        o.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+        o.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+        reinterpret_cast<uint2 *>(p.out + (static_cast<int64_t>(b) * p.hq + h0 + h) * kDv)[d4] = o;
+        if (d4 == 0 && p.lse) p.lse[static_cast<int64_t>(b) * p.hq + h0 + h] = (mx_s[h] + log2f(den_s[h])) * kLn2;
+    }
+}
+
+// ------------------------------------------------------------------ host side
+struct Plan {
+    int chunk, n_chunks_max, hgroups;
+    size_t part_o_bytes, part_lse_bytes;
+};
+
+static void make_plan(const pkv_decode_args *a, Plan &pl) {
+    pl.hgroups = a->num_q_heads / kHeads;
+    if (a->kv_chunk > 0) {
+        pl.chunk = a->kv_chunk;
+    } else {
+        // ~4 items per CTA pair when requests average half of max_seq_len
+        const int64_t pairs = std::max(1, sm_count() / 2);
+        const int64_t L = std::max<int64_t>(1, a->max_seq_len);
+        pl.chunk = kTile;
+        for (int c = 4096; c >= kTile; c >>= 1) {
+            const int64_t items = static_cast<int64_t>(a->batch) * pl.hgroups * ((L + c - 1) / c);
+            if (items / 2 >= 4 * pairs) {
+                pl.chunk = c;
+                break;
+            }
+        }
+    }
+    pl.n_chunks_max = std::max(1, (a->max_seq_len + pl.chunk - 1) / pl.chunk);
+    if (pl.n_chunks_max == 1) {
+        pl.part_o_bytes = pl.part_lse_bytes = 0;
+    } else {
+        const int64_t rows = static_cast<int64_t>(a->batch) * pl.n_chunks_max * a->num_q_heads;
+        pl.part_o_bytes = (static_cast<size_t>(rows) * kDv * 4 + 255) / 256 * 256;
+        pl.part_lse_bytes = (static_cast<size_t>(rows) * 4 + 255) / 256 * 256;
+    }
+}
+
 pkv_status validate(const pkv_decode_args *a, bool check_ptrs) {
-    (void)a;
-    (void)check_ptrs;
-    return fail(PKV_ERR_UNSUPPORTED, "pkv_decode(MLA): not built yet");
+    if (a->batch < 0 || a->num_q_heads < 1 || a->max_seq_len < 0 || a->num_slots < 0)
+        return fail(PKV_ERR_INVALID_ARG, "pkv_decode(MLA): negative or zero size");
+    if (a->num_kv_heads != 1) return fail(PKV_ERR_INVALID_ARG, "pkv_decode(MLA): num_kv_heads must be 1");
+    if (a->head_dim_qk != kDqk || a->head_dim_v != kDv)
+        return fail(PKV_ERR_UNSUPPORTED, "pkv_decode(MLA): head_dim_qk 576 and head_dim_v 512 are supported");
+    if (a->num_q_heads % kHeads)
+        return fail(PKV_ERR_UNSUPPORTED, "pkv_decode(MLA): num_q_heads must be a multiple of 128");
+    if (a->layout != PKV_LAYOUT_VARLEN && (!is_pow2(a->page_size) || a->page_size < 8 || a->page_size > 1024))
+        return fail(PKV_ERR_UNSUPPORTED, "pkv_decode(MLA): page_size must be a power of two in [8, 1024]");
+    if (a->kv_chunk < 0 || a->kv_chunk % kTile)
+        return fail(PKV_ERR_INVALID_ARG, "pkv_decode(MLA): kv_chunk must be a multiple of 64");
+    if (a->layout != PKV_LAYOUT_CSR && a->layout != PKV_LAYOUT_BLOCK_TABLE && a->layout != PKV_LAYOUT_VARLEN)
+        return fail(PKV_ERR_INVALID_ARG, "pkv_decode(MLA): unknown layout");
+    if (a->k_row_stride < kDqk || a->k_row_stride % 8)
+        return fail(PKV_ERR_INVALID_ARG, "pkv_decode(MLA): latent row stride must be >= 576 and 16-byte aligned");
+    if (a->num_slots > INT32_MAX) return fail(PKV_ERR_UNSUPPORTED, "pkv_decode(MLA): pool larger than 2^31 rows");
+    if (a->batch == 0 || !check_ptrs) return PKV_OK;
+    if (!a->q || !a->k_pool || !a->out) return fail(PKV_ERR_INVALID_ARG, "pkv_decode(MLA): null q/k_pool/out");
+    if (a->v_pool && a->v_pool != a->k_pool)
+        return fail(PKV_ERR_INVALID_ARG, "pkv_decode(MLA): values come from the latent pool; pass v_pool = NULL");
+    if (!aligned(a->q, 16) || !aligned(a->k_pool, 16) || !aligned(a->out, 16))
+        return fail(PKV_ERR_INVALID_ARG, "pkv_decode(MLA): q, latent pool and out must be 16-byte aligned");
+    switch (a->layout) {
+        case PKV_LAYOUT_CSR:
+            if (!a->kv_indptr || !a->kv_indices || !a->kv_last_page_len)
+                return fail(PKV_ERR_INVALID_ARG, "pkv_decode(MLA): CSR layout needs kv_indptr/kv_indices/kv_last_page_len");
+            break;
+        case PKV_LAYOUT_BLOCK_TABLE:
+            if (!a->block_table || !a->seq_lens || a->block_table_width < 0)
+                return fail(PKV_ERR_INVALID_ARG, "pkv_decode(MLA): block-table layout needs block_table and seq_lens");
+            break;
+        default:
+            if (!a->cu_seqlens) return fail(PKV_ERR_INVALID_ARG, "pkv_decode(MLA): varlen layout needs cu_seqlens");
+    }
+    return PKV_OK;
 }
 
 size_t workspace_size(const pkv_decode_args *a) {
-    (void)a;
-    return 0;
+    Plan pl;
+    make_plan(a, pl);
+    return pl.part_o_bytes + pl.part_lse_bytes;
 }
 
 pkv_status launch(const pkv_decode_args *a, void *ws, size_t ws_bytes, int32_t *err, cudaStream_t s) {
-    (void)a; (void)ws; (void)ws_bytes; (void)err; (void)s;
-    return fail(PKV_ERR_UNSUPPORTED, "pkv_decode(MLA): not built yet");
+    Plan pl;
+    make_plan(a, pl);
+    if (ws_bytes < pl.part_o_bytes + pl.part_lse_bytes)
+        return fail(PKV_ERR_CAPACITY, "pkv_decode(MLA): workspace of %zu bytes, %zu needed", ws_bytes,
+                    pl.part_o_bytes + pl.part_lse_bytes);
+    if (pl.part_o_bytes && (!ws || !aligned(ws, 256)))
+        return fail(PKV_ERR_INVALID_ARG, "pkv_decode(MLA): workspace must be non-null and 256-byte aligned");
+    if (static_cast<int64_t>(pl.chunk) * pl.n_chunks_max > INT32_MAX / 2)
+        return fail(PKV_ERR_UNSUPPORTED, "pkv_decode(MLA): max_seq_len too large");
+    Params p{};
+    p.layout = a->layout;
+    p.batch = a->batch;
+    p.hq = a->num_q_heads;
+    p.hgroups = pl.hgroups;
+    const int ps = a->layout == PKV_LAYOUT_VARLEN ? kTile : a->page_size;
+    p.ps_shift = ilog2(ps);
+    p.ps_mask = ps - 1;
+    p.scale_log2 = a->sm_scale * kLog2e;
+    p.chunk = pl.chunk;
+    p.n_chunks_max = pl.n_chunks_max;
+    p.bt_width = a->block_table_width;
+    p.box_rows = std::min(ps, kTile);
+    p.num_slots = a->num_slots;
+    p.num_pages = a->num_slots >> p.ps_shift;
+    p.kv_indices_len = a->kv_indices_len;
+    p.kv_indptr = a->kv_indptr;
+    p.kv_indices = a->kv_indices;
+    p.kv_last = a->kv_last_page_len;
+    p.block_table = a->block_table;
+    p.seq_lens = a->seq_lens;
+    p.cu_seqlens = a->cu_seqlens;
+    p.out = static_cast<uint16_t *>(a->out);
+    p.lse = a->lse;
+    p.part_o = static_cast<float *>(ws);
+    p.part_lse = reinterpret_cast<float *>(static_cast<char *>(ws) + pl.part_o_bytes);
+    p.err = err;
+    if (a->layout == PKV_LAYOUT_VARLEN) p.ps_shift = 0, p.ps_mask = 0;
+
+    // TMA maps: q as [B * Hq rows, 576] (box 128 rows x 64 dims), the latent pool
+    // as [num_slots rows, 576] (box box_rows x 64 dims), both 128-byte swizzled.
+    CUtensorMap tmq, tmkv;
+    const uint64_t dq[2] = {static_cast<uint64_t>(kDqk), static_cast<uint64_t>(a->batch) * a->num_q_heads};
+    const uint64_t sq[1] = {static_cast<uint64_t>(kDqk) * 2};
+    const uint32_t bq[2] = {64, static_cast<uint32_t>(kHeads)};
+    const uint64_t dk[2] = {static_cast<uint64_t>(kDqk), static_cast<uint64_t>(a->num_slots)};
+    const uint64_t sk[1] = {static_cast<uint64_t>(a->k_row_stride) * 2};
+    const uint32_t bk[2] = {64, static_cast<uint32_t>(p.box_rows)};
+    if (!encode_tmap_bf16(&tmq, a->q, 2, dq, sq, bq) || !encode_tmap_bf16(&tmkv, a->k_pool, 2, dk, sk, bk))
+        return fail(PKV_ERR_CUDA, "pkv_decode(MLA): cuTensorMapEncodeTiled rejected q or the latent pool");
+
+    static size_t lim = 0;
+    static int max_pairs = 0;
+    const size_t smem = kFixedSmem + (static_cast<size_t>(a->batch) + 1) * 4;
+    if (!lim) {
+        int optin = 0, dev = 0;
+        cudaFuncAttributes fa{};
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaFuncGetAttributes(&fa, mla_decode_kernel) != cudaSuccess)
+            return fail(PKV_ERR_CUDA, "pkv_decode(MLA): cannot query shared-memory limits");
+        const size_t l = static_cast<size_t>(optin) - fa.sharedSizeBytes;
+        if (cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(l)) !=
+            cudaSuccess)
+            return fail(PKV_ERR_CUDA, "pkv_decode(MLA): cannot raise the shared-memory limit");
+        lim = l;
+    }
+    if (smem > lim) return fail(PKV_ERR_UNSUPPORTED, "pkv_decode(MLA): batch too large for the on-chip item table");
+    if (!max_pairs) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(2 * std::max(1, sm_count() / 2));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = lim;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel, &cfg) != cudaSuccess || n < 1)
+            n = std::max(1, sm_count() / 2);
+        max_pairs = n;
+    }
+    const int64_t items_upper = static_cast<int64_t>(a->batch) * pl.hgroups * pl.n_chunks_max;
+    const int pairs = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(items_upper, max_pairs)));
+    mla_decode_kernel<<<2 * pairs, kThreads, smem, s>>>(p, tmq, tmkv);
+    pkv_status st = check_launch("pkv_decode(MLA split kernel)");
+    if (st != PKV_OK || pl.n_chunks_max == 1) return st;
+    const size_t msmem = static_cast<size_t>(16) * pl.n_chunks_max * 4;
+    if (msmem > 200 * 1024) return fail(PKV_ERR_UNSUPPORTED, "pkv_decode(MLA): too many splits for the merge");
+    if (msmem > 48 * 1024 &&
+        cudaFuncSetAttribute(mla_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(msmem)) !=
+            cudaSuccess)
+        return fail(PKV_ERR_CUDA, "pkv_decode(MLA): cannot raise the merge shared-memory limit");
+    mla_merge_kernel<<<dim3(a->batch, a->num_q_heads / 16), 256, msmem, s>>>(p);
+    return check_launch("pkv_decode(MLA merge kernel)");
 }
 
 }  // namespace mla

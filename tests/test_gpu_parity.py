@@ -318,3 +318,71 @@ def test_decode_rejects_small_workspace(B):
     with pytest.raises(B.PkvError) as e:
         B.pkv_decode(pb.args, pb.workspace[:128], step.err)
     assert e.value.status == B.PKV_ERR_CAPACITY
+
+
+# ------------------------------------------------------------------ MLA (latent) decode
+def test_mla_decode_step_parity(B):
+    step = _step("deepseek_v3_mla")
+    sample = _sample(step.wl.batch, 8, seed=2)
+    pre_k = step.k_pool.clone()
+    step.run()
+    torch.cuda.synchronize()
+    assert step.check_errors() == 0
+    _check_decode(step, "self", sample, pre_k, None)
+
+
+def _direct_mla(B, lens, ps, hq=128, chunk=0, layout="block_table", seed=0):
+    dev = torch.device("cuda")
+    rng = np.random.default_rng(seed)
+    gen = torch.Generator().manual_seed(seed)
+    num_pages = 4 + sum(-(-L // ps) for L in lens)
+    r2t, rpi = paged_table(rng, lens, ps, num_pages)
+    lat = torch.randn((num_pages * ps, 576), generator=gen).to(torch.bfloat16)
+    q = torch.randn((len(lens), hq, 576), generator=gen).to(torch.bfloat16)
+    scale = 1 / math.sqrt(192)
+    st, ref, ref_lse = oracle.decode(bits(q), bits(lat), bits(lat), r2t, rpi, lens, scale, head_dim_v=512)
+    assert st == oracle.OK
+    Bn = len(lens)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lens_t = torch.tensor(lens, dtype=torch.int32, device=dev)
+    npages = [-(-L // ps) for L in lens]
+    out = torch.empty((Bn, hq, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((Bn, hq), dtype=torch.float32, device=dev)
+    latd, qd = lat.to(dev), q.to(dev)
+    r2t_d, rpi_d = torch.from_numpy(r2t).to(dev), torch.from_numpy(rpi).to(dev)
+    if layout == "block_table":
+        bt = torch.empty((Bn, max(max(npages), 1)), dtype=torch.int32, device=dev)
+        B.pkv_build_indices(r2t_d, rpi_d, lens_t, ps, num_pages, err, block_table=bt)
+        args = B.make_decode_args(B.PKV_KIND_MLA, B.PKV_LAYOUT_BLOCK_TABLE, qd, latd, None, out, page_size=ps,
+                                  sm_scale=scale, max_seq_len=max(lens), head_dim_v=512, block_table=bt,
+                                  seq_lens=lens_t, lse=lse, kv_chunk=chunk)
+    else:
+        indptr = torch.empty(Bn + 1, dtype=torch.int32, device=dev)
+        idx = torch.empty(max(sum(npages), 1), dtype=torch.int32, device=dev)
+        last = torch.empty(Bn, dtype=torch.int32, device=dev)
+        B.pkv_build_indices(r2t_d, rpi_d, lens_t, ps, num_pages, err, kv_indptr=indptr, kv_indices=idx,
+                            kv_last_page_len=last)
+        args = B.make_decode_args(B.PKV_KIND_MLA, B.PKV_LAYOUT_CSR, qd, latd, None, out, page_size=ps,
+                                  sm_scale=scale, max_seq_len=max(lens), head_dim_v=512, kv_indptr=indptr,
+                                  kv_indices=idx, kv_last_page_len=last, lse=lse, kv_chunk=chunk)
+    ws = torch.empty(max(B.pkv_decode_workspace_size(args), 256), dtype=torch.uint8, device=dev)
+    B.pkv_decode(args, ws, err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    return bf16_to_f64(out), lse.double().cpu().numpy(), ref, ref_lse
+
+
+@pytest.mark.parametrize("layout", ["block_table", "csr"])
+@pytest.mark.parametrize("chunk", [0, 64, 192])
+def test_mla_edge_lengths(B, layout, chunk):
+    lens = [0, 1, 63, 64, 65, 130, 1000]
+    gpu, g_lse, ref, ref_lse = _direct_mla(B, lens, 64, chunk=chunk, layout=layout, seed=7)
+    assert (gpu[0] == 0).all() and np.isneginf(g_lse[0]).all()
+    assert_close(gpu, ref, "MLA edge lengths %s chunk=%d" % (layout, chunk))
+    assert_close(g_lse[1:], ref_lse[1:], "MLA lse")
+
+
+@pytest.mark.parametrize("ps", [16, 128])
+def test_mla_other_page_sizes_and_head_groups(B, ps):
+    gpu, g_lse, ref, ref_lse = _direct_mla(B, [5, 300, 777], ps, hq=256, seed=ps)
+    assert_close(gpu, ref, "MLA ps=%d, 256 heads" % ps)
