@@ -17,13 +17,17 @@
 // distributed shared memory, so both CTAs hold identical full scores and run
 // the same softmax; nothing is loaded or multiplied twice.
 //
-// Per CTA: warp 4 is the TMA producer (the item's Q once, then one 64-key tile
-// per stage, one box per page per 64-dim slab, 128-byte swizzle), warp 5 issues
-// tcgen05 MMAs from one thread (S = Q K^T into a double-buffered TMEM tile,
-// O += P V into 256 TMEM columns, V read as an MN-major operand of the same
-// slabs), warps 0-3 own one head per TMEM lane: read S, exchange, online
-// softmax (base 2, running max raised only past 2^8 headroom so O rescales in
-// TMEM are rare), write P to shared memory, and finally normalise O.
+// Per CTA: warp 4 is the TMA producer (one 64-key tile per stage, one box per
+// page per 64-dim slab, 128-byte swizzle, 4 stages); warp 5 issues tcgen05 MMAs
+// from one thread; warps 0-3 own one head per TMEM lane.  Tensor memory holds
+// S (64 columns), O (256), this CTA's slice of q (<= 160, written by the
+// softmax warps at each item start) and P (32, bf16 pairs): S = Q K^T takes q
+// from TMEM and K from shared memory, O += P V takes P from TMEM and V as an
+// MN-major operand of the same slabs.  The softmax warps read S, swap partials
+// with the peer (st.async into a conflict-free transposed buffer, completion
+// counted in bytes on the receiver's mbarrier), run the online softmax (base 2,
+// running max raised only past 2^8 headroom so O rescales in TMEM are rare),
+// write P to TMEM and finally normalise O.
 // Every wait is bounded (~2 s) and an abort flag lets the CTA drain instead of
 // hanging.
 #include <algorithm>
@@ -39,26 +43,25 @@ namespace mla {
 constexpr int kDqk = 576, kDv = 512, kHeads = 128, kTile = 64;
 constexpr int kVSlabs = 4;                 // 256 value dims per CTA
 constexpr int kMaxSlabs = 5;               // q.k slabs of the wider CTA
-constexpr int kStages = 2;
+constexpr int kStages = 4;
 constexpr int kThreads = 192;              // warps 0-3 softmax, 4 producer, 5 MMA
 constexpr int kProducerWarp = 4, kMmaWarp = 5;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;              // two 64-column score tiles
-constexpr uint32_t kColO = 128;            // 256-column output accumulator
+constexpr uint32_t kColS = 0;              // 64-column score tile
+constexpr uint32_t kColO = 64;             // 256-column output accumulator
+constexpr uint32_t kColQ = 320;            // q of this CTA's dims as the MMA A operand (<= 160 columns)
+constexpr uint32_t kColP = 480;            // P (bf16 probabilities) as the A operand of P V (32 columns)
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kLog2e = 1.44269504088896341f;
 constexpr float kLazy = 8.f;
 
 // shared-memory carve-up (bytes from a 1024-aligned base)
-constexpr int kQBytes = kMaxSlabs * kHeads * 128;           // 80 KB
 constexpr int kSlabBytes = kTile * 128;                     // 8 KB: 64 keys x 64 dims
 constexpr int kStageBytes = kMaxSlabs * kSlabBytes;         // 40 KB
-constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kQBytes;
-constexpr int kOffP = kOffKV + kStages * kStageBytes;       // P: 128 heads x 64 keys bf16, SW128
-constexpr int kOffX = kOffP + kHeads * 128;                 // peer partial scores, fp32 [128][64]
+constexpr int kOffKV = 0;
+constexpr int kOffX = kOffKV + kStages * kStageBytes;       // peer partial scores, fp32, [16 chunks][128 heads] x 16 B
 constexpr int kOffBar = kOffX + kHeads * kTile * 4;
-constexpr int kNumBars = 20;
+constexpr int kNumBars = 24;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;            // tmem slot, abort flag, scan scratch
 constexpr int kOffTable = kOffMisc + 64;
 constexpr int kFixedSmem = kOffTable + 1024;                // + item table + alignment slack
@@ -73,6 +76,7 @@ struct Params {
     int32_t box_rows;
     int64_t num_slots, num_pages, kv_indices_len;
     const int32_t *kv_indptr, *kv_indices, *kv_last, *block_table, *seq_lens, *cu_seqlens;
+    const uint16_t *q;
     uint16_t *out;
     float *lse;
     float *part_o, *part_lse;
@@ -203,17 +207,16 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
 }
 
 enum Bar {
-    kQFull = 0, kQEmpty, kKvFull0, kKvFull1, kKvEmpty0, kKvEmpty1, kSFull0, kSFull1, kSFree0, kSFree1,
-    kPFull, kPFree, kXFull, kXEmpty, kODone, kOFree, kFinal
+    kQFull = 0, kQEmpty, kKvFull0, kKvEmpty0 = kKvFull0 + kStages, kSFull = kKvEmpty0 + kStages, kSFree, kPFull,
+    kPFree, kXFull, kXEmpty, kODone, kOFree, kFinal, kBarCount
 };
+static_assert(kBarCount <= kNumBars, "barrier slots");
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmkv) {
+mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    unsigned char *sQ = smem + kOffQ;
     unsigned char *sKV = smem + kOffKV;
-    unsigned char *sP = smem + kOffP;
     float *sX = reinterpret_cast<float *>(smem + kOffX);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
@@ -229,18 +232,18 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
 
     if (tid == 0) {
         *abort_flag = 0;
-        mbar_init(&bars[kQFull], 1);
-        mbar_init(&bars[kQEmpty], 1);
+        mbar_init(&bars[kQFull], 4);             // the 4 softmax warps after writing q into TMEM
+        mbar_init(&bars[kQEmpty], 1);            // MMA commit after an item's last q.k
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bars[kKvFull0 + s], 1);
             mbar_init(&bars[kKvEmpty0 + s], 1);
-            mbar_init(&bars[kSFull0 + s], 1);
-            mbar_init(&bars[kSFree0 + s], 4);
         }
+        mbar_init(&bars[kSFull], 1);
+        mbar_init(&bars[kSFree], 4);
         mbar_init(&bars[kPFull], 4);
         mbar_init(&bars[kPFree], 1);
-        mbar_init(&bars[kXFull], 128);   // the peer's 128 softmax threads
-        mbar_init(&bars[kXEmpty], 128);
+        mbar_init(&bars[kXFull], 1);             // own expect_tx arrive + the peer's st.async bytes
+        mbar_init(&bars[kXEmpty], 1);            // the peer consumed what this CTA sent
         mbar_init(&bars[kODone], 1);
         mbar_init(&bars[kOFree], 4);
         mbar_init(&bars[kFinal], 1);
@@ -250,10 +253,7 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
         tc05::tmem_alloc(tslot, kTmemCols);
         tc05::tmem_relinquish();
     }
-    if (warp == kProducerWarp && lane == 0) {
-        prefetch_tmap(&tmq);
-        prefetch_tmap(&tmkv);
-    }
+    if (warp == kProducerWarp && lane == 0) prefetch_tmap(&tmkv);
     build_item_table(p, off, scan);   // contains __syncthreads
     tc05::fence_before_sync();
     __syncthreads();
@@ -264,26 +264,14 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
     if (warp == kProducerWarp) {
-        // ------------------------------------------------------------ producer
+        // ------------------------------------------------------------ producer: K/V tiles
         const int box = p.box_rows;
         const int nbox = kTile / box;
         const uint32_t box_bytes = static_cast<uint32_t>(box) * 128u;
-        uint32_t n = 0, ic = 0;
+        uint32_t n = 0;
         bool ok = true;
         for (int w = pair; w < total && ok; w += npairs) {
             const Item it = locate(p, off, w, false);
-            if (it.n_tiles == 0) continue;
-            if (lane == 0) {
-                ok = wait_bar(&bars[kQEmpty], (ic & 1) ^ 1, abort_flag, p.err);
-                if (ok) {
-                    mbar_arrive_expect_tx(&bars[kQFull], static_cast<uint32_t>(nslab) * kHeads * 128u);
-                    const int qrow = it.b * p.hq + it.hg * kHeads;
-                    for (int s = 0; s < nslab; ++s)
-                        tma_load_2d(sQ + s * kHeads * 128, &tmq, (slab0 + s) * 64, qrow, &bars[kQFull]);
-                }
-            }
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            ++ic;
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
                 int row = -1;
                 if (lane < nbox) {
@@ -320,14 +308,12 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
             }
         }
         // drain: the copies this warp issued have landed before shared memory is released
-        if (lane == 0) {
-            if (ic > 0) drain_wait(&bars[kQFull], (ic - 1) & 1);
+        if (lane == 0)
             for (uint32_t k = n > kStages ? n - kStages : 0; k < n; ++k)
                 drain_wait(&bars[kKvFull0 + k % kStages], (k / kStages) & 1);
-        }
         __syncwarp();
     } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issue
+        // ------------------------------------------------------------ MMA issue (one thread)
         const uint32_t id_qk = tc05::idesc_bf16_f32(kHeads, kTile, false, false);
         const uint32_t id_pv = tc05::idesc_bf16_f32(kHeads, 256, false, true);
         uint32_t n = 0, ic = 0;
@@ -352,12 +338,11 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
             if (!ok) return;
             tc05::fence_after_sync();
             if (lane == 0) {
+                const uint64_t vdesc = tc05::smem_desc(st, kSlabBytes, 1024);
 #pragma unroll
-                for (int k = 0; k < kTile / 16; ++k) {
-                    const uint64_t a = tc05::smem_desc(sP + k * 32, 16, 1024);
-                    const uint64_t b = tc05::smem_desc(st + k * 2048, kSlabBytes, 1024);
-                    tc05::mma_ss(tbase + kColO, a, b, id_pv, (tim == 0 && k == 0) ? 0u : 1u);
-                }
+                for (int k = 0; k < kTile / 16; ++k)   // 16 keys per MMA: +2048 bytes of V rows, +8 columns of P
+                    tc05::mma_ts(tbase + kColO, tbase + kColP + k * 8, vdesc + static_cast<uint64_t>(k * 2048 >> 4),
+                                 id_pv, (tim == 0 && k == 0) ? 0u : 1u);
                 tc05::commit(&bars[kPFree]);
                 tc05::commit(&bars[kKvEmpty0 + m % kStages]);
             }
@@ -370,19 +355,18 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
                 const int s = n % kStages;
                 ok = __all_sync(0xffffffffu, wait_bar(&bars[kKvFull0 + s], (n / kStages) & 1, abort_flag, p.err) &&
-                                                 wait_bar(&bars[kSFree0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err));
+                                                 wait_bar(&bars[kSFree], (n & 1) ^ 1, abort_flag, p.err));
                 if (!ok) break;
                 tc05::fence_after_sync();
                 if (lane == 0) {
-                    unsigned char *st = sKV + s * kStageBytes;
+                    const uint64_t kdesc = tc05::smem_desc(sKV + s * kStageBytes, 16, 1024);
                     for (int sl = 0; sl < nslab; ++sl)
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint64_t a = tc05::smem_desc(sQ + sl * kHeads * 128 + k * 32, 16, 1024);
-                            const uint64_t b = tc05::smem_desc(st + sl * kSlabBytes + k * 32, 16, 1024);
-                            tc05::mma_ss(tbase + kColS + s * 64, a, b, id_qk, (sl | k) ? 1u : 0u);
-                        }
-                    tc05::commit(&bars[kSFull0 + s]);
+                        for (int k = 0; k < 4; ++k)   // slab: +8 KB, k-step: +32 bytes (16 dims) / +8 TMEM columns
+                            tc05::mma_ts(tbase + kColS, tbase + kColQ + sl * 32 + k * 8,
+                                         kdesc + static_cast<uint64_t>((sl * kSlabBytes + k * 32) >> 4), id_qk,
+                                         (sl | k) ? 1u : 0u);
+                    tc05::commit(&bars[kSFull]);
                     if (ti == it.n_tiles - 1) tc05::commit(&bars[kQEmpty]);
                 }
                 __syncwarp();
@@ -418,44 +402,67 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
                 if (rank == 0 && p.lse) p.lse[orow] = -INFINITY;
                 continue;
             }
+            // ---- this head's q over this CTA's dims -> TMEM (A operand of q.k) ----
+            {
+                const uint4 *qs = reinterpret_cast<const uint4 *>(p.q + orow * kDqk + slab0 * 64);
+                uint32_t qv[16];
+                ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kQEmpty], (ic & 1) ^ 1, abort_flag, p.err));
+                tc05::fence_after_sync();
+#pragma unroll 1
+                for (int cc = 0; cc < nslab * 2; ++cc) {   // 16 columns = 32 bf16 per store
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint4 v = __ldg(qs + cc * 4 + e);
+                        qv[4 * e] = v.x;
+                        qv[4 * e + 1] = v.y;
+                        qv[4 * e + 2] = v.z;
+                        qv[4 * e + 3] = v.w;
+                    }
+                    if (ok) tc05::st_x16_u32(trow + kColQ + cc * 16, qv);
+                }
+                tc05::wait_st();
+                tc05::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kQFull]);
+            }
             float m = -INFINITY, l = 0.f;
             bool p_free_seen = false;
             for (int ti = 0; ti < it.n_tiles; ++ti, ++n) {
-                const int s = n % kStages;
+                if (tid == 0) mbar_arrive_expect_tx(&bars[kXFull], kHeads * kTile * 4);
                 float sv[64];
-                ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kSFull0 + s], (n / kStages) & 1, abort_flag, p.err));
+                ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kSFull], n & 1, abort_flag, p.err));
                 if (ok) {
                     tc05::fence_after_sync();
-                    tc05::ld_x64(trow + kColS + s * 64, sv);
+                    tc05::ld_x64(trow + kColS, sv);
                 } else {
 #pragma unroll
                     for (int j = 0; j < 64; ++j) sv[j] = 0.f;
                 }
                 tc05::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[kSFree0 + s]);
+                if (lane == 0) mbar_arrive(&bars[kSFree]);
                 // ---- swap partial scores with the peer CTA ----
                 ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kXEmpty], (n & 1) ^ 1, abort_flag, p.err, true));
                 if (ok) {
 #pragma unroll
                     for (int c = 0; c < 16; ++c)
-                        st_cluster_v4(x_peer + (row * 64 + 4 * c) * 4, sv[4 * c], sv[4 * c + 1], sv[4 * c + 2],
-                                      sv[4 * c + 3]);
-                    mbar_arrive_cluster(xf_peer);
+                        st_async_v4(x_peer + (c * kHeads + row) * 16, sv[4 * c], sv[4 * c + 1], sv[4 * c + 2],
+                                    sv[4 * c + 3], xf_peer);
                 }
-                ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kXFull], n & 1, abort_flag, p.err, true));
+                ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kXFull], n & 1, abort_flag, p.err));
                 if (ok) {
-                    const float4 *xr = reinterpret_cast<const float4 *>(sX + row * 64);
+                    const float4 *xr = reinterpret_cast<const float4 *>(sX);
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
-                        const float4 x = xr[c];
+                        const float4 x = xr[c * kHeads + row];
                         sv[4 * c] += x.x;
                         sv[4 * c + 1] += x.y;
                         sv[4 * c + 2] += x.z;
                         sv[4 * c + 3] += x.w;
                     }
-                    mbar_arrive_cluster(xe_peer);
                 }
+                named_bar_sync(1, 128);   // every softmax thread has read X
+                if (tid == 0 && ok) mbar_arrive_cluster(xe_peer);
                 // ---- online softmax over this tile's keys ----
                 const int n_valid = it.t_end - (it.t_begin + ti * kTile);
                 float mx = -INFINITY;
@@ -501,12 +508,19 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const
                 l += lsum;
                 if (!p_free_seen) ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kPFree], (n & 1) ^ 1, abort_flag, p.err));
                 p_free_seen = false;
-                // P row (64 keys, 128 bytes) in the 128-byte-swizzled K-major layout
+                // P row (64 keys as 32 bf16 pairs) into this lane's TMEM columns
+                if (ok) {
+                    tc05::fence_after_sync();
+                    uint32_t h0[16], h1[16];
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint4 *>(sP + row * 128 + ((c ^ (row & 7)) << 4)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                fence_proxy_async_smem();
+                    for (int j = 0; j < 16; ++j) {
+                        h0[j] = pk[j];
+                        h1[j] = pk[16 + j];
+                    }
+                    tc05::st_x16_u32(trow + kColP, h0);
+                    tc05::st_x16_u32(trow + kColP + 16, h1);
+                    tc05::wait_st();
+                }
                 tc05::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[kPFull]);
@@ -726,6 +740,7 @@ pkv_status launch(const pkv_decode_args *a, void *ws, size_t ws_bytes, int32_t *
     p.block_table = a->block_table;
     p.seq_lens = a->seq_lens;
     p.cu_seqlens = a->cu_seqlens;
+    p.q = static_cast<const uint16_t *>(a->q);
     p.out = static_cast<uint16_t *>(a->out);
     p.lse = a->lse;
     p.part_o = static_cast<float *>(ws);
@@ -733,17 +748,13 @@ pkv_status launch(const pkv_decode_args *a, void *ws, size_t ws_bytes, int32_t *
     p.err = err;
     if (a->layout == PKV_LAYOUT_VARLEN) p.ps_shift = 0, p.ps_mask = 0;
 
-    // TMA maps: q as [B * Hq rows, 576] (box 128 rows x 64 dims), the latent pool
-    // as [num_slots rows, 576] (box box_rows x 64 dims), both 128-byte swizzled.
-    CUtensorMap tmq, tmkv;
-    const uint64_t dq[2] = {static_cast<uint64_t>(kDqk), static_cast<uint64_t>(a->batch) * a->num_q_heads};
-    const uint64_t sq[1] = {static_cast<uint64_t>(kDqk) * 2};
-    const uint32_t bq[2] = {64, static_cast<uint32_t>(kHeads)};
+    // TMA map of the latent pool as [num_slots rows, 576] (box box_rows x 64 dims, 128-byte swizzle).
+    CUtensorMap tmkv;
     const uint64_t dk[2] = {static_cast<uint64_t>(kDqk), static_cast<uint64_t>(a->num_slots)};
     const uint64_t sk[1] = {static_cast<uint64_t>(a->k_row_stride) * 2};
     const uint32_t bk[2] = {64, static_cast<uint32_t>(p.box_rows)};
-    if (!encode_tmap_bf16(&tmq, a->q, 2, dq, sq, bq) || !encode_tmap_bf16(&tmkv, a->k_pool, 2, dk, sk, bk))
-        return fail(PKV_ERR_CUDA, "pkv_decode(MLA): cuTensorMapEncodeTiled rejected q or the latent pool");
+    if (!encode_tmap_bf16(&tmkv, a->k_pool, 2, dk, sk, bk))
+        return fail(PKV_ERR_CUDA, "pkv_decode(MLA): cuTensorMapEncodeTiled rejected the latent pool");
 
     static size_t lim = 0;
     static int max_pairs = 0;
@@ -774,7 +785,7 @@ pkv_status launch(const pkv_decode_args *a, void *ws, size_t ws_bytes, int32_t *
     }
     const int64_t items_upper = static_cast<int64_t>(a->batch) * pl.hgroups * pl.n_chunks_max;
     const int pairs = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(items_upper, max_pairs)));
-    mla_decode_kernel<<<2 * pairs, kThreads, smem, s>>>(p, tmq, tmkv);
+    mla_decode_kernel<<<2 * pairs, kThreads, smem, s>>>(p, tmkv);
     pkv_status st = check_launch("pkv_decode(MLA split kernel)");
     if (st != PKV_OK || pl.n_chunks_max == 1) return st;
     const size_t msmem = static_cast<size_t>(16) * pl.n_chunks_max * 4;
