@@ -34,6 +34,8 @@
 #include <cmath>
 #include <mutex>
 
+#include <cuda_fp16.h>
+
 #include "pkv_internal.cuh"
 #include "tc05.cuh"
 
@@ -44,8 +46,9 @@ constexpr int kDqk = 576, kDv = 512, kHeads = 128, kTile = 64;
 constexpr int kVSlabs = 4;                 // 256 value dims per CTA
 constexpr int kMaxSlabs = 5;               // q.k slabs of the wider CTA
 constexpr int kStages = 4;
-constexpr int kThreads = 192;              // warps 0-3 softmax, 4 producer, 5 MMA
-constexpr int kProducerWarp = 4, kMmaWarp = 5;
+constexpr int kSoftmaxWarps = 8;           // two threads per head row: keys 0-31 (warps 0-3), 32-63 (warps 4-7)
+constexpr int kThreads = 352;              // warps 0-7 softmax, 8 producer, 9 q.k MMAs, 10 P.V MMAs
+constexpr int kProducerWarp = 8, kMmaWarp = 9, kPvWarp = 10;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;              // 64-column score tile
 constexpr uint32_t kColO = 64;             // 256-column output accumulator
@@ -59,11 +62,14 @@ constexpr float kLazy = 8.f;
 constexpr int kSlabBytes = kTile * 128;                     // 8 KB: 64 keys x 64 dims
 constexpr int kStageBytes = kMaxSlabs * kSlabBytes;         // 40 KB
 constexpr int kOffKV = 0;
-constexpr int kOffX = kOffKV + kStages * kStageBytes;       // peer partial scores, fp32, [16 chunks][128 heads] x 16 B
-constexpr int kOffBar = kOffX + kHeads * kTile * 4;
+constexpr int kXBytes = kHeads * kTile * 2;                // one tile of peer partial scores, fp16
+constexpr int kXSlots = 3;
+constexpr int kOffX = kOffKV + kStages * kStageBytes;       // kXSlots slots, each [8 chunks][128 heads] x 16 B
+constexpr int kOffBar = kOffX + kXSlots * kXBytes;
 constexpr int kNumBars = 24;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;            // tmem slot, abort flag, scan scratch
-constexpr int kOffTable = kOffMisc + 64;
+constexpr int kOffRed = kOffMisc + 64;                      // row-max / row-sum exchange of the two half rows
+constexpr int kOffTable = kOffRed + 2 * 2 * kHeads * 4;
 constexpr int kFixedSmem = kOffTable + 1024;                // + item table + alignment slack
 
 struct Params {
@@ -82,6 +88,18 @@ struct Params {
     float *part_o, *part_lse;
     int32_t *err;
 };
+
+// bit casts between a 32-bit word and a pair of fp16 values (by value, so arrays stay in registers)
+__device__ __forceinline__ __half2 u2h2(uint32_t u) {
+    __half2_raw r;
+    r.x = static_cast<unsigned short>(u & 0xffffu);
+    r.y = static_cast<unsigned short>(u >> 16);
+    return __half2(r);
+}
+__device__ __forceinline__ uint32_t h22u(__half2 h) {
+    const __half2_raw r = static_cast<__half2_raw>(h);
+    return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
+}
 
 __device__ __forceinline__ float ex2(float x) {
     float y;
@@ -208,7 +226,7 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
 
 enum Bar {
     kQFull = 0, kQEmpty, kKvFull0, kKvEmpty0 = kKvFull0 + kStages, kSFull = kKvEmpty0 + kStages, kSFree, kPFull,
-    kPFree, kXFull, kXEmpty, kODone, kOFree, kFinal, kBarCount
+    kPFree, kXFull0, kODone = kXFull0 + kXSlots, kOFree, kFinal, kFinalPv, kBarCount
 };
 static_assert(kBarCount <= kNumBars, "barrier slots");
 
@@ -232,21 +250,21 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
 
     if (tid == 0) {
         *abort_flag = 0;
-        mbar_init(&bars[kQFull], 4);             // the 4 softmax warps after writing q into TMEM
+        mbar_init(&bars[kQFull], kSoftmaxWarps); // the softmax warps after writing q into TMEM
         mbar_init(&bars[kQEmpty], 1);            // MMA commit after an item's last q.k
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bars[kKvFull0 + s], 1);
             mbar_init(&bars[kKvEmpty0 + s], 1);
         }
         mbar_init(&bars[kSFull], 1);
-        mbar_init(&bars[kSFree], 4);
-        mbar_init(&bars[kPFull], 4);
+        mbar_init(&bars[kSFree], kSoftmaxWarps);
+        mbar_init(&bars[kPFull], kSoftmaxWarps);
         mbar_init(&bars[kPFree], 1);
-        mbar_init(&bars[kXFull], 1);             // own expect_tx arrive + the peer's st.async bytes
-        mbar_init(&bars[kXEmpty], 1);            // the peer consumed what this CTA sent
+        for (int x = 0; x < kXSlots; ++x) mbar_init(&bars[kXFull0 + x], 1);  // own expect_tx arrive + peer bytes
         mbar_init(&bars[kODone], 1);
-        mbar_init(&bars[kOFree], 4);
+        mbar_init(&bars[kOFree], kSoftmaxWarps);
         mbar_init(&bars[kFinal], 1);
+        mbar_init(&bars[kFinalPv], 1);
         mbar_init_fence();
     }
     if (warp == kMmaWarp) {
@@ -313,41 +331,12 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
                 drain_wait(&bars[kKvFull0 + k % kStages], (k / kStages) & 1);
         __syncwarp();
     } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issue (one thread)
+        // ------------------------------------------------------------ q.k MMAs (one thread)
+        // S(n) = Q K(n)^T as soon as the score tile is free (the softmax warps have
+        // read S(n-1)) and K/V tile n has landed; never waits for P V.
         const uint32_t id_qk = tc05::idesc_bf16_f32(kHeads, kTile, false, false);
-        const uint32_t id_pv = tc05::idesc_bf16_f32(kHeads, 256, false, true);
         uint32_t n = 0, ic = 0;
         bool ok = true;
-        // O += P V for tile m (the item's tile index tim), after softmax wrote P.
-        auto pv = [&](uint32_t m, int tim, const Item &it) {
-            ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kPFull], m & 1, abort_flag, p.err));
-            if (!ok) return;
-            unsigned char *st = sKV + (m % kStages) * kStageBytes;
-            const int n_valid = it.t_end - (it.t_begin + tim * kTile);
-            if (n_valid < kTile) {
-                // key rows past the end hold stale data: zero their value dims
-                for (int i = lane; i < (kTile - n_valid) * kVSlabs * 8; i += 32) {
-                    const int key = n_valid + i / (kVSlabs * 8);
-                    const int sl = (i / 8) % kVSlabs, c = i % 8;
-                    *reinterpret_cast<uint4 *>(st + sl * kSlabBytes + key * 128 + (c << 4)) = make_uint4(0, 0, 0, 0);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
-            if (tim == 0) ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kOFree], (ic & 1) ^ 1, abort_flag, p.err));
-            if (!ok) return;
-            tc05::fence_after_sync();
-            if (lane == 0) {
-                const uint64_t vdesc = tc05::smem_desc(st, kSlabBytes, 1024);
-#pragma unroll
-                for (int k = 0; k < kTile / 16; ++k)   // 16 keys per MMA: +2048 bytes of V rows, +8 columns of P
-                    tc05::mma_ts(tbase + kColO, tbase + kColP + k * 8, vdesc + static_cast<uint64_t>(k * 2048 >> 4),
-                                 id_pv, (tim == 0 && k == 0) ? 0u : 1u);
-                tc05::commit(&bars[kPFree]);
-                tc05::commit(&bars[kKvEmpty0 + m % kStages]);
-            }
-            __syncwarp();
-        };
         for (int w = pair; w < total && ok; w += npairs) {
             const Item it = locate(p, off, w, false);
             if (it.n_tiles == 0) continue;
@@ -370,11 +359,7 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
                     if (ti == it.n_tiles - 1) tc05::commit(&bars[kQEmpty]);
                 }
                 __syncwarp();
-                if (ti > 0) pv(n - 1, ti - 1, it);
             }
-            if (ok) pv(n - 1, it.n_tiles - 1, it);
-            if (ok && lane == 0) tc05::commit(&bars[kODone]);
-            __syncwarp();
             ++ic;
         }
         // drain: every MMA this warp issued has completed before TMEM is freed
@@ -383,180 +368,307 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
             drain_wait(&bars[kFinal], 0);
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------------------ softmax warps (one head per thread)
-        const int row = warp * 32 + lane;
-        const uint32_t x_peer = mapa(smem_u32(sX), peer);
-        const uint32_t xf_peer = mapa(smem_u32(&bars[kXFull]), peer);
-        const uint32_t xe_peer = mapa(smem_u32(&bars[kXEmpty]), peer);
-        const uint32_t trow = tc05::taddr(tbase, warp * 32, 0);
+    } else if (warp == kPvWarp) {
+        // ------------------------------------------------------------ P V MMAs (one thread)
+        const uint32_t id_pv = tc05::idesc_bf16_f32(kHeads, 256, false, true);
         uint32_t n = 0, ic = 0;
         bool ok = true;
+        for (int w = pair; w < total && ok; w += npairs) {
+            const Item it = locate(p, off, w, false);
+            if (it.n_tiles == 0) continue;
+            for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
+                ok = __all_sync(0xffffffffu, wait_bar(&bars[kPFull], n & 1, abort_flag, p.err));
+                if (!ok) break;
+                unsigned char *st = sKV + (n % kStages) * kStageBytes;
+                const int n_valid = it.t_end - (it.t_begin + ti * kTile);
+                if (n_valid < kTile) {
+                    // key rows past the end hold stale data: zero their value dims
+                    for (int i = lane; i < (kTile - n_valid) * kVSlabs * 8; i += 32) {
+                        const int key = n_valid + i / (kVSlabs * 8);
+                        const int sl = (i / 8) % kVSlabs, c = i % 8;
+                        *reinterpret_cast<uint4 *>(st + sl * kSlabBytes + key * 128 + (c << 4)) = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                if (ti == 0) ok = __all_sync(0xffffffffu, wait_bar(&bars[kOFree], (ic & 1) ^ 1, abort_flag, p.err));
+                if (!ok) break;
+                tc05::fence_after_sync();
+                if (lane == 0) {
+                    const uint64_t vdesc = tc05::smem_desc(st, kSlabBytes, 1024);
+#pragma unroll
+                    for (int k = 0; k < kTile / 16; ++k)   // 16 keys per MMA: +2048 bytes of V rows, +8 columns of P
+                        tc05::mma_ts(tbase + kColO, tbase + kColP + k * 8, vdesc + static_cast<uint64_t>(k * 2048 >> 4),
+                                     id_pv, (ti == 0 && k == 0) ? 0u : 1u);
+                    tc05::commit(&bars[kPFree]);
+                    tc05::commit(&bars[kKvEmpty0 + n % kStages]);
+                    if (ti == it.n_tiles - 1) tc05::commit(&bars[kODone]);
+                }
+                __syncwarp();
+            }
+            ++ic;
+        }
+        if (lane == 0) {
+            tc05::commit(&bars[kFinalPv]);
+            drain_wait(&bars[kFinalPv], 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax warps
+        // Thread (row, half) owns head `row` (TMEM lane) and keys [32 half, 32 half + 32)
+        // of every tile, value columns [128 half, +128) of O and half of q.
+        const int row = (warp & 3) * 32 + lane;
+        const int half = warp >> 2;
+        // The softmax warps run one tile ahead: in the iteration of tile n they load
+        // S(n + 1), wait for the peer's partial of tile n, send their own partial of
+        // tile n + 1, then do tile n's softmax, so the exchange of n + 1 overlaps
+        // the math of n on both CTAs.  Tile t travels in slot t % 3 of the
+        // receiver's buffer; a CTA sends tile n + 1 only after it received the
+        // peer's tile n, which the peer sends only after it finished reading tile
+        // n - 2 (the slot reused): no explicit release is needed.
+        const uint32_t x_peer = mapa(smem_u32(sX), peer);
+        const uint32_t xf_peer0 = mapa(smem_u32(&bars[kXFull0]), peer);
+        float *red = reinterpret_cast<float *>(smem + kOffRed);   // [2 buffers][2 halves][128 rows]
+        const uint32_t trow = tc05::taddr(tbase, (warp & 3) * 32, 0);
+        const int qcols = nslab * 16;                              // TMEM columns of q per half row
+        uint32_t n = 0, ic = 0;
+        bool ok = true;
+        // q of item `jt` over this CTA's dims (this thread's half of them) -> TMEM, once
+        // the previous item's q.k MMAs are done with the region.  All global loads
+        // are issued before the first TMEM store.
+        auto load_q = [&](const Item &jt, uint32_t jc) {
+            const int64_t qrow = static_cast<int64_t>(jt.b) * p.hq + jt.hg * kHeads + row;
+            const uint4 *qs = reinterpret_cast<const uint4 *>(p.q + qrow * kDqk + slab0 * 64 + half * qcols * 2);
+            ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kQEmpty], (jc & 1) ^ 1, abort_flag, p.err));
+            tc05::fence_after_sync();
+            // two batches (3 + 2 chunks of 16 columns = 32 bf16); each batch's global
+            // loads are all in flight before its TMEM stores
+#pragma unroll
+            for (int b0 = 0; b0 < 5; b0 += 3) {
+                uint4 qv[12];
+#pragma unroll
+                for (int i = 0; i < 12; ++i)
+                    if (b0 * 4 + i < qcols / 4 && i < (5 - b0) * 4) qv[i] = __ldg(qs + b0 * 4 + i);
+#pragma unroll
+                for (int cc = 0; cc < 3; ++cc) {
+                    if (ok && b0 + cc < qcols / 16 && cc < 5 - b0) {
+                        const uint32_t w[16] = {qv[4 * cc].x,     qv[4 * cc].y,     qv[4 * cc].z,     qv[4 * cc].w,
+                                                qv[4 * cc + 1].x, qv[4 * cc + 1].y, qv[4 * cc + 1].z, qv[4 * cc + 1].w,
+                                                qv[4 * cc + 2].x, qv[4 * cc + 2].y, qv[4 * cc + 2].z, qv[4 * cc + 2].w,
+                                                qv[4 * cc + 3].x, qv[4 * cc + 3].y, qv[4 * cc + 3].z, qv[4 * cc + 3].w};
+                        tc05::st_x16_u32(trow + kColQ + half * qcols + (b0 + cc) * 16, w);
+                    }
+                }
+            }
+            tc05::wait_st();
+            tc05::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kQFull]);
+        };
+        bool q_loaded = false;
         for (int w = pair; w < total; w += npairs) {
             const Item it = locate(p, off, w, tid == 0 && rank == 0);
             const int head = it.hg * kHeads + row;
             const int64_t orow = static_cast<int64_t>(it.b) * p.hq + head;
             if (it.n_tiles == 0) {
-                uint4 *o = reinterpret_cast<uint4 *>(p.out + orow * kDv + rank * 256);
-                for (int i = 0; i < 32; ++i) o[i] = make_uint4(0, 0, 0, 0);
-                if (rank == 0 && p.lse) p.lse[orow] = -INFINITY;
+                uint4 *o = reinterpret_cast<uint4 *>(p.out + orow * kDv + rank * 256 + half * 128);
+                for (int i = 0; i < 16; ++i) o[i] = make_uint4(0, 0, 0, 0);
+                if (rank == 0 && half == 0 && p.lse) p.lse[orow] = -INFINITY;
                 continue;
             }
-            // ---- this head's q over this CTA's dims -> TMEM (A operand of q.k) ----
-            {
-                const uint4 *qs = reinterpret_cast<const uint4 *>(p.q + orow * kDqk + slab0 * 64);
-                uint32_t qv[16];
-                ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kQEmpty], (ic & 1) ^ 1, abort_flag, p.err));
-                tc05::fence_after_sync();
-#pragma unroll 1
-                for (int cc = 0; cc < nslab * 2; ++cc) {   // 16 columns = 32 bf16 per store
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const uint4 v = __ldg(qs + cc * 4 + e);
-                        qv[4 * e] = v.x;
-                        qv[4 * e + 1] = v.y;
-                        qv[4 * e + 2] = v.z;
-                        qv[4 * e + 3] = v.w;
-                    }
-                    if (ok) tc05::st_x16_u32(trow + kColQ + cc * 16, qv);
-                }
-                tc05::wait_st();
-                tc05::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[kQFull]);
-            }
+            if (!q_loaded) load_q(it, ic);
+            q_loaded = false;
             float m = -INFINITY, l = 0.f;
-            bool p_free_seen = false;
+            // Scaled partial scores of tile t (this CTA's dims), rounded to fp16: 64
+            // keys as 32 half2 in nxt[].  Both CTAs round their own partial the same
+            // way, so own + peer is bitwise identical in the two CTAs.  (Macros rather
+            // than lambdas keep the arrays in registers.)
+#define PKV_MLA_FETCH(t)                                                                                         \
+    do {                                                                                                       \
+        if (tid == 0) mbar_arrive_expect_tx(&bars[kXFull0 + (t) % kXSlots], kXBytes);                          \
+        ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kSFull], (t) & 1, abort_flag, p.err));              \
+        float a_[64];                                                                                          \
+        if (ok) {                                                                                              \
+            tc05::fence_after_sync();                                                                          \
+            tc05::ld_x64(trow + kColS, a_);                                                                    \
+        } else {                                                                                               \
+            _Pragma("unroll") for (int j = 0; j < 64; ++j) a_[j] = 0.f;                                        \
+        }                                                                                                      \
+        tc05::fence_before_sync();                                                                             \
+        __syncwarp();                                                                                          \
+        if (lane == 0) mbar_arrive(&bars[kSFree]);                                                             \
+        _Pragma("unroll") for (int j = 0; j < 32; ++j)                                                         \
+            nxt[j] = h22u(__floats2half2_rn(a_[2 * j] * p.scale_log2, a_[2 * j + 1] * p.scale_log2));          \
+    } while (0)
+            // this thread's 32 keys of tile t (4 x 16 B) -> slot t % kXSlots of the peer
+#define PKV_MLA_SEND(t)                                                                                          \
+    do {                                                                                                       \
+        if (ok) {                                                                                              \
+            const uint32_t dst_ = x_peer + ((t) % kXSlots) * kXBytes;                                          \
+            const uint32_t bar_ = xf_peer0 + ((t) % kXSlots) * 8;                                              \
+            _Pragma("unroll") for (int c = 0; c < 4; ++c) {                                                    \
+                const int j = 4 * c; /* select, not an index: keeps nxt in registers */                        \
+                st_async_v4(dst_ + ((half * 4 + c) * kHeads + row) * 16, __uint_as_float(half ? nxt[16 + j] : nxt[j]), \
+                            __uint_as_float(half ? nxt[17 + j] : nxt[j + 1]),                                  \
+                            __uint_as_float(half ? nxt[18 + j] : nxt[j + 2]),                                  \
+                            __uint_as_float(half ? nxt[19 + j] : nxt[j + 3]), bar_);                           \
+            }                                                                                                  \
+        }                                                                                                      \
+    } while (0)
+            uint32_t cur[32], nxt[32];
+            PKV_MLA_FETCH(n);
+            PKV_MLA_SEND(n);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
             for (int ti = 0; ti < it.n_tiles; ++ti, ++n) {
-                if (tid == 0) mbar_arrive_expect_tx(&bars[kXFull], kHeads * kTile * 4);
-                float sv[64];
-                ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kSFull], n & 1, abort_flag, p.err));
-                if (ok) {
-                    tc05::fence_after_sync();
-                    tc05::ld_x64(trow + kColS, sv);
-                } else {
+                const bool ahead = ti + 1 < it.n_tiles;
+                if (ahead) PKV_MLA_FETCH(n + 1);
+                // ---- the peer's partial of tile n ----
+                const int xs = n % kXSlots;
+                ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kXFull0 + xs], (n / kXSlots) & 1, abort_flag, p.err));
+                // tile n + 1 may go out now: the peer has finished with the slot it reuses
+                if (ahead) PKV_MLA_SEND(n + 1);
+                const int n_valid = it.t_end - (it.t_begin + ti * kTile);
+                // own + peer partial in half2 (the same bits in both CTAs), row max in half2
+                __half2 x2[32];
+                {
+                    const uint4 *xr = reinterpret_cast<const uint4 *>(reinterpret_cast<unsigned char *>(sX) + xs * kXBytes);
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) sv[j] = 0.f;
-                }
-                tc05::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[kSFree]);
-                // ---- swap partial scores with the peer CTA ----
-                ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kXEmpty], (n & 1) ^ 1, abort_flag, p.err, true));
-                if (ok) {
-#pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        st_async_v4(x_peer + (c * kHeads + row) * 16, sv[4 * c], sv[4 * c + 1], sv[4 * c + 2],
-                                    sv[4 * c + 3], xf_peer);
-                }
-                ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kXFull], n & 1, abort_flag, p.err));
-                if (ok) {
-                    const float4 *xr = reinterpret_cast<const float4 *>(sX);
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const float4 x = xr[c * kHeads + row];
-                        sv[4 * c] += x.x;
-                        sv[4 * c + 1] += x.y;
-                        sv[4 * c + 2] += x.z;
-                        sv[4 * c + 3] += x.w;
+                    for (int c = 0; c < 8; ++c) {
+                        uint4 w4 = make_uint4(0, 0, 0, 0);
+                        if (ok) w4 = xr[c * kHeads + row];
+                        x2[4 * c] = __hadd2(u2h2(cur[4 * c]), u2h2(w4.x));
+                        x2[4 * c + 1] = __hadd2(u2h2(cur[4 * c + 1]), u2h2(w4.y));
+                        x2[4 * c + 2] = __hadd2(u2h2(cur[4 * c + 2]), u2h2(w4.z));
+                        x2[4 * c + 3] = __hadd2(u2h2(cur[4 * c + 3]), u2h2(w4.w));
                     }
                 }
-                named_bar_sync(1, 128);   // every softmax thread has read X
-                if (tid == 0 && ok) mbar_arrive_cluster(xe_peer);
-                // ---- online softmax over this tile's keys ----
-                const int n_valid = it.t_end - (it.t_begin + ti * kTile);
-                float mx = -INFINITY;
+                if (n_valid < kTile) {   // keys past the end: -inf
+                    const __half2 ninf = __halves2half2(__ushort_as_half(0xfc00), __ushort_as_half(0xfc00));
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    sv[j] = j < n_valid ? sv[j] * p.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, sv[j]);
+                    for (int j = 0; j < 32; ++j) {
+                        if (2 * j >= n_valid) x2[j] = ninf;
+                        else if (2 * j + 1 >= n_valid) x2[j] = __halves2half2(__low2half(x2[j]), __ushort_as_half(0xfc00));
+                    }
                 }
+                float mx;
+                {
+                    __half2 m2 = x2[0];
+#pragma unroll
+                    for (int j = 1; j < 32; ++j) m2 = __hmax2(m2, x2[j]);
+                    const float2 mf = __half22float2(m2);
+                    mx = fmaxf(mf.x, mf.y);
+                }
+                // ---- online softmax over this tile's keys ----
                 const bool raise = mx > m + kLazy || (m == -INFINITY && mx != -INFINITY);
                 const float corr = raise ? ex2(m - mx) : 1.f;
-                // O rescale in TMEM (warp-collective; rows whose max did not move use corr = 1)
-                if (__any_sync(0xffffffffu, raise && l > 0.f)) {
-                    // O must be final for the previous tile before it is rescaled
-                    ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kPFree], (n & 1) ^ 1, abort_flag, p.err));
-                    p_free_seen = true;
-                    if (ok) {
-                        tc05::fence_after_sync();
+                // O (and P) are final for tile n - 1 once its P V completed
+                ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kPFree], (n & 1) ^ 1, abort_flag, p.err));
+                if (__any_sync(0xffffffffu, raise && l > 0.f) && ok) {
+                    // rescale this thread's 128 value columns of O in TMEM
+                    tc05::fence_after_sync();
 #pragma unroll 1
-                        for (int cc = 0; cc < 16; ++cc) {
-                            float ov[16];
-                            tc05::ld_x16(trow + kColO + cc * 16, ov);
-                            tc05::wait_ld();
+                    for (int cc = 0; cc < 8; ++cc) {
+                        float ov[16];
+                        tc05::ld_x16(trow + kColO + half * 128 + cc * 16, ov);
+                        tc05::wait_ld();
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) ov[e] *= corr;
-                            tc05::st_x16(trow + kColO + cc * 16, ov);
-                        }
-                        tc05::wait_st();
+                        for (int e = 0; e < 16; ++e) ov[e] *= corr;
+                        tc05::st_x16(trow + kColO + half * 128 + cc * 16, ov);
                     }
+                    tc05::wait_st();
                 }
                 if (raise) {
                     l *= corr;
                     m = mx;
                 }
-                uint32_t pk[32];
+                uint32_t h[16];
                 float lsum = 0.f;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float p0 = m == -INFINITY ? 0.f : ex2(sv[2 * j] - m);
-                    const float p1 = m == -INFINITY ? 0.f : ex2(sv[2 * j + 1] - m);
-                    lsum += p0 + p1;
-                    pk[j] = pack_bf16x2(p0, p1);
+                // this thread's 32 keys (half is warp-uniform: a branch, not an index)
+#define PKV_MLA_EXP(OFF)                                                                         \
+    _Pragma("unroll") for (int j = 0; j < 16; ++j) {                                            \
+        const float2 xf = __half22float2(x2[(OFF) + j]);                                        \
+        const float p0 = m == -INFINITY ? 0.f : ex2(xf.x - m);                                  \
+        const float p1 = m == -INFINITY ? 0.f : ex2(xf.y - m);                                  \
+        lsum += p0 + p1;                                                                        \
+        h[j] = pack_bf16x2(p0, p1);                                                             \
+    }
+                if (half) {
+                    PKV_MLA_EXP(16)
+                } else {
+                    PKV_MLA_EXP(0)
                 }
+#undef PKV_MLA_EXP
                 l += lsum;
-                if (!p_free_seen) ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kPFree], (n & 1) ^ 1, abort_flag, p.err));
-                p_free_seen = false;
-                // P row (64 keys as 32 bf16 pairs) into this lane's TMEM columns
+                // this half's 32 keys of P (16 bf16 pairs) into the lane's TMEM columns
                 if (ok) {
                     tc05::fence_after_sync();
-                    uint32_t h0[16], h1[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        h0[j] = pk[j];
-                        h1[j] = pk[16 + j];
-                    }
-                    tc05::st_x16_u32(trow + kColP, h0);
-                    tc05::st_x16_u32(trow + kColP + 16, h1);
+                    tc05::st_x16_u32(trow + kColP + half * 16, h);
                     tc05::wait_st();
                 }
                 tc05::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[kPFull]);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
+            }
+#undef PKV_MLA_FETCH
+#undef PKV_MLA_SEND
+            // ---- the next item's q goes into TMEM now, so its q.k overlaps this epilogue ----
+            for (int w2 = w + npairs; w2 < total; w2 += npairs) {
+                const Item nt = locate(p, off, w2, false);
+                if (nt.n_tiles > 0) {
+                    load_q(nt, ic + 1);
+                    q_loaded = true;
+                    break;
+                }
             }
             // ---- epilogue: normalise O and write the output (or the split partial) ----
+            // l of the whole row = both halves' partial sums (m is the same in both).
+            // slot n & 1: not the last tile's max slot, and free since tile n - 1's barrier
+            float *lb = red + (n & 1) * 2 * kHeads;
+            lb[half * kHeads + row] = l;
+            named_bar_sync(1, kSoftmaxWarps * 32);
+            l += lb[(half ^ 1) * kHeads + row];
+            named_bar_sync(1, kSoftmaxWarps * 32);
             ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kODone], ic & 1, abort_flag, p.err));
             tc05::fence_after_sync();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const bool single = it.n_chunks == 1;
             const int64_t prow = (static_cast<int64_t>(it.b) * p.n_chunks_max + it.c) * p.hq + head;
 #pragma unroll 1
-            for (int cc = 0; cc < 16; ++cc) {
-                float ov[16];
+            for (int cb = 0; cb < 8; cb += 4) {
+                float ov[4][16];
                 if (ok) {
-                    tc05::ld_x16(trow + kColO + cc * 16, ov);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) tc05::ld_x16(trow + kColO + half * 128 + (cb + q4) * 16, ov[q4]);
                     tc05::wait_ld();
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) ov[e] = 0.f;
+                    for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) ov[q4][e] = 0.f;
                 }
-                const int col = rank * 256 + cc * 16;
-                if (single) {
-                    uint32_t h[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) h[e] = pack_bf16x2(ov[2 * e] * inv, ov[2 * e + 1] * inv);
-                    uint4 *o = reinterpret_cast<uint4 *>(p.out + orow * kDv + col);
-                    o[0] = make_uint4(h[0], h[1], h[2], h[3]);
-                    o[1] = make_uint4(h[4], h[5], h[6], h[7]);
-                } else {
-                    float4 *o = reinterpret_cast<float4 *>(p.part_o + prow * kDv + col);
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int col = rank * 256 + half * 128 + (cb + q4) * 16;
+                    if (single) {
+                        uint32_t hh[8];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        o[e] = make_float4(ov[4 * e] * inv, ov[4 * e + 1] * inv, ov[4 * e + 2] * inv, ov[4 * e + 3] * inv);
+                        for (int e = 0; e < 8; ++e) hh[e] = pack_bf16x2(ov[q4][2 * e] * inv, ov[q4][2 * e + 1] * inv);
+                        uint4 *o = reinterpret_cast<uint4 *>(p.out + orow * kDv + col);
+                        o[0] = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+                        o[1] = make_uint4(hh[4], hh[5], hh[6], hh[7]);
+                    } else {
+                        float4 *o = reinterpret_cast<float4 *>(p.part_o + prow * kDv + col);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            o[e] = make_float4(ov[q4][4 * e] * inv, ov[q4][4 * e + 1] * inv, ov[q4][4 * e + 2] * inv,
+                                               ov[q4][4 * e + 3] * inv);
+                    }
                 }
             }
-            if (rank == 0) {
+            if (rank == 0 && half == 0) {
                 const float lse2 = m + log2f(l);
                 if (single) {
                     if (p.lse) p.lse[orow] = lse2 * kLn2;
