@@ -249,6 +249,21 @@ def oracle_sample_run(wl, budget_key_heads, seed=0, num_threads=0, fetch_rows=No
     return secs, nbytes, desc, oracle.max_threads() if num_threads <= 0 else num_threads
 
 
+# ---------------------------------------------------------------- multi-process plumbing
+def reduce_max(x, dist=None, device="cpu"):
+    """Max of a float over all ranks (identity without a process group)."""
+    if dist is None:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_gbs(world, bytes_per_step, steps, max_ms):
+    """Whole-job GB/s: every rank processed its own replica of the step in max_ms (slowest rank)."""
+    return world * bytes_per_step * steps / (max_ms / 1e3) / 1e9
+
+
 # ---------------------------------------------------------------- arms
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -360,13 +375,9 @@ def run_ours(args):
         dist.barrier()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     dec_ms = [sum(a.elapsed_time(b) for a, b in row) for row in dev_ev]
-    tot_ms = sum(step_ms)
-    if dist is not None:
-        t = torch.tensor([tot_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms = float(t.item())
+    tot_ms = reduce_max(sum(step_ms), dist, "cuda")
     ms_per_step = tot_ms / args.steps
-    value = world * total_bytes * args.steps / (tot_ms / 1e3) / 1e9
+    value = weak_scaling_gbs(world, total_bytes, args.steps, tot_ms)
     if step.check_errors():
         raise SystemExit("device error flags raised: %d" % step.check_errors())
 
@@ -394,12 +405,8 @@ def run_ours(args):
         step.run_from_host(h_in, h_out)
         e_ev[i][1].record(stream)
     torch.cuda.synchronize()
-    e_ms = sum(a.elapsed_time(b) for a, b in e_ev)
-    if dist is not None:
-        t = torch.tensor([e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e_ms = float(t.item())
-    e2e_value = world * total_bytes * args.steps / (e_ms / 1e3) / 1e9
+    e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in e_ev), dist, "cuda")
+    e2e_value = weak_scaling_gbs(world, total_bytes, args.steps, e_ms)
 
     if rank != 0:
         if dist is not None:
