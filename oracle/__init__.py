@@ -41,8 +41,14 @@ def build(force: bool = False) -> str:
 def _load():
     global _lib
     if _lib is None:
-        build()
-        lib = ctypes.CDLL(_LIB)
+        # The mutation tests point this at a deliberately broken copy of the
+        # oracle to show that the pins catch it; nothing else sets it.
+        override = os.environ.get("PKV_ORACLE_LIB")
+        if override:
+            lib = ctypes.CDLL(override)
+        else:
+            build()
+            lib = ctypes.CDLL(_LIB)
         P, I32, I64, D = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double
         lib.pkvo_build_indices.argtypes = [P, I64, I64, I64, P, P, P, I32, I32, I64, P, P, I64, P, P, I32]
         lib.pkvo_build_indices.restype = ctypes.c_int

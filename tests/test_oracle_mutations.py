@@ -1,0 +1,71 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case below plants one mistake in a copy of the oracle's C source (on the
+CPU, in a temporary directory), compiles it, and runs the pin suite against
+the broken library.  The suite must fail for every one of them: a dropped
+term, a wrong sign or index, a swapped operand or stride, a missing offset.
+The committed oracle itself is never modified.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+import sys
+
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+SRC = os.path.join(ROOT, "oracle", "pkv_oracle.c")
+
+# (name, text in the source, replacement, how many occurrences to replace; 0 = all).
+# A deleted statement is replaced by ";" so that the surrounding code keeps its shape.
+MUTANTS = [
+    ("interleaved_kv_head", "kh = h / g;", "kh = h % hkv;", 1),
+    ("dropped_scale", "x[t - t0] = scale * acc;", "x[t - t0] = acc;", 1),
+    ("shared_query_row", "q + bh * dqk", "q + b * dqk", 1),
+    ("v_offset_uses_dqk", "v_pool + slot * v_row_stride + kh * dv", "v_pool + slot * v_row_stride + kh * dqk", 1),
+    ("decode_ignores_kv_start", "r2t[row * row_stride + start + t];\n            if (slot < 0 || slot >= num_slots) { bad",
+     "r2t[row * row_stride + t];\n            if (slot < 0 || slot >= num_slots) { bad", 1),
+    ("lse_without_max", "if (lse) lse[bh] = m + log(den);", "if (lse) lse[bh] = log(den);", 1),
+    ("empty_lse_zero", "if (lse) lse[bh] = -INFINITY;", "if (lse) lse[bh] = 0.0;", 1),
+    ("merge_sign", "const double w = exp(l - m);", "const double w = exp(m - l);", 1),
+    ("merge_unnormalised", "for (int32_t d = 0; d < dv; ++d) o[d] /= wsum;", ";", 1),
+    ("indices_ignore_kv_start", "const int64_t col = start + p * page_size;", "const int64_t col = p * page_size;", 1),
+    ("last_page_len_mod", "(int32_t)(len - (npages - 1) * page_size)", "(int32_t)(len % page_size)", 1),
+    ("no_alignment_check", "if (first % page_size != 0) return PKVO_ERR_CONTIG;", ";", 1),
+    ("no_contiguity_check", "if (r2t[row * row_stride + col + j] != first + j) return PKVO_ERR_CONTIG;", ";", 1),
+    ("block_table_pad_zero", "block_table[(int64_t)b * bt_width + p] = -1;", "block_table[(int64_t)b * bt_width + p] = 0;", 1),
+    ("indptr_not_cumulative", "if (kv_indptr) kv_indptr[b + 1] = (int32_t)running;",
+     "if (kv_indptr) kv_indptr[b + 1] = (int32_t)npages;", 1),
+    ("store_indexes_source_by_slot", "rows + (int64_t)i * src_row_stride_bytes", "rows + slot * src_row_stride_bytes", 1),
+    ("store_ignores_padding", "if (slot < 0) continue;", ";", 1),
+    ("cu_seqlens_not_cumulative", "cu_seqlens[b + 1] = (int32_t)running;", "cu_seqlens[b + 1] = (int32_t)len;", 1),
+    ("gather_ignores_kv_start",
+     "const int64_t slot = r2t[row * row_stride + start + t];\n            if (slot < 0 || slot >= num_slots) return",
+     "const int64_t slot = r2t[row * row_stride + t];\n            if (slot < 0 || slot >= num_slots) return", 1),
+]
+
+
+def _mutate(src: str, old: str, new: str, count: int) -> str:
+    n = src.count(old)
+    assert n >= 1, "mutation anchor not found: %r" % old
+    if count:
+        assert n == count, "mutation anchor %r occurs %d times" % (old, n)
+    return src.replace(old, new)
+
+
+@pytest.mark.parametrize("name,old,new,count", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new, count):
+    with open(SRC) as f:
+        src = f.read()
+    mutated = _mutate(src, old, new, count)
+    c = tmp_path / ("mutant_%s.c" % name)
+    c.write_text(mutated)
+    lib = tmp_path / ("libmutant_%s.so" % name)
+    subprocess.check_call(["gcc", "-O1", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", str(lib), str(c), "-lm"])
+    env = dict(os.environ, PKV_ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(HERE, "test_oracle_pins.py"), "-x", "-q",
+                        "-p", "no:cacheprovider"],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0, "pins did not catch mutant %s:\n%s" % (name, r.stdout[-2000:])

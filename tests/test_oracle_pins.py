@@ -178,11 +178,14 @@ def test_p4_store_worked_example():
 
 
 def test_store_skips_negative_and_flags_out_of_range():
-    pool = np.zeros((8, 4), dtype=np.uint16)
+    # guard rows on both sides of the pool catch a write through a padded (-1)
+    # or out-of-range slot
+    buf = np.zeros((10, 4), dtype=np.uint16)
+    pool = buf[1:9]
     rows = np.arange(12, dtype=np.uint16).reshape(3, 4) + 1
     assert oracle.store(pool, rows, [-1, 3, 9]) == oracle.ERR_RANGE
     assert np.array_equal(pool[3], rows[1])
-    assert pool.sum() == rows[1].sum()
+    assert buf.sum() == rows[1].sum()
 
 
 # ---------------------------------------------------------------- decode
