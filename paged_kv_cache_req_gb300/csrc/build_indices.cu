@@ -1,53 +1,77 @@
 // pkv_build_indices: per-request page lists from the token-granular req_to_token table.
 //
-// One CTA per request.  The CTA finds its kv_indptr offset by summing the page
-// counts of the requests before it (B is small: a few hundred ints from L2),
-// then reads its row once with coalesced loads.  Each position t compares its
-// slot with the slot of its page's first position (a broadcast load), which
-// checks page alignment and contiguity ("From slots to a page table": the
+// Grid (request, span): each CTA owns one span of a request's positions (about
+// 2048, a whole number of pages), so a long row is read by many CTAs at once
+// rather than walked by one.  A CTA finds its kv_indptr offset by summing the
+// page counts of the requests before it (a few hundred ints from L2), then
+// reads its span with eight independent loads per thread.  Each position t
+// compares its slot with the slot of its page's first position, which checks
+// page alignment and contiguity ("From slots to a page table": the
 // stride-and-divide derivation relies on tokens being contiguous inside a
 // page); the thread owning a page's first position writes the page id.
+#include <algorithm>
+
 #include "pkv_internal.cuh"
 
 namespace pkv {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kUnroll = 8;
+constexpr int kSpanTarget = kThreads * kUnroll;
+
+// Positions per CTA: a whole number of pages, close to kSpanTarget.
+int64_t span_for(int32_t ps) { return ps >= kSpanTarget ? ps : static_cast<int64_t>(ps) * (kSpanTarget / ps); }
 
 __global__ void __launch_bounds__(kThreads)
 build_indices_kernel(const int32_t *__restrict__ r2t, int64_t r2t_rows, int64_t row_stride, int64_t width,
                      const int32_t *__restrict__ req_pool_idx, const int32_t *__restrict__ seq_lens,
                      const int32_t *__restrict__ kv_start, int32_t batch, int32_t ps, int64_t num_pool_pages,
-                     int32_t *__restrict__ kv_indptr, int32_t *__restrict__ kv_indices, int64_t cap,
+                     int64_t span, int32_t *__restrict__ kv_indptr, int32_t *__restrict__ kv_indices, int64_t cap,
                      int32_t *__restrict__ last_page_len, int32_t *__restrict__ block_table, int32_t bt_width,
                      int32_t *__restrict__ err) {
     __shared__ long long scratch[32];
     const int b = blockIdx.x;
+    const int64_t c = blockIdx.y;
     if (b >= batch) {  // batch == 0: the single CTA only writes kv_indptr[0]
-        if (threadIdx.x == 0 && kv_indptr) kv_indptr[0] = 0;
+        if (threadIdx.x == 0 && c == 0 && kv_indptr) kv_indptr[0] = 0;
         return;
     }
 
-    // A request whose row/region lies outside the table contributes no pages.
-    auto pages_of = [&](int j, bool &valid) -> long long {
+    // Page count of request j, or -1 when its row/region lies outside the table
+    // (such a request contributes no pages).
+    auto pages_of = [&](int j) -> long long {
         const int64_t row = req_pool_idx[j];
         const int64_t s = kv_start ? kv_start[j] : 0;
         const int64_t L = seq_lens[j];
-        valid = row >= 0 && row < r2t_rows && s >= 0 && L >= 0 && s + L <= width;
-        return valid ? (L + ps - 1) / ps : 0;
+        const bool ok = row >= 0 && row < r2t_rows && s >= 0 && L >= 0 && s + L <= width;
+        return ok ? (L + ps - 1) / ps : -1;
     };
 
-    long long before = 0;
-    for (int j = threadIdx.x; j < b; j += kThreads) {
-        bool v;
-        before += pages_of(j, v);
-    }
-    before = block_sum(before, scratch);
-
-    bool valid;
-    const long long n = pages_of(b, valid);
+    const long long n_or_bad = pages_of(b);
+    const bool valid = n_or_bad >= 0;
+    const long long n = valid ? n_or_bad : 0;
     const int64_t L = valid ? seq_lens[b] : 0;
-    if (threadIdx.x == 0) {
+    const int64_t t_begin = c * span;
+    const int64_t t_end = min(L, t_begin + span);
+    const int64_t p_begin = t_begin / ps, p_end = (t_begin + span) / ps;
+
+    if (block_table) {
+        const int64_t pad_end = min(static_cast<int64_t>(bt_width), p_end);
+        for (int64_t p = max(static_cast<int64_t>(n), p_begin) + threadIdx.x; p < pad_end; p += kThreads)
+            block_table[static_cast<int64_t>(b) * bt_width + p] = -1;
+    }
+
+    const bool header = c == 0;
+    if (!header && t_begin >= t_end) return;  // nothing of this request in this span
+
+    long long before = 0;
+    if (kv_indptr) {  // kv_indptr, kv_indices and kv_last_page_len come together
+        for (int j = threadIdx.x; j < b; j += kThreads) before += max(pages_of(j), 0LL);
+        before = block_sum(before, scratch);
+    }
+
+    if (header && threadIdx.x == 0) {
         if (!valid) raise_flag(err, PKV_DEVERR_RANGE);
         if (kv_indptr) {
             if (b == 0) kv_indptr[0] = 0;
@@ -57,33 +81,46 @@ build_indices_kernel(const int32_t *__restrict__ r2t, int64_t r2t_rows, int64_t 
         if (kv_indices && before + n > cap) raise_flag(err, PKV_DEVERR_CAPACITY);
         if (block_table && n > bt_width) raise_flag(err, PKV_DEVERR_CAPACITY);
     }
+    if (t_begin >= t_end) return;
 
-    const int32_t *row = r2t + (valid ? req_pool_idx[b] * row_stride + (kv_start ? kv_start[b] : 0) : 0);
+    const int32_t *row = r2t + req_pool_idx[b] * row_stride + (kv_start ? kv_start[b] : 0);
     const int64_t pool_slots = num_pool_pages * ps;
     const bool pow2 = (ps & (ps - 1)) == 0;
     const int shift = __ffs(ps) - 1;
-    const int Li = static_cast<int>(L);
+    const int te = static_cast<int>(t_end);  // width <= INT32_MAX (checked on the host)
     int bad = 0;
-    for (int t = threadIdx.x; t < Li; t += kThreads) {
-        const int off = pow2 ? (t & (ps - 1)) : (t % ps);
-        const int pg = pow2 ? (t >> shift) : (t / ps);
-        const int64_t head = __ldg(row + (t - off));   // slot of this page's first position
-        if (off == 0) {
-            if (head < 0 || head >= pool_slots) {
-                bad |= PKV_DEVERR_RANGE;
-                continue;
+    for (int base = static_cast<int>(t_begin) + threadIdx.x; base < te; base += kThreads * kUnroll) {
+        int32_t slot[kUnroll] = {}, head[kUnroll] = {};
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+            const int t = base + k * kThreads;
+            if (t < te) {
+                const int off = pow2 ? (t & (ps - 1)) : (t % ps);
+                slot[k] = __ldg(row + t);
+                head[k] = __ldg(row + (t - off));  // slot of this page's first position
             }
-            if ((pow2 ? (head & (ps - 1)) : (head % ps)) != 0) bad |= PKV_DEVERR_CONTIG;
-            const int32_t page = static_cast<int32_t>(pow2 ? (head >> shift) : (head / ps));
-            if (kv_indices && before + pg < cap) kv_indices[before + pg] = page;
-            if (block_table && pg < bt_width) block_table[static_cast<int64_t>(b) * bt_width + pg] = page;
-        } else if (__ldg(row + t) != head + off) {
-            bad |= PKV_DEVERR_CONTIG;
+        }
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+            const int t = base + k * kThreads;
+            if (t >= te) continue;
+            const int off = pow2 ? (t & (ps - 1)) : (t % ps);
+            const int64_t h = head[k];
+            if (off == 0) {
+                if (h < 0 || h >= pool_slots) {
+                    bad |= PKV_DEVERR_RANGE;
+                    continue;
+                }
+                if ((pow2 ? (h & (ps - 1)) : (h % ps)) != 0) bad |= PKV_DEVERR_CONTIG;
+                const int pg = pow2 ? (t >> shift) : (t / ps);
+                const int32_t page = static_cast<int32_t>(pow2 ? (h >> shift) : (h / ps));
+                if (kv_indices && before + pg < cap) kv_indices[before + pg] = page;
+                if (block_table && pg < bt_width) block_table[static_cast<int64_t>(b) * bt_width + pg] = page;
+            } else if (slot[k] != h + off) {
+                bad |= PKV_DEVERR_CONTIG;
+            }
         }
     }
-    if (block_table)
-        for (int64_t p = n + threadIdx.x; p < bt_width; p += kThreads)
-            block_table[static_cast<int64_t>(b) * bt_width + p] = -1;
     if (bad) raise_flag(err, bad);
 }
 
@@ -108,10 +145,16 @@ extern "C" pkv_status pkv_build_indices(const int32_t *req_to_token, int64_t r2t
     if (batch > 0 && (!req_to_token || !req_pool_idx || !seq_lens))
         return fail(PKV_ERR_INVALID_ARG, "pkv_build_indices: null input table");
     if (num_pool_pages > INT32_MAX) return fail(PKV_ERR_UNSUPPORTED, "pkv_build_indices: more than 2^31 pages");
-    const int grid = batch > 0 ? batch : 1;
+    if (r2t_width > INT32_MAX) return fail(PKV_ERR_UNSUPPORTED, "pkv_build_indices: rows wider than 2^31 columns");
+    // Spans cover every position a row can hold and every block-table column.
+    const int64_t span = span_for(page_size);
+    const int64_t covered = std::max<int64_t>(r2t_width, static_cast<int64_t>(block_table_width) * page_size);
+    const int64_t spans = std::max<int64_t>(1, (covered + span - 1) / span);
+    if (spans > 65535) return fail(PKV_ERR_UNSUPPORTED, "pkv_build_indices: rows too wide for the span grid");
+    const dim3 grid(batch > 0 ? batch : 1, static_cast<unsigned>(spans));
     build_indices_kernel<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
         req_to_token, r2t_rows, r2t_row_stride, r2t_width, req_pool_idx, seq_lens, kv_start, batch, page_size,
-        num_pool_pages, kv_indptr, kv_indices, kv_indices_cap, kv_last_page_len, block_table, block_table_width,
-        err_flags);
+        num_pool_pages, span, kv_indptr, kv_indices, kv_indices_cap, kv_last_page_len, block_table,
+        block_table_width, err_flags);
     return check_launch("pkv_build_indices");
 }

@@ -74,6 +74,47 @@ def test_build_indices_bit_exact(B, name):
         np.testing.assert_array_equal(bt.cpu().numpy(), e_bt)
 
 
+@pytest.mark.parametrize("ps", [1, 3, 64, 4096])
+def test_build_indices_long_rows_and_wide_tables(B, ps):
+    """Rows spanning many CTA spans, page sizes that do not divide the span (3) or
+    exceed it (4096), and a block table wider than any request needs."""
+    dev = torch.device("cuda")
+    rng = np.random.default_rng(ps)
+    lens = [0, 1, 2047, 2048, 2049, 9001, 5 * ps + 1]
+    num_pages = sum(-(-L // ps) for L in lens) + 9
+    starts = [0, ps, 0, 2 * ps, 0, 0, ps]
+    r2t, rpi = paged_table(rng, lens, ps, num_pages, kv_start=starts)
+    width_pages = max(-(-L // ps) for L in lens) + 40
+    cap = sum(-(-L // ps) for L in lens)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    indptr = torch.full((len(lens) + 1,), -7, dtype=torch.int32, device=dev)
+    idx = torch.full((cap,), -7, dtype=torch.int32, device=dev)
+    last = torch.full((len(lens),), -7, dtype=torch.int32, device=dev)
+    bt = torch.full((len(lens), width_pages), -7, dtype=torch.int32, device=dev)
+    B.pkv_build_indices(torch.from_numpy(r2t).to(dev), torch.from_numpy(rpi).to(dev),
+                        torch.tensor(lens, dtype=torch.int32, device=dev), ps, num_pages, err,
+                        kv_start=torch.tensor(starts, dtype=torch.int32, device=dev), kv_indptr=indptr,
+                        kv_indices=idx, kv_last_page_len=last, block_table=bt)
+    st, e_ptr, e_idx, e_last, e_bt = oracle.build_indices(r2t, rpi, lens, ps, num_pages, kv_start=starts,
+                                                          kv_indices_cap=cap, bt_width=width_pages)
+    assert st == oracle.OK and err.item() == 0
+    np.testing.assert_array_equal(indptr.cpu().numpy(), e_ptr)
+    np.testing.assert_array_equal(idx.cpu().numpy(), e_idx)
+    np.testing.assert_array_equal(last.cpu().numpy(), e_last)
+    np.testing.assert_array_equal(bt.cpu().numpy(), e_bt)
+    # a contiguity break deep inside the longest row is still seen (any slot change
+    # breaks a page of more than one key)
+    if ps > 1:
+        bad = r2t.copy()
+        bad[rpi[5], 8001] += 1
+        err.zero_()
+        B.pkv_build_indices(torch.from_numpy(bad).to(dev), torch.from_numpy(rpi).to(dev),
+                            torch.tensor(lens, dtype=torch.int32, device=dev), ps, num_pages, err,
+                            kv_start=torch.tensor(starts, dtype=torch.int32, device=dev), kv_indptr=indptr,
+                            kv_indices=idx, kv_last_page_len=last, block_table=bt)
+        assert err.item() == B.PKV_DEVERR_CONTIG
+
+
 def test_build_indices_flags_bad_tables(B):
     dev = torch.device("cuda")
     rng = np.random.default_rng(1)
