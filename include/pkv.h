@@ -144,7 +144,8 @@ typedef struct pkv_decode_args {
     int32_t page_size;         /* power of two, 1..1024 (CSR / block table); ignored for VARLEN */
     float sm_scale;            /* softmax scale, e.g. 1/sqrt(head_dim) */
     int32_t max_seq_len;       /* host upper bound on every request's key count; sizes the split plan */
-    int32_t kv_chunk;          /* keys per split, a multiple of 64; 0 lets the library choose */
+    int32_t kv_chunk;          /* keys per split, a multiple of 64; 0 lets the library choose.  MLA: keys
+                                  per span of all requests' keys taken in order (see pkv_decode) */
     int32_t block_table_width; /* columns of block_table (BLOCK_TABLE) */
     int64_t num_slots;         /* rows of the pool(s) (VARLEN: rows of the contiguous buffer) */
     int64_t k_row_stride;      /* elements between consecutive rows of k_pool */
@@ -177,14 +178,17 @@ typedef struct pkv_decode_args {
  * with kh = h / (Hq/Hkv) for GQA and kh = 0 for MLA.  L = 0 gives out = 0,
  * lse = -inf.  Long requests are cut into splits of kv_chunk keys whose
  * partial results are combined by a log-sum-exp merge (the num_splits of the
- * FlashMLA metadata, AttentionBackend notes, "init_forward_metadata").
+ * FlashMLA metadata, AttentionBackend notes, "init_forward_metadata").  For
+ * MLA the keys of all requests, taken in request order in tiles of 64, are cut
+ * into equal spans (kv_chunk keys each, or one span per pair of SMs when
+ * kv_chunk is 0); a request that a span boundary cuts is merged the same way.
  * Arithmetic: bf16 inputs, fp32 accumulation and softmax, bf16 output rounded
  * to nearest even.
  *
  * workspace     device scratch of at least pkv_decode_workspace_size(args) bytes,
  *               256-byte aligned; its contents need no initialisation.
  * Supported:    GQA head_dim 64 or 128 with Hq/Hkv in {1,2,4,8,16};
- *               MLA head_dim_qk 576, head_dim_v 512, Hq a multiple of 64.
+ *               MLA head_dim_qk 576, head_dim_v 512, Hq a multiple of 128.
  * A page id outside the pool or a -1 inside a request's page range raises
  * PKV_DEVERR_RANGE; that key reads as zeros.  A kv_indptr range outside
  * [0, kv_indices_len], a kv_last_page_len outside [1, page_size] or a negative

@@ -7,9 +7,13 @@
 // with -1, page_size 64).  For a decode token the work per key is
 // 128 x (576 + 512) x 2 flops on 1152 bytes, close to the HBM/tensor ridge.
 //
+// Work is spread as equal spans of the concatenated key-tile sequence, one
+// span per CTA pair (see next_seg); a request cut by a span boundary is merged
+// from its split partials by a second kernel.
+//
 // The fp32 output accumulator of 128 heads x 512 dims fills all of an SM's
-// tensor memory, so a 2-CTA cluster shares each work item (request, key chunk,
-// 128-head group):
+// tensor memory, so a 2-CTA cluster shares each segment (request, 128-head
+// group, run of 64-key tiles):
 //   CTA 0 owns latent dims [0, 256): it computes the partial scores over them
 //          and accumulates output dims [0, 256);
 //   CTA 1 owns dims [256, 576): partial scores over them, output dims [256, 512).
@@ -77,7 +81,8 @@ struct Params {
     int32_t batch, hq, hgroups;
     int32_t ps_shift, ps_mask;
     float scale_log2;
-    int32_t chunk, n_chunks_max;
+    int32_t span_tiles;    // tiles per span of the concatenated tile sequence; 0: total / pairs, rounded up
+    int32_t max_len;       // keys a request may have (the caller's max_seq_len)
     int32_t bt_width;
     int32_t box_rows;
     int64_t num_slots, num_pages, kv_indices_len;
@@ -85,7 +90,8 @@ struct Params {
     const uint16_t *q;
     uint16_t *out;
     float *lse;
-    float *part_o, *part_lse;
+    float *part_o, *part_lse;  // [span][2 slots][128 heads] x (512 | 1), base-2 lse
+    int32_t *meta;             // [0]: tiles per span, [1 + v]: first tile of row v (rows + 1 entries)
     int32_t *err;
 };
 
@@ -130,7 +136,7 @@ __device__ __forceinline__ int key_count(const Params &p, int b, int64_t &base, 
         L = static_cast<int64_t>(p.cu_seqlens[b + 1]) - base;
         cap = L;
     }
-    const int64_t limit = min(cap, static_cast<int64_t>(p.chunk) * p.n_chunks_max);
+    const int64_t limit = min(cap, static_cast<int64_t>(p.max_len));
     if (L < 0 || L > limit) {
         if (report) raise_flag(p.err, L < 0 ? PKV_DEVERR_RANGE : PKV_DEVERR_CAPACITY);
         L = L < 0 ? 0 : limit;
@@ -138,60 +144,86 @@ __device__ __forceinline__ int key_count(const Params &p, int b, int64_t &base, 
     return static_cast<int>(L);
 }
 
-struct Item {
-    int b, c, hg, L, n_chunks, t_begin, t_end, n_tiles;
+// ---- work distribution ----
+// A row is one (request, 128-head group): v = b * hgroups + hg, with
+// ceil(L_b / 64) key tiles.  The rows' tiles, concatenated in row order, are cut
+// into spans of equal length (the last may be shorter); CTA pair `pair` takes
+// spans pair, pair + npairs, ...  So every pair gets the same number of tiles
+// whatever the length mix, and crosses few row boundaries.  The piece of a row
+// inside one span is a segment.  A segment holding its whole row writes the
+// final output; otherwise it is a split whose (o, lse) partial goes to slot 0
+// of its span (the segment opens the span) or slot 1 (it closes the span), and
+// the merge kernel combines a row's splits.
+struct Seg {
+    int b, hg, L, key_begin, key_end, n_tiles;
+    int part;  // -1: the whole row; else the partial's index, span * 2 + slot
     int64_t base;
 };
 
-__device__ __forceinline__ Item locate(const Params &p, const int *off, int w, bool report) {
-    Item it;
-    int lo = 0, hi = p.batch;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (off[mid] <= w) lo = mid; else hi = mid;
-    }
-    it.b = lo;
-    const int rem = w - off[lo];
-    it.hg = rem % p.hgroups;
-    it.c = rem / p.hgroups;
-    it.L = key_count(p, it.b, it.base, report && it.c == 0 && it.hg == 0);
-    it.n_chunks = max(1, (it.L + p.chunk - 1) / p.chunk);
-    it.t_begin = it.c * p.chunk;
-    it.t_end = min(it.L, it.t_begin + p.chunk);
-    it.n_tiles = it.t_end > it.t_begin ? (it.t_end - it.t_begin + kTile - 1) / kTile : 0;
-    return it;
+struct Cursor {
+    int s, t;  // current span, next tile (index into the concatenated sequence)
+};
+
+__device__ __forceinline__ int row_tiles(const Params &p, int v, bool report) {
+    int64_t base;
+    const int L = key_count(p, v / p.hgroups, base, report);
+    return (L + kTile - 1) / kTile;
 }
 
-// Item table shared by every CTA (same construction as the GQA kernels).
-__device__ __forceinline__ void build_item_table(const Params &p, int *off, int *scratch) {
+// R[v] = first tile of row v, R[V] = total tiles; every CTA builds the same table.
+__device__ __forceinline__ void build_row_table(const Params &p, int V, int *R, int *scratch, bool report) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int B = p.batch;
-    const int seg = (B + kThreads - 1) / kThreads;
-    const int lo = min(B, tid * seg), hi = min(B, lo + seg);
+    const int seg = (V + kThreads - 1) / kThreads;
+    const int lo = min(V, tid * seg), hi = min(V, lo + seg);
     int local = 0;
-    for (int b = lo; b < hi; ++b) {
-        int64_t base;
-        const int L = key_count(p, b, base, false);
-        local += max(1, (L + p.chunk - 1) / p.chunk) * p.hgroups;
-    }
+    for (int v = lo; v < hi; ++v) local += row_tiles(p, v, report && v % p.hgroups == 0);
     int incl = local;
     for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
+        const int x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
     }
     if (lane == 31) scratch[warp] = incl;
     __syncthreads();
     int wbase = 0;
     for (int w = 0; w < warp; ++w) wbase += scratch[w];
     int run = wbase + incl - local;
-    for (int b = lo; b < hi; ++b) {
-        off[b] = run;
-        int64_t base;
-        const int L = key_count(p, b, base, false);
-        run += max(1, (L + p.chunk - 1) / p.chunk) * p.hgroups;
+    for (int v = lo; v < hi; ++v) {
+        R[v] = run;
+        run += row_tiles(p, v, false);
     }
-    if (tid == kThreads - 1) off[B] = wbase + incl;
+    if (tid == kThreads - 1) R[V] = wbase + incl;
     __syncthreads();
+}
+
+// The next segment of this pair's spans (false when there is none left).
+__device__ __forceinline__ bool next_seg(const Params &p, const int *R, int V, int per, int S, int npairs, Cursor &c,
+                                         Seg &g) {
+    const int T = R[V];
+    while (c.s < S) {
+        const int s_begin = c.s * per;
+        const int s_end = min(T, s_begin + per);
+        if (c.t < s_end) {
+            int lo = 0, hi = V;  // R[lo] <= t < R[hi]: row lo holds tile t
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (R[mid] <= c.t) lo = mid; else hi = mid;
+            }
+            const int v = lo;
+            const int t1 = min(s_end, R[v + 1]);
+            g.b = v / p.hgroups;
+            g.hg = v % p.hgroups;
+            g.L = key_count(p, g.b, g.base, false);
+            g.key_begin = (c.t - R[v]) * kTile;
+            g.key_end = min(g.L, (t1 - R[v]) * kTile);
+            g.n_tiles = t1 - c.t;
+            g.part = (c.t == R[v] && t1 == R[v + 1]) ? -1 : c.s * 2 + (c.t == s_begin ? 0 : 1);
+            c.t = t1;
+            return true;
+        }
+        c.s += npairs;
+        c.t = c.s * per;
+    }
+    return false;
 }
 
 // Bounded wait (local or cluster-scope acquire) with the CTA-wide abort flag.
@@ -240,7 +272,7 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
     int *scan = reinterpret_cast<int *>(smem + kOffMisc + 16);
-    int *off = reinterpret_cast<int *>(smem + kOffTable);
+    int *R = reinterpret_cast<int *>(smem + kOffTable);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_rank();
@@ -272,14 +304,21 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
         tc05::tmem_relinquish();
     }
     if (warp == kProducerWarp && lane == 0) prefetch_tmap(&tmkv);
-    build_item_table(p, off, scan);   // contains __syncthreads
+    const int V = p.batch * p.hgroups;
+    build_row_table(p, V, R, scan, blockIdx.x == 0);   // contains __syncthreads
     tc05::fence_before_sync();
     __syncthreads();
     tc05::fence_after_sync();
     cluster_sync_all();                // the peer's barriers exist before any remote arrive
     const uint32_t tbase = *tslot;
-    const int total = off[p.batch];
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+    const int T = R[V];
+    const int per = p.span_tiles > 0 ? p.span_tiles : max(1, (T + npairs - 1) / npairs);
+    const int S = (T + per - 1) / per;
+    if (blockIdx.x == 0) {             // the merge kernel reads the plan back
+        for (int v = tid; v <= V; v += kThreads) p.meta[1 + v] = R[v];
+        if (tid == 0) p.meta[0] = per;
+    }
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer: K/V tiles
@@ -288,13 +327,14 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
         const uint32_t box_bytes = static_cast<uint32_t>(box) * 128u;
         uint32_t n = 0;
         bool ok = true;
-        for (int w = pair; w < total && ok; w += npairs) {
-            const Item it = locate(p, off, w, false);
+        Cursor cur{pair, pair * per};
+        Seg it;
+        while (ok && next_seg(p, R, V, per, S, npairs, cur, it)) {
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
                 int row = -1;
                 if (lane < nbox) {
-                    const int tb = it.t_begin + ti * kTile + lane * box;
-                    if (tb < it.t_end) {
+                    const int tb = it.key_begin + ti * kTile + lane * box;
+                    if (tb < it.key_end) {
                         if (p.layout == PKV_LAYOUT_VARLEN) {
                             row = static_cast<int>(it.base + tb);
                         } else {
@@ -337,9 +377,9 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
         const uint32_t id_qk = tc05::idesc_bf16_f32(kHeads, kTile, false, false);
         uint32_t n = 0, ic = 0;
         bool ok = true;
-        for (int w = pair; w < total && ok; w += npairs) {
-            const Item it = locate(p, off, w, false);
-            if (it.n_tiles == 0) continue;
+        Cursor cur{pair, pair * per};
+        Seg it;
+        while (ok && next_seg(p, R, V, per, S, npairs, cur, it)) {
             ok = __all_sync(0xffffffffu, wait_bar(&bars[kQFull], ic & 1, abort_flag, p.err));
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
                 const int s = n % kStages;
@@ -373,14 +413,14 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
         const uint32_t id_pv = tc05::idesc_bf16_f32(kHeads, 256, false, true);
         uint32_t n = 0, ic = 0;
         bool ok = true;
-        for (int w = pair; w < total && ok; w += npairs) {
-            const Item it = locate(p, off, w, false);
-            if (it.n_tiles == 0) continue;
+        Cursor cur{pair, pair * per};
+        Seg it;
+        while (ok && next_seg(p, R, V, per, S, npairs, cur, it)) {
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
                 ok = __all_sync(0xffffffffu, wait_bar(&bars[kPFull], n & 1, abort_flag, p.err));
                 if (!ok) break;
                 unsigned char *st = sKV + (n % kStages) * kStageBytes;
-                const int n_valid = it.t_end - (it.t_begin + ti * kTile);
+                const int n_valid = it.key_end - (it.key_begin + ti * kTile);
                 if (n_valid < kTile) {
                     // key rows past the end hold stale data: zero their value dims
                     for (int i = lane; i < (kTile - n_valid) * kVSlabs * 8; i += 32) {
@@ -436,7 +476,7 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
         // q of item `jt` over this CTA's dims (this thread's half of them) -> TMEM, once
         // the previous item's q.k MMAs are done with the region.  All global loads
         // are issued before the first TMEM store.
-        auto load_q = [&](const Item &jt, uint32_t jc) {
+        auto load_q = [&](const Seg &jt, uint32_t jc) {
             const int64_t qrow = static_cast<int64_t>(jt.b) * p.hq + jt.hg * kHeads + row;
             const uint4 *qs = reinterpret_cast<const uint4 *>(p.q + qrow * kDqk + slab0 * 64 + half * qcols * 2);
             ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kQEmpty], (jc & 1) ^ 1, abort_flag, p.err));
@@ -465,17 +505,20 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[kQFull]);
         };
+        // rows without keys: out = 0, lse = -inf
+        for (int v = pair; v < V; v += npairs) {
+            if (R[v] != R[v + 1]) continue;
+            const int64_t orow = static_cast<int64_t>(v / p.hgroups) * p.hq + (v % p.hgroups) * kHeads + row;
+            uint4 *o = reinterpret_cast<uint4 *>(p.out + orow * kDv + rank * 256 + half * 128);
+            for (int i = 0; i < 16; ++i) o[i] = make_uint4(0, 0, 0, 0);
+            if (rank == 0 && half == 0 && p.lse) p.lse[orow] = -INFINITY;
+        }
         bool q_loaded = false;
-        for (int w = pair; w < total; w += npairs) {
-            const Item it = locate(p, off, w, tid == 0 && rank == 0);
+        Cursor cs{pair, pair * per};
+        Seg it;
+        while (next_seg(p, R, V, per, S, npairs, cs, it)) {
             const int head = it.hg * kHeads + row;
             const int64_t orow = static_cast<int64_t>(it.b) * p.hq + head;
-            if (it.n_tiles == 0) {
-                uint4 *o = reinterpret_cast<uint4 *>(p.out + orow * kDv + rank * 256 + half * 128);
-                for (int i = 0; i < 16; ++i) o[i] = make_uint4(0, 0, 0, 0);
-                if (rank == 0 && half == 0 && p.lse) p.lse[orow] = -INFINITY;
-                continue;
-            }
             if (!q_loaded) load_q(it, ic);
             q_loaded = false;
             float m = -INFINITY, l = 0.f;
@@ -528,7 +571,7 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
                 ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kXFull0 + xs], (n / kXSlots) & 1, abort_flag, p.err));
                 // tile n + 1 may go out now: the peer has finished with the slot it reuses
                 if (ahead) PKV_MLA_SEND(n + 1);
-                const int n_valid = it.t_end - (it.t_begin + ti * kTile);
+                const int n_valid = it.key_end - (it.key_begin + ti * kTile);
                 // own + peer partial in half2 (the same bits in both CTAs), row max in half2
                 __half2 x2[32];
                 {
@@ -615,12 +658,12 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
 #undef PKV_MLA_FETCH
 #undef PKV_MLA_SEND
             // ---- the next item's q goes into TMEM now, so its q.k overlaps this epilogue ----
-            for (int w2 = w + npairs; w2 < total; w2 += npairs) {
-                const Item nt = locate(p, off, w2, false);
-                if (nt.n_tiles > 0) {
+            {
+                Cursor c2 = cs;
+                Seg nt;
+                if (next_seg(p, R, V, per, S, npairs, c2, nt)) {
                     load_q(nt, ic + 1);
                     q_loaded = true;
-                    break;
                 }
             }
             // ---- epilogue: normalise O and write the output (or the split partial) ----
@@ -634,8 +677,8 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
             ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kODone], ic & 1, abort_flag, p.err));
             tc05::fence_after_sync();
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            const bool single = it.n_chunks == 1;
-            const int64_t prow = (static_cast<int64_t>(it.b) * p.n_chunks_max + it.c) * p.hq + head;
+            const bool single = it.part < 0;
+            const int64_t prow = static_cast<int64_t>(it.part) * kHeads + row;
 #pragma unroll 1
             for (int cb = 0; cb < 8; cb += 4) {
                 float ov[4][16];
@@ -693,87 +736,98 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
     }
 }
 
-// Log-sum-exp merge of the chunk partials of MLA requests: one CTA per
-// (request, 16 heads); base-2 lse in the workspace.
-__global__ void __launch_bounds__(256) mla_merge_kernel(const Params p) {
-    extern __shared__ float wsm[];  // [16][n_chunks_max]
+// Log-sum-exp merge of the splits of MLA rows: one CTA per (row, 16 heads);
+// base-2 lse in the workspace.  The decode kernel left the span length and the
+// row table in meta, from which the CTA finds the spans its row crosses.
+__global__ void __launch_bounds__(256) mla_merge_kernel(const Params p, int max_splits) {
+    extern __shared__ float wsm[];  // [16][max_splits]
     __shared__ float den_s[16], mx_s[16];
-    const int b = blockIdx.x, h0 = blockIdx.y * 16;
-    int64_t base;
-    const int L = key_count(p, b, base, false);
-    const int n = (L + p.chunk - 1) / p.chunk;
-    if (n <= 1) return;
-    const int64_t rb = static_cast<int64_t>(b) * p.n_chunks_max;
+    const int v = blockIdx.x, h0 = blockIdx.y * 16;
+    const int per = p.meta[0];
+    const int r0 = p.meta[1 + v], r1 = p.meta[2 + v];
+    if (r1 <= r0 || per < 1) return;
+    const int s_first = r0 / per, s_last = (r1 - 1) / per;
+    const int n = s_last - s_first + 1;
+    if (n <= 1) return;  // the row sat inside one span: the decode kernel wrote it
+    if (n > max_splits) {
+        if (threadIdx.x == 0 && blockIdx.y == 0) raise_flag(p.err, PKV_DEVERR_CAPACITY);
+        return;
+    }
+    // split i of the row is slot 1 of its span when it does not open the span
+    auto part = [&](int i) -> int64_t {
+        const int s = s_first + i;
+        return static_cast<int64_t>(s) * 2 + ((i == 0 && r0 != s * per) ? 1 : 0);
+    };
     for (int i = threadIdx.x; i < 16 * n; i += blockDim.x) {
         const int h = i / n, c = i % n;
-        wsm[h * p.n_chunks_max + c] = p.part_lse[(rb + c) * p.hq + h0 + h];
+        wsm[h * max_splits + c] = p.part_lse[part(c) * kHeads + h0 + h];
     }
     __syncthreads();
     if (threadIdx.x < 16) {
         const int h = threadIdx.x;
         float M = -INFINITY;
-        for (int c = 0; c < n; ++c) M = fmaxf(M, wsm[h * p.n_chunks_max + c]);
+        for (int c = 0; c < n; ++c) M = fmaxf(M, wsm[h * max_splits + c]);
         float den = 0.f;
         for (int c = 0; c < n; ++c) {
-            const float wgt = ex2(wsm[h * p.n_chunks_max + c] - M);
-            wsm[h * p.n_chunks_max + c] = wgt;
+            const float wgt = ex2(wsm[h * max_splits + c] - M);
+            wsm[h * max_splits + c] = wgt;
             den += wgt;
         }
         den_s[h] = den;
         mx_s[h] = M;
     }
     __syncthreads();
+    const int64_t orow0 = static_cast<int64_t>(v / p.hgroups) * p.hq + (v % p.hgroups) * kHeads + h0;
     for (int i = threadIdx.x; i < 16 * (kDv / 4); i += blockDim.x) {
         const int h = i / (kDv / 4), d4 = i % (kDv / 4);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int c = 0; c < n; ++c) {
-            const float wgt = wsm[h * p.n_chunks_max + c];
-            const float4 v = reinterpret_cast<const float4 *>(p.part_o + ((rb + c) * p.hq + h0 + h) * kDv)[d4];
-            acc.x = fmaf(wgt, v.x, acc.x);
-            acc.y = fmaf(wgt, v.y, acc.y);
-            acc.z = fmaf(wgt, v.z, acc.z);
-            acc.w = fmaf(wgt, v.w, acc.w);
+            const float wgt = wsm[h * max_splits + c];
+            const float4 x = reinterpret_cast<const float4 *>(p.part_o + (part(c) * kHeads + h0 + h) * kDv)[d4];
+            acc.x = fmaf(wgt, x.x, acc.x);
+            acc.y = fmaf(wgt, x.y, acc.y);
+            acc.z = fmaf(wgt, x.z, acc.z);
+            acc.w = fmaf(wgt, x.w, acc.w);
         }
         const float inv = 1.f / den_s[h];
         uint2 o;
         o.x = pack_bf16x2(acc.x * inv, acc.y * inv);
         o.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-        reinterpret_cast<uint2 *>(p.out + (static_cast<int64_t>(b) * p.hq + h0 + h) * kDv)[d4] = o;
-        if (d4 == 0 && p.lse) p.lse[static_cast<int64_t>(b) * p.hq + h0 + h] = (mx_s[h] + log2f(den_s[h])) * kLn2;
+        reinterpret_cast<uint2 *>(p.out + (orow0 + h) * kDv)[d4] = o;
+        if (d4 == 0 && p.lse) p.lse[orow0 + h] = (mx_s[h] + log2f(den_s[h])) * kLn2;
     }
 }
 
 // ------------------------------------------------------------------ host side
 struct Plan {
-    int chunk, n_chunks_max, hgroups;
-    size_t part_o_bytes, part_lse_bytes;
+    int hgroups, span_tiles, max_spans, max_splits;
+    size_t part_o_bytes, part_lse_bytes, meta_bytes;
 };
 
-static void make_plan(const pkv_decode_args *a, Plan &pl) {
+// Spans: kv_chunk / 64 tiles each when the caller fixes kv_chunk, else one span
+// per CTA pair (at most one pair per two SMs).  Each span holds at most two
+// partials.
+static bool make_plan(const pkv_decode_args *a, Plan &pl) {
     pl.hgroups = a->num_q_heads / kHeads;
+    const int64_t rows = static_cast<int64_t>(a->batch) * pl.hgroups;
+    const int64_t tiles_max = (static_cast<int64_t>(std::max(0, a->max_seq_len)) + kTile - 1) / kTile;
+    if (rows * tiles_max > INT32_MAX / 4) return false;
+    int64_t spans;
     if (a->kv_chunk > 0) {
-        pl.chunk = a->kv_chunk;
+        pl.span_tiles = a->kv_chunk / kTile;
+        spans = std::max<int64_t>(1, (rows * tiles_max + pl.span_tiles - 1) / pl.span_tiles);
     } else {
-        // ~4 items per CTA pair when requests average half of max_seq_len
-        const int64_t pairs = std::max(1, sm_count() / 2);
-        const int64_t L = std::max<int64_t>(1, a->max_seq_len);
-        pl.chunk = kTile;
-        for (int c = 4096; c >= kTile; c >>= 1) {
-            const int64_t items = static_cast<int64_t>(a->batch) * pl.hgroups * ((L + c - 1) / c);
-            if (items / 2 >= 4 * pairs) {
-                pl.chunk = c;
-                break;
-            }
-        }
+        pl.span_tiles = 0;
+        spans = std::max(1, sm_count() / 2);
     }
-    pl.n_chunks_max = std::max(1, (a->max_seq_len + pl.chunk - 1) / pl.chunk);
-    if (pl.n_chunks_max == 1) {
-        pl.part_o_bytes = pl.part_lse_bytes = 0;
-    } else {
-        const int64_t rows = static_cast<int64_t>(a->batch) * pl.n_chunks_max * a->num_q_heads;
-        pl.part_o_bytes = (static_cast<size_t>(rows) * kDv * 4 + 255) / 256 * 256;
-        pl.part_lse_bytes = (static_cast<size_t>(rows) * 4 + 255) / 256 * 256;
-    }
+    if (spans > INT32_MAX / 4) return false;
+    pl.max_spans = static_cast<int>(spans);
+    const int64_t per_min = std::max(1, pl.span_tiles);
+    pl.max_splits = static_cast<int>(std::min<int64_t>(spans, (tiles_max + per_min - 1) / per_min + 1));
+    pl.part_o_bytes = (static_cast<size_t>(spans) * 2 * kHeads * kDv * 4 + 255) / 256 * 256;
+    pl.part_lse_bytes = (static_cast<size_t>(spans) * 2 * kHeads * 4 + 255) / 256 * 256;
+    pl.meta_bytes = (static_cast<size_t>(rows + 2) * 4 + 255) / 256 * 256;
+    return true;
 }
 
 pkv_status validate(const pkv_decode_args *a, bool check_ptrs) {
@@ -816,20 +870,19 @@ pkv_status validate(const pkv_decode_args *a, bool check_ptrs) {
 
 size_t workspace_size(const pkv_decode_args *a) {
     Plan pl;
-    make_plan(a, pl);
-    return pl.part_o_bytes + pl.part_lse_bytes;
+    if (a->batch == 0 || !make_plan(a, pl)) return 0;
+    return pl.part_o_bytes + pl.part_lse_bytes + pl.meta_bytes;
 }
 
 pkv_status launch(const pkv_decode_args *a, void *ws, size_t ws_bytes, int32_t *err, cudaStream_t s) {
     Plan pl;
-    make_plan(a, pl);
-    if (ws_bytes < pl.part_o_bytes + pl.part_lse_bytes)
-        return fail(PKV_ERR_CAPACITY, "pkv_decode(MLA): workspace of %zu bytes, %zu needed", ws_bytes,
-                    pl.part_o_bytes + pl.part_lse_bytes);
-    if (pl.part_o_bytes && (!ws || !aligned(ws, 256)))
+    if (!make_plan(a, pl)) return fail(PKV_ERR_UNSUPPORTED, "pkv_decode(MLA): batch x max_seq_len too large");
+    const size_t need = pl.part_o_bytes + pl.part_lse_bytes + pl.meta_bytes;
+    if (ws_bytes < need) return fail(PKV_ERR_CAPACITY, "pkv_decode(MLA): workspace of %zu bytes, %zu needed", ws_bytes, need);
+    if (!ws || !aligned(ws, 256))
         return fail(PKV_ERR_INVALID_ARG, "pkv_decode(MLA): workspace must be non-null and 256-byte aligned");
-    if (static_cast<int64_t>(pl.chunk) * pl.n_chunks_max > INT32_MAX / 2)
-        return fail(PKV_ERR_UNSUPPORTED, "pkv_decode(MLA): max_seq_len too large");
+    const size_t msmem = static_cast<size_t>(16) * pl.max_splits * 4;
+    if (msmem > 200 * 1024) return fail(PKV_ERR_UNSUPPORTED, "pkv_decode(MLA): too many splits for the merge");
     Params p{};
     p.layout = a->layout;
     p.batch = a->batch;
@@ -839,8 +892,8 @@ pkv_status launch(const pkv_decode_args *a, void *ws, size_t ws_bytes, int32_t *
     p.ps_shift = ilog2(ps);
     p.ps_mask = ps - 1;
     p.scale_log2 = a->sm_scale * kLog2e;
-    p.chunk = pl.chunk;
-    p.n_chunks_max = pl.n_chunks_max;
+    p.span_tiles = pl.span_tiles;
+    p.max_len = a->max_seq_len;
     p.bt_width = a->block_table_width;
     p.box_rows = std::min(ps, kTile);
     p.num_slots = a->num_slots;
@@ -857,6 +910,7 @@ pkv_status launch(const pkv_decode_args *a, void *ws, size_t ws_bytes, int32_t *
     p.lse = a->lse;
     p.part_o = static_cast<float *>(ws);
     p.part_lse = reinterpret_cast<float *>(static_cast<char *>(ws) + pl.part_o_bytes);
+    p.meta = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + pl.part_o_bytes + pl.part_lse_bytes);
     p.err = err;
     if (a->layout == PKV_LAYOUT_VARLEN) p.ps_shift = 0, p.ps_mask = 0;
 
@@ -870,7 +924,7 @@ pkv_status launch(const pkv_decode_args *a, void *ws, size_t ws_bytes, int32_t *
 
     static size_t lim = 0;
     static int max_pairs = 0;
-    const size_t smem = kFixedSmem + (static_cast<size_t>(a->batch) + 1) * 4;
+    const size_t smem = kFixedSmem + (static_cast<size_t>(a->batch) * pl.hgroups + 1) * 4;
     if (!lim) {
         int optin = 0, dev = 0;
         cudaFuncAttributes fa{};
@@ -895,18 +949,15 @@ pkv_status launch(const pkv_decode_args *a, void *ws, size_t ws_bytes, int32_t *
             n = std::max(1, sm_count() / 2);
         max_pairs = n;
     }
-    const int64_t items_upper = static_cast<int64_t>(a->batch) * pl.hgroups * pl.n_chunks_max;
-    const int pairs = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(items_upper, max_pairs)));
+    const int pairs = std::max(1, std::min(max_pairs, pl.max_spans));
     mla_decode_kernel<<<2 * pairs, kThreads, smem, s>>>(p, tmkv);
     pkv_status st = check_launch("pkv_decode(MLA split kernel)");
-    if (st != PKV_OK || pl.n_chunks_max == 1) return st;
-    const size_t msmem = static_cast<size_t>(16) * pl.n_chunks_max * 4;
-    if (msmem > 200 * 1024) return fail(PKV_ERR_UNSUPPORTED, "pkv_decode(MLA): too many splits for the merge");
+    if (st != PKV_OK) return st;
     if (msmem > 48 * 1024 &&
         cudaFuncSetAttribute(mla_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(msmem)) !=
             cudaSuccess)
         return fail(PKV_ERR_CUDA, "pkv_decode(MLA): cannot raise the merge shared-memory limit");
-    mla_merge_kernel<<<dim3(a->batch, a->num_q_heads / 16), 256, msmem, s>>>(p);
+    mla_merge_kernel<<<dim3(a->batch * pl.hgroups, kHeads / 16), 256, msmem, s>>>(p, pl.max_splits);
     return check_launch("pkv_decode(MLA merge kernel)");
 }
 
