@@ -47,33 +47,35 @@ namespace pkv {
 namespace mla {
 
 constexpr int kDqk = 576, kDv = 512, kHeads = 128, kTile = 64;
-constexpr int kVSlabs = 4;                 // 256 value dims per CTA
-constexpr int kMaxSlabs = 5;               // q.k slabs of the wider CTA
+constexpr int kVSlabs = 4;                 // 256 value dims per CTA: four 64-dim slabs
 constexpr int kStages = 4;
-constexpr int kSoftmaxWarps = 8;           // two threads per head row: keys 0-31 (warps 0-3), 32-63 (warps 4-7)
-constexpr int kThreads = 352;              // warps 0-7 softmax, 8 producer, 9 q.k MMAs, 10 P.V MMAs
-constexpr int kProducerWarp = 8, kMmaWarp = 9, kPvWarp = 10;
+constexpr int kSoftmaxWarps = 16;          // four threads per head row: keys 16 qt .. 16 qt + 15 in warps 4 qt .. 4 qt + 3
+constexpr int kThreads = 608;              // warps 0-15 softmax, 16 producer, 17 q.k MMAs, 18 P.V MMAs
+constexpr int kProducerWarp = 16, kMmaWarp = 17, kPvWarp = 18;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;              // 64-column score tile
-constexpr uint32_t kColO = 64;             // 256-column output accumulator
-constexpr uint32_t kColQ = 320;            // q of this CTA's dims as the MMA A operand (<= 160 columns)
-constexpr uint32_t kColP = 480;            // P (bf16 probabilities) as the A operand of P V (32 columns)
+constexpr uint32_t kColS = 0;              // two 64-column score tiles
+constexpr uint32_t kColO = 128;            // 256-column output accumulator
+constexpr uint32_t kColQ = 384;            // q over this CTA's first 128 dims, the MMA A operand (64 columns)
+constexpr uint32_t kColP = 448;            // P (bf16 probabilities), A operand of P V: two buffers of 32 columns
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kLog2e = 1.44269504088896341f;
 constexpr float kLazy = 8.f;
 
 // shared-memory carve-up (bytes from a 1024-aligned base)
-constexpr int kSlabBytes = kTile * 128;                     // 8 KB: 64 keys x 64 dims
-constexpr int kStageBytes = kMaxSlabs * kSlabBytes;         // 40 KB
+constexpr int kSlabBytes = kTile * 128;                     // 8 KB: 64 keys x 64 dims, 128-byte swizzle
+constexpr int kRopeBytes = kTile * 64;                      // 4 KB: 64 keys x 32 rope dims, 64-byte swizzle
+constexpr int kStageBytes = kVSlabs * kSlabBytes + kRopeBytes;   // 36 KB
 constexpr int kOffKV = 0;
 constexpr int kXBytes = kHeads * kTile * 2;                // one tile of peer partial scores, fp16
-constexpr int kXSlots = 3;
+constexpr int kXSlots = 2;
 constexpr int kOffX = kOffKV + kStages * kStageBytes;       // kXSlots slots, each [8 chunks][128 heads] x 16 B
-constexpr int kOffBar = kOffX + kXSlots * kXBytes;
+constexpr int kOffQ = kOffX + kXSlots * kXBytes;            // q over the CTA's dims 128-255: two SW128 slabs
+constexpr int kOffQr = kOffQ + 2 * kHeads * 128;            // q over the CTA's 32 rope dims, 64-byte swizzle
+constexpr int kOffBar = kOffQr + kHeads * 64;
 constexpr int kNumBars = 24;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;            // tmem slot, abort flag, scan scratch
-constexpr int kOffRed = kOffMisc + 64;                      // row-max / row-sum exchange of the two half rows
-constexpr int kOffTable = kOffRed + 2 * 2 * kHeads * 4;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;            // tmem slot, abort flag, scan scratch (one int per warp)
+constexpr int kOffRed = kOffMisc + 128;                     // row-max / row-sum exchange of a row's four threads
+constexpr int kOffTable = kOffRed + 2 * 4 * kHeads * 4;
 constexpr int kFixedSmem = kOffTable + 1024;                // + item table + alignment slack
 
 struct Params {
@@ -230,8 +232,8 @@ __device__ __forceinline__ bool next_seg(const Params &p, const int *R, int V, i
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int32_t *err,
                                          bool cluster_scope = false) {
     auto poll = [&]() { return cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
-    if (*abort_flag) return false;
     if (poll()) return true;
+    if (*abort_flag) return false;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
         if (poll()) return true;
@@ -246,6 +248,13 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
     }
 }
 
+// Warp-wide bounded wait (every lane polls; measured faster than one polling lane
+// with the others parked).  `ok` is warp-uniform; so is the result.
+__device__ __forceinline__ bool warp_wait(bool ok, uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          int32_t *err, bool cluster_scope = false) {
+    return __all_sync(0xffffffffu, ok && wait_bar(bar, parity, abort_flag, err, cluster_scope));
+}
+
 // Bounded wait that ignores the abort flag: used only to drain work this CTA
 // itself started (MMAs, TMA copies) before its TMEM and shared memory go away.
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
@@ -257,17 +266,21 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
 }
 
 enum Bar {
-    kQFull = 0, kQEmpty, kKvFull0, kKvEmpty0 = kKvFull0 + kStages, kSFull = kKvEmpty0 + kStages, kSFree, kPFull,
-    kPFree, kXFull0, kODone = kXFull0 + kXSlots, kOFree, kFinal, kFinalPv, kBarCount
+    kQFull = 0, kQEmpty, kKvFull0, kKvEmpty0 = kKvFull0 + kStages, kSFull0 = kKvEmpty0 + kStages, kSFree0 = kSFull0 + 2,
+    kPFull0 = kSFree0 + 2, kPFree0 = kPFull0 + 2, kXFull0 = kPFree0 + 2, kODone = kXFull0 + kXSlots, kOFree,
+    kFinal, kFinalPv, kBarCount
 };
 static_assert(kBarCount <= kNumBars, "barrier slots");
+static_assert(16 + 4 * (kThreads / 32) <= kOffRed - kOffMisc, "scan scratch");
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
+mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, const __grid_constant__ CUtensorMap tmrope) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     unsigned char *sKV = smem + kOffKV;
     float *sX = reinterpret_cast<float *>(smem + kOffX);
+    unsigned char *sQ = smem + kOffQ;
+    unsigned char *sQr = smem + kOffQr;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
@@ -277,8 +290,8 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_rank();
     const uint32_t peer = rank ^ 1u;
-    const int nslab = rank == 0 ? 4 : 5;        // q.k slabs owned by this CTA
-    const int slab0 = rank == 0 ? 0 : 4;        // first 64-dim slab of the latent row
+    const int slab0 = 4 * static_cast<int>(rank);   // first 64-dim slab of the latent row owned by this CTA
+    const int rope0 = 512 + 32 * static_cast<int>(rank);   // first of the CTA's 32 rope dims
 
     if (tid == 0) {
         *abort_flag = 0;
@@ -288,10 +301,14 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
             mbar_init(&bars[kKvFull0 + s], 1);
             mbar_init(&bars[kKvEmpty0 + s], 1);
         }
-        mbar_init(&bars[kSFull], 1);
-        mbar_init(&bars[kSFree], kSoftmaxWarps);
-        mbar_init(&bars[kPFull], kSoftmaxWarps);
-        mbar_init(&bars[kPFree], 1);
+        for (int b2 = 0; b2 < 2; ++b2) {
+            mbar_init(&bars[kSFull0 + b2], 1);
+            mbar_init(&bars[kSFree0 + b2], kSoftmaxWarps);
+        }
+        for (int b2 = 0; b2 < 2; ++b2) {
+            mbar_init(&bars[kPFull0 + b2], kSoftmaxWarps);
+            mbar_init(&bars[kPFree0 + b2], 1);
+        }
         for (int x = 0; x < kXSlots; ++x) mbar_init(&bars[kXFull0 + x], 1);  // own expect_tx arrive + peer bytes
         mbar_init(&bars[kODone], 1);
         mbar_init(&bars[kOFree], kSoftmaxWarps);
@@ -303,7 +320,10 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
         tc05::tmem_alloc(tslot, kTmemCols);
         tc05::tmem_relinquish();
     }
-    if (warp == kProducerWarp && lane == 0) prefetch_tmap(&tmkv);
+    if (warp == kProducerWarp && lane == 0) {
+        prefetch_tmap(&tmkv);
+        prefetch_tmap(&tmrope);
+    }
     const int V = p.batch * p.hgroups;
     build_row_table(p, V, R, scan, blockIdx.x == 0);   // contains __syncthreads
     tc05::fence_before_sync();
@@ -322,44 +342,57 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer: K/V tiles
+        // Lane j < 64 / box handles box j of a tile: one page lookup, then the CTA's
+        // four 64-dim slabs and its 32 rope dims of those rows.  Tiles kPrefetch
+        // ahead of the one being loaded are first pulled into L2, so a stage's own
+        // loads (issued once the stage is free) wait on L2 rather than on HBM.
         const int box = p.box_rows;
         const int nbox = kTile / box;
         const uint32_t box_bytes = static_cast<uint32_t>(box) * 128u;
+        constexpr int kPrefetch = 3;
         uint32_t n = 0;
         bool ok = true;
         Cursor cur{pair, pair * per};
         Seg it;
+        // pool row of this lane's box of tile ti (-1: past the end, -2: bad page id)
+        auto box_row = [&](int ti, bool report) -> int {
+            if (lane >= nbox) return -1;
+            const int tb = it.key_begin + ti * kTile + lane * box;
+            if (tb >= it.key_end) return -1;
+            if (p.layout == PKV_LAYOUT_VARLEN) return static_cast<int>(it.base + tb);
+            const int32_t *tab = p.layout == PKV_LAYOUT_CSR ? p.kv_indices : p.block_table;
+            const int page = __ldg(tab + it.base + (tb >> p.ps_shift));
+            if (page < 0 || page >= p.num_pages) {
+                if (report) raise_flag(p.err, PKV_DEVERR_RANGE);
+                return -2;
+            }
+            return static_cast<int>((static_cast<int64_t>(page) << p.ps_shift) + (tb & p.ps_mask));
+        };
+        auto prefetch = [&](int ti) {
+            const int r = box_row(ti, false);
+            if (r >= 0) {
+                tma_prefetch_2d(&tmrope, rope0, r);
+                for (int sl = 0; sl < kVSlabs; ++sl) tma_prefetch_2d(&tmkv, (slab0 + sl) * 64, r);
+            }
+        };
         while (ok && next_seg(p, R, V, per, S, npairs, cur, it)) {
+            for (int ti = 0; ti < kPrefetch && ti < it.n_tiles; ++ti) prefetch(ti);
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
-                int row = -1;
-                if (lane < nbox) {
-                    const int tb = it.key_begin + ti * kTile + lane * box;
-                    if (tb < it.key_end) {
-                        if (p.layout == PKV_LAYOUT_VARLEN) {
-                            row = static_cast<int>(it.base + tb);
-                        } else {
-                            const int32_t *tab = p.layout == PKV_LAYOUT_CSR ? p.kv_indices : p.block_table;
-                            const int page = __ldg(tab + it.base + (tb >> p.ps_shift));
-                            if (page < 0 || page >= p.num_pages) {
-                                raise_flag(p.err, PKV_DEVERR_RANGE);
-                                row = -2;
-                            } else {
-                                row = static_cast<int>((static_cast<int64_t>(page) << p.ps_shift) + (tb & p.ps_mask));
-                            }
-                        }
-                    }
-                }
+                if (ti + kPrefetch < it.n_tiles) prefetch(ti + kPrefetch);
+                const int row = box_row(ti, true);
                 const int s = n % kStages;
                 if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) break;
                 const uint32_t valid = __ballot_sync(0xffffffffu, row >= 0);
                 if (lane == 0)
-                    mbar_arrive_expect_tx(&bars[kKvFull0 + s], __popc(valid) * box_bytes * static_cast<uint32_t>(nslab));
+                    mbar_arrive_expect_tx(&bars[kKvFull0 + s], __popc(valid) * static_cast<uint32_t>(box) *
+                                                                   static_cast<uint32_t>(kVSlabs * 128 + 64));
                 __syncwarp();
                 if (row >= 0) {
                     unsigned char *st = sKV + s * kStageBytes;
-                    for (int sl = 0; sl < nslab; ++sl)
+                    tma_load_2d(st + kVSlabs * kSlabBytes + lane * box * 64, &tmrope, rope0, row, &bars[kKvFull0 + s]);
+                    for (int sl = 0; sl < kVSlabs; ++sl)
                         tma_load_2d(st + sl * kSlabBytes + lane * box_bytes, &tmkv, (slab0 + sl) * 64, row,
                                     &bars[kKvFull0 + s]);
                 }
@@ -372,30 +405,48 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ q.k MMAs (one thread)
-        // S(n) = Q K(n)^T as soon as the score tile is free (the softmax warps have
-        // read S(n-1)) and K/V tile n has landed; never waits for P V.
+        // S(n) = Q K(n)^T into score buffer n % 2 as soon as it is free (the softmax
+        // warps have read S(n - 2)) and K/V tile n has landed; never waits for P V.
+        // q over the CTA's dims 0-127 comes from TMEM, dims 128-255 and the 32 rope
+        // dims from shared memory.
         const uint32_t id_qk = tc05::idesc_bf16_f32(kHeads, kTile, false, false);
         uint32_t n = 0, ic = 0;
         bool ok = true;
         Cursor cur{pair, pair * per};
         Seg it;
         while (ok && next_seg(p, R, V, per, S, npairs, cur, it)) {
-            ok = __all_sync(0xffffffffu, wait_bar(&bars[kQFull], ic & 1, abort_flag, p.err));
+            ok = warp_wait(ok, &bars[kQFull], ic & 1, abort_flag, p.err);
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
                 const int s = n % kStages;
-                ok = __all_sync(0xffffffffu, wait_bar(&bars[kKvFull0 + s], (n / kStages) & 1, abort_flag, p.err) &&
-                                                 wait_bar(&bars[kSFree], (n & 1) ^ 1, abort_flag, p.err));
+                ok = warp_wait(ok, &bars[kKvFull0 + s], (n / kStages) & 1, abort_flag, p.err);
+                ok = warp_wait(ok, &bars[kSFree0 + (n & 1)], ((n >> 1) & 1) ^ 1, abort_flag, p.err);
                 if (!ok) break;
                 tc05::fence_after_sync();
                 if (lane == 0) {
+                    const uint32_t d = tbase + kColS + (n & 1) * kTile;
                     const uint64_t kdesc = tc05::smem_desc(sKV + s * kStageBytes, 16, 1024);
-                    for (int sl = 0; sl < nslab; ++sl)
+                    const uint64_t qdesc = tc05::smem_desc(sQ, 16, 1024);
+#pragma unroll
+                    for (int sl = 0; sl < 2; ++sl)
 #pragma unroll
                         for (int k = 0; k < 4; ++k)   // slab: +8 KB, k-step: +32 bytes (16 dims) / +8 TMEM columns
-                            tc05::mma_ts(tbase + kColS, tbase + kColQ + sl * 32 + k * 8,
+                            tc05::mma_ts(d, tbase + kColQ + sl * 32 + k * 8,
                                          kdesc + static_cast<uint64_t>((sl * kSlabBytes + k * 32) >> 4), id_qk,
                                          (sl | k) ? 1u : 0u);
-                    tc05::commit(&bars[kSFull]);
+#pragma unroll
+                    for (int sl = 2; sl < 4; ++sl)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)   // q slab: +16 KB (128 rows)
+                            tc05::mma_ss(d, qdesc + static_cast<uint64_t>(((sl - 2) * kHeads * 128 + k * 32) >> 4),
+                                         kdesc + static_cast<uint64_t>((sl * kSlabBytes + k * 32) >> 4), id_qk, 1u);
+                    // the rope dims: 64-byte rows, 64-byte swizzle (layout type 4), 8-row groups 512 bytes apart
+                    const uint64_t rq = tc05::smem_desc(sQr, 16, 512, 4);
+                    const uint64_t rk = tc05::smem_desc(sKV + s * kStageBytes + kVSlabs * kSlabBytes, 16, 512, 4);
+#pragma unroll
+                    for (int k = 0; k < 2; ++k)
+                        tc05::mma_ss(d, rq + static_cast<uint64_t>((k * 32) >> 4), rk + static_cast<uint64_t>((k * 32) >> 4),
+                                     id_qk, 1u);
+                    tc05::commit(&bars[kSFull0 + (n & 1)]);
                     if (ti == it.n_tiles - 1) tc05::commit(&bars[kQEmpty]);
                 }
                 __syncwarp();
@@ -417,7 +468,7 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
         Seg it;
         while (ok && next_seg(p, R, V, per, S, npairs, cur, it)) {
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
-                ok = __all_sync(0xffffffffu, wait_bar(&bars[kPFull], n & 1, abort_flag, p.err));
+                ok = warp_wait(ok, &bars[kPFull0 + (n & 1)], (n >> 1) & 1, abort_flag, p.err);
                 if (!ok) break;
                 unsigned char *st = sKV + (n % kStages) * kStageBytes;
                 const int n_valid = it.key_end - (it.key_begin + ti * kTile);
@@ -431,16 +482,17 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
-                if (ti == 0) ok = __all_sync(0xffffffffu, wait_bar(&bars[kOFree], (ic & 1) ^ 1, abort_flag, p.err));
+                if (ti == 0) ok = warp_wait(ok, &bars[kOFree], (ic & 1) ^ 1, abort_flag, p.err);
                 if (!ok) break;
                 tc05::fence_after_sync();
                 if (lane == 0) {
                     const uint64_t vdesc = tc05::smem_desc(st, kSlabBytes, 1024);
 #pragma unroll
                     for (int k = 0; k < kTile / 16; ++k)   // 16 keys per MMA: +2048 bytes of V rows, +8 columns of P
-                        tc05::mma_ts(tbase + kColO, tbase + kColP + k * 8, vdesc + static_cast<uint64_t>(k * 2048 >> 4),
+                        tc05::mma_ts(tbase + kColO, tbase + kColP + (n & 1) * 32 + k * 8,
+                                     vdesc + static_cast<uint64_t>(k * 2048 >> 4),
                                      id_pv, (ti == 0 && k == 0) ? 0u : 1u);
-                    tc05::commit(&bars[kPFree]);
+                    tc05::commit(&bars[kPFree0 + (n & 1)]);
                     tc05::commit(&bars[kKvEmpty0 + n % kStages]);
                     if (ti == it.n_tiles - 1) tc05::commit(&bars[kODone]);
                 }
@@ -455,51 +507,58 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax warps
-        // Thread (row, half) owns head `row` (TMEM lane) and keys [32 half, 32 half + 32)
-        // of every tile, value columns [128 half, +128) of O and half of q.
+        // Thread (row, qt) owns head `row` (TMEM lane) and, of every tile, keys
+        // [16 qt, 16 qt + 16); of O the value columns [64 qt, +64); of q a quarter of
+        // each of its three parts.  The four threads of a row sit in warps
+        // (row / 32) + 4 qt and combine their row maxima and sums through shared
+        // memory and a 128-thread named barrier.
         const int row = (warp & 3) * 32 + lane;
-        const int half = warp >> 2;
+        const int qt = warp >> 2;
         // The softmax warps run one tile ahead: in the iteration of tile n they load
-        // S(n + 1), wait for the peer's partial of tile n, send their own partial of
-        // tile n + 1, then do tile n's softmax, so the exchange of n + 1 overlaps
-        // the math of n on both CTAs.  Tile t travels in slot t % 3 of the
-        // receiver's buffer; a CTA sends tile n + 1 only after it received the
-        // peer's tile n, which the peer sends only after it finished reading tile
-        // n - 2 (the slot reused): no explicit release is needed.
+        // S(n + 1), wait for and read the peer's partial of tile n, send their own
+        // partial of tile n + 1, then do tile n's softmax, so the exchange of n + 1
+        // overlaps the math of n on both CTAs.  Tile t travels in slot t % 2 of the
+        // receiver's buffer.  The peer writes tile t only after it has received our
+        // tile t - 1, which we send only after reading tile t - 2 out of the same
+        // slot (program order; the complete_tx of st.async has release semantics at
+        // cluster scope, the peer's wait on it acquire), so no release message is
+        // needed.
         const uint32_t x_peer = mapa(smem_u32(sX), peer);
         const uint32_t xf_peer0 = mapa(smem_u32(&bars[kXFull0]), peer);
-        float *red = reinterpret_cast<float *>(smem + kOffRed);   // [2 buffers][2 halves][128 rows]
+        float *red = reinterpret_cast<float *>(smem + kOffRed);   // [2 buffers][4 quarters][128 rows]
         const uint32_t trow = tc05::taddr(tbase, (warp & 3) * 32, 0);
-        const int qcols = nslab * 16;                              // TMEM columns of q per half row
+        const int row_bar = 2 + (warp & 3);                       // named barrier of the row's four warps
         uint32_t n = 0, ic = 0;
         bool ok = true;
-        // q of item `jt` over this CTA's dims (this thread's half of them) -> TMEM, once
-        // the previous item's q.k MMAs are done with the region.  All global loads
-        // are issued before the first TMEM store.
+        // q of segment `jt` -> TMEM (the CTA's dims 0-127: 32 per thread), the two
+        // SW128 slabs (dims 128-255: 32 per thread) and the SW64 rope rows (8 per
+        // thread), once the previous segment's q.k MMAs are done with them.
         auto load_q = [&](const Seg &jt, uint32_t jc) {
             const int64_t qrow = static_cast<int64_t>(jt.b) * p.hq + jt.hg * kHeads + row;
-            const uint4 *qs = reinterpret_cast<const uint4 *>(p.q + qrow * kDqk + slab0 * 64 + half * qcols * 2);
-            ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kQEmpty], (jc & 1) ^ 1, abort_flag, p.err));
+            const uint16_t *qb = p.q + qrow * kDqk;
+            const uint4 *qt4 = reinterpret_cast<const uint4 *>(qb + slab0 * 64 + qt * 32);
+            const uint4 *qs4 = reinterpret_cast<const uint4 *>(qb + slab0 * 64 + 128 + qt * 32);
+            const uint4 *qr4 = reinterpret_cast<const uint4 *>(qb + rope0 + qt * 8);
+            ok = warp_wait(ok, &bars[kQEmpty], (jc & 1) ^ 1, abort_flag, p.err);
             tc05::fence_after_sync();
-            // two batches (3 + 2 chunks of 16 columns = 32 bf16); each batch's global
-            // loads are all in flight before its TMEM stores
+            uint4 qv[9];
 #pragma unroll
-            for (int b0 = 0; b0 < 5; b0 += 3) {
-                uint4 qv[12];
+            for (int i = 0; i < 4; ++i) qv[i] = __ldg(qt4 + i);
 #pragma unroll
-                for (int i = 0; i < 12; ++i)
-                    if (b0 * 4 + i < qcols / 4 && i < (5 - b0) * 4) qv[i] = __ldg(qs + b0 * 4 + i);
-#pragma unroll
-                for (int cc = 0; cc < 3; ++cc) {
-                    if (ok && b0 + cc < qcols / 16 && cc < 5 - b0) {
-                        const uint32_t w[16] = {qv[4 * cc].x,     qv[4 * cc].y,     qv[4 * cc].z,     qv[4 * cc].w,
-                                                qv[4 * cc + 1].x, qv[4 * cc + 1].y, qv[4 * cc + 1].z, qv[4 * cc + 1].w,
-                                                qv[4 * cc + 2].x, qv[4 * cc + 2].y, qv[4 * cc + 2].z, qv[4 * cc + 2].w,
-                                                qv[4 * cc + 3].x, qv[4 * cc + 3].y, qv[4 * cc + 3].z, qv[4 * cc + 3].w};
-                        tc05::st_x16_u32(trow + kColQ + half * qcols + (b0 + cc) * 16, w);
-                    }
-                }
+            for (int i = 0; i < 4; ++i) qv[4 + i] = __ldg(qs4 + i);
+            qv[8] = __ldg(qr4);
+            if (ok) {
+                const uint32_t w[16] = {qv[0].x, qv[0].y, qv[0].z, qv[0].w, qv[1].x, qv[1].y, qv[1].z, qv[1].w,
+                                        qv[2].x, qv[2].y, qv[2].z, qv[2].w, qv[3].x, qv[3].y, qv[3].z, qv[3].w};
+                tc05::st_x16_u32(trow + kColQ + qt * 16, w);
             }
+            // slab qt / 2, 16-byte chunks 4 (qt % 2) + i of the row at chunk ^ (row & 7)
+            unsigned char *slab = sQ + (qt >> 1) * kHeads * 128 + row * 128;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4 *>(slab + ((((qt & 1) * 4 + i) ^ (row & 7)) << 4)) = qv[4 + i];
+            // rope chunk qt of the 64-byte row at chunk ^ ((row >> 1) & 3)
+            *reinterpret_cast<uint4 *>(sQr + row * 64 + ((qt ^ ((row >> 1) & 3)) << 4)) = qv[8];
+            fence_proxy_async_smem();     // the MMAs read these through the async proxy
             tc05::wait_st();
             tc05::fence_before_sync();
             __syncwarp();
@@ -509,9 +568,9 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
         for (int v = pair; v < V; v += npairs) {
             if (R[v] != R[v + 1]) continue;
             const int64_t orow = static_cast<int64_t>(v / p.hgroups) * p.hq + (v % p.hgroups) * kHeads + row;
-            uint4 *o = reinterpret_cast<uint4 *>(p.out + orow * kDv + rank * 256 + half * 128);
-            for (int i = 0; i < 16; ++i) o[i] = make_uint4(0, 0, 0, 0);
-            if (rank == 0 && half == 0 && p.lse) p.lse[orow] = -INFINITY;
+            uint4 *o = reinterpret_cast<uint4 *>(p.out + orow * kDv + rank * 256 + qt * 64);
+            for (int i = 0; i < 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+            if (rank == 0 && qt == 0 && p.lse) p.lse[orow] = -INFINITY;
         }
         bool q_loaded = false;
         Cursor cs{pair, pair * per};
@@ -521,103 +580,109 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
             const int64_t orow = static_cast<int64_t>(it.b) * p.hq + head;
             if (!q_loaded) load_q(it, ic);
             q_loaded = false;
-            float m = -INFINITY, l = 0.f;
-            // Scaled partial scores of tile t (this CTA's dims), rounded to fp16: 64
-            // keys as 32 half2 in nxt[].  Both CTAs round their own partial the same
-            // way, so own + peer is bitwise identical in the two CTAs.  (Macros rather
-            // than lambdas keep the arrays in registers.)
+            float m = -INFINITY, l = 0.f;   // running max (log2 units, scaled) and this thread's part of the sum
+            // Partial scores of tile t over this CTA's dims for this thread's 16 keys,
+            // rounded to fp16 (unscaled: the scale is applied in the exponent), as 8
+            // half2 in nxt[].  Both CTAs round their own partial the same way, so own
+            // + peer is bitwise identical in the two CTAs.  (Macros rather than
+            // lambdas keep the arrays in registers.)
 #define PKV_MLA_FETCH(t)                                                                                         \
     do {                                                                                                       \
         if (tid == 0) mbar_arrive_expect_tx(&bars[kXFull0 + (t) % kXSlots], kXBytes);                          \
-        ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kSFull], (t) & 1, abort_flag, p.err));              \
-        float a_[64];                                                                                          \
+        ok = warp_wait(ok, &bars[kSFull0 + ((t) & 1)], ((t) >> 1) & 1, abort_flag, p.err);                     \
+        float a_[16];                                                                                          \
         if (ok) {                                                                                              \
             tc05::fence_after_sync();                                                                          \
-            tc05::ld_x64(trow + kColS, a_);                                                                    \
+            tc05::ld_x16(trow + kColS + ((t) & 1) * kTile + qt * 16, a_);                                      \
+            tc05::wait_ld();                                                                                   \
         } else {                                                                                               \
-            _Pragma("unroll") for (int j = 0; j < 64; ++j) a_[j] = 0.f;                                        \
+            _Pragma("unroll") for (int j = 0; j < 16; ++j) a_[j] = 0.f;                                        \
         }                                                                                                      \
         tc05::fence_before_sync();                                                                             \
         __syncwarp();                                                                                          \
-        if (lane == 0) mbar_arrive(&bars[kSFree]);                                                             \
-        _Pragma("unroll") for (int j = 0; j < 32; ++j)                                                         \
-            nxt[j] = h22u(__floats2half2_rn(a_[2 * j] * p.scale_log2, a_[2 * j + 1] * p.scale_log2));          \
+        if (lane == 0) mbar_arrive(&bars[kSFree0 + ((t) & 1)]);                                               \
+        _Pragma("unroll") for (int j = 0; j < 8; ++j) nxt[j] = h22u(__floats2half2_rn(a_[2 * j], a_[2 * j + 1])); \
     } while (0)
-            // this thread's 32 keys of tile t (4 x 16 B) -> slot t % kXSlots of the peer
+            // this thread's 16 keys of tile t (2 x 16 B) -> slot t % kXSlots of the peer
 #define PKV_MLA_SEND(t)                                                                                          \
     do {                                                                                                       \
         if (ok) {                                                                                              \
             const uint32_t dst_ = x_peer + ((t) % kXSlots) * kXBytes;                                          \
             const uint32_t bar_ = xf_peer0 + ((t) % kXSlots) * 8;                                              \
-            _Pragma("unroll") for (int c = 0; c < 4; ++c) {                                                    \
-                const int j = 4 * c; /* select, not an index: keeps nxt in registers */                        \
-                st_async_v4(dst_ + ((half * 4 + c) * kHeads + row) * 16, __uint_as_float(half ? nxt[16 + j] : nxt[j]), \
-                            __uint_as_float(half ? nxt[17 + j] : nxt[j + 1]),                                  \
-                            __uint_as_float(half ? nxt[18 + j] : nxt[j + 2]),                                  \
-                            __uint_as_float(half ? nxt[19 + j] : nxt[j + 3]), bar_);                           \
-            }                                                                                                  \
+            _Pragma("unroll") for (int c = 0; c < 2; ++c)                                                      \
+                st_async_v4(dst_ + ((qt * 2 + c) * kHeads + row) * 16, __uint_as_float(nxt[4 * c]),            \
+                            __uint_as_float(nxt[4 * c + 1]), __uint_as_float(nxt[4 * c + 2]),                  \
+                            __uint_as_float(nxt[4 * c + 3]), bar_);                                            \
         }                                                                                                      \
     } while (0)
-            uint32_t cur[32], nxt[32];
+            uint32_t cur[8], nxt[8];
             PKV_MLA_FETCH(n);
             PKV_MLA_SEND(n);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
+            for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
             for (int ti = 0; ti < it.n_tiles; ++ti, ++n) {
                 const bool ahead = ti + 1 < it.n_tiles;
                 if (ahead) PKV_MLA_FETCH(n + 1);
-                // ---- the peer's partial of tile n ----
+                // ---- the peer's partial of tile n (this thread's 16 keys) ----
                 const int xs = n % kXSlots;
-                ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kXFull0 + xs], (n / kXSlots) & 1, abort_flag, p.err));
-                // tile n + 1 may go out now: the peer has finished with the slot it reuses
-                if (ahead) PKV_MLA_SEND(n + 1);
+                ok = warp_wait(ok, &bars[kXFull0 + xs], (n / kXSlots) & 1, abort_flag, p.err);
                 const int n_valid = it.key_end - (it.key_begin + ti * kTile);
-                // own + peer partial in half2 (the same bits in both CTAs), row max in half2
-                __half2 x2[32];
+                // own + peer partial in half2 (the same bits in both CTAs)
+                __half2 x2[8];
                 {
                     const uint4 *xr = reinterpret_cast<const uint4 *>(reinterpret_cast<unsigned char *>(sX) + xs * kXBytes);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
+                    for (int c = 0; c < 2; ++c) {
                         uint4 w4 = make_uint4(0, 0, 0, 0);
-                        if (ok) w4 = xr[c * kHeads + row];
+                        if (ok) w4 = xr[(qt * 2 + c) * kHeads + row];
                         x2[4 * c] = __hadd2(u2h2(cur[4 * c]), u2h2(w4.x));
                         x2[4 * c + 1] = __hadd2(u2h2(cur[4 * c + 1]), u2h2(w4.y));
                         x2[4 * c + 2] = __hadd2(u2h2(cur[4 * c + 2]), u2h2(w4.z));
                         x2[4 * c + 3] = __hadd2(u2h2(cur[4 * c + 3]), u2h2(w4.w));
                     }
                 }
+                // slot n % 2 is read: tile n + 1 may go out (the peer answers it with
+                // tile n + 2 into this slot)
+                if (ahead) PKV_MLA_SEND(n + 1);
                 if (n_valid < kTile) {   // keys past the end: -inf
                     const __half2 ninf = __halves2half2(__ushort_as_half(0xfc00), __ushort_as_half(0xfc00));
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        if (2 * j >= n_valid) x2[j] = ninf;
-                        else if (2 * j + 1 >= n_valid) x2[j] = __halves2half2(__low2half(x2[j]), __ushort_as_half(0xfc00));
+                    for (int j = 0; j < 8; ++j) {
+                        const int key = qt * 16 + 2 * j;
+                        if (key >= n_valid) x2[j] = ninf;
+                        else if (key + 1 >= n_valid) x2[j] = __halves2half2(__low2half(x2[j]), __ushort_as_half(0xfc00));
                     }
                 }
+                // row max of the tile: this thread's 16 keys, then the row's other three
+                // threads' through shared memory
                 float mx;
                 {
                     __half2 m2 = x2[0];
 #pragma unroll
-                    for (int j = 1; j < 32; ++j) m2 = __hmax2(m2, x2[j]);
+                    for (int j = 1; j < 8; ++j) m2 = __hmax2(m2, x2[j]);
                     const float2 mf = __half22float2(m2);
-                    mx = fmaxf(mf.x, mf.y);
+                    float *mb = red + (n & 1) * 4 * kHeads;
+                    mb[qt * kHeads + row] = fmaxf(mf.x, mf.y);
+                    named_bar_sync(row_bar, 128);
+                    mx = fmaxf(fmaxf(mb[row], mb[kHeads + row]), fmaxf(mb[2 * kHeads + row], mb[3 * kHeads + row])) *
+                         p.scale_log2;
                 }
-                // ---- online softmax over this tile's keys ----
+                // ---- online softmax over this tile's keys (log2 units) ----
                 const bool raise = mx > m + kLazy || (m == -INFINITY && mx != -INFINITY);
                 const float corr = raise ? ex2(m - mx) : 1.f;
-                // O (and P) are final for tile n - 1 once its P V completed
-                ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kPFree], (n & 1) ^ 1, abort_flag, p.err));
-                if (__any_sync(0xffffffffu, raise && l > 0.f) && ok) {
-                    // rescale this thread's 128 value columns of O in TMEM
+                if (__any_sync(0xffffffffu, raise && m != -INFINITY) && ok) {
+                    // O is final for tile n - 1 (m finite: it belongs to this segment)
+                    // once its P V completed; then rescale this thread's 64 value columns
+                    ok = warp_wait(ok, &bars[kPFree0 + ((n - 1) & 1)], ((n - 1) >> 1) & 1, abort_flag, p.err);
                     tc05::fence_after_sync();
 #pragma unroll 1
-                    for (int cc = 0; cc < 8; ++cc) {
+                    for (int cc = 0; cc < 4 && ok; ++cc) {
                         float ov[16];
-                        tc05::ld_x16(trow + kColO + half * 128 + cc * 16, ov);
+                        tc05::ld_x16(trow + kColO + qt * 64 + cc * 16, ov);
                         tc05::wait_ld();
 #pragma unroll
                         for (int e = 0; e < 16; ++e) ov[e] *= corr;
-                        tc05::st_x16(trow + kColO + half * 128 + cc * 16, ov);
+                        tc05::st_x16(trow + kColO + qt * 64 + cc * 16, ov);
                     }
                     tc05::wait_st();
                 }
@@ -625,39 +690,35 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
                     l *= corr;
                     m = mx;
                 }
-                uint32_t h[16];
+                uint32_t h[8];
                 float lsum = 0.f;
-                // this thread's 32 keys (half is warp-uniform: a branch, not an index)
-#define PKV_MLA_EXP(OFF)                                                                         \
-    _Pragma("unroll") for (int j = 0; j < 16; ++j) {                                            \
-        const float2 xf = __half22float2(x2[(OFF) + j]);                                        \
-        const float p0 = m == -INFINITY ? 0.f : ex2(xf.x - m);                                  \
-        const float p1 = m == -INFINITY ? 0.f : ex2(xf.y - m);                                  \
-        lsum += p0 + p1;                                                                        \
-        h[j] = pack_bf16x2(p0, p1);                                                             \
-    }
-                if (half) {
-                    PKV_MLA_EXP(16)
-                } else {
-                    PKV_MLA_EXP(0)
+                const float nm = -m;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {   // p = 2^(scale log2(e) x - m)
+                    const float2 xf = __half22float2(x2[j]);
+                    const float p0 = m == -INFINITY ? 0.f : ex2(fmaf(xf.x, p.scale_log2, nm));
+                    const float p1 = m == -INFINITY ? 0.f : ex2(fmaf(xf.y, p.scale_log2, nm));
+                    lsum += p0 + p1;
+                    h[j] = pack_bf16x2(p0, p1);
                 }
-#undef PKV_MLA_EXP
                 l += lsum;
-                // this half's 32 keys of P (16 bf16 pairs) into the lane's TMEM columns
+                // this thread's 16 keys of P (8 bf16 pairs) into buffer n & 1, free once
+                // the P V of tile n - 2 completed
+                ok = warp_wait(ok, &bars[kPFree0 + (n & 1)], ((n >> 1) & 1) ^ 1, abort_flag, p.err);
                 if (ok) {
                     tc05::fence_after_sync();
-                    tc05::st_x16_u32(trow + kColP + half * 16, h);
+                    tc05::st_x8_u32(trow + kColP + (n & 1) * 32 + qt * 8, h);
                     tc05::wait_st();
                 }
                 tc05::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[kPFull]);
+                if (lane == 0) mbar_arrive(&bars[kPFull0 + (n & 1)]);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
+                for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
             }
 #undef PKV_MLA_FETCH
 #undef PKV_MLA_SEND
-            // ---- the next item's q goes into TMEM now, so its q.k overlaps this epilogue ----
+            // ---- the next segment's q goes in now, so its q.k overlaps this epilogue ----
             {
                 Cursor c2 = cs;
                 Seg nt;
@@ -667,38 +728,36 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
                 }
             }
             // ---- epilogue: normalise O and write the output (or the split partial) ----
-            // l of the whole row = both halves' partial sums (m is the same in both).
-            // slot n & 1: not the last tile's max slot, and free since tile n - 1's barrier
-            float *lb = red + (n & 1) * 2 * kHeads;
-            lb[half * kHeads + row] = l;
-            named_bar_sync(1, kSoftmaxWarps * 32);
-            l += lb[(half ^ 1) * kHeads + row];
-            named_bar_sync(1, kSoftmaxWarps * 32);
-            ok = __all_sync(0xffffffffu, ok && wait_bar(&bars[kODone], ic & 1, abort_flag, p.err));
+            // l of the whole row = the four threads' partial sums (m is the same in all).
+            // Buffer n & 1: not the last tile's max buffer, and free since that tile's barrier.
+            float *lb = red + (n & 1) * 4 * kHeads;
+            lb[qt * kHeads + row] = l;
+            named_bar_sync(row_bar, 128);
+            l = (lb[row] + lb[kHeads + row]) + (lb[2 * kHeads + row] + lb[3 * kHeads + row]);
+            named_bar_sync(row_bar, 128);
+            ok = warp_wait(ok, &bars[kODone], ic & 1, abort_flag, p.err);
             tc05::fence_after_sync();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const bool single = it.part < 0;
             const int64_t prow = static_cast<int64_t>(it.part) * kHeads + row;
 #pragma unroll 1
-            for (int cb = 0; cb < 8; cb += 4) {
-                float ov[4][16];
+            for (int cb = 0; cb < 4; cb += 2) {
+                float ov[2][16];
                 if (ok) {
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) tc05::ld_x16(trow + kColO + half * 128 + (cb + q4) * 16, ov[q4]);
+                    tc05::ld_x16(trow + kColO + qt * 64 + cb * 16, ov[0]);
+                    tc05::ld_x16(trow + kColO + qt * 64 + (cb + 1) * 16, ov[1]);
                     tc05::wait_ld();
                 } else {
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) ov[q4][e] = 0.f;
+                    for (int e = 0; e < 16; ++e) ov[0][e] = ov[1][e] = 0.f;
                 }
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int col = rank * 256 + half * 128 + (cb + q4) * 16;
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    const int col = rank * 256 + qt * 64 + (cb + q2) * 16;
                     if (single) {
                         uint32_t hh[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) hh[e] = pack_bf16x2(ov[q4][2 * e] * inv, ov[q4][2 * e + 1] * inv);
+                        for (int e = 0; e < 8; ++e) hh[e] = pack_bf16x2(ov[q2][2 * e] * inv, ov[q2][2 * e + 1] * inv);
                         uint4 *o = reinterpret_cast<uint4 *>(p.out + orow * kDv + col);
                         o[0] = make_uint4(hh[0], hh[1], hh[2], hh[3]);
                         o[1] = make_uint4(hh[4], hh[5], hh[6], hh[7]);
@@ -706,12 +765,12 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv) {
                         float4 *o = reinterpret_cast<float4 *>(p.part_o + prow * kDv + col);
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            o[e] = make_float4(ov[q4][4 * e] * inv, ov[q4][4 * e + 1] * inv, ov[q4][4 * e + 2] * inv,
-                                               ov[q4][4 * e + 3] * inv);
+                            o[e] = make_float4(ov[q2][4 * e] * inv, ov[q2][4 * e + 1] * inv, ov[q2][4 * e + 2] * inv,
+                                               ov[q2][4 * e + 3] * inv);
                     }
                 }
             }
-            if (rank == 0 && half == 0) {
+            if (rank == 0 && qt == 0) {
                 const float lse2 = m + log2f(l);
                 if (single) {
                     if (p.lse) p.lse[orow] = lse2 * kLn2;
@@ -921,6 +980,11 @@ pkv_status launch(const pkv_decode_args *a, void *ws, size_t ws_bytes, int32_t *
     const uint32_t bk[2] = {64, static_cast<uint32_t>(p.box_rows)};
     if (!encode_tmap_bf16(&tmkv, a->k_pool, 2, dk, sk, bk))
         return fail(PKV_ERR_CUDA, "pkv_decode(MLA): cuTensorMapEncodeTiled rejected the latent pool");
+    // the same pool as 32-dim boxes with 64-byte swizzle: each CTA's half of the rope dims
+    CUtensorMap tmrope;
+    const uint32_t br[2] = {32, static_cast<uint32_t>(p.box_rows)};
+    if (!encode_tmap_bf16(&tmrope, a->k_pool, 2, dk, sk, br, 64))
+        return fail(PKV_ERR_CUDA, "pkv_decode(MLA): cuTensorMapEncodeTiled rejected the latent pool (rope view)");
 
     static size_t lim = 0;
     static int max_pairs = 0;
@@ -950,7 +1014,7 @@ pkv_status launch(const pkv_decode_args *a, void *ws, size_t ws_bytes, int32_t *
         max_pairs = n;
     }
     const int pairs = std::max(1, std::min(max_pairs, pl.max_spans));
-    mla_decode_kernel<<<2 * pairs, kThreads, smem, s>>>(p, tmkv);
+    mla_decode_kernel<<<2 * pairs, kThreads, smem, s>>>(p, tmkv, tmrope);
     pkv_status st = check_launch("pkv_decode(MLA split kernel)");
     if (st != PKV_OK) return st;
     if (msmem > 48 * 1024 &&

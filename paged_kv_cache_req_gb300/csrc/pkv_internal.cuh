@@ -20,9 +20,10 @@ pkv_status check_launch(const char *what);
 int sm_count();
 
 // 2-D/3-D tiled TMA descriptor over a bf16 tensor (dims innermost first, strides in
-// bytes for dims 1..rank-1), 128-byte swizzle; false if the driver rejects it.
+// bytes for dims 1..rank-1), 128-byte swizzle (or 64-byte: swizzle_bytes = 64);
+// false if the driver rejects it.
 bool encode_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims, const uint64_t *strides,
-                      const uint32_t *box);
+                      const uint32_t *box, int swizzle_bytes = 128);
 
 inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 inline bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
@@ -149,6 +150,12 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
             "r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
         : "memory");
+}
+// Bring the box at (c0, c1) of a tensor map into L2 (no shared memory, no completion signal).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int c0, int c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n" ::"l"(reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

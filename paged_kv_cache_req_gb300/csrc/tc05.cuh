@@ -80,6 +80,13 @@ __device__ __forceinline__ void st_x16_u32(uint32_t taddr, const uint32_t (&v)[1
         : "memory");
 }
 
+// Raw 32-bit TMEM store of 8 columns.
+__device__ __forceinline__ void st_x8_u32(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr), "r"(v[0]),
+                 "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
 // Arrive once on the mbarrier when every MMA this thread issued so far has completed.
 __device__ __forceinline__ void commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
