@@ -113,10 +113,11 @@ def decode_traffic(workload):
         return None
     with open(path) as f:
         d = json.load(f)
-    src = os.path.join(ROOT, "paged_kv_cache_req_gb300", "csrc", d.get("source", "decode_gqa.cu"))
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     ent = d.get("workloads", {}).get(workload)
-    if not ent or ent.get("source_sha") != h:
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "paged_kv_cache_req_gb300", "csrc", ent.get("source", d.get("source", "decode_gqa.cu")))
+    if ent.get("source_sha") != hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]:
         return None
     return ent.get("bytes_per_launch")
 
