@@ -62,6 +62,12 @@ def _load():
         lib.pkvo_ragged_gather.argtypes = [P, P, I64, I64, I64, P, I64, I64, I64, P, P, P, I32,
                                            P, P, I64, P]
         lib.pkvo_ragged_gather.restype = ctypes.c_int
+        lib.pkvo_alloc_extend.argtypes = [P, P, P, I32, I32, I64, P, I64, P, P, I64]
+        lib.pkvo_alloc_extend.restype = ctypes.c_int
+        lib.pkvo_write_req_to_token.argtypes = [P, I64, I64, I64, P, P, P, P, P, P, I32]
+        lib.pkvo_write_req_to_token.restype = ctypes.c_int
+        lib.pkvo_encoder_merge.argtypes = [P, I64, I64, I64, P, P, I64, P, I64, I64, P]
+        lib.pkvo_encoder_merge.restype = ctypes.c_int
         lib.pkvo_max_threads.argtypes = []
         lib.pkvo_max_threads.restype = ctypes.c_int32
         _lib = lib
@@ -174,3 +180,49 @@ def ragged_gather(k_pool: np.ndarray, v_pool: Optional[np.ndarray], req_to_token
                                     _ptr(r2t), r2t.shape[0], r2t.shape[1], r2t.shape[1], _ptr(rpi),
                                     _ptr(ks), _ptr(sl), B, _ptr(k_out), _ptr(v_out), cap, _ptr(cu))
     return st, k_out[:cap], (None if v_out is None else v_out[:cap]), cu
+
+
+def alloc_extend(prefix_lens, seq_lens, last_loc, page_size, num_pool_pages, free_pages, free_state, out_cap=None):
+    """Page allocation for a batch step.  free_state = [head, count] (updated in place on success).
+    Returns (status, out_cache_loc)."""
+    pl, sl, ll = _i32(prefix_lens), _i32(seq_lens), _i32(last_loc)
+    fp = _i32(free_pages)
+    assert isinstance(free_state, np.ndarray) and free_state.dtype == np.int32 and free_state.flags["C_CONTIGUOUS"]
+    need = int(np.maximum(sl.astype(np.int64) - pl, 0).sum()) if len(sl) else 0
+    cap = need if out_cap is None else int(out_cap)
+    out = np.full(max(cap, 1), -1, dtype=np.int32)
+    st = _load().pkvo_alloc_extend(_ptr(pl), _ptr(sl), _ptr(ll), len(sl), page_size, num_pool_pages, _ptr(fp),
+                                   len(fp), _ptr(free_state), _ptr(out), cap)
+    return st, out[:need]
+
+
+def write_req_to_token(req_to_token, req_pool_idx, prefix_lens, seq_lens, prefix_slots, out_cache_loc,
+                       kv_start=None):
+    """In-place row writer.  prefix_slots: a list with, per request, an int32 array of
+    its reused prefix slots or None (already in place).  Returns the status."""
+    r2t = req_to_token
+    assert r2t.dtype == np.int32 and r2t.flags["C_CONTIGUOUS"]
+    rpi, ks, pl, sl = _i32(req_pool_idx), _i32(kv_start), _i32(prefix_lens), _i32(seq_lens)
+    B = len(sl)
+    keep = [None if a is None else np.ascontiguousarray(a, dtype=np.int32) for a in prefix_slots]
+    ptrs = (ctypes.c_void_p * max(B, 1))(*[(None if a is None else a.ctypes.data) for a in keep] + [None] * (max(B, 1) - B))
+    loc = _i32(out_cache_loc) if out_cache_loc is not None and len(out_cache_loc) else np.zeros(1, np.int32)
+    return _load().pkvo_write_req_to_token(_ptr(r2t), r2t.shape[0], r2t.shape[1], r2t.shape[1], _ptr(rpi), _ptr(ks),
+                                           _ptr(pl), _ptr(sl), ctypes.cast(ptrs, ctypes.c_void_p), _ptr(loc), B)
+
+
+def encoder_merge(buffer: np.ndarray, block_ids, positions, hidden: np.ndarray):
+    """In-place merge of encoder-cache blocks into hidden rows.  buffer [num_blocks, block_size, ...],
+    positions [max_blocks, block_size] int64, hidden [num_tokens, ...] (same row bytes).
+    Returns (status, rows written)."""
+    assert buffer.flags["C_CONTIGUOUS"] and hidden.flags["C_CONTIGUOUS"]
+    nb, bs = buffer.shape[0], buffer.shape[1]
+    row_bytes = buffer[0, 0].nbytes
+    assert hidden[0].nbytes == row_bytes
+    bid = _i32(block_ids)
+    pos = np.ascontiguousarray(positions, dtype=np.int64)
+    assert pos.shape == (len(bid), bs)
+    filled = np.zeros(1, dtype=np.int64)
+    st = _load().pkvo_encoder_merge(_ptr(buffer), nb, bs, row_bytes, _ptr(bid), _ptr(pos), len(bid), _ptr(hidden),
+                                    hidden.shape[0], hidden.strides[0], _ptr(filled))
+    return st, int(filled[0])

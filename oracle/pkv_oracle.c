@@ -280,6 +280,125 @@ int pkvo_ragged_gather(const uint8_t *k_pool, const uint8_t *v_pool, int64_t num
     return PKVO_OK;
 }
 
+/*
+ * Page allocation for one batch step.  [P1 "two pools and a page size",
+ * PagedTokenToKVPoolAllocator alloc_extend / alloc_decode]: the new positions
+ * [prefix_len, seq_len) of a request first continue its partly used last page
+ * (the slots after last_loc, the slot of position prefix_len - 1), then take
+ * whole new pages from the front of the free list, requests in order; page p
+ * covers slots p*ps .. p*ps + ps - 1.  At page_size 1 each new position takes
+ * one entry (TokenToKVPoolAllocator.alloc pops the first need_size slots).
+ * The free list is free_pages[head .. head + count) with free_state = {head,
+ * count}; on success head grows and count shrinks by the pages taken.  A step
+ * needing more pages than count, or more output slots than out_cap, writes
+ * nothing and changes nothing (the allocator's None).  Slots go to
+ * out_cache_loc in request order, positions ascending.
+ */
+int pkvo_alloc_extend(const int32_t *prefix_lens, const int32_t *seq_lens, const int32_t *last_loc, int32_t batch,
+                      int32_t page_size, int64_t num_pool_pages, const int32_t *free_pages, int64_t free_pages_len,
+                      int32_t *free_state, int32_t *out_cache_loc, int64_t out_cap) {
+    if (page_size <= 0 || batch < 0) return PKVO_ERR_ARG;
+    const int64_t ps = page_size;
+    int64_t pages = 0, toks = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+        const int64_t p = prefix_lens[b], s = seq_lens[b];
+        if (p < 0 || s < p) return PKVO_ERR_RANGE;
+        if (p % ps != 0) {   /* the partly used page must hold position p - 1 at its offset */
+            const int64_t ll = last_loc[b];
+            if (ll < 0 || ll >= num_pool_pages * ps) return PKVO_ERR_RANGE;
+            if (ll % ps != (p - 1) % ps) return PKVO_ERR_CONTIG;
+        }
+        pages += (s + ps - 1) / ps - (p + ps - 1) / ps;
+        toks += s - p;
+    }
+    const int64_t head = free_state[0], count = free_state[1];
+    if (toks > out_cap || pages > count || head < 0 || head + pages > free_pages_len) return PKVO_ERR_CAPACITY;
+    for (int64_t k = 0; k < pages; ++k)
+        if (free_pages[head + k] < 0 || free_pages[head + k] >= num_pool_pages) return PKVO_ERR_RANGE;
+    int64_t pg = head, o = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+        const int64_t p = prefix_lens[b], s = seq_lens[b];
+        const int64_t aligned = (p + ps - 1) / ps * ps;   /* first position on a new page */
+        for (int64_t t = p; t < s; ++t) {
+            int64_t slot;
+            if (t < aligned) slot = last_loc[b] + (t - p + 1);
+            else slot = (int64_t)free_pages[pg + (t - aligned) / ps] * ps + t % ps;
+            out_cache_loc[o++] = (int32_t)slot;
+        }
+        pg += (s + ps - 1) / ps - (p + ps - 1) / ps;
+    }
+    free_state[0] = (int32_t)(head + pages);
+    free_state[1] = (int32_t)(count - pages);
+    return PKVO_OK;
+}
+
+/*
+ * Row writer.  [P1 write_cache_indices / write_req_to_token_pool]: for request
+ * b, columns kv_start + [0, prefix_len) of row req_pool_idx[b] receive the
+ * reused prefix slots prefix_slots[b][0 .. prefix_len) (skipped when that
+ * pointer is NULL: they are already in place), and columns kv_start +
+ * [prefix_len, seq_len) the freshly allocated slots out_cache_loc[e_b ..), e_b
+ * being the extend lengths (seq_len - prefix_len) of the requests before b.
+ * A request whose row or columns fall outside the table is skipped with
+ * PKVO_ERR_RANGE (the others are written).
+ */
+int pkvo_write_req_to_token(int32_t *r2t, int64_t num_rows, int64_t row_stride, int64_t row_width,
+                            const int32_t *req_pool_idx, const int32_t *kv_start, const int32_t *prefix_lens,
+                            const int32_t *seq_lens, const int32_t *const *prefix_slots,
+                            const int32_t *out_cache_loc, int32_t batch) {
+    int status = PKVO_OK;
+    int64_t e = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+        const int64_t row = req_pool_idx[b], st = kv_start ? kv_start[b] : 0;
+        const int64_t p = prefix_lens[b], s = seq_lens[b];
+        const int64_t ext = s > p ? s - p : 0;
+        if (row < 0 || row >= num_rows || st < 0 || p < 0 || s < p || st + s > row_width) {
+            status = PKVO_ERR_RANGE;
+            e += ext;
+            continue;
+        }
+        int32_t *r = r2t + row * row_stride + st;
+        if (prefix_slots && prefix_slots[b])
+            for (int64_t t = 0; t < p; ++t) r[t] = prefix_slots[b][t];
+        for (int64_t t = p; t < s; ++t) r[t] = out_cache_loc[e + (t - p)];
+        e += ext;
+    }
+    return status;
+}
+
+/*
+ * Encoder-cache merge (Neuron encoder cache, "Merge Inside Compiled Graph" and
+ * "Read Path"): the blocks block_ids[i] of buffer [num_blocks, block_size, row]
+ * are stacked and flattened, and token j of block i lands in hidden row
+ * positions[i][j] when that position lies in [0, num_tokens); a position at or
+ * past num_tokens (the sentinel) writes nothing (the discarded dummy row).  A
+ * negative position or a block id outside the buffer is PKVO_ERR_RANGE and that
+ * entry is skipped.  *filled counts the rows written, for the check that every
+ * scheduled position was filled.  Rows are opaque bytes.
+ */
+int pkvo_encoder_merge(const uint8_t *buffer, int64_t num_blocks, int64_t block_size, int64_t row_bytes,
+                       const int32_t *block_ids, const int64_t *positions, int64_t max_blocks, uint8_t *hidden,
+                       int64_t num_tokens, int64_t hidden_row_stride_bytes, int64_t *filled) {
+    int status = PKVO_OK;
+    int64_t n = 0;
+    for (int64_t i = 0; i < max_blocks; ++i) {
+        const int64_t blk = block_ids[i];
+        for (int64_t j = 0; j < block_size; ++j) {
+            const int64_t pos = positions[i * block_size + j];
+            if (pos >= num_tokens) continue;
+            if (pos < 0 || blk < 0 || blk >= num_blocks) {
+                status = PKVO_ERR_RANGE;
+                continue;
+            }
+            memcpy(hidden + pos * hidden_row_stride_bytes, buffer + (blk * block_size + j) * row_bytes,
+                   (size_t)row_bytes);
+            ++n;
+        }
+    }
+    if (filled) *filled = n;
+    return status;
+}
+
 /* Threads the decode would use (reported beside CPU-baseline timings). */
 int32_t pkvo_max_threads(void) {
 #ifdef _OPENMP

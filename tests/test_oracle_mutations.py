@@ -41,6 +41,16 @@ MUTANTS = [
     ("store_indexes_source_by_slot", "rows + (int64_t)i * src_row_stride_bytes", "rows + slot * src_row_stride_bytes", 1),
     ("store_ignores_padding", "if (slot < 0) continue;", ";", 1),
     ("cu_seqlens_not_cumulative", "cu_seqlens[b + 1] = (int32_t)running;", "cu_seqlens[b + 1] = (int32_t)len;", 1),
+    ("alloc_partial_page_off_by_one", "if (t < aligned) slot = last_loc[b] + (t - p + 1);",
+     "if (t < aligned) slot = last_loc[b] + (t - p);", 1),
+    ("alloc_no_partial_page", "const int64_t aligned = (p + ps - 1) / ps * ps;", "const int64_t aligned = p;", 1),
+    ("alloc_pages_not_advanced", "        pg += (s + ps - 1) / ps - (p + ps - 1) / ps;", "        pg += 0;", 1),
+    ("alloc_state_not_updated", "free_state[0] = (int32_t)(head + pages);", "free_state[0] = (int32_t)head;", 1),
+    ("alloc_no_capacity_check", "if (toks > out_cap || pages > count ||", "if (toks > out_cap ||", 1),
+    ("write_skips_prefix", "for (int64_t t = 0; t < p; ++t) r[t] = prefix_slots[b][t];", ";", 1),
+    ("write_new_slots_not_offset", "for (int64_t t = p; t < s; ++t) r[t] = out_cache_loc[e + (t - p)];",
+     "for (int64_t t = p; t < s; ++t) r[t] = out_cache_loc[t - p];", 1),
+    ("merge_ignores_block_ids", "buffer + (blk * block_size + j) * row_bytes", "buffer + (i * block_size + j) * row_bytes", 1),
     ("gather_ignores_kv_start",
      "const int64_t slot = r2t[row * row_stride + start + t];\n            if (slot < 0 || slot >= num_slots) return",
      "const int64_t slot = r2t[row * row_stride + t];\n            if (slot < 0 || slot >= num_slots) return", 1),

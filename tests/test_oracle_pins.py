@@ -374,3 +374,116 @@ def test_ragged_gather_contiguous_and_cu_seqlens():
     np.testing.assert_array_equal(ko, pool_k[flat])
     np.testing.assert_array_equal(vo, pool_v[flat])
     assert oracle.ragged_gather(pool_k, pool_v, r2t2, rpi, lens, out_rows_cap=10)[0] == oracle.ERR_CAPACITY
+
+
+# ---------------------------------------------------------------- allocator and row writer
+def _rows_after_prefix(rng, lens, ps, num_pages, width):
+    """Rows already holding `lens` tokens each (whole shuffled pages), the rest of the
+    pool as the free list; returns (r2t, rpi, free_pages)."""
+    r2t, rpi = paged_table(rng, lens, ps, num_pages, width=width)
+    used = set()
+    for b, L in enumerate(lens):
+        used.update((r2t[rpi[b], :L] // ps).tolist())
+    free = np.array([p for p in rng.permutation(np.arange(1, num_pages)) if p not in used], dtype=np.int32)
+    return r2t, rpi, free
+
+
+def test_alloc_page_size_one_pops_the_front_of_the_free_list():
+    # TokenToKVPoolAllocator: alloc(need) returns the first `need` free slots
+    free = np.array([7, 3, 9, 1, 12, 5], dtype=np.int32)
+    state = np.array([0, 6], dtype=np.int32)
+    st, out = oracle.alloc_extend([0, 2], [2, 5], [-1, 4], 1, 16, free, state)
+    assert st == oracle.OK and out.tolist() == [7, 3, 9, 1, 12] and state.tolist() == [5, 1]
+
+
+def test_alloc_extend_equals_one_token_at_a_time_for_one_request():
+    # alloc_extend of positions [p, s) equals s - p alloc_decode steps of one request
+    ps, p, s = 8, 13, 42
+    rng = np.random.default_rng(3)
+    free = rng.permutation(np.arange(2, 40)).astype(np.int32)
+    last = 5 * ps + (p - 1) % ps
+    st, out = oracle.alloc_extend([p], [s], [last], ps, 40, free, np.array([0, len(free)], np.int32))
+    assert st == oracle.OK
+    state = np.array([0, len(free)], np.int32)
+    step, prev = [], last
+    for t in range(p, s):
+        st, o = oracle.alloc_extend([t], [t + 1], [prev], ps, 40, free, state)
+        assert st == oracle.OK
+        step.append(int(o[0]))
+        prev = int(o[0])
+    assert out.tolist() == step
+
+
+@pytest.mark.parametrize("ps", [1, 4, 16])
+def test_alloc_then_write_keeps_pages_contiguous(ps):
+    # the allocator's invariant ("keeps a sequence's tokens contiguous within each
+    # page"): after alloc_extend + write_req_to_token every row passes build_indices,
+    # the new pages are the front of the free list, each owned by one request
+    rng = np.random.default_rng(ps)
+    num_pages = 400 // ps + 40
+    prefix = [0, 1, ps, 3 * ps + 1, 5]
+    seq = [3, 1 + 2 * ps, 4 * ps, 3 * ps + 2, 5 + 7 * ps]
+    r2t, rpi, free = _rows_after_prefix(rng, prefix, ps, num_pages, max(seq) + 8)
+    last = [int(r2t[rpi[b], p - 1]) if p else -1 for b, p in enumerate(prefix)]
+    state = np.array([2, len(free) - 2], np.int32)
+    st, out = oracle.alloc_extend(prefix, seq, last, ps, num_pages, free, state)
+    assert st == oracle.OK
+    taken = sum(-(-s // ps) - (-(-p // ps)) for p, s in zip(prefix, seq))
+    assert state.tolist() == [2 + taken, len(free) - 2 - taken]
+    new_pages = sorted(set((out // ps).tolist()) - set(last_p // ps for last_p in last if last_p >= 0))
+    assert new_pages == sorted(free[2:2 + taken].tolist())
+    assert len(set(out.tolist())) == len(out)
+    assert oracle.write_req_to_token(r2t, rpi, prefix, seq, [None] * len(seq), out) == oracle.OK
+    st, *_ = oracle.build_indices(r2t, rpi, seq, ps, num_pages)
+    assert st == oracle.OK
+    e = 0
+    for b, (p, s) in enumerate(zip(prefix, seq)):   # brute force: the row is prefix then the new slots
+        assert r2t[rpi[b], p:s].tolist() == out[e:e + s - p].tolist()
+        e += s - p
+
+
+def test_alloc_out_of_pages_changes_nothing():
+    free = np.arange(10, 20, dtype=np.int32)                                         # entries past the count
+    state = np.array([1, 2], np.int32)                                               # are not free
+    st, out = oracle.alloc_extend([0, 0], [16, 20], [-1, -1], 16, 64, free, state)   # needs 3 pages, 2 free
+    assert st == oracle.ERR_CAPACITY and state.tolist() == [1, 2] and (out == -1).all()
+    st, _ = oracle.alloc_extend([5], [6], [2 * 16 + 3], 16, 64, free, state)        # last_loc at the wrong offset
+    assert st == oracle.ERR_CONTIG and state.tolist() == [1, 2]
+
+
+def test_write_req_to_token_prefix_and_new_slots():
+    r2t = np.full((4, 12), -5, dtype=np.int32)
+    pre = [np.array([40, 41, 42], np.int32), None, np.array([9], np.int32)]
+    st = oracle.write_req_to_token(r2t, [2, 1, 3], [3, 2, 1], [5, 4, 2], pre, np.array([7, 8, 100, 101, 55]),
+                                   kv_start=[0, 4, 8])
+    assert st == oracle.OK
+    assert r2t[2].tolist() == [40, 41, 42, 7, 8] + [-5] * 7
+    assert r2t[1].tolist() == [-5] * 4 + [-5, -5, 100, 101] + [-5] * 4      # NULL prefix: columns 4, 5 untouched
+    assert r2t[3].tolist() == [-5] * 8 + [9, 55, -5, -5]
+    assert (r2t[0] == -5).all()
+    assert oracle.write_req_to_token(r2t, [2], [0], [13], [None], np.arange(13)) == oracle.ERR_RANGE
+
+
+# ---------------------------------------------------------------- encoder-cache merge
+def test_encoder_merge_matches_numpy_indexing():
+    rng = np.random.default_rng(11)
+    nb, bs, d, ntok = 6, 8, 5, 30
+    buf = rng.integers(-1000, 1000, size=(nb, bs, d)).astype(np.int32)
+    block_ids = np.array([0, 2, 3, 4, 5], np.int32)                 # an image, a 3-block video, the scratch block
+    pos = np.full((5, bs), ntok, dtype=np.int64)                    # sentinel everywhere ...
+    perm = rng.permutation(ntok)
+    pos[0, :6] = perm[:6]                                           # ... but 6 image tokens,
+    pos[1:4, :] = perm[6:30].reshape(3, 8)                          # 24 video tokens
+    pos[4, 3] = ntok + 7                                            # past the end: also a don't-care
+    hidden = np.full((ntok, d), -1, np.int32)
+    st, filled = oracle.encoder_merge(buf, block_ids, pos, hidden)
+    assert st == oracle.OK and filled == 30
+    ref = np.full((ntok, d), -1, np.int32)
+    flat = buf[block_ids].reshape(-1, d)
+    valid = (pos.reshape(-1) < ntok)
+    ref[pos.reshape(-1)[valid]] = flat[valid]
+    assert np.array_equal(hidden, ref)
+    bad = pos.copy()
+    bad[0, 6] = -1
+    assert oracle.encoder_merge(buf, block_ids, bad, hidden.copy())[0] == oracle.ERR_RANGE
+    assert oracle.encoder_merge(buf, np.array([0, 2, 3, 4, 9], np.int32), pos, hidden.copy())[0] == oracle.OK  # all sentinel
