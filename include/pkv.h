@@ -253,6 +253,80 @@ pkv_status pkv_ragged_gather(const void *k_pool, const void *v_pool, int64_t num
                              void *v_out, int64_t out_rows_cap, int32_t *cu_seqlens,
                              int32_t *err_flags, pkv_stream_t stream);
 
+/*
+ * pkv_alloc_extend -- page allocation for one batch step, on the device.
+ *
+ * The paged allocator's growth path ("Enabling Encoder-Decoder Models on Intel
+ * XPU in SGLang", "two pools and a page size": PagedTokenToKVPoolAllocator
+ * alloc_extend / alloc_decode): request b grows from prefix_lens[b] to
+ * seq_lens[b] tokens.  Its new positions first continue its partly used last
+ * page, on the slots after last_loc[b] (the slot of position prefix_lens[b] - 1;
+ * read only when prefix_lens[b] % page_size != 0), then take whole new pages
+ * from the front of the free list, requests in order; page p covers slots
+ * p*page_size .. p*page_size + page_size - 1.  At page_size 1 every new position
+ * takes one entry (TokenToKVPoolAllocator.alloc).  This keeps every request's
+ * tokens contiguous inside each page, as pkv_build_indices requires.
+ *
+ * free_pages     device int32 [free_pages_len]; the free list is
+ *                free_pages[head .. head + count).
+ * free_state     device int32 [2] = {head, count}, read and, on success,
+ *                advanced by the pages taken (head += n, count -= n).
+ * out_cache_loc  device int32 [out_cap]: the new slots, request order,
+ *                positions ascending (sum of seq_lens - prefix_lens entries).
+ * A step that needs more pages than count or more slots than out_cap raises
+ * PKV_DEVERR_CAPACITY and writes nothing (the allocator returning None); a
+ * negative or shrinking length, a last_loc outside the pool or a free page id
+ * outside [0, num_pool_pages) raises PKV_DEVERR_RANGE, a last_loc at the wrong
+ * page offset PKV_DEVERR_CONTIG, and nothing is written either.
+ * Supported: batch <= 8192.  Asynchronous on `stream`.
+ */
+pkv_status pkv_alloc_extend(const int32_t *prefix_lens, const int32_t *seq_lens, const int32_t *last_loc,
+                            int32_t batch, int32_t page_size, int64_t num_pool_pages,
+                            const int32_t *free_pages, int64_t free_pages_len, int32_t *free_state,
+                            int32_t *out_cache_loc, int64_t out_cap, int32_t *err_flags,
+                            pkv_stream_t stream);
+
+/*
+ * pkv_write_req_to_token -- lay a step's slots into the requests' rows.
+ *
+ * write_cache_indices / write_req_to_token_pool (same page, "how those slot
+ * numbers are handed out"): for request b, columns kv_start[b] + [0,
+ * prefix_lens[b]) of row req_pool_idx[b] receive prefix_slots[b][0 ..
+ * prefix_lens[b]) (the reused prefix; a NULL entry, or prefix_slots NULL, leaves
+ * those columns as they are), and columns kv_start[b] + [prefix_lens[b],
+ * seq_lens[b]) receive out_cache_loc[e_b ..], e_b being the sum of
+ * seq_lens - prefix_lens over the requests before b.  prefix_slots is a device
+ * array of device pointers.  kv_start may be NULL (0).  A request whose row or
+ * columns fall outside the table raises PKV_DEVERR_RANGE and is skipped.
+ */
+pkv_status pkv_write_req_to_token(int32_t *req_to_token, int64_t r2t_rows, int64_t r2t_row_stride,
+                                  int64_t r2t_width, const int32_t *req_pool_idx, const int32_t *kv_start,
+                                  const int32_t *prefix_lens, const int32_t *seq_lens,
+                                  const int32_t *const *prefix_slots, const int32_t *out_cache_loc,
+                                  int32_t batch, int32_t *err_flags, pkv_stream_t stream);
+
+/*
+ * pkv_encoder_merge -- gather encoder-cache blocks into positioned hidden rows.
+ *
+ * The Neuron encoder cache ("Read Path", "Merge Inside Compiled Graph"): the
+ * buffer holds [num_blocks, block_size] rows of row_bytes bytes (the last
+ * block is scratch); block slot i of the step names block block_ids[i], and
+ * positions [max_blocks, block_size] (int64) says where each of its tokens
+ * lands:
+ *     hidden[positions[i][j]] = buffer[block_ids[i]][j]   if 0 <= positions[i][j] < num_tokens
+ * A position at or past num_tokens is the sentinel (a don't-care: nothing is
+ * written, the pages' discarded dummy row).  A negative position, or a block id
+ * outside [0, num_blocks) for a non-sentinel position, raises PKV_DEVERR_RANGE
+ * and that entry is skipped.  hidden rows are hidden_row_stride_bytes apart.
+ * filled (device uint64, nullable) is incremented by the number of rows
+ * written, for the fail-loud check that every scheduled position was filled;
+ * zero it before the call.  Positions are expected to be distinct.
+ */
+pkv_status pkv_encoder_merge(const void *buffer, int64_t num_blocks, int64_t block_size, int64_t row_bytes,
+                             const int32_t *block_ids, const int64_t *positions, int64_t max_blocks,
+                             void *hidden, int64_t num_tokens, int64_t hidden_row_stride_bytes,
+                             uint64_t *filled, int32_t *err_flags, pkv_stream_t stream);
+
 /* Static description of a status code. */
 const char *pkv_status_string(pkv_status status);
 

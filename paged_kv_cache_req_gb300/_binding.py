@@ -22,8 +22,8 @@ PKV_KIND_GQA, PKV_KIND_MLA = 0, 1
 PKV_LAYOUT_CSR, PKV_LAYOUT_BLOCK_TABLE, PKV_LAYOUT_VARLEN = 0, 1, 2
 
 EXPORTED_SYMBOLS = ("pkv_build_indices", "pkv_store", "pkv_decode", "pkv_decode_workspace_size",
-                    "pkv_decode_no_alloc", "pkv_ragged_gather", "pkv_status_string", "pkv_last_error",
-                    "pkv_abi_version")
+                    "pkv_decode_no_alloc", "pkv_ragged_gather", "pkv_alloc_extend", "pkv_write_req_to_token",
+                    "pkv_encoder_merge", "pkv_status_string", "pkv_last_error", "pkv_abi_version")
 
 
 class PkvError(RuntimeError):
@@ -69,6 +69,11 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
     lib.pkv_ragged_gather.argtypes = [P, P, I64, I64, I64, P, I64, I64, I64, P, P, P, I32, I32, P, P, I64, P, P, P]
     for f in ("pkv_build_indices", "pkv_store", "pkv_decode", "pkv_decode_no_alloc", "pkv_ragged_gather"):
         getattr(lib, f).restype = ctypes.c_int
+    lib.pkv_alloc_extend.argtypes = [P, P, P, I32, I32, I64, P, I64, P, P, I64, P, P]
+    lib.pkv_write_req_to_token.argtypes = [P, I64, I64, I64, P, P, P, P, P, P, I32, P, P]
+    lib.pkv_encoder_merge.argtypes = [P, I64, I64, I64, P, P, I64, P, I64, I64, P, P, P]
+    for fn in (lib.pkv_alloc_extend, lib.pkv_write_req_to_token, lib.pkv_encoder_merge):
+        fn.restype = ctypes.c_int
     lib.pkv_status_string.argtypes = [ctypes.c_int]
     lib.pkv_status_string.restype = ctypes.c_char_p
     lib.pkv_last_error.argtypes = []
@@ -192,6 +197,49 @@ def pkv_ragged_gather(k_pool, v_pool, req_to_token, req_pool_idx, seq_lens, max_
                                 _p(v_out), k_out.shape[0], _p(_i32(cu_seqlens, "cu_seqlens")), _p(err_flags),
                                 _stream(stream))
     _check(st, "pkv_ragged_gather")
+
+
+def pkv_alloc_extend(prefix_lens, seq_lens, last_loc, page_size, num_pool_pages, free_pages, free_state,
+                     out_cache_loc, err_flags, stream=None):
+    """Device page allocation for one step; free_state is a device int32 [2] = {head, count}."""
+    B = seq_lens.numel()
+    st = _lib.pkv_alloc_extend(_p(_i32(prefix_lens, "prefix_lens")), _p(_i32(seq_lens, "seq_lens")),
+                               _p(_i32(last_loc, "last_loc")), B, int(page_size), int(num_pool_pages),
+                               _p(_i32(free_pages, "free_pages")), free_pages.numel(),
+                               _p(_i32(free_state, "free_state")), _p(_i32(out_cache_loc, "out_cache_loc")),
+                               out_cache_loc.numel(), _p(err_flags), _stream(stream))
+    _check(st, "pkv_alloc_extend")
+
+
+def pkv_write_req_to_token(req_to_token, req_pool_idx, prefix_lens, seq_lens, out_cache_loc, err_flags,
+                           prefix_slots=None, kv_start=None, stream=None):
+    """prefix_slots: None, or a device int64 tensor [B] of device pointers (0 = leave the prefix as is)."""
+    B = seq_lens.numel()
+    if prefix_slots is not None and (prefix_slots.dtype != torch.int64 or prefix_slots.numel() != B):
+        raise ValueError("prefix_slots must be an int64 tensor of B device pointers")
+    st = _lib.pkv_write_req_to_token(_p(_i32(req_to_token, "req_to_token")), req_to_token.shape[0],
+                                     req_to_token.stride(0), req_to_token.shape[1],
+                                     _p(_i32(req_pool_idx, "req_pool_idx")), _p(_i32(kv_start, "kv_start")),
+                                     _p(_i32(prefix_lens, "prefix_lens")), _p(_i32(seq_lens, "seq_lens")),
+                                     _p(prefix_slots), _p(_i32(out_cache_loc, "out_cache_loc")), B, _p(err_flags),
+                                     _stream(stream))
+    _check(st, "pkv_write_req_to_token")
+
+
+def pkv_encoder_merge(buffer, block_ids, positions, hidden, err_flags, filled=None, stream=None):
+    """buffer [num_blocks, block_size, ...], positions int64 [max_blocks, block_size], hidden [num_tokens, ...]."""
+    if positions.dtype != torch.int64 or not positions.is_contiguous():
+        raise ValueError("positions must be a contiguous int64 tensor")
+    if not buffer.is_contiguous():
+        raise ValueError("buffer must be contiguous")
+    nb, bs = buffer.shape[0], buffer.shape[1]
+    row_bytes = buffer[0, 0].numel() * buffer.element_size()
+    if hidden[0].numel() * hidden.element_size() != row_bytes or hidden.stride(-1) != 1:
+        raise ValueError("hidden rows must match the buffer's rows")
+    st = _lib.pkv_encoder_merge(_p(buffer), nb, bs, row_bytes, _p(_i32(block_ids, "block_ids")), _p(positions),
+                                block_ids.numel(), _p(hidden), hidden.shape[0], hidden.stride(0) * hidden.element_size(),
+                                _p(filled), _p(err_flags), _stream(stream))
+    _check(st, "pkv_encoder_merge")
 
 
 def pkv_status_string(status: int) -> str:

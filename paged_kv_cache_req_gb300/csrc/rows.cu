@@ -1,5 +1,6 @@
-// Row movement: pkv_store (scatter new K/V rows into pool slots) and
-// pkv_ragged_gather (pack token-granular K/V rows into contiguous varlen buffers).
+// Row movement: pkv_store (scatter new K/V rows into pool slots),
+// pkv_ragged_gather (pack token-granular K/V rows into contiguous varlen buffers)
+// and pkv_encoder_merge (gather encoder-cache blocks into positioned hidden rows).
 //
 // Both are pure indexed copies of whole rows.  One warp moves one row with
 // 16-byte vector accesses (the mini-sglang store kernel's "one warp per token,
@@ -99,6 +100,58 @@ ragged_gather_kernel(const uint16_t *__restrict__ k_pool, const uint16_t *__rest
     }
 }
 
+constexpr int kMergeThreads = 256;
+
+// One warp per (block slot i, token j) of the position map: position
+// positions[i][j] in [0, num_tokens) receives row j of block block_ids[i];
+// sentinel positions (>= num_tokens) write nothing.  Rows move as 16-byte
+// streaming vectors, four per lane in flight (or bytes when unaligned).
+template <bool kVec>
+__global__ void __launch_bounds__(kMergeThreads, 4)
+encoder_merge_kernel(const uint8_t *__restrict__ buffer, int64_t num_blocks, int64_t block_size, int64_t row_bytes,
+                     const int32_t *__restrict__ block_ids, const int64_t *__restrict__ positions, int64_t entries,
+                     uint8_t *__restrict__ hidden, int64_t num_tokens, int64_t hidden_stride,
+                     unsigned long long *__restrict__ filled, int32_t *__restrict__ err) {
+    __shared__ int cnt;
+    if (threadIdx.x == 0) cnt = 0;
+    __syncthreads();
+    const int64_t e = static_cast<int64_t>(blockIdx.x) * (kMergeThreads / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (e < entries) {
+        const int64_t pos = positions[e];
+        if (pos < num_tokens) {
+            const int64_t i = e / block_size, j = e % block_size;
+            const int64_t blk = block_ids[i];
+            if (pos < 0 || blk < 0 || blk >= num_blocks) {
+                if (lane == 0) raise_flag(err, PKV_DEVERR_RANGE);
+            } else {
+                const uint8_t *src = buffer + (blk * block_size + j) * row_bytes;
+                uint8_t *dst = hidden + pos * hidden_stride;
+                if (kVec) {
+                    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+                    const int64_t n16 = row_bytes >> 4;
+                    int64_t k = lane;
+                    for (; k + 96 < n16; k += 128) {
+                        uint4 v[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) v[u] = ld_stream_16(s4 + k + 32 * u);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) st_stream_16(d4 + k + 32 * u, v[u]);
+                    }
+                    for (; k < n16; k += 32) st_stream_16(d4 + k, ld_stream_16(s4 + k));
+                } else {
+                    for (int64_t k = lane; k < row_bytes; k += 32) dst[k] = src[k];
+                }
+                if (lane == 0) atomicAdd(&cnt, 1);
+            }
+        }
+    }
+    if (!filled) return;
+    __syncthreads();
+    if (threadIdx.x == 0 && cnt) atomicAdd(filled, static_cast<unsigned long long>(cnt));
+}
+
 }  // namespace
 }  // namespace pkv
 
@@ -172,4 +225,33 @@ extern "C" pkv_status pkv_ragged_gather(const void *k_pool, const void *v_pool, 
             kp, vp, num_slots, pool_row_stride, row_elems, req_to_token, r2t_rows, r2t_row_stride, r2t_width,
             req_pool_idx, kv_start, seq_lens, batch, ko, vo, out_rows_cap, cu_seqlens, err_flags);
     return check_launch("pkv_ragged_gather");
+}
+
+extern "C" pkv_status pkv_encoder_merge(const void *buffer, int64_t num_blocks, int64_t block_size, int64_t row_bytes,
+                                        const int32_t *block_ids, const int64_t *positions, int64_t max_blocks,
+                                        void *hidden, int64_t num_tokens, int64_t hidden_row_stride_bytes,
+                                        uint64_t *filled, int32_t *err_flags, pkv_stream_t stream) {
+    using namespace pkv;
+    if (num_blocks < 0 || block_size < 0 || row_bytes < 0 || max_blocks < 0 || num_tokens < 0 ||
+        hidden_row_stride_bytes < row_bytes)
+        return fail(PKV_ERR_INVALID_ARG, "pkv_encoder_merge: negative or inconsistent size");
+    if (!err_flags) return fail(PKV_ERR_INVALID_ARG, "pkv_encoder_merge: err_flags is required");
+    const int64_t entries = max_blocks * block_size;
+    if (entries == 0 || row_bytes == 0) return ok();
+    if (!buffer || !block_ids || !positions || (num_tokens > 0 && !hidden))
+        return fail(PKV_ERR_INVALID_ARG, "pkv_encoder_merge: null input");
+    const int64_t grid = (entries + kMergeThreads / 32 - 1) / (kMergeThreads / 32);
+    if (grid > INT32_MAX) return fail(PKV_ERR_UNSUPPORTED, "pkv_encoder_merge: position map too large");
+    const bool vec = aligned(buffer, 16) && aligned(hidden, 16) && row_bytes % 16 == 0 && hidden_row_stride_bytes % 16 == 0;
+    auto s = reinterpret_cast<cudaStream_t>(stream);
+    auto *cnt = reinterpret_cast<unsigned long long *>(filled);
+    if (vec)
+        encoder_merge_kernel<true><<<static_cast<unsigned>(grid), kMergeThreads, 0, s>>>(
+            static_cast<const uint8_t *>(buffer), num_blocks, block_size, row_bytes, block_ids, positions, entries,
+            static_cast<uint8_t *>(hidden), num_tokens, hidden_row_stride_bytes, cnt, err_flags);
+    else
+        encoder_merge_kernel<false><<<static_cast<unsigned>(grid), kMergeThreads, 0, s>>>(
+            static_cast<const uint8_t *>(buffer), num_blocks, block_size, row_bytes, block_ids, positions, entries,
+            static_cast<uint8_t *>(hidden), num_tokens, hidden_row_stride_bytes, cnt, err_flags);
+    return check_launch("pkv_encoder_merge");
 }

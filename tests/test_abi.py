@@ -92,6 +92,24 @@ def test_host_side_validation_needs_no_gpu(binding):
     # gather: row stride smaller than a row
     assert lib.pkv_ragged_gather(None, None, 4, 4, 8, None, 1, 1, 1, None, None, None, 0, 0, None, None, 0,
                                  ctypes.byref(flag), ctypes.byref(flag), None) == binding.PKV_ERR_INVALID_ARG
+    # allocator: page size 0, missing free_state, too many requests; an empty step is a no-op
+    state = (ctypes.c_int32 * 2)(0, 0)
+    dummy = ctypes.c_void_p(16)
+    assert lib.pkv_alloc_extend(dummy, dummy, dummy, 1, 0, 8, dummy, 1, state, dummy, 1, ctypes.byref(flag),
+                                None) == binding.PKV_ERR_INVALID_ARG
+    assert lib.pkv_alloc_extend(dummy, dummy, dummy, 1, 16, 8, dummy, 1, None, dummy, 1, ctypes.byref(flag),
+                                None) == binding.PKV_ERR_INVALID_ARG
+    assert lib.pkv_alloc_extend(dummy, dummy, dummy, 9000, 16, 8, dummy, 1, state, dummy, 1, ctypes.byref(flag),
+                                None) == binding.PKV_ERR_UNSUPPORTED
+    assert lib.pkv_alloc_extend(None, None, None, 0, 16, 8, None, 0, state, None, 0, ctypes.byref(flag),
+                                None) == binding.PKV_OK
+    # row writer: stride narrower than the rows; encoder merge: hidden rows narrower than buffer rows
+    assert lib.pkv_write_req_to_token(dummy, 4, 8, 16, dummy, None, dummy, dummy, None, dummy, 1,
+                                      ctypes.byref(flag), None) == binding.PKV_ERR_INVALID_ARG
+    assert lib.pkv_encoder_merge(dummy, 4, 8, 64, dummy, dummy, 2, dummy, 10, 32, None, ctypes.byref(flag),
+                                 None) == binding.PKV_ERR_INVALID_ARG
+    assert lib.pkv_encoder_merge(None, 4, 8, 64, None, None, 0, None, 10, 64, None, ctypes.byref(flag),
+                                 None) == binding.PKV_OK
     assert flag.value == 0
 
 
