@@ -50,12 +50,16 @@ WORKLOAD_TEXT = {
     "llama3_8b": "Llama-3-8B-shaped large-batch decode: batch 256, cached lengths log-U[128,32768], 32 q / 8 kv heads x 128, page_size 64, groups of 16 share a 2048-token prefix",
     "whisper_encdec": "Whisper-large-shaped encoder-decoder step: batch 64, decoder lengths U[1,448] + cross-attention over 1500 encoder tokens, 20 heads x 64, page_size 16",
     "deepseek_v3_mla": "DeepSeek-V3-shaped MLA decode: batch 128, cached lengths U[512,16384], 128 q heads over a 512+64 latent, page_size 64",
+    "encoder_merge": "Qwen3-VL-32B-shaped encoder-cache read path: 30 cached 512x512 images (256 tokens each, one 512-row block each) of fat_dim 20480 bf16 gathered into an 8672-row prefill sequence",
 }
+MERGE_METRIC = "encoder-cache merge GB/s (bytes read + written)"
 
 
 # ---------------------------------------------------------------- accounting
-def step_bytes(wl, cross_mode="paged"):
-    """Algorithmic bytes of one step and of its decode launches (unique slots once)."""
+def step_bytes(wl, cross_mode="paged", alloc=False):
+    """Algorithmic bytes of one step and of its decode launches (unique slots once).
+    With device allocation: per request its lengths and last slot read, one slot
+    written to the output and one to its row, and the free-list pages taken."""
     r2t = wl.req_to_token.numpy()
     rpi = wl.req_pool_idx.numpy().astype(np.int64)
     if wl.kind == "mla":
@@ -82,6 +86,9 @@ def step_bytes(wl, cross_mode="paged"):
             total += dec + int(lens.sum()) * 4 + pages * 4        # table read + page-list write
         if p.stores:
             total += 2 * wl.batch * store_row                   # read new rows + write pool rows
+            if alloc:
+                new_pages = int((lens % wl.page_size == 1).sum()) if wl.page_size > 1 else wl.batch
+                total += wl.batch * (3 * 4 + 4 + 4) + new_pages * 4
     return total, decode
 
 
@@ -273,10 +280,168 @@ def dist_env():
     return world, rank, local
 
 
+# ---------------------------------------------------------------- encoder-cache merge
+def merge_oracle_pass(mw, buf_bits, hidden_bits):
+    """One oracle merge of the whole step on host copies; returns (seconds, rows)."""
+    import oracle
+    t0 = time.perf_counter()
+    st, filled = oracle.encoder_merge(buf_bits, mw.block_ids, mw.positions, hidden_bits)
+    secs = time.perf_counter() - t0
+    if st != oracle.OK or filled != mw.rows_moved:
+        raise SystemExit("oracle merge failed: status %d, %d rows" % (st, filled))
+    return secs, filled
+
+
+def merge_bytes(mw):
+    return mw.rows_moved * mw.row_bytes * 2 + mw.positions.nbytes + mw.block_ids.nbytes
+
+
+def reference_merge(args, world):
+    from paged_kv_cache_req_gb300.workloads import fill_merge_buffers, make_encoder_merge
+    import oracle
+    oracle.build()
+    mw = make_encoder_merge(seed=args.seed)
+    buf, hidden = fill_merge_buffers(mw)
+    bb = buf.view(torch.int16).numpy().view(np.uint16)
+    hb = hidden.view(torch.int16).numpy().view(np.uint16)
+    for _ in range(args.warmup):
+        merge_oracle_pass(mw, bb, hb)
+    times = [merge_oracle_pass(mw, bb, hb)[0] for _ in range(args.steps)]
+    value = merge_bytes(mw) * len(times) / sum(times) / 1e9
+    desc = "whole step: %d rows of %d B gathered by the byte-copy oracle on 1 host thread" % (
+        mw.rows_moved, mw.row_bytes)
+    line = {"impl": "reference", "metric": MERGE_METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * sum(times) / len(times), 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT["encoder_merge"], "name": "encoder_merge"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_merge(args, world, rank, local, dist):
+    """One step = one pkv_encoder_merge of the whole prefill's cached images."""
+    from paged_kv_cache_req_gb300 import _binding as B
+    from paged_kv_cache_req_gb300.workloads import fill_merge_buffers, make_encoder_merge
+    mw = make_encoder_merge(seed=args.seed)
+    dev = torch.device("cuda", local)
+    buf, hidden = fill_merge_buffers(mw, device=dev)
+    bid = torch.from_numpy(mw.block_ids).to(dev)
+    pos = torch.from_numpy(mw.positions).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    filled = torch.zeros(1, dtype=torch.int64, device=dev)
+    nbytes = merge_bytes(mw)
+    flush = nbytes < 4 * L2_BYTES
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    stream = torch.cuda.current_stream()
+
+    def step():
+        B.pkv_encoder_merge(buf, bid, pos, hidden, err, filled=filled)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if err.item() or filled.item() != args.warmup * mw.rows_moved:
+        raise SystemExit("merge check failed: err %d, filled %d" % (err.item(), filled.item()))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local, enabled=not args.profile_run)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        if flush:
+            flush_buf.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    soak = 0
+    if clocks.proc is not None and not args.profile_run and clocks.count() - clocks.start_count < 5:
+        t_soak = time.perf_counter()
+        while clocks.count() - clocks.start_count < 5 and time.perf_counter() - t_soak < 3.0:
+            for _ in range(max(1, args.steps)):
+                step()
+                soak += 1
+            torch.cuda.synchronize()
+    clk = clocks.stop()
+    if clk is not None:
+        clk["window"] = "timed region" + (" + %d untimed steps of the same load" % soak if soak else "")
+    tot_ms = reduce_max(sum(a.elapsed_time(b) for a, b in ev), dist, "cuda")
+    value = weak_scaling_gbs(world, nbytes, args.steps, tot_ms)
+    if args.profile_run:
+        if rank == 0:
+            print(json.dumps({"profile_run": True, "workload": "encoder_merge", "ms_per_step": round(tot_ms / args.steps, 4)}))
+        return 0
+    # end to end: the step's index inputs from pinned host memory, the filled count back
+    h_bid, h_pos = torch.from_numpy(mw.block_ids).pin_memory(), torch.from_numpy(mw.positions).pin_memory()
+    h_filled = torch.zeros(1, dtype=torch.int64).pin_memory()
+    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        if flush:
+            flush_buf.zero_()
+        e_ev[i][0].record(stream)
+        bid.copy_(h_bid, non_blocking=True)
+        pos.copy_(h_pos, non_blocking=True)
+        filled.zero_()
+        step()
+        h_filled.copy_(filled, non_blocking=True)
+        e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if int(h_filled.item()) != mw.rows_moved or err.item():
+        raise SystemExit("merge check failed in the end-to-end pass")
+    e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in e_ev), dist, "cuda")
+    if rank != 0:
+        return 0
+    hbm, _, _, peak_kind = measured_peaks()
+    avg_ms = tot_ms / args.steps
+    achieved = nbytes / (avg_ms / 1e3) / 1e9
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        bb = buf.cpu().view(torch.int16).numpy().view(np.uint16)
+        hb = hidden.cpu().view(torch.int16).numpy().view(np.uint16)
+        tot_s, passes = 0.0, 0
+        while passes < 20 and (tot_s < 3.0 or passes == 0):
+            tot_s += merge_oracle_pass(mw, bb, hb)[0]
+            passes += 1
+        cpu = {"value": round(nbytes * passes / tot_s / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": "whole step (%d rows of %d B); %d pass(es), %.1f s on 1 host thread" % (
+                   mw.rows_moved, mw.row_bytes, passes, tot_s), "host_cpus": os.cpu_count()}
+    line = {
+        "metric": MERGE_METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(avg_ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT["encoder_merge"], "name": "encoder_merge", "items": mw.items,
+                   "rows_moved": mw.rows_moved, "row_bytes": mw.row_bytes, "num_blocks": mw.num_blocks,
+                   "num_tokens": mw.num_tokens, "algorithmic_bytes_per_step": nbytes,
+                   "l2": "flushed between steps (2x L2 write)" if flush else "inputs larger than L2",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": "pkv_encoder_merge", "achieved": round(achieved, 2), "peak": hbm,
+                     "unit": "GB/s", "frac": round(achieved / hbm, 4), "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": round(avg_ms, 4), "traffic": None},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(weak_scaling_gbs(world, nbytes, args.steps, e_ms), 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(mw.block_ids.nbytes + mw.positions.nbytes), "d2h_bytes_per_step": 8,
+                "ms_per_step": round(e_ms / args.steps, 4)},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
+    if args.workload == "encoder_merge":
+        return reference_merge(args, world)
     from paged_kv_cache_req_gb300.workloads import make_workload
     wl = make_workload(args.workload, batch=args.batch)
     import oracle
@@ -319,9 +484,12 @@ def run_ours(args):
     from paged_kv_cache_req_gb300.engine import DecodeStep
     from paged_kv_cache_req_gb300.workloads import make_workload
 
+    if args.workload == "encoder_merge":
+        return run_merge(args, world, rank, local, dist)
     wl = make_workload(args.workload, seed=args.seed, batch=args.batch)
-    step = DecodeStep(wl, device="cuda", cross_mode=args.cross_mode, kv_chunk=args.kv_chunk, seed=args.seed)
-    total_bytes, decode_bytes = step_bytes(wl, args.cross_mode)
+    step = DecodeStep(wl, device="cuda", cross_mode=args.cross_mode, kv_chunk=args.kv_chunk, seed=args.seed,
+                      alloc=args.alloc)
+    total_bytes, decode_bytes = step_bytes(wl, args.cross_mode, alloc=args.alloc)
     flush = total_bytes < 4 * L2_BYTES
     flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda") if flush else None
     stream = torch.cuda.current_stream()
@@ -346,6 +514,8 @@ def run_ours(args):
         if flush:
             flush_buf.zero_()
         ev[i][0].record(stream)
+        if step.alloc:
+            step.allocate()
         for j, (name, pb) in enumerate(step.problems.items()):
             if pb.gather:
                 step.gather(name)
@@ -447,6 +617,8 @@ def run_ours(args):
         "decode_steps_per_s": round(world * 1e3 / ms_per_step, 2),
         "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "batch": wl.batch,
                    "cross_mode": args.cross_mode if wl.kind == "gqa" and len(wl.problems) > 1 else None,
+                   "new_slots": "allocated on the device each step (pkv_alloc_extend + pkv_write_req_to_token)"
+                   if args.alloc else "given by the workload",
                    "keys_per_step": {k: v[0] for k, v in keys.items()},
                    "unique_keys_per_step": {k: v[1] for k, v in keys.items()},
                    "algorithmic_bytes_per_step": total_bytes,
@@ -482,6 +654,8 @@ def main(argv=None):
     ap.add_argument("--kv-chunk", type=int, default=0)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--alloc", action="store_true",
+                    help="allocate each step's new slots on the device (pkv_alloc_extend + pkv_write_req_to_token)")
     ap.add_argument("--profile-run", action="store_true",
                     help="only warm-up + timed steps (for ncu); prints a short line")
     ap.add_argument("--batch", type=int, default=None, help="smaller batch of the same recipe (profiling)")

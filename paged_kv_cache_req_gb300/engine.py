@@ -8,6 +8,15 @@ calls on the current stream:
     pkv_store           this step's new K/V rows -> their pool slots
     pkv_decode          attention of every request's new token over its pages
 
+With ``alloc=True`` the new token's slot is not taken from the workload but
+allocated on the device first, as a serving loop would:
+
+    pkv_alloc_extend        each request grows by one position: the slot after
+                            its last one, or a fresh page from the free list
+    pkv_write_req_to_token  that slot into the request's row of req_to_token
+
+(the free list is restored before every step, so steps stay idempotent).
+
 For an encoder-decoder workload the cross-attention over the encoder region
 runs either through its own page list ("paged": the page-aligned encoder of
 "Approach 1") or through pkv_ragged_gather into a contiguous varlen buffer
@@ -19,6 +28,7 @@ from __future__ import annotations
 
 from typing import Dict, Optional
 
+import numpy as np
 import torch
 
 from . import _binding as B
@@ -33,7 +43,8 @@ class _ProblemBuffers:
 
 class DecodeStep:
     def __init__(self, wl: Workload, device="cuda", cross_mode: str = "paged", kv_chunk: int = 0,
-                 pools=None, values: Optional[Dict[str, torch.Tensor]] = None, seed: Optional[int] = None):
+                 pools=None, values: Optional[Dict[str, torch.Tensor]] = None, seed: Optional[int] = None,
+                 alloc: bool = False):
         if cross_mode not in ("paged", "gather"):
             raise ValueError(cross_mode)
         self.wl = wl
@@ -92,6 +103,55 @@ class DecodeStep:
             pb.ws_bytes = nbytes
             pb.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
             self.problems[p.name] = pb
+        self.alloc = bool(alloc)
+        if self.alloc:
+            self._setup_alloc(seed)
+
+    def _setup_alloc(self, seed):
+        """Free list = the pool pages no cached position uses (page 0 is padding), in a
+        seeded order; each request grows from its cached length by one position."""
+        wl = self.wl
+        ps = wl.page_size
+        r2t = wl.req_to_token.numpy()
+        rpi = wl.req_pool_idx.numpy().astype(np.int64)
+        names = [n for n, pb in self.problems.items() if pb.spec.stores]
+        if len(names) != 1:
+            raise ValueError("device allocation needs exactly one problem that stores new tokens")
+        self.alloc_problem = names[0]
+        used = [np.zeros(1, dtype=np.int64)]
+        for pb in self.problems.values():
+            lens = pb.spec.seq_lens.numpy().astype(np.int64)
+            starts = pb.spec.kv_start.numpy().astype(np.int64)
+            cached = lens - 1 if pb.spec.stores else lens
+            for b in range(wl.batch):
+                used.append(r2t[rpi[b], starts[b]:starts[b] + cached[b]].astype(np.int64) // ps)
+        used_pages = np.unique(np.concatenate(used))
+        free = np.setdiff1d(np.arange(wl.num_pool_pages, dtype=np.int64), used_pages)
+        free = np.random.default_rng(0 if seed is None else seed).permutation(free).astype(np.int32)
+        spec = self.problems[self.alloc_problem].spec
+        lens = spec.seq_lens.numpy().astype(np.int64)
+        starts = spec.kv_start.numpy().astype(np.int64)
+        prefix = lens - 1
+        last = np.array([r2t[rpi[b], starts[b] + prefix[b] - 1] if prefix[b] > 0 else -1
+                         for b in range(wl.batch)], dtype=np.int32)
+        dev = self.device
+        self.free_pages = torch.from_numpy(free).to(dev)
+        self.free_state0 = torch.tensor([0, len(free)], dtype=torch.int32, device=dev)
+        self.free_state = self.free_state0.clone()
+        self.prefix_lens = torch.from_numpy(prefix.astype(np.int32)).to(dev)
+        self.last_loc = torch.from_numpy(last).to(dev)
+        self.out_cache_loc = torch.empty(wl.batch, dtype=torch.int32, device=dev)
+        self.problems[self.alloc_problem].slot_mapping = self.out_cache_loc
+
+    def allocate(self):
+        """This step's slots on the device: one position per request, then into the rows."""
+        wl = self.wl
+        pb = self.problems[self.alloc_problem]
+        self.free_state.copy_(self.free_state0, non_blocking=True)
+        B.pkv_alloc_extend(self.prefix_lens, pb.seq_lens, self.last_loc, wl.page_size, wl.num_pool_pages,
+                           self.free_pages, self.free_state, self.out_cache_loc, self.err)
+        B.pkv_write_req_to_token(self.r2t, self.req_pool_idx, self.prefix_lens, pb.seq_lens, self.out_cache_loc,
+                                 self.err, kv_start=pb.kv_start)
 
     # ------------------------------------------------------------------ steps
     def build_indices(self, name: str):
@@ -121,7 +181,9 @@ class DecodeStep:
         B.pkv_decode(pb.args, pb.workspace, self.err)
 
     def run(self):
-        """One decode step: for each problem, page lists, (store), (gather), attention."""
+        """One decode step: (allocation), then for each problem page lists, (store), (gather), attention."""
+        if self.alloc:
+            self.allocate()
         for name, pb in self.problems.items():
             if pb.gather:
                 self.gather(name)
@@ -133,7 +195,7 @@ class DecodeStep:
 
     def launches_per_step(self) -> int:
         """libpkv kernel launches one ``run()`` issues."""
-        n = 0
+        n = 2 if self.alloc else 0                  # alloc_extend + write_req_to_token
         for pb in self.problems.values():
             n += 1                                   # gather or build_indices
             n += 1 if pb.spec.stores else 0          # store
@@ -154,7 +216,10 @@ class DecodeStep:
         for name, pb in self.problems.items():
             h_in["q_" + name] = pb.q.cpu().pin_memory()
             h_in["seq_lens_" + name] = pb.seq_lens.cpu().pin_memory()
-            if pb.slot_mapping is not None:
+            if self.alloc and name == self.alloc_problem:
+                h_in["prefix_lens"] = self.prefix_lens.cpu().pin_memory()
+                h_in["last_loc"] = self.last_loc.cpu().pin_memory()
+            elif pb.slot_mapping is not None:
                 h_in["slot_mapping_" + name] = pb.slot_mapping.cpu().pin_memory()
             h_out[name] = torch.empty_like(pb.out, device="cpu").pin_memory()
         h_in["req_pool_idx"] = self.req_pool_idx.cpu().pin_memory()
@@ -169,7 +234,10 @@ class DecodeStep:
         for name, pb in self.problems.items():
             pb.q.copy_(h_in["q_" + name], non_blocking=True)
             pb.seq_lens.copy_(h_in["seq_lens_" + name], non_blocking=True)
-            if pb.slot_mapping is not None:
+            if self.alloc and name == self.alloc_problem:
+                self.prefix_lens.copy_(h_in["prefix_lens"], non_blocking=True)
+                self.last_loc.copy_(h_in["last_loc"], non_blocking=True)
+            elif pb.slot_mapping is not None:
                 pb.slot_mapping.copy_(h_in["slot_mapping_" + name], non_blocking=True)
         self.run()
         for name, pb in self.problems.items():

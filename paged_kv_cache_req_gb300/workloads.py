@@ -42,6 +42,9 @@ __all__ = [
     "fill_pool",
     "make_values",
     "round_up",
+    "MergeWorkload",
+    "make_encoder_merge",
+    "fill_merge_buffers",
 ]
 
 
@@ -316,3 +319,72 @@ def make_values(wl: Workload, seed: Optional[int] = None) -> dict:
         out["k_new"] = torch.randn((B, wl.num_kv_heads, wl.head_dim_qk), generator=gen).to(torch.bfloat16)
         out["v_new"] = torch.randn((B, wl.num_kv_heads, wl.head_dim_v), generator=gen).to(torch.bfloat16)
     return out
+
+
+# --------------------------------------------------------------------------
+# Encoder-cache merge (the Neuron encoder cache's read path)
+# --------------------------------------------------------------------------
+@dataclass
+class MergeWorkload:
+    """A prefill step's encoder-cache gather: `items` cached images, each one block of
+    `block_size` rows of `fat_dim` bf16 values, of which `tokens_per_item` are real;
+    the position map places them in a sequence of `num_tokens` rows."""
+    name: str
+    num_blocks: int          # cache blocks, the last one scratch
+    block_size: int
+    fat_dim: int
+    max_blocks: int          # fixed shape of the step's block-id / position inputs
+    num_tokens: int
+    items: int
+    tokens_per_item: int
+    block_ids: np.ndarray    # int32 [max_blocks]
+    positions: np.ndarray    # int64 [max_blocks, block_size]; num_tokens = sentinel
+    seed: int = 0
+
+    @property
+    def rows_moved(self) -> int:
+        return int((self.positions < self.num_tokens).sum())
+
+    @property
+    def row_bytes(self) -> int:
+        return self.fat_dim * 2
+
+
+def make_encoder_merge(seed: int = 0, items: int = 30, tokens_per_item: int = 256, fat_dim: int = 5120 * 4,
+                       block_size: int = 2048 // 4, cache_tokens: int = 16384, text_tokens: int = 16,
+                       lead_tokens: int = 512) -> MergeWorkload:
+    """Qwen3-VL-32B-shaped read path: fat_dim 5120 x (1 + 3 deepstack levels), blocks of
+    2048 / 4 = 512 post-merger tokens, one 512x512 image = 256 tokens per block, 30
+    images.  The cache holds ceil(cache_tokens / block_size) blocks + 1 scratch; the
+    step's fixed shape has room for all of them; unused slots name the scratch block
+    with sentinel positions.  The sequence is `lead_tokens` of text, then for every
+    image `text_tokens` of text followed by its image tokens."""
+    rng = np.random.default_rng(seed)
+    num_blocks = -(-cache_tokens // block_size) + 1
+    max_blocks = num_blocks - 1
+    if items > max_blocks:
+        raise ValueError("more items than cache blocks")
+    num_tokens = lead_tokens + items * (text_tokens + tokens_per_item)
+    block_ids = np.full(max_blocks, num_blocks - 1, dtype=np.int32)
+    block_ids[:items] = rng.permutation(num_blocks - 1)[:items]       # cache hits anywhere in the buffer
+    positions = np.full((max_blocks, block_size), num_tokens, dtype=np.int64)
+    for k in range(items):
+        start = lead_tokens + k * (text_tokens + tokens_per_item) + text_tokens
+        positions[k, :tokens_per_item] = np.arange(start, start + tokens_per_item)
+    return MergeWorkload(name="encoder_merge", num_blocks=num_blocks, block_size=block_size, fat_dim=fat_dim,
+                         max_blocks=max_blocks, num_tokens=num_tokens, items=items, tokens_per_item=tokens_per_item,
+                         block_ids=block_ids, positions=positions, seed=seed)
+
+
+def fill_merge_buffers(mw: MergeWorkload, device="cpu", chunk_elems: int = 1 << 28):
+    """bf16 N(0,1) cache buffer [num_blocks, block_size, fat_dim] and hidden rows [num_tokens, fat_dim]."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(3_000_017 + mw.seed)
+    out = []
+    for shape in ((mw.num_blocks, mw.block_size, mw.fat_dim), (mw.num_tokens, mw.fat_dim)):
+        t = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        flat = t.view(-1)
+        for i in range(0, flat.numel(), chunk_elems):
+            flat[i:i + chunk_elems].normal_(generator=gen)
+        out.append(t)
+    return out[0], out[1]

@@ -68,22 +68,27 @@ def compact(r2t: np.ndarray, rpi: np.ndarray, lens: np.ndarray, starts: np.ndarr
     return allslots, t, np.arange(1, len(sample) + 1, dtype=np.int32), relabel
 
 
-def oracle_decode_problem(step, name, sample, pre_k=None, pre_v=None, store=True):
+def oracle_decode_problem(step, name, sample, pre_k=None, pre_v=None, store=True, r2t=None, slot_mapping=None):
     """fp64 oracle output of one problem of a DecodeStep for the sampled requests.
 
     pre_k / pre_v: the pool rows as they were before the GPU step ran (host
     tensors indexed by slot), or None to read them now from the device (valid
     when the step does not store into this problem's rows, or before it runs).
-    The oracle applies the store itself, then decodes.
+    The oracle applies the store itself, then decodes.  r2t / slot_mapping
+    replace the workload's table and new-token slots (the oracle's own
+    allocation, for steps that allocate on the device).
     """
     wl = step.wl
     pb = step.problems[name]
-    r2t = wl.req_to_token.numpy()
+    r2t = wl.req_to_token.numpy() if r2t is None else r2t
     rpi = wl.req_pool_idx.numpy()
     lens = pb.spec.seq_lens.numpy()
     starts = pb.spec.kv_start.numpy()
     sample = list(sample)
-    new_slots = pb.spec.slot_mapping.numpy()[sample] if (store and pb.spec.stores) else []
+    new_slots = []
+    if store and pb.spec.stores:
+        sm_all = pb.spec.slot_mapping.numpy() if slot_mapping is None else np.asarray(slot_mapping)
+        new_slots = sm_all[sample]
     allslots, t, rpi_c, relabel = compact(r2t, rpi, lens, starts, sample, extra_slots=new_slots)
     idx = torch.from_numpy(allslots)
     src_k = pre_k if pre_k is not None else step.k_pool

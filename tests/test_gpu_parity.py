@@ -210,6 +210,42 @@ def test_decode_step_parity(B, name, sample_k):
         _check_decode(step, pname, sample, pre_k, pre_v)
 
 
+@pytest.mark.parametrize("name,sample_k", [("tiny_gqa", 4), ("qwen3_0p6b", 16), ("llama3_8b", 8),
+                                           ("whisper_encdec", 8), ("deepseek_v3_mla", 6)])
+def test_decode_step_with_device_allocation(B, name, sample_k):
+    """alloc_extend + write_req_to_token ahead of the step: slots, free-list state and the
+    whole table bit-exact against the oracle's own allocation, then attention against
+    the oracle on the oracle's table."""
+    kw = {"batch": 32} if name == "deepseek_v3_mla" else {}
+    step = _step(name, alloc=True, **kw)
+    wl = step.wl
+    pb = step.problems[step.alloc_problem]
+    prefix = step.prefix_lens.cpu().numpy()
+    last = step.last_loc.cpu().numpy()
+    free = step.free_pages.cpu().numpy()
+    pre_k = step.k_pool.clone()
+    pre_v = step.v_pool.clone() if step.v_pool is not None else None
+    step.run()
+    torch.cuda.synchronize()
+    assert step.check_errors() == 0
+    state = np.array([0, len(free)], np.int32)
+    seq = pb.spec.seq_lens.numpy()
+    st, loc = oracle.alloc_extend(prefix, seq, last, wl.page_size, wl.num_pool_pages, free, state)
+    assert st == oracle.OK
+    assert np.array_equal(step.out_cache_loc.cpu().numpy(), loc)
+    assert step.free_state.cpu().numpy().tolist() == state.tolist()
+    table = wl.req_to_token.numpy().copy()
+    assert oracle.write_req_to_token(table, wl.req_pool_idx.numpy(), prefix, seq, [None] * wl.batch, loc,
+                                     kv_start=pb.spec.kv_start.numpy()) == oracle.OK
+    assert np.array_equal(step.r2t.cpu().numpy(), table)
+    sample = _sample(wl.batch, sample_k, seed=4)
+    for pname in step.problems:
+        out, lse = oracle_decode_problem(step, pname, sample, pre_k=pre_k, pre_v=pre_v, r2t=table,
+                                         slot_mapping=loc if pname == step.alloc_problem else None)
+        assert_close(bf16_to_f64(step.problems[pname].out)[sample], out, "%s/%s out (allocated)" % (name, pname))
+        assert_close(step.problems[pname].lse.double().cpu().numpy()[sample], lse, "%s/%s lse" % (name, pname))
+
+
 def test_whisper_cross_attention_gather_mode(B):
     step = _step("whisper_encdec", cross_mode="gather")
     sample = _sample(step.wl.batch, 12, seed=1)
