@@ -68,6 +68,11 @@ def _load():
         lib.pkvo_write_req_to_token.restype = ctypes.c_int
         lib.pkvo_encoder_merge.argtypes = [P, I64, I64, I64, P, P, I64, P, I64, I64, P]
         lib.pkvo_encoder_merge.restype = ctypes.c_int
+        lib.pkvo_extend.argtypes = [P, I64, I32, P, P, I32, I32, I32, I32, P, I64, P, I64, I64, P, I64, I64, I64,
+                                    P, P, P, D, P, P, I32]
+        lib.pkvo_extend.restype = ctypes.c_int
+        lib.pkvo_span_plan.argtypes = [I32, P, P, P, P, P, P, P, I64]
+        lib.pkvo_span_plan.restype = ctypes.c_int
         lib.pkvo_max_threads.argtypes = []
         lib.pkvo_max_threads.restype = ctypes.c_int32
         _lib = lib
@@ -226,3 +231,45 @@ def encoder_merge(buffer: np.ndarray, block_ids, positions, hidden: np.ndarray):
     st = _load().pkvo_encoder_merge(_ptr(buffer), nb, bs, row_bytes, _ptr(bid), _ptr(pos), len(bid), _ptr(hidden),
                                     hidden.shape[0], hidden.strides[0], _ptr(filled))
     return st, int(filled[0])
+
+
+def extend(q, k_pool, v_pool, req_to_token, req_pool_idx, seq_lens, qo_indptr, kv_end, scale, kv_start=None,
+           num_threads=0):
+    """fp64 multi-query attention: q [total_q, Hq, D] uint16 (bf16 bits), query row j of request b
+    (qo_indptr[b] <= j < qo_indptr[b+1]) sees keys [0, kv_end[j]).  Returns (status, out, lse)."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    k = np.ascontiguousarray(k_pool, dtype=np.uint16)
+    v = np.ascontiguousarray(v_pool, dtype=np.uint16)
+    T, hq, dqk = q.shape
+    hkv, dv = k.shape[1], v.shape[2]
+    r2t = _i32(req_to_token)
+    rpi, sl, ks, qi, ke = _i32(req_pool_idx), _i32(seq_lens), _i32(kv_start), _i32(qo_indptr), _i32(kv_end)
+    out = np.zeros((T, hq, dv), dtype=np.float64)
+    lse = np.zeros((T, hq), dtype=np.float64)
+    st = _load().pkvo_extend(_ptr(q), T, len(sl), _ptr(qi), _ptr(ke), hq, hkv, dqk, dv, _ptr(k), k.shape[1] * k.shape[2],
+                             _ptr(v), v.shape[1] * v.shape[2], k.shape[0], _ptr(r2t), r2t.shape[0], r2t.shape[1],
+                             r2t.shape[1], _ptr(rpi), _ptr(ks), _ptr(sl), float(scale), _ptr(out), _ptr(lse),
+                             int(num_threads))
+    return st, out, lse
+
+
+def span_plan(segments, cap=None):
+    """segments: per request a list of (kind, start, end), kind 0 = causal, 1 = full.
+    Returns (status, qo_indptr, q_pos, kv_end)."""
+    B = len(segments)
+    ind = np.zeros(B + 1, dtype=np.int32)
+    kinds, starts, ends = [], [], []
+    for b, segs in enumerate(segments):
+        for kd, a, e in segs:
+            kinds.append(kd)
+            starts.append(a)
+            ends.append(e)
+        ind[b + 1] = len(kinds)
+    total = sum(max(e - a, 0) for segs in segments for _, a, e in segs)
+    cap = total if cap is None else int(cap)
+    qo = np.zeros(B + 1, dtype=np.int32)
+    qp = np.zeros(max(cap, 1), dtype=np.int32)
+    ke = np.zeros(max(cap, 1), dtype=np.int32)
+    st = _load().pkvo_span_plan(B, _ptr(ind), _ptr(_i32(kinds or [0])), _ptr(_i32(starts or [0])),
+                                _ptr(_i32(ends or [0])), _ptr(qo), _ptr(qp), _ptr(ke), cap)
+    return st, qo, qp[:total], ke[:total]

@@ -399,6 +399,115 @@ int pkvo_encoder_merge(const uint8_t *buffer, int64_t num_blocks, int64_t block_
     return status;
 }
 
+/*
+ * Multi-query attention through the page table (extend / chunked prefill,
+ * speculative target-verify, and the mixed causal/full segments of the
+ * diffusion KV path).  Query row j (qo_indptr[b] <= j < qo_indptr[b+1]) belongs
+ * to request b and sees the keys t in [0, kv_end[j]) of that request's row,
+ * slot req_to_token[row, kv_start + t] ([P1 "From slots to a page table"]);
+ * for query head h, with kh = h / (Hq / Hkv):
+ *     x_t = scale * q[j,h,:] . K[slot_t, kh, :]
+ *     out[j,h,:] = sum_t exp(x_t - m) V[slot_t, kh, :] / sum_t exp(x_t - m),  lse = m + ln sum
+ * A causal extend over the last n positions of an L-key request has
+ * kv_end = L - n + i + 1 for its i-th query row (AttentionBackend notes: extend
+ * with qo_indptr, target-verify with draft tokens); a full segment [a, b) gives
+ * its rows kv_end = b (vllm-omni "Attention execution").  kv_end outside
+ * [0, L] is PKVO_ERR_RANGE; kv_end = 0 gives out = 0, lse = -inf.
+ */
+int pkvo_extend(const uint16_t *q, int64_t total_q, int32_t batch, const int32_t *qo_indptr, const int32_t *kv_end,
+                int32_t hq, int32_t hkv, int32_t dqk, int32_t dv, const uint16_t *k_pool, int64_t k_row_stride,
+                const uint16_t *v_pool, int64_t v_row_stride, int64_t num_slots, const int32_t *r2t, int64_t num_rows,
+                int64_t row_stride, int64_t row_width, const int32_t *req_pool_idx, const int32_t *kv_start,
+                const int32_t *seq_lens, double scale, double *out, double *lse, int32_t num_threads) {
+    if (hkv <= 0 || hq % hkv != 0 || batch < 0) return PKVO_ERR_ARG;
+    if (batch > 0 && (qo_indptr[0] != 0 || qo_indptr[batch] != total_q)) return PKVO_ERR_ARG;
+    const int32_t g = hq / hkv;
+    int status = PKVO_OK;
+    const int64_t pairs = total_q * hq;
+#ifdef _OPENMP
+    if (num_threads <= 0) num_threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads) reduction(max : status)
+#endif
+    for (int64_t jh = 0; jh < pairs; ++jh) {
+        const int64_t j = jh / hq, h = jh % hq, kh = h / g;
+        int32_t b = 0;   /* the request owning query row j */
+        while (b + 1 < batch && qo_indptr[b + 1] <= j) ++b;
+        double *o = out + jh * dv;
+        for (int32_t d = 0; d < dv; ++d) o[d] = 0.0;
+        const int64_t row = req_pool_idx[b], start = kv_start ? kv_start[b] : 0, len = seq_lens[b];
+        const int64_t te = kv_end[j];
+        if (row < 0 || row >= num_rows || start < 0 || len < 0 || start + len > row_width || te < 0 || te > len) {
+            status = PKVO_ERR_RANGE;
+            if (lse) lse[jh] = -INFINITY;
+            continue;
+        }
+        if (te == 0) {
+            if (lse) lse[jh] = -INFINITY;
+            continue;
+        }
+        double *x = (double *)malloc(sizeof(double) * (size_t)te);
+        const uint16_t *qv = q + jh * dqk;
+        int bad = 0;
+        for (int64_t t = 0; t < te; ++t) {
+            const int64_t slot = r2t[row * row_stride + start + t];
+            if (slot < 0 || slot >= num_slots) { bad = 1; break; }
+            const uint16_t *kr = k_pool + slot * k_row_stride + kh * dqk;
+            double acc = 0.0;
+            for (int32_t d = 0; d < dqk; ++d) acc += widen_bf16(qv[d]) * widen_bf16(kr[d]);
+            x[t] = scale * acc;
+        }
+        if (bad) {
+            free(x);
+            status = PKVO_ERR_RANGE;
+            continue;
+        }
+        double m = -INFINITY;
+        for (int64_t t = 0; t < te; ++t) m = x[t] > m ? x[t] : m;
+        double den = 0.0;
+        for (int64_t t = 0; t < te; ++t) {
+            const double w = exp(x[t] - m);
+            const int64_t slot = r2t[row * row_stride + start + t];
+            const uint16_t *vr = v_pool + slot * v_row_stride + kh * dv;
+            for (int32_t d = 0; d < dv; ++d) o[d] += w * widen_bf16(vr[d]);
+            den += w;
+        }
+        for (int32_t d = 0; d < dv; ++d) o[d] /= den;
+        if (lse) lse[jh] = m + log(den);
+        free(x);
+    }
+    return status;
+}
+
+/*
+ * Query rows and key bounds of a row's attention segments (vllm-omni diffusion
+ * KV, "Attention execution"): request b's segments seg_indptr[b] ..
+ * seg_indptr[b+1]-1, each (kind, start, end) over positions [start, end) of
+ * its sequence: a causal segment's position p sees keys [0, p + 1), a full
+ * segment's positions see [0, end).  The query rows of b are its segments'
+ * positions in order: q_pos[j] = p, kv_end[j] = the bound above, rows counted
+ * from qo_indptr[b] (qo_indptr[0] = 0, qo_indptr[b+1] = qo_indptr[b] + the
+ * lengths of b's segments).  end < start, start < 0 or more rows than cap is an
+ * error.
+ */
+int pkvo_span_plan(int32_t batch, const int32_t *seg_indptr, const int32_t *seg_kind, const int32_t *seg_start,
+                   const int32_t *seg_end, int32_t *qo_indptr, int32_t *q_pos, int32_t *kv_end, int64_t cap) {
+    int64_t j = 0;
+    qo_indptr[0] = 0;
+    for (int32_t b = 0; b < batch; ++b) {
+        for (int32_t s = seg_indptr[b]; s < seg_indptr[b + 1]; ++s) {
+            const int64_t a = seg_start[s], e = seg_end[s];
+            if (a < 0 || e < a || (seg_kind[s] != 0 && seg_kind[s] != 1)) return PKVO_ERR_RANGE;
+            if (j + (e - a) > cap) return PKVO_ERR_CAPACITY;
+            for (int64_t p = a; p < e; ++p, ++j) {
+                q_pos[j] = (int32_t)p;
+                kv_end[j] = (int32_t)(seg_kind[s] == 0 ? p + 1 : e);
+            }
+        }
+        qo_indptr[b + 1] = (int32_t)j;
+    }
+    return PKVO_OK;
+}
+
 /* Threads the decode would use (reported beside CPU-baseline timings). */
 int32_t pkvo_max_threads(void) {
 #ifdef _OPENMP

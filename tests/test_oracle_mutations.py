@@ -21,12 +21,13 @@ SRC = os.path.join(ROOT, "oracle", "pkv_oracle.c")
 # (name, text in the source, replacement, how many occurrences to replace; 0 = all).
 # A deleted statement is replaced by ";" so that the surrounding code keeps its shape.
 MUTANTS = [
-    ("interleaved_kv_head", "kh = h / g;", "kh = h % hkv;", 1),
+    ("interleaved_kv_head", "const int64_t b = bh / hq, h = bh % hq, kh = h / g;",
+     "const int64_t b = bh / hq, h = bh % hq, kh = h % hkv;", 1),
     ("dropped_scale", "x[t - t0] = scale * acc;", "x[t - t0] = acc;", 1),
     ("shared_query_row", "q + bh * dqk", "q + b * dqk", 1),
-    ("v_offset_uses_dqk", "v_pool + slot * v_row_stride + kh * dv", "v_pool + slot * v_row_stride + kh * dqk", 1),
-    ("decode_ignores_kv_start", "r2t[row * row_stride + start + t];\n            if (slot < 0 || slot >= num_slots) { bad",
-     "r2t[row * row_stride + t];\n            if (slot < 0 || slot >= num_slots) { bad", 1),
+    ("v_offset_uses_dqk", "v_pool + slot * v_row_stride + kh * dv", "v_pool + slot * v_row_stride + kh * dqk", 0),
+    ("decode_ignores_kv_start", "for (int64_t t = t0; t < t1; ++t) {\n            const int64_t slot = r2t[row * row_stride + start + t];",
+     "for (int64_t t = t0; t < t1; ++t) {\n            const int64_t slot = r2t[row * row_stride + t];", 1),
     ("lse_without_max", "if (lse) lse[bh] = m + log(den);", "if (lse) lse[bh] = log(den);", 1),
     ("empty_lse_zero", "if (lse) lse[bh] = -INFINITY;", "if (lse) lse[bh] = 0.0;", 1),
     ("merge_sign", "const double w = exp(l - m);", "const double w = exp(m - l);", 1),
@@ -51,6 +52,11 @@ MUTANTS = [
     ("write_new_slots_not_offset", "for (int64_t t = p; t < s; ++t) r[t] = out_cache_loc[e + (t - p)];",
      "for (int64_t t = p; t < s; ++t) r[t] = out_cache_loc[t - p];", 1),
     ("merge_ignores_block_ids", "buffer + (blk * block_size + j) * row_bytes", "buffer + (i * block_size + j) * row_bytes", 1),
+    ("extend_bound_off_by_one", "        for (int64_t t = 0; t < te; ++t) {\n            const int64_t slot = r2t[row * row_stride + start + t];\n            if (slot < 0 || slot >= num_slots) { bad = 1; break; }",
+     "        for (int64_t t = 0; t < te - (te > 1); ++t) {\n            const int64_t slot = r2t[row * row_stride + start + t];\n            if (slot < 0 || slot >= num_slots) { bad = 1; break; }", 1),
+    ("extend_head_mapping", "const int64_t j = jh / hq, h = jh % hq, kh = h / g;", "const int64_t j = jh / hq, h = jh % hq, kh = h % hkv;", 1),
+    ("span_causal_bound", "kv_end[j] = (int32_t)(seg_kind[s] == 0 ? p + 1 : e);", "kv_end[j] = (int32_t)(seg_kind[s] == 0 ? p : e);", 1),
+    ("span_full_bound", "kv_end[j] = (int32_t)(seg_kind[s] == 0 ? p + 1 : e);", "kv_end[j] = (int32_t)(seg_kind[s] == 0 ? p + 1 : p + 1);", 1),
     ("gather_ignores_kv_start",
      "const int64_t slot = r2t[row * row_stride + start + t];\n            if (slot < 0 || slot >= num_slots) return",
      "const int64_t slot = r2t[row * row_stride + t];\n            if (slot < 0 || slot >= num_slots) return", 1),

@@ -487,3 +487,99 @@ def test_encoder_merge_matches_numpy_indexing():
     bad[0, 6] = -1
     assert oracle.encoder_merge(buf, block_ids, bad, hidden.copy())[0] == oracle.ERR_RANGE
     assert oracle.encoder_merge(buf, np.array([0, 2, 3, 4, 9], np.int32), pos, hidden.copy())[0] == oracle.OK  # all sentinel
+
+
+# ---------------------------------------------------------------- multi-query (extend / verify / spans)
+def _sdpa_masked(q_bits, k_bits, v_bits, r2t, rpi, lens, qo, kv_end, scale):
+    """Library attention with an explicit boolean mask from the key bounds."""
+    outs = []
+    for b in range(len(lens)):
+        slots = r2t[rpi[b], :lens[b]].astype(np.int64)
+        q = bits_to_f64(q_bits[qo[b]:qo[b + 1]]).permute(1, 0, 2)[None]          # [1, Hq, n, D]
+        k = bits_to_f64(k_bits[slots]).permute(1, 0, 2)[None]                     # [1, Hkv, L, D]
+        v = bits_to_f64(v_bits[slots]).permute(1, 0, 2)[None]
+        mask = torch.arange(lens[b])[None, :] < torch.as_tensor(kv_end[qo[b]:qo[b + 1]])[:, None]
+        o = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=mask[None, None], scale=scale,
+                                                             enable_gqa=True)
+        outs.append(o[0].permute(1, 0, 2).numpy())
+    return np.concatenate(outs)
+
+
+@pytest.mark.parametrize("hq,hkv,d,ps,kind", [(8, 2, 32, 4, "extend"), (4, 4, 16, 1, "verify"), (8, 2, 32, 16, "spans"),
+                                             (6, 3, 16, 8, "extend")])
+def test_extend_matches_masked_library_attention(hq, hkv, d, ps, kind):
+    rng = np.random.default_rng(hq * 10 + ps)
+    gen = torch.Generator().manual_seed(ps)
+    lens = [37, 64, 9, 120]
+    r2t, rpi = paged_table(rng, lens, ps, 200 // ps + 40)
+    slots = (200 // ps + 40) * ps
+    k = _rand_bits(gen, (slots, hkv, d))
+    v = _rand_bits(gen, (slots, hkv, d))
+    if kind == "extend":        # the last n positions are new, causal
+        n = [5, 64, 1, 17]
+        kv_end = np.concatenate([np.arange(L - m, L) + 1 for L, m in zip(lens, n)])
+    elif kind == "verify":      # 4 draft tokens each
+        n = [4] * 4
+        kv_end = np.concatenate([np.arange(L - 4, L) + 1 for L in lens])
+    else:                       # causal prefix then a full span (a diffusion row), through the planner
+        segs = [[(0, 0, 20), (1, 20, 37)], [(1, 32, 64)], [(0, 0, 9)], [(1, 100, 120)]]
+        st, qo, q_pos, kv_end = oracle.span_plan(segs)
+        assert st == oracle.OK
+        n = np.diff(qo).tolist()
+    qo = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    q = _rand_bits(gen, (int(qo[-1]), hq, d))
+    st, out, lse = oracle.extend(q, k, v, r2t, rpi, lens, qo, kv_end, 1 / math.sqrt(d))
+    assert st == oracle.OK
+    ref = _sdpa_masked(q, k, v, r2t, rpi, lens, qo, kv_end, 1 / math.sqrt(d))
+    np.testing.assert_allclose(out, ref, rtol=1e-10, atol=1e-12)
+    # lse against the log-sum-exp of the same scores
+    j, h = int(qo[1]) + 3, hq - 1
+    b = 1
+    slots_b = r2t[rpi[b], :kv_end[j]].astype(np.int64)
+    sc = (bits_to_f64(k[slots_b][:, h // (hq // hkv)]) @ bits_to_f64(q[j, h])) / math.sqrt(d)
+    assert abs(lse[j, h] - float(torch.logsumexp(sc, 0))) < 1e-10
+
+
+def test_extend_prefill_is_library_causal_attention():
+    # prefix 0: every position is new, the mask is the ordinary causal one
+    rng = np.random.default_rng(2)
+    gen = torch.Generator().manual_seed(2)
+    L, hq, hkv, d = 50, 4, 2, 16
+    r2t, rpi = paged_table(rng, [L], 1, 80)
+    k = _rand_bits(gen, (80, hkv, d))
+    v = _rand_bits(gen, (80, hkv, d))
+    q = _rand_bits(gen, (L, hq, d))
+    st, out, _ = oracle.extend(q, k, v, r2t, rpi, [L], [0, L], np.arange(1, L + 1), 0.25)
+    assert st == oracle.OK
+    slots = r2t[rpi[0], :L].astype(np.int64)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        bits_to_f64(q).permute(1, 0, 2)[None], bits_to_f64(k[slots]).permute(1, 0, 2)[None],
+        bits_to_f64(v[slots]).permute(1, 0, 2)[None], is_causal=True, scale=0.25, enable_gqa=True)
+    np.testing.assert_allclose(out, ref[0].permute(1, 0, 2).numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_extend_closed_forms():
+    rng = np.random.default_rng(4)
+    gen = torch.Generator().manual_seed(4)
+    r2t, rpi = paged_table(rng, [10, 10], 2, 20)
+    k = _rand_bits(gen, (40, 2, 8))
+    v = _rand_bits(gen, (40, 2, 8))
+    q = _rand_bits(gen, (3, 4, 8))
+    st, out, lse = oracle.extend(q, k, v, r2t, rpi, [10, 10], [0, 2, 3], [1, 0, 10], 0.3)
+    assert st == oracle.OK
+    first = r2t[rpi[0], 0]
+    np.testing.assert_array_equal(out[0, :2], bits_to_f64(v[first][0:1]).numpy().repeat(2, 0))   # one key: V
+    assert (out[1] == 0).all() and np.isneginf(lse[1]).all()                                     # no keys
+    assert oracle.extend(q, k, v, r2t, rpi, [10, 10], [0, 2, 3], [1, 11, 10], 0.3)[0] == oracle.ERR_RANGE
+
+
+def test_span_plan_follows_the_segment_table():
+    g = golden("span_segments.json")
+    st, qo, q_pos, kv_end = oracle.span_plan([[tuple(s) for s in g["first_step"]["segments"]],
+                                              [tuple(s) for s in g["later_step"]["segments"]]])
+    assert st == oracle.OK
+    assert qo.tolist() == [0, 7, 10]
+    assert q_pos.tolist() == g["first_step"]["q_pos"] + g["later_step"]["q_pos"]
+    assert kv_end.tolist() == g["first_step"]["kv_end"] + g["later_step"]["kv_end"]
+    assert g["later_step"]["kv_end"][0] == g["later_step"]["prefix_len"] + g["later_step"]["target_len"]
+    assert oracle.span_plan([[(1, 5, 3)]])[0] == oracle.ERR_RANGE
