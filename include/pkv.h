@@ -254,6 +254,85 @@ pkv_status pkv_ragged_gather(const void *k_pool, const void *v_pool, int64_t num
                              int32_t *err_flags, pkv_stream_t stream);
 
 /*
+ * Arguments of pkv_extend (multi-query attention through the page table).
+ * Pools and layouts as for pkv_decode (CSR or BLOCK_TABLE; page_size a power
+ * of two in [8, 1024]).
+ */
+typedef struct pkv_extend_args {
+    int32_t layout;            /* PKV_LAYOUT_CSR or PKV_LAYOUT_BLOCK_TABLE */
+    int32_t batch;             /* B >= 0 */
+    int32_t num_q_heads;       /* Hq */
+    int32_t num_kv_heads;      /* Hkv; Hq / Hkv in {1, 2, 4, 8, 16} */
+    int32_t head_dim;          /* 64 or 128 (K and V) */
+    int32_t page_size;
+    float sm_scale;
+    int32_t max_seq_len;       /* host upper bound on every request's key count */
+    int32_t kv_chunk;          /* keys per split (multiple of 64); 0 lets the library choose */
+    int32_t block_table_width;
+    int64_t total_q;           /* query rows: qo_indptr[B] */
+    int64_t num_slots;         /* pool rows */
+    int64_t k_row_stride;      /* elements between pool rows */
+    int64_t v_row_stride;
+    int64_t kv_indices_len;    /* CSR: entries of kv_indices */
+    const void *q;             /* bf16 [total_q, Hq, head_dim] */
+    const void *k_pool;        /* bf16 rows [Hkv, head_dim] */
+    const void *v_pool;
+    const int32_t *qo_indptr;  /* [B+1]: query rows of request b are qo_indptr[b] .. qo_indptr[b+1]-1 */
+    const int32_t *kv_end;     /* [total_q] key bound of each query row, or NULL: causal over the last positions */
+    const int32_t *kv_indptr;        /* CSR [B+1] */
+    const int32_t *kv_indices;       /* CSR pages */
+    const int32_t *kv_last_page_len; /* CSR [B] */
+    const int32_t *block_table;      /* BLOCK_TABLE [B, block_table_width] */
+    const int32_t *seq_lens;         /* BLOCK_TABLE [B] */
+    void *out;                 /* bf16 [total_q, Hq, head_dim] */
+    float *lse;                /* fp32 [total_q, Hq] natural-log softmax denominators; nullable */
+} pkv_extend_args;
+
+/*
+ * pkv_extend -- attention of many query tokens per request through the page table.
+ *
+ * Extend / chunked prefill and speculative target-verify (AttentionBackend
+ * notes: qo_indptr from seq_lens - prefix_lens; target-verify over draft
+ * tokens), and the mixed causal/full segments of a diffusion row (vllm-omni,
+ * "Attention execution").  Query row j of request b (qo_indptr[b] <= j <
+ * qo_indptr[b+1]) sees the keys t < kv_end[j] of request b, read through its
+ * page list exactly as pkv_decode reads them; kv_end NULL means the causal
+ * bound of the request's last n_b positions: kv_end = L_b - n_b + i + 1 for its
+ * i-th row (n_b <= L_b required).  For query head h, kh = h / (Hq / Hkv):
+ *     out[j,h,:] = softmax_{t < kv_end[j]}(sm_scale * q[j,h,:] . K[t, kh, :]) V[t, kh, :]
+ * kv_end[j] = 0 gives out = 0, lse = -inf; kv_end outside [0, L_b] raises
+ * PKV_DEVERR_RANGE and the row is treated as empty.  The new tokens' K/V must
+ * already be in the pool (pkv_store first).  Arithmetic: bf16 inputs, fp32
+ * accumulation and softmax, bf16 output.  The key range of a block of rows may
+ * be split into kv_chunk chunks whose partials are merged by log-sum-exp.
+ * workspace: at least pkv_extend_workspace_size(args) bytes, 256-byte aligned.
+ */
+pkv_status pkv_extend(const pkv_extend_args *args, void *workspace, size_t workspace_bytes,
+                      int32_t *err_flags, pkv_stream_t stream);
+
+/* Workspace bytes pkv_extend needs for these arguments (0 on invalid arguments or no split). */
+size_t pkv_extend_workspace_size(const pkv_extend_args *args);
+
+/*
+ * pkv_span_plan -- query rows and key bounds of attention segments.
+ *
+ * The diffusion KV path's segments (vllm-omni, "Attention execution"): request
+ * b has segments seg_indptr[b] .. seg_indptr[b+1]-1, each (kind, start, end)
+ * over positions [start, end) of its sequence; kind 0 is causal (position p
+ * sees keys [0, p + 1)), kind 1 is full (every position sees [0, end)).  The
+ * query rows of b are its segments' positions in order:
+ *     q_pos[j] = p,  kv_end[j] = the bound above,  qo_indptr[b+1] = qo_indptr[b] + sum of b's segment lengths
+ * (qo_indptr[0] = 0) -- the inputs pkv_extend takes, with q gathered at q_pos.
+ * A segment with end < start, start < 0 or another kind raises
+ * PKV_DEVERR_RANGE and is skipped; rows past cap raise PKV_DEVERR_CAPACITY and
+ * are not written.  One CTA per request.
+ */
+pkv_status pkv_span_plan(int32_t batch, const int32_t *seg_indptr, const int32_t *seg_kind,
+                         const int32_t *seg_start, const int32_t *seg_end, int32_t *qo_indptr,
+                         int32_t *q_pos, int32_t *kv_end, int64_t cap, int32_t *err_flags,
+                         pkv_stream_t stream);
+
+/*
  * pkv_alloc_extend -- page allocation for one batch step, on the device.
  *
  * The paged allocator's growth path ("Enabling Encoder-Decoder Models on Intel

@@ -23,7 +23,8 @@ PKV_LAYOUT_CSR, PKV_LAYOUT_BLOCK_TABLE, PKV_LAYOUT_VARLEN = 0, 1, 2
 
 EXPORTED_SYMBOLS = ("pkv_build_indices", "pkv_store", "pkv_decode", "pkv_decode_workspace_size",
                     "pkv_decode_no_alloc", "pkv_ragged_gather", "pkv_alloc_extend", "pkv_write_req_to_token",
-                    "pkv_encoder_merge", "pkv_status_string", "pkv_last_error", "pkv_abi_version")
+                    "pkv_encoder_merge", "pkv_extend", "pkv_extend_workspace_size", "pkv_span_plan",
+                    "pkv_status_string", "pkv_last_error", "pkv_abi_version")
 
 
 class PkvError(RuntimeError):
@@ -55,6 +56,22 @@ class DecodeArgs(ctypes.Structure):
     ]
 
 
+class ExtendArgs(ctypes.Structure):
+    """Mirror of ``pkv_extend_args`` (field order and types must match include/pkv.h)."""
+    _fields_ = [
+        ("layout", ctypes.c_int32), ("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("page_size", ctypes.c_int32),
+        ("sm_scale", ctypes.c_float), ("max_seq_len", ctypes.c_int32), ("kv_chunk", ctypes.c_int32),
+        ("block_table_width", ctypes.c_int32), ("total_q", ctypes.c_int64), ("num_slots", ctypes.c_int64),
+        ("k_row_stride", ctypes.c_int64), ("v_row_stride", ctypes.c_int64), ("kv_indices_len", ctypes.c_int64),
+        ("q", ctypes.c_void_p), ("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+        ("qo_indptr", ctypes.c_void_p), ("kv_end", ctypes.c_void_p),
+        ("kv_indptr", ctypes.c_void_p), ("kv_indices", ctypes.c_void_p), ("kv_last_page_len", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+    ]
+
+
 def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
     if not os.path.exists(path):
         raise ImportError("libpkv.so is not built (%s); run `python -m paged_kv_cache_req_gb300.build`" % path)
@@ -72,7 +89,12 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
     lib.pkv_alloc_extend.argtypes = [P, P, P, I32, I32, I64, P, I64, P, P, I64, P, P]
     lib.pkv_write_req_to_token.argtypes = [P, I64, I64, I64, P, P, P, P, P, P, I32, P, P]
     lib.pkv_encoder_merge.argtypes = [P, I64, I64, I64, P, P, I64, P, I64, I64, P, P, P]
-    for fn in (lib.pkv_alloc_extend, lib.pkv_write_req_to_token, lib.pkv_encoder_merge):
+    lib.pkv_extend.argtypes = [ctypes.POINTER(ExtendArgs), P, SZ, P, P]
+    lib.pkv_extend_workspace_size.argtypes = [ctypes.POINTER(ExtendArgs)]
+    lib.pkv_extend_workspace_size.restype = SZ
+    lib.pkv_span_plan.argtypes = [I32, P, P, P, P, P, P, P, I64, P, P]
+    for fn in (lib.pkv_alloc_extend, lib.pkv_write_req_to_token, lib.pkv_encoder_merge, lib.pkv_extend,
+               lib.pkv_span_plan):
         fn.restype = ctypes.c_int
     lib.pkv_status_string.argtypes = [ctypes.c_int]
     lib.pkv_status_string.restype = ctypes.c_char_p
@@ -240,6 +262,46 @@ def pkv_encoder_merge(buffer, block_ids, positions, hidden, err_flags, filled=No
                                 block_ids.numel(), _p(hidden), hidden.shape[0], hidden.stride(0) * hidden.element_size(),
                                 _p(filled), _p(err_flags), _stream(stream))
     _check(st, "pkv_encoder_merge")
+
+
+def make_extend_args(layout, q, k_pool, v_pool, out, qo_indptr, *, page_size, sm_scale, max_seq_len,
+                     kv_end=None, kv_indptr=None, kv_indices=None, kv_last_page_len=None, block_table=None,
+                     seq_lens=None, lse=None, kv_chunk=0) -> ExtendArgs:
+    """q [total_q, Hq, D]; pools [slots, Hkv, D]."""
+    T, hq, d = q.shape
+    a = ExtendArgs()
+    a.layout, a.batch = layout, qo_indptr.numel() - 1
+    a.num_q_heads, a.num_kv_heads, a.head_dim = hq, k_pool.shape[1], d
+    a.page_size, a.sm_scale, a.max_seq_len, a.kv_chunk = int(page_size), float(sm_scale), int(max_seq_len), int(kv_chunk)
+    a.block_table_width = block_table.shape[1] if block_table is not None else 0
+    a.total_q, a.num_slots = T, k_pool.shape[0]
+    a.k_row_stride, a.v_row_stride = k_pool.stride(0), v_pool.stride(0)
+    a.kv_indices_len = kv_indices.numel() if kv_indices is not None else 0
+    for name, t in (("q", q), ("k_pool", k_pool), ("v_pool", v_pool), ("qo_indptr", qo_indptr), ("kv_end", kv_end),
+                    ("kv_indptr", kv_indptr), ("kv_indices", kv_indices), ("kv_last_page_len", kv_last_page_len),
+                    ("block_table", block_table), ("seq_lens", seq_lens), ("out", out), ("lse", lse)):
+        setattr(a, name, None if t is None else _p(t).value)
+    return a
+
+
+def pkv_extend_workspace_size(args: ExtendArgs) -> int:
+    return int(_lib.pkv_extend_workspace_size(ctypes.byref(args)))
+
+
+def pkv_extend(args: ExtendArgs, workspace: Optional[torch.Tensor], err_flags, stream=None):
+    ws_ptr = _p(workspace) if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = _lib.pkv_extend(ctypes.byref(args), ws_ptr, ws_bytes, _p(err_flags), _stream(stream))
+    _check(st, "pkv_extend")
+
+
+def pkv_span_plan(seg_indptr, seg_kind, seg_start, seg_end, qo_indptr, q_pos, kv_end, err_flags, stream=None):
+    B = seg_indptr.numel() - 1
+    st = _lib.pkv_span_plan(B, _p(_i32(seg_indptr, "seg_indptr")), _p(_i32(seg_kind, "seg_kind")),
+                            _p(_i32(seg_start, "seg_start")), _p(_i32(seg_end, "seg_end")),
+                            _p(_i32(qo_indptr, "qo_indptr")), _p(_i32(q_pos, "q_pos")), _p(_i32(kv_end, "kv_end")),
+                            q_pos.numel(), _p(err_flags), _stream(stream))
+    _check(st, "pkv_span_plan")
 
 
 def pkv_status_string(status: int) -> str:

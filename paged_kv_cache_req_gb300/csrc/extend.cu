@@ -1,0 +1,889 @@
+// pkv_extend: attention of many query tokens per request through the page table
+// (extend / chunked prefill, speculative target-verify, and the mixed
+// causal/full segments of a diffusion row), on the 5th-generation tensor cores.
+//
+// Query row j of request b sees the keys [0, kv_end[j]) of that request (by
+// default the causal bound of the request's last positions).  A work item is
+// (request, kv head, block of 128 query rows, chunk of keys): the rows are the
+// (token, query head) pairs of 128 / g consecutive tokens times the g query
+// heads sharing the kv head, so every K/V tile serves the whole block.  Per CTA:
+//   warp 4     TMA producer: the block's q (one 3-D box per 64-dim slab, rows
+//              token-major), then K/V tiles of 64 keys (one box per page per
+//              slab) through a 4-stage ring, tiles three ahead pulled into L2;
+//   warp 5     S = Q K^T (M = 128, N = 64) into one of two TMEM score buffers;
+//   warp 6     O += P V (N = head_dim) from one of two TMEM P buffers;
+//   warps 0-3  one query row per thread: mask keys at or past the row's bound,
+//              online softmax (base 2, running max raised only past 2^8), P.
+// Items whose block is cut into several key chunks write fp32 (o, lse)
+// partials that ext_merge_kernel combines.  Every wait is bounded (~2 s).
+#include <algorithm>
+
+#include "pkv_internal.cuh"
+#include "tc05.cuh"
+
+namespace pkv {
+namespace ext {
+
+constexpr int kRows = 128, kTile = 64, kStages = 4;
+constexpr int kThreads = 224;              // warps 0-3 softmax, 4 producer, 5 q.k, 6 P.V
+constexpr int kProducerWarp = 4, kQkWarp = 5, kPvWarp = 6;
+constexpr int kPrefetch = 3;
+constexpr float kLn2 = 0.69314718055994531f;
+constexpr float kLog2e = 1.44269504088896341f;
+constexpr float kLazy = 8.f;
+
+template <int D>
+struct Cfg {
+    static constexpr int kSl = D / 64;                         // 64-dim slabs
+    static constexpr int kQBytes = kSl * kRows * 128;          // q block, SW128 K-major
+    static constexpr int kKBytes = kSl * kTile * 128;          // one K (or V) tile
+    static constexpr int kStageBytes = 2 * kKBytes;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffKV = kOffQ + kQBytes;
+    static constexpr int kOffBar = kOffKV + kStages * kStageBytes;
+    static constexpr int kNumBars = 24;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;    // tmem slot, abort flag, scan scratch
+    static constexpr int kOffTable = kOffMisc + 64;
+    static constexpr int kFixedSmem = kOffTable + 1024;        // + item table + alignment slack
+    static constexpr uint32_t kColS = 0;                       // two 64-column score buffers
+    static constexpr uint32_t kColO = 128;
+    static constexpr uint32_t kColP = 128 + D;                 // two 32-column P buffers
+    static constexpr uint32_t kTmemCols = (kColP + 64 <= 256) ? 256 : 512;
+};
+
+struct Params {
+    int32_t layout, batch, hq, hkv, g, g_shift, T;
+    int32_t ps_shift, ps_mask, box_rows, bt_width, chunk, max_len;
+    float scale_log2;
+    int64_t num_pages, kv_indices_len, total_q;
+    const int32_t *qo_indptr, *kv_end, *kv_indptr, *kv_indices, *kv_last, *block_table, *seq_lens;
+    uint16_t *out;
+    float *lse, *part_o, *part_lse;
+    int32_t *err;
+};
+
+// Keys of request b (0 and a flag for malformed inputs).
+__device__ __forceinline__ int key_count(const Params &p, int b, int64_t &base, bool report) {
+    int64_t L, cap;
+    if (p.layout == PKV_LAYOUT_CSR) {
+        const int64_t lo = p.kv_indptr[b], hi = p.kv_indptr[b + 1], n = hi - lo;
+        const int last = n > 0 ? p.kv_last[b] : 0;
+        base = lo;
+        if (lo < 0 || n < 0 || hi > p.kv_indices_len || (n > 0 && (last < 1 || last > (1 << p.ps_shift)))) {
+            if (report) raise_flag(p.err, PKV_DEVERR_RANGE);
+            base = 0;
+            return 0;
+        }
+        L = n > 0 ? ((n - 1) << p.ps_shift) + last : 0;
+        cap = L;
+    } else {
+        base = static_cast<int64_t>(b) * p.bt_width;
+        L = p.seq_lens[b];
+        cap = static_cast<int64_t>(p.bt_width) << p.ps_shift;
+    }
+    const int64_t limit = min(cap, static_cast<int64_t>(p.max_len));
+    if (L < 0 || L > limit) {
+        if (report) raise_flag(p.err, L < 0 ? PKV_DEVERR_RANGE : PKV_DEVERR_CAPACITY);
+        L = L < 0 ? 0 : limit;
+    }
+    return static_cast<int>(L);
+}
+
+// Query rows of request b (0 for a malformed qo_indptr).
+__device__ __forceinline__ int q_count(const Params &p, int b, bool report) {
+    const int64_t lo = p.qo_indptr[b], hi = p.qo_indptr[b + 1];
+    if (lo < 0 || hi < lo || hi > p.total_q) {
+        if (report) raise_flag(p.err, PKV_DEVERR_RANGE);
+        return 0;
+    }
+    return static_cast<int>(hi - lo);
+}
+
+// Key bound of query block qblk: the causal bound of its last token, or all keys
+// when the caller gives its own bounds (the rows then mask the rest).
+__device__ __forceinline__ int block_keys(const Params &p, int L, int n, int qblk) {
+    if (p.kv_end) return L;
+    const int last = min(n, (qblk + 1) * p.T);
+    return max(0, L - n + last);
+}
+
+__device__ __forceinline__ int chunks_of(const Params &p, int kmax) { return max(1, (kmax + p.chunk - 1) / p.chunk); }
+
+// Items of request b: hkv x sum over its query blocks of their key chunks.
+__device__ __forceinline__ int per_head_items(const Params &p, int L, int n) {
+    const int nq = (n + p.T - 1) / p.T;
+    int s = 0;
+    for (int q = 0; q < nq; ++q) s += chunks_of(p, block_keys(p, L, n, q));
+    return s;
+}
+
+struct Item {
+    int b, kh, qblk, c, L, n, nch, k0, k1, n_tiles;
+    int64_t base, w;
+};
+
+__device__ __forceinline__ Item locate(const Params &p, const int *off, int64_t w) {
+    Item it;
+    int lo = 0, hi = p.batch;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (off[mid] <= w) lo = mid; else hi = mid;
+    }
+    it.b = lo;
+    it.w = w;
+    it.L = key_count(p, it.b, it.base, false);
+    it.n = it.L >= 0 ? q_count(p, it.b, false) : 0;
+    if (!p.kv_end && it.n > it.L) it.n = 0;                   // causal rows need their keys
+    const int per = per_head_items(p, it.L, it.n);
+    int rem = static_cast<int>(w - off[it.b]);
+    it.kh = rem / per;
+    rem -= it.kh * per;
+    int q = 0;
+    for (;; ++q) {
+        const int c = chunks_of(p, block_keys(p, it.L, it.n, q));
+        if (rem < c) break;
+        rem -= c;
+    }
+    it.qblk = q;
+    it.c = rem;
+    const int kmax = block_keys(p, it.L, it.n, q);
+    it.nch = chunks_of(p, kmax);
+    it.k0 = it.c * p.chunk;
+    it.k1 = min(kmax, it.k0 + p.chunk);
+    it.n_tiles = it.k1 > it.k0 ? (it.k1 - it.k0 + kTile - 1) / kTile : 0;
+    return it;
+}
+
+// off[b] = first item of request b; every CTA builds the same table.
+__device__ __forceinline__ void build_item_table(const Params &p, int *off, int *scratch) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int B = p.batch;
+    const int seg = (B + kThreads - 1) / kThreads;
+    const int lo = min(B, tid * seg), hi = min(B, lo + seg);
+    auto items = [&](int b, bool report) {
+        int64_t base;
+        const int L = key_count(p, b, base, report);
+        int n = q_count(p, b, report);
+        if (!p.kv_end && n > L) {
+            if (report) raise_flag(p.err, PKV_DEVERR_RANGE);
+            n = 0;
+        }
+        return p.hkv * per_head_items(p, L, n);
+    };
+    int local = 0;
+    for (int b = lo; b < hi; ++b) local += items(b, blockIdx.x == 0);
+    int incl = local;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
+    }
+    if (lane == 31) scratch[warp] = incl;
+    __syncthreads();
+    int wbase = 0;
+    for (int w = 0; w < warp; ++w) wbase += scratch[w];
+    int run = wbase + incl - local;
+    for (int b = lo; b < hi; ++b) {
+        off[b] = run;
+        run += items(b, false);
+    }
+    if (tid == kThreads - 1) off[B] = wbase + incl;
+    __syncthreads();
+}
+
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int32_t *err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63) == 0) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > 2000000000ull) {
+                *abort_flag = 1;
+                raise_flag(err, PKV_DEVERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ bool warp_wait(bool ok, uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                          int32_t *err) {
+    return __all_sync(0xffffffffu, ok && wait_bar(bar, parity, abort_flag, err));
+}
+// Bounded wait that ignores the abort flag: drains work this CTA started.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait(bar, parity)) return;
+        if ((i & 63) == 63 && global_ns() - t0 > 2000000000ull) return;
+    }
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+enum Bar {
+    kQFull = 0, kQEmpty, kKvFull0, kKvEmpty0 = kKvFull0 + kStages, kSFull0 = kKvEmpty0 + kStages,
+    kSFree0 = kSFull0 + 2, kPFull0 = kSFree0 + 2, kPFree0 = kPFull0 + 2, kODone = kPFree0 + 2, kOFree, kFinalQk,
+    kFinalPv, kBarCount
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+           const __grid_constant__ CUtensorMap tmv) {
+    using C = Cfg<D>;
+    static_assert(kBarCount <= C::kNumBars, "barrier slots");
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    unsigned char *sQ = smem + C::kOffQ;
+    unsigned char *sKV = smem + C::kOffKV;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
+    int *scan = reinterpret_cast<int *>(smem + C::kOffMisc + 16);
+    int *off = reinterpret_cast<int *>(smem + C::kOffTable);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        *abort_flag = 0;
+        mbar_init(&bars[kQFull], 1);
+        mbar_init(&bars[kQEmpty], 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bars[kKvFull0 + s], 1);
+            mbar_init(&bars[kKvEmpty0 + s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[kSFull0 + i], 1);
+            mbar_init(&bars[kSFree0 + i], 4);
+            mbar_init(&bars[kPFull0 + i], 4);
+            mbar_init(&bars[kPFree0 + i], 1);
+        }
+        mbar_init(&bars[kODone], 1);
+        mbar_init(&bars[kOFree], 4);
+        mbar_init(&bars[kFinalQk], 1);
+        mbar_init(&bars[kFinalPv], 1);
+        mbar_init_fence();
+    }
+    if (warp == kQkWarp) {
+        tc05::tmem_alloc(tslot, C::kTmemCols);
+        tc05::tmem_relinquish();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        prefetch_tmap(&tmq);
+        prefetch_tmap(&tmk);
+        prefetch_tmap(&tmv);
+    }
+    build_item_table(p, off, scan);
+    tc05::fence_before_sync();
+    __syncthreads();
+    tc05::fence_after_sync();
+    const uint32_t tbase = *tslot;
+    const int64_t total = off[p.batch];
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ producer
+        const int box = p.box_rows;
+        const int nbox = kTile / box;
+        uint32_t n = 0, iq = 0;
+        bool ok = true;
+        for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
+            const Item it = locate(p, off, w);
+            if (it.n_tiles == 0) continue;
+            // q of the block: one box of 128 rows (T tokens x g heads) per slab
+            if (lane == 0) {
+                ok = wait_bar(&bars[kQEmpty], (iq & 1) ^ 1, abort_flag, p.err);
+                if (ok) {
+                    mbar_arrive_expect_tx(&bars[kQFull], C::kQBytes);
+                    const int tok = p.qo_indptr[it.b] + it.qblk * p.T;
+                    for (int sl = 0; sl < C::kSl; ++sl)
+                        tma_load_3d(sQ + sl * kRows * 128, &tmq, sl * 64, it.kh * p.g, tok, &bars[kQFull]);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            ++iq;
+            auto box_row = [&](int ti, bool report) -> int {
+                if (lane >= nbox) return -1;
+                const int tb = it.k0 + ti * kTile + lane * box;
+                if (tb >= it.k1) return -1;
+                const int32_t *tab = p.layout == PKV_LAYOUT_CSR ? p.kv_indices : p.block_table;
+                const int page = __ldg(tab + it.base + (tb >> p.ps_shift));
+                if (page < 0 || page >= p.num_pages) {
+                    if (report) raise_flag(p.err, PKV_DEVERR_RANGE);
+                    return -2;
+                }
+                return static_cast<int>((static_cast<int64_t>(page) << p.ps_shift) + (tb & p.ps_mask));
+            };
+            auto prefetch = [&](int ti) {
+                const int r = box_row(ti, false);
+                if (r >= 0)
+                    for (int sl = 0; sl < C::kSl; ++sl) {
+                        tma_prefetch_3d(&tmk, sl * 64, it.kh, r);
+                        tma_prefetch_3d(&tmv, sl * 64, it.kh, r);
+                    }
+            };
+            for (int ti = 0; ti < kPrefetch && ti < it.n_tiles; ++ti) prefetch(ti);
+            for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
+                if (ti + kPrefetch < it.n_tiles) prefetch(ti + kPrefetch);
+                const int row = box_row(ti, true);
+                const int s = n % kStages;
+                if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
+                const uint32_t valid = __ballot_sync(0xffffffffu, row >= 0);
+                if (lane == 0)
+                    mbar_arrive_expect_tx(&bars[kKvFull0 + s],
+                                          __popc(valid) * static_cast<uint32_t>(box) * 128u * 2u * C::kSl);
+                __syncwarp();
+                if (row >= 0) {
+                    unsigned char *st = sKV + s * C::kStageBytes;
+                    for (int sl = 0; sl < C::kSl; ++sl) {
+                        tma_load_3d(st + sl * kTile * 128 + lane * box * 128, &tmk, sl * 64, it.kh, row,
+                                    &bars[kKvFull0 + s]);
+                        tma_load_3d(st + C::kKBytes + sl * kTile * 128 + lane * box * 128, &tmv, sl * 64, it.kh, row,
+                                    &bars[kKvFull0 + s]);
+                    }
+                }
+            }
+        }
+        if (lane == 0) {   // drain: the copies this warp issued have landed
+            for (uint32_t k = n > kStages ? n - kStages : 0; k < n; ++k)
+                drain_wait(&bars[kKvFull0 + k % kStages], (k / kStages) & 1);
+            if (iq) drain_wait(&bars[kQFull], (iq - 1) & 1);
+        }
+        __syncwarp();
+    } else if (warp == kQkWarp) {
+        // ------------------------------------------------------------ S = Q K^T
+        const uint32_t idesc = tc05::idesc_bf16_f32(kRows, kTile, false, false);
+        uint32_t n = 0, iq = 0;
+        bool ok = true;
+        for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
+            const Item it = locate(p, off, w);
+            if (it.n_tiles == 0) continue;
+            ok = warp_wait(ok, &bars[kQFull], iq & 1, abort_flag, p.err);
+            ++iq;
+            for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
+                const int s = n % kStages;
+                ok = warp_wait(ok, &bars[kKvFull0 + s], (n / kStages) & 1, abort_flag, p.err);
+                ok = warp_wait(ok, &bars[kSFree0 + (n & 1)], ((n >> 1) & 1) ^ 1, abort_flag, p.err);
+                if (!ok) break;
+                tc05::fence_after_sync();
+                if (lane == 0) {
+                    const uint64_t kd = tc05::smem_desc(sKV + s * C::kStageBytes, 16, 1024);
+                    const uint64_t qd = tc05::smem_desc(sQ, 16, 1024);
+#pragma unroll
+                    for (int sl = 0; sl < C::kSl; ++sl)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)   // slab: q +16 KB, K +8 KB; k-step +32 bytes
+                            tc05::mma_ss(tbase + C::kColS + (n & 1) * kTile,
+                                         qd + static_cast<uint64_t>((sl * kRows * 128 + k * 32) >> 4),
+                                         kd + static_cast<uint64_t>((sl * kTile * 128 + k * 32) >> 4), idesc,
+                                         (sl | k) ? 1u : 0u);
+                    tc05::commit(&bars[kSFull0 + (n & 1)]);
+                    if (ti == it.n_tiles - 1) tc05::commit(&bars[kQEmpty]);
+                }
+                __syncwarp();
+            }
+        }
+        if (lane == 0) {
+            tc05::commit(&bars[kFinalQk]);
+            drain_wait(&bars[kFinalQk], 0);
+        }
+        __syncwarp();
+    } else if (warp == kPvWarp) {
+        // ------------------------------------------------------------ O += P V
+        const uint32_t idesc = tc05::idesc_bf16_f32(kRows, D, false, true);
+        uint32_t n = 0, io = 0;
+        bool ok = true;
+        for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
+            const Item it = locate(p, off, w);
+            if (it.n_tiles == 0) continue;
+            for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
+                ok = warp_wait(ok, &bars[kPFull0 + (n & 1)], (n >> 1) & 1, abort_flag, p.err);
+                if (!ok) break;
+                unsigned char *v = sKV + (n % kStages) * C::kStageBytes + C::kKBytes;
+                const int n_valid = it.k1 - (it.k0 + ti * kTile);
+                if (n_valid < kTile) {   // key rows past the chunk hold stale data: zero them
+                    for (int i = lane; i < (kTile - n_valid) * C::kSl * 8; i += 32) {
+                        const int key = n_valid + i / (C::kSl * 8);
+                        const int sl = (i / 8) % C::kSl, c = i % 8;
+                        *reinterpret_cast<uint4 *>(v + sl * kTile * 128 + key * 128 + (c << 4)) = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                if (ti == 0) ok = warp_wait(ok, &bars[kOFree], (io & 1) ^ 1, abort_flag, p.err);
+                if (!ok) break;
+                tc05::fence_after_sync();
+                if (lane == 0) {
+                    const uint64_t vd = tc05::smem_desc(v, kTile * 128, 1024);
+#pragma unroll
+                    for (int k = 0; k < kTile / 16; ++k)   // 16 keys: +2048 bytes of V, +8 columns of P
+                        tc05::mma_ts(tbase + C::kColO, tbase + C::kColP + (n & 1) * 32 + k * 8,
+                                     vd + static_cast<uint64_t>((k * 2048) >> 4), idesc,
+                                     (ti == 0 && k == 0) ? 0u : 1u);
+                    tc05::commit(&bars[kPFree0 + (n & 1)]);
+                    tc05::commit(&bars[kKvEmpty0 + n % kStages]);
+                    if (ti == it.n_tiles - 1) tc05::commit(&bars[kODone]);
+                }
+                __syncwarp();
+            }
+            ++io;
+        }
+        if (lane == 0) {
+            tc05::commit(&bars[kFinalPv]);
+            drain_wait(&bars[kFinalPv], 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax (one row per thread)
+        const int r = warp * 32 + lane;
+        const uint32_t trow = tc05::taddr(tbase, warp * 32, 0);
+        const int tok = r >> p.g_shift, hh = r & (p.g - 1);
+        uint32_t n = 0, io = 0;
+        bool ok = true;
+        for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
+            const Item it = locate(p, off, w);
+            const int tb = it.qblk * p.T + tok;                  // token within the request
+            const bool valid = tb < it.n;
+            const int64_t qrow = static_cast<int64_t>(p.qo_indptr[it.b]) + tb;
+            int kend = 0;
+            if (valid) {
+                kend = p.kv_end ? p.kv_end[qrow] : it.L - it.n + tb + 1;
+                if (kend < 0 || kend > it.L) {
+                    if (it.c == 0 && it.kh == 0) raise_flag(p.err, PKV_DEVERR_RANGE);
+                    kend = 0;
+                }
+            }
+            const int head = it.kh * p.g + hh;
+            const bool single = it.nch == 1;
+            const int64_t prow = it.w * kRows + r;
+            float m = -INFINITY, l = 0.f;
+            if (it.n_tiles == 0) {   // no keys: out = 0, lse = -inf
+                if (valid && single) {
+                    uint4 *o = reinterpret_cast<uint4 *>(p.out + (qrow * p.hq + head) * D);
+                    for (int i = 0; i < D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+                    if (p.lse) p.lse[qrow * p.hq + head] = -INFINITY;
+                }
+                continue;
+            }
+            for (int ti = 0; ti < it.n_tiles; ++ti, ++n) {
+                const int key0 = it.k0 + ti * kTile;
+                const int vis = max(0, min(min(kend, it.k1) - key0, kTile));
+                ok = warp_wait(ok, &bars[kSFull0 + (n & 1)], (n >> 1) & 1, abort_flag, p.err);
+                float x[64];
+                if (ok) {
+                    tc05::fence_after_sync();
+                    tc05::ld_x64(trow + C::kColS + (n & 1) * kTile, x);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) x[j] = 0.f;
+                }
+                tc05::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kSFree0 + (n & 1)]);
+                float mx = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    x[j] = j < vis ? x[j] * p.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, x[j]);
+                }
+                const bool raise = mx > m + kLazy || (m == -INFINITY && mx != -INFINITY);
+                const float corr = raise ? ex2(m - mx) : 1.f;
+                if (__any_sync(0xffffffffu, raise && m != -INFINITY) && ok) {
+                    // O is final for tile n - 1 once its P V completed; rescale the row
+                    ok = warp_wait(ok, &bars[kPFree0 + ((n - 1) & 1)], ((n - 1) >> 1) & 1, abort_flag, p.err);
+                    tc05::fence_after_sync();
+#pragma unroll 1
+                    for (int cc = 0; cc < D / 16 && ok; ++cc) {
+                        float ov[16];
+                        tc05::ld_x16(trow + C::kColO + cc * 16, ov);
+                        tc05::wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) ov[e] *= corr;
+                        tc05::st_x16(trow + C::kColO + cc * 16, ov);
+                    }
+                    tc05::wait_st();
+                }
+                if (raise) {
+                    l *= corr;
+                    m = mx;
+                }
+                uint32_t h[32];
+                float lsum = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float p0 = m == -INFINITY ? 0.f : ex2(x[2 * j] - m);
+                    const float p1 = m == -INFINITY ? 0.f : ex2(x[2 * j + 1] - m);
+                    lsum += p0 + p1;
+                    h[j] = pack_bf16x2(p0, p1);
+                }
+                l += lsum;
+                ok = warp_wait(ok, &bars[kPFree0 + (n & 1)], ((n >> 1) & 1) ^ 1, abort_flag, p.err);
+                if (ok) {
+                    tc05::fence_after_sync();
+                    uint32_t h0[16], h1[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        h0[j] = h[j];
+                        h1[j] = h[16 + j];
+                    }
+                    tc05::st_x16_u32(trow + C::kColP + (n & 1) * 32, h0);
+                    tc05::st_x16_u32(trow + C::kColP + (n & 1) * 32 + 16, h1);
+                    tc05::wait_st();
+                }
+                tc05::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars[kPFull0 + (n & 1)]);
+            }
+            // ---- epilogue: normalise O, write the row (or the split partial) ----
+            ok = warp_wait(ok, &bars[kODone], io & 1, abort_flag, p.err);
+            tc05::fence_after_sync();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+            for (int cb = 0; cb < D / 16; cb += 2) {
+                float ov[2][16];
+                if (ok) {
+                    tc05::ld_x16(trow + C::kColO + cb * 16, ov[0]);
+                    tc05::ld_x16(trow + C::kColO + (cb + 1) * 16, ov[1]);
+                    tc05::wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) ov[0][e] = ov[1][e] = 0.f;
+                }
+                if (valid) {
+#pragma unroll
+                    for (int q2 = 0; q2 < 2; ++q2) {
+                        const int col = (cb + q2) * 16;
+                        if (single) {
+                            uint32_t hh2[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                hh2[e] = pack_bf16x2(ov[q2][2 * e] * inv, ov[q2][2 * e + 1] * inv);
+                            uint4 *o = reinterpret_cast<uint4 *>(p.out + (qrow * p.hq + head) * D + col);
+                            o[0] = make_uint4(hh2[0], hh2[1], hh2[2], hh2[3]);
+                            o[1] = make_uint4(hh2[4], hh2[5], hh2[6], hh2[7]);
+                        } else {
+                            float4 *o = reinterpret_cast<float4 *>(p.part_o + prow * D + col);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                o[e] = make_float4(ov[q2][4 * e] * inv, ov[q2][4 * e + 1] * inv,
+                                                   ov[q2][4 * e + 2] * inv, ov[q2][4 * e + 3] * inv);
+                        }
+                    }
+                }
+            }
+            if (valid) {
+                const float lse2 = l > 0.f ? m + log2f(l) : -INFINITY;
+                if (single) {
+                    if (p.lse) p.lse[qrow * p.hq + head] = lse2 * kLn2;
+                } else {
+                    p.part_lse[prow] = lse2;
+                }
+            }
+            tc05::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kOFree]);
+            ++io;
+        }
+    }
+
+    tc05::fence_before_sync();
+    __syncthreads();
+    if (warp == kQkWarp) {
+        tc05::fence_after_sync();
+        tc05::tmem_dealloc(tbase, C::kTmemCols);
+    }
+}
+
+// Log-sum-exp merge of the key chunks of one (request, kv head, query block):
+// one CTA per such group (found by walking the requests), rows x head_dim.
+template <int D>
+__global__ void __launch_bounds__(256) ext_merge_kernel(const Params p, int64_t groups) {
+    const int64_t gi = blockIdx.x;
+    if (gi >= groups) return;
+    // locate the group and its first item
+    int64_t g0 = 0, w0 = 0;
+    int b = 0, L = 0, n = 0;
+    for (; b < p.batch; ++b) {
+        int64_t base;
+        L = key_count(p, b, base, false);
+        n = q_count(p, b, false);
+        if (!p.kv_end && n > L) n = 0;
+        const int nq = (n + p.T - 1) / p.T;
+        const int64_t gb = static_cast<int64_t>(p.hkv) * nq;
+        if (gi < g0 + gb) break;
+        g0 += gb;
+        w0 += static_cast<int64_t>(p.hkv) * per_head_items(p, L, n);
+    }
+    if (b >= p.batch) return;
+    const int nq = (n + p.T - 1) / p.T;
+    const int rem = static_cast<int>(gi - g0);
+    const int kh = rem / nq, qblk = rem % nq;
+    const int nch = chunks_of(p, block_keys(p, L, n, qblk));
+    if (nch <= 1) return;
+    w0 += static_cast<int64_t>(kh) * per_head_items(p, L, n);
+    for (int q = 0; q < qblk; ++q) w0 += chunks_of(p, block_keys(p, L, n, q));
+    for (int i = threadIdx.x; i < kRows * (D / 4); i += blockDim.x) {
+        const int r = i / (D / 4), d4 = i % (D / 4);
+        const int tok = r >> p.g_shift, hh = r & (p.g - 1);
+        const int tb = qblk * p.T + tok;
+        if (tb >= n) continue;
+        float M = -INFINITY;
+        for (int c = 0; c < nch; ++c) M = fmaxf(M, p.part_lse[(w0 + c) * kRows + r]);
+        float den = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M != -INFINITY) {
+            for (int c = 0; c < nch; ++c) {
+                const float lc = p.part_lse[(w0 + c) * kRows + r];
+                if (lc == -INFINITY) continue;
+                const float wgt = ex2(lc - M);
+                const float4 x = reinterpret_cast<const float4 *>(p.part_o + ((w0 + c) * kRows + r) * D)[d4];
+                acc.x = fmaf(wgt, x.x, acc.x);
+                acc.y = fmaf(wgt, x.y, acc.y);
+                acc.z = fmaf(wgt, x.z, acc.z);
+                acc.w = fmaf(wgt, x.w, acc.w);
+                den += wgt;
+            }
+        }
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        const int64_t qrow = static_cast<int64_t>(p.qo_indptr[b]) + tb;
+        const int head = kh * p.g + hh;
+        uint2 o;
+        o.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+        o.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+        reinterpret_cast<uint2 *>(p.out + (qrow * p.hq + head) * D)[d4] = o;
+        if (d4 == 0 && p.lse) p.lse[qrow * p.hq + head] = den > 0.f ? (M + log2f(den)) * kLn2 : -INFINITY;
+    }
+}
+
+// ------------------------------------------------------------------ span planner
+// One CTA per request: its segments' positions and key bounds, rows counted from
+// the sum of the segment lengths of the requests before it.
+__global__ void __launch_bounds__(256)
+span_plan_kernel(int32_t batch, const int32_t *__restrict__ seg_indptr, const int32_t *__restrict__ seg_kind,
+                 const int32_t *__restrict__ seg_start, const int32_t *__restrict__ seg_end, int32_t *__restrict__ qo,
+                 int32_t *__restrict__ q_pos, int32_t *__restrict__ kv_end, int64_t cap, int32_t *__restrict__ err) {
+    __shared__ long long scratch[32];
+    const int b = blockIdx.x;
+    auto seg_len = [&](int s) -> long long {
+        const int64_t a = seg_start[s], e = seg_end[s];
+        return (a < 0 || e < a || (seg_kind[s] != 0 && seg_kind[s] != 1)) ? 0 : e - a;
+    };
+    long long before = 0;
+    for (int s = threadIdx.x; s < seg_indptr[b]; s += blockDim.x) before += seg_len(s);
+    before = block_sum(before, scratch);
+    long long mine = 0;
+    for (int s = seg_indptr[b] + threadIdx.x; s < seg_indptr[b + 1]; s += blockDim.x) mine += seg_len(s);
+    mine = block_sum(mine, scratch);
+    if (threadIdx.x == 0) {
+        if (b == 0) qo[0] = 0;
+        qo[b + 1] = static_cast<int32_t>(before + mine);
+        if (before + mine > cap) raise_flag(err, PKV_DEVERR_CAPACITY);
+    }
+    long long j = before;
+    for (int s = seg_indptr[b]; s < seg_indptr[b + 1]; ++s) {   // segments in order, positions in parallel
+        const int64_t a = seg_start[s], e = seg_end[s];
+        if (a < 0 || e < a || (seg_kind[s] != 0 && seg_kind[s] != 1)) {
+            if (threadIdx.x == 0) raise_flag(err, PKV_DEVERR_RANGE);
+            continue;
+        }
+        for (int64_t t = threadIdx.x; t < e - a; t += blockDim.x) {
+            if (j + t >= cap) break;
+            q_pos[j + t] = static_cast<int32_t>(a + t);
+            kv_end[j + t] = static_cast<int32_t>(seg_kind[s] == 0 ? a + t + 1 : e);
+        }
+        j += e - a;
+    }
+}
+
+// ------------------------------------------------------------------ host side
+struct Plan {
+    int g, T, chunk, nch_max;
+    int64_t items_max, groups_max;
+    size_t part_o_bytes, part_lse_bytes;
+};
+
+static bool make_plan(const pkv_extend_args *a, Plan &pl) {
+    pl.g = a->num_q_heads / a->num_kv_heads;
+    pl.T = kRows / pl.g;
+    const int64_t blocks_max = a->total_q / pl.T + a->batch;      // query blocks, upper bound
+    pl.groups_max = static_cast<int64_t>(a->num_kv_heads) * blocks_max;
+    const int64_t L = std::max(1, a->max_seq_len);
+    if (a->kv_chunk > 0) {
+        pl.chunk = a->kv_chunk;
+    } else {   // split the keys only when the query blocks alone leave SMs idle
+        const int64_t target = 2 * static_cast<int64_t>(sm_count());
+        const int64_t groups = std::max<int64_t>(1, static_cast<int64_t>(a->num_kv_heads) *
+                                                        std::max<int64_t>(a->batch, a->total_q / pl.T));
+        const int64_t want = (target + groups - 1) / groups;
+        int64_t c = (L + want - 1) / want;
+        c = std::max<int64_t>(512, (c + kTile - 1) / kTile * kTile);
+        pl.chunk = static_cast<int>(std::min<int64_t>(c, (L + kTile - 1) / kTile * kTile));
+    }
+    pl.nch_max = static_cast<int>((L + pl.chunk - 1) / pl.chunk);
+    pl.items_max = pl.groups_max * pl.nch_max;
+    if (pl.items_max > INT32_MAX / kRows) return false;
+    if (pl.nch_max <= 1) {
+        pl.part_o_bytes = pl.part_lse_bytes = 0;
+    } else {
+        const int64_t rows = pl.items_max * kRows;
+        pl.part_o_bytes = (static_cast<size_t>(rows) * a->head_dim * 4 + 255) / 256 * 256;
+        pl.part_lse_bytes = (static_cast<size_t>(rows) * 4 + 255) / 256 * 256;
+    }
+    return true;
+}
+
+static pkv_status validate(const pkv_extend_args *a, bool check_ptrs) {
+    if (a->batch < 0 || a->num_q_heads < 1 || a->num_kv_heads < 1 || a->total_q < 0 || a->max_seq_len < 0 ||
+        a->num_slots < 0)
+        return fail(PKV_ERR_INVALID_ARG, "pkv_extend: negative or zero size");
+    if (a->num_q_heads % a->num_kv_heads) return fail(PKV_ERR_INVALID_ARG, "pkv_extend: Hq not a multiple of Hkv");
+    const int g = a->num_q_heads / a->num_kv_heads;
+    if (!is_pow2(g) || g > 16) return fail(PKV_ERR_UNSUPPORTED, "pkv_extend: Hq/Hkv must be 1, 2, 4, 8 or 16");
+    if (a->head_dim != 64 && a->head_dim != 128) return fail(PKV_ERR_UNSUPPORTED, "pkv_extend: head_dim 64 or 128");
+    if (!is_pow2(a->page_size) || a->page_size < 8 || a->page_size > 1024)
+        return fail(PKV_ERR_UNSUPPORTED, "pkv_extend: page_size must be a power of two in [8, 1024]");
+    if (a->layout != PKV_LAYOUT_CSR && a->layout != PKV_LAYOUT_BLOCK_TABLE)
+        return fail(PKV_ERR_INVALID_ARG, "pkv_extend: layout must be CSR or BLOCK_TABLE");
+    if (a->kv_chunk < 0 || a->kv_chunk % kTile) return fail(PKV_ERR_INVALID_ARG, "pkv_extend: kv_chunk multiple of 64");
+    const int64_t rowq = static_cast<int64_t>(a->num_kv_heads) * a->head_dim;
+    if (a->k_row_stride < rowq || a->v_row_stride < rowq || a->k_row_stride % 8 || a->v_row_stride % 8)
+        return fail(PKV_ERR_INVALID_ARG, "pkv_extend: pool row strides must hold Hkv x head_dim and be 16-byte aligned");
+    if (a->num_slots > INT32_MAX || a->total_q > INT32_MAX)
+        return fail(PKV_ERR_UNSUPPORTED, "pkv_extend: more than 2^31 pool rows or query rows");
+    if (a->batch == 0 || !check_ptrs) return PKV_OK;
+    if (!a->q || !a->k_pool || !a->v_pool || !a->out || !a->qo_indptr)
+        return fail(PKV_ERR_INVALID_ARG, "pkv_extend: null q/k_pool/v_pool/out/qo_indptr");
+    if (!aligned(a->q, 16) || !aligned(a->k_pool, 16) || !aligned(a->v_pool, 16) || !aligned(a->out, 16))
+        return fail(PKV_ERR_INVALID_ARG, "pkv_extend: q, pools and out must be 16-byte aligned");
+    if (a->layout == PKV_LAYOUT_CSR && (!a->kv_indptr || !a->kv_indices || !a->kv_last_page_len))
+        return fail(PKV_ERR_INVALID_ARG, "pkv_extend: CSR layout needs kv_indptr/kv_indices/kv_last_page_len");
+    if (a->layout == PKV_LAYOUT_BLOCK_TABLE && (!a->block_table || !a->seq_lens || a->block_table_width < 0))
+        return fail(PKV_ERR_INVALID_ARG, "pkv_extend: block-table layout needs block_table and seq_lens");
+    return PKV_OK;
+}
+
+template <int D>
+static pkv_status launch_t(const pkv_extend_args *a, const Plan &pl, void *ws, int32_t *err, cudaStream_t s) {
+    using C = Cfg<D>;
+    Params p{};
+    p.layout = a->layout;
+    p.batch = a->batch;
+    p.hq = a->num_q_heads;
+    p.hkv = a->num_kv_heads;
+    p.g = pl.g;
+    p.g_shift = ilog2(pl.g);
+    p.T = pl.T;
+    p.ps_shift = ilog2(a->page_size);
+    p.ps_mask = a->page_size - 1;
+    p.box_rows = std::min(a->page_size, kTile);
+    p.bt_width = a->block_table_width;
+    p.chunk = pl.chunk;
+    p.max_len = a->max_seq_len;
+    p.scale_log2 = a->sm_scale * kLog2e;
+    p.num_pages = a->num_slots >> p.ps_shift;
+    p.kv_indices_len = a->kv_indices_len;
+    p.total_q = a->total_q;
+    p.qo_indptr = a->qo_indptr;
+    p.kv_end = a->kv_end;
+    p.kv_indptr = a->kv_indptr;
+    p.kv_indices = a->kv_indices;
+    p.kv_last = a->kv_last_page_len;
+    p.block_table = a->block_table;
+    p.seq_lens = a->seq_lens;
+    p.out = static_cast<uint16_t *>(a->out);
+    p.lse = a->lse;
+    p.part_o = static_cast<float *>(ws);
+    p.part_lse = reinterpret_cast<float *>(static_cast<char *>(ws) + pl.part_o_bytes);
+    p.err = err;
+
+    CUtensorMap tmq, tmk, tmv;
+    {   // q [total_q, Hq, D]: boxes of 64 dims x g heads x T tokens = 128 rows of 128 bytes
+        const uint64_t dq[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a->num_q_heads),
+                                static_cast<uint64_t>(std::max<int64_t>(a->total_q, 1))};
+        const uint64_t sq[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(a->num_q_heads) * D * 2};
+        const uint32_t bq[3] = {64, static_cast<uint32_t>(pl.g), static_cast<uint32_t>(pl.T)};
+        if (!encode_tmap_bf16(&tmq, a->q, 3, dq, sq, bq))
+            return fail(PKV_ERR_CUDA, "pkv_extend: cuTensorMapEncodeTiled rejected q");
+        const uint64_t dk[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a->num_kv_heads),
+                                static_cast<uint64_t>(a->num_slots)};
+        const uint64_t sk[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(a->k_row_stride) * 2};
+        const uint64_t sv[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(a->v_row_stride) * 2};
+        const uint32_t bk[3] = {64, 1, static_cast<uint32_t>(p.box_rows)};
+        if (!encode_tmap_bf16(&tmk, a->k_pool, 3, dk, sk, bk) || !encode_tmap_bf16(&tmv, a->v_pool, 3, dk, sv, bk))
+            return fail(PKV_ERR_CUDA, "pkv_extend: cuTensorMapEncodeTiled rejected the pools");
+    }
+    static size_t lim = 0;
+    if (!lim) {
+        int optin = 0, dev = 0;
+        cudaFuncAttributes fa{};
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaFuncGetAttributes(&fa, ext_kernel<D>) != cudaSuccess)
+            return fail(PKV_ERR_CUDA, "pkv_extend: cannot query shared-memory limits");
+        const size_t l = static_cast<size_t>(optin) - fa.sharedSizeBytes;
+        if (cudaFuncSetAttribute(ext_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(l)) !=
+            cudaSuccess)
+            return fail(PKV_ERR_CUDA, "pkv_extend: cannot raise the shared-memory limit");
+        lim = l;
+    }
+    const size_t smem = C::kFixedSmem + (static_cast<size_t>(a->batch) + 1) * 4;
+    if (smem > lim) return fail(PKV_ERR_UNSUPPORTED, "pkv_extend: batch too large for the on-chip item table");
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(pl.items_max, sm_count()));
+    ext_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p, tmq, tmk, tmv);
+    pkv_status st = check_launch("pkv_extend (attention kernel)");
+    if (st != PKV_OK || pl.nch_max <= 1) return st;
+    ext_merge_kernel<D><<<static_cast<unsigned>(pl.groups_max), 256, 0, s>>>(p, pl.groups_max);
+    return check_launch("pkv_extend (merge kernel)");
+}
+
+}  // namespace ext
+}  // namespace pkv
+
+extern "C" size_t pkv_extend_workspace_size(const pkv_extend_args *args) {
+    using namespace pkv::ext;
+    if (!args || validate(args, false) != PKV_OK) return 0;
+    Plan pl;
+    if (!make_plan(args, pl)) return 0;
+    return pl.part_o_bytes + pl.part_lse_bytes;
+}
+
+extern "C" pkv_status pkv_extend(const pkv_extend_args *args, void *workspace, size_t workspace_bytes,
+                                 int32_t *err_flags, pkv_stream_t stream) {
+    using namespace pkv;
+    using namespace pkv::ext;
+    if (!args) return fail(PKV_ERR_INVALID_ARG, "pkv_extend: null args");
+    if (!err_flags) return fail(PKV_ERR_INVALID_ARG, "pkv_extend: err_flags is required");
+    pkv_status st = validate(args, true);
+    if (st != PKV_OK) return st;
+    if (args->batch == 0 || args->total_q == 0) return ok();
+    Plan pl;
+    if (!make_plan(args, pl)) return fail(PKV_ERR_UNSUPPORTED, "pkv_extend: too many work items");
+    const size_t need = pl.part_o_bytes + pl.part_lse_bytes;
+    if (workspace_bytes < need)
+        return fail(PKV_ERR_CAPACITY, "pkv_extend: workspace of %zu bytes, %zu needed", workspace_bytes, need);
+    if (need && (!workspace || !aligned(workspace, 256)))
+        return fail(PKV_ERR_INVALID_ARG, "pkv_extend: workspace must be non-null and 256-byte aligned");
+    auto s = reinterpret_cast<cudaStream_t>(stream);
+    return args->head_dim == 128 ? launch_t<128>(args, pl, workspace, err_flags, s)
+                                 : launch_t<64>(args, pl, workspace, err_flags, s);
+}
+
+extern "C" pkv_status pkv_span_plan(int32_t batch, const int32_t *seg_indptr, const int32_t *seg_kind,
+                                    const int32_t *seg_start, const int32_t *seg_end, int32_t *qo_indptr,
+                                    int32_t *q_pos, int32_t *kv_end, int64_t cap, int32_t *err_flags,
+                                    pkv_stream_t stream) {
+    using namespace pkv;
+    if (batch < 0 || cap < 0) return fail(PKV_ERR_INVALID_ARG, "pkv_span_plan: negative size");
+    if (!err_flags) return fail(PKV_ERR_INVALID_ARG, "pkv_span_plan: err_flags is required");
+    if (batch == 0) return ok();
+    if (!seg_indptr || !seg_kind || !seg_start || !seg_end || !qo_indptr || (cap > 0 && (!q_pos || !kv_end)))
+        return fail(PKV_ERR_INVALID_ARG, "pkv_span_plan: null input");
+    ext::span_plan_kernel<<<batch, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        batch, seg_indptr, seg_kind, seg_start, seg_end, qo_indptr, q_pos, kv_end, cap, err_flags);
+    return check_launch("pkv_span_plan");
+}

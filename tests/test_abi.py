@@ -54,6 +54,33 @@ def test_decode_args_layout_matches_c(binding, tmp_path):
         assert getattr(binding.DecodeArgs, f).offset == off, f
 
 
+def test_extend_args_layout_matches_c(binding, tmp_path):
+    fields = [f[0] for f in binding.ExtendArgs._fields_]
+    src = tmp_path / "layout_ext.c"
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "pkv.h"', "int main(void){",
+             'printf("%zu\\n", sizeof(pkv_extend_args));']
+    lines += ['printf("%%zu\\n", offsetof(pkv_extend_args, %s));' % f for f in fields]
+    lines += ["return 0;}"]
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout_ext"
+    subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    vals = [int(x) for x in subprocess.check_output([str(exe)]).split()]
+    assert vals[0] == ctypes.sizeof(binding.ExtendArgs)
+    for f, off in zip(fields, vals[1:]):
+        assert getattr(binding.ExtendArgs, f).offset == off, f
+    # host-side validation before any launch
+    a = binding.ExtendArgs()
+    flag = ctypes.c_int32(0)
+    a.batch, a.num_q_heads, a.num_kv_heads, a.head_dim, a.page_size = 1, 12, 4, 128, 16
+    assert binding._lib.pkv_extend(ctypes.byref(a), None, 0, ctypes.byref(flag), None) == binding.PKV_ERR_UNSUPPORTED
+    a.num_q_heads, a.head_dim = 16, 96
+    assert binding._lib.pkv_extend(ctypes.byref(a), None, 0, ctypes.byref(flag), None) == binding.PKV_ERR_UNSUPPORTED
+    a.head_dim, a.page_size = 128, 4
+    assert binding._lib.pkv_extend(ctypes.byref(a), None, 0, ctypes.byref(flag), None) == binding.PKV_ERR_UNSUPPORTED
+    assert binding._lib.pkv_extend_workspace_size(ctypes.byref(a)) == 0
+    assert flag.value == 0
+
+
 def test_status_strings_and_version(binding):
     assert binding.pkv_abi_version() == 1
     assert binding.pkv_status_string(0) == "ok"

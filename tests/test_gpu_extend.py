@@ -1,0 +1,140 @@
+"""GPU parity of pkv_extend (multi-query paged attention) and pkv_span_plan against the oracle.
+
+Outputs are compared with the fp64 oracle elementwise within
+|gpu - oracle| <= 2e-2 + 2e-2 |oracle| (bf16 output, fp32 accumulation); the
+span planner's rows and bounds bit for bit.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _harness import assert_close, bf16_to_f64, bits, paged_table
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from paged_kv_cache_req_gb300 import build
+    build.build()
+    from paged_kv_cache_req_gb300 import _binding
+    return _binding
+
+
+def _dev(a, dtype=torch.int32):
+    return torch.as_tensor(np.asarray(a)).to(dtype).cuda()
+
+
+def _case(seed, lens, nq, hq, hkv, d, ps):
+    rng = np.random.default_rng(seed)
+    gen = torch.Generator().manual_seed(seed)
+    num_pages = sum(-(-L // ps) for L in lens) + 8
+    r2t, rpi = paged_table(rng, lens, ps, num_pages)
+    k = torch.randn((num_pages * ps, hkv, d), generator=gen).to(torch.bfloat16)
+    v = torch.randn((num_pages * ps, hkv, d), generator=gen).to(torch.bfloat16)
+    qo = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    q = torch.randn((int(qo[-1]), hq, d), generator=gen).to(torch.bfloat16)
+    return r2t, rpi, num_pages, k, v, q, qo
+
+
+def _run(B, r2t, rpi, num_pages, k, v, q, qo, lens, ps, kv_end=None, chunk=0, layout="csr"):
+    dev = torch.device("cuda")
+    hq, d = q.shape[1], q.shape[2]
+    scale = 1 / math.sqrt(d)
+    st, indptr, indices, last, bt = oracle.build_indices(r2t, rpi, lens, ps, num_pages)
+    assert st == oracle.OK
+    out = torch.full(tuple(q.shape), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((q.shape[0], hq), dtype=torch.float32, device=dev)
+    kw = dict(page_size=ps, sm_scale=scale, max_seq_len=max(max(lens), 1), lse=lse, kv_chunk=chunk,
+              kv_end=None if kv_end is None else _dev(kv_end))
+    kd, vd, qd = k.to(dev), v.to(dev), q.to(dev)
+    if layout == "csr":
+        args = B.make_extend_args(B.PKV_LAYOUT_CSR, qd, kd, vd, out, _dev(qo), kv_indptr=_dev(indptr),
+                                  kv_indices=_dev(indices if len(indices) else [0]), kv_last_page_len=_dev(last), **kw)
+    else:
+        args = B.make_extend_args(B.PKV_LAYOUT_BLOCK_TABLE, qd, kd, vd, out, _dev(qo), block_table=_dev(bt),
+                                  seq_lens=_dev(lens), **kw)
+    ws = torch.empty(max(B.pkv_extend_workspace_size(args), 256), dtype=torch.uint8, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    B.pkv_extend(args, ws, err)
+    torch.cuda.synchronize()
+    if kv_end is None:
+        kv_end = np.concatenate([np.arange(L - n, L) + 1 for L, n in zip(lens, np.diff(qo))]).astype(np.int32)
+    st, ref, ref_lse = oracle.extend(bits(q), bits(k), bits(v), r2t, rpi, lens, qo, kv_end, scale)
+    return err.item(), bf16_to_f64(out), lse.double().cpu().numpy(), st, ref, ref_lse
+
+
+@pytest.mark.parametrize("hq,hkv,d,ps", [(32, 8, 128, 64), (16, 16, 128, 16), (8, 1, 64, 8), (32, 4, 128, 32),
+                                         (16, 1, 128, 64)])
+def test_extend_causal_mix(B, hq, hkv, d, ps):
+    # prefill (n = L), chunked prefill (n < L), one new token, 4 draft tokens, long prefix
+    lens = [300, 517, 129, 1000, 64, 3001]
+    nq = [300, 200, 1, 4, 64, 37]
+    case = _case(hq + d + ps, lens, nq, hq, hkv, d, ps)
+    e, gpu, g_lse, st, ref, ref_lse = _run(B, *case, lens, ps)
+    assert e == 0 and st == oracle.OK
+    assert_close(gpu, ref, "extend out hq=%d hkv=%d d=%d ps=%d" % (hq, hkv, d, ps))
+    assert_close(g_lse, ref_lse, "extend lse")
+
+
+@pytest.mark.parametrize("chunk", [64, 192, 1024])
+@pytest.mark.parametrize("layout", ["csr", "block_table"])
+def test_extend_split_keys_and_layouts(B, chunk, layout):
+    lens = [2000, 77, 900, 4100]
+    nq = [4, 77, 16, 9]
+    case = _case(chunk, lens, nq, 32, 8, 128, 16)
+    e, gpu, g_lse, st, ref, ref_lse = _run(B, *case, lens, 16, chunk=chunk, layout=layout)
+    assert e == 0 and st == oracle.OK
+    assert_close(gpu, ref, "extend split %d %s" % (chunk, layout))
+    assert_close(g_lse, ref_lse, "extend split lse")
+
+
+def test_span_plan_and_span_attention(B):
+    # a diffusion row: causal text prefix then a full image span, and a later step
+    # that queries only the image span against prefix + image
+    segs = [[(0, 0, 100), (1, 100, 356)], [(1, 100, 356)], [(0, 0, 40)], []]
+    ind, kinds, starts, ends = [0], [], [], []
+    for row in segs:
+        for kd, a, e in row:
+            kinds.append(kd)
+            starts.append(a)
+            ends.append(e)
+        ind.append(len(kinds))
+    st, qo_ref, qpos_ref, kend_ref = oracle.span_plan(segs)
+    assert st == oracle.OK
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qo = torch.empty(len(segs) + 1, dtype=torch.int32, device="cuda")
+    qpos = torch.empty(len(qpos_ref), dtype=torch.int32, device="cuda")
+    kend = torch.empty(len(qpos_ref), dtype=torch.int32, device="cuda")
+    B.pkv_span_plan(_dev(ind), _dev(kinds), _dev(starts), _dev(ends), qo, qpos, kend, err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert qo.cpu().numpy().tolist() == qo_ref.tolist()
+    assert np.array_equal(qpos.cpu().numpy(), qpos_ref) and np.array_equal(kend.cpu().numpy(), kend_ref)
+    lens = [356, 356, 40, 10]
+    case = list(_case(11, lens, np.diff(qo_ref).tolist(), 16, 4, 128, 16))
+    e, gpu, g_lse, st, ref, ref_lse = _run(B, *case, lens, 16, kv_end=kend_ref)
+    assert e == 0 and st == oracle.OK
+    assert_close(gpu, ref, "span attention")
+    assert_close(g_lse, ref_lse, "span attention lse")
+
+
+def test_extend_edges(B):
+    # a request with no query rows, an empty request with kv_end 0, a row whose bound is 1
+    lens = [50, 0, 20, 33]
+    nq = [0, 2, 3, 1]
+    case = list(_case(5, lens, nq, 8, 2, 64, 8))
+    kv_end = np.array([0, 0, 1, 5, 20, 33], np.int32)
+    e, gpu, g_lse, st, ref, ref_lse = _run(B, *case, lens, 8, kv_end=kv_end)
+    assert e == 0 and st == oracle.OK
+    assert (gpu[:2] == 0).all() and np.isneginf(g_lse[:2]).all()
+    assert_close(gpu, ref, "extend edges")
+    # a bound past the request's keys is a range error; that row reads as empty
+    bad = kv_end.copy()
+    bad[3] = 21
+    e, gpu, g_lse, st, ref, ref_lse = _run(B, *case, lens, 8, kv_end=bad)
+    assert e == B.PKV_DEVERR_RANGE and st == oracle.ERR_RANGE
+    assert (gpu[3] == 0).all()
