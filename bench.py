@@ -53,6 +53,15 @@ WORKLOAD_TEXT = {
     "encoder_merge": "Qwen3-VL-32B-shaped encoder-cache read path: 30 cached 512x512 images (256 tokens each, one 512-row block each) of fat_dim 20480 bf16 gathered into an 8672-row prefill sequence",
 }
 MERGE_METRIC = "encoder-cache merge GB/s (bytes read + written)"
+WORKLOAD_TEXT.update({
+    "llama3_8b_verify": "Llama-3-8B-shaped speculative target-verify: batch 128, cached lengths log-U[128,32768] + 4 draft tokens per request (causal), 32 q / 8 kv heads x 128, page_size 64",
+    "qwen3_0p6b_prefill": "Qwen3-0.6B-shaped chunked prefill: 8 requests, cached prefix U[0,4096] + a 1024-token chunk each (causal), 16 q / 8 kv heads x 128, page_size 16",
+    "hunyuan_image_spans": "HunyuanImage-shaped first denoising step: 4 rows (2 requests x 2 CFG branches) of a 1024-token causal text segment + a 4096-token full image segment, all 5120 positions queried, 32 q / 8 kv heads x 128, page_size 64",
+})
+EXTEND_WORKLOADS = ("llama3_8b_verify", "qwen3_0p6b_prefill", "hunyuan_image_spans")
+EXTEND_METRIC = {"llama3_8b_verify": ("paged multi-query attention KV-read GB/s (target-verify)", "GB/s", "hbm"),
+                 "qwen3_0p6b_prefill": ("paged multi-query attention TFLOP/s (chunked prefill)", "TFLOP/s", "tensor"),
+                 "hunyuan_image_spans": ("paged multi-query attention TFLOP/s (causal + full spans)", "TFLOP/s", "tensor")}
 
 
 # ---------------------------------------------------------------- accounting
@@ -436,12 +445,244 @@ def run_merge(args, world, rank, local, dist):
     return 0
 
 
+# ---------------------------------------------------------------- multi-query steps
+def extend_rows(ew):
+    """Per request: its query rows' key bounds (numpy int64)."""
+    import oracle
+    lens = ew.seq_lens.numpy().astype(np.int64)
+    qo = ew.qo_lens.numpy().astype(np.int64)
+    if ew.segments is not None:
+        st, _, _, kend = oracle.span_plan(ew.segments)
+        assert st == oracle.OK
+        ind = np.concatenate([[0], np.cumsum(qo)])
+        return [kend[ind[b]:ind[b + 1]].astype(np.int64) for b in range(ew.batch)]
+    return [np.arange(L - n, L) + 1 for L, n in zip(lens, qo)]
+
+
+def extend_amounts(ew):
+    """(attention flops of the step, algorithmic bytes of the step, bytes of the extend launch)."""
+    kv_row = 2 * ew.num_kv_heads * ew.head_dim * 2
+    rows = extend_rows(ew)
+    flops = sum(4.0 * ew.num_q_heads * ew.head_dim * float(r.sum()) for r in rows)
+    lens = ew.seq_lens.numpy().astype(np.int64)
+    keys = int(sum(int(r.max()) if len(r) else 0 for r in rows))       # keys a block of the request reads
+    total_q = int(ew.qo_lens.sum())
+    pages = int((-(-lens // ew.page_size)).sum())
+    launch = keys * kv_row + total_q * ew.num_q_heads * ew.head_dim * 2 * 2 + pages * 4
+    step = launch + int(lens.sum()) * 4 + pages * 4 + 2 * int(ew.new_lens.sum()) * kv_row   # + table, page list, store
+    return flops, step, launch
+
+
+def extend_oracle_sample(ew, budget_pairs, fetch_kv=None, seed=0, num_threads=0):
+    """fp64 oracle on a bounded sample: whole requests while they fit the budget in
+    (row, head, visible key) units, else evenly spaced rows of one request.
+    Returns (seconds, flops, bytes, description, threads)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    rows = extend_rows(ew)
+    r2t = ew.req_to_token.numpy()
+    rpi = ew.req_pool_idx.numpy().astype(np.int64)
+    lens = ew.seq_lens.numpy().astype(np.int64)
+    sel = []
+    acc = 0
+    for b in rng.permutation(ew.batch):
+        cost = int(rows[b].sum()) * ew.num_q_heads
+        if acc + cost <= budget_pairs:
+            sel.append((int(b), np.arange(len(rows[b]))))
+            acc += cost
+        else:
+            room = max(1, (budget_pairs - acc) // max(1, int(rows[b].mean()) * ew.num_q_heads))
+            pick = np.linspace(0, len(rows[b]) - 1, num=min(len(rows[b]), room)).astype(np.int64)
+            sel.append((int(b), pick))
+            acc += int(rows[b][pick].sum()) * ew.num_q_heads
+            break
+    used = [r2t[rpi[b], :lens[b]].astype(np.int64) for b, _ in sel]
+    allslots = np.unique(np.concatenate(used))
+    table = np.zeros((len(sel) + 1, max(int(lens.max()), 1)), dtype=np.int32)
+    for i, (b, _) in enumerate(sel):
+        table[i + 1, :lens[b]] = np.searchsorted(allslots, used[i])
+    if fetch_kv is not None:
+        k, v = fetch_kv(allslots)
+    else:
+        nrng = np.random.default_rng(17 + seed)
+        shape = (len(allslots), ew.num_kv_heads, ew.head_dim)
+        k = (nrng.standard_normal(size=shape, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        v = (nrng.standard_normal(size=shape, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    kend = np.concatenate([rows[b][pick] for b, pick in sel]).astype(np.int32)
+    qo = np.concatenate([[0], np.cumsum([len(pick) for _, pick in sel])]).astype(np.int32)
+    gen = torch.Generator().manual_seed(23 + seed)
+    q = torch.randn((int(qo[-1]), ew.num_q_heads, ew.head_dim), generator=gen).to(torch.bfloat16) \
+        .view(torch.int16).numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    st, out, lse = oracle.extend(q, k, v, table, np.arange(1, len(sel) + 1, dtype=np.int32),
+                                 [int(lens[b]) for b, _ in sel], qo, kend, ew.sm_scale, num_threads=num_threads)
+    secs = time.perf_counter() - t0
+    assert st == oracle.OK
+    flops = 4.0 * ew.num_q_heads * ew.head_dim * float(kend.sum())
+    kv_row = 2 * ew.num_kv_heads * ew.head_dim * 2
+    nbytes = len(allslots) * kv_row + int(qo[-1]) * ew.num_q_heads * ew.head_dim * 4
+    desc = "%d query rows of %d request(s) (%d row x head x key triples), compact host pool" % (
+        int(qo[-1]), len(sel), int(kend.sum()) * ew.num_q_heads)
+    return secs, flops, nbytes, desc, (oracle.max_threads() if num_threads <= 0 else num_threads)
+
+
+def reference_extend(args, world):
+    from paged_kv_cache_req_gb300.workloads import make_extend_workload
+    import oracle
+    oracle.build()
+    ew = make_extend_workload(args.workload, seed=args.seed, batch=args.batch)
+    metric, unit, _ = EXTEND_METRIC[args.workload]
+    for _ in range(args.warmup):
+        extend_oracle_sample(ew, args.ref_key_heads // 8, seed=0)
+    secs = flops = nbytes = 0.0
+    desc, threads = "", 0
+    for i in range(args.steps):
+        s_, f_, b_, desc, threads = extend_oracle_sample(ew, args.ref_key_heads // 2, seed=i)
+        secs += s_
+        flops += f_
+        nbytes += b_
+    value = (flops / secs / 1e12) if unit == "TFLOP/s" else (nbytes / secs / 1e9)
+    line = {"impl": "reference", "metric": metric, "value": round(value, 6), "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "batch": ew.batch},
+            "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": threads, "kind": "oracle",
+                             "sample": "each step: " + desc},
+            "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_extend(args, world, rank, local, dist):
+    from paged_kv_cache_req_gb300.engine import ExtendStep
+    from paged_kv_cache_req_gb300.workloads import make_extend_workload
+    import oracle
+    oracle.build()
+    ew = make_extend_workload(args.workload, seed=args.seed, batch=args.batch)
+    metric, unit, bound = EXTEND_METRIC[args.workload]
+    step = ExtendStep(ew, device="cuda", kv_chunk=args.kv_chunk, seed=args.seed)
+    flops, step_bytes_, launch_bytes = extend_amounts(ew)
+    amount = flops / 1e12 if unit == "TFLOP/s" else step_bytes_ / 1e9
+    launch_amount = flops / 1e12 if unit == "TFLOP/s" else launch_bytes / 1e9
+    flush = step_bytes_ < 4 * L2_BYTES
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda") if flush else None
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    if step.check_errors():
+        raise SystemExit("device error flags raised: %d" % step.check_errors())
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local, enabled=not args.profile_run)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        if flush:
+            flush_buf.zero_()
+        ev[i][0].record(stream)
+        step.build_indices()
+        step.store()
+        step.plan()
+        kev[i][0].record(stream)
+        step.attend()
+        kev[i][1].record(stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    soak = 0
+    if clocks.proc is not None and not args.profile_run and clocks.count() - clocks.start_count < 5:
+        t_soak = time.perf_counter()
+        while clocks.count() - clocks.start_count < 5 and time.perf_counter() - t_soak < 3.0:
+            for _ in range(max(1, args.steps)):
+                step.run()
+                soak += 1
+            torch.cuda.synchronize()
+    clk = clocks.stop()
+    if clk is not None:
+        clk["window"] = "timed region" + (" + %d untimed steps of the same load" % soak if soak else "")
+    if step.check_errors():
+        raise SystemExit("device error flags raised: %d" % step.check_errors())
+    tot_ms = reduce_max(sum(a.elapsed_time(b) for a, b in ev), dist, "cuda")
+    k_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
+    value = world * amount * args.steps / (tot_ms / 1e3)
+    if args.profile_run:
+        if rank == 0:
+            print(json.dumps({"profile_run": True, "workload": args.workload, "ms_per_step": round(tot_ms / args.steps, 4),
+                              "extend_ms": round(k_ms, 4)}))
+        return 0
+    h_in, h_out = step.host_step_tensors()
+    from paged_kv_cache_req_gb300.engine import DecodeStep
+    h2d, d2h = DecodeStep.bytes_of(h_in), DecodeStep.bytes_of(h_out)
+    for _ in range(2):
+        step.run_from_host(h_in, h_out)
+    torch.cuda.synchronize()
+    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        if flush:
+            flush_buf.zero_()
+        e_ev[i][0].record(stream)
+        step.run_from_host(h_in, h_out)
+        e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in e_ev), dist, "cuda")
+    if rank != 0:
+        return 0
+    hbm, bf16, bf16_sus, peak_kind = measured_peaks()
+    peak = hbm if bound == "hbm" else bf16
+    achieved = launch_amount / (k_ms / 1e3)
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        def fetch(slots):
+            idx = torch.from_numpy(slots).cuda()
+            return (step.k_pool[idx].cpu().view(torch.int16).numpy().view(np.uint16),
+                    step.v_pool[idx].cpu().view(torch.int16).numpy().view(np.uint16))
+        tot_s = tot_f = tot_b = 0.0
+        passes, desc, threads = 0, "", 0
+        while passes < 10 and (tot_s < 3.0 or passes == 0):
+            s_, f_, b_, desc, threads = extend_oracle_sample(ew, args.cpu_key_heads // 4, fetch_kv=fetch, seed=passes)
+            tot_s += s_
+            tot_f += f_
+            tot_b += b_
+            passes += 1
+        cv = tot_f / tot_s / 1e12 if unit == "TFLOP/s" else tot_b / tot_s / 1e9
+        cpu = {"value": round(cv, 6), "unit": unit, "cores": threads, "kind": "oracle",
+               "sample": desc + "; %d pass(es), %.1f s of fp64 attention on %d host threads" % (passes, tot_s, threads),
+               "host_cpus": os.cpu_count()}
+    line = {
+        "metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(tot_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "accumulate": "fp32", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "batch": ew.batch,
+                   "query_rows": int(ew.qo_lens.sum()), "keys": int(ew.seq_lens.sum()),
+                   "attention_flops_per_step": flops, "algorithmic_bytes_per_step": step_bytes_,
+                   "l2": "flushed between steps (2x L2 write)" if flush else "inputs larger than L2",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": bound, "kernel": "pkv_extend (attention kernel + merge)", "achieved": round(achieved, 3),
+                     "peak": peak, "unit": unit, "frac": round(achieved / peak, 4),
+                     "peak_kind": peak_kind + (" (bf16 dense, burst)" if bound == "tensor" else ""),
+                     "avg_launch_ms": round(k_ms, 4), "traffic": None},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(world * amount * args.steps / (e_ms / 1e3), 3), "unit": unit,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms / args.steps, 4)},
+        "gpu_launches": step.launches_per_step() * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
     if args.workload == "encoder_merge":
         return reference_merge(args, world)
+    if args.workload in EXTEND_WORKLOADS:
+        return reference_extend(args, world)
     from paged_kv_cache_req_gb300.workloads import make_workload
     wl = make_workload(args.workload, batch=args.batch)
     import oracle
@@ -486,6 +727,8 @@ def run_ours(args):
 
     if args.workload == "encoder_merge":
         return run_merge(args, world, rank, local, dist)
+    if args.workload in EXTEND_WORKLOADS:
+        return run_extend(args, world, rank, local, dist)
     wl = make_workload(args.workload, seed=args.seed, batch=args.batch)
     step = DecodeStep(wl, device="cuda", cross_mode=args.cross_mode, kv_chunk=args.kv_chunk, seed=args.seed,
                       alloc=args.alloc)

@@ -34,7 +34,7 @@ import torch
 from . import _binding as B
 from .workloads import Workload, fill_pool, make_values
 
-__all__ = ["DecodeStep"]
+__all__ = ["DecodeStep", "ExtendStep"]
 
 
 class _ProblemBuffers:
@@ -246,3 +246,113 @@ class DecodeStep:
     @staticmethod
     def bytes_of(tensors) -> int:
         return int(sum(t.numel() * t.element_size() for t in tensors.values()))
+
+
+class ExtendStep:
+    """One multi-query step over a paged KV cache (extend / target-verify / span rows):
+
+        pkv_build_indices   req_to_token -> kv_indptr / kv_indices
+        pkv_store           this step's new tokens' K/V -> their pool slots
+        pkv_span_plan       (rows with segments) segment lists -> query rows and key bounds
+        pkv_extend          attention of every query row over its visible keys
+    """
+
+    def __init__(self, ew, device="cuda", kv_chunk: int = 0, seed: Optional[int] = None):
+        self.ew = ew
+        dev = self.device = torch.device(device)
+        seed = ew.seed if seed is None else seed
+        B_ = ew.batch
+        self.r2t = ew.req_to_token.to(dev)
+        self.req_pool_idx = ew.req_pool_idx.to(dev)
+        self.seq_lens = ew.seq_lens.to(dev)
+        self.slot_mapping = ew.slot_mapping.to(dev)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(4_000_037 + seed)
+        shape = (ew.num_slots, ew.num_kv_heads, ew.head_dim)
+        self.k_pool = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+        self.v_pool = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+        for t in (self.k_pool, self.v_pool):
+            flat = t.view(-1)
+            for i in range(0, flat.numel(), 1 << 28):
+                flat[i:i + (1 << 28)].normal_(generator=gen)
+        cgen = torch.Generator().manual_seed(5_000_011 + seed)
+        total_q = int(ew.qo_lens.sum())
+        n_new = int(ew.new_lens.sum())
+        self.q = torch.randn((total_q, ew.num_q_heads, ew.head_dim), generator=cgen).to(torch.bfloat16).to(dev)
+        self.k_new = torch.randn((n_new, ew.num_kv_heads, ew.head_dim), generator=cgen).to(torch.bfloat16).to(dev)
+        self.v_new = torch.randn((n_new, ew.num_kv_heads, ew.head_dim), generator=cgen).to(torch.bfloat16).to(dev)
+        qo = np.concatenate([[0], np.cumsum(ew.qo_lens.numpy())]).astype(np.int32)
+        self.qo_indptr = torch.from_numpy(qo).to(dev)
+        self.kv_end = None
+        if ew.segments is not None:
+            ind, kinds, starts, ends = [0], [], [], []
+            for segs in ew.segments:
+                for kd, a, e in segs:
+                    kinds.append(kd)
+                    starts.append(a)
+                    ends.append(e)
+                ind.append(len(kinds))
+            self.seg = [torch.tensor(x, dtype=torch.int32, device=dev) for x in (ind, kinds, starts, ends)]
+            self.plan_qo = torch.empty(B_ + 1, dtype=torch.int32, device=dev)
+            self.q_pos = torch.empty(total_q, dtype=torch.int32, device=dev)
+            self.kv_end = torch.empty(total_q, dtype=torch.int32, device=dev)
+        ps = ew.page_size
+        pages = int((-(-ew.seq_lens.numpy().astype(np.int64) // ps)).sum())
+        self.kv_indptr = torch.empty(B_ + 1, dtype=torch.int32, device=dev)
+        self.kv_indices = torch.empty(max(pages, 1), dtype=torch.int32, device=dev)
+        self.kv_last = torch.empty(B_, dtype=torch.int32, device=dev)
+        self.out = torch.empty((total_q, ew.num_q_heads, ew.head_dim), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((total_q, ew.num_q_heads), dtype=torch.float32, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.args = B.make_extend_args(B.PKV_LAYOUT_CSR, self.q, self.k_pool, self.v_pool, self.out, self.qo_indptr,
+                                       page_size=ps, sm_scale=ew.sm_scale, max_seq_len=int(ew.seq_lens.max()),
+                                       kv_end=self.kv_end, kv_indptr=self.kv_indptr, kv_indices=self.kv_indices,
+                                       kv_last_page_len=self.kv_last, lse=self.lse, kv_chunk=kv_chunk)
+        self.ws_bytes = B.pkv_extend_workspace_size(self.args)
+        self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
+
+    def build_indices(self):
+        ew = self.ew
+        B.pkv_build_indices(self.r2t, self.req_pool_idx, self.seq_lens, ew.page_size, ew.num_pool_pages, self.err,
+                            kv_indptr=self.kv_indptr, kv_indices=self.kv_indices, kv_last_page_len=self.kv_last)
+
+    def store(self):
+        B.pkv_store(self.k_pool, self.v_pool, self.k_new, self.v_new, self.slot_mapping, self.err)
+
+    def plan(self):
+        if self.kv_end is not None:
+            B.pkv_span_plan(*self.seg, self.plan_qo, self.q_pos, self.kv_end, self.err)
+
+    def attend(self):
+        B.pkv_extend(self.args, self.workspace, self.err)
+
+    def run(self):
+        self.build_indices()
+        self.store()
+        self.plan()
+        self.attend()
+
+    def launches_per_step(self) -> int:
+        return 3 + (1 if self.kv_end is not None else 0) + (1 if self.ws_bytes > 0 else 0)
+
+    def check_errors(self) -> int:
+        return int(self.err.item())
+
+    def host_step_tensors(self):
+        h_in = {"q": self.q.cpu().pin_memory(), "k_new": self.k_new.cpu().pin_memory(),
+                "v_new": self.v_new.cpu().pin_memory(), "seq_lens": self.seq_lens.cpu().pin_memory(),
+                "slot_mapping": self.slot_mapping.cpu().pin_memory(), "qo_indptr": self.qo_indptr.cpu().pin_memory()}
+        if self.kv_end is not None:
+            for i, t in enumerate(self.seg):
+                h_in["seg%d" % i] = t.cpu().pin_memory()
+        return h_in, {"out": torch.empty_like(self.out, device="cpu").pin_memory()}
+
+    def run_from_host(self, h_in, h_out):
+        for name, t in (("q", self.q), ("k_new", self.k_new), ("v_new", self.v_new), ("seq_lens", self.seq_lens),
+                        ("slot_mapping", self.slot_mapping), ("qo_indptr", self.qo_indptr)):
+            t.copy_(h_in[name], non_blocking=True)
+        if self.kv_end is not None:
+            for i, t in enumerate(self.seg):
+                t.copy_(h_in["seg%d" % i], non_blocking=True)
+        self.run()
+        h_out["out"].copy_(self.out, non_blocking=True)

@@ -45,6 +45,9 @@ __all__ = [
     "MergeWorkload",
     "make_encoder_merge",
     "fill_merge_buffers",
+    "EXTEND_CONFIGS",
+    "ExtendWorkload",
+    "make_extend_workload",
 ]
 
 
@@ -388,3 +391,93 @@ def fill_merge_buffers(mw: MergeWorkload, device="cpu", chunk_elems: int = 1 << 
             flat[i:i + chunk_elems].normal_(generator=gen)
         out.append(t)
     return out[0], out[1]
+
+
+# --------------------------------------------------------------------------
+# Multi-query steps: target-verify, chunked prefill, diffusion rows with spans
+# --------------------------------------------------------------------------
+EXTEND_CONFIGS: Dict[str, dict] = {
+    # Llama-3-8B shapes, speculative target-verify of 4 draft tokens per request
+    # over cached lengths log-U[128, 32768] (the large-batch decode mix), page 64.
+    "llama3_8b_verify": dict(batch=128, hq=32, hkv=8, d=128, ps=64, cached=("loguniform", 128, 32768),
+                             new=("fixed", 4, 4)),
+    # Qwen3-0.6B shapes, chunked prefill: 8 requests with a cached prefix U[0, 4096]
+    # and a 1024-token chunk each (causal), page 16.
+    "qwen3_0p6b_prefill": dict(batch=8, hq=16, hkv=8, d=128, ps=16, cached=("uniform", 0, 4096),
+                               new=("fixed", 1024, 1024)),
+    # HunyuanImage-shaped first denoising step: 2 requests x 2 CFG rows, a 1024-token
+    # text prefix (causal segment) then 4096 image tokens (one full segment), all
+    # positions queried, 32 q / 8 kv heads x 128, page 64.
+    "hunyuan_image_spans": dict(batch=4, hq=32, hkv=8, d=128, ps=64, cached=("fixed", 0, 0),
+                                new=("fixed", 5120, 5120), spans=((0, 0, 1024), (1, 1024, 5120))),
+}
+
+
+@dataclass
+class ExtendWorkload:
+    """Index structures of a multi-query step: request b holds seq_lens[b] keys, the
+    last new_lens[b] of which are stored this step; its qo_lens[b] query rows are
+    its last positions (causal) or, with `segments`, its segments' positions."""
+    name: str
+    batch: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    sm_scale: float
+    num_slots: int
+    req_to_token: torch.Tensor     # int32 [rows, W]
+    req_pool_idx: torch.Tensor     # int32 [B]
+    seq_lens: torch.Tensor         # int32 [B]
+    new_lens: torch.Tensor         # int32 [B]
+    qo_lens: torch.Tensor          # int32 [B]
+    slot_mapping: torch.Tensor     # int32 [sum new_lens]: slots of the stored positions
+    segments: Optional[List[List[tuple]]] = None
+    seed: int = 0
+
+    @property
+    def num_pool_pages(self) -> int:
+        return self.num_slots // self.page_size
+
+
+def _draw(rng, spec, batch):
+    kind, lo, hi = spec
+    if kind == "fixed":
+        return np.full(batch, lo, dtype=np.int64)
+    return _draw_lengths(rng, (kind, lo, hi), batch)
+
+
+def make_extend_workload(name: str, seed: int = 0, batch: Optional[int] = None) -> ExtendWorkload:
+    cfg = dict(EXTEND_CONFIGS[name])
+    B = int(batch if batch is not None else cfg["batch"])
+    rng = np.random.default_rng(seed)
+    ps = int(cfg["ps"])
+    cached = _draw(rng, cfg["cached"], B)
+    new = _draw(rng, cfg["new"], B)
+    lens = cached + new
+    need_pages = int((-(-lens // ps)).sum())
+    num_pages = int(math.ceil(need_pages * 1.25)) + 8
+    width = round_up(int(lens.max()) + 1, 32)
+    r2t = np.zeros((B + 1, width), dtype=np.int32)
+    rpi = (rng.permutation(B) + 1).astype(np.int32)
+    alloc = _PageAllocator(rng, num_pages)
+    slots_new = []
+    for b in range(B):
+        pages = alloc.take(int(-(-lens[b] // ps)))
+        row = _pages_to_slots(pages, ps, int(lens[b]))
+        r2t[rpi[b], :lens[b]] = row
+        slots_new.append(row[cached[b]:])
+    segments = None
+    if "spans" in cfg:
+        segments = [[tuple(sp) for sp in cfg["spans"]] for _ in range(B)]
+        qo = np.array([sum(e - a for _, a, e in segs) for segs in segments], dtype=np.int64)
+    else:
+        qo = new
+    return ExtendWorkload(name=name, batch=B, num_q_heads=cfg["hq"], num_kv_heads=cfg["hkv"], head_dim=cfg["d"],
+                          page_size=ps, sm_scale=1.0 / math.sqrt(cfg["d"]), num_slots=num_pages * ps,
+                          req_to_token=torch.from_numpy(r2t), req_pool_idx=torch.from_numpy(rpi),
+                          seq_lens=torch.from_numpy(lens.astype(np.int32)),
+                          new_lens=torch.from_numpy(new.astype(np.int32)),
+                          qo_lens=torch.from_numpy(qo.astype(np.int32)),
+                          slot_mapping=torch.from_numpy(np.concatenate(slots_new).astype(np.int32)),
+                          segments=segments, seed=seed)
