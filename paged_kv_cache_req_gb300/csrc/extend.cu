@@ -24,7 +24,7 @@
 namespace pkv {
 namespace ext {
 
-constexpr int kRows = 128, kTile = 64, kStages = 4;
+constexpr int kRows = 128, kTile = 64;
 constexpr int kThreads = 224;              // warps 0-3 softmax, 4 producer, 5 q.k, 6 P.V
 constexpr int kProducerWarp = 4, kQkWarp = 5, kPvWarp = 6;
 constexpr int kPrefetch = 3;
@@ -34,6 +34,7 @@ constexpr float kLazy = 8.f;
 
 template <int D>
 struct Cfg {
+    static constexpr int kStages = D == 128 ? 5 : 8;           // K/V ring depth (about 190 KB either way)
     static constexpr int kSl = D / 64;                         // 64-dim slabs
     static constexpr int kQBytes = kSl * kRows * 128;          // q block, SW128 K-major
     static constexpr int kKBytes = kSl * kTile * 128;          // one K (or V) tile
@@ -41,7 +42,7 @@ struct Cfg {
     static constexpr int kOffQ = 0;
     static constexpr int kOffKV = kOffQ + kQBytes;
     static constexpr int kOffBar = kOffKV + kStages * kStageBytes;
-    static constexpr int kNumBars = 24;
+    static constexpr int kNumBars = 32;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;    // tmem slot, abort flag, scan scratch
     static constexpr int kOffTable = kOffMisc + 64;
     static constexpr int kFixedSmem = kOffTable + 1024;        // + item table + alignment slack
@@ -226,7 +227,7 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 enum Bar {
-    kQFull = 0, kQEmpty, kKvFull0, kKvEmpty0 = kKvFull0 + kStages, kSFull0 = kKvEmpty0 + kStages,
+    kQFull = 0, kQEmpty, kKvFull0, kKvEmpty0 = kKvFull0 + 8, kSFull0 = kKvEmpty0 + 8,
     kSFree0 = kSFull0 + 2, kPFull0 = kSFree0 + 2, kPFree0 = kPFull0 + 2, kODone = kPFree0 + 2, kOFree, kFinalQk,
     kFinalPv, kBarCount
 };
@@ -236,7 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
            const __grid_constant__ CUtensorMap tmv) {
     using C = Cfg<D>;
-    static_assert(kBarCount <= C::kNumBars, "barrier slots");
+    constexpr int kStages = C::kStages;
+    static_assert(kBarCount <= C::kNumBars && kStages <= 8, "barrier slots");
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     unsigned char *sQ = smem + C::kOffQ;
@@ -472,7 +474,9 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             }
             for (int ti = 0; ti < it.n_tiles; ++ti, ++n) {
                 const int key0 = it.k0 + ti * kTile;
-                const int vis = max(0, min(min(kend, it.k1) - key0, kTile));
+                // rows past the block's tokens are never written: they only mask the
+                // keys past the chunk (stale data), which keeps full tiles select-free
+                const int vis = max(0, min(min(valid ? kend : it.k1, it.k1) - key0, kTile));
                 ok = warp_wait(ok, &bars[kSFull0 + (n & 1)], (n >> 1) & 1, abort_flag, p.err);
                 float x[64];
                 if (ok) {
@@ -485,11 +489,22 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                 tc05::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[kSFree0 + (n & 1)]);
-                float mx = -INFINITY;
+                // keys at or past the row's bound read as -inf (no selects when the
+                // whole tile is inside every row's bound); max over a tree of pairs
+                if (!__all_sync(0xffffffffu, vis == kTile)) {
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    x[j] = j < vis ? x[j] * p.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, x[j]);
+                    for (int j = 0; j < 64; ++j) x[j] = j < vis ? x[j] : -INFINITY;
+                }
+                float mx;
+                {
+                    float t[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) t[j] = fmaxf(x[2 * j], x[2 * j + 1]);
+#pragma unroll
+                    for (int w2 = 16; w2 >= 1; w2 >>= 1)
+#pragma unroll
+                        for (int j = 0; j < w2; ++j) t[j] = fmaxf(t[j], t[j + w2]);
+                    mx = t[0] * p.scale_log2;   // scores are unscaled up to here (the scale is positive)
                 }
                 const bool raise = mx > m + kLazy || (m == -INFINITY && mx != -INFINITY);
                 const float corr = raise ? ex2(m - mx) : 1.f;
@@ -514,10 +529,11 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                 }
                 uint32_t h[32];
                 float lsum = 0.f;
+                const float nm = -m;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float p0 = m == -INFINITY ? 0.f : ex2(x[2 * j] - m);
-                    const float p1 = m == -INFINITY ? 0.f : ex2(x[2 * j + 1] - m);
+                for (int j = 0; j < 32; ++j) {   // p = 2^(scale log2(e) s - m)
+                    const float p0 = m == -INFINITY ? 0.f : ex2(fmaf(x[2 * j], p.scale_log2, nm));
+                    const float p1 = m == -INFINITY ? 0.f : ex2(fmaf(x[2 * j + 1], p.scale_log2, nm));
                     lsum += p0 + p1;
                     h[j] = pack_bf16x2(p0, p1);
                 }

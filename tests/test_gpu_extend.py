@@ -138,3 +138,16 @@ def test_extend_edges(B):
     e, gpu, g_lse, st, ref, ref_lse = _run(B, *case, lens, 8, kv_end=bad)
     assert e == B.PKV_DEVERR_RANGE and st == oracle.ERR_RANGE
     assert (gpu[3] == 0).all()
+
+
+def test_extend_verify_long_rows(B):
+    # few live rows per block (4 draft tokens x 4 heads of 128) over long key ranges, many
+    # items per CTA: the idle row groups must stay in step with the live one
+    rng = np.random.default_rng(21)
+    lens = rng.integers(6000, 20000, 24).tolist()
+    nq = [4] * 24
+    case = _case(21, lens, nq, 32, 8, 128, 64)
+    e, gpu, g_lse, st, ref, ref_lse = _run(B, *case, lens, 64)
+    assert e == 0 and st == oracle.OK
+    assert_close(gpu, ref, "verify long rows")
+    assert_close(g_lse, ref_lse, "verify long rows lse")
