@@ -7,10 +7,12 @@
 // (request, kv head, block of 128 query rows, chunk of keys): the rows are the
 // (token, query head) pairs of 128 / g consecutive tokens times the g query
 // heads sharing the kv head, so every K/V tile serves the whole block.  Per CTA:
-//   warp 4     TMA producer: the block's q (one 3-D box per 64-dim slab, rows
-//              token-major), then K/V tiles of 64 keys (one box per page per
-//              slab) through a 4-stage ring, tiles three ahead pulled into L2;
-//   warp 5     S = Q K^T (M = 128, N = 64) into one of two TMEM score buffers;
+//   warp 4     TMA producer: K/V tiles of 64 keys (one box per page per slab)
+//              through a 5-stage ring (8 at head_dim 64), pool rows looked up
+//              32 boxes at a time, the next q block pulled into L2;
+//   warp 5     loads the block's q (one 3-D box per 64-dim slab, rows
+//              token-major), then S = Q K^T (M = 128, N = 64) into one of two
+//              TMEM score buffers;
 //   warp 6     O += P V (N = head_dim) from one of two TMEM P buffers;
 //   warps 0-3  one query row per thread: mask keys at or past the row's bound,
 //              online softmax (base 2, running max raised only past 2^8), P.
@@ -27,7 +29,6 @@ namespace ext {
 constexpr int kRows = 128, kTile = 64;
 constexpr int kThreads = 224;              // warps 0-3 softmax, 4 producer, 5 q.k, 6 P.V
 constexpr int kProducerWarp = 4, kQkWarp = 5, kPvWarp = 6;
-constexpr int kPrefetch = 3;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kLog2e = 1.44269504088896341f;
 constexpr float kLazy = 8.f;
@@ -226,6 +227,13 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Three-input maximum (one instruction on this architecture).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 enum Bar {
     kQFull = 0, kQEmpty, kKvFull0, kKvEmpty0 = kKvFull0 + 8, kSFull0 = kKvEmpty0 + 8,
     kSFree0 = kSFull0 + 2, kPFull0 = kSFree0 + 2, kPFree0 = kPFull0 + 2, kODone = kPFree0 + 2, kOFree, kFinalQk,
@@ -287,85 +295,91 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
     const int64_t total = off[p.batch];
 
     if (warp == kProducerWarp) {
-        // ------------------------------------------------------------ producer
+        // ------------------------------------------------------------ producer: K/V tiles
+        // A box is `box` keys of one page; a tile is `nbox` boxes.  The pool rows of
+        // an item's boxes are looked up 32 at a time, one window ahead (lane j holds
+        // box 32 win + j), so no page-table load sits between two tile issues; the
+        // producer waits only for ring stages and runs ahead across items.  The TMA
+        // unit's time per box is what bounds this loop, so K/V tiles are not also
+        // prefetched into L2; the next item's q block is.
         const int box = p.box_rows;
         const int nbox = kTile / box;
-        uint32_t n = 0, iq = 0;
+        const int32_t *tab = p.layout == PKV_LAYOUT_CSR ? p.kv_indices : p.block_table;
+        uint32_t n = 0;
         bool ok = true;
         for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
             const Item it = locate(p, off, w);
             if (it.n_tiles == 0) continue;
-            // q of the block: one box of 128 rows (T tokens x g heads) per slab
-            if (lane == 0) {
-                ok = wait_bar(&bars[kQEmpty], (iq & 1) ^ 1, abort_flag, p.err);
-                if (ok) {
-                    mbar_arrive_expect_tx(&bars[kQFull], C::kQBytes);
-                    const int tok = p.qo_indptr[it.b] + it.qblk * p.T;
+            if (w + gridDim.x < total) {
+                const Item nx = locate(p, off, w + gridDim.x);
+                if (lane == 0 && nx.n_tiles > 0)
                     for (int sl = 0; sl < C::kSl; ++sl)
-                        tma_load_3d(sQ + sl * kRows * 128, &tmq, sl * 64, it.kh * p.g, tok, &bars[kQFull]);
-                }
+                        tma_prefetch_3d(&tmq, sl * 64, nx.kh * p.g, p.qo_indptr[nx.b] + nx.qblk * p.T);
             }
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            ++iq;
-            auto box_row = [&](int ti, bool report) -> int {
-                if (lane >= nbox) return -1;
-                const int tb = it.k0 + ti * kTile + lane * box;
+            // pool row of box bx: -1 past the item's keys, -2 for a page outside the pool
+            auto box_row = [&](int bx) -> int {
+                const int tb = it.k0 + bx * box;
                 if (tb >= it.k1) return -1;
-                const int32_t *tab = p.layout == PKV_LAYOUT_CSR ? p.kv_indices : p.block_table;
                 const int page = __ldg(tab + it.base + (tb >> p.ps_shift));
-                if (page < 0 || page >= p.num_pages) {
-                    if (report) raise_flag(p.err, PKV_DEVERR_RANGE);
-                    return -2;
-                }
+                if (page < 0 || page >= p.num_pages) return -2;
                 return static_cast<int>((static_cast<int64_t>(page) << p.ps_shift) + (tb & p.ps_mask));
             };
-            auto prefetch = [&](int ti) {
-                const int r = box_row(ti, false);
-                if (r >= 0)
-                    for (int sl = 0; sl < C::kSl; ++sl) {
-                        tma_prefetch_3d(&tmk, sl * 64, it.kh, r);
-                        tma_prefetch_3d(&tmv, sl * 64, it.kh, r);
-                    }
-            };
-            for (int ti = 0; ti < kPrefetch && ti < it.n_tiles; ++ti) prefetch(ti);
+            int win = 0;
+            int cur = box_row(lane), nxt = box_row(32 + lane);
+            // one copy per lane: lane = (box j, slab, K or V), at most 32 per tile
+            const int nops = nbox * C::kSl * 2;
+            const int j_box = (lane / (C::kSl * 2)) & (nbox - 1), sl_op = (lane >> 1) % C::kSl;
+            const bool is_v = (lane & 1) != 0;
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
-                if (ti + kPrefetch < it.n_tiles) prefetch(ti + kPrefetch);
-                const int row = box_row(ti, true);
+                if (((ti * nbox) >> 5) != win) {
+                    ++win;
+                    cur = nxt;
+                    nxt = box_row(32 * (win + 1) + lane);
+                }
+                // pool row of this lane's box (a tile's boxes share one window: win or win + 1)
+                const int bx0 = ti * nbox;
+                int row = __shfl_sync(0xffffffffu, (bx0 >> 5) == win ? cur : nxt, (bx0 & 31) + j_box);
+                if (lane >= nops) row = -1;
+                if (row == -2 && lane < 2 * C::kSl * nbox && lane % (2 * C::kSl) == 0) raise_flag(p.err, PKV_DEVERR_RANGE);
                 const int s = n % kStages;
                 if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) break;
                 const uint32_t valid = __ballot_sync(0xffffffffu, row >= 0);
                 if (lane == 0)
-                    mbar_arrive_expect_tx(&bars[kKvFull0 + s],
-                                          __popc(valid) * static_cast<uint32_t>(box) * 128u * 2u * C::kSl);
+                    mbar_arrive_expect_tx(&bars[kKvFull0 + s], __popc(valid) * static_cast<uint32_t>(box) * 128u);
                 __syncwarp();
-                if (row >= 0) {
-                    unsigned char *st = sKV + s * C::kStageBytes;
-                    for (int sl = 0; sl < C::kSl; ++sl) {
-                        tma_load_3d(st + sl * kTile * 128 + lane * box * 128, &tmk, sl * 64, it.kh, row,
-                                    &bars[kKvFull0 + s]);
-                        tma_load_3d(st + C::kKBytes + sl * kTile * 128 + lane * box * 128, &tmv, sl * 64, it.kh, row,
-                                    &bars[kKvFull0 + s]);
-                    }
-                }
+                if (row >= 0)
+                    tma_load_3d(sKV + s * C::kStageBytes + (is_v ? C::kKBytes : 0) + sl_op * kTile * 128 +
+                                    j_box * box * 128,
+                                is_v ? &tmv : &tmk, sl_op * 64, it.kh, row, &bars[kKvFull0 + s]);
             }
         }
-        if (lane == 0) {   // drain: the copies this warp issued have landed
+        if (lane == 0)   // drain: the copies this warp issued have landed
             for (uint32_t k = n > kStages ? n - kStages : 0; k < n; ++k)
                 drain_wait(&bars[kKvFull0 + k % kStages], (k / kStages) & 1);
-            if (iq) drain_wait(&bars[kQFull], (iq - 1) & 1);
-        }
         __syncwarp();
     } else if (warp == kQkWarp) {
         // ------------------------------------------------------------ S = Q K^T
+        // This warp also loads each item's q block, once the previous item's q.k
+        // MMAs have completed (the block was pulled into L2 by the producer).
         const uint32_t idesc = tc05::idesc_bf16_f32(kRows, kTile, false, false);
         uint32_t n = 0, iq = 0;
-        bool ok = true;
+        bool ok = true, q_pending = false;
         for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
             const Item it = locate(p, off, w);
             if (it.n_tiles == 0) continue;
+            ok = warp_wait(ok, &bars[kQEmpty], (iq & 1) ^ 1, abort_flag, p.err);
+            if (ok && lane == 0) {
+                mbar_arrive_expect_tx(&bars[kQFull], C::kQBytes);
+                const int tok = p.qo_indptr[it.b] + it.qblk * p.T;
+                for (int sl = 0; sl < C::kSl; ++sl)
+                    tma_load_3d(sQ + sl * kRows * 128, &tmq, sl * 64, it.kh * p.g, tok, &bars[kQFull]);
+            }
+            q_pending = ok;
+            __syncwarp();
             ok = warp_wait(ok, &bars[kQFull], iq & 1, abort_flag, p.err);
+            if (ok) q_pending = false;
             ++iq;
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
                 const int s = n % kStages;
@@ -391,6 +405,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             }
         }
         if (lane == 0) {
+            if (q_pending) drain_wait(&bars[kQFull], (iq - 1) & 1);
             tc05::commit(&bars[kFinalQk]);
             drain_wait(&bars[kFinalQk], 0);
         }
@@ -496,15 +511,17 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                     for (int j = 0; j < 64; ++j) x[j] = j < vis ? x[j] : -INFINITY;
                 }
                 float mx;
-                {
-                    float t[32];
+                {   // a tree of three-input maxima: 64 -> 22 -> 8 -> 3 -> 1
+                    float t[22];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) t[j] = fmaxf(x[2 * j], x[2 * j + 1]);
+                    for (int j = 0; j < 21; ++j) t[j] = fmax3(x[3 * j], x[3 * j + 1], x[3 * j + 2]);
+                    t[21] = x[63];
+                    float u[8];
 #pragma unroll
-                    for (int w2 = 16; w2 >= 1; w2 >>= 1)
-#pragma unroll
-                        for (int j = 0; j < w2; ++j) t[j] = fmaxf(t[j], t[j + w2]);
-                    mx = t[0] * p.scale_log2;   // scores are unscaled up to here (the scale is positive)
+                    for (int j = 0; j < 7; ++j) u[j] = fmax3(t[3 * j], t[3 * j + 1], t[3 * j + 2]);
+                    u[7] = t[21];
+                    mx = fmax3(fmax3(u[0], u[1], u[2]), fmax3(u[3], u[4], u[5]), fmaxf(u[6], u[7])) *
+                         p.scale_log2;   // scores are unscaled up to here (the scale is positive)
                 }
                 const bool raise = mx > m + kLazy || (m == -INFINITY && mx != -INFINITY);
                 const float corr = raise ? ex2(m - mx) : 1.f;
@@ -529,11 +546,12 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                 }
                 uint32_t h[32];
                 float lsum = 0.f;
-                const float nm = -m;
+                // a row with no keys yet (m = -inf) has only -inf scores: offset 0 gives p = 0
+                const float nm = m == -INFINITY ? 0.f : -m;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {   // p = 2^(scale log2(e) s - m)
-                    const float p0 = m == -INFINITY ? 0.f : ex2(fmaf(x[2 * j], p.scale_log2, nm));
-                    const float p1 = m == -INFINITY ? 0.f : ex2(fmaf(x[2 * j + 1], p.scale_log2, nm));
+                    const float p0 = ex2(fmaf(x[2 * j], p.scale_log2, nm));
+                    const float p1 = ex2(fmaf(x[2 * j + 1], p.scale_log2, nm));
                     lsum += p0 + p1;
                     h[j] = pack_bf16x2(p0, p1);
                 }
@@ -738,6 +756,9 @@ static bool make_plan(const pkv_extend_args *a, Plan &pl) {
         const int64_t want = (target + groups - 1) / groups;
         int64_t c = (L + want - 1) / want;
         c = std::max<int64_t>(512, (c + kTile - 1) / kTile * kTile);
+        // long rows of uneven length: cap an item at 4096 keys so no single item
+        // outlasts the others' share
+        if (L > 8192) c = std::min<int64_t>(c, 4096);
         pl.chunk = static_cast<int>(std::min<int64_t>(c, (L + kTile - 1) / kTile * kTile));
     }
     pl.nch_max = static_cast<int>((L + pl.chunk - 1) / pl.chunk);
