@@ -7,17 +7,23 @@
 // (request, kv head, block of 128 query rows, chunk of keys): the rows are the
 // (token, query head) pairs of 128 / g consecutive tokens times the g query
 // heads sharing the kv head, so every K/V tile serves the whole block.  Per CTA:
-//   warp 4     TMA producer: K/V tiles of 64 keys (one box per page per slab)
-//              through a 5-stage ring (8 at head_dim 64), pool rows looked up
-//              32 boxes at a time, the next q block pulled into L2;
-//   warp 5     loads the block's q (one 3-D box per 64-dim slab, rows
-//              token-major), then S = Q K^T (M = 128, N = 64) into one of two
-//              TMEM score buffers;
-//   warp 6     O += P V (N = head_dim) from one of two TMEM P buffers;
+//   warp 4     TMA producer: K/V tiles of 64 keys (one box per page per slab,
+//              one copy per lane) through a 4-stage ring (8 at head_dim 64),
+//              pool rows looked up 32 boxes at a time;
+//   warp 5     loads the q blocks (one 3-D box per 64-dim slab, rows
+//              token-major) into two buffers, the next item's while this one
+//              runs, and issues S = Q K^T (M = 128, N = 64) into one of two TMEM
+//              score buffers;
+//   warp 6     O += P V (N = head_dim) from one of two TMEM P buffers into one
+//              of two accumulators (items alternate);
 //   warps 0-3  one query row per thread: mask keys at or past the row's bound,
-//              online softmax (base 2, running max raised only past 2^8), P.
-// Items whose block is cut into several key chunks write fp32 (o, lse)
-// partials that ext_merge_kernel combines.  Every wait is bounded (~2 s).
+//              online softmax (base 2, running max raised only past 2^8), P;
+//   warps 7-10 epilogue: normalise an item's O and write it while warps 0-3
+//              already run the next item.
+// Per-request values sit in shared memory (when they fit), so moving from one
+// item to the next costs no global loads.  Items whose block is cut into
+// several key chunks write fp32 (o, lse) partials that ext_merge_kernel
+// combines.  Every wait is bounded (~2 s).
 #include <algorithm>
 
 #include "pkv_internal.cuh"
@@ -27,30 +33,32 @@ namespace pkv {
 namespace ext {
 
 constexpr int kRows = 128, kTile = 64;
-constexpr int kThreads = 224;              // warps 0-3 softmax, 4 producer, 5 q.k, 6 P.V
-constexpr int kProducerWarp = 4, kQkWarp = 5, kPvWarp = 6;
+constexpr int kThreads = 352;              // warps 0-3 softmax, 4 producer, 5 q.k, 6 P.V, 7-10 epilogue
+constexpr int kProducerWarp = 4, kQkWarp = 5, kPvWarp = 6, kEpiWarp0 = 7;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kLog2e = 1.44269504088896341f;
 constexpr float kLazy = 8.f;
 
 template <int D>
 struct Cfg {
-    static constexpr int kStages = D == 128 ? 5 : 8;           // K/V ring depth (about 190 KB either way)
+    static constexpr int kStages = D == 128 ? 4 : 8;           // K/V ring depth (128 KB either way)
     static constexpr int kSl = D / 64;                         // 64-dim slabs
-    static constexpr int kQBytes = kSl * kRows * 128;          // q block, SW128 K-major
+    static constexpr int kQBytes = kSl * kRows * 128;          // one q block, SW128 K-major
     static constexpr int kKBytes = kSl * kTile * 128;          // one K (or V) tile
     static constexpr int kStageBytes = 2 * kKBytes;
-    static constexpr int kOffQ = 0;
-    static constexpr int kOffKV = kOffQ + kQBytes;
+    static constexpr int kOffQ = 0;                            // two q blocks: this item's and the next
+    static constexpr int kOffKV = kOffQ + 2 * kQBytes;
     static constexpr int kOffBar = kOffKV + kStages * kStageBytes;
-    static constexpr int kNumBars = 32;
+    static constexpr int kNumBars = 48;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;    // tmem slot, abort flag, scan scratch
-    static constexpr int kOffTable = kOffMisc + 64;
-    static constexpr int kFixedSmem = kOffTable + 1024;        // + item table + alignment slack
+    static constexpr int kOffStats = kOffMisc + 128;           // [2 items][128 rows] of (m, l) for the epilogue
+    static constexpr int kOffTable = kOffStats + 2 * kRows * 8;
+    static constexpr int kFixedSmem = kOffTable + 1024;        // + request tables + alignment slack
     static constexpr uint32_t kColS = 0;                       // two 64-column score buffers
-    static constexpr uint32_t kColO = 128;
-    static constexpr uint32_t kColP = 128 + D;                 // two 32-column P buffers
-    static constexpr uint32_t kTmemCols = (kColP + 64 <= 256) ? 256 : 512;
+    static constexpr uint32_t kColO = 128;                     // two D-column output accumulators
+    static constexpr uint32_t kColP = 128 + 2 * D;             // two 32-column P buffers
+    static constexpr uint32_t kTmemCols = 512;
+    static_assert(kColP + 64 <= kTmemCols, "tensor memory");
 };
 
 struct Params {
@@ -62,6 +70,8 @@ struct Params {
     uint16_t *out;
     float *lse, *part_o, *part_lse;
     int32_t *err;
+    int32_t cache_requests;   // per-request values kept in shared memory (they fit)
+    int32_t item_cache;       // items per CTA decoded once into shared memory
 };
 
 // Keys of request b (0 and a flag for malformed inputs).
@@ -119,32 +129,76 @@ __device__ __forceinline__ int per_head_items(const Params &p, int L, int n) {
     return s;
 }
 
-struct Item {
-    int b, kh, qblk, c, L, n, nch, k0, k1, n_tiles;
-    int64_t base, w;
+// Shared-memory tables of one launch: off[b] = first item of request b (B + 1
+// entries) and, when they fit, each request's key count, query rows, first
+// query row and page-list base, so that finding an item costs no global loads.
+struct Tables {
+    int *off, *keys, *nq, *qo0, *base;   // keys..base null when not cached
 };
 
-__device__ __forceinline__ Item locate(const Params &p, const int *off, int64_t w) {
+struct Req {
+    int L, n, qo0;
+    int64_t base;
+};
+
+// Request b from the inputs (flags raised only with `report`); causal rows need their keys.
+__device__ __forceinline__ Req load_req(const Params &p, int b, bool report) {
+    Req r;
+    r.L = key_count(p, b, r.base, report);
+    r.n = q_count(p, b, report);
+    if (!p.kv_end && r.n > r.L) {
+        if (report) raise_flag(p.err, PKV_DEVERR_RANGE);
+        r.n = 0;
+    }
+    r.qo0 = r.n > 0 ? p.qo_indptr[b] : 0;
+    return r;
+}
+
+__device__ __forceinline__ Req get_req(const Params &p, const Tables &t, int b) {
+    if (!t.keys) return load_req(p, b, false);
+    Req r;
+    r.L = t.keys[b];
+    r.n = t.nq[b];
+    r.qo0 = t.qo0[b];
+    r.base = p.layout == PKV_LAYOUT_CSR ? static_cast<int64_t>(t.base[b]) : static_cast<int64_t>(b) * p.bt_width;
+    return r;
+}
+
+struct Item {
+    int64_t base, w;
+    int b, kh, qblk, c, L, n, qo0, nch, k0, k1, n_tiles;
+};
+
+__device__ __forceinline__ Item locate(const Params &p, const Tables &t, int64_t w) {
     Item it;
     int lo = 0, hi = p.batch;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (off[mid] <= w) lo = mid; else hi = mid;
+        if (t.off[mid] <= w) lo = mid; else hi = mid;
     }
     it.b = lo;
     it.w = w;
-    it.L = key_count(p, it.b, it.base, false);
-    it.n = it.L >= 0 ? q_count(p, it.b, false) : 0;
-    if (!p.kv_end && it.n > it.L) it.n = 0;                   // causal rows need their keys
-    const int per = per_head_items(p, it.L, it.n);
-    int rem = static_cast<int>(w - off[it.b]);
+    const Req r = get_req(p, t, lo);
+    it.L = r.L;
+    it.n = r.n;
+    it.qo0 = r.qo0;
+    it.base = r.base;
+    const int nq = (it.n + p.T - 1) / p.T;
+    const bool one = p.chunk >= it.L;   // every query block is a single chunk
+    const int per = one ? nq : per_head_items(p, it.L, it.n);
+    int rem = static_cast<int>(w - t.off[it.b]);
     it.kh = rem / per;
     rem -= it.kh * per;
     int q = 0;
-    for (;; ++q) {
-        const int c = chunks_of(p, block_keys(p, it.L, it.n, q));
-        if (rem < c) break;
-        rem -= c;
+    if (one) {
+        q = rem;
+        rem = 0;
+    } else {
+        for (;; ++q) {
+            const int c = chunks_of(p, block_keys(p, it.L, it.n, q));
+            if (rem < c) break;
+            rem -= c;
+        }
     }
     it.qblk = q;
     it.c = rem;
@@ -156,24 +210,23 @@ __device__ __forceinline__ Item locate(const Params &p, const int *off, int64_t 
     return it;
 }
 
-// off[b] = first item of request b; every CTA builds the same table.
-__device__ __forceinline__ void build_item_table(const Params &p, int *off, int *scratch) {
+// Every CTA builds the same tables (CTA 0 reports malformed inputs).
+__device__ __forceinline__ void build_tables(const Params &p, const Tables &t, int *scratch) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = p.batch;
     const int seg = (B + kThreads - 1) / kThreads;
     const int lo = min(B, tid * seg), hi = min(B, lo + seg);
-    auto items = [&](int b, bool report) {
-        int64_t base;
-        const int L = key_count(p, b, base, report);
-        int n = q_count(p, b, report);
-        if (!p.kv_end && n > L) {
-            if (report) raise_flag(p.err, PKV_DEVERR_RANGE);
-            n = 0;
-        }
-        return p.hkv * per_head_items(p, L, n);
-    };
     int local = 0;
-    for (int b = lo; b < hi; ++b) local += items(b, blockIdx.x == 0);
+    for (int b = lo; b < hi; ++b) {
+        const Req r = load_req(p, b, blockIdx.x == 0);
+        local += p.hkv * per_head_items(p, r.L, r.n);
+        if (t.keys) {
+            t.keys[b] = r.L;
+            t.nq[b] = r.n;
+            t.qo0[b] = r.qo0;
+            t.base[b] = static_cast<int>(r.base);
+        }
+    }
     int incl = local;
     for (int o = 1; o < 32; o <<= 1) {
         const int x = __shfl_up_sync(0xffffffffu, incl, o);
@@ -185,10 +238,11 @@ __device__ __forceinline__ void build_item_table(const Params &p, int *off, int 
     for (int w = 0; w < warp; ++w) wbase += scratch[w];
     int run = wbase + incl - local;
     for (int b = lo; b < hi; ++b) {
-        off[b] = run;
-        run += items(b, false);
+        t.off[b] = run;
+        const Req r = t.keys ? get_req(p, t, b) : load_req(p, b, false);
+        run += p.hkv * per_head_items(p, r.L, r.n);
     }
-    if (tid == kThreads - 1) off[B] = wbase + incl;
+    if (tid == kThreads - 1) t.off[B] = wbase + incl;
     __syncthreads();
 }
 
@@ -235,10 +289,28 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 }
 
 enum Bar {
-    kQFull = 0, kQEmpty, kKvFull0, kKvEmpty0 = kKvFull0 + 8, kSFull0 = kKvEmpty0 + 8,
-    kSFree0 = kSFull0 + 2, kPFull0 = kSFree0 + 2, kPFree0 = kPFull0 + 2, kODone = kPFree0 + 2, kOFree, kFinalQk,
-    kFinalPv, kBarCount
+    kQFull0 = 0, kQEmpty0 = 2, kKvFull0 = 4, kKvEmpty0 = kKvFull0 + 8, kSFull0 = kKvEmpty0 + 8,
+    kSFree0 = kSFull0 + 2, kPFull0 = kSFree0 + 2, kPFree0 = kPFull0 + 2, kODone0 = kPFree0 + 2, kOFree0 = kODone0 + 2,
+    kStatFull0 = kOFree0 + 2, kFinalQk = kStatFull0 + 2, kFinalPv, kBarCount
 };
+
+// This CTA's item j (w = blockIdx.x + j * gridDim.x): from the shared-memory copy
+// made when the CTA starts (decoding an item is a long dependent chain for one
+// warp), or decoded afresh past the copy's end.
+__device__ __forceinline__ Item cta_item(const Params &p, const Tables &t, const Item *ic, int64_t j) {
+    if (j < p.item_cache) return ic[j];
+    return locate(p, t, blockIdx.x + j * gridDim.x);
+}
+
+// First item j' >= j of this CTA that has keys (n_items if none).
+__device__ __forceinline__ int64_t next_live(const Params &p, const Tables &t, const Item *ic, int64_t j,
+                                             int64_t n_items, Item &it) {
+    for (; j < n_items; ++j) {
+        it = cta_item(p, t, ic, j);
+        if (it.n_tiles > 0) return j;
+    }
+    return n_items;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -255,25 +327,36 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
     int *scan = reinterpret_cast<int *>(smem + C::kOffMisc + 16);
-    int *off = reinterpret_cast<int *>(smem + C::kOffTable);
+    float2 *stats = reinterpret_cast<float2 *>(smem + C::kOffStats);
+    Tables tb;
+    tb.off = reinterpret_cast<int *>(smem + C::kOffTable);
+    if (p.cache_requests) {
+        tb.keys = tb.off + p.batch + 1;
+        tb.nq = tb.keys + p.batch;
+        tb.qo0 = tb.nq + p.batch;
+        tb.base = tb.qo0 + p.batch;
+    } else {
+        tb.keys = tb.nq = tb.qo0 = tb.base = nullptr;
+    }
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
         *abort_flag = 0;
-        mbar_init(&bars[kQFull], 1);
-        mbar_init(&bars[kQEmpty], 1);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bars[kKvFull0 + s], 1);
-            mbar_init(&bars[kKvEmpty0 + s], 1);
-        }
         for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[kQFull0 + i], 1);
+            mbar_init(&bars[kQEmpty0 + i], 1);
             mbar_init(&bars[kSFull0 + i], 1);
             mbar_init(&bars[kSFree0 + i], 4);
             mbar_init(&bars[kPFull0 + i], 4);
             mbar_init(&bars[kPFree0 + i], 1);
+            mbar_init(&bars[kODone0 + i], 1);
+            mbar_init(&bars[kOFree0 + i], 4);
+            mbar_init(&bars[kStatFull0 + i], 4);
         }
-        mbar_init(&bars[kODone], 1);
-        mbar_init(&bars[kOFree], 4);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bars[kKvFull0 + s], 1);
+            mbar_init(&bars[kKvEmpty0 + s], 1);
+        }
         mbar_init(&bars[kFinalQk], 1);
         mbar_init(&bars[kFinalPv], 1);
         mbar_init_fence();
@@ -287,12 +370,18 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
         prefetch_tmap(&tmk);
         prefetch_tmap(&tmv);
     }
-    build_item_table(p, off, scan);
+    build_tables(p, tb, scan);
     tc05::fence_before_sync();
     __syncthreads();
     tc05::fence_after_sync();
     const uint32_t tbase = *tslot;
-    const int64_t total = off[p.batch];
+    const int64_t total = tb.off[p.batch];
+    const int64_t n_items = total > blockIdx.x ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    Item *icache = reinterpret_cast<Item *>(
+        smem + ((C::kOffTable + (p.batch + 1) * 4 + (p.cache_requests ? 16 * p.batch : 0) + 15) & ~15));
+    for (int64_t j = tid; j < min(n_items, static_cast<int64_t>(p.item_cache)); j += kThreads)
+        icache[j] = locate(p, tb, blockIdx.x + j * gridDim.x);
+    __syncthreads();
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer: K/V tiles
@@ -300,36 +389,29 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
         // an item's boxes are looked up 32 at a time, one window ahead (lane j holds
         // box 32 win + j), so no page-table load sits between two tile issues; the
         // producer waits only for ring stages and runs ahead across items.  The TMA
-        // unit's time per box is what bounds this loop, so K/V tiles are not also
-        // prefetched into L2; the next item's q block is.
+        // unit's time per box bounds this loop, so nothing is prefetched into L2.
         const int box = p.box_rows;
         const int nbox = kTile / box;
         const int32_t *tab = p.layout == PKV_LAYOUT_CSR ? p.kv_indices : p.block_table;
+        // one copy per lane: lane = (box j, slab, K or V), at most 32 per tile
+        const int nops = nbox * C::kSl * 2;
+        const int j_box = (lane / (C::kSl * 2)) & (nbox - 1), sl_op = (lane >> 1) % C::kSl;
+        const bool is_v = (lane & 1) != 0;
         uint32_t n = 0;
         bool ok = true;
-        for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
-            const Item it = locate(p, off, w);
+        for (int64_t j = 0; j < n_items && ok; ++j) {
+            const Item it = cta_item(p, tb, icache, j);
             if (it.n_tiles == 0) continue;
-            if (w + gridDim.x < total) {
-                const Item nx = locate(p, off, w + gridDim.x);
-                if (lane == 0 && nx.n_tiles > 0)
-                    for (int sl = 0; sl < C::kSl; ++sl)
-                        tma_prefetch_3d(&tmq, sl * 64, nx.kh * p.g, p.qo_indptr[nx.b] + nx.qblk * p.T);
-            }
             // pool row of box bx: -1 past the item's keys, -2 for a page outside the pool
             auto box_row = [&](int bx) -> int {
-                const int tb = it.k0 + bx * box;
-                if (tb >= it.k1) return -1;
-                const int page = __ldg(tab + it.base + (tb >> p.ps_shift));
+                const int kb = it.k0 + bx * box;
+                if (kb >= it.k1) return -1;
+                const int page = __ldg(tab + it.base + (kb >> p.ps_shift));
                 if (page < 0 || page >= p.num_pages) return -2;
-                return static_cast<int>((static_cast<int64_t>(page) << p.ps_shift) + (tb & p.ps_mask));
+                return static_cast<int>((static_cast<int64_t>(page) << p.ps_shift) + (kb & p.ps_mask));
             };
             int win = 0;
             int cur = box_row(lane), nxt = box_row(32 + lane);
-            // one copy per lane: lane = (box j, slab, K or V), at most 32 per tile
-            const int nops = nbox * C::kSl * 2;
-            const int j_box = (lane / (C::kSl * 2)) & (nbox - 1), sl_op = (lane >> 1) % C::kSl;
-            const bool is_v = (lane & 1) != 0;
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
                 if (((ti * nbox) >> 5) != win) {
                     ++win;
@@ -340,7 +422,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                 const int bx0 = ti * nbox;
                 int row = __shfl_sync(0xffffffffu, (bx0 >> 5) == win ? cur : nxt, (bx0 & 31) + j_box);
                 if (lane >= nops) row = -1;
-                if (row == -2 && lane < 2 * C::kSl * nbox && lane % (2 * C::kSl) == 0) raise_flag(p.err, PKV_DEVERR_RANGE);
+                if (row == -2 && lane % (2 * C::kSl) == 0) raise_flag(p.err, PKV_DEVERR_RANGE);
                 const int s = n % kStages;
                 if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -361,26 +443,33 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
         __syncwarp();
     } else if (warp == kQkWarp) {
         // ------------------------------------------------------------ S = Q K^T
-        // This warp also loads each item's q block, once the previous item's q.k
-        // MMAs have completed (the block was pulled into L2 by the producer).
+        // This warp also loads the q blocks, into two buffers: item i + 1's block is
+        // requested once item i's first tile is issued (its buffer was freed by the
+        // completion of item i - 1's last q.k), so q never waits at an item boundary.
         const uint32_t idesc = tc05::idesc_bf16_f32(kRows, kTile, false, false);
-        uint32_t n = 0, iq = 0;
-        bool ok = true, q_pending = false;
-        for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
-            const Item it = locate(p, off, w);
-            if (it.n_tiles == 0) continue;
-            ok = warp_wait(ok, &bars[kQEmpty], (iq & 1) ^ 1, abort_flag, p.err);
+        uint32_t n = 0, iq = 0, q_issued = 0;
+        bool ok = true;
+        auto load_q = [&](const Item &qi, uint32_t slot_use) {   // slot_use: how many q loads came before
+            const int sl = slot_use & 1;
+            ok = warp_wait(ok, &bars[kQEmpty0 + sl], ((slot_use >> 1) & 1) ^ 1, abort_flag, p.err);
             if (ok && lane == 0) {
-                mbar_arrive_expect_tx(&bars[kQFull], C::kQBytes);
-                const int tok = p.qo_indptr[it.b] + it.qblk * p.T;
-                for (int sl = 0; sl < C::kSl; ++sl)
-                    tma_load_3d(sQ + sl * kRows * 128, &tmq, sl * 64, it.kh * p.g, tok, &bars[kQFull]);
+                mbar_arrive_expect_tx(&bars[kQFull0 + sl], C::kQBytes);
+                const int tok = qi.qo0 + qi.qblk * p.T;
+                for (int k = 0; k < C::kSl; ++k)
+                    tma_load_3d(sQ + sl * C::kQBytes + k * kRows * 128, &tmq, k * 64, qi.kh * p.g, tok,
+                                &bars[kQFull0 + sl]);
             }
-            q_pending = ok;
             __syncwarp();
-            ok = warp_wait(ok, &bars[kQFull], iq & 1, abort_flag, p.err);
-            if (ok) q_pending = false;
-            ++iq;
+            if (ok) ++q_issued;
+        };
+        Item it;
+        int64_t j = next_live(p, tb, icache, 0, n_items, it);
+        if (j < n_items) load_q(it, 0);
+        while (j < n_items && ok) {
+            Item nx;
+            const int64_t jn = next_live(p, tb, icache, j + 1, n_items, nx);
+            const int sl = iq & 1;
+            ok = warp_wait(ok, &bars[kQFull0 + sl], (iq >> 1) & 1, abort_flag, p.err);
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
                 const int s = n % kStages;
                 ok = warp_wait(ok, &bars[kKvFull0 + s], (n / kStages) & 1, abort_flag, p.err);
@@ -389,35 +478,43 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                 tc05::fence_after_sync();
                 if (lane == 0) {
                     const uint64_t kd = tc05::smem_desc(sKV + s * C::kStageBytes, 16, 1024);
-                    const uint64_t qd = tc05::smem_desc(sQ, 16, 1024);
+                    const uint64_t qd = tc05::smem_desc(sQ + sl * C::kQBytes, 16, 1024);
 #pragma unroll
-                    for (int sl = 0; sl < C::kSl; ++sl)
+                    for (int k2 = 0; k2 < C::kSl; ++k2)
 #pragma unroll
                         for (int k = 0; k < 4; ++k)   // slab: q +16 KB, K +8 KB; k-step +32 bytes
                             tc05::mma_ss(tbase + C::kColS + (n & 1) * kTile,
-                                         qd + static_cast<uint64_t>((sl * kRows * 128 + k * 32) >> 4),
-                                         kd + static_cast<uint64_t>((sl * kTile * 128 + k * 32) >> 4), idesc,
-                                         (sl | k) ? 1u : 0u);
+                                         qd + static_cast<uint64_t>((k2 * kRows * 128 + k * 32) >> 4),
+                                         kd + static_cast<uint64_t>((k2 * kTile * 128 + k * 32) >> 4), idesc,
+                                         (k2 | k) ? 1u : 0u);
                     tc05::commit(&bars[kSFull0 + (n & 1)]);
-                    if (ti == it.n_tiles - 1) tc05::commit(&bars[kQEmpty]);
+                    if (ti == it.n_tiles - 1) tc05::commit(&bars[kQEmpty0 + sl]);
                 }
                 __syncwarp();
+                if (ti == 0 && jn < n_items) load_q(nx, iq + 1);
             }
+            ++iq;
+            j = jn;
+            it = nx;
         }
         if (lane == 0) {
-            if (q_pending) drain_wait(&bars[kQFull], (iq - 1) & 1);
+            // q loads issued but not waited for have landed before shared memory is released
+            for (uint32_t k = iq; k < q_issued; ++k) drain_wait(&bars[kQFull0 + (k & 1)], (k >> 1) & 1);
             tc05::commit(&bars[kFinalQk]);
             drain_wait(&bars[kFinalQk], 0);
         }
         __syncwarp();
     } else if (warp == kPvWarp) {
         // ------------------------------------------------------------ O += P V
+        // Items alternate between two accumulators, so an item's first P V does not
+        // wait for the previous item's epilogue.
         const uint32_t idesc = tc05::idesc_bf16_f32(kRows, D, false, true);
         uint32_t n = 0, io = 0;
         bool ok = true;
-        for (int64_t w = blockIdx.x; w < total && ok; w += gridDim.x) {
-            const Item it = locate(p, off, w);
+        for (int64_t j = 0; j < n_items && ok; ++j) {
+            const Item it = cta_item(p, tb, icache, j);
             if (it.n_tiles == 0) continue;
+            const int ko = io & 1;
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
                 ok = warp_wait(ok, &bars[kPFull0 + (n & 1)], (n >> 1) & 1, abort_flag, p.err);
                 if (!ok) break;
@@ -432,19 +529,19 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
-                if (ti == 0) ok = warp_wait(ok, &bars[kOFree], (io & 1) ^ 1, abort_flag, p.err);
+                if (ti == 0) ok = warp_wait(ok, &bars[kOFree0 + ko], ((io >> 1) & 1) ^ 1, abort_flag, p.err);
                 if (!ok) break;
                 tc05::fence_after_sync();
                 if (lane == 0) {
                     const uint64_t vd = tc05::smem_desc(v, kTile * 128, 1024);
 #pragma unroll
                     for (int k = 0; k < kTile / 16; ++k)   // 16 keys: +2048 bytes of V, +8 columns of P
-                        tc05::mma_ts(tbase + C::kColO, tbase + C::kColP + (n & 1) * 32 + k * 8,
+                        tc05::mma_ts(tbase + C::kColO + ko * D, tbase + C::kColP + (n & 1) * 32 + k * 8,
                                      vd + static_cast<uint64_t>((k * 2048) >> 4), idesc,
                                      (ti == 0 && k == 0) ? 0u : 1u);
                     tc05::commit(&bars[kPFree0 + (n & 1)]);
                     tc05::commit(&bars[kKvEmpty0 + n % kStages]);
-                    if (ti == it.n_tiles - 1) tc05::commit(&bars[kODone]);
+                    if (ti == it.n_tiles - 1) tc05::commit(&bars[kODone0 + ko]);
                 }
                 __syncwarp();
             }
@@ -455,6 +552,79 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             drain_wait(&bars[kFinalPv], 0);
         }
         __syncwarp();
+    } else if (warp >= kEpiWarp0) {
+        // ------------------------------------------------------------ epilogue (one row per thread)
+        // Normalises an item's O once its last P V is done and the softmax warps have
+        // left the row's (m, l), writes the bf16 row (or the fp32 split partial) and
+        // frees the accumulator, while the softmax warps already run the next item.
+        const int quarter = warp & 3;                 // TMEM lanes this warp may read
+        const int r = quarter * 32 + lane;
+        const uint32_t trow = tc05::taddr(tbase, quarter * 32, 0);
+        const int tok = r >> p.g_shift, hh = r & (p.g - 1);
+        uint32_t io = 0;
+        bool ok = true;
+        for (int64_t j = 0; j < n_items; ++j) {
+            const Item it = cta_item(p, tb, icache, j);
+            if (it.n_tiles == 0) continue;
+            const int ko = io & 1;
+            ok = warp_wait(ok, &bars[kStatFull0 + ko], (io >> 1) & 1, abort_flag, p.err);
+            const float2 ml = stats[ko * kRows + r];
+            ok = warp_wait(ok, &bars[kODone0 + ko], (io >> 1) & 1, abort_flag, p.err);
+            tc05::fence_after_sync();
+            const int tq = it.qblk * p.T + tok;
+            const bool valid = tq < it.n;
+            const int64_t qrow = static_cast<int64_t>(it.qo0) + tq;
+            const int head = it.kh * p.g + hh;
+            const bool single = it.nch == 1;
+            const int64_t prow = it.w * kRows + r;
+            const float inv = ml.y > 0.f ? 1.f / ml.y : 0.f;
+#pragma unroll 1
+            for (int cb = 0; cb < D / 16; cb += 4) {
+                float ov[4][16];
+                if (ok) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) tc05::ld_x16(trow + C::kColO + ko * D + (cb + q4) * 16, ov[q4]);
+                    tc05::wait_ld();
+                } else {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) ov[q4][e] = 0.f;
+                }
+                if (valid) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int col = (cb + q4) * 16;
+                        if (single) {
+                            uint32_t h2[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) h2[e] = pack_bf16x2(ov[q4][2 * e] * inv, ov[q4][2 * e + 1] * inv);
+                            uint4 *o = reinterpret_cast<uint4 *>(p.out + (qrow * p.hq + head) * D + col);
+                            o[0] = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+                            o[1] = make_uint4(h2[4], h2[5], h2[6], h2[7]);
+                        } else {
+                            float4 *o = reinterpret_cast<float4 *>(p.part_o + prow * D + col);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                o[e] = make_float4(ov[q4][4 * e] * inv, ov[q4][4 * e + 1] * inv,
+                                                   ov[q4][4 * e + 2] * inv, ov[q4][4 * e + 3] * inv);
+                        }
+                    }
+                }
+            }
+            if (valid) {
+                const float lse2 = ml.y > 0.f ? ml.x + log2f(ml.y) : -INFINITY;
+                if (single) {
+                    if (p.lse) p.lse[qrow * p.hq + head] = lse2 * kLn2;
+                } else {
+                    p.part_lse[prow] = lse2;
+                }
+            }
+            tc05::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kOFree0 + ko]);
+            ++io;
+        }
     } else {
         // ------------------------------------------------------------ softmax (one row per thread)
         const int r = warp * 32 + lane;
@@ -462,31 +632,46 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
         const int tok = r >> p.g_shift, hh = r & (p.g - 1);
         uint32_t n = 0, io = 0;
         bool ok = true;
-        for (int64_t w = blockIdx.x; w < total; w += gridDim.x) {
-            const Item it = locate(p, off, w);
-            const int tb = it.qblk * p.T + tok;                  // token within the request
-            const bool valid = tb < it.n;
-            const int64_t qrow = static_cast<int64_t>(p.qo_indptr[it.b]) + tb;
-            int kend = 0;
-            if (valid) {
-                kend = p.kv_end ? p.kv_end[qrow] : it.L - it.n + tb + 1;
-                if (kend < 0 || kend > it.L) {
-                    if (it.c == 0 && it.kh == 0) raise_flag(p.err, PKV_DEVERR_RANGE);
-                    kend = 0;
-                }
+        // the row's key bound; its load for the next item is issued an item early
+        auto row_bound = [&](const Item &qi) -> int {
+            const int tq = qi.qblk * p.T + tok;
+            if (tq >= qi.n) return 0;
+            int kend = p.kv_end ? __ldg(p.kv_end + static_cast<int64_t>(qi.qo0) + tq) : qi.L - qi.n + tq + 1;
+            if (kend < 0 || kend > qi.L) {
+                if (qi.c == 0 && qi.kh == 0) raise_flag(p.err, PKV_DEVERR_RANGE);
+                kend = 0;
             }
+            return kend;
+        };
+        Item it;
+        int kend = 0;
+        if (n_items > 0) {
+            it = cta_item(p, tb, icache, 0);
+            kend = row_bound(it);
+        }
+        for (int64_t j = 0; j < n_items; ++j) {
+            Item nx;
+            int kend_nx = 0;
+            if (j + 1 < n_items) {
+                nx = cta_item(p, tb, icache, j + 1);
+                kend_nx = row_bound(nx);
+            }
+            const int tq = it.qblk * p.T + tok;                  // token within the request
+            const bool valid = tq < it.n;
+            const int64_t qrow = static_cast<int64_t>(it.qo0) + tq;
             const int head = it.kh * p.g + hh;
-            const bool single = it.nch == 1;
-            const int64_t prow = it.w * kRows + r;
             float m = -INFINITY, l = 0.f;
             if (it.n_tiles == 0) {   // no keys: out = 0, lse = -inf
-                if (valid && single) {
+                if (valid && it.nch == 1) {
                     uint4 *o = reinterpret_cast<uint4 *>(p.out + (qrow * p.hq + head) * D);
                     for (int i = 0; i < D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
                     if (p.lse) p.lse[qrow * p.hq + head] = -INFINITY;
                 }
+                it = nx;
+                kend = kend_nx;
                 continue;
             }
+            const int ko = io & 1;
             for (int ti = 0; ti < it.n_tiles; ++ti, ++n) {
                 const int key0 = it.k0 + ti * kTile;
                 // rows past the block's tokens are never written: they only mask the
@@ -532,11 +717,11 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
 #pragma unroll 1
                     for (int cc = 0; cc < D / 16 && ok; ++cc) {
                         float ov[16];
-                        tc05::ld_x16(trow + C::kColO + cc * 16, ov);
+                        tc05::ld_x16(trow + C::kColO + ko * D + cc * 16, ov);
                         tc05::wait_ld();
 #pragma unroll
                         for (int e = 0; e < 16; ++e) ov[e] *= corr;
-                        tc05::st_x16(trow + C::kColO + cc * 16, ov);
+                        tc05::st_x16(trow + C::kColO + ko * D + cc * 16, ov);
                     }
                     tc05::wait_st();
                 }
@@ -573,55 +758,15 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars[kPFull0 + (n & 1)]);
             }
-            // ---- epilogue: normalise O, write the row (or the split partial) ----
-            ok = warp_wait(ok, &bars[kODone], io & 1, abort_flag, p.err);
-            tc05::fence_after_sync();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll 1
-            for (int cb = 0; cb < D / 16; cb += 2) {
-                float ov[2][16];
-                if (ok) {
-                    tc05::ld_x16(trow + C::kColO + cb * 16, ov[0]);
-                    tc05::ld_x16(trow + C::kColO + (cb + 1) * 16, ov[1]);
-                    tc05::wait_ld();
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) ov[0][e] = ov[1][e] = 0.f;
-                }
-                if (valid) {
-#pragma unroll
-                    for (int q2 = 0; q2 < 2; ++q2) {
-                        const int col = (cb + q2) * 16;
-                        if (single) {
-                            uint32_t hh2[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                hh2[e] = pack_bf16x2(ov[q2][2 * e] * inv, ov[q2][2 * e + 1] * inv);
-                            uint4 *o = reinterpret_cast<uint4 *>(p.out + (qrow * p.hq + head) * D + col);
-                            o[0] = make_uint4(hh2[0], hh2[1], hh2[2], hh2[3]);
-                            o[1] = make_uint4(hh2[4], hh2[5], hh2[6], hh2[7]);
-                        } else {
-                            float4 *o = reinterpret_cast<float4 *>(p.part_o + prow * D + col);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                o[e] = make_float4(ov[q2][4 * e] * inv, ov[q2][4 * e + 1] * inv,
-                                                   ov[q2][4 * e + 2] * inv, ov[q2][4 * e + 3] * inv);
-                        }
-                    }
-                }
-            }
-            if (valid) {
-                const float lse2 = l > 0.f ? m + log2f(l) : -INFINITY;
-                if (single) {
-                    if (p.lse) p.lse[qrow * p.hq + head] = lse2 * kLn2;
-                } else {
-                    p.part_lse[prow] = lse2;
-                }
-            }
-            tc05::fence_before_sync();
+            // hand (m, l) to the epilogue warps; the buffer is free once they are done
+            // with the item two back (the same phase that freed its accumulator)
+            ok = warp_wait(ok, &bars[kOFree0 + ko], ((io >> 1) & 1) ^ 1, abort_flag, p.err);
+            stats[ko * kRows + r] = make_float2(m, l);
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kOFree]);
+            if (lane == 0) mbar_arrive(&bars[kStatFull0 + ko]);
             ++io;
+            it = nx;
+            kend = kend_nx;
         }
     }
 
@@ -868,8 +1013,16 @@ static pkv_status launch_t(const pkv_extend_args *a, const Plan &pl, void *ws, i
             return fail(PKV_ERR_CUDA, "pkv_extend: cannot raise the shared-memory limit");
         lim = l;
     }
-    const size_t smem = C::kFixedSmem + (static_cast<size_t>(a->batch) + 1) * 4;
+    // item table (B + 1 ints), plus four ints per request when they fit as well
+    size_t smem = C::kFixedSmem + (static_cast<size_t>(a->batch) + 1) * 4;
     if (smem > lim) return fail(PKV_ERR_UNSUPPORTED, "pkv_extend: batch too large for the on-chip item table");
+    const size_t cached = smem + static_cast<size_t>(a->batch) * 16;
+    p.cache_requests = cached <= lim ? 1 : 0;
+    if (p.cache_requests) smem = cached;
+    // then this CTA's decoded items, as many as fit (up to 256)
+    smem = (smem + 15) & ~static_cast<size_t>(15);
+    p.item_cache = smem < lim ? static_cast<int32_t>(std::min<size_t>(256, (lim - smem) / sizeof(Item))) : 0;
+    smem += static_cast<size_t>(p.item_cache) * sizeof(Item);
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(pl.items_max, sm_count()));
     ext_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p, tmq, tmk, tmv);
     pkv_status st = check_launch("pkv_extend (attention kernel)");
