@@ -305,12 +305,14 @@ typedef struct pkv_extend_args {
  * already be in the pool (pkv_store first).  Arithmetic: bf16 inputs, fp32
  * accumulation and softmax, bf16 output.  The key range of a block of rows may
  * be split into kv_chunk chunks whose partials are merged by log-sum-exp.
- * workspace: at least pkv_extend_workspace_size(args) bytes, 256-byte aligned.
+ * workspace: at least pkv_extend_workspace_size(args) bytes, 256-byte aligned,
+ * non-null, caller-owned, not shared with a concurrent call: it holds the split
+ * partials and a work counter that the call resets on the stream before use.
  */
 pkv_status pkv_extend(const pkv_extend_args *args, void *workspace, size_t workspace_bytes,
                       int32_t *err_flags, pkv_stream_t stream);
 
-/* Workspace bytes pkv_extend needs for these arguments (0 on invalid arguments or no split). */
+/* Workspace bytes pkv_extend needs for these arguments (at least 256; 0 on invalid arguments). */
 size_t pkv_extend_workspace_size(const pkv_extend_args *args);
 
 /*

@@ -38,6 +38,8 @@ constexpr int kProducerWarp = 4, kQkWarp = 5, kPvWarp = 6, kEpiWarp0 = 7;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kLog2e = 1.44269504088896341f;
 constexpr float kLazy = 8.f;
+constexpr int kRing = 8;                   // slots of the item queue
+constexpr int kItemReaders = 11;           // warps that read every queued item
 
 template <int D>
 struct Cfg {
@@ -49,10 +51,11 @@ struct Cfg {
     static constexpr int kOffQ = 0;                            // two q blocks: this item's and the next
     static constexpr int kOffKV = kOffQ + 2 * kQBytes;
     static constexpr int kOffBar = kOffKV + kStages * kStageBytes;
-    static constexpr int kNumBars = 48;
+    static constexpr int kNumBars = 56;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;    // tmem slot, abort flag, scan scratch
     static constexpr int kOffStats = kOffMisc + 128;           // [2 items][128 rows] of (m, l) for the epilogue
-    static constexpr int kOffTable = kOffStats + 2 * kRows * 8;
+    static constexpr int kOffRing = kOffStats + 2 * kRows * 8; // the CTA's next items, as the producer claims them
+    static constexpr int kOffTable = kOffRing + kRing * 64;
     static constexpr int kFixedSmem = kOffTable + 1024;        // + request tables + alignment slack
     static constexpr uint32_t kColS = 0;                       // two 64-column score buffers
     static constexpr uint32_t kColO = 128;                     // two D-column output accumulators
@@ -71,7 +74,9 @@ struct Params {
     float *lse, *part_o, *part_lse;
     int32_t *err;
     int32_t cache_requests;   // per-request values kept in shared memory (they fit)
-    int32_t item_cache;       // items per CTA decoded once into shared memory
+    int32_t *counter;         // items handed out past the first wave (zeroed before the launch)
+    int32_t *goff, *ioff;     // [B + 1] first (kv head, query block) group / first item of each request,
+                              // written by CTA 0 for the merge kernel
 };
 
 // Keys of request b (0 and a flag for malformed inputs).
@@ -244,6 +249,34 @@ __device__ __forceinline__ void build_tables(const Params &p, const Tables &t, i
     }
     if (tid == kThreads - 1) t.off[B] = wbase + incl;
     __syncthreads();
+    if (blockIdx.x == 0) {   // the merge kernel's tables: items and groups per request, as prefixes
+        int gl = 0;
+        for (int b = lo; b < hi; ++b) {
+            const Req r = t.keys ? get_req(p, t, b) : load_req(p, b, false);
+            gl += p.hkv * ((r.n + p.T - 1) / p.T);
+        }
+        int gi = gl;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int x = __shfl_up_sync(0xffffffffu, gi, o);
+            if (lane >= o) gi += x;
+        }
+        if (lane == 31) scratch[warp] = gi;
+        __syncthreads();
+        int gbase = 0;
+        for (int w = 0; w < warp; ++w) gbase += scratch[w];
+        int grun = gbase + gi - gl;
+        for (int b = lo; b < hi; ++b) {
+            p.goff[b] = grun;
+            p.ioff[b] = t.off[b];
+            const Req r = t.keys ? get_req(p, t, b) : load_req(p, b, false);
+            grun += p.hkv * ((r.n + p.T - 1) / p.T);
+        }
+        if (tid == kThreads - 1) {
+            p.goff[B] = gbase + gi;
+            p.ioff[B] = t.off[B];
+        }
+        __syncthreads();
+    }
 }
 
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int32_t *err) {
@@ -291,25 +324,25 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 enum Bar {
     kQFull0 = 0, kQEmpty0 = 2, kKvFull0 = 4, kKvEmpty0 = kKvFull0 + 8, kSFull0 = kKvEmpty0 + 8,
     kSFree0 = kSFull0 + 2, kPFull0 = kSFree0 + 2, kPFree0 = kPFull0 + 2, kODone0 = kPFree0 + 2, kOFree0 = kODone0 + 2,
-    kStatFull0 = kOFree0 + 2, kFinalQk = kStatFull0 + 2, kFinalPv, kBarCount
+    kStatFull0 = kOFree0 + 2, kItemFull0 = kStatFull0 + 2, kItemEmpty0 = kItemFull0 + kRing,
+    kFinalQk = kItemEmpty0 + kRing, kFinalPv, kBarCount
 };
 
-// This CTA's item j (w = blockIdx.x + j * gridDim.x): from the shared-memory copy
-// made when the CTA starts (decoding an item is a long dependent chain for one
-// warp), or decoded afresh past the copy's end.
-__device__ __forceinline__ Item cta_item(const Params &p, const Tables &t, const Item *ic, int64_t j) {
-    if (j < p.item_cache) return ic[j];
-    return locate(p, t, blockIdx.x + j * gridDim.x);
-}
-
-// First item j' >= j of this CTA that has keys (n_items if none).
-__device__ __forceinline__ int64_t next_live(const Params &p, const Tables &t, const Item *ic, int64_t j,
-                                             int64_t n_items, Item &it) {
-    for (; j < n_items; ++j) {
-        it = cta_item(p, t, ic, j);
-        if (it.n_tiles > 0) return j;
+// Item k of this CTA's sequence from the queue (w < 0: no more items, or an
+// abort).  Every reader warp takes every item once, in order, and frees its slot.
+__device__ __forceinline__ Item ring_read(const Item *ring, uint64_t *bars, uint32_t k, bool &ok,
+                                          volatile int *abort_flag, int32_t *err) {
+    ok = warp_wait(ok, &bars[kItemFull0 + k % kRing], (k / kRing) & 1, abort_flag, err);
+    Item it;
+    if (ok) {
+        it = ring[k % kRing];
+    } else {
+        it.w = -1;
+        it.n_tiles = 0;
     }
-    return n_items;
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&bars[kItemEmpty0 + k % kRing]);
+    return it;
 }
 
 template <int D>
@@ -357,6 +390,10 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             mbar_init(&bars[kKvFull0 + s], 1);
             mbar_init(&bars[kKvEmpty0 + s], 1);
         }
+        for (int s = 0; s < kRing; ++s) {
+            mbar_init(&bars[kItemFull0 + s], 1);
+            mbar_init(&bars[kItemEmpty0 + s], kItemReaders);
+        }
         mbar_init(&bars[kFinalQk], 1);
         mbar_init(&bars[kFinalPv], 1);
         mbar_init_fence();
@@ -376,12 +413,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
     tc05::fence_after_sync();
     const uint32_t tbase = *tslot;
     const int64_t total = tb.off[p.batch];
-    const int64_t n_items = total > blockIdx.x ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-    Item *icache = reinterpret_cast<Item *>(
-        smem + ((C::kOffTable + (p.batch + 1) * 4 + (p.cache_requests ? 16 * p.batch : 0) + 15) & ~15));
-    for (int64_t j = tid; j < min(n_items, static_cast<int64_t>(p.item_cache)); j += kThreads)
-        icache[j] = locate(p, tb, blockIdx.x + j * gridDim.x);
-    __syncthreads();
+    Item *ring = reinterpret_cast<Item *>(smem + C::kOffRing);
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer: K/V tiles
@@ -397,44 +429,82 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
         const int nops = nbox * C::kSl * 2;
         const int j_box = (lane / (C::kSl * 2)) & (nbox - 1), sl_op = (lane >> 1) % C::kSl;
         const bool is_v = (lane & 1) != 0;
-        uint32_t n = 0;
+        uint32_t n = 0, kpub = 0;
         bool ok = true;
-        for (int64_t j = 0; j < n_items && ok; ++j) {
-            const Item it = cta_item(p, tb, icache, j);
-            if (it.n_tiles == 0) continue;
-            // pool row of box bx: -1 past the item's keys, -2 for a page outside the pool
-            auto box_row = [&](int bx) -> int {
-                const int kb = it.k0 + bx * box;
-                if (kb >= it.k1) return -1;
-                const int page = __ldg(tab + it.base + (kb >> p.ps_shift));
-                if (page < 0 || page >= p.num_pages) return -2;
-                return static_cast<int>((static_cast<int64_t>(page) << p.ps_shift) + (kb & p.ps_mask));
-            };
-            int win = 0;
-            int cur = box_row(lane), nxt = box_row(32 + lane);
-            for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
-                if (((ti * nbox) >> 5) != win) {
-                    ++win;
-                    cur = nxt;
-                    nxt = box_row(32 * (win + 1) + lane);
+        // The queue: the CTA's first item is blockIdx.x; later ones are claimed from a
+        // global counter (dynamic balance), two items ahead of the one being issued,
+        // decoded here and published to every reader warp.  A negative w ends it.
+        auto publish = [&](int64_t w) {
+            const uint32_t slot = kpub % kRing;
+            ok = warp_wait(ok, &bars[kItemEmpty0 + slot], ((kpub / kRing) & 1) ^ 1, abort_flag, p.err);
+            Item qi;
+            if (w >= 0 && w < total) {
+                qi = locate(p, tb, w);
+            } else {
+                qi.w = -1;
+                qi.n_tiles = 0;
+            }
+            if (lane == 0 && ok) {
+                ring[slot] = qi;
+                mbar_arrive(&bars[kItemFull0 + slot]);
+            }
+            __syncwarp();
+            ++kpub;
+        };
+        bool more = blockIdx.x < total;
+        publish(more ? static_cast<int64_t>(blockIdx.x) : -1);
+        if (more) {
+            int got = 0;
+            if (lane == 0) got = atomicAdd(p.counter, 1);
+            const int64_t w1 = static_cast<int64_t>(gridDim.x) + __shfl_sync(0xffffffffu, got, 0);
+            more = w1 < total;
+            publish(more ? w1 : -1);
+        }
+        for (uint32_t k = 0; ok; ++k) {
+            const Item it = ring_read(ring, bars, k, ok, abort_flag, p.err);
+            if (it.w < 0) break;
+            int got = 0;   // the claim's latency hides behind this item's tiles
+            if (more && lane == 0) got = atomicAdd(p.counter, 1);
+            if (it.n_tiles > 0) {
+                // pool row of box bx: -1 past the item's keys, -2 for a page outside the pool
+                auto box_row = [&](int bx) -> int {
+                    const int kb = it.k0 + bx * box;
+                    if (kb >= it.k1) return -1;
+                    const int page = __ldg(tab + it.base + (kb >> p.ps_shift));
+                    if (page < 0 || page >= p.num_pages) return -2;
+                    return static_cast<int>((static_cast<int64_t>(page) << p.ps_shift) + (kb & p.ps_mask));
+                };
+                int win = 0;
+                int cur = box_row(lane), nxt = box_row(32 + lane);
+                for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
+                    if (((ti * nbox) >> 5) != win) {
+                        ++win;
+                        cur = nxt;
+                        nxt = box_row(32 * (win + 1) + lane);
+                    }
+                    // pool row of this lane's box (a tile's boxes share one window: win or win + 1)
+                    const int bx0 = ti * nbox;
+                    int row = __shfl_sync(0xffffffffu, (bx0 >> 5) == win ? cur : nxt, (bx0 & 31) + j_box);
+                    if (lane >= nops) row = -1;
+                    if (row == -2 && lane % (2 * C::kSl) == 0) raise_flag(p.err, PKV_DEVERR_RANGE);
+                    const int s = n % kStages;
+                    if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
+                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                    if (!ok) break;
+                    const uint32_t valid = __ballot_sync(0xffffffffu, row >= 0);
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(&bars[kKvFull0 + s], __popc(valid) * static_cast<uint32_t>(box) * 128u);
+                    __syncwarp();
+                    if (row >= 0)
+                        tma_load_3d(sKV + s * C::kStageBytes + (is_v ? C::kKBytes : 0) + sl_op * kTile * 128 +
+                                        j_box * box * 128,
+                                    is_v ? &tmv : &tmk, sl_op * 64, it.kh, row, &bars[kKvFull0 + s]);
                 }
-                // pool row of this lane's box (a tile's boxes share one window: win or win + 1)
-                const int bx0 = ti * nbox;
-                int row = __shfl_sync(0xffffffffu, (bx0 >> 5) == win ? cur : nxt, (bx0 & 31) + j_box);
-                if (lane >= nops) row = -1;
-                if (row == -2 && lane % (2 * C::kSl) == 0) raise_flag(p.err, PKV_DEVERR_RANGE);
-                const int s = n % kStages;
-                if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
-                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                if (!ok) break;
-                const uint32_t valid = __ballot_sync(0xffffffffu, row >= 0);
-                if (lane == 0)
-                    mbar_arrive_expect_tx(&bars[kKvFull0 + s], __popc(valid) * static_cast<uint32_t>(box) * 128u);
-                __syncwarp();
-                if (row >= 0)
-                    tma_load_3d(sKV + s * C::kStageBytes + (is_v ? C::kKBytes : 0) + sl_op * kTile * 128 +
-                                    j_box * box * 128,
-                                is_v ? &tmv : &tmk, sl_op * 64, it.kh, row, &bars[kKvFull0 + s]);
+            }
+            if (more) {
+                const int64_t w2 = static_cast<int64_t>(gridDim.x) + __shfl_sync(0xffffffffu, got, 0);
+                more = w2 < total;
+                publish(more ? w2 : -1);
             }
         }
         if (lane == 0)   // drain: the copies this warp issued have landed
@@ -462,40 +532,46 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             __syncwarp();
             if (ok) ++q_issued;
         };
-        Item it;
-        int64_t j = next_live(p, tb, icache, 0, n_items, it);
-        if (j < n_items) load_q(it, 0);
-        while (j < n_items && ok) {
-            Item nx;
-            const int64_t jn = next_live(p, tb, icache, j + 1, n_items, nx);
-            const int sl = iq & 1;
-            ok = warp_wait(ok, &bars[kQFull0 + sl], (iq >> 1) & 1, abort_flag, p.err);
-            for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
-                const int s = n % kStages;
-                ok = warp_wait(ok, &bars[kKvFull0 + s], (n / kStages) & 1, abort_flag, p.err);
-                ok = warp_wait(ok, &bars[kSFree0 + (n & 1)], ((n >> 1) & 1) ^ 1, abort_flag, p.err);
-                if (!ok) break;
-                tc05::fence_after_sync();
-                if (lane == 0) {
-                    const uint64_t kd = tc05::smem_desc(sKV + s * C::kStageBytes, 16, 1024);
-                    const uint64_t qd = tc05::smem_desc(sQ + sl * C::kQBytes, 16, 1024);
-#pragma unroll
-                    for (int k2 = 0; k2 < C::kSl; ++k2)
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)   // slab: q +16 KB, K +8 KB; k-step +32 bytes
-                            tc05::mma_ss(tbase + C::kColS + (n & 1) * kTile,
-                                         qd + static_cast<uint64_t>((k2 * kRows * 128 + k * 32) >> 4),
-                                         kd + static_cast<uint64_t>((k2 * kTile * 128 + k * 32) >> 4), idesc,
-                                         (k2 | k) ? 1u : 0u);
-                    tc05::commit(&bars[kSFull0 + (n & 1)]);
-                    if (ti == it.n_tiles - 1) tc05::commit(&bars[kQEmpty0 + sl]);
+        uint32_t kr = 0;
+        Item it = ring_read(ring, bars, kr++, ok, abort_flag, p.err);
+        bool q_req = false;   // it's q block already requested
+        while (it.w >= 0 && ok) {
+            const Item nx = ring_read(ring, bars, kr++, ok, abort_flag, p.err);   // may be the end
+            bool nx_req = false;
+            if (it.n_tiles > 0) {
+                if (!q_req) load_q(it, iq);
+                const int sl = iq & 1;
+                ok = warp_wait(ok, &bars[kQFull0 + sl], (iq >> 1) & 1, abort_flag, p.err);
+                for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
+                    const int s = n % kStages;
+                    ok = warp_wait(ok, &bars[kKvFull0 + s], (n / kStages) & 1, abort_flag, p.err);
+                    ok = warp_wait(ok, &bars[kSFree0 + (n & 1)], ((n >> 1) & 1) ^ 1, abort_flag, p.err);
+                    if (!ok) break;
+                    tc05::fence_after_sync();
+                    if (lane == 0) {
+                        const uint64_t kd = tc05::smem_desc(sKV + s * C::kStageBytes, 16, 1024);
+                        const uint64_t qd = tc05::smem_desc(sQ + sl * C::kQBytes, 16, 1024);
+    #pragma unroll
+                        for (int k2 = 0; k2 < C::kSl; ++k2)
+    #pragma unroll
+                            for (int k = 0; k < 4; ++k)   // slab: q +16 KB, K +8 KB; k-step +32 bytes
+                                tc05::mma_ss(tbase + C::kColS + (n & 1) * kTile,
+                                             qd + static_cast<uint64_t>((k2 * kRows * 128 + k * 32) >> 4),
+                                             kd + static_cast<uint64_t>((k2 * kTile * 128 + k * 32) >> 4), idesc,
+                                             (k2 | k) ? 1u : 0u);
+                        tc05::commit(&bars[kSFull0 + (n & 1)]);
+                        if (ti == it.n_tiles - 1) tc05::commit(&bars[kQEmpty0 + sl]);
+                    }
+                    __syncwarp();
+                    if (ti == 0 && nx.w >= 0 && nx.n_tiles > 0) {
+                        load_q(nx, iq + 1);
+                        nx_req = true;
+                    }
                 }
-                __syncwarp();
-                if (ti == 0 && jn < n_items) load_q(nx, iq + 1);
+                ++iq;
             }
-            ++iq;
-            j = jn;
             it = nx;
+            q_req = nx_req;
         }
         if (lane == 0) {
             // q loads issued but not waited for have landed before shared memory is released
@@ -511,8 +587,9 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
         const uint32_t idesc = tc05::idesc_bf16_f32(kRows, D, false, true);
         uint32_t n = 0, io = 0;
         bool ok = true;
-        for (int64_t j = 0; j < n_items && ok; ++j) {
-            const Item it = cta_item(p, tb, icache, j);
+        for (uint32_t k = 0; ok; ++k) {
+            const Item it = ring_read(ring, bars, k, ok, abort_flag, p.err);
+            if (it.w < 0) break;
             if (it.n_tiles == 0) continue;
             const int ko = io & 1;
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
@@ -563,8 +640,9 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
         const int tok = r >> p.g_shift, hh = r & (p.g - 1);
         uint32_t io = 0;
         bool ok = true;
-        for (int64_t j = 0; j < n_items; ++j) {
-            const Item it = cta_item(p, tb, icache, j);
+        for (uint32_t k = 0;; ++k) {
+            const Item it = ring_read(ring, bars, k, ok, abort_flag, p.err);
+            if (it.w < 0) break;
             if (it.n_tiles == 0) continue;
             const int ko = io & 1;
             ok = warp_wait(ok, &bars[kStatFull0 + ko], (io >> 1) & 1, abort_flag, p.err);
@@ -643,19 +721,12 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             }
             return kend;
         };
-        Item it;
-        int kend = 0;
-        if (n_items > 0) {
-            it = cta_item(p, tb, icache, 0);
-            kend = row_bound(it);
-        }
-        for (int64_t j = 0; j < n_items; ++j) {
-            Item nx;
-            int kend_nx = 0;
-            if (j + 1 < n_items) {
-                nx = cta_item(p, tb, icache, j + 1);
-                kend_nx = row_bound(nx);
-            }
+        uint32_t kr = 0;
+        Item it = ring_read(ring, bars, kr++, ok, abort_flag, p.err);
+        int kend = it.w >= 0 ? row_bound(it) : 0;
+        while (it.w >= 0) {
+            const Item nx = ring_read(ring, bars, kr++, ok, abort_flag, p.err);   // may be the end
+            const int kend_nx = nx.w >= 0 ? row_bound(nx) : 0;
             const int tq = it.qblk * p.T + tok;                  // token within the request
             const bool valid = tq < it.n;
             const int64_t qrow = static_cast<int64_t>(it.qo0) + tq;
@@ -779,32 +850,28 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
 }
 
 // Log-sum-exp merge of the key chunks of one (request, kv head, query block):
-// one CTA per such group (found by walking the requests), rows x head_dim.
+// one CTA per such group (found in the prefix tables the attention kernel left),
+// rows x head_dim.
 template <int D>
 __global__ void __launch_bounds__(256) ext_merge_kernel(const Params p, int64_t groups) {
     const int64_t gi = blockIdx.x;
     if (gi >= groups) return;
-    // locate the group and its first item
-    int64_t g0 = 0, w0 = 0;
-    int b = 0, L = 0, n = 0;
-    for (; b < p.batch; ++b) {
-        int64_t base;
-        L = key_count(p, b, base, false);
-        n = q_count(p, b, false);
-        if (!p.kv_end && n > L) n = 0;
-        const int nq = (n + p.T - 1) / p.T;
-        const int64_t gb = static_cast<int64_t>(p.hkv) * nq;
-        if (gi < g0 + gb) break;
-        g0 += gb;
-        w0 += static_cast<int64_t>(p.hkv) * per_head_items(p, L, n);
+    // the group's request by binary search over the prefix tables, then its first item
+    if (gi >= p.goff[p.batch]) return;
+    int lo = 0, hi = p.batch;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.goff[mid] <= gi) lo = mid; else hi = mid;
     }
-    if (b >= p.batch) return;
+    const int b = lo;
+    const Req rq = load_req(p, b, false);
+    const int L = rq.L, n = rq.n;
     const int nq = (n + p.T - 1) / p.T;
-    const int rem = static_cast<int>(gi - g0);
+    const int rem = static_cast<int>(gi - p.goff[b]);
     const int kh = rem / nq, qblk = rem % nq;
     const int nch = chunks_of(p, block_keys(p, L, n, qblk));
     if (nch <= 1) return;
-    w0 += static_cast<int64_t>(kh) * per_head_items(p, L, n);
+    int64_t w0 = p.ioff[b] + static_cast<int64_t>(kh) * per_head_items(p, L, n);
     for (int q = 0; q < qblk; ++q) w0 += chunks_of(p, block_keys(p, L, n, q));
     for (int i = threadIdx.x; i < kRows * (D / 4); i += blockDim.x) {
         const int r = i / (D / 4), d4 = i % (D / 4);
@@ -829,7 +896,7 @@ __global__ void __launch_bounds__(256) ext_merge_kernel(const Params p, int64_t 
             }
         }
         const float inv = den > 0.f ? 1.f / den : 0.f;
-        const int64_t qrow = static_cast<int64_t>(p.qo_indptr[b]) + tb;
+        const int64_t qrow = static_cast<int64_t>(rq.qo0) + tb;
         const int head = kh * p.g + hh;
         uint2 o;
         o.x = pack_bf16x2(acc.x * inv, acc.y * inv);
@@ -884,6 +951,8 @@ struct Plan {
     int g, T, chunk, nch_max;
     int64_t items_max, groups_max;
     size_t part_o_bytes, part_lse_bytes;
+    static constexpr size_t kCounterBytes = 256;   // the item counter, after the partials
+    size_t table_bytes;                            // then the merge kernel's two prefix tables
 };
 
 static bool make_plan(const pkv_extend_args *a, Plan &pl) {
@@ -916,6 +985,7 @@ static bool make_plan(const pkv_extend_args *a, Plan &pl) {
         pl.part_o_bytes = (static_cast<size_t>(rows) * a->head_dim * 4 + 255) / 256 * 256;
         pl.part_lse_bytes = (static_cast<size_t>(rows) * 4 + 255) / 256 * 256;
     }
+    pl.table_bytes = (2 * (static_cast<size_t>(a->batch) + 1) * 4 + 255) / 256 * 256;
     return true;
 }
 
@@ -981,6 +1051,10 @@ static pkv_status launch_t(const pkv_extend_args *a, const Plan &pl, void *ws, i
     p.lse = a->lse;
     p.part_o = static_cast<float *>(ws);
     p.part_lse = reinterpret_cast<float *>(static_cast<char *>(ws) + pl.part_o_bytes);
+    p.counter = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + pl.part_o_bytes + pl.part_lse_bytes);
+    p.goff = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + pl.part_o_bytes + pl.part_lse_bytes +
+                                         Plan::kCounterBytes);
+    p.ioff = p.goff + a->batch + 1;
     p.err = err;
 
     CUtensorMap tmq, tmk, tmv;
@@ -1019,11 +1093,9 @@ static pkv_status launch_t(const pkv_extend_args *a, const Plan &pl, void *ws, i
     const size_t cached = smem + static_cast<size_t>(a->batch) * 16;
     p.cache_requests = cached <= lim ? 1 : 0;
     if (p.cache_requests) smem = cached;
-    // then this CTA's decoded items, as many as fit (up to 256)
-    smem = (smem + 15) & ~static_cast<size_t>(15);
-    p.item_cache = smem < lim ? static_cast<int32_t>(std::min<size_t>(256, (lim - smem) / sizeof(Item))) : 0;
-    smem += static_cast<size_t>(p.item_cache) * sizeof(Item);
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(pl.items_max, sm_count()));
+    if (cudaMemsetAsync(p.counter, 0, sizeof(int32_t), s) != cudaSuccess)
+        return fail(PKV_ERR_CUDA, "pkv_extend: cannot reset the item counter");
     ext_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p, tmq, tmk, tmv);
     pkv_status st = check_launch("pkv_extend (attention kernel)");
     if (st != PKV_OK || pl.nch_max <= 1) return st;
@@ -1039,7 +1111,7 @@ extern "C" size_t pkv_extend_workspace_size(const pkv_extend_args *args) {
     if (!args || validate(args, false) != PKV_OK) return 0;
     Plan pl;
     if (!make_plan(args, pl)) return 0;
-    return pl.part_o_bytes + pl.part_lse_bytes;
+    return pl.part_o_bytes + pl.part_lse_bytes + Plan::kCounterBytes + pl.table_bytes;
 }
 
 extern "C" pkv_status pkv_extend(const pkv_extend_args *args, void *workspace, size_t workspace_bytes,
@@ -1053,10 +1125,10 @@ extern "C" pkv_status pkv_extend(const pkv_extend_args *args, void *workspace, s
     if (args->batch == 0 || args->total_q == 0) return ok();
     Plan pl;
     if (!make_plan(args, pl)) return fail(PKV_ERR_UNSUPPORTED, "pkv_extend: too many work items");
-    const size_t need = pl.part_o_bytes + pl.part_lse_bytes;
+    const size_t need = pl.part_o_bytes + pl.part_lse_bytes + Plan::kCounterBytes + pl.table_bytes;
     if (workspace_bytes < need)
         return fail(PKV_ERR_CAPACITY, "pkv_extend: workspace of %zu bytes, %zu needed", workspace_bytes, need);
-    if (need && (!workspace || !aligned(workspace, 256)))
+    if (!workspace || !aligned(workspace, 256))
         return fail(PKV_ERR_INVALID_ARG, "pkv_extend: workspace must be non-null and 256-byte aligned");
     auto s = reinterpret_cast<cudaStream_t>(stream);
     return args->head_dim == 128 ? launch_t<128>(args, pl, workspace, err_flags, s)
