@@ -123,7 +123,7 @@ def measured_peaks():
 
 
 def decode_traffic(workload):
-    """Per-launch DRAM bytes of the decode launch from a committed ncu summary, if the kernel is unchanged."""
+    """Per-launch DRAM bytes of the workload's dominant kernel from a committed ncu summary, if the kernel is unchanged."""
     path = os.path.join(ROOT, "profiles", "decode_traffic.json")
     if not os.path.exists(path):
         return None
@@ -663,7 +663,7 @@ def run_extend(args, world, rank, local, dist):
         "roofline": {"bound": bound, "kernel": "pkv_extend (attention kernel + merge)", "achieved": round(achieved, 3),
                      "peak": peak, "unit": unit, "frac": round(achieved / peak, 4),
                      "peak_kind": peak_kind + (" (bf16 dense, burst)" if bound == "tensor" else ""),
-                     "avg_launch_ms": round(k_ms, 4), "traffic": None},
+                     "avg_launch_ms": round(k_ms, 4), "traffic": decode_traffic(args.workload)},
         "cpu_baseline": cpu,
         "e2e": {"value": round(world * amount * args.steps / (e_ms / 1e3), 3), "unit": unit,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms / args.steps, 4)},
