@@ -97,6 +97,15 @@ struct Params {
     int32_t *err;
 };
 
+// Marks the 16 floats as written here, so that no use of registers an asynchronous
+// TMEM load fills is scheduled before the wait that follows that load.
+__device__ __forceinline__ void reg_fence16(float (&v)[16]) {
+    asm volatile(""
+                 : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]), "+f"(v[7]),
+                   "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]), "+f"(v[12]), "+f"(v[13]), "+f"(v[14]),
+                   "+f"(v[15]));
+}
+
 // bit casts between a 32-bit word and a pair of fp16 values (by value, so arrays stay in registers)
 __device__ __forceinline__ __half2 u2h2(uint32_t u) {
     __half2_raw r;
@@ -586,18 +595,22 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
             // half2 in nxt[].  Both CTAs round their own partial the same way, so own
             // + peer is bitwise identical in the two CTAs.  (Macros rather than
             // lambdas keep the arrays in registers.)
-#define PKV_MLA_FETCH(t)                                                                                         \
+#define PKV_MLA_FETCH_ISSUE(t)                                                                                   \
     do {                                                                                                       \
         if (tid == 0) mbar_arrive_expect_tx(&bars[kXFull0 + (t) % kXSlots], kXBytes);                          \
         ok = warp_wait(ok, &bars[kSFull0 + ((t) & 1)], ((t) >> 1) & 1, abort_flag, p.err);                     \
-        float a_[16];                                                                                          \
         if (ok) {                                                                                              \
             tc05::fence_after_sync();                                                                          \
             tc05::ld_x16(trow + kColS + ((t) & 1) * kTile + qt * 16, a_);                                      \
-            tc05::wait_ld();                                                                                   \
         } else {                                                                                               \
             _Pragma("unroll") for (int j = 0; j < 16; ++j) a_[j] = 0.f;                                        \
         }                                                                                                      \
+    } while (0)
+            // the load lands: free the score buffer, round to fp16 into nxt[]
+#define PKV_MLA_FETCH_DONE(t)                                                                                    \
+    do {                                                                                                       \
+        tc05::wait_ld();                                                                                       \
+        reg_fence16(a_);                                                                                       \
         tc05::fence_before_sync();                                                                             \
         __syncwarp();                                                                                          \
         if (lane == 0) mbar_arrive(&bars[kSFree0 + ((t) & 1)]);                                               \
@@ -616,13 +629,16 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
         }                                                                                                      \
     } while (0)
             uint32_t cur[8], nxt[8];
-            PKV_MLA_FETCH(n);
+            float a_[16];
+            PKV_MLA_FETCH_ISSUE(n);
+            PKV_MLA_FETCH_DONE(n);
             PKV_MLA_SEND(n);
 #pragma unroll
             for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
             for (int ti = 0; ti < it.n_tiles; ++ti, ++n) {
                 const bool ahead = ti + 1 < it.n_tiles;
-                if (ahead) PKV_MLA_FETCH(n + 1);
+                // the scores of tile n + 1 load while the peer's partial of tile n is read
+                if (ahead) PKV_MLA_FETCH_ISSUE(n + 1);
                 // ---- the peer's partial of tile n (this thread's 16 keys) ----
                 const int xs = n % kXSlots;
                 ok = warp_wait(ok, &bars[kXFull0 + xs], (n / kXSlots) & 1, abort_flag, p.err);
@@ -643,7 +659,10 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
                 }
                 // slot n % 2 is read: tile n + 1 may go out (the peer answers it with
                 // tile n + 2 into this slot)
-                if (ahead) PKV_MLA_SEND(n + 1);
+                if (ahead) {
+                    PKV_MLA_FETCH_DONE(n + 1);
+                    PKV_MLA_SEND(n + 1);
+                }
                 if (n_valid < kTile) {   // keys past the end: -inf
                     const __half2 ninf = __halves2half2(__ushort_as_half(0xfc00), __ushort_as_half(0xfc00));
 #pragma unroll
@@ -716,7 +735,8 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
 #pragma unroll
                 for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
             }
-#undef PKV_MLA_FETCH
+#undef PKV_MLA_FETCH_ISSUE
+#undef PKV_MLA_FETCH_DONE
 #undef PKV_MLA_SEND
             // ---- the next segment's q goes in now, so its q.k overlaps this epilogue ----
             {
