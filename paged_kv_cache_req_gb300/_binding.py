@@ -183,11 +183,14 @@ def make_decode_args(kind, layout, q, k_pool, v_pool, out, *, page_size=1, sm_sc
     a.num_slots = k_pool.shape[0]
     a.k_row_stride, a.v_row_stride = k_pool.stride(0), v_stride
     a.kv_indices_len = kv_indices.numel() if kv_indices is not None else 0
-    for name, t in (("q", q), ("k_pool", k_pool), ("v_pool", v_pool), ("kv_indptr", kv_indptr),
-                    ("kv_indices", kv_indices), ("kv_last_page_len", kv_last_page_len),
-                    ("block_table", block_table), ("seq_lens", seq_lens), ("cu_seqlens", cu_seqlens),
-                    ("out", out), ("lse", lse)):
+    tensors = (("q", q), ("k_pool", k_pool), ("v_pool", v_pool), ("kv_indptr", kv_indptr),
+               ("kv_indices", kv_indices), ("kv_last_page_len", kv_last_page_len),
+               ("block_table", block_table), ("seq_lens", seq_lens), ("cu_seqlens", cu_seqlens),
+               ("out", out), ("lse", lse))
+    for name, t in tensors:
         setattr(a, name, None if t is None else _p(t).value)
+    # the struct holds raw pointers: keep the tensors alive as long as it lives
+    a._keep = tuple(t for _, t in tensors if t is not None)
     return a
 
 
@@ -277,10 +280,13 @@ def make_extend_args(layout, q, k_pool, v_pool, out, qo_indptr, *, page_size, sm
     a.total_q, a.num_slots = T, k_pool.shape[0]
     a.k_row_stride, a.v_row_stride = k_pool.stride(0), v_pool.stride(0)
     a.kv_indices_len = kv_indices.numel() if kv_indices is not None else 0
-    for name, t in (("q", q), ("k_pool", k_pool), ("v_pool", v_pool), ("qo_indptr", qo_indptr), ("kv_end", kv_end),
-                    ("kv_indptr", kv_indptr), ("kv_indices", kv_indices), ("kv_last_page_len", kv_last_page_len),
-                    ("block_table", block_table), ("seq_lens", seq_lens), ("out", out), ("lse", lse)):
+    tensors = (("q", q), ("k_pool", k_pool), ("v_pool", v_pool), ("qo_indptr", qo_indptr), ("kv_end", kv_end),
+               ("kv_indptr", kv_indptr), ("kv_indices", kv_indices), ("kv_last_page_len", kv_last_page_len),
+               ("block_table", block_table), ("seq_lens", seq_lens), ("out", out), ("lse", lse))
+    for name, t in tensors:
         setattr(a, name, None if t is None else _p(t).value)
+    # the struct holds raw pointers: keep the tensors alive as long as it lives
+    a._keep = tuple(t for _, t in tensors if t is not None)
     return a
 
 

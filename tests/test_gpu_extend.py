@@ -151,3 +151,30 @@ def test_extend_verify_long_rows(B):
     assert e == 0 and st == oracle.OK
     assert_close(gpu, ref, "verify long rows")
     assert_close(g_lse, ref_lse, "verify long rows lse")
+
+
+def test_args_structs_keep_their_tensors_alive(B):
+    # the structs hold raw pointers: a temporary passed in must outlive the call that built
+    # them (a freed q whose memory the next allocation reuses reads back as that allocation)
+    import gc
+    import weakref
+    dev = torch.device("cuda")
+    q = torch.zeros((4, 8, 64), dtype=torch.bfloat16, device=dev)
+    ref = weakref.ref(q)
+    a = B.make_extend_args(B.PKV_LAYOUT_CSR, q, torch.zeros((16, 2, 64), dtype=torch.bfloat16, device=dev),
+                           torch.zeros((16, 2, 64), dtype=torch.bfloat16, device=dev),
+                           torch.zeros((4, 8, 64), dtype=torch.bfloat16, device=dev),
+                           torch.zeros(2, dtype=torch.int32, device=dev), page_size=8, sm_scale=0.125, max_seq_len=16)
+    del q
+    gc.collect()
+    assert ref() is not None and a.q == ref().data_ptr()
+    lat = torch.zeros((64, 576), dtype=torch.bfloat16, device=dev)
+    lref = weakref.ref(lat)
+    d = B.make_decode_args(B.PKV_KIND_MLA, B.PKV_LAYOUT_BLOCK_TABLE,
+                           torch.zeros((2, 128, 576), dtype=torch.bfloat16, device=dev), lat, None,
+                           torch.zeros((2, 128, 512), dtype=torch.bfloat16, device=dev), page_size=64, sm_scale=0.07,
+                           max_seq_len=64, head_dim_v=512, block_table=torch.zeros((2, 1), dtype=torch.int32, device=dev),
+                           seq_lens=torch.zeros(2, dtype=torch.int32, device=dev))
+    del lat
+    gc.collect()
+    assert lref() is not None and d.k_pool == lref().data_ptr()
