@@ -19,6 +19,10 @@
  *     library allocates nothing and keeps no state between calls except a
  *     per-device cache of the SM count.
  *   - Every call is asynchronous on the caller's stream and never synchronizes.
+ *     Kernels are launched as programmatic dependents of the kernel before them in
+ *     the stream: they may be scheduled while it drains, but each waits for its
+ *     completion (and the visibility of its writes) before touching memory, so
+ *     stream order holds exactly as for ordinary launches.
  *   - Tensors are row-major with the last dimension contiguous.  K/V/q/out are
  *     bf16; tables are int32; lse is fp32.
  *   - Errors the host can see (null pointers, bad sizes, unsupported shapes,

@@ -64,6 +64,8 @@ alloc_extend_kernel(const int32_t *__restrict__ prefix_lens, const int32_t *__re
                     const int32_t *__restrict__ last_loc, int32_t batch, int32_t ps, int64_t num_pool_pages,
                     const int32_t *__restrict__ free_pages, int64_t free_pages_len, int32_t *__restrict__ free_state,
                     int32_t *__restrict__ out, int64_t out_cap, int32_t *__restrict__ err) {
+    pdl_wait();          // inputs may come from the previous kernel of the stream
+    pdl_launch_next();
     extern __shared__ int32_t sh[];
     int32_t *pages = sh;                       // [batch] new pages of each request
     int32_t *toks = sh + (batch + 1);          // [batch] new positions of each request
@@ -144,6 +146,8 @@ write_req_to_token_kernel(int32_t *__restrict__ r2t, int64_t r2t_rows, int64_t r
                           const int32_t *__restrict__ prefix_lens, const int32_t *__restrict__ seq_lens,
                           const int32_t *const *__restrict__ prefix_slots, const int32_t *__restrict__ out_cache_loc,
                           int32_t batch, int32_t *__restrict__ err) {
+    pdl_wait();          // inputs may come from the previous kernel of the stream
+    pdl_launch_next();
     __shared__ long long scratch[32];
     const int b = blockIdx.x;
     const int64_t c0 = static_cast<int64_t>(blockIdx.y) * kWriteSpan;
@@ -193,10 +197,11 @@ extern "C" pkv_status pkv_alloc_extend(const int32_t *prefix_lens, const int32_t
     if (smem > 48 * 1024 && cudaFuncSetAttribute(alloc_extend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(smem)) != cudaSuccess)
         return fail(PKV_ERR_CUDA, "pkv_alloc_extend: cannot raise the shared-memory limit");
-    alloc_extend_kernel<<<1, kAllocThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
-        prefix_lens, seq_lens, last_loc, batch, page_size, num_pool_pages, free_pages, free_pages_len, free_state,
-        out_cache_loc, out_cap, err_flags);
-    return check_launch("pkv_alloc_extend");
+    return launch_status(
+        launch_chained(alloc_extend_kernel, dim3(1), dim3(kAllocThreads), smem, reinterpret_cast<cudaStream_t>(stream),
+                       prefix_lens, seq_lens, last_loc, batch, page_size, num_pool_pages, free_pages, free_pages_len,
+                       free_state, out_cache_loc, out_cap, err_flags),
+        "pkv_alloc_extend");
 }
 
 extern "C" pkv_status pkv_write_req_to_token(int32_t *req_to_token, int64_t r2t_rows, int64_t r2t_row_stride,
@@ -213,9 +218,9 @@ extern "C" pkv_status pkv_write_req_to_token(int32_t *req_to_token, int64_t r2t_
     if (batch == 0) return ok();
     const int64_t spans = std::max<int64_t>(1, (r2t_width + kWriteSpan - 1) / kWriteSpan);
     if (spans > 65535) return fail(PKV_ERR_UNSUPPORTED, "pkv_write_req_to_token: rows too wide");
-    write_req_to_token_kernel<<<dim3(batch, static_cast<unsigned>(spans)), kWriteThreads, 0,
-                                reinterpret_cast<cudaStream_t>(stream)>>>(
-        req_to_token, r2t_rows, r2t_row_stride, r2t_width, req_pool_idx, kv_start, prefix_lens, seq_lens, prefix_slots,
-        out_cache_loc, batch, err_flags);
-    return check_launch("pkv_write_req_to_token");
+    return launch_status(launch_chained(write_req_to_token_kernel, dim3(batch, static_cast<unsigned>(spans)),
+                                        dim3(kWriteThreads), 0, reinterpret_cast<cudaStream_t>(stream), req_to_token,
+                                        r2t_rows, r2t_row_stride, r2t_width, req_pool_idx, kv_start, prefix_lens,
+                                        seq_lens, prefix_slots, out_cache_loc, batch, err_flags),
+                         "pkv_write_req_to_token");
 }

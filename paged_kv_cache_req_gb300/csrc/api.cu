@@ -29,6 +29,14 @@ pkv_status check_launch(const char *what) {
     return ok();
 }
 
+pkv_status launch_status(cudaError_t e, const char *what) {
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    }
+    return check_launch(what);
+}
+
 bool encode_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims, const uint64_t *strides,
                       const uint32_t *box, int swizzle_bytes) {
     using encode_fn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,

@@ -30,6 +30,8 @@ build_indices_kernel(const int32_t *__restrict__ r2t, int64_t r2t_rows, int64_t 
                      int64_t span, int32_t *__restrict__ kv_indptr, int32_t *__restrict__ kv_indices, int64_t cap,
                      int32_t *__restrict__ last_page_len, int32_t *__restrict__ block_table, int32_t bt_width,
                      int32_t *__restrict__ err) {
+    pdl_wait();          // inputs may come from the previous kernel of the stream
+    pdl_launch_next();
     __shared__ long long scratch[32];
     const int b = blockIdx.x;
     const int64_t c = blockIdx.y;
@@ -152,9 +154,10 @@ extern "C" pkv_status pkv_build_indices(const int32_t *req_to_token, int64_t r2t
     const int64_t spans = std::max<int64_t>(1, (covered + span - 1) / span);
     if (spans > 65535) return fail(PKV_ERR_UNSUPPORTED, "pkv_build_indices: rows too wide for the span grid");
     const dim3 grid(batch > 0 ? batch : 1, static_cast<unsigned>(spans));
-    build_indices_kernel<<<grid, kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        req_to_token, r2t_rows, r2t_row_stride, r2t_width, req_pool_idx, seq_lens, kv_start, batch, page_size,
-        num_pool_pages, span, kv_indptr, kv_indices, kv_indices_cap, kv_last_page_len, block_table,
-        block_table_width, err_flags);
-    return check_launch("pkv_build_indices");
+    return launch_status(launch_chained(build_indices_kernel, grid, dim3(kThreads), 0,
+                                        reinterpret_cast<cudaStream_t>(stream), req_to_token, r2t_rows, r2t_row_stride,
+                                        r2t_width, req_pool_idx, seq_lens, kv_start, batch, page_size, num_pool_pages,
+                                        span, kv_indptr, kv_indices, kv_indices_cap, kv_last_page_len, block_table,
+                                        block_table_width, err_flags),
+                         "pkv_build_indices");
 }

@@ -571,6 +571,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_cp_async_kernel(const Para
     int *off = reinterpret_cast<int *>(smem + kStages * T::kStageBytes + RedLayout<D, GC>::kBytes);
     __shared__ int scan_scratch[kWarps];
 
+    pdl_wait();          // lengths, tables and pool rows may come from the previous kernel
+    pdl_launch_next();
     build_item_table(p, off, scan_scratch, kThreads);
     const int total = off[p.batch];
 
@@ -682,6 +684,8 @@ decode_tma_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const
         prefetch_tmap(&tmk);
         prefetch_tmap(&tmv);
     }
+    pdl_wait();          // lengths, tables and pool rows may come from the previous kernel
+    pdl_launch_next();
     build_item_table(p, off, scan, kThreads + 32);
     const int total = off[p.batch];
 
@@ -799,6 +803,8 @@ decode_tma_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const
 // Log-sum-exp merge of a request's chunk partials (base-2 lse inside the workspace).
 template <int D, int GC>
 __global__ void __launch_bounds__(kThreads) merge_kernel(const Params p) {
+    pdl_wait();          // inputs may come from the previous kernel of the stream
+    pdl_launch_next();
     extern __shared__ float wsm[];  // [GC][n_chunks_max] weights
     const int idx = blockIdx.x;
     const int hs = idx % p.hsplit;
@@ -959,8 +965,8 @@ static pkv_status launch_merge(const Params &p, cudaStream_t s) {
                                  static_cast<int>(msmem)) != cudaSuccess)
             return fail(PKV_ERR_CUDA, "pkv_decode: cannot raise the merge shared-memory limit");
     }
-    merge_kernel<D, GC><<<p.batch * p.hkv * p.hsplit, kThreads, msmem, s>>>(p);
-    return check_launch("pkv_decode(GQA merge kernel)");
+    return launch_status(launch_chained(merge_kernel<D, GC>, dim3(p.batch * p.hkv * p.hsplit), dim3(kThreads), msmem, s, p),
+                         "pkv_decode(GQA merge kernel)");
 }
 
 template <int D, int GC, bool MMA>
@@ -983,7 +989,8 @@ static pkv_status launch_t(const Params &p, const pkv_decode_args *a, bool tma, 
         if (!encode_tmap_bf16(&tmk, a->k_pool, 3, dk, sk, box) || !encode_tmap_bf16(&tmv, a->v_pool, 3, dk, sv, box))
             return fail(PKV_ERR_CUDA, "pkv_decode: cuTensorMapEncodeTiled rejected the pool layout");
         const int grid = persistent_grid(kernel, kThreads + 32, smem, p);
-        kernel<<<grid, kThreads + 32, smem, s>>>(p, tmk, tmv);
+        st = launch_status(launch_chained(kernel, dim3(grid), dim3(kThreads + 32), smem, s, p, tmk, tmv),
+                           "pkv_decode(GQA split kernel)");
     } else {
         const auto kernel = decode_cp_async_kernel<D, GC, MMA>;
         static size_t lim = 0;
@@ -991,9 +998,8 @@ static pkv_status launch_t(const Params &p, const pkv_decode_args *a, bool tma, 
         const size_t smem = kStages * T::kStageBytes + RedLayout<D, GC>::kBytes + (static_cast<size_t>(p.batch) + 1) * 4;
         if (smem > lim) return fail(PKV_ERR_UNSUPPORTED, "pkv_decode: batch too large for the on-chip item table");
         const int grid = persistent_grid(kernel, kThreads, smem, p);
-        kernel<<<grid, kThreads, smem, s>>>(p);
+        st = launch_status(launch_chained(kernel, dim3(grid), dim3(kThreads), smem, s, p), "pkv_decode(GQA split kernel)");
     }
-    st = check_launch("pkv_decode(GQA split kernel)");
     if (st != PKV_OK) return st;
     return launch_merge<D, GC>(p, s);
 }

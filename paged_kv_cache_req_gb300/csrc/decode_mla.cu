@@ -333,6 +333,8 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
         prefetch_tmap(&tmkv);
         prefetch_tmap(&tmrope);
     }
+    pdl_wait();          // lengths, tables, q and the pool may come from the previous kernel
+    pdl_launch_next();
     const int V = p.batch * p.hgroups;
     build_row_table(p, V, R, scan, blockIdx.x == 0);   // contains __syncthreads
     tc05::fence_before_sync();
@@ -819,6 +821,8 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
 // base-2 lse in the workspace.  The decode kernel left the span length and the
 // row table in meta, from which the CTA finds the spans its row crosses.
 __global__ void __launch_bounds__(256) mla_merge_kernel(const Params p, int max_splits) {
+    pdl_wait();          // inputs may come from the previous kernel of the stream
+    pdl_launch_next();
     extern __shared__ float wsm[];  // [16][max_splits]
     __shared__ float den_s[16], mx_s[16];
     const int v = blockIdx.x, h0 = blockIdx.y * 16;
@@ -1034,15 +1038,16 @@ pkv_status launch(const pkv_decode_args *a, void *ws, size_t ws_bytes, int32_t *
         max_pairs = n;
     }
     const int pairs = std::max(1, std::min(max_pairs, pl.max_spans));
-    mla_decode_kernel<<<2 * pairs, kThreads, smem, s>>>(p, tmkv, tmrope);
-    pkv_status st = check_launch("pkv_decode(MLA split kernel)");
+    pkv_status st = launch_status(launch_chained(mla_decode_kernel, dim3(2 * pairs), dim3(kThreads), smem, s, p, tmkv, tmrope),
+                                  "pkv_decode(MLA split kernel)");
     if (st != PKV_OK) return st;
     if (msmem > 48 * 1024 &&
         cudaFuncSetAttribute(mla_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(msmem)) !=
             cudaSuccess)
         return fail(PKV_ERR_CUDA, "pkv_decode(MLA): cannot raise the merge shared-memory limit");
-    mla_merge_kernel<<<dim3(a->batch * pl.hgroups, kHeads / 16), 256, msmem, s>>>(p, pl.max_splits);
-    return check_launch("pkv_decode(MLA merge kernel)");
+    return launch_status(launch_chained(mla_merge_kernel, dim3(a->batch * pl.hgroups, kHeads / 16), dim3(256), msmem, s, p,
+                                        pl.max_splits),
+                         "pkv_decode(MLA merge kernel)");
 }
 
 }  // namespace mla

@@ -407,6 +407,8 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
         prefetch_tmap(&tmk);
         prefetch_tmap(&tmv);
     }
+    pdl_wait();          // lengths, bounds, q and the pools may come from the previous kernel
+    pdl_launch_next();
     build_tables(p, tb, scan);
     tc05::fence_before_sync();
     __syncthreads();
@@ -854,6 +856,8 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
 // rows x head_dim.
 template <int D>
 __global__ void __launch_bounds__(256) ext_merge_kernel(const Params p, int64_t groups) {
+    pdl_wait();          // inputs may come from the previous kernel of the stream
+    pdl_launch_next();
     const int64_t gi = blockIdx.x;
     if (gi >= groups) return;
     // the group's request by binary search over the prefix tables, then its first item
@@ -913,6 +917,8 @@ __global__ void __launch_bounds__(256)
 span_plan_kernel(int32_t batch, const int32_t *__restrict__ seg_indptr, const int32_t *__restrict__ seg_kind,
                  const int32_t *__restrict__ seg_start, const int32_t *__restrict__ seg_end, int32_t *__restrict__ qo,
                  int32_t *__restrict__ q_pos, int32_t *__restrict__ kv_end, int64_t cap, int32_t *__restrict__ err) {
+    pdl_wait();          // inputs may come from the previous kernel of the stream
+    pdl_launch_next();
     __shared__ long long scratch[32];
     const int b = blockIdx.x;
     auto seg_len = [&](int s) -> long long {
@@ -1099,8 +1105,9 @@ static pkv_status launch_t(const pkv_extend_args *a, const Plan &pl, void *ws, i
     ext_kernel<D><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p, tmq, tmk, tmv);
     pkv_status st = check_launch("pkv_extend (attention kernel)");
     if (st != PKV_OK || pl.nch_max <= 1) return st;
-    ext_merge_kernel<D><<<static_cast<unsigned>(pl.groups_max), 256, 0, s>>>(p, pl.groups_max);
-    return check_launch("pkv_extend (merge kernel)");
+    return launch_status(launch_chained(ext_merge_kernel<D>, dim3(static_cast<unsigned>(pl.groups_max)), dim3(256), 0, s,
+                                        p, pl.groups_max),
+                         "pkv_extend (merge kernel)");
 }
 
 }  // namespace ext
@@ -1145,7 +1152,8 @@ extern "C" pkv_status pkv_span_plan(int32_t batch, const int32_t *seg_indptr, co
     if (batch == 0) return ok();
     if (!seg_indptr || !seg_kind || !seg_start || !seg_end || !qo_indptr || (cap > 0 && (!q_pos || !kv_end)))
         return fail(PKV_ERR_INVALID_ARG, "pkv_span_plan: null input");
-    ext::span_plan_kernel<<<batch, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-        batch, seg_indptr, seg_kind, seg_start, seg_end, qo_indptr, q_pos, kv_end, cap, err_flags);
-    return check_launch("pkv_span_plan");
+    return launch_status(launch_chained(ext::span_plan_kernel, dim3(batch), dim3(256), 0,
+                                        reinterpret_cast<cudaStream_t>(stream), batch, seg_indptr, seg_kind, seg_start,
+                                        seg_end, qo_indptr, q_pos, kv_end, cap, err_flags),
+                         "pkv_span_plan");
 }

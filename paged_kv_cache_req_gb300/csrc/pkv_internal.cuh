@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "pkv.h"
 
 namespace pkv {
@@ -18,6 +20,29 @@ pkv_status ok();
 pkv_status check_launch(const char *what);
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
+
+// Launches `kernel` on stream `s` as a programmatic dependent of the kernel before it
+// in the stream: it may be scheduled while that kernel drains.  Every kernel of this
+// library calls pdl_wait() before its first global-memory access, which returns once
+// the previous kernel has completed and its writes are visible, so only the launch
+// and the on-chip prologue overlap.  Returns the launch error, if any.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                           Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+// Status of a launch_chained() call (clears the runtime's last-error state on failure).
+pkv_status launch_status(cudaError_t e, const char *what);
 
 // 2-D/3-D tiled TMA descriptor over a bf16 tensor (dims innermost first, strides in
 // bytes for dims 1..rank-1), 128-byte swizzle (or 64-byte: swizzle_bytes = 64);
@@ -166,6 +191,11 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int c0, 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
+// Programmatic dependent launch.  pdl_wait: block until the previous kernel of the
+// stream has completed and its memory is visible (returns at once when this launch was
+// not chained to it).  pdl_launch_next: allow the next chained kernel to be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_next() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");

@@ -34,6 +34,8 @@ store_kernel(uint16_t *__restrict__ k_pool, uint16_t *__restrict__ v_pool, int64
              int64_t v_stride, int64_t k_elems, int64_t v_elems, const uint16_t *__restrict__ k_new,
              const uint16_t *__restrict__ v_new, const int32_t *__restrict__ slot_mapping, int32_t n,
              int32_t *__restrict__ err) {
+    pdl_wait();          // inputs may come from the previous kernel of the stream
+    pdl_launch_next();
     const int warp = (blockIdx.x * kStoreThreads + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     const int rows_per_token = v_pool ? 2 : 1;
@@ -62,6 +64,8 @@ ragged_gather_kernel(const uint16_t *__restrict__ k_pool, const uint16_t *__rest
                      const int32_t *__restrict__ kv_start, const int32_t *__restrict__ seq_lens, int32_t batch,
                      uint16_t *__restrict__ k_out, uint16_t *__restrict__ v_out, int64_t cap,
                      int32_t *__restrict__ cu_seqlens, int32_t *__restrict__ err) {
+    pdl_wait();          // inputs may come from the previous kernel of the stream
+    pdl_launch_next();
     __shared__ long long scratch[32];
     const int b = blockIdx.x;
     if (b >= batch) {
@@ -112,6 +116,8 @@ encoder_merge_kernel(const uint8_t *__restrict__ buffer, int64_t num_blocks, int
                      const int32_t *__restrict__ block_ids, const int64_t *__restrict__ positions, int64_t entries,
                      uint8_t *__restrict__ hidden, int64_t num_tokens, int64_t hidden_stride,
                      unsigned long long *__restrict__ filled, int32_t *__restrict__ err) {
+    pdl_wait();          // inputs may come from the previous kernel of the stream
+    pdl_launch_next();
     __shared__ int cnt;
     if (threadIdx.x == 0) cnt = 0;
     __syncthreads();
@@ -180,12 +186,14 @@ extern "C" pkv_status pkv_store(void *k_pool, void *v_pool, int64_t num_slots, i
     auto kp = static_cast<uint16_t *>(k_pool), vp = static_cast<uint16_t *>(v_pool);
     auto kn = static_cast<const uint16_t *>(k_new), vn = static_cast<const uint16_t *>(v_new);
     if (vec)
-        store_kernel<true><<<blocks, kStoreThreads, 0, s>>>(kp, vp, num_slots, k_row_stride, v_row_stride, k_elems,
-                                                            v_elems, kn, vn, slot_mapping, n_tokens, err_flags);
-    else
-        store_kernel<false><<<blocks, kStoreThreads, 0, s>>>(kp, vp, num_slots, k_row_stride, v_row_stride, k_elems,
-                                                             v_elems, kn, vn, slot_mapping, n_tokens, err_flags);
-    return check_launch("pkv_store");
+        return launch_status(launch_chained(store_kernel<true>, dim3(blocks), dim3(kStoreThreads), 0, s, kp, vp,
+                                            num_slots, k_row_stride, v_row_stride, k_elems, v_elems, kn, vn,
+                                            slot_mapping, n_tokens, err_flags),
+                             "pkv_store");
+    return launch_status(launch_chained(store_kernel<false>, dim3(blocks), dim3(kStoreThreads), 0, s, kp, vp, num_slots,
+                                        k_row_stride, v_row_stride, k_elems, v_elems, kn, vn, slot_mapping, n_tokens,
+                                        err_flags),
+                         "pkv_store");
 }
 
 extern "C" pkv_status pkv_ragged_gather(const void *k_pool, const void *v_pool, int64_t num_slots,
@@ -217,14 +225,16 @@ extern "C" pkv_status pkv_ragged_gather(const void *k_pool, const void *v_pool, 
     auto kp = static_cast<const uint16_t *>(k_pool), vp = static_cast<const uint16_t *>(v_pool);
     auto ko = static_cast<uint16_t *>(k_out), vo = static_cast<uint16_t *>(v_out);
     if (vec)
-        ragged_gather_kernel<true><<<grid, kGatherThreads, 0, s>>>(
-            kp, vp, num_slots, pool_row_stride, row_elems, req_to_token, r2t_rows, r2t_row_stride, r2t_width,
-            req_pool_idx, kv_start, seq_lens, batch, ko, vo, out_rows_cap, cu_seqlens, err_flags);
-    else
-        ragged_gather_kernel<false><<<grid, kGatherThreads, 0, s>>>(
-            kp, vp, num_slots, pool_row_stride, row_elems, req_to_token, r2t_rows, r2t_row_stride, r2t_width,
-            req_pool_idx, kv_start, seq_lens, batch, ko, vo, out_rows_cap, cu_seqlens, err_flags);
-    return check_launch("pkv_ragged_gather");
+        return launch_status(launch_chained(ragged_gather_kernel<true>, dim3(grid), dim3(kGatherThreads), 0, s, kp, vp,
+                                            num_slots, pool_row_stride, row_elems, req_to_token, r2t_rows,
+                                            r2t_row_stride, r2t_width, req_pool_idx, kv_start, seq_lens, batch, ko, vo,
+                                            out_rows_cap, cu_seqlens, err_flags),
+                             "pkv_ragged_gather");
+    return launch_status(launch_chained(ragged_gather_kernel<false>, dim3(grid), dim3(kGatherThreads), 0, s, kp, vp,
+                                        num_slots, pool_row_stride, row_elems, req_to_token, r2t_rows, r2t_row_stride,
+                                        r2t_width, req_pool_idx, kv_start, seq_lens, batch, ko, vo, out_rows_cap,
+                                        cu_seqlens, err_flags),
+                         "pkv_ragged_gather");
 }
 
 extern "C" pkv_status pkv_encoder_merge(const void *buffer, int64_t num_blocks, int64_t block_size, int64_t row_bytes,
@@ -246,12 +256,16 @@ extern "C" pkv_status pkv_encoder_merge(const void *buffer, int64_t num_blocks, 
     auto s = reinterpret_cast<cudaStream_t>(stream);
     auto *cnt = reinterpret_cast<unsigned long long *>(filled);
     if (vec)
-        encoder_merge_kernel<true><<<static_cast<unsigned>(grid), kMergeThreads, 0, s>>>(
-            static_cast<const uint8_t *>(buffer), num_blocks, block_size, row_bytes, block_ids, positions, entries,
-            static_cast<uint8_t *>(hidden), num_tokens, hidden_row_stride_bytes, cnt, err_flags);
-    else
-        encoder_merge_kernel<false><<<static_cast<unsigned>(grid), kMergeThreads, 0, s>>>(
-            static_cast<const uint8_t *>(buffer), num_blocks, block_size, row_bytes, block_ids, positions, entries,
-            static_cast<uint8_t *>(hidden), num_tokens, hidden_row_stride_bytes, cnt, err_flags);
-    return check_launch("pkv_encoder_merge");
+        return launch_status(launch_chained(encoder_merge_kernel<true>, dim3(static_cast<unsigned>(grid)),
+                                            dim3(kMergeThreads), 0, s, static_cast<const uint8_t *>(buffer),
+                                            num_blocks, block_size, row_bytes, block_ids, positions, entries,
+                                            static_cast<uint8_t *>(hidden), num_tokens, hidden_row_stride_bytes, cnt,
+                                            err_flags),
+                             "pkv_encoder_merge");
+    return launch_status(launch_chained(encoder_merge_kernel<false>, dim3(static_cast<unsigned>(grid)),
+                                        dim3(kMergeThreads), 0, s, static_cast<const uint8_t *>(buffer), num_blocks,
+                                        block_size, row_bytes, block_ids, positions, entries,
+                                        static_cast<uint8_t *>(hidden), num_tokens, hidden_row_stride_bytes, cnt,
+                                        err_flags),
+                         "pkv_encoder_merge");
 }
