@@ -364,7 +364,7 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
         uint32_t n = 0;
         bool ok = true;
         Cursor cur{pair, pair * per};
-        Seg it;
+        Seg it{};
         // pool row of this lane's box of tile ti (-1: past the end, -2: bad page id)
         auto box_row = [&](int ti, bool report) -> int {
             if (lane >= nbox) return -1;
@@ -424,7 +424,7 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
         uint32_t n = 0, ic = 0;
         bool ok = true;
         Cursor cur{pair, pair * per};
-        Seg it;
+        Seg it{};
         while (ok && next_seg(p, R, V, per, S, npairs, cur, it)) {
             ok = warp_wait(ok, &bars[kQFull], ic & 1, abort_flag, p.err);
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
@@ -476,7 +476,7 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
         uint32_t n = 0, ic = 0;
         bool ok = true;
         Cursor cur{pair, pair * per};
-        Seg it;
+        Seg it{};
         while (ok && next_seg(p, R, V, per, S, npairs, cur, it)) {
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
                 ok = warp_wait(ok, &bars[kPFull0 + (n & 1)], (n >> 1) & 1, abort_flag, p.err);
@@ -585,7 +585,7 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
         }
         bool q_loaded = false;
         Cursor cs{pair, pair * per};
-        Seg it;
+        Seg it{};
         while (next_seg(p, R, V, per, S, npairs, cs, it)) {
             const int head = it.hg * kHeads + row;
             const int64_t orow = static_cast<int64_t>(it.b) * p.hq + head;
