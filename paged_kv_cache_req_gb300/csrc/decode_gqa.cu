@@ -855,13 +855,19 @@ struct Plan {
 };
 
 static int choose_chunk(const pkv_decode_args *a, int units) {
-    // Largest chunk (<= 1024 keys) that still gives ~4 waves of work when the
-    // requests average half of max_seq_len.
-    const int64_t target = 4ll * std::max(1, sm_count()) * 2;
+    // Fewest equal chunks of the longest request (each a multiple of 64 keys, at most
+    // 1024) that still give about two waves of work items when the requests average
+    // half of max_seq_len.  Equal chunks keep the items of one request alike, and a
+    // request short enough for one chunk needs no merge at all.
+    const int64_t target = 2ll * std::max(1, sm_count()) * 2;
     const int64_t L = std::max<int64_t>(1, a->max_seq_len);
-    for (int c = 1024; c > kTile; c >>= 1) {
-        const int64_t items = static_cast<int64_t>(a->batch) * units * ((L + c - 1) / c);
-        if (items / 2 >= target) return c;
+    const int64_t half = std::max<int64_t>(1, L / 2);
+    for (int64_t n = std::max<int64_t>(1, (L + 1023) / 1024); n <= L; ++n) {
+        const int64_t c = ((L + n - 1) / n + kTile - 1) / kTile * kTile;
+        if (c > 1024) continue;
+        if (c <= kTile) break;
+        const int64_t items = static_cast<int64_t>(a->batch) * units * ((half + c - 1) / c);
+        if (items >= target) return static_cast<int>(c);
     }
     return kTile;
 }
