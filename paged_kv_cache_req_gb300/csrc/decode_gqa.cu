@@ -179,8 +179,11 @@ __device__ __forceinline__ Item locate(const Params &p, const int *off, int w, b
     it.L = key_count(p, it.b, it.base, report && it.c == 0 && it.kh == 0 && it.hs == 0);
     it.n_chunks = max(1, (it.L + p.chunk - 1) / p.chunk);
     it.head0 = it.kh * p.g + it.hs * GC;
-    it.t_begin = it.c * p.chunk;
-    it.t_end = min(it.L, it.t_begin + p.chunk);
+    // the request's n_chunks pieces are made equal (a multiple of 64 keys, at most
+    // p.chunk), so its last piece is not a stub that leaves the others waiting
+    const int span = ((it.L + it.n_chunks - 1) / it.n_chunks + kTile - 1) / kTile * kTile;
+    it.t_begin = it.c * span;
+    it.t_end = min(it.L, it.t_begin + span);
     return it;
 }
 

@@ -209,8 +209,10 @@ __device__ __forceinline__ Item locate(const Params &p, const Tables &t, int64_t
     it.c = rem;
     const int kmax = block_keys(p, it.L, it.n, q);
     it.nch = chunks_of(p, kmax);
-    it.k0 = it.c * p.chunk;
-    it.k1 = min(kmax, it.k0 + p.chunk);
+    // the block's nch pieces are made equal (a multiple of 64 keys, at most p.chunk)
+    const int span = ((kmax + it.nch - 1) / it.nch + kTile - 1) / kTile * kTile;
+    it.k0 = it.c * span;
+    it.k1 = min(kmax, it.k0 + span);
     it.n_tiles = it.k1 > it.k0 ? (it.k1 - it.k0 + kTile - 1) / kTile : 0;
     return it;
 }
