@@ -260,7 +260,7 @@ pkv_status pkv_ragged_gather(const void *k_pool, const void *v_pool, int64_t num
 /*
  * Arguments of pkv_extend (multi-query attention through the page table).
  * Pools and layouts as for pkv_decode (CSR or BLOCK_TABLE; page_size a power
- * of two in [8, 1024]).
+ * of two in [1, 1024]; pages under 8 keys are gathered row by row).
  */
 typedef struct pkv_extend_args {
     int32_t layout;            /* PKV_LAYOUT_CSR or PKV_LAYOUT_BLOCK_TABLE */

@@ -77,6 +77,8 @@ struct Params {
     int32_t *counter;         // items handed out past the first wave (zeroed before the launch)
     int32_t *goff, *ioff;     // [B + 1] first (kv head, query block) group / first item of each request,
                               // written by CTA 0 for the merge kernel
+    const uint16_t *k_pool, *v_pool;   // pages under 8 keys: rows gathered with cp.async
+    int64_t k_stride, v_stride;        // elements between pool rows
 };
 
 // Keys of request b (0 and a flag for malformed inputs).
@@ -435,10 +437,29 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
         const bool is_v = (lane & 1) != 0;
         uint32_t n = 0, kpub = 0;
         bool ok = true;
+        // Pages under 8 keys: the producer gathers a tile's rows itself with 16-byte
+        // cp.async copies (one commit group per tile), written in the same swizzled
+        // layout the TMA boxes produce.  A tile's full barrier is arrived once its
+        // group has completed and the warp has fenced its writes for the tensor
+        // cores' async proxy; up to two tiles stay in flight (`pend`).
+        const bool gather = box < 8;
+        uint32_t pend = 0, n_arr = 0;   // tiles in flight; the oldest of them
+        auto settle_one = [&]() {
+            if (pend >= 3) cp_async_wait<2>();
+            else if (pend == 2) cp_async_wait<1>();
+            else cp_async_wait<0>();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kKvFull0 + n_arr % kStages]);
+            ++n_arr;
+            --pend;
+        };
+        auto settle_all = [&]() { while (pend > 0) settle_one(); };
         // The queue: the CTA's first item is blockIdx.x; later ones are claimed from a
         // global counter (dynamic balance), two items ahead of the one being issued,
         // decoded here and published to every reader warp.  A negative w ends it.
         auto publish = [&](int64_t w) {
+            settle_all();   // the readers of the queue may be waiting for these tiles
             const uint32_t slot = kpub % kRing;
             ok = warp_wait(ok, &bars[kItemEmpty0 + slot], ((kpub / kRing) & 1) ^ 1, abort_flag, p.err);
             Item qi;
@@ -478,6 +499,43 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                     if (page < 0 || page >= p.num_pages) return -2;
                     return static_cast<int>((static_cast<int64_t>(page) << p.ps_shift) + (kb & p.ps_mask));
                 };
+                if (gather) {
+                    for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
+                        const int kt0 = it.k0 + ti * kTile;
+                        // pool row of key j of the tile: -1 past the item's keys, -2 outside the pool
+                        auto key_row = [&](int j) -> int {
+                            const int kk = kt0 + j;
+                            if (kk >= it.k1) return -1;
+                            const int page = __ldg(tab + it.base + (kk >> p.ps_shift));
+                            if (page < 0 || page >= p.num_pages) return -2;
+                            return static_cast<int>((static_cast<int64_t>(page) << p.ps_shift) + (kk & p.ps_mask));
+                        };
+                        const int r0 = key_row(lane), r1 = key_row(lane + 32);
+                        if (r0 == -2 || r1 == -2) raise_flag(p.err, PKV_DEVERR_RANGE);
+                        const int s = n % kStages;
+                        if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
+                        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                        if (!ok) break;
+                        constexpr int CPR = D / 8;       // 16-byte chunks per row
+                        constexpr int KPI = 32 / CPR;    // rows per warp instruction
+                        const int c = lane % CPR, sl = c >> 3, cc = c & 7;
+                        unsigned char *kst = sKV + s * C::kStageBytes, *vst = kst + C::kKBytes;
+#pragma unroll 4
+                        for (int j0 = 0; j0 < kTile; j0 += KPI) {
+                            const int j = j0 + lane / CPR;
+                            const int a0 = __shfl_sync(0xffffffffu, r0, j & 31), a1 = __shfl_sync(0xffffffffu, r1, j & 31);
+                            const int row = j < 32 ? a0 : a1;
+                            const bool live = row >= 0;
+                            const int off = sl * kTile * 128 + j * 128 + ((cc ^ (j & 7)) << 4);
+                            const int64_t col = static_cast<int64_t>(it.kh) * D + c * 8;
+                            cp_async_16(kst + off, live ? p.k_pool + row * p.k_stride + col : p.k_pool, live ? 16 : 0);
+                            cp_async_16(vst + off, live ? p.v_pool + row * p.v_stride + col : p.v_pool, live ? 16 : 0);
+                        }
+                        cp_async_commit();
+                        ++pend;
+                        if (pend > 2) settle_one();
+                    }
+                } else {
                 int win = 0;
                 int cur = box_row(lane), nxt = box_row(32 + lane);
                 for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
@@ -504,6 +562,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                                         j_box * box * 128,
                                     is_v ? &tmv : &tmk, sl_op * 64, it.kh, row, &bars[kKvFull0 + s]);
                 }
+                }
             }
             if (more) {
                 const int64_t w2 = static_cast<int64_t>(gridDim.x) + __shfl_sync(0xffffffffu, got, 0);
@@ -511,6 +570,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                 publish(more ? w2 : -1);
             }
         }
+        settle_all();
         if (lane == 0)   // drain: the copies this warp issued have landed
             for (uint32_t k = n > kStages ? n - kStages : 0; k < n; ++k)
                 drain_wait(&bars[kKvFull0 + k % kStages], (k / kStages) & 1);
@@ -1005,8 +1065,8 @@ static pkv_status validate(const pkv_extend_args *a, bool check_ptrs) {
     const int g = a->num_q_heads / a->num_kv_heads;
     if (!is_pow2(g) || g > 16) return fail(PKV_ERR_UNSUPPORTED, "pkv_extend: Hq/Hkv must be 1, 2, 4, 8 or 16");
     if (a->head_dim != 64 && a->head_dim != 128) return fail(PKV_ERR_UNSUPPORTED, "pkv_extend: head_dim 64 or 128");
-    if (!is_pow2(a->page_size) || a->page_size < 8 || a->page_size > 1024)
-        return fail(PKV_ERR_UNSUPPORTED, "pkv_extend: page_size must be a power of two in [8, 1024]");
+    if (!is_pow2(a->page_size) || a->page_size > 1024)
+        return fail(PKV_ERR_UNSUPPORTED, "pkv_extend: page_size must be a power of two in [1, 1024]");
     if (a->layout != PKV_LAYOUT_CSR && a->layout != PKV_LAYOUT_BLOCK_TABLE)
         return fail(PKV_ERR_INVALID_ARG, "pkv_extend: layout must be CSR or BLOCK_TABLE");
     if (a->kv_chunk < 0 || a->kv_chunk % kTile) return fail(PKV_ERR_INVALID_ARG, "pkv_extend: kv_chunk multiple of 64");
@@ -1064,6 +1124,10 @@ static pkv_status launch_t(const pkv_extend_args *a, const Plan &pl, void *ws, i
                                          Plan::kCounterBytes);
     p.ioff = p.goff + a->batch + 1;
     p.err = err;
+    p.k_pool = static_cast<const uint16_t *>(a->k_pool);
+    p.v_pool = static_cast<const uint16_t *>(a->v_pool);
+    p.k_stride = a->k_row_stride;
+    p.v_stride = a->v_row_stride;
 
     CUtensorMap tmq, tmk, tmv;
     {   // q [total_q, Hq, D]: boxes of 64 dims x g heads x T tokens = 128 rows of 128 bytes

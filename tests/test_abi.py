@@ -75,7 +75,7 @@ def test_extend_args_layout_matches_c(binding, tmp_path):
     assert binding._lib.pkv_extend(ctypes.byref(a), None, 0, ctypes.byref(flag), None) == binding.PKV_ERR_UNSUPPORTED
     a.num_q_heads, a.head_dim = 16, 96
     assert binding._lib.pkv_extend(ctypes.byref(a), None, 0, ctypes.byref(flag), None) == binding.PKV_ERR_UNSUPPORTED
-    a.head_dim, a.page_size = 128, 4
+    a.head_dim, a.page_size = 128, 24                  # not a power of two
     assert binding._lib.pkv_extend(ctypes.byref(a), None, 0, ctypes.byref(flag), None) == binding.PKV_ERR_UNSUPPORTED
     assert binding._lib.pkv_extend_workspace_size(ctypes.byref(a)) == 0
     assert flag.value == 0

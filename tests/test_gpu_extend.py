@@ -80,6 +80,20 @@ def test_extend_causal_mix(B, hq, hkv, d, ps):
     assert_close(g_lse, ref_lse, "extend lse")
 
 
+@pytest.mark.parametrize("ps", [1, 2, 4])
+@pytest.mark.parametrize("hq,hkv,d", [(32, 8, 128), (8, 2, 64)])
+def test_extend_small_pages_gathered_by_rows(B, ps, hq, hkv, d):
+    # pages under 8 keys: the producer gathers rows with cp.async instead of TMA boxes
+    lens = [300, 77, 1000, 1, 129]
+    nq = [300, 5, 64, 1, 16]
+    for chunk in (0, 64):
+        case = _case(ps * 10 + d + chunk, lens, nq, hq, hkv, d, ps)
+        e, gpu, g_lse, st, ref, ref_lse = _run(B, *case, lens, ps, chunk=chunk)
+        assert e == 0 and st == oracle.OK
+        assert_close(gpu, ref, "extend ps=%d d=%d chunk=%d" % (ps, d, chunk))
+        assert_close(g_lse, ref_lse, "extend lse ps=%d" % ps)
+
+
 @pytest.mark.parametrize("chunk", [64, 192, 1024])
 @pytest.mark.parametrize("layout", ["csr", "block_table"])
 def test_extend_split_keys_and_layouts(B, chunk, layout):

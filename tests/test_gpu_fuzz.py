@@ -75,7 +75,7 @@ def test_mla_decode_random_configs(B, seed):
 def test_extend_random_configs(B, seed):
     rng = np.random.default_rng(3000 + seed)
     hq, hkv, d = [(32, 8, 128), (16, 16, 128), (8, 1, 64), (32, 4, 128), (16, 2, 64)][seed % 5]
-    ps = int(rng.choice([8, 16, 32, 64, 128, 256]))   # pkv_extend takes pages of 8 to 1024 keys
+    ps = int(rng.choice([1, 2, 4, 8, 16, 32, 64, 128, 256]))
     nb = int(rng.integers(1, 6))
     lens = [int(x) for x in rng.integers(1, 1200, size=nb)]
     nq = [int(rng.integers(1, min(L, 128) + 1)) for L in lens]
