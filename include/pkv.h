@@ -145,7 +145,7 @@ typedef struct pkv_decode_args {
     int32_t num_kv_heads;      /* Hkv (must be 1 for MLA) */
     int32_t head_dim_qk;       /* GQA: 64 or 128; MLA: 576 */
     int32_t head_dim_v;        /* GQA: equal to head_dim_qk; MLA: 512 */
-    int32_t page_size;         /* power of two (CSR / block table): GQA 1..1024, MLA 8..1024; ignored for VARLEN */
+    int32_t page_size;         /* power of two, 1..1024 (CSR / block table); ignored for VARLEN */
     float sm_scale;            /* softmax scale, e.g. 1/sqrt(head_dim) */
     int32_t max_seq_len;       /* host upper bound on every request's key count; sizes the split plan */
     int32_t kv_chunk;          /* keys per split, a multiple of 64; 0 lets the library choose.  MLA: keys

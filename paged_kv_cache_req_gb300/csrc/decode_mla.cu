@@ -95,6 +95,8 @@ struct Params {
     float *part_o, *part_lse;  // [span][2 slots][128 heads] x (512 | 1), base-2 lse
     int32_t *meta;             // [0]: tiles per span, [1 + v]: first tile of row v (rows + 1 entries)
     int32_t *err;
+    const uint16_t *pool;      // latent rows (read directly when pages are under 8 keys)
+    int64_t pool_stride;       // elements between latent rows
 };
 
 // Marks the 16 floats as written here, so that no use of registers an asynchronous
@@ -282,6 +284,7 @@ enum Bar {
 static_assert(kBarCount <= kNumBars, "barrier slots");
 static_assert(16 + 4 * (kThreads / 32) <= kOffRed - kOffMisc, "scan scratch");
 
+template <bool kGather>   // pages under 8 keys: rows gathered with cp.async instead of TMA boxes
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, const __grid_constant__ CUtensorMap tmrope) {
     extern __shared__ unsigned char smem_raw[];
@@ -386,7 +389,70 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
                 for (int sl = 0; sl < kVSlabs; ++sl) tma_prefetch_2d(&tmkv, (slab0 + sl) * 64, r);
             }
         };
+        // Pages under 8 keys: the warp gathers each tile's rows with 16-byte cp.async
+        // copies into the layout the TMA boxes would produce (128-byte swizzle for the
+        // value slabs, 64-byte for the rope rows), one commit group per tile; a
+        // tile's full barrier is arrived once its group completed and the writes are
+        // fenced for the tensor cores' async proxy.  Up to two tiles stay in flight.
+        constexpr bool gather = kGather;
+        uint32_t pend = 0, n_arr = 0;
+        auto settle_one = [&]() {
+            if (pend >= 3) cp_async_wait<2>();
+            else if (pend == 2) cp_async_wait<1>();
+            else cp_async_wait<0>();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[kKvFull0 + n_arr % kStages]);
+            ++n_arr;
+            --pend;
+        };
         while (ok && next_seg(p, R, V, per, S, npairs, cur, it)) {
+            if constexpr (gather) {
+                for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
+                    const int kt0 = it.key_begin + ti * kTile;
+                    auto key_row = [&](int j) -> int {   // -1 past the segment, -2 outside the pool
+                        const int kk = kt0 + j;
+                        if (kk >= it.key_end) return -1;
+                        if (p.layout == PKV_LAYOUT_VARLEN) return static_cast<int>(it.base + kk);
+                        const int32_t *tab = p.layout == PKV_LAYOUT_CSR ? p.kv_indices : p.block_table;
+                        const int page = __ldg(tab + it.base + (kk >> p.ps_shift));
+                        if (page < 0 || page >= p.num_pages) return -2;
+                        return static_cast<int>((static_cast<int64_t>(page) << p.ps_shift) + (kk & p.ps_mask));
+                    };
+                    const int r0 = key_row(lane), r1 = key_row(lane + 32);
+                    if (r0 == -2 || r1 == -2) raise_flag(p.err, PKV_DEVERR_RANGE);
+                    const int s = n % kStages;
+                    if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
+                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                    if (!ok) break;
+                    unsigned char *st = sKV + s * kStageBytes;
+                    // value slabs: lane = 16-byte chunk (slab lane / 8, chunk lane % 8) of one key row
+                    const int sl = lane >> 3, cc = lane & 7;
+#pragma unroll 4
+                    for (int j = 0; j < kTile; ++j) {
+                        const int a0 = __shfl_sync(0xffffffffu, r0, j & 31), a1 = __shfl_sync(0xffffffffu, r1, j & 31);
+                        const int row = j < 32 ? a0 : a1;
+                        const bool live = row >= 0;
+                        cp_async_16(st + sl * kSlabBytes + j * 128 + ((cc ^ (j & 7)) << 4),
+                                    live ? p.pool + row * p.pool_stride + (slab0 + sl) * 64 + cc * 8 : p.pool,
+                                    live ? 16 : 0);
+                    }
+                    // rope rows: 4 chunks of 64 bytes per key, 8 keys per instruction
+#pragma unroll
+                    for (int j0 = 0; j0 < kTile; j0 += 8) {
+                        const int j = j0 + (lane >> 2), c = lane & 3;
+                        const int a0 = __shfl_sync(0xffffffffu, r0, j & 31), a1 = __shfl_sync(0xffffffffu, r1, j & 31);
+                        const int row = j < 32 ? a0 : a1;
+                        const bool live = row >= 0;
+                        cp_async_16(st + kVSlabs * kSlabBytes + j * 64 + ((c ^ ((j >> 1) & 3)) << 4),
+                                    live ? p.pool + row * p.pool_stride + rope0 + c * 8 : p.pool, live ? 16 : 0);
+                    }
+                    cp_async_commit();
+                    ++pend;
+                    if (pend > 2) settle_one();
+                }
+                continue;
+            }
             for (int ti = 0; ti < kPrefetch && ti < it.n_tiles; ++ti) prefetch(ti);
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
                 if (ti + kPrefetch < it.n_tiles) prefetch(ti + kPrefetch);
@@ -409,6 +475,7 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
                 }
             }
         }
+        while (pend > 0) settle_one();
         // drain: the copies this warp issued have landed before shared memory is released
         if (lane == 0)
             for (uint32_t k = n > kStages ? n - kStages : 0; k < n; ++k)
@@ -921,8 +988,8 @@ pkv_status validate(const pkv_decode_args *a, bool check_ptrs) {
         return fail(PKV_ERR_UNSUPPORTED, "pkv_decode(MLA): head_dim_qk 576 and head_dim_v 512 are supported");
     if (a->num_q_heads % kHeads)
         return fail(PKV_ERR_UNSUPPORTED, "pkv_decode(MLA): num_q_heads must be a multiple of 128");
-    if (a->layout != PKV_LAYOUT_VARLEN && (!is_pow2(a->page_size) || a->page_size < 8 || a->page_size > 1024))
-        return fail(PKV_ERR_UNSUPPORTED, "pkv_decode(MLA): page_size must be a power of two in [8, 1024]");
+    if (a->layout != PKV_LAYOUT_VARLEN && (!is_pow2(a->page_size) || a->page_size > 1024))
+        return fail(PKV_ERR_UNSUPPORTED, "pkv_decode(MLA): page_size must be a power of two in [1, 1024]");
     if (a->kv_chunk < 0 || a->kv_chunk % kTile)
         return fail(PKV_ERR_INVALID_ARG, "pkv_decode(MLA): kv_chunk must be a multiple of 64");
     if (a->layout != PKV_LAYOUT_CSR && a->layout != PKV_LAYOUT_BLOCK_TABLE && a->layout != PKV_LAYOUT_VARLEN)
@@ -955,6 +1022,38 @@ size_t workspace_size(const pkv_decode_args *a) {
     Plan pl;
     if (a->batch == 0 || !make_plan(a, pl)) return 0;
     return pl.part_o_bytes + pl.part_lse_bytes + pl.meta_bytes;
+}
+
+// Opt-in shared memory (raised once) and the most co-resident CTA pairs of one
+// instantiation of the decode kernel.
+template <bool G>
+static pkv_status kernel_limits(size_t &lim_out, int &pairs_out) {
+    static size_t lim = 0;
+    static int max_pairs = 0;
+    if (!lim) {
+        int optin = 0, dev = 0;
+        cudaFuncAttributes fa{};
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaFuncGetAttributes(&fa, mla_decode_kernel<G>) != cudaSuccess)
+            return fail(PKV_ERR_CUDA, "pkv_decode(MLA): cannot query shared-memory limits");
+        const size_t l = static_cast<size_t>(optin) - fa.sharedSizeBytes;
+        if (cudaFuncSetAttribute(mla_decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(l)) != cudaSuccess)
+            return fail(PKV_ERR_CUDA, "pkv_decode(MLA): cannot raise the shared-memory limit");
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(2 * std::max(1, sm_count() / 2));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = l;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel<G>, &cfg) != cudaSuccess || n < 1)
+            n = std::max(1, sm_count() / 2);
+        max_pairs = n;
+        lim = l;
+    }
+    lim_out = lim;
+    pairs_out = max_pairs;
+    return PKV_OK;
 }
 
 pkv_status launch(const pkv_decode_args *a, void *ws, size_t ws_bytes, int32_t *err, cudaStream_t s) {
@@ -995,6 +1094,8 @@ pkv_status launch(const pkv_decode_args *a, void *ws, size_t ws_bytes, int32_t *
     p.part_lse = reinterpret_cast<float *>(static_cast<char *>(ws) + pl.part_o_bytes);
     p.meta = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + pl.part_o_bytes + pl.part_lse_bytes);
     p.err = err;
+    p.pool = static_cast<const uint16_t *>(a->k_pool);
+    p.pool_stride = a->k_row_stride;
     if (a->layout == PKV_LAYOUT_VARLEN) p.ps_shift = 0, p.ps_mask = 0;
 
     // TMA map of the latent pool as [num_slots rows, 576] (box box_rows x 64 dims, 128-byte swizzle).
@@ -1010,36 +1111,19 @@ pkv_status launch(const pkv_decode_args *a, void *ws, size_t ws_bytes, int32_t *
     if (!encode_tmap_bf16(&tmrope, a->k_pool, 2, dk, sk, br, 64))
         return fail(PKV_ERR_CUDA, "pkv_decode(MLA): cuTensorMapEncodeTiled rejected the latent pool (rope view)");
 
-    static size_t lim = 0;
-    static int max_pairs = 0;
+    const bool gather = p.box_rows < 8;
+    size_t lim = 0;
+    int max_pairs = 0;
+    pkv_status st = gather ? kernel_limits<true>(lim, max_pairs) : kernel_limits<false>(lim, max_pairs);
+    if (st != PKV_OK) return st;
     const size_t smem = kFixedSmem + (static_cast<size_t>(a->batch) * pl.hgroups + 1) * 4;
-    if (!lim) {
-        int optin = 0, dev = 0;
-        cudaFuncAttributes fa{};
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-            cudaFuncGetAttributes(&fa, mla_decode_kernel) != cudaSuccess)
-            return fail(PKV_ERR_CUDA, "pkv_decode(MLA): cannot query shared-memory limits");
-        const size_t l = static_cast<size_t>(optin) - fa.sharedSizeBytes;
-        if (cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(l)) !=
-            cudaSuccess)
-            return fail(PKV_ERR_CUDA, "pkv_decode(MLA): cannot raise the shared-memory limit");
-        lim = l;
-    }
     if (smem > lim) return fail(PKV_ERR_UNSUPPORTED, "pkv_decode(MLA): batch too large for the on-chip item table");
-    if (!max_pairs) {
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3(2 * std::max(1, sm_count() / 2));
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = lim;
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel, &cfg) != cudaSuccess || n < 1)
-            n = std::max(1, sm_count() / 2);
-        max_pairs = n;
-    }
     const int pairs = std::max(1, std::min(max_pairs, pl.max_spans));
-    pkv_status st = launch_status(launch_chained(mla_decode_kernel, dim3(2 * pairs), dim3(kThreads), smem, s, p, tmkv, tmrope),
-                                  "pkv_decode(MLA split kernel)");
+    st = launch_status(gather ? launch_chained(mla_decode_kernel<true>, dim3(2 * pairs), dim3(kThreads), smem, s, p,
+                                               tmkv, tmrope)
+                              : launch_chained(mla_decode_kernel<false>, dim3(2 * pairs), dim3(kThreads), smem, s, p,
+                                               tmkv, tmrope),
+                       "pkv_decode(MLA split kernel)");
     if (st != PKV_OK) return st;
     if (msmem > 48 * 1024 &&
         cudaFuncSetAttribute(mla_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(msmem)) !=

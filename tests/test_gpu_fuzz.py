@@ -59,7 +59,7 @@ def test_gqa_decode_random_configs(B, seed):
 @pytest.mark.parametrize("seed", range(6))
 def test_mla_decode_random_configs(B, seed):
     rng = np.random.default_rng(2000 + seed)
-    ps = int(rng.choice([8, 16, 32, 64, 128, 256]))
+    ps = int(rng.choice([1, 2, 4, 8, 16, 32, 64, 128, 256]))
     lens = _lengths(rng, int(rng.integers(1, 6)), int(rng.choice([100, 1500, 3000])))
     chunk = int(rng.choice([0, 64, 128, 320]))
     layout = "csr" if rng.random() < 0.5 else "block_table"

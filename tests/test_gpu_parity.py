@@ -459,6 +459,18 @@ def test_mla_edge_lengths(B, layout, chunk):
     assert_close(g_lse[1:], ref_lse[1:], "MLA lse")
 
 
+@pytest.mark.parametrize("ps", [1, 2, 4])
+@pytest.mark.parametrize("layout", ["block_table", "csr"])
+def test_mla_small_pages_gathered_by_rows(B, ps, layout):
+    # pages under 8 keys: the producer gathers the latent rows with cp.async instead of TMA boxes
+    lens = [0, 1, 63, 65, 300, 1000]
+    for chunk in (0, 64):
+        gpu, g_lse, ref, ref_lse = _direct_mla(B, lens, ps, chunk=chunk, layout=layout, seed=ps + chunk)
+        assert (gpu[0] == 0).all() and np.isneginf(g_lse[0]).all()
+        assert_close(gpu, ref, "MLA ps=%d %s chunk=%d" % (ps, layout, chunk))
+        assert_close(g_lse[1:], ref_lse[1:], "MLA lse ps=%d" % ps)
+
+
 @pytest.mark.parametrize("ps", [16, 128])
 def test_mla_other_page_sizes_and_head_groups(B, ps):
     gpu, g_lse, ref, ref_lse = _direct_mla(B, [5, 300, 777], ps, hq=256, seed=ps)
