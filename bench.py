@@ -432,7 +432,8 @@ def run_merge(args, world, rank, local, dist):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "kernel": "pkv_encoder_merge", "achieved": round(achieved, 2), "peak": hbm,
                      "unit": "GB/s", "frac": round(achieved / hbm, 4), "peak_kind": peak_kind,
-                     "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": round(avg_ms, 4), "traffic": None},
+                     "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": round(avg_ms, 4),
+                     "traffic": decode_traffic("encoder_merge")},
         "cpu_baseline": cpu,
         "e2e": {"value": round(weak_scaling_gbs(world, nbytes, args.steps, e_ms), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(mw.block_ids.nbytes + mw.positions.nbytes), "d2h_bytes_per_step": 8,
