@@ -741,8 +741,19 @@ decode_tma_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const
             if (lane == 0) ok = wait_or_abort(&empty[s], ((n / S) & 1) ^ 1, abort_flag, p.err);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) return;
-            if (row == -2) raise_flag(p.err, PKV_DEVERR_RANGE);
+            if (row == -2) {   // a page outside the pool reads as zeros (and raises the flag)
+                raise_flag(p.err, PKV_DEVERR_RANGE);
+                unsigned char *kst = smem + s * T::kStageBytes;
+                for (int h = 0; h < T::kSlabs; ++h)
+                    for (uint32_t o = 0; o < box_bytes; o += 16) {
+                        *reinterpret_cast<uint4 *>(kst + h * (kTile * 128) + lane * box_bytes + o) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(kst + T::kBytes + h * (kTile * 128) + lane * box_bytes + o) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                fence_proxy_async_smem();   // before later TMA writes into this stage
+            }
             const uint32_t valid = __ballot_sync(0xffffffffu, row >= 0);
+            __syncwarp();
             if (lane == 0) mbar_arrive_expect_tx(&full[s], __popc(valid) * box_bytes * T::kSlabs * 2u);
             __syncwarp();
             if (row >= 0) {

@@ -461,7 +461,17 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
                 if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) break;
+                if (row == -2) {   // a page outside the pool reads as zeros (the flag is raised by box_row)
+                    unsigned char *st = sKV + s * kStageBytes;
+                    for (int sl = 0; sl < kVSlabs; ++sl)
+                        for (uint32_t o = 0; o < box_bytes; o += 16)
+                            *reinterpret_cast<uint4 *>(st + sl * kSlabBytes + lane * box_bytes + o) = make_uint4(0, 0, 0, 0);
+                    for (int o = 0; o < box * 64; o += 16)
+                        *reinterpret_cast<uint4 *>(st + kVSlabs * kSlabBytes + lane * box * 64 + o) = make_uint4(0, 0, 0, 0);
+                    fence_proxy_async_smem();   // for the tensor cores and later TMA writes
+                }
                 const uint32_t valid = __ballot_sync(0xffffffffu, row >= 0);
+                __syncwarp();
                 if (lane == 0)
                     mbar_arrive_expect_tx(&bars[kKvFull0 + s], __popc(valid) * static_cast<uint32_t>(box) *
                                                                    static_cast<uint32_t>(kVSlabs * 128 + 64));

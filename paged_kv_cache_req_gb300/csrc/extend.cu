@@ -553,7 +553,14 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                     if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
                     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                     if (!ok) break;
+                    if (row == -2) {   // a page outside the pool reads as zeros
+                        unsigned char *dz = sKV + s * C::kStageBytes + (is_v ? C::kKBytes : 0) + sl_op * kTile * 128 +
+                                            j_box * box * 128;
+                        for (int o = 0; o < box * 128; o += 16) *reinterpret_cast<uint4 *>(dz + o) = make_uint4(0, 0, 0, 0);
+                        fence_proxy_async_smem();   // for the tensor cores and later TMA writes
+                    }
                     const uint32_t valid = __ballot_sync(0xffffffffu, row >= 0);
+                    __syncwarp();
                     if (lane == 0)
                         mbar_arrive_expect_tx(&bars[kKvFull0 + s], __popc(valid) * static_cast<uint32_t>(box) * 128u);
                     __syncwarp();

@@ -192,3 +192,39 @@ def test_args_structs_keep_their_tensors_alive(B):
     del lat
     gc.collect()
     assert lref() is not None and d.k_pool == lref().data_ptr()
+
+
+@pytest.mark.parametrize("ps", [2, 16])
+def test_extend_flags_out_of_pool_pages(B, ps):
+    """A page id outside the pool raises PKV_DEVERR_RANGE and reads as zeros, in both producers
+    (row gather for pages under 8 keys, TMA boxes otherwise); other requests stay exact."""
+    dev = torch.device("cuda")
+    lens, nq = [40, 24], [4, 3]
+    case = _case(ps, lens, nq, 16, 4, 128, ps)
+    r2t, rpi, num_pages, k, v, q, qo = case
+    st, indptr, indices, last, bt = oracle.build_indices(r2t, rpi, lens, ps, num_pages)
+    assert st == oracle.OK
+    bad = np.array(indices, dtype=np.int32)
+    bad[0] = num_pages + 5                       # first page of request 0: outside the pool
+    out = torch.zeros(tuple(q.shape), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    args = B.make_extend_args(B.PKV_LAYOUT_CSR, q.to(dev), k.to(dev), v.to(dev), out, _dev(qo), page_size=ps,
+                              sm_scale=1 / math.sqrt(128), max_seq_len=max(lens), kv_indptr=_dev(indptr),
+                              kv_indices=_dev(bad), kv_last_page_len=_dev(last))
+    ws = torch.empty(max(B.pkv_extend_workspace_size(args), 256), dtype=torch.uint8, device=dev)
+    B.pkv_extend(args, ws, err)
+    torch.cuda.synchronize()
+    assert err.item() & B.PKV_DEVERR_RANGE
+    assert torch.isfinite(out.float()).all()
+    kv_end = np.concatenate([np.arange(L - n, L) + 1 for L, n in zip(lens, nq)]).astype(np.int32)
+    st, ref, _ = oracle.extend(bits(q), bits(k), bits(v), r2t, rpi, lens, qo, kv_end, 1 / math.sqrt(128))
+    assert st == oracle.OK
+    assert_close(bf16_to_f64(out)[qo[1]:], ref[qo[1]:], "valid request next to a bad one, ps=%d" % ps)
+    # the bad page reads as zeros: the oracle over a pool whose rows of that page are zero
+    page = int(indices[0])
+    kz, vz = k.clone(), v.clone()
+    kz[page * ps:(page + 1) * ps] = 0
+    vz[page * ps:(page + 1) * ps] = 0
+    st, refz, _ = oracle.extend(bits(q), bits(kz), bits(vz), r2t, rpi, lens, qo, kv_end, 1 / math.sqrt(128))
+    assert st == oracle.OK
+    assert_close(bf16_to_f64(out)[:qo[1]], refz[:qo[1]], "out-of-pool page reads as zeros, ps=%d" % ps)

@@ -387,6 +387,49 @@ def test_decode_flags_out_of_pool_pages(B):
     st, ref, _ = oracle.decode(bits(q[1:].cpu()), bits(k.cpu()), bits(v.cpu()),
                                np.asarray([[0] * 5, [32, 33, 34, 35, 36]], dtype=np.int32), [1], [5], 0.1)
     assert_close(bf16_to_f64(out[1:]), ref, "valid request next to a bad one")
+    # the bad page reads as zeros: request 0 over page 1 and a page of zero rows
+    kz = torch.cat([k.cpu(), torch.zeros((16, hkv, d), dtype=torch.bfloat16)])
+    vz = torch.cat([v.cpu(), torch.zeros((16, hkv, d), dtype=torch.bfloat16)])
+    row0 = np.asarray([list(range(16, 32)) + list(range(64, 80))], dtype=np.int32)
+    st, refz, _ = oracle.decode(bits(q[:1].cpu()), bits(kz), bits(vz), np.vstack([np.zeros((1, 32), np.int32), row0]),
+                                [1], [32], 0.1)
+    assert_close(bf16_to_f64(out[:1]), refz, "out-of-pool page reads as zeros")
+
+
+@pytest.mark.parametrize("ps", [2, 64])
+def test_mla_flags_out_of_pool_pages(B, ps):
+    """MLA: a page id outside the pool raises PKV_DEVERR_RANGE in both producers; the other request is exact."""
+    dev = torch.device("cuda")
+    lens = [3 * ps, 70]
+    num_pages = 4 + sum(-(-L // ps) for L in lens)
+    rng = np.random.default_rng(ps)
+    r2t, rpi = paged_table(rng, lens, ps, num_pages)
+    gen = torch.Generator().manual_seed(ps)
+    lat = torch.randn((num_pages * ps, 576), generator=gen).to(torch.bfloat16)
+    q = torch.randn((2, 128, 576), generator=gen).to(torch.bfloat16)
+    st, indptr, indices, last, bt = oracle.build_indices(r2t, rpi, lens, ps, num_pages)
+    assert st == oracle.OK
+    bad = np.array(indices, dtype=np.int32)
+    bad[1] = num_pages + 3                       # second page of request 0: outside the pool
+    out = torch.zeros((2, 128, 512), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+    args = B.make_decode_args(B.PKV_KIND_MLA, B.PKV_LAYOUT_CSR, q.to(dev), lat.to(dev), None, out, page_size=ps,
+                              sm_scale=1 / math.sqrt(192), max_seq_len=max(lens), head_dim_v=512,
+                              kv_indptr=t(indptr), kv_indices=t(bad), kv_last_page_len=t(last))
+    ws = torch.empty(max(B.pkv_decode_workspace_size(args), 256), dtype=torch.uint8, device=dev)
+    B.pkv_decode(args, ws, err)
+    torch.cuda.synchronize()
+    assert err.item() & B.PKV_DEVERR_RANGE
+    assert torch.isfinite(out.float()).all()
+    st, ref, _ = oracle.decode(bits(q), bits(lat), bits(lat), r2t, rpi, lens, 1 / math.sqrt(192), head_dim_v=512)
+    assert_close(bf16_to_f64(out)[1:], ref[1:], "MLA valid request next to a bad one, ps=%d" % ps)
+    # the bad page reads as zeros: the oracle over a pool whose rows of that page are zero
+    page = int(indices[1])
+    latz = lat.clone()
+    latz[page * ps:(page + 1) * ps] = 0
+    st, refz, _ = oracle.decode(bits(q), bits(latz), bits(latz), r2t, rpi, lens, 1 / math.sqrt(192), head_dim_v=512)
+    assert_close(bf16_to_f64(out)[:1], refz[:1], "MLA out-of-pool page reads as zeros, ps=%d" % ps)
 
 
 def test_decode_rejects_small_workspace(B):
