@@ -432,6 +432,56 @@ def test_mla_flags_out_of_pool_pages(B, ps):
     assert_close(bf16_to_f64(out)[:1], refz[:1], "MLA out-of-pool page reads as zeros, ps=%d" % ps)
 
 
+def test_decode_clamps_requests_past_max_seq_len(B):
+    """A request longer than max_seq_len raises PKV_DEVERR_CAPACITY and attends only its first keys:
+    up to the split plan's reach for GQA (here 2 chunks of 64 keys), up to max_seq_len for MLA."""
+    dev = torch.device("cuda")
+    rng = np.random.default_rng(11)
+    gen = torch.Generator().manual_seed(11)
+    lens, ps = [200, 50], 16
+    num_pages = 4 + sum(-(-L // ps) for L in lens)
+    r2t, rpi = paged_table(rng, lens, ps, num_pages)
+    r2t_d, rpi_d = torch.from_numpy(r2t).to(dev), torch.from_numpy(rpi).to(dev)
+    lens_t = torch.tensor(lens, dtype=torch.int32, device=dev)
+    npages = [-(-L // ps) for L in lens]
+    # GQA, CSR pages, kv_chunk 64 and max_seq_len 100: the plan reaches 128 keys
+    k = torch.randn((num_pages * ps, 2, 128), generator=gen).to(torch.bfloat16)
+    v = torch.randn((num_pages * ps, 2, 128), generator=gen).to(torch.bfloat16)
+    q = torch.randn((2, 8, 128), generator=gen).to(torch.bfloat16)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    indptr = torch.empty(3, dtype=torch.int32, device=dev)
+    idx = torch.empty(sum(npages), dtype=torch.int32, device=dev)
+    last = torch.empty(2, dtype=torch.int32, device=dev)
+    B.pkv_build_indices(r2t_d, rpi_d, lens_t, ps, num_pages, err, kv_indptr=indptr, kv_indices=idx, kv_last_page_len=last)
+    out = torch.empty((2, 8, 128), dtype=torch.bfloat16, device=dev)
+    args = B.make_decode_args(B.PKV_KIND_GQA, B.PKV_LAYOUT_CSR, q.to(dev), k.to(dev), v.to(dev), out, page_size=ps,
+                              sm_scale=0.09, max_seq_len=100, kv_indptr=indptr, kv_indices=idx, kv_last_page_len=last,
+                              kv_chunk=64)
+    ws = torch.empty(max(B.pkv_decode_workspace_size(args), 256), dtype=torch.uint8, device=dev)
+    B.pkv_decode(args, ws, err)
+    torch.cuda.synchronize()
+    assert err.item() == B.PKV_DEVERR_CAPACITY
+    st, ref, _ = oracle.decode(bits(q), bits(k), bits(v), r2t, rpi, [128, 50], 0.09)
+    assert st == oracle.OK
+    assert_close(bf16_to_f64(out), ref, "GQA request clamped to the plan's reach")
+    # MLA, block table, max_seq_len 100
+    lat = torch.randn((num_pages * ps, 576), generator=gen).to(torch.bfloat16)
+    qm = torch.randn((2, 128, 576), generator=gen).to(torch.bfloat16)
+    err.zero_()
+    bt = torch.empty((2, max(npages)), dtype=torch.int32, device=dev)
+    B.pkv_build_indices(r2t_d, rpi_d, lens_t, ps, num_pages, err, block_table=bt)
+    outm = torch.empty((2, 128, 512), dtype=torch.bfloat16, device=dev)
+    args = B.make_decode_args(B.PKV_KIND_MLA, B.PKV_LAYOUT_BLOCK_TABLE, qm.to(dev), lat.to(dev), None, outm,
+                              page_size=ps, sm_scale=1 / math.sqrt(192), max_seq_len=100, head_dim_v=512,
+                              block_table=bt, seq_lens=lens_t)
+    ws = torch.empty(max(B.pkv_decode_workspace_size(args), 256), dtype=torch.uint8, device=dev)
+    B.pkv_decode(args, ws, err)
+    torch.cuda.synchronize()
+    assert err.item() == B.PKV_DEVERR_CAPACITY
+    st, refm, _ = oracle.decode(bits(qm), bits(lat), bits(lat), r2t, rpi, [100, 50], 1 / math.sqrt(192), head_dim_v=512)
+    assert_close(bf16_to_f64(outm), refm, "MLA request clamped to max_seq_len")
+
+
 def test_decode_rejects_small_workspace(B):
     step = _step("qwen3_0p6b", kv_chunk=64)
     pb = step.problems["self"]
