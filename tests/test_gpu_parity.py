@@ -365,6 +365,38 @@ def test_decode_varlen_layout_direct(B):
     assert_close(bf16_to_f64(out), ref, "varlen")
 
 
+@pytest.mark.parametrize("chunk", [0, 64])
+def test_mla_varlen_layout_direct(B, chunk):
+    """MLA over a contiguous latent buffer: keys of request b are rows cu[b]..cu[b+1]-1."""
+    dev = torch.device("cuda")
+    gen = torch.Generator().manual_seed(5 + chunk)
+    lens = [3, 0, 1500, 77, 64]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    lat = torch.randn((int(cu[-1]), 576), generator=gen).to(torch.bfloat16)
+    q = torch.randn((len(lens), 128, 576), generator=gen).to(torch.bfloat16)
+    r2t = np.zeros((len(lens) + 1, max(lens)), dtype=np.int32)
+    for b, L in enumerate(lens):
+        r2t[b + 1, :L] = np.arange(cu[b], cu[b] + L)
+    scale = 1 / math.sqrt(192)
+    st, ref, ref_lse = oracle.decode(bits(q), bits(lat), bits(lat), r2t, np.arange(1, len(lens) + 1), lens, scale,
+                                     head_dim_v=512)
+    assert st == oracle.OK
+    out = torch.empty((len(lens), 128, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((len(lens), 128), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    args = B.make_decode_args(B.PKV_KIND_MLA, B.PKV_LAYOUT_VARLEN, q.to(dev), lat.to(dev), None, out,
+                              sm_scale=scale, max_seq_len=max(lens), head_dim_v=512,
+                              cu_seqlens=torch.from_numpy(cu).to(dev), lse=lse, kv_chunk=chunk)
+    ws = torch.empty(max(B.pkv_decode_workspace_size(args), 256), dtype=torch.uint8, device=dev)
+    B.pkv_decode(args, ws, err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert_close(bf16_to_f64(out), ref, "MLA varlen chunk=%d" % chunk)
+    live = [b for b, L in enumerate(lens) if L > 0]
+    assert_close(lse.double().cpu().numpy()[live], ref_lse[live], "MLA varlen lse")
+    assert (bf16_to_f64(out)[1] == 0).all() and np.isneginf(lse[1].cpu().numpy()).all()
+
+
 def test_decode_flags_out_of_pool_pages(B):
     dev = torch.device("cuda")
     hq, hkv, d, ps = 8, 2, 128, 16
