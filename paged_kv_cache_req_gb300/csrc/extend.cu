@@ -536,39 +536,39 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                         if (pend > 2) settle_one();
                     }
                 } else {
-                int win = 0;
-                int cur = box_row(lane), nxt = box_row(32 + lane);
-                for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
-                    if (((ti * nbox) >> 5) != win) {
-                        ++win;
-                        cur = nxt;
-                        nxt = box_row(32 * (win + 1) + lane);
+                    int win = 0;
+                    int cur = box_row(lane), nxt = box_row(32 + lane);
+                    for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
+                        if (((ti * nbox) >> 5) != win) {
+                            ++win;
+                            cur = nxt;
+                            nxt = box_row(32 * (win + 1) + lane);
+                        }
+                        // pool row of this lane's box (a tile's boxes share one window: win or win + 1)
+                        const int bx0 = ti * nbox;
+                        int row = __shfl_sync(0xffffffffu, (bx0 >> 5) == win ? cur : nxt, (bx0 & 31) + j_box);
+                        if (lane >= nops) row = -1;
+                        if (row == -2 && lane % (2 * C::kSl) == 0) raise_flag(p.err, PKV_DEVERR_RANGE);
+                        const int s = n % kStages;
+                        if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
+                        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                        if (!ok) break;
+                        if (row == -2) {   // a page outside the pool reads as zeros
+                            unsigned char *dz = sKV + s * C::kStageBytes + (is_v ? C::kKBytes : 0) + sl_op * kTile * 128 +
+                                                j_box * box * 128;
+                            for (int o = 0; o < box * 128; o += 16) *reinterpret_cast<uint4 *>(dz + o) = make_uint4(0, 0, 0, 0);
+                            fence_proxy_async_smem();   // for the tensor cores and later TMA writes
+                        }
+                        const uint32_t valid = __ballot_sync(0xffffffffu, row >= 0);
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive_expect_tx(&bars[kKvFull0 + s], __popc(valid) * static_cast<uint32_t>(box) * 128u);
+                        __syncwarp();
+                        if (row >= 0)
+                            tma_load_3d(sKV + s * C::kStageBytes + (is_v ? C::kKBytes : 0) + sl_op * kTile * 128 +
+                                            j_box * box * 128,
+                                        is_v ? &tmv : &tmk, sl_op * 64, it.kh, row, &bars[kKvFull0 + s]);
                     }
-                    // pool row of this lane's box (a tile's boxes share one window: win or win + 1)
-                    const int bx0 = ti * nbox;
-                    int row = __shfl_sync(0xffffffffu, (bx0 >> 5) == win ? cur : nxt, (bx0 & 31) + j_box);
-                    if (lane >= nops) row = -1;
-                    if (row == -2 && lane % (2 * C::kSl) == 0) raise_flag(p.err, PKV_DEVERR_RANGE);
-                    const int s = n % kStages;
-                    if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
-                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                    if (!ok) break;
-                    if (row == -2) {   // a page outside the pool reads as zeros
-                        unsigned char *dz = sKV + s * C::kStageBytes + (is_v ? C::kKBytes : 0) + sl_op * kTile * 128 +
-                                            j_box * box * 128;
-                        for (int o = 0; o < box * 128; o += 16) *reinterpret_cast<uint4 *>(dz + o) = make_uint4(0, 0, 0, 0);
-                        fence_proxy_async_smem();   // for the tensor cores and later TMA writes
-                    }
-                    const uint32_t valid = __ballot_sync(0xffffffffu, row >= 0);
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive_expect_tx(&bars[kKvFull0 + s], __popc(valid) * static_cast<uint32_t>(box) * 128u);
-                    __syncwarp();
-                    if (row >= 0)
-                        tma_load_3d(sKV + s * C::kStageBytes + (is_v ? C::kKBytes : 0) + sl_op * kTile * 128 +
-                                        j_box * box * 128,
-                                    is_v ? &tmv : &tmk, sl_op * 64, it.kh, row, &bars[kKvFull0 + s]);
-                }
                 }
             }
             if (more) {
