@@ -1,24 +1,29 @@
 // pkv_decode for GQA / MHA: one query token per request attending through a page table.
 //
-// Work decomposition (split-KV): a work item is (request b, key chunk c, kv head
-// kh, head slice hs).  It covers keys [c*chunk, min(L, (c+1)*chunk)) of kv head kh
-// for up to 4 of the query heads that share kh, so every K/V tile is read from
-// HBM once for the whole GQA group.  Items are ordered request-major with the
-// kv heads of one chunk adjacent (they read the same pool pages) and are
-// handed out round-robin to a persistent grid of SM-count x occupancy CTAs;
-// each CTA derives the item list from the lengths in its prologue, so no host
-// synchronisation is needed.
+// Work decomposition (split-KV): a work item is (request b, key piece c, kv head
+// kh, head slice hs).  A request of L keys is cut into n = ceil(L / chunk) equal
+// pieces (multiples of 64 keys); the item covers piece c of kv head kh for the
+// query heads of the slice that share kh (up to 16: the whole GQA group), so every
+// K/V tile is read from HBM once per group.  Items are ordered request-major with
+// the kv heads of one piece adjacent (they read the same pool pages) and are
+// handed out round-robin to a persistent grid of SM-count x occupancy CTAs; each
+// CTA derives the item list from the device-side lengths in its prologue, so no
+// host synchronisation is needed.  The slot of key t is
+// page_table[b][t / ps] * ps + t % ps ("From slots to a page table").
 //
-// Inside an item, 64-key tiles of K and V stream through a 3-stage cp.async
-// pipeline (16-byte chunks; 16 lanes cover one 256-byte row, so a warp copies
-// two rows per instruction).  The slot of key t is
-// page_table[b][t / ps] * ps + t % ps ("From slots to a page table").  Each
-// warp takes 16 keys of a tile; 8 lanes share a key (each lane owns 16 of the
-// 128 dims), reduce q.k with three xor-shuffles, and keep their own online-
-// softmax state (base-2, scale * log2 e folded into q).  States are combined
-// across lane groups and warps at the end of the item.  A request with one
-// chunk writes bf16 output directly; longer ones write fp32 partials and their
-// log-sum-exp, combined by merge_kernel.
+// decode_tma_kernel (pages of >= 8 keys, and contiguous varlen rows): one producer
+// warp issues a TMA box per page and 64-dim slab (128-byte swizzle) into a ring of
+// 64-key stages (3 at head_dim 128, 5 at 64), completion counted in bytes on the
+// stage's mbarrier, running ahead across items.  decode_cp_async_kernel (pages of
+// 1-4 keys): every thread gathers 16-byte row chunks with cp.async into the same
+// layout.  Math (four warps, 16 keys of each tile per warp, each with its own
+// online softmax in base 2 whose running max is raised only past 2^8): for GQA
+// groups, S = q K^T and O += P V are m16n8k16 bf16 MMAs with the group's heads as
+// the MMA rows (K via ldmatrix, V via ldmatrix.trans); for one head per kv head,
+// CUDA cores with 8 lanes per key and xor-shuffle reductions.  The warps' states
+// are combined at the end of the item.  A request with one piece writes bf16
+// output directly; longer ones write fp32 partials and their log-sum-exp,
+// combined by merge_kernel.  Every wait is bounded (~2 s).
 #include <algorithm>
 #include <cmath>
 #include <mutex>

@@ -13,25 +13,23 @@
 //
 // The fp32 output accumulator of 128 heads x 512 dims fills all of an SM's
 // tensor memory, so a 2-CTA cluster shares each segment (request, 128-head
-// group, run of 64-key tiles):
-//   CTA 0 owns latent dims [0, 256): it computes the partial scores over them
-//          and accumulates output dims [0, 256);
-//   CTA 1 owns dims [256, 576): partial scores over them, output dims [256, 512).
-// The two partial score tiles (128 heads x 64 keys, fp32) are swapped through
-// distributed shared memory, so both CTAs hold identical full scores and run
+// group, run of 64-key tiles): CTA r owns value dims [256 r, 256 r + 256) and
+// rope dims [512 + 32 r, 512 + 32 r + 32).  It computes the partial scores over
+// those 288 dims and accumulates its 256 output dims.  The two partial score
+// tiles (128 heads x 64 keys) are swapped as fp16 through distributed shared
+// memory one tile ahead, so both CTAs hold bitwise-identical full scores and run
 // the same softmax; nothing is loaded or multiplied twice.
 //
-// Per CTA: warp 4 is the TMA producer (one 64-key tile per stage, one box per
-// page per 64-dim slab, 128-byte swizzle, 4 stages); warp 5 issues tcgen05 MMAs
-// from one thread; warps 0-3 own one head per TMEM lane.  Tensor memory holds
-// S (64 columns), O (256), this CTA's slice of q (<= 160, written by the
-// softmax warps at each item start) and P (32, bf16 pairs): S = Q K^T takes q
-// from TMEM and K from shared memory, O += P V takes P from TMEM and V as an
-// MN-major operand of the same slabs.  The softmax warps read S, swap partials
-// with the peer (st.async into a conflict-free transposed buffer, completion
-// counted in bytes on the receiver's mbarrier), run the online softmax (base 2,
-// running max raised only past 2^8 headroom so O rescales in TMEM are rare),
-// write P to TMEM and finally normalise O.
+// Per CTA: warps 0-15 softmax (four threads per head row, 16 keys each), warp 16
+// producer (TMA boxes per page and 64-dim slab into 4 stages of 36 KB, with tiles
+// three ahead prefetched into L2; for pages under 8 keys a second instance of the
+// kernel gathers rows with cp.async), warp 17 issues S = Q K^T, warp 18 O += P V.
+// Tensor memory holds two 64-column score buffers, O (256 columns), q over the
+// CTA's first 128 dims (64 columns, the A operand of eight of the 18 q.k MMAs)
+// and two 32-column P buffers (the A operand of P V); q over the other 160 dims
+// comes from shared memory.  The online softmax works in base 2 with the running
+// max raised only past 2^8 headroom, so O rescales in TMEM are rare; the softmax
+// warps also normalise O and write the output or the split partials.
 // Every wait is bounded (~2 s) and an abort flag lets the CTA drain instead of
 // hanging.
 #include <algorithm>

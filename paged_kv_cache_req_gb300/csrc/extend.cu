@@ -7,9 +7,10 @@
 // (request, kv head, block of 128 query rows, chunk of keys): the rows are the
 // (token, query head) pairs of 128 / g consecutive tokens times the g query
 // heads sharing the kv head, so every K/V tile serves the whole block.  Per CTA:
-//   warp 4     TMA producer: K/V tiles of 64 keys (one box per page per slab,
-//              one copy per lane) through a 4-stage ring (8 at head_dim 64),
-//              pool rows looked up 32 boxes at a time;
+//   warp 4     producer: K/V tiles of 64 keys through a 4-stage ring (8 at
+//              head_dim 64): one TMA box per page per slab, one copy per lane,
+//              pool rows looked up 32 boxes at a time; pages under 8 keys are
+//              gathered row by row with cp.async instead;
 //   warp 5     loads the q blocks (one 3-D box per 64-dim slab, rows
 //              token-major) into two buffers, the next item's while this one
 //              runs, and issues S = Q K^T (M = 128, N = 64) into one of two TMEM
