@@ -2,7 +2,7 @@
 // pkv_ragged_gather (pack token-granular K/V rows into contiguous varlen buffers)
 // and pkv_encoder_merge (gather encoder-cache blocks into positioned hidden rows).
 //
-// Both are pure indexed copies of whole rows.  One warp moves one row with
+// All three are pure indexed copies of whole rows.  One warp moves one row with
 // 16-byte vector accesses (the mini-sglang store kernel's "one warp per token,
 // 16 bytes per move"); every row start is checked to be 16-byte aligned on the
 // host, otherwise a 2-byte element path is used.
