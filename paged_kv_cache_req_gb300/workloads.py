@@ -131,12 +131,6 @@ class Workload:
     def num_pool_pages(self) -> int:
         return self.num_slots // self.page_size
 
-    @property
-    def pool_row_elems(self) -> int:
-        """Elements of one pool row (all kv heads of one token)."""
-        if self.kind == "mla":
-            return self.head_dim_qk
-        return self.num_kv_heads * self.head_dim_qk
 
     @property
     def has_v_pool(self) -> bool:
