@@ -131,7 +131,6 @@ class Workload:
     def num_pool_pages(self) -> int:
         return self.num_slots // self.page_size
 
-
     @property
     def has_v_pool(self) -> bool:
         return self.kind != "mla"
