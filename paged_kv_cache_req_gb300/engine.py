@@ -41,6 +41,28 @@ class _ProblemBuffers:
     pass
 
 
+def _pack(owners, device):
+    """Moves tensors into consecutive 256-byte aligned slices of one new device buffer.
+
+    ``owners`` lists (object, attribute) pairs; each attribute is replaced by a view of
+    the buffer holding the same values, so one copy of the buffer fills them all (the
+    per-step inputs come from the host in a single transfer, the outputs go back in one).
+    Returns the buffer.
+    """
+    sizes = [getattr(o, a).numel() * getattr(o, a).element_size() for o, a in owners]
+    offs, total = [], 0
+    for nb in sizes:
+        offs.append(total)
+        total += (nb + 255) // 256 * 256
+    buf = torch.empty(max(total, 256), dtype=torch.uint8, device=device)
+    for (o, a), off, nb in zip(owners, offs, sizes):
+        t = getattr(o, a)
+        v = buf[off:off + nb].view(t.dtype).view(t.shape)
+        v.copy_(t)
+        setattr(o, a, v)
+    return buf
+
+
 class DecodeStep:
     def __init__(self, wl: Workload, device="cuda", cross_mode: str = "paged", kv_chunk: int = 0,
                  pools=None, values: Optional[Dict[str, torch.Tensor]] = None, seed: Optional[int] = None,
@@ -74,8 +96,24 @@ class DecodeStep:
             pb.q = vals["q_" + p.name].to(dev)
             pb.out = torch.empty((Bn, wl.num_q_heads, wl.head_dim_v), dtype=torch.bfloat16, device=dev)
             pb.lse = torch.empty((Bn, wl.num_q_heads), dtype=torch.float32, device=dev)
-            max_pages = -(-pb.max_len // ps) if pb.max_len else 0
             pb.gather = (p.name == "cross" and cross_mode == "gather")
+            self.problems[p.name] = pb
+        self.alloc = bool(alloc)
+        if self.alloc:
+            self._setup_alloc(seed)
+        # the step's host inputs and its outputs each live in one buffer (one copy per direction)
+        ins = [(self, "k_new"), (self, "req_pool_idx")] + ([(self, "v_new")] if self.v_new is not None else [])
+        for name, pb in self.problems.items():
+            ins += [(pb, "q"), (pb, "seq_lens")]
+            if pb.slot_mapping is not None and not (self.alloc and name == self.alloc_problem):
+                ins.append((pb, "slot_mapping"))
+        if self.alloc:
+            ins += [(self, "prefix_lens"), (self, "last_loc")]
+        self.in_buf = _pack(ins, dev)
+        self.out_buf = _pack([(pb, "out") for pb in self.problems.values()], dev)
+        for pb in self.problems.values():
+            p = pb.spec
+            max_pages = -(-pb.max_len // ps) if pb.max_len else 0
             if pb.gather:
                 rows = int(p.seq_lens.sum())
                 pb.k_rag = torch.empty((max(rows, 1),) + tuple(self.k_pool.shape[1:]), dtype=torch.bfloat16, device=dev)
@@ -102,10 +140,6 @@ class DecodeStep:
             nbytes = B.pkv_decode_workspace_size(pb.args)
             pb.ws_bytes = nbytes
             pb.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
-            self.problems[p.name] = pb
-        self.alloc = bool(alloc)
-        if self.alloc:
-            self._setup_alloc(seed)
 
     def _setup_alloc(self, seed):
         """Free list = the pool pages no cached position uses (page 0 is padding), in a
@@ -208,40 +242,15 @@ class DecodeStep:
 
     # ------------------------------------------------------------------ host I/O
     def host_step_tensors(self):
-        """Pinned host copies of the per-step inputs and outputs (for end-to-end timing)."""
-        h_in = {"k_new": self.k_new.cpu().pin_memory()}
-        if self.v_new is not None:
-            h_in["v_new"] = self.v_new.cpu().pin_memory()
-        h_out = {}
-        for name, pb in self.problems.items():
-            h_in["q_" + name] = pb.q.cpu().pin_memory()
-            h_in["seq_lens_" + name] = pb.seq_lens.cpu().pin_memory()
-            if self.alloc and name == self.alloc_problem:
-                h_in["prefix_lens"] = self.prefix_lens.cpu().pin_memory()
-                h_in["last_loc"] = self.last_loc.cpu().pin_memory()
-            elif pb.slot_mapping is not None:
-                h_in["slot_mapping_" + name] = pb.slot_mapping.cpu().pin_memory()
-            h_out[name] = torch.empty_like(pb.out, device="cpu").pin_memory()
-        h_in["req_pool_idx"] = self.req_pool_idx.cpu().pin_memory()
-        return h_in, h_out
+        """Pinned host copies of the step's packed inputs and outputs (for end-to-end timing)."""
+        return {"inputs": self.in_buf.cpu().pin_memory()}, {"outputs": torch.empty_like(self.out_buf, device="cpu").pin_memory()}
 
     def run_from_host(self, h_in, h_out):
-        """Copies this step's inputs from pinned host memory, runs the step, copies outputs back."""
-        self.k_new.copy_(h_in["k_new"], non_blocking=True)
-        if self.v_new is not None:
-            self.v_new.copy_(h_in["v_new"], non_blocking=True)
-        self.req_pool_idx.copy_(h_in["req_pool_idx"], non_blocking=True)
-        for name, pb in self.problems.items():
-            pb.q.copy_(h_in["q_" + name], non_blocking=True)
-            pb.seq_lens.copy_(h_in["seq_lens_" + name], non_blocking=True)
-            if self.alloc and name == self.alloc_problem:
-                self.prefix_lens.copy_(h_in["prefix_lens"], non_blocking=True)
-                self.last_loc.copy_(h_in["last_loc"], non_blocking=True)
-            elif pb.slot_mapping is not None:
-                pb.slot_mapping.copy_(h_in["slot_mapping_" + name], non_blocking=True)
+        """One host-to-device copy of the step's inputs (new K/V rows, q, lengths, slots, row
+        indices: packed in one buffer), the step, one device-to-host copy of the outputs."""
+        self.in_buf.copy_(h_in["inputs"], non_blocking=True)
         self.run()
-        for name, pb in self.problems.items():
-            h_out[name].copy_(pb.out, non_blocking=True)
+        h_out["outputs"].copy_(self.out_buf, non_blocking=True)
 
     @staticmethod
     def bytes_of(tensors) -> int:
@@ -304,6 +313,17 @@ class ExtendStep:
         self.out = torch.empty((total_q, ew.num_q_heads, ew.head_dim), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((total_q, ew.num_q_heads), dtype=torch.float32, device=dev)
         self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        # the step's host inputs in one buffer (one copy per step)
+        ins = [(self, "q"), (self, "k_new"), (self, "v_new"), (self, "seq_lens"), (self, "slot_mapping"),
+               (self, "qo_indptr"), (self, "req_pool_idx")]
+        if self.kv_end is not None:
+            self._seg_holder = _ProblemBuffers()
+            for i, t in enumerate(self.seg):
+                setattr(self._seg_holder, "s%d" % i, t)
+            ins += [(self._seg_holder, "s%d" % i) for i in range(len(self.seg))]
+        self.in_buf = _pack(ins, dev)
+        if self.kv_end is not None:
+            self.seg = [getattr(self._seg_holder, "s%d" % i) for i in range(len(self.seg))]
         self.args = B.make_extend_args(B.PKV_LAYOUT_CSR, self.q, self.k_pool, self.v_pool, self.out, self.qo_indptr,
                                        page_size=ps, sm_scale=ew.sm_scale, max_seq_len=int(ew.seq_lens.max()),
                                        kv_end=self.kv_end, kv_indptr=self.kv_indptr, kv_indices=self.kv_indices,
@@ -339,20 +359,12 @@ class ExtendStep:
         return int(self.err.item())
 
     def host_step_tensors(self):
-        h_in = {"q": self.q.cpu().pin_memory(), "k_new": self.k_new.cpu().pin_memory(),
-                "v_new": self.v_new.cpu().pin_memory(), "seq_lens": self.seq_lens.cpu().pin_memory(),
-                "slot_mapping": self.slot_mapping.cpu().pin_memory(), "qo_indptr": self.qo_indptr.cpu().pin_memory()}
-        if self.kv_end is not None:
-            for i, t in enumerate(self.seg):
-                h_in["seg%d" % i] = t.cpu().pin_memory()
-        return h_in, {"out": torch.empty_like(self.out, device="cpu").pin_memory()}
+        """Pinned host copies of the step's packed inputs and of its output (for end-to-end timing)."""
+        return {"inputs": self.in_buf.cpu().pin_memory()}, {"out": torch.empty_like(self.out, device="cpu").pin_memory()}
 
     def run_from_host(self, h_in, h_out):
-        for name, t in (("q", self.q), ("k_new", self.k_new), ("v_new", self.v_new), ("seq_lens", self.seq_lens),
-                        ("slot_mapping", self.slot_mapping), ("qo_indptr", self.qo_indptr)):
-            t.copy_(h_in[name], non_blocking=True)
-        if self.kv_end is not None:
-            for i, t in enumerate(self.seg):
-                t.copy_(h_in["seg%d" % i], non_blocking=True)
+        """One host-to-device copy of the step's inputs (q, new K/V rows, lengths, slots, query
+        offsets, segments: packed in one buffer), the step, one copy of the output back."""
+        self.in_buf.copy_(h_in["inputs"], non_blocking=True)
         self.run()
         h_out["out"].copy_(self.out, non_blocking=True)
