@@ -1,7 +1,9 @@
 // Status plumbing and device queries shared by the libpkv entry points.
 #include <cstdarg>
 #include <cstdio>
+#include <map>
 #include <mutex>
+#include <tuple>
 #include <vector>
 
 #include "pkv_internal.cuh"
@@ -64,6 +66,15 @@ bool encode_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+std::atomic<int64_t> *device_memo(const void *key, int tag) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, const void *, int>, std::atomic<int64_t>> memo;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    return &memo[std::make_tuple(dev, key, tag)];   // map nodes never move
 }
 
 int sm_count() {

@@ -972,6 +972,20 @@ static pkv_status smem_limit(K kernel, size_t &lim) {
     return PKV_OK;
 }
 
+// smem_limit once per device (kernel attributes are per device); the limit is cached.
+template <typename K>
+static pkv_status device_smem_limit(K kernel, size_t &lim) {
+    std::atomic<int64_t> *m = device_memo(reinterpret_cast<const void *>(kernel));
+    if (!m) return fail(PKV_ERR_CUDA, "pkv_decode: cannot query the current device");
+    if (m->load() == 0) {
+        pkv_status st = smem_limit(kernel, lim);
+        if (st != PKV_OK) return st;
+        m->store(static_cast<int64_t>(lim));
+    }
+    lim = static_cast<size_t>(m->load());
+    return PKV_OK;
+}
+
 template <typename K>
 static int persistent_grid(K kernel, int threads, size_t smem, const Params &p) {
     int occ = 0;
@@ -1000,8 +1014,8 @@ static pkv_status launch_t(const Params &p, const pkv_decode_args *a, bool tma, 
     pkv_status st;
     if (tma) {
         const auto kernel = decode_tma_kernel<D, GC, MMA>;
-        static size_t lim = 0;
-        if (!lim && (st = smem_limit(kernel, lim)) != PKV_OK) return st;
+        size_t lim = 0;
+        if ((st = device_smem_limit(kernel, lim)) != PKV_OK) return st;
         const size_t smem = 1024 + TmaCfg<D>::kStagesN * T::kStageBytes + RedLayout<D, GC>::kBytes +
                             2 * TmaCfg<D>::kStagesN * 8 + 32 + (static_cast<size_t>(p.batch) + 1) * 4;
         if (smem > lim) return fail(PKV_ERR_UNSUPPORTED, "pkv_decode: batch too large for the on-chip item table");
@@ -1018,8 +1032,8 @@ static pkv_status launch_t(const Params &p, const pkv_decode_args *a, bool tma, 
                            "pkv_decode(GQA split kernel)");
     } else {
         const auto kernel = decode_cp_async_kernel<D, GC, MMA>;
-        static size_t lim = 0;
-        if (!lim && (st = smem_limit(kernel, lim)) != PKV_OK) return st;
+        size_t lim = 0;
+        if ((st = device_smem_limit(kernel, lim)) != PKV_OK) return st;
         const size_t smem = kStages * T::kStageBytes + RedLayout<D, GC>::kBytes + (static_cast<size_t>(p.batch) + 1) * 4;
         if (smem > lim) return fail(PKV_ERR_UNSUPPORTED, "pkv_decode: batch too large for the on-chip item table");
         const int grid = persistent_grid(kernel, kThreads, smem, p);

@@ -1036,9 +1036,10 @@ size_t workspace_size(const pkv_decode_args *a) {
 // instantiation of the decode kernel.
 template <bool G>
 static pkv_status kernel_limits(size_t &lim_out, int &pairs_out) {
-    static size_t lim = 0;
-    static int max_pairs = 0;
-    if (!lim) {
+    std::atomic<int64_t> *m_lim = device_memo(reinterpret_cast<const void *>(mla_decode_kernel<G>), 0);
+    std::atomic<int64_t> *m_pairs = device_memo(reinterpret_cast<const void *>(mla_decode_kernel<G>), 1);
+    if (!m_lim || !m_pairs) return fail(PKV_ERR_CUDA, "pkv_decode(MLA): cannot query the current device");
+    if (m_lim->load() == 0 || m_pairs->load() == 0) {
         int optin = 0, dev = 0;
         cudaFuncAttributes fa{};
         if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -1056,11 +1057,11 @@ static pkv_status kernel_limits(size_t &lim_out, int &pairs_out) {
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel<G>, &cfg) != cudaSuccess || n < 1)
             n = std::max(1, sm_count() / 2);
-        max_pairs = n;
-        lim = l;
+        m_pairs->store(n);
+        m_lim->store(static_cast<int64_t>(l));
     }
-    lim_out = lim;
-    pairs_out = max_pairs;
+    lim_out = static_cast<size_t>(m_lim->load());
+    pairs_out = static_cast<int>(m_pairs->load());
     return PKV_OK;
 }
 

@@ -1153,8 +1153,9 @@ static pkv_status launch_t(const pkv_extend_args *a, const Plan &pl, void *ws, i
         if (!encode_tmap_bf16(&tmk, a->k_pool, 3, dk, sk, bk) || !encode_tmap_bf16(&tmv, a->v_pool, 3, dk, sv, bk))
             return fail(PKV_ERR_CUDA, "pkv_extend: cuTensorMapEncodeTiled rejected the pools");
     }
-    static size_t lim = 0;
-    if (!lim) {
+    std::atomic<int64_t> *m_lim = device_memo(reinterpret_cast<const void *>(ext_kernel<D>));
+    if (!m_lim) return fail(PKV_ERR_CUDA, "pkv_extend: cannot query the current device");
+    if (m_lim->load() == 0) {   // kernel attributes are per device
         int optin = 0, dev = 0;
         cudaFuncAttributes fa{};
         if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -1165,8 +1166,9 @@ static pkv_status launch_t(const pkv_extend_args *a, const Plan &pl, void *ws, i
         if (cudaFuncSetAttribute(ext_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(l)) !=
             cudaSuccess)
             return fail(PKV_ERR_CUDA, "pkv_extend: cannot raise the shared-memory limit");
-        lim = l;
+        m_lim->store(static_cast<int64_t>(l));
     }
+    const size_t lim = static_cast<size_t>(m_lim->load());
     // item table (B + 1 ints), plus four ints per request when they fit as well
     size_t smem = C::kFixedSmem + (static_cast<size_t>(a->batch) + 1) * 4;
     if (smem > lim) return fail(PKV_ERR_UNSUPPORTED, "pkv_extend: batch too large for the on-chip item table");

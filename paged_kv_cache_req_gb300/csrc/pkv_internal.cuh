@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "pkv.h"
@@ -20,6 +21,10 @@ pkv_status ok();
 pkv_status check_launch(const char *what);
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
+// A value remembered per (current device, key, tag): kernel attributes such as the
+// raised shared-memory limit are per device, so they are set and cached per device.
+// Starts at 0; nullptr if the current device cannot be queried.  Thread-safe.
+std::atomic<int64_t> *device_memo(const void *key, int tag = 0);
 
 // Launches `kernel` on stream `s` as a programmatic dependent of the kernel before it
 // in the stream: it may be scheduled while that kernel drains.  Every kernel of this
