@@ -281,12 +281,66 @@ def weak_scaling_gbs(world, bytes_per_step, steps, max_ms):
     return world * bytes_per_step * steps / (max_ms / 1e3) / 1e9
 
 
-# ---------------------------------------------------------------- arms
-def dist_env():
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return world, rank, local
+# ---------------------------------------------------------------- configs (shared by both arms)
+def parallelism(world):
+    return "replicas" if world > 1 else "single GPU"
+
+
+def l2_note(nbytes):
+    return "flushed between steps (2x L2 write)" if nbytes < 4 * L2_BYTES else "inputs larger than L2"
+
+
+def decode_config(wl, cross_mode, alloc, world):
+    """The `config` object of a decode line: the same dict in both arms."""
+    keys = unique_keys(wl)
+    total_bytes, _ = step_bytes(wl, cross_mode, alloc=alloc)
+    return {"workload": WORKLOAD_TEXT[wl.name], "name": wl.name, "batch": wl.batch,
+            "cross_mode": cross_mode if wl.kind == "gqa" and len(wl.problems) > 1 else None,
+            "new_slots": "allocated on the device each step (pkv_alloc_extend + pkv_write_req_to_token)"
+            if alloc else "given by the workload",
+            "keys_per_step": {k: v[0] for k, v in keys.items()},
+            "unique_keys_per_step": {k: v[1] for k, v in keys.items()},
+            "algorithmic_bytes_per_step": total_bytes,
+            "l2": l2_note(total_bytes), "parallelism": parallelism(world)}
+
+
+def extend_config(ew, world):
+    flops, step_bytes_, _ = extend_amounts(ew)
+    return {"workload": WORKLOAD_TEXT[ew.name], "name": ew.name, "batch": ew.batch,
+            "query_rows": int(ew.qo_lens.sum()), "keys": int(ew.seq_lens.sum()),
+            "attention_flops_per_step": flops, "algorithmic_bytes_per_step": step_bytes_,
+            "l2": l2_note(step_bytes_), "parallelism": parallelism(world)}
+
+
+def merge_config(mw, world):
+    nbytes = merge_bytes(mw)
+    return {"workload": WORKLOAD_TEXT["encoder_merge"], "name": "encoder_merge", "items": mw.items,
+            "rows_moved": mw.rows_moved, "row_bytes": mw.row_bytes, "num_blocks": mw.num_blocks,
+            "num_tokens": mw.num_tokens, "algorithmic_bytes_per_step": nbytes,
+            "l2": l2_note(nbytes), "parallelism": parallelism(world)}
+
+
+def finish_clocks(clocks, opts, soak_step):
+    """Stops the sampler; a region shorter than a few samples is extended, untimed, by the same load."""
+    soak = 0
+    if clocks.proc is not None and not opts.profile_run and clocks.count() - clocks.start_count < 5:
+        t_soak = time.perf_counter()
+        while clocks.count() - clocks.start_count < 5 and time.perf_counter() - t_soak < 3.0:
+            for _ in range(max(1, opts.steps)):
+                soak_step()
+                soak += 1
+            torch.cuda.synchronize()
+    clk = clocks.stop()
+    if clk is not None:
+        clk["window"] = "timed region" + (" + %d untimed steps of the same load" % soak if soak else "")
+    return clk
+
+
+def with_cycles(clk, ms_per_step):
+    """Adds the step's length in SM cycles at the sampled median clock (time x MHz)."""
+    if clk is not None and clk.get("sm_mhz"):
+        clk["sm_cycles_per_step"] = int(round(ms_per_step * 1e3 * clk["sm_mhz"]))
+    return clk
 
 
 # ---------------------------------------------------------------- encoder-cache merge
@@ -319,22 +373,20 @@ def reference_merge(args, world):
     value = merge_bytes(mw) * len(times) / sum(times) / 1e9
     desc = "whole step: %d rows of %d B gathered by the byte-copy oracle on 1 host thread" % (
         mw.rows_moved, mw.row_bytes)
-    line = {"impl": "reference", "metric": MERGE_METRIC, "value": round(value, 4), "unit": "GB/s",
+    return {"impl": "reference", "metric": MERGE_METRIC, "value": round(value, 4), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * sum(times) / len(times), 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-            "config": {"workload": WORKLOAD_TEXT["encoder_merge"], "name": "encoder_merge"},
+            "config": merge_config(mw, world),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
-    return 0
 
 
-def run_merge(args, world, rank, local, dist):
+def measure_merge(opts, world, rank, local, dist):
     """One step = one pkv_encoder_merge of the whole prefill's cached images."""
     from paged_kv_cache_req_gb300 import _binding as B
     from paged_kv_cache_req_gb300.workloads import fill_merge_buffers, make_encoder_merge
-    mw = make_encoder_merge(seed=args.seed)
+    mw = make_encoder_merge(seed=opts.seed)
     dev = torch.device("cuda", local)
     buf, hidden = fill_merge_buffers(mw, device=dev)
     bid = torch.from_numpy(mw.block_ids).to(dev)
@@ -349,18 +401,18 @@ def run_merge(args, world, rank, local, dist):
     def step():
         B.pkv_encoder_merge(buf, bid, pos, hidden, err, filled=filled)
 
-    for _ in range(args.warmup):
+    for _ in range(opts.warmup):
         step()
     torch.cuda.synchronize()
-    if err.item() or filled.item() != args.warmup * mw.rows_moved:
+    if err.item() or filled.item() != opts.warmup * mw.rows_moved:
         raise SystemExit("merge check failed: err %d, filled %d" % (err.item(), filled.item()))
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(opts.steps)]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks = ClockSampler(local, enabled=not args.profile_run)
+    clocks = ClockSampler(local, enabled=not opts.profile_run)
     wall0 = time.perf_counter()
-    for i in range(args.steps):
+    for i in range(opts.steps):
         if flush:
             flush_buf.zero_()
         ev[i][0].record(stream)
@@ -368,28 +420,18 @@ def run_merge(args, world, rank, local, dist):
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
-    soak = 0
-    if clocks.proc is not None and not args.profile_run and clocks.count() - clocks.start_count < 5:
-        t_soak = time.perf_counter()
-        while clocks.count() - clocks.start_count < 5 and time.perf_counter() - t_soak < 3.0:
-            for _ in range(max(1, args.steps)):
-                step()
-                soak += 1
-            torch.cuda.synchronize()
-    clk = clocks.stop()
-    if clk is not None:
-        clk["window"] = "timed region" + (" + %d untimed steps of the same load" % soak if soak else "")
+    clk = finish_clocks(clocks, opts, step)
     tot_ms = reduce_max(sum(a.elapsed_time(b) for a, b in ev), dist, "cuda")
-    value = weak_scaling_gbs(world, nbytes, args.steps, tot_ms)
-    if args.profile_run:
+    value = weak_scaling_gbs(world, nbytes, opts.steps, tot_ms)
+    if opts.profile_run:
         if rank == 0:
-            print(json.dumps({"profile_run": True, "workload": "encoder_merge", "ms_per_step": round(tot_ms / args.steps, 4)}))
-        return 0
+            print(json.dumps({"profile_run": True, "workload": "encoder_merge", "ms_per_step": round(tot_ms / opts.steps, 4)}))
+        return None
     # end to end: the step's index inputs from pinned host memory, the filled count back
     h_bid, h_pos = torch.from_numpy(mw.block_ids).pin_memory(), torch.from_numpy(mw.positions).pin_memory()
     h_filled = torch.zeros(1, dtype=torch.int64).pin_memory()
-    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for i in range(args.steps):
+    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(opts.steps)]
+    for i in range(opts.steps):
         if flush:
             flush_buf.zero_()
         e_ev[i][0].record(stream)
@@ -404,12 +446,12 @@ def run_merge(args, world, rank, local, dist):
         raise SystemExit("merge check failed in the end-to-end pass")
     e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in e_ev), dist, "cuda")
     if rank != 0:
-        return 0
+        return None
     hbm, _, _, peak_kind = measured_peaks()
-    avg_ms = tot_ms / args.steps
+    avg_ms = tot_ms / opts.steps
     achieved = nbytes / (avg_ms / 1e3) / 1e9
     cpu = None
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not opts.no_cpu_baseline:
         import oracle
         oracle.build()
         bb = buf.cpu().view(torch.int16).numpy().view(np.uint16)
@@ -421,29 +463,23 @@ def run_merge(args, world, rank, local, dist):
         cpu = {"value": round(nbytes * passes / tot_s / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": "whole step (%d rows of %d B); %d pass(es), %.1f s on 1 host thread" % (
                    mw.rows_moved, mw.row_bytes, passes, tot_s), "host_cpus": os.cpu_count()}
-    line = {
-        "metric": MERGE_METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(avg_ms, 4), "higher_is_better": True, "scaling": "weak",
+    return {
+        "metric": MERGE_METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": opts.steps,
+        "warmup": opts.warmup, "ms_per_step": round(avg_ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT["encoder_merge"], "name": "encoder_merge", "items": mw.items,
-                   "rows_moved": mw.rows_moved, "row_bytes": mw.row_bytes, "num_blocks": mw.num_blocks,
-                   "num_tokens": mw.num_tokens, "algorithmic_bytes_per_step": nbytes,
-                   "l2": "flushed between steps (2x L2 write)" if flush else "inputs larger than L2",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "config": merge_config(mw, world),
         "roofline": {"bound": "hbm", "kernel": "pkv_encoder_merge", "achieved": round(achieved, 2), "peak": hbm,
                      "unit": "GB/s", "frac": round(achieved / hbm, 4), "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": nbytes, "avg_launch_ms": round(avg_ms, 4),
                      "traffic": decode_traffic("encoder_merge")},
         "cpu_baseline": cpu,
-        "e2e": {"value": round(weak_scaling_gbs(world, nbytes, args.steps, e_ms), 2), "unit": "GB/s",
+        "e2e": {"value": round(weak_scaling_gbs(world, nbytes, opts.steps, e_ms), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(mw.block_ids.nbytes + mw.positions.nbytes), "d2h_bytes_per_step": 8,
-                "ms_per_step": round(e_ms / args.steps, 4)},
-        "gpu_launches": args.steps,
-        "clocks": clk,
+                "ms_per_step": round(e_ms / opts.steps, 4)},
+        "gpu_launches": opts.steps,
+        "clocks": with_cycles(clk, avg_ms),
         "wall_s_timed_region": round(wall, 3),
     }
-    print(json.dumps(line), flush=True)
-    return 0
 
 
 # ---------------------------------------------------------------- multi-query steps
@@ -543,44 +579,42 @@ def reference_extend(args, world):
         flops += f_
         nbytes += b_
     value = (flops / secs / 1e12) if unit == "TFLOP/s" else (nbytes / secs / 1e9)
-    line = {"impl": "reference", "metric": metric, "value": round(value, 6), "unit": unit, "n_gpus": world,
+    return {"impl": "reference", "metric": metric, "value": round(value, 6), "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "batch": ew.batch},
+            "config": extend_config(ew, world),
             "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": threads, "kind": "oracle",
                              "sample": "each step: " + desc},
             "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
-    return 0
 
 
-def run_extend(args, world, rank, local, dist):
-    from paged_kv_cache_req_gb300.engine import ExtendStep
+def measure_extend(opts, world, rank, local, dist):
+    from paged_kv_cache_req_gb300.engine import DecodeStep, ExtendStep
     from paged_kv_cache_req_gb300.workloads import make_extend_workload
     import oracle
     oracle.build()
-    ew = make_extend_workload(args.workload, seed=args.seed, batch=args.batch)
-    metric, unit, bound = EXTEND_METRIC[args.workload]
-    step = ExtendStep(ew, device="cuda", kv_chunk=args.kv_chunk, seed=args.seed)
+    ew = make_extend_workload(opts.workload, seed=opts.seed, batch=opts.batch)
+    metric, unit, bound = EXTEND_METRIC[opts.workload]
+    step = ExtendStep(ew, device="cuda", kv_chunk=opts.kv_chunk, seed=opts.seed)
     flops, step_bytes_, launch_bytes = extend_amounts(ew)
     amount = flops / 1e12 if unit == "TFLOP/s" else step_bytes_ / 1e9
     launch_amount = flops / 1e12 if unit == "TFLOP/s" else launch_bytes / 1e9
     flush = step_bytes_ < 4 * L2_BYTES
     flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda") if flush else None
     stream = torch.cuda.current_stream()
-    for _ in range(args.warmup):
+    for _ in range(opts.warmup):
         step.run()
     torch.cuda.synchronize()
     if step.check_errors():
         raise SystemExit("device error flags raised: %d" % step.check_errors())
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(opts.steps)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(opts.steps)]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks = ClockSampler(local, enabled=not args.profile_run)
+    clocks = ClockSampler(local, enabled=not opts.profile_run)
     wall0 = time.perf_counter()
-    for i in range(args.steps):
+    for i in range(opts.steps):
         if flush:
             flush_buf.zero_()
         ev[i][0].record(stream)
@@ -593,35 +627,24 @@ def run_extend(args, world, rank, local, dist):
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
-    soak = 0
-    if clocks.proc is not None and not args.profile_run and clocks.count() - clocks.start_count < 5:
-        t_soak = time.perf_counter()
-        while clocks.count() - clocks.start_count < 5 and time.perf_counter() - t_soak < 3.0:
-            for _ in range(max(1, args.steps)):
-                step.run()
-                soak += 1
-            torch.cuda.synchronize()
-    clk = clocks.stop()
-    if clk is not None:
-        clk["window"] = "timed region" + (" + %d untimed steps of the same load" % soak if soak else "")
+    clk = finish_clocks(clocks, opts, step.run)
     if step.check_errors():
         raise SystemExit("device error flags raised: %d" % step.check_errors())
     tot_ms = reduce_max(sum(a.elapsed_time(b) for a, b in ev), dist, "cuda")
-    k_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
-    value = world * amount * args.steps / (tot_ms / 1e3)
-    if args.profile_run:
+    k_ms = sum(a.elapsed_time(b) for a, b in kev) / opts.steps
+    value = world * amount * opts.steps / (tot_ms / 1e3)
+    if opts.profile_run:
         if rank == 0:
-            print(json.dumps({"profile_run": True, "workload": args.workload, "ms_per_step": round(tot_ms / args.steps, 4),
+            print(json.dumps({"profile_run": True, "workload": opts.workload, "ms_per_step": round(tot_ms / opts.steps, 4),
                               "extend_ms": round(k_ms, 4)}))
-        return 0
+        return None
     h_in, h_out = step.host_step_tensors()
-    from paged_kv_cache_req_gb300.engine import DecodeStep
     h2d, d2h = DecodeStep.bytes_of(h_in), DecodeStep.bytes_of(h_out)
     for _ in range(2):
         step.run_from_host(h_in, h_out)
     torch.cuda.synchronize()
-    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for i in range(args.steps):
+    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(opts.steps)]
+    for i in range(opts.steps):
         if flush:
             flush_buf.zero_()
         e_ev[i][0].record(stream)
@@ -630,12 +653,12 @@ def run_extend(args, world, rank, local, dist):
     torch.cuda.synchronize()
     e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in e_ev), dist, "cuda")
     if rank != 0:
-        return 0
+        return None
     hbm, bf16, bf16_sus, peak_kind = measured_peaks()
     peak = hbm if bound == "hbm" else bf16
     achieved = launch_amount / (k_ms / 1e3)
     cpu = None
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not opts.no_cpu_baseline:
         def fetch(slots):
             idx = torch.from_numpy(slots).cuda()
             return (step.k_pool[idx].cpu().view(torch.int16).numpy().view(np.uint16),
@@ -643,7 +666,7 @@ def run_extend(args, world, rank, local, dist):
         tot_s = tot_f = tot_b = 0.0
         passes, desc, threads = 0, "", 0
         while passes < 10 and (tot_s < 3.0 or passes == 0):
-            s_, f_, b_, desc, threads = extend_oracle_sample(ew, args.cpu_key_heads // 4, fetch_kv=fetch, seed=passes)
+            s_, f_, b_, desc, threads = extend_oracle_sample(ew, opts.cpu_key_heads // 4, fetch_kv=fetch, seed=passes)
             tot_s += s_
             tot_f += f_
             tot_b += b_
@@ -652,109 +675,70 @@ def run_extend(args, world, rank, local, dist):
         cpu = {"value": round(cv, 6), "unit": unit, "cores": threads, "kind": "oracle",
                "sample": desc + "; %d pass(es), %.1f s of fp64 attention on %d host threads" % (passes, tot_s, threads),
                "host_cpus": os.cpu_count()}
-    line = {
-        "metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(tot_ms / args.steps, 4), "higher_is_better": True,
+    roof = {"bound": bound, "kernel": "pkv_extend (attention kernel + merge)", "achieved": round(achieved, 3),
+            "peak": peak, "unit": unit, "frac": round(achieved / peak, 4),
+            "peak_kind": peak_kind + (" (bf16 dense, burst)" if bound == "tensor" else ""),
+            "avg_launch_ms": round(k_ms, 4), "traffic": decode_traffic(opts.workload)}
+    if bound == "tensor":
+        roof["frac_of_sustained"] = round(achieved / bf16_sus, 4)
+    return {
+        "metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": opts.steps,
+        "warmup": opts.warmup, "ms_per_step": round(tot_ms / opts.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "accumulate": "fp32", "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "batch": ew.batch,
-                   "query_rows": int(ew.qo_lens.sum()), "keys": int(ew.seq_lens.sum()),
-                   "attention_flops_per_step": flops, "algorithmic_bytes_per_step": step_bytes_,
-                   "l2": "flushed between steps (2x L2 write)" if flush else "inputs larger than L2",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"bound": bound, "kernel": "pkv_extend (attention kernel + merge)", "achieved": round(achieved, 3),
-                     "peak": peak, "unit": unit, "frac": round(achieved / peak, 4),
-                     "peak_kind": peak_kind + (" (bf16 dense, burst)" if bound == "tensor" else ""),
-                     "avg_launch_ms": round(k_ms, 4), "traffic": decode_traffic(args.workload)},
+        "config": extend_config(ew, world),
+        "roofline": roof,
         "cpu_baseline": cpu,
-        "e2e": {"value": round(world * amount * args.steps / (e_ms / 1e3), 3), "unit": unit,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms / args.steps, 4)},
-        "gpu_launches": step.launches_per_step() * args.steps,
-        "clocks": clk,
+        "e2e": {"value": round(world * amount * opts.steps / (e_ms / 1e3), 3), "unit": unit,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms / opts.steps, 4)},
+        "gpu_launches": step.launches_per_step() * opts.steps,
+        "clocks": with_cycles(clk, tot_ms / opts.steps),
         "wall_s_timed_region": round(wall, 3),
     }
-    print(json.dumps(line), flush=True)
-    return 0
 
 
-def run_reference(args):
-    world, rank, _ = dist_env()
-    if rank != 0:
-        return 0
-    if args.workload == "encoder_merge":
-        return reference_merge(args, world)
-    if args.workload in EXTEND_WORKLOADS:
-        return reference_extend(args, world)
-    from paged_kv_cache_req_gb300.workloads import make_workload
-    wl = make_workload(args.workload, batch=args.batch)
-    import oracle
-    oracle.build()
-    budget = args.ref_key_heads
-    for _ in range(args.warmup):
-        oracle_sample_run(wl, budget // 4, seed=0)
-    times, total_bytes, desc, threads = [], 0, "", 0
-    for i in range(args.steps):
-        secs, nb, desc, threads = oracle_sample_run(wl, budget, seed=i)
-        times.append(secs)
-        total_bytes += nb
-    value = total_bytes / sum(times) / 1e9
-    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(1e3 * sum(times) / len(times), 3), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "batch": wl.batch},
-            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-                             "sample": "each step: " + desc},
-            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
-    return 0
+# ---------------------------------------------------------------- decode steps
+def decode_cpu_baseline(wl, budget, fetch, threads=0):
+    """The oracle (store + decode) on bounded samples of the workload, repeated for at least 3 s."""
+    tot_s, tot_b, passes = 0.0, 0, 0
+    desc, used = "", 0
+    while passes < 10 and (tot_s < 3.0 or passes == 0):
+        secs, nb, desc, used = oracle_sample_run(wl, budget, seed=passes, fetch_rows=fetch, num_threads=threads)
+        tot_s += secs
+        tot_b += nb
+        passes += 1
+    return {"value": round(tot_b / tot_s / 1e9, 4), "unit": "GB/s", "cores": used, "kind": "oracle",
+            "sample": desc + "; %d pass(es), %.1f s of fp64 store+decode on %d host thread(s)" % (passes, tot_s, used),
+            "host_cpus": os.cpu_count()}
 
 
-def run_ours(args):
-    world, rank, local = dist_env()
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
-    torch.cuda.set_device(local)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    from paged_kv_cache_req_gb300 import build
-    if rank == 0 or world == 1:
-        build.build()
-    if dist is not None:
-        dist.barrier()
+def measure_decode(opts, world, rank, local, dist, one_thread_baseline=False):
     from paged_kv_cache_req_gb300.engine import DecodeStep
     from paged_kv_cache_req_gb300.workloads import make_workload
-
-    if args.workload == "encoder_merge":
-        return run_merge(args, world, rank, local, dist)
-    if args.workload in EXTEND_WORKLOADS:
-        return run_extend(args, world, rank, local, dist)
-    wl = make_workload(args.workload, seed=args.seed, batch=args.batch)
-    step = DecodeStep(wl, device="cuda", cross_mode=args.cross_mode, kv_chunk=args.kv_chunk, seed=args.seed,
-                      alloc=args.alloc)
-    total_bytes, decode_bytes = step_bytes(wl, args.cross_mode, alloc=args.alloc)
+    wl = make_workload(opts.workload, seed=opts.seed, batch=opts.batch)
+    step = DecodeStep(wl, device="cuda", cross_mode=opts.cross_mode, kv_chunk=opts.kv_chunk, seed=opts.seed,
+                      alloc=opts.alloc)
+    total_bytes, decode_bytes = step_bytes(wl, opts.cross_mode, alloc=opts.alloc)
     flush = total_bytes < 4 * L2_BYTES
     flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda") if flush else None
     stream = torch.cuda.current_stream()
 
-    for _ in range(args.warmup):
+    for _ in range(opts.warmup):
         step.run()
     torch.cuda.synchronize()
     if step.check_errors():
         raise SystemExit("device error flags raised: %d" % step.check_errors())
 
     # ---- device-timed steps (inputs resident) ----
-    n_dec = len([p for p in step.problems.values()])
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    n_dec = len(step.problems)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(opts.steps)]
     dev_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_dec)]
-              for _ in range(args.steps)]
+              for _ in range(opts.steps)]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks = ClockSampler(local, enabled=not args.profile_run)
+    clocks = ClockSampler(local, enabled=not opts.profile_run)
     wall0 = time.perf_counter()
-    for i in range(args.steps):
+    for i in range(opts.steps):
         if flush:
             flush_buf.zero_()
         ev[i][0].record(stream)
@@ -773,37 +757,23 @@ def run_ours(args):
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
-    soak_steps = 0
-    if clocks.proc is not None and not args.profile_run and clocks.count() - clocks.start_count < 5:
-        # The timed region was shorter than a few sampling intervals: keep the same
-        # load running, untimed, until the sampler has seen it.
-        t_soak = time.perf_counter()
-        while clocks.count() - clocks.start_count < 5 and time.perf_counter() - t_soak < 3.0:
-            for _ in range(max(1, args.steps)):
-                step.run()
-                soak_steps += 1
-            torch.cuda.synchronize()
-    clk = clocks.stop()
-    if clk is not None:
-        clk["window"] = "timed region" + (" + %d untimed steps of the same load" % soak_steps if soak_steps else "")
+    clk = finish_clocks(clocks, opts, step.run)
     if dist is not None:
         dist.barrier()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     dec_ms = [sum(a.elapsed_time(b) for a, b in row) for row in dev_ev]
     tot_ms = reduce_max(sum(step_ms), dist, "cuda")
-    ms_per_step = tot_ms / args.steps
-    value = weak_scaling_gbs(world, total_bytes, args.steps, tot_ms)
+    ms_per_step = tot_ms / opts.steps
+    value = weak_scaling_gbs(world, total_bytes, opts.steps, tot_ms)
     if step.check_errors():
         raise SystemExit("device error flags raised: %d" % step.check_errors())
 
-    if args.profile_run:
+    if opts.profile_run:
         if rank == 0:
-            print(json.dumps({"profile_run": True, "workload": args.workload, "batch": wl.batch,
-                              "ms_per_step": round(tot_ms / args.steps, 4),
+            print(json.dumps({"profile_run": True, "workload": opts.workload, "batch": wl.batch,
+                              "ms_per_step": round(tot_ms / opts.steps, 4),
                               "decode_ms": round(sum(dec_ms) / len(dec_ms), 4)}), flush=True)
-        if dist is not None:
-            dist.destroy_process_group()
-        return 0
+        return None
 
     # ---- end to end through the host-buffer API ----
     h_in, h_out = step.host_step_tensors()
@@ -812,8 +782,8 @@ def run_ours(args):
     for _ in range(2):
         step.run_from_host(h_in, h_out)
     torch.cuda.synchronize()
-    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for i in range(args.steps):
+    e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(opts.steps)]
+    for i in range(opts.steps):
         if flush:
             flush_buf.zero_()
         e_ev[i][0].record(stream)
@@ -821,67 +791,169 @@ def run_ours(args):
         e_ev[i][1].record(stream)
     torch.cuda.synchronize()
     e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in e_ev), dist, "cuda")
-    e2e_value = weak_scaling_gbs(world, total_bytes, args.steps, e_ms)
-
+    e2e_value = weak_scaling_gbs(world, total_bytes, opts.steps, e_ms)
     if rank != 0:
-        if dist is not None:
-            dist.destroy_process_group()
-        return 0
+        return None
 
-    hbm, _, _, peak_kind = measured_peaks()
+    hbm, bf16, bf16_sus, peak_kind = measured_peaks()
     dec_avg_ms = sum(dec_ms) / len(dec_ms)
     achieved = decode_bytes / (dec_avg_ms / 1e3) / 1e9
-    traffic = decode_traffic(args.workload)
-    launches = step.launches_per_step() * args.steps
+    roof = {"bound": "hbm", "kernel": "pkv_decode (split kernel + merge)",
+            "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved / hbm, 4), "peak_kind": peak_kind,
+            "frac_of_8TBs": round(achieved / 8000.0, 4),
+            "algorithmic_bytes_per_launch": decode_bytes, "avg_launch_ms": round(dec_avg_ms, 4),
+            "traffic": decode_traffic(opts.workload)}
+    if wl.kind == "mla":
+        # near the ridge: the tensor pipe's share too (q.k over 576 dims + P.V over 512 per key and head)
+        keys = sum(int(p.seq_lens.sum()) for p in wl.problems)
+        flops = 2.0 * keys * wl.num_q_heads * (wl.head_dim_qk + wl.head_dim_v)
+        tfs = flops / (dec_avg_ms / 1e3) / 1e12
+        roof["tensor"] = {"achieved": round(tfs, 2), "unit": "TFLOP/s", "flops_per_launch": flops,
+                          "peak": bf16, "frac": round(tfs / bf16, 4), "peak_sustained": bf16_sus,
+                          "frac_of_sustained": round(tfs / bf16_sus, 4)}
 
-    cpu = None
-    if world == 1 and not args.no_cpu_baseline:
+    cpu = cpu1 = None
+    if world == 1 and not opts.no_cpu_baseline:
         import oracle
         oracle.build()
+
         def fetch(slots):
             idx = torch.from_numpy(slots).cuda()
             kb = step.k_pool[idx].cpu().view(torch.int16).numpy().view(np.uint16)
             vb = None if step.v_pool is None else step.v_pool[idx].cpu().view(torch.int16).numpy().view(np.uint16)
             return kb, vb
-        tot_s, tot_b, passes = 0.0, 0, 0
-        while passes < 10 and (tot_s < 3.0 or passes == 0):
-            secs, nb, desc, threads = oracle_sample_run(wl, args.cpu_key_heads, seed=passes, fetch_rows=fetch)
-            tot_s += secs
-            tot_b += nb
-            passes += 1
-        cpu = {"value": round(tot_b / tot_s / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": desc + "; %d pass(es), %.1f s of fp64 store+decode on %d host threads" % (passes, tot_s, threads),
-               "host_cpus": os.cpu_count()}
+        cpu = decode_cpu_baseline(wl, opts.cpu_key_heads, fetch)
+        if one_thread_baseline:
+            cpu1 = decode_cpu_baseline(wl, max(1, opts.cpu_key_heads // 16), fetch, threads=1)
 
-    keys = unique_keys(wl)
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": opts.steps,
+        "warmup": opts.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "accumulate": "fp32", "data": "synthetic",
         "decode_steps_per_s": round(world * 1e3 / ms_per_step, 2),
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "batch": wl.batch,
-                   "cross_mode": args.cross_mode if wl.kind == "gqa" and len(wl.problems) > 1 else None,
-                   "new_slots": "allocated on the device each step (pkv_alloc_extend + pkv_write_req_to_token)"
-                   if args.alloc else "given by the workload",
-                   "keys_per_step": {k: v[0] for k, v in keys.items()},
-                   "unique_keys_per_step": {k: v[1] for k, v in keys.items()},
-                   "algorithmic_bytes_per_step": total_bytes,
-                   "l2": "flushed between steps (2x L2 write)" if flush else "inputs larger than L2",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "kernel": "pkv_decode (split kernel + merge)",
-                     "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "peak_kind": peak_kind,
-                     "frac_of_8TBs": round(achieved / 8000.0, 4),
-                     "algorithmic_bytes_per_launch": decode_bytes, "avg_launch_ms": round(dec_avg_ms, 4),
-                     "traffic": traffic},
+        "config": decode_config(wl, opts.cross_mode, opts.alloc, world),
+        "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e_ms / args.steps, 4)},
-        "gpu_launches": launches,
-        "clocks": clk,
+                "ms_per_step": round(e_ms / opts.steps, 4)},
+        "gpu_launches": step.launches_per_step() * opts.steps,
+        "clocks": with_cycles(clk, ms_per_step),
         "wall_s_timed_region": round(wall, 3),
     }
+    if cpu1 is not None:
+        line["cpu_baseline_1thread"] = cpu1
+    return line
+
+
+# ---------------------------------------------------------------- arms
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measure(opts, world, rank, local, dist, one_thread_baseline=False):
+    if opts.workload == "encoder_merge":
+        return measure_merge(opts, world, rank, local, dist)
+    if opts.workload in EXTEND_WORKLOADS:
+        return measure_extend(opts, world, rank, local, dist)
+    return measure_decode(opts, world, rank, local, dist, one_thread_baseline=one_thread_baseline)
+
+
+# Every other recipe, measured after the headline on the same GPU (N = 1): workload,
+# cross-attention mode, timed steps.  Each entry carries its own clocks, roofline,
+# traffic and CPU baseline; the configurations the oracle runs in seconds also carry
+# a 1-thread oracle time.
+PER_CONFIG = (
+    ("tiny_gqa", "paged", 200),
+    ("qwen3_0p6b", "paged", 200),
+    ("whisper_encdec", "paged", 200),
+    ("whisper_encdec", "gather", 200),
+    ("deepseek_v3_mla", "paged", 100),
+    ("llama3_8b_verify", "paged", 100),
+    ("qwen3_0p6b_prefill", "paged", 100),
+    ("hunyuan_image_spans", "paged", 50),
+    ("encoder_merge", "paged", 200),
+)
+ONE_THREAD_BASELINE = ("tiny_gqa", "qwen3_0p6b")
+
+
+def per_config_entries(args, world, rank, local, dist):
+    out = {}
+    for name, cross, steps in PER_CONFIG:
+        if name == args.workload and cross == args.cross_mode:
+            continue
+        opts = argparse.Namespace(**vars(args))
+        opts.workload, opts.cross_mode, opts.steps = name, cross, steps
+        opts.alloc, opts.kv_chunk, opts.batch = False, 0, None
+        opts.cpu_key_heads = args.cpu_key_heads // 3
+        line = measure(opts, world, rank, local, dist, one_thread_baseline=name in ONE_THREAD_BASELINE)
+        torch.cuda.empty_cache()
+        if line is None:
+            continue
+        for k in ("n_gpus", "higher_is_better", "scaling", "vs_baseline", "data", "warmup"):
+            line.pop(k, None)
+        key = name if name != "whisper_encdec" else "whisper_encdec_" + cross
+        out[key] = line
+    return out
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    if args.workload == "encoder_merge":
+        line = reference_merge(args, world)
+    elif args.workload in EXTEND_WORKLOADS:
+        line = reference_extend(args, world)
+    else:
+        from paged_kv_cache_req_gb300.workloads import make_workload
+        wl = make_workload(args.workload, seed=args.seed, batch=args.batch)
+        import oracle
+        oracle.build()
+        budget = args.ref_key_heads
+        for _ in range(args.warmup):
+            oracle_sample_run(wl, budget // 4, seed=0)
+        times, total_bytes, desc, threads = [], 0, "", 0
+        for i in range(args.steps):
+            secs, nb, desc, threads = oracle_sample_run(wl, budget, seed=i)
+            times.append(secs)
+            total_bytes += nb
+        value = total_bytes / sum(times) / 1e9
+        line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(1e3 * sum(times) / len(times), 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": decode_config(wl, args.cross_mode, args.alloc, world),
+                "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                 "sample": "each step: " + desc},
+                "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from paged_kv_cache_req_gb300 import build
+    if rank == 0 or world == 1:
+        build.build()
+    if dist is not None:
+        dist.barrier()
+    line = measure(args, world, rank, local, dist)
+    if line is not None and world == 1 and not args.profile_run and not args.no_per_config \
+            and args.batch is None and args.workload == DEFAULT_WORKLOAD and not args.alloc:
+        line["per_config"] = per_config_entries(args, world, rank, local, dist)
+    if line is not None:
+        print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
     return 0
@@ -890,7 +962,7 @@ def run_ours(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOAD_TEXT))
@@ -898,6 +970,8 @@ def main(argv=None):
     ap.add_argument("--kv-chunk", type=int, default=0)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="headline workload only (no per_config entries for the other recipes)")
     ap.add_argument("--alloc", action="store_true",
                     help="allocate each step's new slots on the device (pkv_alloc_extend + pkv_write_req_to_token)")
     ap.add_argument("--profile-run", action="store_true",

@@ -77,3 +77,22 @@ def test_reference_arm_runs_on_rank0_only(rank):
         assert d["n_gpus"] == 2
     else:
         assert lines == []
+
+
+@pytest.mark.parametrize("workload", ["tiny_gqa", "qwen3_0p6b_prefill", "encoder_merge"])
+def test_reference_arm_prints_the_config_of_the_gpu_arm(workload):
+    """Both arms describe one workload with the same `config` object (built on the host)."""
+    import bench
+    from paged_kv_cache_req_gb300.workloads import make_encoder_merge, make_extend_workload, make_workload
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                          workload, "--steps", "1", "--warmup", "3", "--ref-key-heads", "2000000"],
+                         capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    d = json.loads([l for l in out.stdout.splitlines() if l.strip()][-1])
+    if workload == "encoder_merge":
+        want = bench.merge_config(make_encoder_merge(seed=0), 1)
+    elif workload in bench.EXTEND_WORKLOADS:
+        want = bench.extend_config(make_extend_workload(workload, seed=0), 1)
+    else:
+        want = bench.decode_config(make_workload(workload, seed=0), "paged", False, 1)
+    assert d["config"] == json.loads(json.dumps(want))
