@@ -63,7 +63,8 @@ typedef enum pkv_status {
 #define PKV_DEVERR_RANGE 1    /* slot, page, row or position outside its pool or table */
 #define PKV_DEVERR_CONTIG 2   /* a page's tokens are not page-aligned and contiguous */
 #define PKV_DEVERR_CAPACITY 4 /* an output had too little room; the excess was not written */
-#define PKV_DEVERR_TIMEOUT 8  /* a device-side wait gave up after ~2 s; outputs of the launch unspecified */
+#define PKV_DEVERR_TIMEOUT 8  /* a device-side wait ran past its limit (pkv_set_wait_limit, ~2 s by
+                                 default); outputs of the launch unspecified */
 
 #define PKV_ABI_VERSION 1
 
@@ -83,6 +84,8 @@ typedef enum pkv_status {
  *   kv_indices[kv_indptr[b]+p]  = req_to_token[r, s + p*ps] / ps          (p < n)
  *   kv_last_page_len[b]         = L - (n-1)*ps, or 0 when L = 0
  *   block_table[b, p]           = the same page for p < n, -1 for n <= p < block_table_width
+ * Each CTA streams the page counts of all requests once to find its offsets,
+ * so the work is linear in the batch.
  * Every position is checked: each page's first slot must be a multiple of ps,
  * the following ones must continue it (PKV_DEVERR_CONTIG otherwise) and every
  * page must lie in [0, num_pool_pages) (PKV_DEVERR_RANGE).  A row or region
@@ -226,7 +229,10 @@ size_t pkv_decode_workspace_size(const pkv_decode_args *args);
  *   kv_chunk or a smaller batch brings it under the limit.
  * - The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture.
+ *   before any stream capture.  The address is cached for the life of the
+ *   process: after cudaDeviceReset (or any teardown of the device's primary
+ *   context) the array may move, so do not call this entry point again on
+ *   that device until the library has been unloaded and loaded again.
  * - All calls share the one array and it keeps the last call's contents.  No
  *   part of it needs to start at zero (every partial is written before it is
  *   read), but calls whose kernels overlap on the GPU (other streams, other
@@ -245,9 +251,14 @@ pkv_status pkv_decode_no_alloc(const pkv_decode_args *args, int32_t *err_flags, 
  *   k_out[cu_seqlens[b] + t] = k_pool[req_to_token[req_pool_idx[b], s_b + t]]   (t < seq_lens[b])
  * and the same for v.  Rows are row_elems bf16 elements (Hkv * head_dim),
  * pool rows pool_row_stride elements apart, output rows packed.  Rows beyond
- * out_rows_cap raise PKV_DEVERR_CAPACITY and are not written.  max_seq_len is
- * a host upper bound on seq_lens (grid sizing only; longer requests are still
- * copied whole).  v_pool / v_out may both be NULL (latent pool).
+ * out_rows_cap raise PKV_DEVERR_CAPACITY and are not written.  A request whose
+ * row or region lies outside the table, and a slot outside [0, num_slots),
+ * raise PKV_DEVERR_RANGE; the output rows reserved for them are zero-filled
+ * (so a following VARLEN pkv_decode reads zeros there, as it does for a bad
+ * page).  max_seq_len is a host upper bound on seq_lens (grid sizing only;
+ * longer requests are still copied whole).  v_pool / v_out may both be NULL
+ * (latent pool).  Each CTA scans the lengths of all requests once, so the
+ * work is linear in the batch.
  */
 pkv_status pkv_ragged_gather(const void *k_pool, const void *v_pool, int64_t num_slots,
                              int64_t pool_row_stride, int64_t row_elems, const int32_t *req_to_token,
@@ -420,6 +431,28 @@ const char *pkv_last_error(void);
 
 /* PKV_ABI_VERSION of the loaded library. */
 int32_t pkv_abi_version(void);
+
+/*
+ * pkv_set_wait_limit -- bound of every wait inside the library's kernels.
+ *
+ * Failure detection without a hang, after the fail-loud checks of the AWS
+ * Neuron encoder-cache doc ("Read Path"): the kernels that pipeline through
+ * mbarriers (the TMA decode, MLA decode and pkv_extend kernels) wait on them
+ * for at most this many nanoseconds.  A wait that runs out raises
+ * PKV_DEVERR_TIMEOUT in err_flags and makes its CTA give up: every CTA that
+ * sees the flag stops waiting, lets the copies and MMAs it already issued
+ * complete, frees its tensor memory and returns, so the launch ends and the
+ * context stays usable; the launch's outputs are unspecified.  The limit
+ * applies to launches issued after the call, from any host thread.
+ * nanoseconds = 0 restores the default (about 2 s, far above any legitimate
+ * wait); a limit of a few nanoseconds makes the first wait that is not already
+ * satisfied give up, which is how the give-up path is exercised in tests.
+ * Always returns PKV_OK.
+ */
+pkv_status pkv_set_wait_limit(uint64_t nanoseconds);
+
+/* The current wait limit in nanoseconds. */
+uint64_t pkv_wait_limit(void);
 
 #ifdef __cplusplus
 }

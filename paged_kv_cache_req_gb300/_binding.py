@@ -17,14 +17,15 @@ import torch
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpkv.so")
 
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CAPACITY, PKV_ERR_CUDA = range(5)
-PKV_DEVERR_RANGE, PKV_DEVERR_CONTIG, PKV_DEVERR_CAPACITY = 1, 2, 4
+PKV_DEVERR_RANGE, PKV_DEVERR_CONTIG, PKV_DEVERR_CAPACITY, PKV_DEVERR_TIMEOUT = 1, 2, 4, 8
 PKV_KIND_GQA, PKV_KIND_MLA = 0, 1
 PKV_LAYOUT_CSR, PKV_LAYOUT_BLOCK_TABLE, PKV_LAYOUT_VARLEN = 0, 1, 2
 
 EXPORTED_SYMBOLS = ("pkv_build_indices", "pkv_store", "pkv_decode", "pkv_decode_workspace_size",
                     "pkv_decode_no_alloc", "pkv_ragged_gather", "pkv_alloc_extend", "pkv_write_req_to_token",
                     "pkv_encoder_merge", "pkv_extend", "pkv_extend_workspace_size", "pkv_span_plan",
-                    "pkv_status_string", "pkv_last_error", "pkv_abi_version")
+                    "pkv_status_string", "pkv_last_error", "pkv_abi_version", "pkv_set_wait_limit",
+                    "pkv_wait_limit")
 
 
 class PkvError(RuntimeError):
@@ -102,6 +103,10 @@ def load_library(path: str = _LIB_PATH) -> ctypes.CDLL:
     lib.pkv_last_error.restype = ctypes.c_char_p
     lib.pkv_abi_version.argtypes = []
     lib.pkv_abi_version.restype = ctypes.c_int32
+    lib.pkv_set_wait_limit.argtypes = [ctypes.c_uint64]
+    lib.pkv_set_wait_limit.restype = ctypes.c_int
+    lib.pkv_wait_limit.argtypes = []
+    lib.pkv_wait_limit.restype = ctypes.c_uint64
     return lib
 
 
@@ -316,3 +321,12 @@ def pkv_status_string(status: int) -> str:
 
 def pkv_abi_version() -> int:
     return int(_lib.pkv_abi_version())
+
+
+def pkv_set_wait_limit(nanoseconds: int = 0):
+    """Bound of every in-kernel wait for launches issued from now on (0: the default, about 2 s)."""
+    _check(_lib.pkv_set_wait_limit(int(nanoseconds)), "pkv_set_wait_limit")
+
+
+def pkv_wait_limit() -> int:
+    return int(_lib.pkv_wait_limit())

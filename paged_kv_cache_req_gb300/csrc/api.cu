@@ -77,6 +77,13 @@ std::atomic<int64_t> *device_memo(const void *key, int tag) {
     return &memo[std::make_tuple(dev, key, tag)];   // map nodes never move
 }
 
+namespace {
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitNs};
+}  // namespace
+
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
 int sm_count() {
     static std::mutex mu;
     static std::vector<int> cache;
@@ -108,3 +115,10 @@ extern "C" const char *pkv_status_string(pkv_status status) {
 extern "C" const char *pkv_last_error(void) { return pkv::g_last_error; }
 
 extern "C" int32_t pkv_abi_version(void) { return PKV_ABI_VERSION; }
+
+extern "C" pkv_status pkv_set_wait_limit(uint64_t nanoseconds) {
+    pkv::g_wait_limit_ns.store(nanoseconds ? nanoseconds : pkv::kDefaultWaitNs, std::memory_order_relaxed);
+    return pkv::ok();
+}
+
+extern "C" uint64_t pkv_wait_limit(void) { return pkv::wait_limit_ns(); }

@@ -57,6 +57,7 @@ struct Params {
     float *lse;
     float *part_o, *part_lse;
     int32_t *err;
+    uint64_t wait_ns;   // bound of every mbarrier wait (pkv_set_wait_limit)
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -636,22 +637,34 @@ __global__ void __launch_bounds__(kThreads, 2) decode_cp_async_kernel(const Para
 // (and rows of pages that do not exist) may hold stale data: K is masked by
 // the scores' select, V rows are zeroed by the warp that reads them.
 // Bounded mbarrier wait shared by the producer and the math warps: gives up
-// when another warp already gave up (abort flag) or after ~2 s, raising
-// PKV_DEVERR_TIMEOUT once; afterwards no warp of the CTA waits again.
-__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int32_t *err) {
+// when another warp already gave up (abort flag) or once `limit_ns` have passed
+// (checked after the second poll and every 64 polls), raising
+// PKV_DEVERR_TIMEOUT; afterwards no warp of the CTA waits again.
+__device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int32_t *err,
+                                              uint64_t limit_ns) {
     if (*abort_flag) return false;
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63) == 0) {
+        if ((i & 63) == 1) {
             if (*abort_flag) return false;
-            if (global_ns() - t0 > 2000000000ull) {
+            if (global_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
                 raise_flag(err, PKV_DEVERR_TIMEOUT);
                 return false;
             }
         }
+    }
+}
+
+// Bounded wait that ignores the abort flag: lets the TMA copies a warp issued land
+// before its CTA exits (~2 s at most, whatever the wait limit).
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait(bar, parity)) return;
+        if ((i & 63) == 63 && global_ns() - t0 > 2000000000ull) return;
     }
 }
 
@@ -731,7 +744,8 @@ decode_tma_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const
             return static_cast<int>((static_cast<int64_t>(page) << p.ps_shift) + (tb & p.ps_mask));
         };
         int row = lookup();
-        for (uint32_t n = 0; have; ++n) {
+        uint32_t n = 0;
+        for (; have; ++n) {
             const int kh = it.kh;
             // advance the cursor and start the next tile's lookups
             const int n_tiles = (it.t_end - it.t_begin + kTile - 1) / kTile;
@@ -743,9 +757,9 @@ decode_tma_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const
             const int next_row = lookup();
             const int s = n % S;
             bool ok = true;
-            if (lane == 0) ok = wait_or_abort(&empty[s], ((n / S) & 1) ^ 1, abort_flag, p.err);
+            if (lane == 0) ok = wait_or_abort(&empty[s], ((n / S) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            if (!ok) return;
+            if (!ok) break;
             if (row == -2) {   // a page outside the pool reads as zeros (and raises the flag)
                 raise_flag(p.err, PKV_DEVERR_RANGE);
                 unsigned char *kst = smem + s * T::kStageBytes;
@@ -772,6 +786,11 @@ decode_tma_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const
             }
             row = next_row;
         }
+        // drain: the copies of the last (at most S) tiles issued land before the CTA
+        // may exit; consumers that gave up no longer wait for them
+        if (lane == 0)
+            for (uint32_t k = n > static_cast<uint32_t>(S) ? n - S : 0; k < n; ++k) drain_wait(&full[k % S], (k / S) & 1);
+        __syncwarp();
         return;
     }
 
@@ -788,7 +807,7 @@ decode_tma_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const
         const int n_tiles = (it.t_end - it.t_begin + kTile - 1) / kTile;
         for (int ti = 0; ti < n_tiles; ++ti, ++n) {
             const int s = n % S;
-            if (!wait_or_abort(&full[s], (n / S) & 1, abort_flag, p.err)) {
+            if (!wait_or_abort(&full[s], (n / S) & 1, abort_flag, p.err, p.wait_ns)) {
                 // abandoned launch: keep releasing stages and reaching barriers, compute nothing
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
@@ -1000,9 +1019,17 @@ static pkv_status launch_merge(const Params &p, cudaStream_t s) {
     const size_t msmem = static_cast<size_t>(GC) * p.n_chunks_max * 4;
     if (msmem > 200 * 1024) return fail(PKV_ERR_UNSUPPORTED, "pkv_decode: too many splits for the merge");
     if (msmem > 48 * 1024) {
-        if (cudaFuncSetAttribute(merge_kernel<D, GC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(msmem)) != cudaSuccess)
-            return fail(PKV_ERR_CUDA, "pkv_decode: cannot raise the merge shared-memory limit");
+        // the raised limit is per device: remember the largest one set on this device
+        std::atomic<int64_t> *m = device_memo(reinterpret_cast<const void *>(merge_kernel<D, GC>));
+        if (!m) return fail(PKV_ERR_CUDA, "pkv_decode: cannot query the current device");
+        if (m->load() < static_cast<int64_t>(msmem)) {
+            if (cudaFuncSetAttribute(merge_kernel<D, GC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(msmem)) != cudaSuccess)
+                return fail(PKV_ERR_CUDA, "pkv_decode: cannot raise the merge shared-memory limit");
+            int64_t cur = m->load();
+            while (cur < static_cast<int64_t>(msmem) && !m->compare_exchange_weak(cur, static_cast<int64_t>(msmem))) {
+            }
+        }
     }
     return launch_status(launch_chained(merge_kernel<D, GC>, dim3(p.batch * p.hkv * p.hsplit), dim3(kThreads), msmem, s, p),
                          "pkv_decode(GQA merge kernel)");
@@ -1098,6 +1125,7 @@ pkv_status launch(const pkv_decode_args *a, void *ws, size_t ws_bytes, int32_t *
     p.part_o = static_cast<float *>(ws);
     p.part_lse = reinterpret_cast<float *>(static_cast<char *>(ws) + pl.part_o_bytes);
     p.err = err;
+    p.wait_ns = wait_limit_ns();
     // Whole pages of >= 8 keys (or contiguous rows) stream in as TMA boxes; smaller
     // pages are gathered row by row with cp.async.
     const bool tma = (a->layout == PKV_LAYOUT_VARLEN || a->page_size >= 8) && a->num_slots <= INT32_MAX;

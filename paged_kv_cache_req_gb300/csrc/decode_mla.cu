@@ -93,6 +93,7 @@ struct Params {
     float *part_o, *part_lse;  // [span][2 slots][128 heads] x (512 | 1), base-2 lse
     int32_t *meta;             // [0]: tiles per span, [1 + v]: first tile of row v (rows + 1 entries)
     int32_t *err;
+    uint64_t wait_ns;          // bound of every mbarrier wait (pkv_set_wait_limit)
     const uint16_t *pool;      // latent rows (read directly when pages are under 8 keys)
     int64_t pool_stride;       // elements between latent rows
 };
@@ -237,18 +238,20 @@ __device__ __forceinline__ bool next_seg(const Params &p, const int *R, int V, i
     return false;
 }
 
-// Bounded wait (local or cluster-scope acquire) with the CTA-wide abort flag.
+// Bounded wait (local or cluster-scope acquire) with the CTA-wide abort flag: gives
+// up once another warp gave up or `limit_ns` have passed (checked after the second
+// poll and every 64 polls).
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int32_t *err,
-                                         bool cluster_scope = false) {
+                                         uint64_t limit_ns, bool cluster_scope = false) {
     auto poll = [&]() { return cluster_scope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
     if (poll()) return true;
     if (*abort_flag) return false;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
         if (poll()) return true;
-        if ((i & 63) == 0) {
+        if ((i & 63) == 1) {
             if (*abort_flag) return false;
-            if (global_ns() - t0 > 2000000000ull) {
+            if (global_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
                 raise_flag(err, PKV_DEVERR_TIMEOUT);
                 return false;
@@ -260,8 +263,8 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
 // Warp-wide bounded wait (every lane polls; measured faster than one polling lane
 // with the others parked).  `ok` is warp-uniform; so is the result.
 __device__ __forceinline__ bool warp_wait(bool ok, uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          int32_t *err, bool cluster_scope = false) {
-    return __all_sync(0xffffffffu, ok && wait_bar(bar, parity, abort_flag, err, cluster_scope));
+                                          int32_t *err, uint64_t limit_ns, bool cluster_scope = false) {
+    return __all_sync(0xffffffffu, ok && wait_bar(bar, parity, abort_flag, err, limit_ns, cluster_scope));
 }
 
 // Bounded wait that ignores the abort flag: used only to drain work this CTA
@@ -420,7 +423,7 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
                     const int r0 = key_row(lane), r1 = key_row(lane + 32);
                     if (r0 == -2 || r1 == -2) raise_flag(p.err, PKV_DEVERR_RANGE);
                     const int s = n % kStages;
-                    if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
+                    if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
                     ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                     if (!ok) break;
                     unsigned char *st = sKV + s * kStageBytes;
@@ -456,7 +459,7 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
                 if (ti + kPrefetch < it.n_tiles) prefetch(ti + kPrefetch);
                 const int row = box_row(ti, true);
                 const int s = n % kStages;
-                if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
+                if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) break;
                 if (row == -2) {   // a page outside the pool reads as zeros (the flag is raised by box_row)
@@ -501,11 +504,11 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
         Cursor cur{pair, pair * per};
         Seg it{};
         while (ok && next_seg(p, R, V, per, S, npairs, cur, it)) {
-            ok = warp_wait(ok, &bars[kQFull], ic & 1, abort_flag, p.err);
+            ok = warp_wait(ok, &bars[kQFull], ic & 1, abort_flag, p.err, p.wait_ns);
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
                 const int s = n % kStages;
-                ok = warp_wait(ok, &bars[kKvFull0 + s], (n / kStages) & 1, abort_flag, p.err);
-                ok = warp_wait(ok, &bars[kSFree0 + (n & 1)], ((n >> 1) & 1) ^ 1, abort_flag, p.err);
+                ok = warp_wait(ok, &bars[kKvFull0 + s], (n / kStages) & 1, abort_flag, p.err, p.wait_ns);
+                ok = warp_wait(ok, &bars[kSFree0 + (n & 1)], ((n >> 1) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
                 if (!ok) break;
                 tc05::fence_after_sync();
                 if (lane == 0) {
@@ -554,7 +557,7 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
         Seg it{};
         while (ok && next_seg(p, R, V, per, S, npairs, cur, it)) {
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
-                ok = warp_wait(ok, &bars[kPFull0 + (n & 1)], (n >> 1) & 1, abort_flag, p.err);
+                ok = warp_wait(ok, &bars[kPFull0 + (n & 1)], (n >> 1) & 1, abort_flag, p.err, p.wait_ns);
                 if (!ok) break;
                 unsigned char *st = sKV + (n % kStages) * kStageBytes;
                 const int n_valid = it.key_end - (it.key_begin + ti * kTile);
@@ -568,7 +571,7 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
-                if (ti == 0) ok = warp_wait(ok, &bars[kOFree], (ic & 1) ^ 1, abort_flag, p.err);
+                if (ti == 0) ok = warp_wait(ok, &bars[kOFree], (ic & 1) ^ 1, abort_flag, p.err, p.wait_ns);
                 if (!ok) break;
                 tc05::fence_after_sync();
                 if (lane == 0) {
@@ -625,7 +628,7 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
             const uint4 *qt4 = reinterpret_cast<const uint4 *>(qb + slab0 * 64 + qt * 32);
             const uint4 *qs4 = reinterpret_cast<const uint4 *>(qb + slab0 * 64 + 128 + qt * 32);
             const uint4 *qr4 = reinterpret_cast<const uint4 *>(qb + rope0 + qt * 8);
-            ok = warp_wait(ok, &bars[kQEmpty], (jc & 1) ^ 1, abort_flag, p.err);
+            ok = warp_wait(ok, &bars[kQEmpty], (jc & 1) ^ 1, abort_flag, p.err, p.wait_ns);
             tc05::fence_after_sync();
             uint4 qv[9];
 #pragma unroll
@@ -675,7 +678,7 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
 #define PKV_MLA_FETCH_ISSUE(t)                                                                                   \
     do {                                                                                                       \
         if (tid == 0) mbar_arrive_expect_tx(&bars[kXFull0 + (t) % kXSlots], kXBytes);                          \
-        ok = warp_wait(ok, &bars[kSFull0 + ((t) & 1)], ((t) >> 1) & 1, abort_flag, p.err);                     \
+        ok = warp_wait(ok, &bars[kSFull0 + ((t) & 1)], ((t) >> 1) & 1, abort_flag, p.err, p.wait_ns);                     \
         if (ok) {                                                                                              \
             tc05::fence_after_sync();                                                                          \
             tc05::ld_x16(trow + kColS + ((t) & 1) * kTile + qt * 16, a_);                                      \
@@ -718,7 +721,7 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
                 if (ahead) PKV_MLA_FETCH_ISSUE(n + 1);
                 // ---- the peer's partial of tile n (this thread's 16 keys) ----
                 const int xs = n % kXSlots;
-                ok = warp_wait(ok, &bars[kXFull0 + xs], (n / kXSlots) & 1, abort_flag, p.err);
+                ok = warp_wait(ok, &bars[kXFull0 + xs], (n / kXSlots) & 1, abort_flag, p.err, p.wait_ns);
                 const int n_valid = it.key_end - (it.key_begin + ti * kTile);
                 // own + peer partial in half2 (the same bits in both CTAs)
                 __half2 x2[8];
@@ -769,7 +772,7 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
                 if (__any_sync(0xffffffffu, raise && m != -INFINITY) && ok) {
                     // O is final for tile n - 1 (m finite: it belongs to this segment)
                     // once its P V completed; then rescale this thread's 64 value columns
-                    ok = warp_wait(ok, &bars[kPFree0 + ((n - 1) & 1)], ((n - 1) >> 1) & 1, abort_flag, p.err);
+                    ok = warp_wait(ok, &bars[kPFree0 + ((n - 1) & 1)], ((n - 1) >> 1) & 1, abort_flag, p.err, p.wait_ns);
                     tc05::fence_after_sync();
 #pragma unroll 1
                     for (int cc = 0; cc < 4 && ok; ++cc) {
@@ -800,7 +803,7 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
                 l += lsum;
                 // this thread's 16 keys of P (8 bf16 pairs) into buffer n & 1, free once
                 // the P V of tile n - 2 completed
-                ok = warp_wait(ok, &bars[kPFree0 + (n & 1)], ((n >> 1) & 1) ^ 1, abort_flag, p.err);
+                ok = warp_wait(ok, &bars[kPFree0 + (n & 1)], ((n >> 1) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
                 if (ok) {
                     tc05::fence_after_sync();
                     tc05::st_x8_u32(trow + kColP + (n & 1) * 32 + qt * 8, h);
@@ -832,7 +835,7 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
             named_bar_sync(row_bar, 128);
             l = (lb[row] + lb[kHeads + row]) + (lb[2 * kHeads + row] + lb[3 * kHeads + row]);
             named_bar_sync(row_bar, 128);
-            ok = warp_wait(ok, &bars[kODone], ic & 1, abort_flag, p.err);
+            ok = warp_wait(ok, &bars[kODone], ic & 1, abort_flag, p.err, p.wait_ns);
             tc05::fence_after_sync();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const bool single = it.part < 0;
@@ -1103,6 +1106,7 @@ pkv_status launch(const pkv_decode_args *a, void *ws, size_t ws_bytes, int32_t *
     p.part_lse = reinterpret_cast<float *>(static_cast<char *>(ws) + pl.part_o_bytes);
     p.meta = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + pl.part_o_bytes + pl.part_lse_bytes);
     p.err = err;
+    p.wait_ns = wait_limit_ns();
     p.pool = static_cast<const uint16_t *>(a->k_pool);
     p.pool_stride = a->k_row_stride;
     if (a->layout == PKV_LAYOUT_VARLEN) p.ps_shift = 0, p.ps_mask = 0;

@@ -74,6 +74,7 @@ struct Params {
     uint16_t *out;
     float *lse, *part_o, *part_lse;
     int32_t *err;
+    uint64_t wait_ns;          // bound of every mbarrier wait (pkv_set_wait_limit)
     int32_t cache_requests;   // per-request values kept in shared memory (they fit)
     int32_t *counter;         // items handed out past the first wave (zeroed before the launch)
     int32_t *goff, *ioff;     // [B + 1] first (kv head, query block) group / first item of each request,
@@ -284,15 +285,18 @@ __device__ __forceinline__ void build_tables(const Params &p, const Tables &t, i
     }
 }
 
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int32_t *err) {
+// Bounded wait with the CTA-wide abort flag: gives up once another warp gave up or
+// `limit_ns` have passed (checked after the second poll and every 64 polls).
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int32_t *err,
+                                         uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63) == 0) {
+        if ((i & 63) == 1) {
             if (*abort_flag) return false;
-            if (global_ns() - t0 > 2000000000ull) {
+            if (global_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
                 raise_flag(err, PKV_DEVERR_TIMEOUT);
                 return false;
@@ -301,8 +305,8 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
     }
 }
 __device__ __forceinline__ bool warp_wait(bool ok, uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                          int32_t *err) {
-    return __all_sync(0xffffffffu, ok && wait_bar(bar, parity, abort_flag, err));
+                                          int32_t *err, uint64_t limit_ns) {
+    return __all_sync(0xffffffffu, ok && wait_bar(bar, parity, abort_flag, err, limit_ns));
 }
 // Bounded wait that ignores the abort flag: drains work this CTA started.
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
@@ -336,8 +340,8 @@ enum Bar {
 // Item k of this CTA's sequence from the queue (w < 0: no more items, or an
 // abort).  Every reader warp takes every item once, in order, and frees its slot.
 __device__ __forceinline__ Item ring_read(const Item *ring, uint64_t *bars, uint32_t k, bool &ok,
-                                          volatile int *abort_flag, int32_t *err) {
-    ok = warp_wait(ok, &bars[kItemFull0 + k % kRing], (k / kRing) & 1, abort_flag, err);
+                                          volatile int *abort_flag, int32_t *err, uint64_t limit_ns) {
+    ok = warp_wait(ok, &bars[kItemFull0 + k % kRing], (k / kRing) & 1, abort_flag, err, limit_ns);
     Item it;
     if (ok) {
         it = ring[k % kRing];
@@ -462,7 +466,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
         auto publish = [&](int64_t w) {
             settle_all();   // the readers of the queue may be waiting for these tiles
             const uint32_t slot = kpub % kRing;
-            ok = warp_wait(ok, &bars[kItemEmpty0 + slot], ((kpub / kRing) & 1) ^ 1, abort_flag, p.err);
+            ok = warp_wait(ok, &bars[kItemEmpty0 + slot], ((kpub / kRing) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
             Item qi;
             if (w >= 0 && w < total) {
                 qi = locate(p, tb, w);
@@ -487,7 +491,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             publish(more ? w1 : -1);
         }
         for (uint32_t k = 0; ok; ++k) {
-            const Item it = ring_read(ring, bars, k, ok, abort_flag, p.err);
+            const Item it = ring_read(ring, bars, k, ok, abort_flag, p.err, p.wait_ns);
             if (it.w < 0) break;
             int got = 0;   // the claim's latency hides behind this item's tiles
             if (more && lane == 0) got = atomicAdd(p.counter, 1);
@@ -514,7 +518,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                         const int r0 = key_row(lane), r1 = key_row(lane + 32);
                         if (r0 == -2 || r1 == -2) raise_flag(p.err, PKV_DEVERR_RANGE);
                         const int s = n % kStages;
-                        if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
+                        if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
                         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                         if (!ok) break;
                         constexpr int CPR = D / 8;       // 16-byte chunks per row
@@ -551,7 +555,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                         if (lane >= nops) row = -1;
                         if (row == -2 && lane % (2 * C::kSl) == 0) raise_flag(p.err, PKV_DEVERR_RANGE);
                         const int s = n % kStages;
-                        if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err);
+                        if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
                         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                         if (!ok) break;
                         if (row == -2) {   // a page outside the pool reads as zeros
@@ -593,7 +597,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
         bool ok = true;
         auto load_q = [&](const Item &qi, uint32_t slot_use) {   // slot_use: how many q loads came before
             const int sl = slot_use & 1;
-            ok = warp_wait(ok, &bars[kQEmpty0 + sl], ((slot_use >> 1) & 1) ^ 1, abort_flag, p.err);
+            ok = warp_wait(ok, &bars[kQEmpty0 + sl], ((slot_use >> 1) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
             if (ok && lane == 0) {
                 mbar_arrive_expect_tx(&bars[kQFull0 + sl], C::kQBytes);
                 const int tok = qi.qo0 + qi.qblk * p.T;
@@ -605,19 +609,19 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             if (ok) ++q_issued;
         };
         uint32_t kr = 0;
-        Item it = ring_read(ring, bars, kr++, ok, abort_flag, p.err);
+        Item it = ring_read(ring, bars, kr++, ok, abort_flag, p.err, p.wait_ns);
         bool q_req = false;   // it's q block already requested
         while (it.w >= 0 && ok) {
-            const Item nx = ring_read(ring, bars, kr++, ok, abort_flag, p.err);   // may be the end
+            const Item nx = ring_read(ring, bars, kr++, ok, abort_flag, p.err, p.wait_ns);   // may be the end
             bool nx_req = false;
             if (it.n_tiles > 0) {
                 if (!q_req) load_q(it, iq);
                 const int sl = iq & 1;
-                ok = warp_wait(ok, &bars[kQFull0 + sl], (iq >> 1) & 1, abort_flag, p.err);
+                ok = warp_wait(ok, &bars[kQFull0 + sl], (iq >> 1) & 1, abort_flag, p.err, p.wait_ns);
                 for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
                     const int s = n % kStages;
-                    ok = warp_wait(ok, &bars[kKvFull0 + s], (n / kStages) & 1, abort_flag, p.err);
-                    ok = warp_wait(ok, &bars[kSFree0 + (n & 1)], ((n >> 1) & 1) ^ 1, abort_flag, p.err);
+                    ok = warp_wait(ok, &bars[kKvFull0 + s], (n / kStages) & 1, abort_flag, p.err, p.wait_ns);
+                    ok = warp_wait(ok, &bars[kSFree0 + (n & 1)], ((n >> 1) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
                     if (!ok) break;
                     tc05::fence_after_sync();
                     if (lane == 0) {
@@ -660,12 +664,12 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
         uint32_t n = 0, io = 0;
         bool ok = true;
         for (uint32_t k = 0; ok; ++k) {
-            const Item it = ring_read(ring, bars, k, ok, abort_flag, p.err);
+            const Item it = ring_read(ring, bars, k, ok, abort_flag, p.err, p.wait_ns);
             if (it.w < 0) break;
             if (it.n_tiles == 0) continue;
             const int ko = io & 1;
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
-                ok = warp_wait(ok, &bars[kPFull0 + (n & 1)], (n >> 1) & 1, abort_flag, p.err);
+                ok = warp_wait(ok, &bars[kPFull0 + (n & 1)], (n >> 1) & 1, abort_flag, p.err, p.wait_ns);
                 if (!ok) break;
                 unsigned char *v = sKV + (n % kStages) * C::kStageBytes + C::kKBytes;
                 const int n_valid = it.k1 - (it.k0 + ti * kTile);
@@ -678,7 +682,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
-                if (ti == 0) ok = warp_wait(ok, &bars[kOFree0 + ko], ((io >> 1) & 1) ^ 1, abort_flag, p.err);
+                if (ti == 0) ok = warp_wait(ok, &bars[kOFree0 + ko], ((io >> 1) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
                 if (!ok) break;
                 tc05::fence_after_sync();
                 if (lane == 0) {
@@ -713,13 +717,13 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
         uint32_t io = 0;
         bool ok = true;
         for (uint32_t k = 0;; ++k) {
-            const Item it = ring_read(ring, bars, k, ok, abort_flag, p.err);
+            const Item it = ring_read(ring, bars, k, ok, abort_flag, p.err, p.wait_ns);
             if (it.w < 0) break;
             if (it.n_tiles == 0) continue;
             const int ko = io & 1;
-            ok = warp_wait(ok, &bars[kStatFull0 + ko], (io >> 1) & 1, abort_flag, p.err);
+            ok = warp_wait(ok, &bars[kStatFull0 + ko], (io >> 1) & 1, abort_flag, p.err, p.wait_ns);
             const float2 ml = stats[ko * kRows + r];
-            ok = warp_wait(ok, &bars[kODone0 + ko], (io >> 1) & 1, abort_flag, p.err);
+            ok = warp_wait(ok, &bars[kODone0 + ko], (io >> 1) & 1, abort_flag, p.err, p.wait_ns);
             tc05::fence_after_sync();
             const int tq = it.qblk * p.T + tok;
             const bool valid = tq < it.n;
@@ -794,10 +798,10 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             return kend;
         };
         uint32_t kr = 0;
-        Item it = ring_read(ring, bars, kr++, ok, abort_flag, p.err);
+        Item it = ring_read(ring, bars, kr++, ok, abort_flag, p.err, p.wait_ns);
         int kend = it.w >= 0 ? row_bound(it) : 0;
         while (it.w >= 0) {
-            const Item nx = ring_read(ring, bars, kr++, ok, abort_flag, p.err);   // may be the end
+            const Item nx = ring_read(ring, bars, kr++, ok, abort_flag, p.err, p.wait_ns);   // may be the end
             const int kend_nx = nx.w >= 0 ? row_bound(nx) : 0;
             const int tq = it.qblk * p.T + tok;                  // token within the request
             const bool valid = tq < it.n;
@@ -820,7 +824,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                 // rows past the block's tokens are never written: they only mask the
                 // keys past the chunk (stale data), which keeps full tiles select-free
                 const int vis = max(0, min(min(valid ? kend : it.k1, it.k1) - key0, kTile));
-                ok = warp_wait(ok, &bars[kSFull0 + (n & 1)], (n >> 1) & 1, abort_flag, p.err);
+                ok = warp_wait(ok, &bars[kSFull0 + (n & 1)], (n >> 1) & 1, abort_flag, p.err, p.wait_ns);
                 float x[64];
                 if (ok) {
                     tc05::fence_after_sync();
@@ -855,7 +859,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                 const float corr = raise ? ex2(m - mx) : 1.f;
                 if (__any_sync(0xffffffffu, raise && m != -INFINITY) && ok) {
                     // O is final for tile n - 1 once its P V completed; rescale the row
-                    ok = warp_wait(ok, &bars[kPFree0 + ((n - 1) & 1)], ((n - 1) >> 1) & 1, abort_flag, p.err);
+                    ok = warp_wait(ok, &bars[kPFree0 + ((n - 1) & 1)], ((n - 1) >> 1) & 1, abort_flag, p.err, p.wait_ns);
                     tc05::fence_after_sync();
 #pragma unroll 1
                     for (int cc = 0; cc < D / 16 && ok; ++cc) {
@@ -884,7 +888,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                     h[j] = pack_bf16x2(p0, p1);
                 }
                 l += lsum;
-                ok = warp_wait(ok, &bars[kPFree0 + (n & 1)], ((n >> 1) & 1) ^ 1, abort_flag, p.err);
+                ok = warp_wait(ok, &bars[kPFree0 + (n & 1)], ((n >> 1) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
                 if (ok) {
                     tc05::fence_after_sync();
                     uint32_t h0[16], h1[16];
@@ -903,7 +907,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             }
             // hand (m, l) to the epilogue warps; the buffer is free once they are done
             // with the item two back (the same phase that freed its accumulator)
-            ok = warp_wait(ok, &bars[kOFree0 + ko], ((io >> 1) & 1) ^ 1, abort_flag, p.err);
+            ok = warp_wait(ok, &bars[kOFree0 + ko], ((io >> 1) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
             stats[ko * kRows + r] = make_float2(m, l);
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[kStatFull0 + ko]);
@@ -1132,6 +1136,7 @@ static pkv_status launch_t(const pkv_extend_args *a, const Plan &pl, void *ws, i
                                          Plan::kCounterBytes);
     p.ioff = p.goff + a->batch + 1;
     p.err = err;
+    p.wait_ns = wait_limit_ns();
     p.k_pool = static_cast<const uint16_t *>(a->k_pool);
     p.v_pool = static_cast<const uint16_t *>(a->v_pool);
     p.k_stride = a->k_row_stride;

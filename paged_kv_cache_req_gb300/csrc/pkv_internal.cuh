@@ -21,6 +21,9 @@ pkv_status ok();
 pkv_status check_launch(const char *what);
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
+// Bound of every in-kernel wait, in nanoseconds, for launches issued from now on
+// (pkv_set_wait_limit; about 2 s by default).  Kernels carry it in their parameters.
+uint64_t wait_limit_ns();
 // A value remembered per (current device, key, tag): kernel attributes such as the
 // raised shared-memory limit are per device, so they are set and cached per device.
 // Starts at 0; nullptr if the current device cannot be queried.  Thread-safe.

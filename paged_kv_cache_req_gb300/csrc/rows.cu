@@ -54,53 +54,114 @@ store_kernel(uint16_t *__restrict__ k_pool, uint16_t *__restrict__ v_pool, int64
         warp_copy_row<kVec>(k_pool + slot * k_stride, k_new + i * k_elems, k_elems, lane);
 }
 
-// Grid (batch, splits).  CTA (b, s) finds cu_seqlens[b] by summing earlier
-// lengths, then its warps copy rows t = s*W + w, s*W + w + splits*W, ... of request b.
+// Zeroes `elems` bf16 elements at dst with one warp.
+template <bool kVec>
+__device__ __forceinline__ void warp_zero_row(uint16_t *__restrict__ dst, int64_t elems, int lane) {
+    if (kVec) {
+        uint4 *d = reinterpret_cast<uint4 *>(dst);
+        for (int64_t i = lane; i < elems / 8; i += 32) st_stream_16(d + i, make_uint4(0, 0, 0, 0));
+    } else {
+        for (int64_t i = lane; i < elems; i += 32) dst[i] = 0;
+    }
+}
+
+constexpr int kGatherChunk = kGatherThreads * 8;   // requests per step of the offset scan
+
+// Exclusive block-wide prefix of one value per thread; *total gets the sum.
+__device__ __forceinline__ long long gather_block_scan(long long v, long long *warp_sums, long long *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    long long incl = v;
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    long long before = 0, all = 0;
+    for (int w = 0; w < kGatherThreads / 32; ++w) {
+        const long long x = warp_sums[w];
+        if (w < warp) before += x;
+        all += x;
+    }
+    *total = all;
+    __syncthreads();
+    return before + incl - v;
+}
+
+// Work items are (request b, split y); the grid is persistent and every CTA takes
+// items blockIdx.x, blockIdx.x + gridDim.x, ... in request order.  cu_seqlens[b] is
+// the sum of the lengths before b: each CTA streams all lengths once, 2048 at a
+// time, carrying the running total (linear in the batch over the whole grid).  The
+// warps of item (b, y) copy rows t = y*W + w, y*W + w + splits*W, ... of request b.
+// A request whose row or region lies outside the table, and a slot outside the
+// pool, raise PKV_DEVERR_RANGE and leave zeros in the rows reserved for them, as a
+// bad key reads as zeros in pkv_decode.
 template <bool kVec>
 __global__ void __launch_bounds__(kGatherThreads)
 ragged_gather_kernel(const uint16_t *__restrict__ k_pool, const uint16_t *__restrict__ v_pool, int64_t num_slots,
                      int64_t pool_stride, int64_t row_elems, const int32_t *__restrict__ r2t, int64_t r2t_rows,
                      int64_t row_stride, int64_t width, const int32_t *__restrict__ req_pool_idx,
                      const int32_t *__restrict__ kv_start, const int32_t *__restrict__ seq_lens, int32_t batch,
-                     uint16_t *__restrict__ k_out, uint16_t *__restrict__ v_out, int64_t cap,
+                     int64_t splits, uint16_t *__restrict__ k_out, uint16_t *__restrict__ v_out, int64_t cap,
                      int32_t *__restrict__ cu_seqlens, int32_t *__restrict__ err) {
     pdl_wait();          // inputs may come from the previous kernel of the stream
     pdl_launch_next();
-    __shared__ long long scratch[32];
-    const int b = blockIdx.x;
-    if (b >= batch) {
-        if (threadIdx.x == 0 && blockIdx.y == 0) cu_seqlens[0] = 0;
-        return;
-    }
-    long long before = 0;
-    for (int j = threadIdx.x; j < b; j += kGatherThreads) before += max(seq_lens[j], 0);
-    before = block_sum(before, scratch);
-
-    const int64_t row = req_pool_idx[b];
-    const int64_t s = kv_start ? kv_start[b] : 0;
-    int64_t L = max(seq_lens[b], 0);
-    if (threadIdx.x == 0 && blockIdx.y == 0) {
-        if (b == 0) cu_seqlens[0] = 0;
-        cu_seqlens[b + 1] = static_cast<int32_t>(before + L);
-        if (before + L > cap) raise_flag(err, PKV_DEVERR_CAPACITY);
-    }
-    if (row < 0 || row >= r2t_rows || s < 0 || s + L > width || seq_lens[b] < 0) {
-        if (threadIdx.x == 0 && blockIdx.y == 0) raise_flag(err, PKV_DEVERR_RANGE);
-        return;
-    }
-    if (before + L > cap) L = cap > before ? cap - before : 0;
-    const int32_t *rrow = r2t + row * row_stride + s;
+    __shared__ long long warp_sums[kGatherThreads / 32];
+    __shared__ long long off_s[kGatherChunk];
+    if (blockIdx.x == 0 && threadIdx.x == 0) cu_seqlens[0] = 0;
+    if (batch <= 0) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int W = kGatherThreads / 32;
-    for (int64_t t = static_cast<int64_t>(blockIdx.y) * W + warp; t < L; t += static_cast<int64_t>(gridDim.y) * W) {
-        const int64_t slot = __ldg(rrow + t);
-        if (slot < 0 || slot >= num_slots) {
-            if (lane == 0) raise_flag(err, PKV_DEVERR_RANGE);
-            continue;
+    const int64_t items = static_cast<int64_t>(batch) * splits;
+    int64_t w = blockIdx.x;
+    long long carry = 0;
+    for (int c0 = 0; c0 < batch && w < items; c0 += kGatherChunk) {
+        long long n8[8];
+        long long mine = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int j = c0 + threadIdx.x * 8 + k;
+            n8[k] = j < batch ? max(seq_lens[j], 0) : 0;
+            mine += n8[k];
         }
-        const int64_t o = before + t;
-        warp_copy_row<kVec>(k_out + o * row_elems, k_pool + slot * pool_stride, row_elems, lane);
-        if (v_pool) warp_copy_row<kVec>(v_out + o * row_elems, v_pool + slot * pool_stride, row_elems, lane);
+        long long total = 0;
+        long long run = carry + gather_block_scan(mine, warp_sums, &total);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            off_s[threadIdx.x * 8 + k] = run;
+            run += n8[k];
+        }
+        carry += total;
+        __syncthreads();
+        for (; w < items && w / splits < c0 + kGatherChunk; w += gridDim.x) {
+            const int b = static_cast<int>(w / splits);
+            const int64_t y = w % splits;
+            const long long before = off_s[b - c0];
+            const int64_t row = req_pool_idx[b];
+            const int64_t s = kv_start ? kv_start[b] : 0;
+            int64_t L = max(seq_lens[b], 0);
+            const bool valid = row >= 0 && row < r2t_rows && s >= 0 && s + L <= width && seq_lens[b] >= 0;
+            if (y == 0 && threadIdx.x == 0) {
+                cu_seqlens[b + 1] = static_cast<int32_t>(before + L);
+                if (before + L > cap) raise_flag(err, PKV_DEVERR_CAPACITY);
+                if (!valid) raise_flag(err, PKV_DEVERR_RANGE);
+            }
+            if (before + L > cap) L = cap > before ? cap - before : 0;
+            const int32_t *rrow = valid ? r2t + row * row_stride + s : nullptr;
+            for (int64_t t = y * W + warp; t < L; t += splits * W) {
+                const int64_t o = before + t;
+                const int64_t slot = valid ? __ldg(rrow + t) : -1;
+                if (slot < 0 || slot >= num_slots) {
+                    if (valid && lane == 0) raise_flag(err, PKV_DEVERR_RANGE);
+                    warp_zero_row<kVec>(k_out + o * row_elems, row_elems, lane);
+                    if (v_pool) warp_zero_row<kVec>(v_out + o * row_elems, row_elems, lane);
+                    continue;
+                }
+                warp_copy_row<kVec>(k_out + o * row_elems, k_pool + slot * pool_stride, row_elems, lane);
+                if (v_pool) warp_copy_row<kVec>(v_out + o * row_elems, v_pool + slot * pool_stride, row_elems, lane);
+            }
+        }
+        __syncthreads();   // off_s is rewritten by the next chunk
     }
 }
 
@@ -220,19 +281,20 @@ extern "C" pkv_status pkv_ragged_gather(const void *k_pool, const void *v_pool, 
     const int64_t want = 2ll * sm_count() * (2048 / kGatherThreads);
     if (batch > 0) splits = std::min<int64_t>(splits, std::max<int64_t>(1, (want + batch - 1) / batch));
     splits = std::max<int64_t>(1, std::min<int64_t>(splits, 65535));
-    dim3 grid(batch > 0 ? batch : 1, static_cast<unsigned>(splits));
+    const int64_t items = static_cast<int64_t>(std::max(batch, 1)) * splits;
+    const dim3 grid(static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(items, 8ll * std::max(1, sm_count())))));
     auto s = reinterpret_cast<cudaStream_t>(stream);
     auto kp = static_cast<const uint16_t *>(k_pool), vp = static_cast<const uint16_t *>(v_pool);
     auto ko = static_cast<uint16_t *>(k_out), vo = static_cast<uint16_t *>(v_out);
     if (vec)
         return launch_status(launch_chained(ragged_gather_kernel<true>, dim3(grid), dim3(kGatherThreads), 0, s, kp, vp,
                                             num_slots, pool_row_stride, row_elems, req_to_token, r2t_rows,
-                                            r2t_row_stride, r2t_width, req_pool_idx, kv_start, seq_lens, batch, ko, vo,
-                                            out_rows_cap, cu_seqlens, err_flags),
+                                            r2t_row_stride, r2t_width, req_pool_idx, kv_start, seq_lens, batch, splits,
+                                            ko, vo, out_rows_cap, cu_seqlens, err_flags),
                              "pkv_ragged_gather");
     return launch_status(launch_chained(ragged_gather_kernel<false>, dim3(grid), dim3(kGatherThreads), 0, s, kp, vp,
                                         num_slots, pool_row_stride, row_elems, req_to_token, r2t_rows, r2t_row_stride,
-                                        r2t_width, req_pool_idx, kv_start, seq_lens, batch, ko, vo, out_rows_cap,
+                                        r2t_width, req_pool_idx, kv_start, seq_lens, batch, splits, ko, vo, out_rows_cap,
                                         cu_seqlens, err_flags),
                          "pkv_ragged_gather");
 }

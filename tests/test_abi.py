@@ -156,3 +156,13 @@ def test_workspace_size_follows_split_plan(binding):
 
 def lib_ws(binding, a):
     return int(binding._lib.pkv_decode_workspace_size(ctypes.byref(a)))
+
+
+def test_wait_limit_round_trip(binding):
+    """pkv_set_wait_limit is host state only; 0 restores the ~2 s default."""
+    default = binding.pkv_wait_limit()
+    assert default == 2_000_000_000
+    binding.pkv_set_wait_limit(12345)
+    assert binding.pkv_wait_limit() == 12345
+    binding.pkv_set_wait_limit(0)
+    assert binding.pkv_wait_limit() == default
