@@ -65,10 +65,12 @@ EXTEND_METRIC = {"llama3_8b_verify": ("paged multi-query attention KV-read GB/s 
 
 
 # ---------------------------------------------------------------- accounting
-def step_bytes(wl, cross_mode="paged", alloc=False):
+def step_bytes(wl, cross_mode="paged", alloc=False, fused=False):
     """Algorithmic bytes of one step and of its decode launches (unique slots once).
     With device allocation: per request its lengths and last slot read, one slot
-    written to the output and one to its row, and the free-list pages taken."""
+    written to the output and one to its row, and the free-list pages taken.
+    Fused (the decode reads the page starts from req_to_token and stores the new
+    rows itself): no full-row table read and no page-list write."""
     r2t = wl.req_to_token.numpy()
     rpi = wl.req_pool_idx.numpy().astype(np.int64)
     if wl.kind == "mla":
@@ -91,6 +93,8 @@ def step_bytes(wl, cross_mode="paged", alloc=False):
         decode += dec
         if p.name == "cross" and cross_mode == "gather":
             total += dec + 2 * int(lens.sum()) * kv_row + int(lens.sum()) * 4
+        elif fused:
+            total += dec                                        # page starts: the 4 B per page in dec
         else:
             total += dec + int(lens.sum()) * 4 + pages * 4        # table read + page-list write
         if p.stores:
@@ -290,12 +294,14 @@ def l2_note(nbytes):
     return "flushed between steps (2x L2 write)" if nbytes < 4 * L2_BYTES else "inputs larger than L2"
 
 
-def decode_config(wl, cross_mode, alloc, world):
+def decode_config(wl, cross_mode, alloc, world, fused=False):
     """The `config` object of a decode line: the same dict in both arms."""
     keys = unique_keys(wl)
-    total_bytes, _ = step_bytes(wl, cross_mode, alloc=alloc)
+    total_bytes, _ = step_bytes(wl, cross_mode, alloc=alloc, fused=fused)
     return {"workload": WORKLOAD_TEXT[wl.name], "name": wl.name, "batch": wl.batch,
             "cross_mode": cross_mode if wl.kind == "gqa" and len(wl.problems) > 1 else None,
+            "page_table": "req_to_token read by pkv_decode, new rows stored by it (fused)" if fused
+            else "pkv_build_indices page lists, then pkv_store and pkv_decode",
             "new_slots": "allocated on the device each step (pkv_alloc_extend + pkv_write_req_to_token)"
             if alloc else "given by the workload",
             "keys_per_step": {k: v[0] for k, v in keys.items()},
@@ -716,8 +722,8 @@ def measure_decode(opts, world, rank, local, dist, one_thread_baseline=False):
     from paged_kv_cache_req_gb300.workloads import make_workload
     wl = make_workload(opts.workload, seed=opts.seed, batch=opts.batch)
     step = DecodeStep(wl, device="cuda", cross_mode=opts.cross_mode, kv_chunk=opts.kv_chunk, seed=opts.seed,
-                      alloc=opts.alloc)
-    total_bytes, decode_bytes = step_bytes(wl, opts.cross_mode, alloc=opts.alloc)
+                      alloc=opts.alloc, fused=opts.fused)
+    total_bytes, decode_bytes = step_bytes(wl, opts.cross_mode, alloc=opts.alloc, fused=opts.fused)
     flush = total_bytes < 4 * L2_BYTES
     flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda") if flush else None
     stream = torch.cuda.current_stream()
@@ -832,7 +838,7 @@ def measure_decode(opts, world, rank, local, dist, one_thread_baseline=False):
         "warmup": opts.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "accumulate": "fp32", "data": "synthetic",
         "decode_steps_per_s": round(world * 1e3 / ms_per_step, 2),
-        "config": decode_config(wl, opts.cross_mode, opts.alloc, world),
+        "config": decode_config(wl, opts.cross_mode, opts.alloc, world, fused=opts.fused),
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -867,26 +873,30 @@ def measure(opts, world, rank, local, dist, one_thread_baseline=False):
 # traffic and CPU baseline; the configurations the oracle runs in seconds also carry
 # a 1-thread oracle time.
 PER_CONFIG = (
-    ("tiny_gqa", "paged", 200),
-    ("qwen3_0p6b", "paged", 200),
-    ("whisper_encdec", "paged", 200),
-    ("whisper_encdec", "gather", 200),
-    ("deepseek_v3_mla", "paged", 100),
-    ("llama3_8b_verify", "paged", 100),
-    ("qwen3_0p6b_prefill", "paged", 100),
-    ("hunyuan_image_spans", "paged", 50),
-    ("encoder_merge", "paged", 200),
+    ("tiny_gqa", "paged", 200, False),
+    ("qwen3_0p6b", "paged", 200, False),
+    ("qwen3_0p6b", "paged", 200, True),
+    ("whisper_encdec", "paged", 200, False),
+    ("whisper_encdec", "paged", 200, True),
+    ("whisper_encdec", "gather", 200, False),
+    ("whisper_encdec", "gather", 200, True),
+    ("llama3_8b", "paged", 100, True),
+    ("deepseek_v3_mla", "paged", 100, False),
+    ("llama3_8b_verify", "paged", 100, False),
+    ("qwen3_0p6b_prefill", "paged", 100, False),
+    ("hunyuan_image_spans", "paged", 50, False),
+    ("encoder_merge", "paged", 200, False),
 )
 ONE_THREAD_BASELINE = ("tiny_gqa", "qwen3_0p6b")
 
 
 def per_config_entries(args, world, rank, local, dist):
     out = {}
-    for name, cross, steps in PER_CONFIG:
-        if name == args.workload and cross == args.cross_mode:
+    for name, cross, steps, fused in PER_CONFIG:
+        if name == args.workload and cross == args.cross_mode and fused == args.fused:
             continue
         opts = argparse.Namespace(**vars(args))
-        opts.workload, opts.cross_mode, opts.steps = name, cross, steps
+        opts.workload, opts.cross_mode, opts.steps, opts.fused = name, cross, steps, fused
         opts.alloc, opts.kv_chunk, opts.batch = False, 0, None
         opts.cpu_key_heads = args.cpu_key_heads // 3
         line = measure(opts, world, rank, local, dist, one_thread_baseline=name in ONE_THREAD_BASELINE)
@@ -896,7 +906,7 @@ def per_config_entries(args, world, rank, local, dist):
         for k in ("n_gpus", "higher_is_better", "scaling", "vs_baseline", "data", "warmup"):
             line.pop(k, None)
         key = name if name != "whisper_encdec" else "whisper_encdec_" + cross
-        out[key] = line
+        out[key + ("_fused" if fused else "")] = line
     return out
 
 
@@ -926,7 +936,7 @@ def run_reference(args):
                 "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": round(1e3 * sum(times) / len(times), 3), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": decode_config(wl, args.cross_mode, args.alloc, world),
+                "config": decode_config(wl, args.cross_mode, args.alloc, world, fused=args.fused),
                 "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                                  "sample": "each step: " + desc},
                 "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -972,6 +982,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
                     help="headline workload only (no per_config entries for the other recipes)")
+    ap.add_argument("--fused", action="store_true",
+                    help="GQA decode reads its pages from req_to_token and stores the new rows itself "
+                         "(one launch per attention problem, no pkv_build_indices / pkv_store)")
     ap.add_argument("--alloc", action="store_true",
                     help="allocate each step's new slots on the device (pkv_alloc_extend + pkv_write_req_to_token)")
     ap.add_argument("--profile-run", action="store_true",

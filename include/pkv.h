@@ -66,7 +66,7 @@ typedef enum pkv_status {
 #define PKV_DEVERR_TIMEOUT 8  /* a device-side wait ran past its limit (pkv_set_wait_limit, ~2 s by
                                  default); outputs of the launch unspecified */
 
-#define PKV_ABI_VERSION 1
+#define PKV_ABI_VERSION 2
 
 /*
  * pkv_build_indices -- page lists from the token-granular table.
@@ -137,7 +137,9 @@ typedef enum pkv_kind {
 typedef enum pkv_layout {
     PKV_LAYOUT_CSR = 0,         /* kv_indptr / kv_indices / kv_last_page_len */
     PKV_LAYOUT_BLOCK_TABLE = 1, /* block_table [B, block_table_width] + seq_lens */
-    PKV_LAYOUT_VARLEN = 2       /* contiguous rows: keys of b are rows cu_seqlens[b] .. cu_seqlens[b+1]-1 */
+    PKV_LAYOUT_VARLEN = 2,      /* contiguous rows: keys of b are rows cu_seqlens[b] .. cu_seqlens[b+1]-1 */
+    PKV_LAYOUT_REQ_TO_TOKEN = 3 /* the token table itself: req_to_token + req_pool_idx (+ kv_start) + seq_lens;
+                                   page of key t = req_to_token[row, s + t - t % ps] / ps (GQA only) */
 } pkv_layout;
 
 typedef struct pkv_decode_args {
@@ -169,6 +171,16 @@ typedef struct pkv_decode_args {
     const int32_t *cu_seqlens;       /* VARLEN [B+1] */
     void *out;                 /* bf16 [B, Hq, head_dim_v] */
     float *lse;                /* fp32 [B, Hq], natural log of the softmax denominator; nullable */
+    /* PKV_LAYOUT_REQ_TO_TOKEN (added in ABI version 2) */
+    const int32_t *req_to_token;     /* int32 [r2t_rows, r2t_row_stride] */
+    int64_t r2t_rows;
+    int64_t r2t_row_stride;
+    int64_t r2t_width;               /* valid columns of a row */
+    const int32_t *req_pool_idx;     /* [B] row of request b */
+    const int32_t *kv_start;         /* [B] column of b's first key (a multiple of page_size), or NULL for 0 */
+    /* fused store (added in ABI version 2; GQA, any layout but VARLEN): both NULL, or both set */
+    const void *k_new;               /* bf16 [B, Hkv, head_dim]: the new token's K */
+    const void *v_new;               /* bf16 [B, Hkv, head_dim]: the new token's V */
 } pkv_decode_args;
 
 /*
@@ -202,6 +214,26 @@ typedef struct pkv_decode_args {
  * length raises PKV_DEVERR_RANGE and the request is treated as empty.  A
  * request longer than max_seq_len raises PKV_DEVERR_CAPACITY and only its
  * first keys (up to the split plan's reach) are attended.
+ *
+ * PKV_LAYOUT_REQ_TO_TOKEN (GQA) reads the pages straight from the token table,
+ * with no pkv_build_indices launch and no page list in between ("From slots to
+ * a page table": the page of position t is req_to_token[row, t - t % ps] / ps):
+ * request b has L = seq_lens[b] keys at columns s .. s + L - 1 of row
+ * req_pool_idx[b] (s = kv_start[b], or 0), and key t lives at slot
+ * req_to_token[row, s + t - t % ps] + t % ps.  A row or region outside the
+ * table (or s not a multiple of ps) raises PKV_DEVERR_RANGE and the request is
+ * treated as empty; a page's first slot outside the pool raises
+ * PKV_DEVERR_RANGE and one that is not a multiple of ps PKV_DEVERR_CONTIG, and
+ * its keys read as zeros.  Unlike pkv_build_indices it reads only each page's
+ * first position, so it does not check that the other positions continue it.
+ *
+ * Fused store (k_new and v_new set; GQA; not with VARLEN): the step's new token
+ * is request b's last key, t = L - 1.  Before attending, the call writes
+ * k_new[b] and v_new[b] into the pools at that key's slot (pkv_store's write,
+ * mini-sglang handbook "The KV pool": store_kv before attention), and the
+ * attention uses those values for the key.  k_pool and v_pool must then be
+ * writable.  A request that raises PKV_DEVERR_CAPACITY (longer than
+ * max_seq_len) is not stored.
  */
 pkv_status pkv_decode(const pkv_decode_args *args, void *workspace, size_t workspace_bytes,
                       int32_t *err_flags, pkv_stream_t stream);

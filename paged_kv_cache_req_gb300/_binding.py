@@ -19,7 +19,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpkv.so"
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CAPACITY, PKV_ERR_CUDA = range(5)
 PKV_DEVERR_RANGE, PKV_DEVERR_CONTIG, PKV_DEVERR_CAPACITY, PKV_DEVERR_TIMEOUT = 1, 2, 4, 8
 PKV_KIND_GQA, PKV_KIND_MLA = 0, 1
-PKV_LAYOUT_CSR, PKV_LAYOUT_BLOCK_TABLE, PKV_LAYOUT_VARLEN = 0, 1, 2
+PKV_LAYOUT_CSR, PKV_LAYOUT_BLOCK_TABLE, PKV_LAYOUT_VARLEN, PKV_LAYOUT_REQ_TO_TOKEN = 0, 1, 2, 3
 
 EXPORTED_SYMBOLS = ("pkv_build_indices", "pkv_store", "pkv_decode", "pkv_decode_workspace_size",
                     "pkv_decode_no_alloc", "pkv_ragged_gather", "pkv_alloc_extend", "pkv_write_req_to_token",
@@ -54,6 +54,9 @@ class DecodeArgs(ctypes.Structure):
         ("kv_last_page_len", ctypes.c_void_p), ("block_table", ctypes.c_void_p),
         ("seq_lens", ctypes.c_void_p), ("cu_seqlens", ctypes.c_void_p),
         ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("req_to_token", ctypes.c_void_p), ("r2t_rows", ctypes.c_int64), ("r2t_row_stride", ctypes.c_int64),
+        ("r2t_width", ctypes.c_int64), ("req_pool_idx", ctypes.c_void_p), ("kv_start", ctypes.c_void_p),
+        ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
     ]
 
 
@@ -170,7 +173,8 @@ def pkv_store(k_pool, v_pool, k_new, v_new, slot_mapping, err_flags, stream=None
 def make_decode_args(kind, layout, q, k_pool, v_pool, out, *, page_size=1, sm_scale, max_seq_len,
                      num_kv_heads=None, head_dim_v=None, kv_indptr=None, kv_indices=None,
                      kv_last_page_len=None, block_table=None, seq_lens=None, cu_seqlens=None, lse=None,
-                     kv_chunk=0) -> DecodeArgs:
+                     kv_chunk=0, req_to_token=None, req_pool_idx=None, kv_start=None, k_new=None,
+                     v_new=None) -> DecodeArgs:
     B, hq, dqk = q.shape
     if kind == PKV_KIND_MLA:
         hkv = 1
@@ -188,10 +192,15 @@ def make_decode_args(kind, layout, q, k_pool, v_pool, out, *, page_size=1, sm_sc
     a.num_slots = k_pool.shape[0]
     a.k_row_stride, a.v_row_stride = k_pool.stride(0), v_stride
     a.kv_indices_len = kv_indices.numel() if kv_indices is not None else 0
+    if req_to_token is not None:
+        _i32(req_to_token, "req_to_token")
+        a.r2t_rows, a.r2t_row_stride, a.r2t_width = req_to_token.shape[0], req_to_token.stride(0), req_to_token.shape[1]
     tensors = (("q", q), ("k_pool", k_pool), ("v_pool", v_pool), ("kv_indptr", kv_indptr),
                ("kv_indices", kv_indices), ("kv_last_page_len", kv_last_page_len),
                ("block_table", block_table), ("seq_lens", seq_lens), ("cu_seqlens", cu_seqlens),
-               ("out", out), ("lse", lse))
+               ("out", out), ("lse", lse), ("req_to_token", req_to_token),
+               ("req_pool_idx", _i32(req_pool_idx, "req_pool_idx")), ("kv_start", _i32(kv_start, "kv_start")),
+               ("k_new", k_new), ("v_new", v_new))
     for name, t in tensors:
         setattr(a, name, None if t is None else _p(t).value)
     # the struct holds raw pointers: keep the tensors alive as long as it lives

@@ -58,6 +58,12 @@ struct Params {
     float *part_o, *part_lse;
     int32_t *err;
     uint64_t wait_ns;   // bound of every mbarrier wait (pkv_set_wait_limit)
+    // PKV_LAYOUT_REQ_TO_TOKEN: the token table itself
+    const int32_t *r2t, *req_pool_idx, *kv_start;
+    int64_t r2t_rows, r2t_stride, r2t_width;
+    // fused store: the new token's rows (nullptr: none), written into the pools
+    const uint16_t *k_new, *v_new;
+    uint16_t *k_pool_w, *v_pool_w;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -68,9 +74,22 @@ __device__ __forceinline__ float ex2(float x) {
 
 // Key count of request b (clamped to what its page table can address) and the
 // base offset of its page list.
-__device__ __forceinline__ int key_count(const Params &p, int b, int64_t &base, bool report) {
+__device__ __forceinline__ int key_count(const Params &p, int b, int64_t &base, bool report, bool *clamped = nullptr) {
     int64_t L, cap;
-    if (p.layout == PKV_LAYOUT_CSR) {
+    if (clamped) *clamped = false;
+    if (p.layout == PKV_LAYOUT_REQ_TO_TOKEN) {
+        // keys at columns s .. s + L - 1 of the request's row; base = offset of column s
+        const int64_t row = p.req_pool_idx[b];
+        const int64_t s = p.kv_start ? p.kv_start[b] : 0;
+        L = p.seq_lens[b];
+        if (row < 0 || row >= p.r2t_rows || s < 0 || L < 0 || s + L > p.r2t_width || (s & p.ps_mask)) {
+            if (report) raise_flag(p.err, PKV_DEVERR_RANGE);
+            base = 0;
+            return 0;
+        }
+        base = row * p.r2t_stride + s;
+        cap = L;
+    } else if (p.layout == PKV_LAYOUT_CSR) {
         const int64_t lo = p.kv_indptr[b], hi = p.kv_indptr[b + 1];
         const int64_t n = hi - lo;
         const int last = n > 0 ? p.kv_last[b] : 0;
@@ -94,15 +113,25 @@ __device__ __forceinline__ int key_count(const Params &p, int b, int64_t &base, 
     const int64_t limit = min(cap, static_cast<int64_t>(p.chunk) * p.n_chunks_max);
     if (L < 0 || L > limit) {
         if (report) raise_flag(p.err, L < 0 ? PKV_DEVERR_RANGE : PKV_DEVERR_CAPACITY);
+        if (clamped) *clamped = true;
         L = L < 0 ? 0 : limit;
     }
     return static_cast<int>(L);
 }
 
+// Pool slot of key t (base from key_count): -1 when its page lies outside the pool,
+// -2 when the token table gives a page start that is not a multiple of the page size.
 __device__ __forceinline__ int64_t slot_of(const Params &p, int64_t base, int t) {
     if (p.layout == PKV_LAYOUT_VARLEN) {
         const int64_t s = base + t;
         return (s >= 0 && s < p.num_slots) ? s : -1;
+    }
+    if (p.layout == PKV_LAYOUT_REQ_TO_TOKEN) {
+        // the slot of the page's first position, then the offset inside the page
+        const int64_t first = __ldg(p.r2t + base + (t & ~p.ps_mask));
+        if (first < 0 || first >= (p.num_pages << p.ps_shift)) return -1;
+        if (first & p.ps_mask) return -2;
+        return first + (t & p.ps_mask);
     }
     const int32_t *tab = p.layout == PKV_LAYOUT_CSR ? p.kv_indices : p.block_table;
     const int page = __ldg(tab + base + (t >> p.ps_shift));
@@ -166,6 +195,7 @@ __device__ __forceinline__ void build_item_table(const Params &p, int *off, int 
 struct Item {
     int b, c, kh, hs, L, n_chunks, head0, t_begin, t_end;
     int64_t base;
+    bool store;   // fused store: this item's keys end with the request's new token
 };
 
 template <int GC>
@@ -182,7 +212,8 @@ __device__ __forceinline__ Item locate(const Params &p, const int *off, int w, b
     rem /= p.hsplit;
     it.kh = rem % p.hkv;
     it.c = rem / p.hkv;
-    it.L = key_count(p, it.b, it.base, report && it.c == 0 && it.kh == 0 && it.hs == 0);
+    bool clamped = false;
+    it.L = key_count(p, it.b, it.base, report && it.c == 0 && it.kh == 0 && it.hs == 0, &clamped);
     it.n_chunks = max(1, (it.L + p.chunk - 1) / p.chunk);
     it.head0 = it.kh * p.g + it.hs * GC;
     // the request's n_chunks pieces are made equal (a multiple of 64 keys, at most
@@ -190,7 +221,35 @@ __device__ __forceinline__ Item locate(const Params &p, const int *off, int w, b
     const int span = ((it.L + it.n_chunks - 1) / it.n_chunks + kTile - 1) / kTile * kTile;
     it.t_begin = it.c * span;
     it.t_end = min(it.L, it.t_begin + span);
+    it.store = p.k_new != nullptr && !clamped && it.L > 0 && it.t_end == it.L;
     return it;
+}
+
+// Fused store of the new token (key L - 1 of the request, kv head kh): the pool rows
+// are written here, with plain stores (run by one warp of the item).  The key itself
+// is masked out of its tile (whatever the tile load read from its stale slot is
+// ignored) and added to the warp's softmax state afterwards from k_new / v_new
+// (Math::add_key), so the tile loop is the same code with or without the store.
+template <int D>
+__device__ __forceinline__ void store_new_rows(const Params &p, const Item &it) {
+    const int lane = threadIdx.x & 31;
+    const int64_t slot = slot_of(p, it.base, it.L - 1);
+    if (slot < 0) return;   // the loads of that page raised the flag
+    const int64_t row = (static_cast<int64_t>(it.b) * p.hkv + it.kh) * D;
+    for (int i = lane; i < 2 * (D / 8); i += 32) {
+        const bool is_v = i >= D / 8;
+        const int c = is_v ? i - D / 8 : i;
+        const uint4 val = __ldg(reinterpret_cast<const uint4 *>((is_v ? p.v_new : p.k_new) + row + c * 8));
+        uint16_t *dst = is_v ? p.v_pool_w + slot * p.v_stride : p.k_pool_w + slot * p.k_stride;
+        *reinterpret_cast<uint4 *>(dst + it.kh * D + c * 8) = val;
+    }
+}
+
+// Valid keys of the tile starting at t0 for the math: with the fused store the new
+// token (the item's last key) is left out of its tile.
+__device__ __forceinline__ int tile_keys(const Item &it, int t0) {
+    const int n = it.t_end - t0;
+    return (it.store && n <= kTile) ? n - 1 : n;
 }
 
 template <int D, int GC>
@@ -379,6 +438,67 @@ __device__ __forceinline__ void mma_store(MmaState<D, GC> &st, float *red_o, flo
     }
 }
 
+// One more key, given as bf16 rows kn / vn in global memory, added to this warp's
+// state (the fused store's new token).  The thread holds q of rows g and g + 8 in
+// the A-fragment layout: dims 16 ks + 2 tig + {0, 1} and + 8; the four threads of a
+// row reduce their partial dot products with xor-shuffles.  P stays in fp32; l is
+// counted once per row (by tig 0), as the row sum is reduced over tig at the end.
+template <int D, int GC>
+__device__ __forceinline__ void mma_add_key(MmaState<D, GC> &st, const uint16_t *kn, const uint16_t *vn,
+                                            float scale_log2) {
+    constexpr bool kRows8 = MmaState<D, GC>::kRows8;
+    constexpr float kLazy = 8.f;
+    const int lane = threadIdx.x & 31, tig = lane & 3;
+    const uint32_t *k32 = reinterpret_cast<const uint32_t *>(kn);
+    float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < MmaState<D, GC>::KS; ++ks) {
+        const uint32_t klo = __ldg(k32 + ks * 8 + tig), khi = __ldg(k32 + ks * 8 + 4 + tig);
+        d0 = fmaf(bf16_lo(st.qa[ks][0]), bf16_lo(klo), d0);
+        d0 = fmaf(bf16_hi(st.qa[ks][0]), bf16_hi(klo), d0);
+        d0 = fmaf(bf16_lo(st.qa[ks][2]), bf16_lo(khi), d0);
+        d0 = fmaf(bf16_hi(st.qa[ks][2]), bf16_hi(khi), d0);
+        d1 = fmaf(bf16_lo(st.qa[ks][1]), bf16_lo(klo), d1);
+        d1 = fmaf(bf16_hi(st.qa[ks][1]), bf16_hi(klo), d1);
+        d1 = fmaf(bf16_lo(st.qa[ks][3]), bf16_lo(khi), d1);
+        d1 = fmaf(bf16_hi(st.qa[ks][3]), bf16_hi(khi), d1);
+    }
+    d0 += __shfl_xor_sync(0xffffffffu, d0, 1);
+    d0 += __shfl_xor_sync(0xffffffffu, d0, 2);
+    d1 += __shfl_xor_sync(0xffffffffu, d1, 1);
+    d1 += __shfl_xor_sync(0xffffffffu, d1, 2);
+    const float s0 = d0 * scale_log2, s1 = d1 * scale_log2;
+    if (s0 > st.m0 + kLazy || st.m0 == -INFINITY) {
+        const float corr = ex2(st.m0 - s0);
+        st.l0 *= corr;
+#pragma unroll
+        for (int nt = 0; nt < MmaState<D, GC>::NT; ++nt) { st.o[nt][0] *= corr; st.o[nt][1] *= corr; }
+        st.m0 = s0;
+    }
+    if (kRows8 && (s1 > st.m1 + kLazy || st.m1 == -INFINITY)) {
+        const float corr = ex2(st.m1 - s1);
+        st.l1 *= corr;
+#pragma unroll
+        for (int nt = 0; nt < MmaState<D, GC>::NT; ++nt) { st.o[nt][2] *= corr; st.o[nt][3] *= corr; }
+        st.m1 = s1;
+    }
+    const float p0 = ex2(s0 - st.m0);
+    const float p1 = kRows8 ? ex2(s1 - st.m1) : 0.f;
+    if (tig == 0) {
+        st.l0 += p0;
+        st.l1 += p1;
+    }
+    const uint32_t *v32 = reinterpret_cast<const uint32_t *>(vn);
+#pragma unroll
+    for (int nt = 0; nt < MmaState<D, GC>::NT; ++nt) {
+        const uint32_t vv = __ldg(v32 + nt * 4 + tig);   // dims 8 nt + 2 tig, + 1
+        st.o[nt][0] = fmaf(p0, bf16_lo(vv), st.o[nt][0]);
+        st.o[nt][1] = fmaf(p0, bf16_hi(vv), st.o[nt][1]);
+        st.o[nt][2] = fmaf(p1, bf16_lo(vv), st.o[nt][2]);
+        st.o[nt][3] = fmaf(p1, bf16_hi(vv), st.o[nt][3]);
+    }
+}
+
 // ---------------------------------------------------------------- CUDA-core math (one head per kv head)
 // Each warp takes 16 keys of a tile; 8 lanes share a key (each lane owns D/8
 // dims), reduce q.k with three xor-shuffles, and keep their own online-softmax
@@ -519,6 +639,58 @@ __device__ __forceinline__ void simt_store(SimtState<D, GC> &st, float *red_o, f
     }
 }
 
+// One more key (the fused store's new token) added to the state of lane group 0
+// (lanes 0-7: each owns D / 8 dims; q is already scaled by scale * log2 e).  The
+// groups' states are combined in simt_store, so one group taking the key counts it
+// once.
+template <int D, int GC>
+__device__ __forceinline__ void simt_add_key(SimtState<D, GC> &st, const uint16_t *kn, const uint16_t *vn) {
+    constexpr int NC = SimtState<D, GC>::NC;
+    const int lane = threadIdx.x & 31, grp = lane >> 3, part = lane & 7;
+    float s[GC];
+#pragma unroll
+    for (int h = 0; h < GC; ++h) s[h] = 0.f;
+#pragma unroll
+    for (int ci = 0; ci < NC; ++ci) {
+        float kf[8];
+        widen8(__ldg(reinterpret_cast<const uint4 *>(kn + (part + 8 * ci) * 8)), kf);
+#pragma unroll
+        for (int h = 0; h < GC; ++h)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) s[h] = fmaf(st.q[h][ci][e], kf[e], s[h]);
+    }
+#pragma unroll
+    for (int h = 0; h < GC; ++h) {
+        s[h] += __shfl_xor_sync(0xffffffffu, s[h], 1);
+        s[h] += __shfl_xor_sync(0xffffffffu, s[h], 2);
+        s[h] += __shfl_xor_sync(0xffffffffu, s[h], 4);
+    }
+    if (grp != 0) return;
+#pragma unroll
+    for (int h = 0; h < GC; ++h) {
+        if (s[h] > st.m[h]) {
+            const float corr = ex2(st.m[h] - s[h]);   // m = -inf gives 0
+            st.l[h] *= corr;
+#pragma unroll
+            for (int ci = 0; ci < NC; ++ci)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) st.o[h][ci][e] *= corr;
+            st.m[h] = s[h];
+        }
+        s[h] = ex2(s[h] - st.m[h]);
+        st.l[h] += s[h];
+    }
+#pragma unroll
+    for (int ci = 0; ci < NC; ++ci) {
+        float vf[8];
+        widen8(__ldg(reinterpret_cast<const uint4 *>(vn + (part + 8 * ci) * 8)), vf);
+#pragma unroll
+        for (int h = 0; h < GC; ++h)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) st.o[h][ci][e] = fmaf(s[h], vf[e], st.o[h][ci][e]);
+    }
+}
+
 template <int D, int GC, bool MMA>
 struct Math;
 template <int D, int GC>
@@ -529,6 +701,9 @@ struct Math<D, GC, true> {
         mma_tile<D, GC>(s, k, v, n, sc);
     }
     static __device__ __forceinline__ void store(State &s, float *o, float *m, float *l) { mma_store<D, GC>(s, o, m, l); }
+    static __device__ __forceinline__ void add_key(State &s, const uint16_t *kn, const uint16_t *vn, float sc) {
+        mma_add_key<D, GC>(s, kn, vn, sc);
+    }
 };
 template <int D, int GC>
 struct Math<D, GC, false> {
@@ -538,7 +713,20 @@ struct Math<D, GC, false> {
         simt_tile<D, GC>(s, k, v, n);
     }
     static __device__ __forceinline__ void store(State &s, float *o, float *m, float *l) { simt_store<D, GC>(s, o, m, l); }
+    static __device__ __forceinline__ void add_key(State &s, const uint16_t *kn, const uint16_t *vn, float) {
+        simt_add_key<D, GC>(s, kn, vn);
+    }
 };
+
+// The fused store's new token: math warp 0 adds it to its state (it was left out of
+// the item's last tile) and writes its rows into the pools.
+template <int D, int GC, bool MMA>
+__device__ __forceinline__ void add_new_key(typename Math<D, GC, MMA>::State &st, const Params &p, const Item &it) {
+    if (!it.store || (threadIdx.x >> 5) != 0) return;
+    const int64_t row = (static_cast<int64_t>(it.b) * p.hkv + it.kh) * D;
+    Math<D, GC, MMA>::add_key(st, p.k_new + row, p.v_new + row, p.scale_log2);
+    store_new_rows<D>(p, it);
+}
 
 // ---------------------------------------------------------------- cp.async kernel (page_size < 8)
 // Issue the cp.async copies of one 64-key tile (K and V) of kv head kh; keys
@@ -557,7 +745,7 @@ __device__ __forceinline__ void load_tile_cp_async(const Params &p, uint16_t *ks
         int64_t slot = -1;
         if (t < t1) {
             slot = slot_of(p, base, t);
-            if (slot < 0 && chunk == 0) raise_flag(p.err, PKV_DEVERR_RANGE);
+            if (slot < 0 && chunk == 0) raise_flag(p.err, slot == -2 ? PKV_DEVERR_CONTIG : PKV_DEVERR_RANGE);
         }
         const bool ok = slot >= 0;
         const uint16_t *ksrc = ok ? p.k_pool + slot * p.k_stride + kh * D + chunk * 8 : p.k_pool;
@@ -615,9 +803,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_cp_async_kernel(const Para
                 cp_async_commit();
             }
             const uint16_t *kt = tiles + (ti % kStages) * 2 * T::kElems;
-            M::tile(st, kt, kt + T::kElems, it.t_end - (it.t_begin + ti * kTile), p.scale_log2);
+            M::tile(st, kt, kt + T::kElems, tile_keys(it, it.t_begin + ti * kTile), p.scale_log2);
         }
         cp_async_wait<0>();
+        add_new_key<D, GC, MMA>(st, p, it);
         M::store(st, red_o, red_m, red_l);
         __syncthreads();
         finish_item<D, GC>(p, it, red_o, red_m, red_l);
@@ -723,21 +912,43 @@ decode_tma_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const
         int w = blockIdx.x, ti = 0;
         Item it{};
         bool have = false;
+        // With the token table every page start sits in its own part of the request's
+        // row, so the lookups miss L2 far more often than in a packed page list: when
+        // the cursor reaches an item, the page starts of this CTA's following item are
+        // pulled into L2 (one 128-byte line holds 32 positions).
+        auto prefetch_pages = [&](int wn) {
+            if (p.layout != PKV_LAYOUT_REQ_TO_TOKEN || wn >= total) return;
+            const Item nx = locate<GC>(p, off, wn, false);
+            if (nx.t_end <= nx.t_begin) return;
+            const int step = max(1, 32 >> p.ps_shift);   // pages per line
+            const int last = (nx.t_end - 1) >> p.ps_shift;
+            for (int pg = (nx.t_begin >> p.ps_shift) + lane * step; pg <= last; pg += 32 * step)
+                prefetch_l2(p.r2t + nx.base + (static_cast<int64_t>(pg) << p.ps_shift));
+        };
         auto next_item = [&]() {
             while (w < total) {
                 it = locate<GC>(p, off, w, false);
-                if (it.t_end > it.t_begin) return true;
+                if (it.t_end > it.t_begin) {
+                    prefetch_pages(w + gridDim.x);
+                    return true;
+                }
                 w += gridDim.x;
             }
             return false;
         };
+        prefetch_pages(blockIdx.x);
         have = next_item();
-        // row of this lane's box for the cursor's tile (-1: no box, -2: bad page)
+        // row of this lane's box for the cursor's tile (-1: no box, -2: page outside the
+        // pool, -3: a token-table page start that is not page-aligned)
         auto lookup = [&]() -> int {
             if (!have || !own) return -1;
             const int tb = it.t_begin + ti * kTile + lane * box;
             if (tb >= it.t_end) return -1;
             if (p.layout == PKV_LAYOUT_VARLEN) return static_cast<int>(it.base + tb);
+            if (p.layout == PKV_LAYOUT_REQ_TO_TOKEN) {
+                const int64_t s = slot_of(p, it.base, tb);   // tb starts a box, inside one page
+                return s == -2 ? -3 : s < 0 ? -2 : static_cast<int>(s);
+            }
             const int32_t *tab = p.layout == PKV_LAYOUT_CSR ? p.kv_indices : p.block_table;
             const int page = __ldg(tab + it.base + (tb >> p.ps_shift));
             if (page < 0 || page >= p.num_pages) return -2;
@@ -760,8 +971,8 @@ decode_tma_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const
             if (lane == 0) ok = wait_or_abort(&empty[s], ((n / S) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) break;
-            if (row == -2) {   // a page outside the pool reads as zeros (and raises the flag)
-                raise_flag(p.err, PKV_DEVERR_RANGE);
+            if (row <= -2) {   // a bad page reads as zeros (and raises the flag)
+                raise_flag(p.err, row == -2 ? PKV_DEVERR_RANGE : PKV_DEVERR_CONTIG);
                 unsigned char *kst = smem + s * T::kStageBytes;
                 for (int h = 0; h < T::kSlabs; ++h)
                     for (uint32_t o = 0; o < box_bytes; o += 16) {
@@ -815,7 +1026,7 @@ decode_tma_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const
             }
             uint16_t *kt = tiles + s * 2 * T::kElems;
             uint16_t *vt = kt + T::kElems;
-            const int n_valid = it.t_end - (it.t_begin + ti * kTile);
+            const int n_valid = tile_keys(it, it.t_begin + ti * kTile);
             if (n_valid < kTile) {
                 // zero the V rows of this warp's keys past the end (stale or never loaded)
                 for (int i = lane; i < 16 * (D / 8); i += 32) {
@@ -830,6 +1041,7 @@ decode_tma_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
+        add_new_key<D, GC, MMA>(st, p, it);
         M::store(st, red_o, red_m, red_l);
         named_bar_sync(1, kThreads);
         finish_item<D, GC>(p, it, red_o, red_m, red_l);
@@ -958,9 +1170,21 @@ pkv_status validate(const pkv_decode_args *a, bool check_ptrs) {
         case PKV_LAYOUT_VARLEN:
             if (!a->cu_seqlens) return fail(PKV_ERR_INVALID_ARG, "pkv_decode: varlen layout needs cu_seqlens");
             break;
+        case PKV_LAYOUT_REQ_TO_TOKEN:
+            if (!a->req_to_token || !a->req_pool_idx || !a->seq_lens)
+                return fail(PKV_ERR_INVALID_ARG, "pkv_decode: token-table layout needs req_to_token, req_pool_idx, seq_lens");
+            if (a->r2t_rows < 0 || a->r2t_width < 0 || a->r2t_row_stride < a->r2t_width || a->r2t_width > INT32_MAX)
+                return fail(PKV_ERR_INVALID_ARG, "pkv_decode: bad req_to_token shape");
+            break;
         default:
             return fail(PKV_ERR_INVALID_ARG, "pkv_decode: unknown layout");
     }
+    if ((a->k_new == nullptr) != (a->v_new == nullptr))
+        return fail(PKV_ERR_INVALID_ARG, "pkv_decode: k_new and v_new go together");
+    if (a->k_new && a->layout == PKV_LAYOUT_VARLEN)
+        return fail(PKV_ERR_INVALID_ARG, "pkv_decode: the fused store needs a pool layout (not VARLEN)");
+    if (a->k_new && (!aligned(a->k_new, 16) || !aligned(a->v_new, 16)))
+        return fail(PKV_ERR_INVALID_ARG, "pkv_decode: k_new and v_new must be 16-byte aligned");
     const int64_t row = static_cast<int64_t>(a->num_kv_heads) * a->head_dim_qk;
     if (a->k_row_stride < row || a->v_row_stride < row)
         return fail(PKV_ERR_INVALID_ARG, "pkv_decode: pool row stride smaller than a row");
@@ -1126,6 +1350,17 @@ pkv_status launch(const pkv_decode_args *a, void *ws, size_t ws_bytes, int32_t *
     p.part_lse = reinterpret_cast<float *>(static_cast<char *>(ws) + pl.part_o_bytes);
     p.err = err;
     p.wait_ns = wait_limit_ns();
+    p.r2t = a->req_to_token;
+    p.req_pool_idx = a->req_pool_idx;
+    p.kv_start = a->kv_start;
+    p.r2t_rows = a->r2t_rows;
+    p.r2t_stride = a->r2t_row_stride;
+    p.r2t_width = a->r2t_width;
+    p.k_new = static_cast<const uint16_t *>(a->k_new);
+    p.v_new = static_cast<const uint16_t *>(a->v_new);
+    // the fused store writes into the caller's pools (documented: writable when k_new is set)
+    p.k_pool_w = const_cast<uint16_t *>(p.k_pool);
+    p.v_pool_w = const_cast<uint16_t *>(p.v_pool);
     // Whole pages of >= 8 keys (or contiguous rows) stream in as TMA boxes; smaller
     // pages are gathered row by row with cp.async.
     const bool tma = (a->layout == PKV_LAYOUT_VARLEN || a->page_size >= 8) && a->num_slots <= INT32_MAX;

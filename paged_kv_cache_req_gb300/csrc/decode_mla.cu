@@ -176,13 +176,20 @@ struct Cursor {
     int s, t;  // current span, next tile (index into the concatenated sequence)
 };
 
+// A row with keys enters the concatenated sequence as kSegCost stand-in tiles (the
+// cost of starting a segment: loading its q, the pipeline's refill, the epilogue)
+// followed by its real tiles, so that spans of equal length also even out the
+// segment starts a pair makes.  Stand-in tiles produce no work.
+constexpr int kSegCost = 4;
+
 __device__ __forceinline__ int row_tiles(const Params &p, int v, bool report) {
     int64_t base;
     const int L = key_count(p, v / p.hgroups, base, report);
-    return (L + kTile - 1) / kTile;
+    return L > 0 ? (L + kTile - 1) / kTile + kSegCost : 0;
 }
 
-// R[v] = first tile of row v, R[V] = total tiles; every CTA builds the same table.
+// R[v] = first tile (stand-ins included) of row v, R[V] = total; every CTA builds
+// the same table.
 __device__ __forceinline__ void build_row_table(const Params &p, int V, int *R, int *scratch, bool report) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int seg = (V + kThreads - 1) / kThreads;
@@ -207,29 +214,36 @@ __device__ __forceinline__ void build_row_table(const Params &p, int V, int *R, 
     __syncthreads();
 }
 
-// The next segment of this pair's spans (false when there is none left).
+// The next segment of this pair's spans (false when there is none left).  A
+// segment is the real tiles of one row inside one span; a span that holds only
+// stand-in tiles of a row holds no segment of it.  A split segment's partial goes to
+// slot 0 of its span when it is the span's first segment (its row began at or
+// before the span's first tile), else to slot 1.
 __device__ __forceinline__ bool next_seg(const Params &p, const int *R, int V, int per, int S, int npairs, Cursor &c,
                                          Seg &g) {
     const int T = R[V];
     while (c.s < S) {
         const int s_begin = c.s * per;
         const int s_end = min(T, s_begin + per);
-        if (c.t < s_end) {
+        while (c.t < s_end) {
             int lo = 0, hi = V;  // R[lo] <= t < R[hi]: row lo holds tile t
             while (hi - lo > 1) {
                 const int mid = (lo + hi) >> 1;
                 if (R[mid] <= c.t) lo = mid; else hi = mid;
             }
             const int v = lo;
+            const int real0 = R[v] + kSegCost;       // the row's first real tile
+            const int t0 = max(c.t, real0);
             const int t1 = min(s_end, R[v + 1]);
+            c.t = t1;
+            if (t0 >= t1) continue;                  // only stand-in tiles of row v in this span
             g.b = v / p.hgroups;
             g.hg = v % p.hgroups;
             g.L = key_count(p, g.b, g.base, false);
-            g.key_begin = (c.t - R[v]) * kTile;
-            g.key_end = min(g.L, (t1 - R[v]) * kTile);
-            g.n_tiles = t1 - c.t;
-            g.part = (c.t == R[v] && t1 == R[v + 1]) ? -1 : c.s * 2 + (c.t == s_begin ? 0 : 1);
-            c.t = t1;
+            g.key_begin = (t0 - real0) * kTile;
+            g.key_end = min(g.L, (t1 - real0) * kTile);
+            g.n_tiles = t1 - t0;
+            g.part = (t0 == real0 && t1 == R[v + 1]) ? -1 : c.s * 2 + (R[v] <= s_begin ? 0 : 1);
             return true;
         }
         c.s += npairs;
@@ -395,6 +409,20 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
         // value slabs, 64-byte for the rope rows), one commit group per tile; a
         // tile's full barrier is arrived once its group completed and the writes are
         // fenced for the tensor cores' async proxy.  Up to two tiles stay in flight.
+        // The next segment's q (this CTA's 288 dims of 128 heads: four 128-byte lines
+        // and one rope line per head) into L2 while this segment's last tile loads, a
+        // few tiles before the softmax warps read it.  (Earlier, the streaming K/V
+        // would evict it again.)
+        auto prefetch_next_q = [&]() {
+            Cursor c2 = cur;
+            Seg nx;
+            if (!next_seg(p, R, V, per, S, npairs, c2, nx)) return;
+            const char *qb = reinterpret_cast<const char *>(p.q + (static_cast<int64_t>(nx.b) * p.hq + nx.hg * kHeads) * kDqk);
+            for (int i = lane; i < kHeads * 5; i += 32) {
+                const int h = i / 5, k = i % 5;
+                prefetch_l2(qb + h * (kDqk * 2) + (k < 4 ? slab0 * 128 + k * 128 : rope0 * 2));
+            }
+        };
         constexpr bool gather = kGather;
         uint32_t pend = 0, n_arr = 0;
         auto settle_one = [&]() {
@@ -451,12 +479,15 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
                     cp_async_commit();
                     ++pend;
                     if (pend > 2) settle_one();
+                    if (ti == it.n_tiles - 1) prefetch_next_q();
                 }
                 continue;
             }
-            for (int ti = 0; ti < kPrefetch && ti < it.n_tiles; ++ti) prefetch(ti);
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
-                if (ti + kPrefetch < it.n_tiles) prefetch(ti + kPrefetch);
+                // a segment's first tile is loaded before anything is prefetched (its
+                // page lookups are the only loads ahead of it); later tiles prefetch the
+                // tile kPrefetch ahead while they wait for a free stage
+                if (ti > 0 && ti + kPrefetch < it.n_tiles) prefetch(ti + kPrefetch);
                 const int row = box_row(ti, true);
                 const int s = n % kStages;
                 if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
@@ -484,6 +515,9 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
                         tma_load_2d(st + sl * kSlabBytes + lane * box_bytes, &tmkv, (slab0 + sl) * 64, row,
                                     &bars[kKvFull0 + s]);
                 }
+                if (ti == 0)
+                    for (int k = 1; k <= kPrefetch && k < it.n_tiles; ++k) prefetch(k);
+                if (ti == it.n_tiles - 1) prefetch_next_q();
             }
         }
         while (pend > 0) settle_one();
@@ -862,11 +896,14 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
                         o[0] = make_uint4(hh[0], hh[1], hh[2], hh[3]);
                         o[1] = make_uint4(hh[4], hh[5], hh[6], hh[7]);
                     } else {
-                        float4 *o = reinterpret_cast<float4 *>(p.part_o + prow * kDv + col);
+                        // partial layout [part][128 chunks of 4 dims][128 heads] x 16 B: a warp's
+                        // store covers 32 consecutive heads of one chunk, 512 contiguous bytes
+                        float4 *o = reinterpret_cast<float4 *>(p.part_o) +
+                                    (static_cast<int64_t>(it.part) * (kDv / 4) + col / 4) * kHeads + row;
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            o[e] = make_float4(ov[q2][4 * e] * inv, ov[q2][4 * e + 1] * inv, ov[q2][4 * e + 2] * inv,
-                                               ov[q2][4 * e + 3] * inv);
+                            o[e * kHeads] = make_float4(ov[q2][4 * e] * inv, ov[q2][4 * e + 1] * inv,
+                                                        ov[q2][4 * e + 2] * inv, ov[q2][4 * e + 3] * inv);
                     }
                 }
             }
@@ -905,19 +942,20 @@ __global__ void __launch_bounds__(256) mla_merge_kernel(const Params p, int max_
     __shared__ float den_s[16], mx_s[16];
     const int v = blockIdx.x, h0 = blockIdx.y * 16;
     const int per = p.meta[0];
-    const int r0 = p.meta[1 + v], r1 = p.meta[2 + v];
-    if (r1 <= r0 || per < 1) return;
-    const int s_first = r0 / per, s_last = (r1 - 1) / per;
+    const int r0 = p.meta[1 + v], r1 = p.meta[2 + v];   // the row's tiles, stand-ins first
+    if (r1 <= r0 + kSegCost || per < 1) return;
+    const int s_first = (r0 + kSegCost) / per, s_last = (r1 - 1) / per;
     const int n = s_last - s_first + 1;
     if (n <= 1) return;  // the row sat inside one span: the decode kernel wrote it
     if (n > max_splits) {
         if (threadIdx.x == 0 && blockIdx.y == 0) raise_flag(p.err, PKV_DEVERR_CAPACITY);
         return;
     }
-    // split i of the row is slot 1 of its span when it does not open the span
+    // split i of the row is slot 1 of its span when another row's segment opens the
+    // span (only the first split can be: its row began after the span's first tile)
     auto part = [&](int i) -> int64_t {
         const int s = s_first + i;
-        return static_cast<int64_t>(s) * 2 + ((i == 0 && r0 != s * per) ? 1 : 0);
+        return static_cast<int64_t>(s) * 2 + ((i == 0 && r0 > s * per) ? 1 : 0);
     };
     for (int i = threadIdx.x; i < 16 * n; i += blockDim.x) {
         const int h = i / n, c = i % n;
@@ -939,12 +977,13 @@ __global__ void __launch_bounds__(256) mla_merge_kernel(const Params p, int max_
     }
     __syncthreads();
     const int64_t orow0 = static_cast<int64_t>(v / p.hgroups) * p.hq + (v % p.hgroups) * kHeads + h0;
+    // partials are [part][chunk of 4 dims][head]: consecutive threads take consecutive heads
     for (int i = threadIdx.x; i < 16 * (kDv / 4); i += blockDim.x) {
-        const int h = i / (kDv / 4), d4 = i % (kDv / 4);
+        const int h = i % 16, d4 = i / 16;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int c = 0; c < n; ++c) {
             const float wgt = wsm[h * max_splits + c];
-            const float4 x = reinterpret_cast<const float4 *>(p.part_o + (part(c) * kHeads + h0 + h) * kDv)[d4];
+            const float4 x = reinterpret_cast<const float4 *>(p.part_o)[(part(c) * (kDv / 4) + d4) * kHeads + h0 + h];
             acc.x = fmaf(wgt, x.x, acc.x);
             acc.y = fmaf(wgt, x.y, acc.y);
             acc.z = fmaf(wgt, x.z, acc.z);
@@ -971,7 +1010,8 @@ struct Plan {
 static bool make_plan(const pkv_decode_args *a, Plan &pl) {
     pl.hgroups = a->num_q_heads / kHeads;
     const int64_t rows = static_cast<int64_t>(a->batch) * pl.hgroups;
-    const int64_t tiles_max = (static_cast<int64_t>(std::max(0, a->max_seq_len)) + kTile - 1) / kTile;
+    // tiles a row can take in the concatenated sequence, its stand-ins included
+    const int64_t tiles_max = (static_cast<int64_t>(std::max(0, a->max_seq_len)) + kTile - 1) / kTile + kSegCost;
     if (rows * tiles_max > INT32_MAX / 4) return false;
     int64_t spans;
     if (a->kv_chunk > 0) {
@@ -1003,6 +1043,8 @@ pkv_status validate(const pkv_decode_args *a, bool check_ptrs) {
         return fail(PKV_ERR_UNSUPPORTED, "pkv_decode(MLA): page_size must be a power of two in [1, 1024]");
     if (a->kv_chunk < 0 || a->kv_chunk % kTile)
         return fail(PKV_ERR_INVALID_ARG, "pkv_decode(MLA): kv_chunk must be a multiple of 64");
+    if (a->layout == PKV_LAYOUT_REQ_TO_TOKEN || a->k_new || a->v_new)
+        return fail(PKV_ERR_UNSUPPORTED, "pkv_decode(MLA): the token-table layout and the fused store are GQA only");
     if (a->layout != PKV_LAYOUT_CSR && a->layout != PKV_LAYOUT_BLOCK_TABLE && a->layout != PKV_LAYOUT_VARLEN)
         return fail(PKV_ERR_INVALID_ARG, "pkv_decode(MLA): unknown layout");
     if (a->k_row_stride < kDqk || a->k_row_stride % 8)

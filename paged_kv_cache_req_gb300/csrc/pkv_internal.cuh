@@ -196,6 +196,10 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int c0, 
                  "r"(c0), "r"(c1), "r"(c2)
                  : "memory");
 }
+// Bring the 128-byte line holding `p` into L2.
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -17,6 +17,12 @@ allocated on the device first, as a serving loop would:
 
 (the free list is restored before every step, so steps stay idempotent).
 
+With ``fused=True`` (GQA) the decode call reads its pages straight from
+req_to_token (PKV_LAYOUT_REQ_TO_TOKEN: no pkv_build_indices launch, no page list
+in between) and, for the problem that stores, writes the new token's K/V into
+the pool itself before attending (the fused store): a step is then one decode
+launch (+ its merge) per problem.
+
 For an encoder-decoder workload the cross-attention over the encoder region
 runs either through its own page list ("paged": the page-aligned encoder of
 "Approach 1") or through pkv_ragged_gather into a contiguous varlen buffer
@@ -66,9 +72,12 @@ def _pack(owners, device):
 class DecodeStep:
     def __init__(self, wl: Workload, device="cuda", cross_mode: str = "paged", kv_chunk: int = 0,
                  pools=None, values: Optional[Dict[str, torch.Tensor]] = None, seed: Optional[int] = None,
-                 alloc: bool = False):
+                 alloc: bool = False, fused: bool = False):
         if cross_mode not in ("paged", "gather"):
             raise ValueError(cross_mode)
+        if fused and wl.kind != "gqa":
+            raise ValueError("the token-table layout and the fused store are GQA only")
+        self.fused = bool(fused)
         self.wl = wl
         self.device = torch.device(device)
         self.cross_mode = cross_mode
@@ -123,6 +132,15 @@ class DecodeStep:
                 pb.args = B.make_decode_args(B.PKV_KIND_GQA, layout, pb.q, pb.k_rag, pb.v_rag, pb.out,
                                              sm_scale=wl.sm_scale, max_seq_len=pb.max_len,
                                              cu_seqlens=pb.cu, lse=pb.lse, kv_chunk=self.kv_chunk)
+            elif self.fused:
+                # pages straight from req_to_token; the problem that stores writes its new rows itself
+                kn, vn = (self.k_new, self.v_new) if p.stores else (None, None)
+                pb.args = B.make_decode_args(B.PKV_KIND_GQA, B.PKV_LAYOUT_REQ_TO_TOKEN, pb.q, self.k_pool,
+                                             self.v_pool, pb.out, page_size=ps, sm_scale=wl.sm_scale,
+                                             max_seq_len=pb.max_len, seq_lens=pb.seq_lens, lse=pb.lse,
+                                             kv_chunk=self.kv_chunk, req_to_token=self.r2t,
+                                             req_pool_idx=self.req_pool_idx, kv_start=pb.kv_start,
+                                             k_new=kn, v_new=vn)
             elif wl.kind == "mla":
                 pb.block_table = torch.empty((Bn, max(max_pages, 1)), dtype=torch.int32, device=dev)
                 pb.args = B.make_decode_args(B.PKV_KIND_MLA, B.PKV_LAYOUT_BLOCK_TABLE, pb.q, self.k_pool, None,
@@ -191,7 +209,7 @@ class DecodeStep:
     def build_indices(self, name: str):
         pb = self.problems[name]
         wl = self.wl
-        if pb.gather:
+        if pb.gather or self.fused:
             return
         if wl.kind == "mla":
             B.pkv_build_indices(self.r2t, self.req_pool_idx, pb.seq_lens, wl.page_size, wl.num_pool_pages,
@@ -203,6 +221,8 @@ class DecodeStep:
 
     def store(self, name: str = "self"):
         pb = self.problems[name]
+        if self.fused and not pb.gather:
+            return                                   # the decode call stores the new rows itself
         B.pkv_store(self.k_pool, self.v_pool, self.k_new, self.v_new, pb.slot_mapping, self.err)
 
     def gather(self, name: str):
@@ -231,8 +251,9 @@ class DecodeStep:
         """libpkv kernel launches one ``run()`` issues."""
         n = 2 if self.alloc else 0                  # alloc_extend + write_req_to_token
         for pb in self.problems.values():
-            n += 1                                   # gather or build_indices
-            n += 1 if pb.spec.stores else 0          # store
+            if not self.fused or pb.gather:
+                n += 1                               # gather or build_indices
+                n += 1 if pb.spec.stores else 0      # store
             n += 1 + (1 if pb.ws_bytes > 0 else 0)   # split kernel (+ merge when requests can split)
         return n
 

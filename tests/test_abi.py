@@ -82,7 +82,7 @@ def test_extend_args_layout_matches_c(binding, tmp_path):
 
 
 def test_status_strings_and_version(binding):
-    assert binding.pkv_abi_version() == 1
+    assert binding.pkv_abi_version() == 2
     assert binding.pkv_status_string(0) == "ok"
     assert binding.pkv_status_string(2) == "unsupported shape"
 
