@@ -925,11 +925,36 @@ decode_tma_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const
             for (int pg = (nx.t_begin >> p.ps_shift) + lane * step; pg <= last; pg += 32 * step)
                 prefetch_l2(p.r2t + nx.base + (static_cast<int64_t>(pg) << p.ps_shift));
         };
+        // Token table: on entering an item the warp loads the slots of all its page
+        // starts at once (lane j holds pages j, j + 32, ...; an item has at most 128
+        // pages of >= 8 keys when pieces are <= 1024 keys), so a tile's lookup is a
+        // register shuffle instead of a load that would wait on L2 one tile ahead.
+        constexpr int kBatch = 4;
+        int firsts[kBatch];
+        int pg0 = 0;
+        bool batched = false;
+        auto load_firsts = [&]() {
+            const int npg = ((it.t_end - 1) >> p.ps_shift) - (it.t_begin >> p.ps_shift) + 1;
+            batched = p.layout == PKV_LAYOUT_REQ_TO_TOKEN && npg <= 32 * kBatch;
+            if (!batched) return;
+            pg0 = it.t_begin >> p.ps_shift;
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int pg = lane + 32 * k;
+                firsts[k] = pg < npg ? __ldg(p.r2t + it.base + (static_cast<int64_t>(pg0 + pg) << p.ps_shift)) : -1;
+            }
+        };
         auto next_item = [&]() {
             while (w < total) {
                 it = locate<GC>(p, off, w, false);
                 if (it.t_end > it.t_begin) {
+                    // the item's q rows into L2 a few tiles before the math warps load them
+                    constexpr int kQLines = (GC * D * 2 + 127) / 128;
+                    if (lane < kQLines)
+                        prefetch_l2(reinterpret_cast<const char *>(p.q + (static_cast<int64_t>(it.b) * p.hq + it.head0) * D) +
+                                    lane * 128);
                     prefetch_pages(w + gridDim.x);
+                    load_firsts();
                     return true;
                 }
                 w += gridDim.x;
@@ -941,6 +966,20 @@ decode_tma_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const
         // row of this lane's box for the cursor's tile (-1: no box, -2: page outside the
         // pool, -3: a token-table page start that is not page-aligned)
         auto lookup = [&]() -> int {
+            if (have && batched) {   // warp-uniform: every lane takes part in the shuffles
+                const int tb = it.t_begin + ti * kTile + lane * box;
+                const int pi = own && tb < it.t_end ? (tb >> p.ps_shift) - pg0 : 0;
+                int first = -1;
+#pragma unroll
+                for (int k = 0; k < kBatch; ++k) {
+                    const int v = __shfl_sync(0xffffffffu, firsts[k], pi & 31);
+                    if ((pi >> 5) == k) first = v;
+                }
+                if (!own || tb >= it.t_end) return -1;
+                if (first < 0 || first >= (p.num_pages << p.ps_shift)) return -2;
+                if (first & p.ps_mask) return -3;
+                return first + (tb & p.ps_mask);
+            }
             if (!have || !own) return -1;
             const int tb = it.t_begin + ti * kTile + lane * box;
             if (tb >= it.t_end) return -1;
