@@ -708,10 +708,13 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
             // rounded to fp16 (unscaled: the scale is applied in the exponent), as 8
             // half2 in nxt[].  Both CTAs round their own partial the same way, so own
             // + peer is bitwise identical in the two CTAs.  (Macros rather than
-            // lambdas keep the arrays in registers.)
+            // lambdas keep the arrays in registers.)  The exchange barrier of tile t
+            // is armed only while the warp is live: once the CTA gave up, the tiles it
+            // skips must not arrive again on a phase still waiting for bytes that
+            // will never come.
 #define PKV_MLA_FETCH_ISSUE(t)                                                                                   \
     do {                                                                                                       \
-        if (tid == 0) mbar_arrive_expect_tx(&bars[kXFull0 + (t) % kXSlots], kXBytes);                          \
+        if (tid == 0 && ok) mbar_arrive_expect_tx(&bars[kXFull0 + (t) % kXSlots], kXBytes);                    \
         ok = warp_wait(ok, &bars[kSFull0 + ((t) & 1)], ((t) >> 1) & 1, abort_flag, p.err, p.wait_ns);                     \
         if (ok) {                                                                                              \
             tc05::fence_after_sync();                                                                          \
@@ -925,6 +928,16 @@ mla_decode_kernel(const Params p, const __grid_constant__ CUtensorMap tmkv, cons
     // ---------------------------------------------------------------- teardown
     tc05::fence_before_sync();
     __syncthreads();
+    cluster_sync_all();   // both CTAs have issued everything they will issue
+    // In a launch that gave up (either CTA), a partial score the peer sent with st.async
+    // before it stopped may not have been waited for: give such stores time to land
+    // before either CTA releases its shared memory.  (Every send is waited for
+    // otherwise.)
+    if (*abort_flag || ld_cluster_s32(mapa(smem_u32(const_cast<int *>(abort_flag)), peer)) != 0) {
+        const uint64_t t0 = global_ns();
+        while (global_ns() - t0 < 20000ull) {
+        }
+    }
     cluster_sync_all();   // the peer no longer touches this CTA's shared memory
     if (warp == kMmaWarp) {
         tc05::fence_after_sync();

@@ -249,6 +249,12 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, flo
                  "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
                  : "memory");
 }
+// 32-bit load from another CTA's shared memory (a cluster address from mapa).
+__device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
+    int v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];\n" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }

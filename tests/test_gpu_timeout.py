@@ -56,3 +56,40 @@ def test_gqa_tma_decode_gives_up_and_the_next_call_is_correct(B):
     from paged_kv_cache_req_gb300.workloads import make_workload
     step = DecodeStep(make_workload("qwen3_0p6b", batch=16), kv_chunk=256)
     _give_up_then_recover(B, step, "self", list(range(0, 16, 3)))
+
+
+def test_mla_decode_gives_up_and_the_next_call_is_correct(B):
+    """mla_decode_kernel: a 2-CTA cluster that swaps partial scores; a CTA that gives up
+    stops sending, its peer's waits run out too, and both let what was sent land
+    before releasing shared memory."""
+    from paged_kv_cache_req_gb300.engine import DecodeStep
+    from paged_kv_cache_req_gb300.workloads import make_workload
+    step = DecodeStep(make_workload("deepseek_v3_mla", batch=6), kv_chunk=1024)
+    _give_up_then_recover(B, step, "self", [0, 2, 5])
+
+
+def test_extend_gives_up_and_the_next_call_is_correct(B):
+    """ext_kernel (tcgen05, the item queue between warps, a global work counter)."""
+    from test_gpu_extend_full import _check
+    from paged_kv_cache_req_gb300.engine import ExtendStep
+    from paged_kv_cache_req_gb300.workloads import make_extend_workload
+    ew = make_extend_workload("qwen3_0p6b_prefill", batch=3)
+    step = ExtendStep(ew, device="cuda")
+    step.build_indices()
+    step.store()
+    step.plan()
+    torch.cuda.synchronize()
+    assert step.check_errors() == 0
+    B.pkv_set_wait_limit(1)
+    try:
+        step.attend()
+        torch.cuda.synchronize()          # the abandoned launch ends
+    finally:
+        B.pkv_set_wait_limit(0)
+    assert step.check_errors() & B.PKV_DEVERR_TIMEOUT
+    step.err.zero_()
+    step.out.fill_(0)
+    step.attend()                         # default limit, same stream
+    torch.cuda.synchronize()
+    assert step.check_errors() == 0
+    _check(step, [0, 2], lambda b, n: sorted(set([0, 1, n // 2, n - 1])))
