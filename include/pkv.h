@@ -153,8 +153,9 @@ typedef struct pkv_decode_args {
     int32_t page_size;         /* power of two, 1..1024 (CSR / block table); ignored for VARLEN */
     float sm_scale;            /* softmax scale, e.g. 1/sqrt(head_dim) */
     int32_t max_seq_len;       /* host upper bound on every request's key count; sizes the split plan */
-    int32_t kv_chunk;          /* keys per split, a multiple of 64; 0 lets the library choose.  MLA: keys
-                                  per span of all requests' keys taken in order (see pkv_decode) */
+    int32_t kv_chunk;          /* keys per split, a multiple of 64; 0 lets the library choose (for GQA
+                                  and small batches, equal spans; see pkv_decode).  MLA: keys per span
+                                  of all requests' keys taken in order */
     int32_t block_table_width; /* columns of block_table (BLOCK_TABLE) */
     int64_t num_slots;         /* rows of the pool(s) (VARLEN: rows of the contiguous buffer) */
     int64_t k_row_stride;      /* elements between consecutive rows of k_pool */
@@ -201,6 +202,11 @@ typedef struct pkv_decode_args {
  * MLA the keys of all requests, taken in request order in tiles of 64, are cut
  * into equal spans (kv_chunk keys each, or one span per pair of SMs when
  * kv_chunk is 0); a request that a span boundary cuts is merged the same way.
+ * For GQA with kv_chunk 0, pages of >= 8 keys (or VARLEN) and a batch so small
+ * that even max_seq_len keys per request would give each of about two spans per
+ * SM at most 128 tiles of 64 keys, the keys of each kv head's requests are cut
+ * the same way into equal spans (the same number for every kv head); the
+ * workspace size then depends on the SM count, not on the batch.
  * Arithmetic: bf16 inputs, fp32 accumulation and softmax, bf16 output rounded
  * to nearest even.
  *

@@ -8,8 +8,10 @@
 // the kv heads of one piece adjacent (they read the same pool pages) and are
 // handed out round-robin to a persistent grid of SM-count x occupancy CTAs; each
 // CTA derives the item list from the device-side lengths in its prologue, so no
-// host synchronisation is needed.  The slot of key t is
-// page_table[b][t / ps] * ps + t % ps ("From slots to a page table").
+// host synchronisation is needed.  Small batches (a few items per CTA) are cut
+// instead into equal spans of 64-key tiles (see "work items" below), with the
+// rows that a span boundary cuts combined by merge_spans_kernel.  The slot of key
+// t is page_table[b][t / ps] * ps + t % ps ("From slots to a page table").
 //
 // decode_tma_kernel (pages of >= 8 keys, and contiguous varlen rows): one producer
 // warp issues a TMA box per page and 64-dim slab (128-byte swizzle) into a ring of
@@ -48,6 +50,7 @@ struct Params {
     int32_t ps_shift, ps_mask;
     float scale_log2;
     int32_t chunk, n_chunks_max;
+    int32_t spans;      // 0: pieces of `chunk` keys dealt round-robin; else the number of equal spans
     int32_t bt_width;
     int64_t num_slots, num_pages, k_stride, v_stride, kv_indices_len;
     int32_t box_rows;   // TMA box height (keys per box)
@@ -64,6 +67,8 @@ struct Params {
     // fused store: the new token's rows (nullptr: none), written into the pools
     const uint16_t *k_new, *v_new;
     uint16_t *k_pool_w, *v_pool_w;
+    // span mode: [0] tiles per span, then one int4 per span (see SpanCut)
+    int32_t *meta;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -156,21 +161,55 @@ struct Tile {
     static constexpr int kStageBytes = 2 * kBytes;    // K + V
 };
 
-// ---------------------------------------------------------------- item table
-// off[b] = first work item of request b (exclusive scan of its item count),
-// off[B] = total.  Every CTA builds the same table from the lengths, with
-// `nthreads` threads (a multiple of 32) and one barrier id.
-__device__ __forceinline__ void build_item_table(const Params &p, int *off, int *scratch, int nthreads) {
+// ---------------------------------------------------------------- work items
+// Two ways to cut the work into items, both derived by every CTA from the
+// device-side lengths (no host synchronisation):
+//
+// Pieces (p.spans == 0): request b's keys are cut into n = ceil(L / chunk) equal
+// pieces and item (b, c, kh, hs) is piece c of kv head kh for head slice hs.  Items
+// are numbered request-major (pieces, then kv heads, then slices) and dealt
+// round-robin to the CTAs, so the items of one request run at about the same time
+// and pages that several requests share (a common prefix) are read while they are
+// still in L2.  This is the choice for large batches, where every CTA gets many
+// items and round-robin evens them out.
+//
+// Spans (p.spans = S > 0; small batches): for each unit u = (kv head kh, head
+// slice hs) the requests' rows form one sequence of 64-key tiles, each row entering
+// as kSegCost stand-in tiles (the cost of starting an item: its q, the epilogue)
+// followed by its real tiles.  Each unit's sequence is cut into S / U equal spans
+// (U units), span s = j * U + u, and CTA c takes spans c, c + grid, ...; an item
+// is the real tiles of one row inside one span.  With two or three items per
+// CTA, dealing whole pieces leaves some CTAs with half again the average work;
+// equal spans leave them within one stand-in tile of each other.  Cutting every
+// unit's sequence at the same places keeps U neighbouring CTAs on the same keys of
+// different kv heads at the same time, so the DRAM rows of a key (all kv heads side
+// by side) are read together, as in the piece order.  A row that a span
+// boundary cuts writes one fp32 partial per span: to slot 0 of its span when it is
+// the span's first item (its row began at or before the span's first tile), else
+// to slot 1 (only the span's last item can be cut there); merge_spans_kernel
+// combines them.
+constexpr int kSegCost = 1;
+
+// Work units of request b with L keys: items (pieces, all units) or tiles of one
+// unit's row (spans).
+__device__ __forceinline__ int request_units(const Params &p, int L) {
+    if (p.spans) return L > 0 ? (L + kTile - 1) / kTile + kSegCost : 0;
+    return max(1, (L + p.chunk - 1) / p.chunk) * p.hkv * p.hsplit;
+}
+
+// off[b] = first unit of request b (exclusive scan of its units), off[B] = total.
+// Every CTA builds the same table from the lengths, with `nthreads` threads (a
+// multiple of 32) and one barrier id; `report` raises the requests' range and
+// capacity flags (spans: CTA 0; pieces report as they are located).
+__device__ __forceinline__ void build_item_table(const Params &p, int *off, int *scratch, int nthreads, bool report) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int B = p.batch;
-    const int per_chunk = p.hkv * p.hsplit;
     const int seg = (B + nthreads - 1) / nthreads;
     const int lo = min(B, tid * seg), hi = min(B, lo + seg);
     int local = 0;
     for (int b = lo; b < hi; ++b) {
         int64_t base;
-        const int L = key_count(p, b, base, false);
-        local += max(1, (L + p.chunk - 1) / p.chunk) * per_chunk;
+        local += request_units(p, key_count(p, b, base, report));
     }
     int incl = local;
     for (int o = 1; o < 32; o <<= 1) {
@@ -185,44 +224,139 @@ __device__ __forceinline__ void build_item_table(const Params &p, int *off, int 
     for (int b = lo; b < hi; ++b) {
         off[b] = run;
         int64_t base;
-        const int L = key_count(p, b, base, false);
-        run += max(1, (L + p.chunk - 1) / p.chunk) * per_chunk;
+        run += request_units(p, key_count(p, b, base, false));
     }
     if (tid == nthreads - 1) off[B] = wbase + incl;
     __syncthreads();
 }
 
 struct Item {
-    int b, c, kh, hs, L, n_chunks, head0, t_begin, t_end;
+    int b, kh, hs, L, head0, t_begin, t_end;
+    int part;     // -1: the item is its row's only one and writes bf16 output; else its fp32 partial
     int64_t base;
     bool store;   // fused store: this item's keys end with the request's new token
 };
 
-template <int GC>
-__device__ __forceinline__ Item locate(const Params &p, const int *off, int w, bool report) {
-    Item it;
-    int lo = 0, hi = p.batch;  // off[lo] <= w < off[lo + 1]
+// Request holding unit w: the last b with off[b] <= w (empty requests are skipped).
+__device__ __forceinline__ int request_of(const int *off, int batch, int w) {
+    int lo = 0, hi = batch;  // off[lo] <= w < off[hi]
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
         if (off[mid] <= w) lo = mid; else hi = mid;
     }
-    it.b = lo;
-    int rem = w - off[lo];
+    return lo;
+}
+
+// Spans of one unit's sequence, and the tiles of each.
+__device__ __forceinline__ int unit_spans(const Params &p) { return p.spans / (p.hkv * p.hsplit); }
+__device__ __forceinline__ int span_tiles(const Params &p, const int *off) {
+    const int sk = unit_spans(p);
+    return max(1, (off[p.batch] + sk - 1) / sk);
+}
+
+// Pieces: item w.
+template <int GC>
+__device__ __forceinline__ Item locate(const Params &p, const int *off, int w, bool report) {
+    Item it;
+    it.b = request_of(off, p.batch, w);
+    int rem = w - off[it.b];
     it.hs = rem % p.hsplit;
     rem /= p.hsplit;
     it.kh = rem % p.hkv;
-    it.c = rem / p.hkv;
+    const int c = rem / p.hkv;
     bool clamped = false;
-    it.L = key_count(p, it.b, it.base, report && it.c == 0 && it.kh == 0 && it.hs == 0, &clamped);
-    it.n_chunks = max(1, (it.L + p.chunk - 1) / p.chunk);
+    it.L = key_count(p, it.b, it.base, report && c == 0 && it.kh == 0 && it.hs == 0, &clamped);
+    const int n_chunks = max(1, (it.L + p.chunk - 1) / p.chunk);
     it.head0 = it.kh * p.g + it.hs * GC;
     // the request's n_chunks pieces are made equal (a multiple of 64 keys, at most
     // p.chunk), so its last piece is not a stub that leaves the others waiting
-    const int span = ((it.L + it.n_chunks - 1) / it.n_chunks + kTile - 1) / kTile * kTile;
-    it.t_begin = it.c * span;
-    it.t_end = min(it.L, it.t_begin + span);
+    const int piece = ((it.L + n_chunks - 1) / n_chunks + kTile - 1) / kTile * kTile;
+    it.t_begin = c * piece;
+    it.t_end = min(it.L, it.t_begin + piece);
+    it.part = n_chunks == 1 ? -1
+                            : static_cast<int>(((static_cast<int64_t>(it.b) * p.hkv + it.kh) * p.hsplit + it.hs) *
+                                                   p.n_chunks_max + c);
     it.store = p.k_new != nullptr && !clamped && it.L > 0 && it.t_end == it.L;
     return it;
+}
+
+// A CTA's walk over its items: pieces w = blockIdx.x, + gridDim.x, ...; spans
+// s = blockIdx.x, + gridDim.x, ..., each from its first tile (w = next tile of
+// the span's unit sequence).
+struct Cursor {
+    int w, s;
+};
+
+__device__ __forceinline__ Cursor first_cursor(const Params &p, const int *off) {
+    const int c = static_cast<int>(blockIdx.x);
+    return p.spans ? Cursor{(c / (p.hkv * p.hsplit)) * span_tiles(p, off), c} : Cursor{c, 0};
+}
+
+// The CTA's next item (false when there is none left).  Pieces may be empty
+// (t_end <= t_begin: a request without keys); span items never are.
+template <int GC>
+__device__ __forceinline__ bool next_item(const Params &p, const int *off, Cursor &c, Item &it, bool report) {
+    const int total = off[p.batch];
+    if (!p.spans) {
+        if (c.w >= total) return false;
+        it = locate<GC>(p, off, c.w, report);
+        c.w += gridDim.x;
+        return true;
+    }
+    const int per = span_tiles(p, off), U = p.hkv * p.hsplit;
+    while (c.s < p.spans) {
+        const int u = c.s % U;
+        const int s_begin = (c.s / U) * per;
+        const int s_end = min(total, s_begin + per);
+        while (c.w < s_end) {
+            const int b = request_of(off, p.batch, c.w);
+            bool clamped = false;
+            int64_t base;
+            const int L = key_count(p, b, base, false, &clamped);
+            const int r0 = off[b], r1 = off[b + 1];     // the row's tiles, stand-ins first
+            const int real0 = r0 + kSegCost;
+            const int t0 = max(c.w, real0), t1 = min(s_end, r1);
+            c.w = t1;
+            if (t0 >= t1) continue;   // only stand-in tiles of this row in this span
+            it.b = b;
+            it.hs = u % p.hsplit;
+            it.kh = u / p.hsplit;
+            it.L = L;
+            it.base = base;
+            it.head0 = it.kh * p.g + it.hs * GC;
+            it.t_begin = (t0 - real0) * kTile;
+            it.t_end = min(L, (t1 - real0) * kTile);
+            it.part = (t0 == real0 && t1 == r1) ? -1 : c.s * 2 + (r0 <= s_begin ? 0 : 1);
+            it.store = p.k_new != nullptr && !clamped && it.t_end == L;
+            return true;
+        }
+        c.s += gridDim.x;
+        c.w = (c.s / U) * per;
+    }
+    return false;
+}
+
+// Span mode: what merge_spans_kernel needs about the row that the first tile of
+// span s cuts, {request, unit, first tile of the row, tiles of the row} (tiles
+// within the unit's sequence), or b = -1 when that tile cuts no row or the row was
+// already cut by an earlier span boundary (each cut row is merged once, for its
+// first cut).
+struct SpanCut {
+    int b, u, r0, rs;
+};
+
+__device__ __forceinline__ SpanCut span_cut(const Params &p, const int *off, int s) {
+    const int per = span_tiles(p, off), U = p.hkv * p.hsplit;
+    const int u = s % U, j = s / U;
+    const int x = j * per;
+    SpanCut cut{-1, 0, 0, 0};
+    if (j < 1 || x >= off[p.batch]) return cut;
+    const int b = request_of(off, p.batch, x);
+    const int r0 = off[b];
+    const int real0 = r0 + kSegCost;
+    // cut: real tiles on both sides of x; first cut: the row's first real tile lies in span j - 1
+    if (real0 < x && real0 / per == j - 1) cut = SpanCut{b, u, r0, off[b + 1] - r0};
+    return cut;
 }
 
 // Fused store of the new token (key L - 1 of the request, kv head kh): the pool rows
@@ -267,7 +401,7 @@ __device__ __forceinline__ void write_empty(const Params &p, const Item &it) {
 template <int D, int GC>
 __device__ __forceinline__ void finish_item(const Params &p, const Item &it, const float *red_o, const float *red_m,
                                             const float *red_l) {
-    const int64_t pidx = ((static_cast<int64_t>(it.b) * p.hkv + it.kh) * p.hsplit + it.hs) * p.n_chunks_max + it.c;
+    const int64_t pidx = it.part;
     for (int i = threadIdx.x; i < GC * D; i += kThreads) {
         const int h = i / D, d = i % D;
         float M = -INFINITY;
@@ -282,7 +416,7 @@ __device__ __forceinline__ void finish_item(const Params &p, const Item &it, con
             den = fmaf(red_l[ww * GC + h], sc, den);
         }
         const float val = num / den;
-        if (it.n_chunks == 1) {
+        if (it.part < 0) {
             p.out[(static_cast<int64_t>(it.b) * p.hq + it.head0 + h) * D + d] =
                 __bfloat16_as_ushort(__float2bfloat16_rn(val));
             if (d == 0 && p.lse) p.lse[static_cast<int64_t>(it.b) * p.hq + it.head0 + h] = (M + log2f(den)) * kLn2;
@@ -770,11 +904,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_cp_async_kernel(const Para
 
     pdl_wait();          // lengths, tables and pool rows may come from the previous kernel
     pdl_launch_next();
-    build_item_table(p, off, scan_scratch, kThreads);
-    const int total = off[p.batch];
+    build_item_table(p, off, scan_scratch, kThreads, false);   // pieces only (p.spans == 0)
 
-    for (int w = blockIdx.x; w < total; w += gridDim.x) {
-        const Item it = locate<GC>(p, off, w, threadIdx.x == 0);
+    Cursor cur = first_cursor(p, off);
+    Item it;
+    while (next_item<GC>(p, off, cur, it, threadIdx.x == 0)) {
         if (it.t_end <= it.t_begin) {
             write_empty<D, GC>(p, it);
             continue;
@@ -862,8 +996,11 @@ struct TmaCfg {
     static constexpr int kStagesN = D == 128 ? 3 : 5;
 };
 
+// Two CTAs per SM (the shared memory of D = 128 with up to 8 heads per group allows
+// it) put three of the pair's ten warps on one SM sub-partition, whose share of the
+// register file is 16K: hence at most 168 registers a thread there.
 template <int D, int GC, bool MMA>
-__global__ void __launch_bounds__(kThreads + 32, 1)
+__global__ void __launch_bounds__(kThreads + 32, 1) __maxnreg__((D == 128 && GC < 16) ? 168 : 255)
 decode_tma_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
     using T = Tile<D>;
     using M = Math<D, GC, MMA>;
@@ -896,8 +1033,7 @@ decode_tma_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const
     }
     pdl_wait();          // lengths, tables and pool rows may come from the previous kernel
     pdl_launch_next();
-    build_item_table(p, off, scan, kThreads + 32);
-    const int total = off[p.batch];
+    build_item_table(p, off, scan, kThreads + 32, p.spans != 0 && blockIdx.x == 0);
 
     if (warp == kWarps) {
         // ---------------- producer ----------------
@@ -909,60 +1045,65 @@ decode_tma_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const
         const uint32_t box_bytes = static_cast<uint32_t>(box) * 128u;
         const bool own = lane < nbox;
         // cursor over (item, tile), skipping empty items
-        int w = blockIdx.x, ti = 0;
+        Cursor cur = first_cursor(p, off);
+        int ti = 0;
         Item it{};
         bool have = false;
         // With the token table every page start sits in its own part of the request's
         // row, so the lookups miss L2 far more often than in a packed page list: when
         // the cursor reaches an item, the page starts of this CTA's following item are
         // pulled into L2 (one 128-byte line holds 32 positions).
-        auto prefetch_pages = [&](int wn) {
-            if (p.layout != PKV_LAYOUT_REQ_TO_TOKEN || wn >= total) return;
-            const Item nx = locate<GC>(p, off, wn, false);
-            if (nx.t_end <= nx.t_begin) return;
+        auto prefetch_pages = [&]() {
+            if (p.layout != PKV_LAYOUT_REQ_TO_TOKEN) return;
+            Cursor c2 = cur;
+            Item nx;
+            if (!next_item<GC>(p, off, c2, nx, false) || nx.t_end <= nx.t_begin) return;
             const int step = max(1, 32 >> p.ps_shift);   // pages per line
             const int last = (nx.t_end - 1) >> p.ps_shift;
             for (int pg = (nx.t_begin >> p.ps_shift) + lane * step; pg <= last; pg += 32 * step)
                 prefetch_l2(p.r2t + nx.base + (static_cast<int64_t>(pg) << p.ps_shift));
         };
-        // Token table: on entering an item the warp loads the slots of all its page
-        // starts at once (lane j holds pages j, j + 32, ...; an item has at most 128
-        // pages of >= 8 keys when pieces are <= 1024 keys), so a tile's lookup is a
-        // register shuffle instead of a load that would wait on L2 one tile ahead.
+        // Token table: the warp holds the slots of a window of 32 * kBatch page starts
+        // (lane j: pages pg0 + j, pg0 + j + 32, ...), loaded at once when the cursor
+        // enters an item and again when a tile passes the window, so a tile's lookup
+        // is a register shuffle instead of a load that would wait on L2 one tile ahead.
         constexpr int kBatch = 4;
         int firsts[kBatch];
         int pg0 = 0;
-        bool batched = false;
-        auto load_firsts = [&]() {
-            const int npg = ((it.t_end - 1) >> p.ps_shift) - (it.t_begin >> p.ps_shift) + 1;
-            batched = p.layout == PKV_LAYOUT_REQ_TO_TOKEN && npg <= 32 * kBatch;
-            if (!batched) return;
-            pg0 = it.t_begin >> p.ps_shift;
+        const bool batched = p.layout == PKV_LAYOUT_REQ_TO_TOKEN;
+        auto load_firsts = [&](int t) {   // window from the page of key t
+            pg0 = t >> p.ps_shift;
+            const int npg = ((it.t_end - 1) >> p.ps_shift) - pg0 + 1;
 #pragma unroll
             for (int k = 0; k < kBatch; ++k) {
                 const int pg = lane + 32 * k;
                 firsts[k] = pg < npg ? __ldg(p.r2t + it.base + (static_cast<int64_t>(pg0 + pg) << p.ps_shift)) : -1;
             }
         };
-        auto next_item = [&]() {
-            while (w < total) {
-                it = locate<GC>(p, off, w, false);
-                if (it.t_end > it.t_begin) {
-                    // the item's q rows into L2 a few tiles before the math warps load them
+        auto next_nonempty = [&]() {
+            Item nx;
+            while (next_item<GC>(p, off, cur, nx, false)) {
+                if (nx.t_end > nx.t_begin) {
+                    it = nx;
+                    // the item's q rows into L2 a few tiles before the math warps load them,
+                    // and with the fused store the new token's K and V rows, which warp 0
+                    // adds to its softmax state after the tile loop
                     constexpr int kQLines = (GC * D * 2 + 127) / 128;
                     if (lane < kQLines)
                         prefetch_l2(reinterpret_cast<const char *>(p.q + (static_cast<int64_t>(it.b) * p.hq + it.head0) * D) +
                                     lane * 128);
-                    prefetch_pages(w + gridDim.x);
-                    load_firsts();
+                    if (it.store && lane < 2 * (D / 64)) {
+                        const uint16_t *nrow = (lane < D / 64 ? p.k_new : p.v_new) + (static_cast<int64_t>(it.b) * p.hkv + it.kh) * D;
+                        prefetch_l2(reinterpret_cast<const char *>(nrow) + (lane % (D / 64)) * 128);
+                    }
+                    prefetch_pages();
+                    if (batched) load_firsts(it.t_begin);
                     return true;
                 }
-                w += gridDim.x;
             }
             return false;
         };
-        prefetch_pages(blockIdx.x);
-        have = next_item();
+        have = next_nonempty();
         // row of this lane's box for the cursor's tile (-1: no box, -2: page outside the
         // pool, -3: a token-table page start that is not page-aligned)
         auto lookup = [&]() -> int {
@@ -984,10 +1125,6 @@ decode_tma_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const
             const int tb = it.t_begin + ti * kTile + lane * box;
             if (tb >= it.t_end) return -1;
             if (p.layout == PKV_LAYOUT_VARLEN) return static_cast<int>(it.base + tb);
-            if (p.layout == PKV_LAYOUT_REQ_TO_TOKEN) {
-                const int64_t s = slot_of(p, it.base, tb);   // tb starts a box, inside one page
-                return s == -2 ? -3 : s < 0 ? -2 : static_cast<int>(s);
-            }
             const int32_t *tab = p.layout == PKV_LAYOUT_CSR ? p.kv_indices : p.block_table;
             const int page = __ldg(tab + it.base + (tb >> p.ps_shift));
             if (page < 0 || page >= p.num_pages) return -2;
@@ -1001,8 +1138,9 @@ decode_tma_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const
             const int n_tiles = (it.t_end - it.t_begin + kTile - 1) / kTile;
             if (++ti >= n_tiles) {
                 ti = 0;
-                w += gridDim.x;
-                have = next_item();
+                have = next_nonempty();
+            } else if (batched && ((it.t_begin + ti * kTile + kTile - 1) >> p.ps_shift) - pg0 >= 32 * kBatch) {
+                load_firsts(it.t_begin + ti * kTile);
             }
             const int next_row = lookup();
             const int s = n % S;
@@ -1045,9 +1183,28 @@ decode_tma_kernel(const Params p, const __grid_constant__ CUtensorMap tmk, const
     }
 
     // ---------------- math warps ----------------
+    if (p.spans) {
+        // rows without keys take no tiles: their outputs are written here, and the
+        // merge's view of the spans (tiles per span, the row each boundary cuts)
+        for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
+            if (off[b + 1] != off[b]) continue;
+            Item e{};
+            e.b = b;
+            for (int u = 0; u < p.hkv * p.hsplit; ++u) {
+                e.head0 = (u / p.hsplit) * p.g + (u % p.hsplit) * GC;
+                write_empty<D, GC>(p, e);
+            }
+        }
+        if (tid == 0 && blockIdx.x == 0) p.meta[0] = span_tiles(p, off);
+        for (int s = blockIdx.x + tid * gridDim.x; s < p.spans; s += gridDim.x * kThreads) {
+            const SpanCut c = span_cut(p, off, s);
+            reinterpret_cast<int4 *>(p.meta + 4)[s] = make_int4(c.b, c.u, c.r0, c.rs);
+        }
+    }
     uint32_t n = 0;
-    for (int w = blockIdx.x; w < total; w += gridDim.x) {
-        const Item it = locate<GC>(p, off, w, tid == 0);
+    Cursor cur = first_cursor(p, off);
+    Item it;
+    while (next_item<GC>(p, off, cur, it, tid == 0)) {
         if (it.t_end <= it.t_begin) {
             write_empty<D, GC>(p, it);
             continue;
@@ -1136,12 +1293,69 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const Params p) {
     }
 }
 
+// Span mode: log-sum-exp merge of the rows cut by span boundaries, one CTA per
+// span s (the row whose first cut is the span's first tile; see span_cut).  The
+// row's real tiles lie in spans s - 1 .. of its unit; its item in span s - 1 wrote
+// slot 1 of that span when another row opened the span, every later one slot 0.
+template <int D, int GC>
+__global__ void __launch_bounds__(kThreads) merge_spans_kernel(const Params p) {
+    pdl_wait();          // the split kernel's partials and span records
+    pdl_launch_next();
+    extern __shared__ float wsm[];  // [GC][spans] weights
+    __shared__ float den_s[kMaxRows], mx_s[kMaxRows];
+    const int s = blockIdx.x;
+    const int4 cut = reinterpret_cast<const int4 *>(p.meta + 4)[s];
+    if (cut.x < 0) return;
+    const int b = cut.x, u = cut.y, r0 = cut.z, rs = cut.w;
+    const int per = p.meta[0];
+    const int U = p.hkv * p.hsplit;
+    const int j_first = s / U - 1, j_last = (r0 + rs - 1) / per;   // spans of the row within its unit
+    const int n = j_last - j_first + 1;
+    auto part = [&](int i) -> int64_t {
+        return static_cast<int64_t>((j_first + i) * U + u) * 2 + ((i == 0 && r0 > j_first * per) ? 1 : 0);
+    };
+    for (int i = threadIdx.x; i < GC * n; i += kThreads) {
+        const int h = i / n, c = i % n;
+        wsm[h * p.spans + c] = p.part_lse[part(c) * GC + h];
+    }
+    __syncthreads();
+    if (threadIdx.x < GC) {
+        const int h = threadIdx.x;
+        float M = -INFINITY;
+        for (int c = 0; c < n; ++c) M = fmaxf(M, wsm[h * p.spans + c]);
+        float den = 0.f;
+        for (int c = 0; c < n; ++c) {
+            const float wgt = ex2(wsm[h * p.spans + c] - M);
+            wsm[h * p.spans + c] = wgt;
+            den += wgt;
+        }
+        den_s[h] = den;
+        mx_s[h] = M;
+    }
+    __syncthreads();
+    const int head0 = (u / p.hsplit) * p.g + (u % p.hsplit) * GC;
+    for (int i = threadIdx.x; i < GC * D; i += kThreads) {
+        const int h = i / D, d = i % D;
+        float acc = 0.f;
+        for (int c = 0; c < n; ++c) acc = fmaf(wsm[h * p.spans + c], p.part_o[(part(c) * GC + h) * D + d], acc);
+        acc /= den_s[h];
+        p.out[(static_cast<int64_t>(b) * p.hq + head0 + h) * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+        if (d == 0 && p.lse) p.lse[static_cast<int64_t>(b) * p.hq + head0 + h] = (mx_s[h] + log2f(den_s[h])) * kLn2;
+    }
+}
+
 // ------------------------------------------------------------------ host side
 struct Plan {
-    bool mma;
+    bool mma, tma;
     int gc, hsplit, chunk, n_chunks_max;
-    size_t part_o_bytes, part_lse_bytes;
+    int spans;   // 0: pieces
+    size_t part_o_bytes, part_lse_bytes, meta_bytes;
+    size_t bytes() const { return part_o_bytes + part_lse_bytes + meta_bytes; }
 };
+
+// Equal spans replace round-robin pieces when even the longest possible requests
+// would give each span at most this many tiles (a few items per CTA).
+constexpr int64_t kSpanTilesMax = 128;
 
 static int choose_chunk(const pkv_decode_args *a, int units) {
     // Fewest equal chunks of the longest request (each a multiple of 64 keys, at most
@@ -1170,7 +1384,23 @@ static pkv_status make_plan(const pkv_decode_args *a, Plan &pl) {
     pl.hsplit = g / pl.gc;
     pl.chunk = a->kv_chunk > 0 ? a->kv_chunk : choose_chunk(a, a->num_kv_heads * pl.hsplit);
     pl.n_chunks_max = std::max(1, (a->max_seq_len + pl.chunk - 1) / pl.chunk);
-    if (pl.n_chunks_max == 1) {
+    // Whole pages of >= 8 keys (or contiguous rows) stream in as TMA boxes; smaller
+    // pages are gathered row by row with cp.async.
+    pl.tma = (a->layout == PKV_LAYOUT_VARLEN || a->page_size >= 8) && a->num_slots <= INT32_MAX;
+    // Spans (TMA kernel, library-chosen split): about two per SM whatever the
+    // occupancy, the same number for every unit (kv head, head slice).
+    const int64_t units = static_cast<int64_t>(a->num_kv_heads) * pl.hsplit;
+    const int64_t spans = units * (2ll * std::max(1, sm_count()) / units);
+    const int64_t tiles_ub = static_cast<int64_t>(a->batch) * units * ((a->max_seq_len + kTile - 1) / kTile + kSegCost);
+    pl.spans = (pl.tma && a->kv_chunk == 0 && a->batch > 0 && spans > 0 && tiles_ub <= kSpanTilesMax * spans)
+                   ? static_cast<int>(spans) : 0;
+    pl.meta_bytes = 0;
+    if (pl.spans) {
+        const int64_t parts = 2 * spans * pl.gc;   // two slots per span
+        pl.part_o_bytes = (static_cast<size_t>(parts) * a->head_dim_v * 4 + 255) / 256 * 256;
+        pl.part_lse_bytes = (static_cast<size_t>(parts) * 4 + 255) / 256 * 256;
+        pl.meta_bytes = (static_cast<size_t>(spans + 1) * 16 + 255) / 256 * 256;
+    } else if (pl.n_chunks_max == 1) {
         pl.part_o_bytes = pl.part_lse_bytes = 0;
     } else {
         const int64_t parts = static_cast<int64_t>(a->batch) * a->num_kv_heads * pl.hsplit * pl.n_chunks_max * pl.gc;
@@ -1236,7 +1466,7 @@ pkv_status validate(const pkv_decode_args *a, bool check_ptrs) {
 size_t workspace_size(const pkv_decode_args *a) {
     Plan pl;
     make_plan(a, pl);
-    return pl.part_o_bytes + pl.part_lse_bytes;
+    return pl.bytes();
 }
 
 // Opt-in dynamic shared memory of a kernel (device limit minus its static part), set once.
@@ -1272,12 +1502,17 @@ template <typename K>
 static int persistent_grid(K kernel, int threads, size_t smem, const Params &p) {
     int occ = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, smem) != cudaSuccess || occ < 1) occ = 1;
-    const int64_t upper = static_cast<int64_t>(p.batch) * p.hkv * p.hsplit * p.n_chunks_max;
+    const int64_t upper = p.spans ? p.spans : static_cast<int64_t>(p.batch) * p.hkv * p.hsplit * p.n_chunks_max;
     return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(upper, static_cast<int64_t>(sm_count()) * occ)));
 }
 
 template <int D, int GC>
 static pkv_status launch_merge(const Params &p, cudaStream_t s) {
+    if (p.spans) {
+        const size_t msmem = static_cast<size_t>(GC) * p.spans * 4;   // at most 16 x 2 x SMs weights
+        return launch_status(launch_chained(merge_spans_kernel<D, GC>, dim3(p.spans), dim3(kThreads), msmem, s, p),
+                             "pkv_decode(GQA span merge kernel)");
+    }
     if (p.n_chunks_max == 1) return PKV_OK;
     const size_t msmem = static_cast<size_t>(GC) * p.n_chunks_max * 4;
     if (msmem > 200 * 1024) return fail(PKV_ERR_UNSUPPORTED, "pkv_decode: too many splits for the merge");
@@ -1347,12 +1582,12 @@ static pkv_status launch_d(const Plan &pl, const Params &p, const pkv_decode_arg
 pkv_status launch(const pkv_decode_args *a, void *ws, size_t ws_bytes, int32_t *err, cudaStream_t s) {
     Plan pl;
     make_plan(a, pl);
-    if (ws_bytes < pl.part_o_bytes + pl.part_lse_bytes)
-        return fail(PKV_ERR_CAPACITY, "pkv_decode: workspace of %zu bytes, %zu needed", ws_bytes,
-                    pl.part_o_bytes + pl.part_lse_bytes);
-    if (pl.part_o_bytes && (!ws || !aligned(ws, 256)))
+    if (ws_bytes < pl.bytes())
+        return fail(PKV_ERR_CAPACITY, "pkv_decode: workspace of %zu bytes, %zu needed", ws_bytes, pl.bytes());
+    if (pl.bytes() && (!ws || !aligned(ws, 256)))
         return fail(PKV_ERR_INVALID_ARG, "pkv_decode: workspace must be non-null and 256-byte aligned");
-    if (static_cast<int64_t>(pl.chunk) * pl.n_chunks_max > INT32_MAX / 2)
+    if (static_cast<int64_t>(pl.chunk) * pl.n_chunks_max > INT32_MAX / 2 ||
+        static_cast<int64_t>(a->batch) * a->num_kv_heads * pl.hsplit * pl.n_chunks_max > INT32_MAX)
         return fail(PKV_ERR_UNSUPPORTED, "pkv_decode: max_seq_len too large");
     Params p{};
     p.layout = a->layout;
@@ -1387,6 +1622,8 @@ pkv_status launch(const pkv_decode_args *a, void *ws, size_t ws_bytes, int32_t *
     p.lse = a->lse;
     p.part_o = static_cast<float *>(ws);
     p.part_lse = reinterpret_cast<float *>(static_cast<char *>(ws) + pl.part_o_bytes);
+    p.spans = pl.spans;
+    p.meta = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + pl.part_o_bytes + pl.part_lse_bytes);
     p.err = err;
     p.wait_ns = wait_limit_ns();
     p.r2t = a->req_to_token;
@@ -1400,9 +1637,7 @@ pkv_status launch(const pkv_decode_args *a, void *ws, size_t ws_bytes, int32_t *
     // the fused store writes into the caller's pools (documented: writable when k_new is set)
     p.k_pool_w = const_cast<uint16_t *>(p.k_pool);
     p.v_pool_w = const_cast<uint16_t *>(p.v_pool);
-    // Whole pages of >= 8 keys (or contiguous rows) stream in as TMA boxes; smaller
-    // pages are gathered row by row with cp.async.
-    const bool tma = (a->layout == PKV_LAYOUT_VARLEN || a->page_size >= 8) && a->num_slots <= INT32_MAX;
+    const bool tma = pl.tma;
     p.box_rows = a->layout == PKV_LAYOUT_VARLEN ? kTile : std::min(a->page_size, kTile);
     return a->head_dim_qk == 128 ? launch_d<128>(pl, p, a, tma, s) : launch_d<64>(pl, p, a, tma, s);
 }

@@ -50,11 +50,15 @@ def _give_up_then_recover(B, step, name, sample):
     assert_close(bf16_to_f64(pb.out)[sample], ref, "decode after a timed-out launch")
 
 
-def test_gqa_tma_decode_gives_up_and_the_next_call_is_correct(B):
-    """decode_tma_kernel (page_size 16, GQA groups of 2 on the tensor-core path)."""
+@pytest.mark.parametrize("kv_chunk", [256, 0])
+def test_gqa_tma_decode_gives_up_and_the_next_call_is_correct(B, kv_chunk):
+    """decode_tma_kernel (page_size 16, GQA groups of 2 on the tensor-core path), with
+    the work cut into pieces of 256 keys and into equal spans (the library's choice
+    at this batch): the span merge reads only records the split kernel writes before
+    its first wait."""
     from paged_kv_cache_req_gb300.engine import DecodeStep
     from paged_kv_cache_req_gb300.workloads import make_workload
-    step = DecodeStep(make_workload("qwen3_0p6b", batch=16), kv_chunk=256)
+    step = DecodeStep(make_workload("qwen3_0p6b", batch=16), kv_chunk=kv_chunk)
     _give_up_then_recover(B, step, "self", list(range(0, 16, 3)))
 
 
