@@ -6,21 +6,26 @@
 // default the causal bound of the request's last positions).  A work item is
 // (request, kv head, block of 128 query rows, chunk of keys): the rows are the
 // (token, query head) pairs of 128 / g consecutive tokens times the g query
-// heads sharing the kv head, so every K/V tile serves the whole block.  Per CTA:
-//   warp 4     producer: K/V tiles of 64 keys through a 4-stage ring (8 at
+// heads sharing the kv head, so every K/V tile serves the whole block.  The
+// tiles of an item alternate between two softmax groups, each with its own
+// online-softmax state and accumulator, so the tensor cores run one group's
+// Q K^T and P V while the other group computes its exponentials.  Per CTA:
+//   warp 8     producer: K/V tiles of 64 keys through a 4-stage ring (8 at
 //              head_dim 64): one TMA box per page per slab, one copy per lane,
 //              pool rows looked up 32 boxes at a time; pages under 8 keys are
 //              gathered row by row with cp.async instead;
-//   warp 5     loads the q blocks (one 3-D box per 64-dim slab, rows
+//   warp 9     loads the q blocks (one 3-D box per 64-dim slab, rows
 //              token-major) into two buffers, the next item's while this one
-//              runs, and issues S = Q K^T (M = 128, N = 64) into one of two TMEM
-//              score buffers;
-//   warp 6     O += P V (N = head_dim) from one of two TMEM P buffers into one
-//              of two accumulators (items alternate);
-//   warps 0-3  one query row per thread: mask keys at or past the row's bound,
-//              online softmax (base 2, running max raised only past 2^8), P;
-//   warps 7-10 epilogue: normalise an item's O and write it while warps 0-3
-//              already run the next item.
+//              runs, and issues S = Q K^T (M = 128, N = 64) for tile n into
+//              score buffer (n mod 2, n / 2 mod 2) of TMEM;
+//   warp 10    O_g += P V (N = head_dim) for tile n into group g = n mod 2's
+//              accumulator, P read from the tile's score buffer;
+//   warps 0-7  two groups of four warps, one query row per thread: group g
+//              takes the tiles n = g mod 2: mask keys at or past the row's
+//              bound, online softmax (base 2, running max raised only past
+//              2^8), P written over the tile's scores;
+//   warps 11-14 epilogue: combine the two groups' (m, l, O) by log-sum-exp,
+//              normalise and write the item while the groups run the next.
 // Per-request values sit in shared memory (when they fit), so moving from one
 // item to the next costs no global loads.  Items whose block is cut into
 // several key chunks write fp32 (o, lse) partials that ext_merge_kernel
@@ -34,13 +39,13 @@ namespace pkv {
 namespace ext {
 
 constexpr int kRows = 128, kTile = 64;
-constexpr int kThreads = 352;              // warps 0-3 softmax, 4 producer, 5 q.k, 6 P.V, 7-10 epilogue
-constexpr int kProducerWarp = 4, kQkWarp = 5, kPvWarp = 6, kEpiWarp0 = 7;
+constexpr int kThreads = 480;              // warps 0-7 softmax (two groups), 8 producer, 9 q.k, 10 P.V, 11-14 epilogue
+constexpr int kProducerWarp = 8, kQkWarp = 9, kPvWarp = 10, kEpiWarp0 = 11;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kLog2e = 1.44269504088896341f;
 constexpr float kLazy = 8.f;
 constexpr int kRing = 8;                   // slots of the item queue
-constexpr int kItemReaders = 11;           // warps that read every queued item
+constexpr int kItemReaders = 15;           // warps that read every queued item
 
 template <int D>
 struct Cfg {
@@ -54,15 +59,14 @@ struct Cfg {
     static constexpr int kOffBar = kOffKV + kStages * kStageBytes;
     static constexpr int kNumBars = 56;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;    // tmem slot, abort flag, scan scratch
-    static constexpr int kOffStats = kOffMisc + 128;           // [2 items][128 rows] of (m, l) for the epilogue
-    static constexpr int kOffRing = kOffStats + 2 * kRows * 8; // the CTA's next items, as the producer claims them
+    static constexpr int kOffStats = kOffMisc + 128;           // [2 items][2 groups][128 rows] of (m, l) for the epilogue
+    static constexpr int kOffRing = kOffStats + 4 * kRows * 8; // the CTA's next items, as the producer claims them
     static constexpr int kOffTable = kOffRing + kRing * 64;
     static constexpr int kFixedSmem = kOffTable + 1024;        // + request tables + alignment slack
-    static constexpr uint32_t kColS = 0;                       // two 64-column score buffers
-    static constexpr uint32_t kColO = 128;                     // two D-column output accumulators
-    static constexpr uint32_t kColP = 128 + 2 * D;             // two 32-column P buffers
+    static constexpr uint32_t kColS = 0;                       // four 64-column score buffers (two per group), P over S
+    static constexpr uint32_t kColO = 256;                     // the two groups' D-column accumulators
     static constexpr uint32_t kTmemCols = 512;
-    static_assert(kColP + 64 <= kTmemCols, "tensor memory");
+    static_assert(kColO + 2 * D <= kTmemCols, "tensor memory");
 };
 
 struct Params {
@@ -332,10 +336,16 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 
 enum Bar {
     kQFull0 = 0, kQEmpty0 = 2, kKvFull0 = 4, kKvEmpty0 = kKvFull0 + 8, kSFull0 = kKvEmpty0 + 8,
-    kSFree0 = kSFull0 + 2, kPFull0 = kSFree0 + 2, kPFree0 = kPFull0 + 2, kODone0 = kPFree0 + 2, kOFree0 = kODone0 + 2,
+    kSFree0 = kSFull0 + 4, kPFull0 = kSFree0 + 4, kODone0 = kPFull0 + 4, kOFree0 = kODone0 + 2,
     kStatFull0 = kOFree0 + 2, kItemFull0 = kStatFull0 + 2, kItemEmpty0 = kItemFull0 + kRing,
     kFinalQk = kItemEmpty0 + kRing, kFinalPv, kBarCount
 };
+
+// Tile ti of an item goes to group ti mod 2 (by its place in the item, so an item's
+// result does not depend on which CTA runs it), and the group's c-th tile in the
+// CTA's sequence uses its score buffer c mod 2, so the group's Q K^T for its next
+// tile never waits for its softmax of this one; that buffer's use is c / 2.
+__device__ __forceinline__ int sbuf(int grp, uint32_t c) { return grp * 2 + static_cast<int>(c & 1); }
 
 // Item k of this CTA's sequence from the queue (w < 0: no more items, or an
 // abort).  Every reader warp takes every item once, in order, and frees its slot.
@@ -354,8 +364,10 @@ __device__ __forceinline__ Item ring_read(const Item *ring, uint64_t *bars, uint
     return it;
 }
 
+// Fifteen warps: four of them on one SM sub-partition share its 16K registers, so
+// at most 128 registers a thread.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(128)
 ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
            const __grid_constant__ CUtensorMap tmv) {
     using C = Cfg<D>;
@@ -387,13 +399,14 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars[kQFull0 + i], 1);
             mbar_init(&bars[kQEmpty0 + i], 1);
-            mbar_init(&bars[kSFull0 + i], 1);
-            mbar_init(&bars[kSFree0 + i], 4);
-            mbar_init(&bars[kPFull0 + i], 4);
-            mbar_init(&bars[kPFree0 + i], 1);
             mbar_init(&bars[kODone0 + i], 1);
             mbar_init(&bars[kOFree0 + i], 4);
-            mbar_init(&bars[kStatFull0 + i], 4);
+            mbar_init(&bars[kStatFull0 + i], 8);
+        }
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&bars[kSFull0 + i], 1);   // q.k done
+            mbar_init(&bars[kSFree0 + i], 1);   // the P V that read P over these scores done
+            mbar_init(&bars[kPFull0 + i], 4);   // the group's four warps stored P
         }
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bars[kKvFull0 + s], 1);
@@ -608,7 +621,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             __syncwarp();
             if (ok) ++q_issued;
         };
-        uint32_t kr = 0;
+        uint32_t kr = 0, c0 = 0, c1 = 0;   // tiles issued per group
         Item it = ring_read(ring, bars, kr++, ok, abort_flag, p.err, p.wait_ns);
         bool q_req = false;   // it's q block already requested
         while (it.w >= 0 && ok) {
@@ -619,9 +632,11 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                 const int sl = iq & 1;
                 ok = warp_wait(ok, &bars[kQFull0 + sl], (iq >> 1) & 1, abort_flag, p.err, p.wait_ns);
                 for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
-                    const int s = n % kStages;
+                    const int g = ti & 1;
+                    const uint32_t c = g ? c1++ : c0++;
+                    const int s = n % kStages, sb = sbuf(g, c);
                     ok = warp_wait(ok, &bars[kKvFull0 + s], (n / kStages) & 1, abort_flag, p.err, p.wait_ns);
-                    ok = warp_wait(ok, &bars[kSFree0 + (n & 1)], ((n >> 1) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
+                    ok = warp_wait(ok, &bars[kSFree0 + sb], ((c >> 1) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
                     if (!ok) break;
                     tc05::fence_after_sync();
                     if (lane == 0) {
@@ -631,11 +646,11 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                         for (int k2 = 0; k2 < C::kSl; ++k2)
     #pragma unroll
                             for (int k = 0; k < 4; ++k)   // slab: q +16 KB, K +8 KB; k-step +32 bytes
-                                tc05::mma_ss(tbase + C::kColS + (n & 1) * kTile,
+                                tc05::mma_ss(tbase + C::kColS + sb * kTile,
                                              qd + static_cast<uint64_t>((k2 * kRows * 128 + k * 32) >> 4),
                                              kd + static_cast<uint64_t>((k2 * kTile * 128 + k * 32) >> 4), idesc,
                                              (k2 | k) ? 1u : 0u);
-                        tc05::commit(&bars[kSFull0 + (n & 1)]);
+                        tc05::commit(&bars[kSFull0 + sb]);
                         if (ti == it.n_tiles - 1) tc05::commit(&bars[kQEmpty0 + sl]);
                     }
                     __syncwarp();
@@ -657,19 +672,22 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
         }
         __syncwarp();
     } else if (warp == kPvWarp) {
-        // ------------------------------------------------------------ O += P V
-        // Items alternate between two accumulators, so an item's first P V does not
-        // wait for the previous item's epilogue.
+        // ------------------------------------------------------------ O_g += P V
+        // Tile ti goes to group ti mod 2's accumulator.  An item's first two tiles (one
+        // per group) start their accumulators afresh, once the epilogue has read the
+        // previous item's.
         const uint32_t idesc = tc05::idesc_bf16_f32(kRows, D, false, true);
-        uint32_t n = 0, io = 0;
+        uint32_t n = 0, io = 0, c0 = 0, c1 = 0;   // tiles per group
         bool ok = true;
         for (uint32_t k = 0; ok; ++k) {
             const Item it = ring_read(ring, bars, k, ok, abort_flag, p.err, p.wait_ns);
             if (it.w < 0) break;
             if (it.n_tiles == 0) continue;
-            const int ko = io & 1;
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
-                ok = warp_wait(ok, &bars[kPFull0 + (n & 1)], (n >> 1) & 1, abort_flag, p.err, p.wait_ns);
+                const int g = ti & 1;
+                const uint32_t c = g ? c1++ : c0++;
+                const int sb = sbuf(g, c);
+                ok = warp_wait(ok, &bars[kPFull0 + sb], (c >> 1) & 1, abort_flag, p.err, p.wait_ns);
                 if (!ok) break;
                 unsigned char *v = sKV + (n % kStages) * C::kStageBytes + C::kKBytes;
                 const int n_valid = it.k1 - (it.k0 + ti * kTile);
@@ -682,19 +700,20 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
-                if (ti == 0) ok = warp_wait(ok, &bars[kOFree0 + ko], ((io >> 1) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
+                if (ti == 0 && io > 0)
+                    ok = warp_wait(ok, &bars[kOFree0 + ((io - 1) & 1)], ((io - 1) >> 1) & 1, abort_flag, p.err, p.wait_ns);
                 if (!ok) break;
                 tc05::fence_after_sync();
                 if (lane == 0) {
                     const uint64_t vd = tc05::smem_desc(v, kTile * 128, 1024);
 #pragma unroll
                     for (int k = 0; k < kTile / 16; ++k)   // 16 keys: +2048 bytes of V, +8 columns of P
-                        tc05::mma_ts(tbase + C::kColO + ko * D, tbase + C::kColP + (n & 1) * 32 + k * 8,
+                        tc05::mma_ts(tbase + C::kColO + g * D, tbase + C::kColS + sb * kTile + k * 8,
                                      vd + static_cast<uint64_t>((k * 2048) >> 4), idesc,
-                                     (ti == 0 && k == 0) ? 0u : 1u);
-                    tc05::commit(&bars[kPFree0 + (n & 1)]);
+                                     (ti < 2 && k == 0) ? 0u : 1u);
+                    tc05::commit(&bars[kSFree0 + sb]);
                     tc05::commit(&bars[kKvEmpty0 + n % kStages]);
-                    if (ti == it.n_tiles - 1) tc05::commit(&bars[kODone0 + ko]);
+                    if (ti == it.n_tiles - 1) tc05::commit(&bars[kODone0 + (io & 1)]);
                 }
                 __syncwarp();
             }
@@ -707,9 +726,12 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
         __syncwarp();
     } else if (warp >= kEpiWarp0) {
         // ------------------------------------------------------------ epilogue (one row per thread)
-        // Normalises an item's O once its last P V is done and the softmax warps have
-        // left the row's (m, l), writes the bf16 row (or the fp32 split partial) and
-        // frees the accumulator, while the softmax warps already run the next item.
+        // Once an item's last P V is done and both groups have left the row's (m, l),
+        // combines the groups: o = (2^(mA - M) OA + 2^(mB - M) OB) / (2^(mA - M) lA +
+        // 2^(mB - M) lB) with M = max(mA, mB), writes the bf16 row (or the fp32 split
+        // partial) and frees the accumulators, while the groups already run the next
+        // item.  A group without keys in the item (l = 0) is left out: its
+        // accumulator was not written for this item.
         const int quarter = warp & 3;                 // TMEM lanes this warp may read
         const int r = quarter * 32 + lane;
         const uint32_t trow = tc05::taddr(tbase, quarter * 32, 0);
@@ -722,37 +744,47 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             if (it.n_tiles == 0) continue;
             const int ko = io & 1;
             ok = warp_wait(ok, &bars[kStatFull0 + ko], (io >> 1) & 1, abort_flag, p.err, p.wait_ns);
-            const float2 ml = stats[ko * kRows + r];
+            const float2 sa = stats[(ko * 2) * kRows + r], sb2 = stats[(ko * 2 + 1) * kRows + r];
             ok = warp_wait(ok, &bars[kODone0 + ko], (io >> 1) & 1, abort_flag, p.err, p.wait_ns);
             tc05::fence_after_sync();
+            const float M = fmaxf(sa.x, sb2.x);
+            const float wa = sa.y > 0.f ? ex2(sa.x - M) : 0.f, wb = sb2.y > 0.f ? ex2(sb2.x - M) : 0.f;
+            const float den = sa.y * wa + sb2.y * wb;
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+            const float ca = wa * inv, cb2 = wb * inv;
             const int tq = it.qblk * p.T + tok;
             const bool valid = tq < it.n;
             const int64_t qrow = static_cast<int64_t>(it.qo0) + tq;
             const int head = it.kh * p.g + hh;
             const bool single = it.nch == 1;
             const int64_t prow = it.w * kRows + r;
-            const float inv = ml.y > 0.f ? 1.f / ml.y : 0.f;
 #pragma unroll 1
-            for (int cb = 0; cb < D / 16; cb += 4) {
-                float ov[4][16];
+            for (int cb = 0; cb < D / 16; cb += 2) {
+                float oa[2][16], ob[2][16];
                 if (ok) {
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) tc05::ld_x16(trow + C::kColO + ko * D + (cb + q4) * 16, ov[q4]);
+                    for (int q2 = 0; q2 < 2; ++q2) {
+                        tc05::ld_x16(trow + C::kColO + (cb + q2) * 16, oa[q2]);
+                        tc05::ld_x16(trow + C::kColO + D + (cb + q2) * 16, ob[q2]);
+                    }
                     tc05::wait_ld();
-                } else {
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) ov[q4][e] = 0.f;
                 }
                 if (valid) {
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        const int col = (cb + q4) * 16;
+                    for (int q2 = 0; q2 < 2; ++q2) {
+                        float ov[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            // selects, not products: an accumulator left out may hold anything
+                            const float xa = ok && wa != 0.f ? oa[q2][e] * ca : 0.f;
+                            const float xb = ok && wb != 0.f ? ob[q2][e] * cb2 : 0.f;
+                            ov[e] = xa + xb;
+                        }
+                        const int col = (cb + q2) * 16;
                         if (single) {
                             uint32_t h2[8];
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) h2[e] = pack_bf16x2(ov[q4][2 * e] * inv, ov[q4][2 * e + 1] * inv);
+                            for (int e = 0; e < 8; ++e) h2[e] = pack_bf16x2(ov[2 * e], ov[2 * e + 1]);
                             uint4 *o = reinterpret_cast<uint4 *>(p.out + (qrow * p.hq + head) * D + col);
                             o[0] = make_uint4(h2[0], h2[1], h2[2], h2[3]);
                             o[1] = make_uint4(h2[4], h2[5], h2[6], h2[7]);
@@ -760,14 +792,13 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                             float4 *o = reinterpret_cast<float4 *>(p.part_o + prow * D + col);
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
-                                o[e] = make_float4(ov[q4][4 * e] * inv, ov[q4][4 * e + 1] * inv,
-                                                   ov[q4][4 * e + 2] * inv, ov[q4][4 * e + 3] * inv);
+                                o[e] = make_float4(ov[4 * e], ov[4 * e + 1], ov[4 * e + 2], ov[4 * e + 3]);
                         }
                     }
                 }
             }
             if (valid) {
-                const float lse2 = ml.y > 0.f ? ml.x + log2f(ml.y) : -INFINITY;
+                const float lse2 = den > 0.f ? M + log2f(den) : -INFINITY;
                 if (single) {
                     if (p.lse) p.lse[qrow * p.hq + head] = lse2 * kLn2;
                 } else {
@@ -781,10 +812,13 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
         }
     } else {
         // ------------------------------------------------------------ softmax (one row per thread)
-        const int r = warp * 32 + lane;
-        const uint32_t trow = tc05::taddr(tbase, warp * 32, 0);
+        // Group grp = warp / 4 takes the tiles ti of each item with ti mod 2 = grp,
+        // keeping its own (m, l) and accumulator; warp w reads TMEM lanes 32 (w mod 4) ...
+        const int grp = warp >> 2, quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const uint32_t trow = tc05::taddr(tbase, quarter * 32, 0);
         const int tok = r >> p.g_shift, hh = r & (p.g - 1);
-        uint32_t n = 0, io = 0;
+        uint32_t io = 0, c = 0;   // items, and this group's tiles so far
         bool ok = true;
         // the row's key bound; its load for the next item is issued an item early
         auto row_bound = [&](const Item &qi) -> int {
@@ -809,7 +843,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             const int head = it.kh * p.g + hh;
             float m = -INFINITY, l = 0.f;
             if (it.n_tiles == 0) {   // no keys: out = 0, lse = -inf
-                if (valid && it.nch == 1) {
+                if (grp == 0 && valid && it.nch == 1) {
                     uint4 *o = reinterpret_cast<uint4 *>(p.out + (qrow * p.hq + head) * D);
                     for (int i = 0; i < D / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
                     if (p.lse) p.lse[qrow * p.hq + head] = -INFINITY;
@@ -819,23 +853,21 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                 continue;
             }
             const int ko = io & 1;
-            for (int ti = 0; ti < it.n_tiles; ++ti, ++n) {
+            for (int ti = grp; ti < it.n_tiles; ti += 2, ++c) {   // this group's tiles
+                const int sb = sbuf(grp, c);
                 const int key0 = it.k0 + ti * kTile;
                 // rows past the block's tokens are never written: they only mask the
                 // keys past the chunk (stale data), which keeps full tiles select-free
                 const int vis = max(0, min(min(valid ? kend : it.k1, it.k1) - key0, kTile));
-                ok = warp_wait(ok, &bars[kSFull0 + (n & 1)], (n >> 1) & 1, abort_flag, p.err, p.wait_ns);
+                ok = warp_wait(ok, &bars[kSFull0 + sb], (c >> 1) & 1, abort_flag, p.err, p.wait_ns);
                 float x[64];
                 if (ok) {
                     tc05::fence_after_sync();
-                    tc05::ld_x64(trow + C::kColS + (n & 1) * kTile, x);
+                    tc05::ld_x64(trow + C::kColS + sb * kTile, x);
                 } else {
 #pragma unroll
                     for (int j = 0; j < 64; ++j) x[j] = 0.f;
                 }
-                tc05::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[kSFree0 + (n & 1)]);
                 // keys at or past the row's bound read as -inf (no selects when the
                 // whole tile is inside every row's bound); max over a tree of pairs
                 if (!__all_sync(0xffffffffu, vis == kTile)) {
@@ -858,17 +890,19 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                 const bool raise = mx > m + kLazy || (m == -INFINITY && mx != -INFINITY);
                 const float corr = raise ? ex2(m - mx) : 1.f;
                 if (__any_sync(0xffffffffu, raise && m != -INFINITY) && ok) {
-                    // O is final for tile n - 1 once its P V completed; rescale the row
-                    ok = warp_wait(ok, &bars[kPFree0 + ((n - 1) & 1)], ((n - 1) >> 1) & 1, abort_flag, p.err, p.wait_ns);
+                    // the group's accumulator is final for its previous tile (of this item:
+                    // m is finite) once that tile's P V completed; rescale the row
+                    const uint32_t cp = c - 1;
+                    ok = warp_wait(ok, &bars[kSFree0 + sbuf(grp, cp)], (cp >> 1) & 1, abort_flag, p.err, p.wait_ns);
                     tc05::fence_after_sync();
 #pragma unroll 1
                     for (int cc = 0; cc < D / 16 && ok; ++cc) {
                         float ov[16];
-                        tc05::ld_x16(trow + C::kColO + ko * D + cc * 16, ov);
+                        tc05::ld_x16(trow + C::kColO + grp * D + cc * 16, ov);
                         tc05::wait_ld();
 #pragma unroll
                         for (int e = 0; e < 16; ++e) ov[e] *= corr;
-                        tc05::st_x16(trow + C::kColO + ko * D + cc * 16, ov);
+                        tc05::st_x16(trow + C::kColO + grp * D + cc * 16, ov);
                     }
                     tc05::wait_st();
                 }
@@ -888,27 +922,25 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                     h[j] = pack_bf16x2(p0, p1);
                 }
                 l += lsum;
-                ok = warp_wait(ok, &bars[kPFree0 + (n & 1)], ((n >> 1) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
-                if (ok) {
-                    tc05::fence_after_sync();
+                if (ok) {   // P (bf16 pairs) over the first 32 columns of the scores just read
                     uint32_t h0[16], h1[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         h0[j] = h[j];
                         h1[j] = h[16 + j];
                     }
-                    tc05::st_x16_u32(trow + C::kColP + (n & 1) * 32, h0);
-                    tc05::st_x16_u32(trow + C::kColP + (n & 1) * 32 + 16, h1);
+                    tc05::st_x16_u32(trow + C::kColS + sb * kTile, h0);
+                    tc05::st_x16_u32(trow + C::kColS + sb * kTile + 16, h1);
                     tc05::wait_st();
                 }
                 tc05::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[kPFull0 + (n & 1)]);
+                if (lane == 0) mbar_arrive(&bars[kPFull0 + sb]);
             }
             // hand (m, l) to the epilogue warps; the buffer is free once they are done
-            // with the item two back (the same phase that freed its accumulator)
+            // with the item two back
             ok = warp_wait(ok, &bars[kOFree0 + ko], ((io >> 1) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
-            stats[ko * kRows + r] = make_float2(m, l);
+            stats[(ko * 2 + grp) * kRows + r] = make_float2(m, l);
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[kStatFull0 + ko]);
             ++io;
