@@ -320,7 +320,8 @@ typedef struct pkv_extend_args {
     int32_t page_size;
     float sm_scale;
     int32_t max_seq_len;       /* host upper bound on every request's key count */
-    int32_t kv_chunk;          /* keys per split (multiple of 64); 0 lets the library choose */
+    int32_t kv_chunk;          /* keys per split (multiple of 64, rounded up to whole 128-key tiles);
+                                  0 lets the library choose */
     int32_t block_table_width;
     int64_t total_q;           /* query rows: qo_indptr[B] */
     int64_t num_slots;         /* pool rows */

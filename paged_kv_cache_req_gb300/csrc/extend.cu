@@ -7,23 +7,26 @@
 // (request, kv head, block of 128 query rows, chunk of keys): the rows are the
 // (token, query head) pairs of 128 / g consecutive tokens times the g query
 // heads sharing the kv head, so every K/V tile serves the whole block.  The
-// tiles of an item alternate between two softmax groups, each with its own
-// online-softmax state and accumulator, so the tensor cores run one group's
-// Q K^T and P V while the other group computes its exponentials.  Per CTA:
-//   warp 8     producer: K/V tiles of 64 keys through a 4-stage ring (8 at
-//              head_dim 64): one TMA box per page per slab, one copy per lane,
+// two halves of each 128-key tile go to two softmax groups, each with its own
+// online-softmax state and accumulator: one Q K^T of N = 128 serves both, and
+// the tensor cores run the next tile's Q K^T and the groups' P V while the
+// groups compute their exponentials.  Per CTA:
+//   warp 8     producer: K and V tiles through rings of their own (2 stages each,
+//              4 at head_dim 64), so a K stage is refilled once its Q K^T is
+//              done: one TMA box per page per slab, one copy per lane and ring,
 //              pool rows looked up 32 boxes at a time; pages under 8 keys are
 //              gathered row by row with cp.async instead;
 //   warp 9     loads the q blocks (one 3-D box per 64-dim slab, rows
 //              token-major) into two buffers, the next item's while this one
-//              runs, and issues S = Q K^T (M = 128, N = 64) for tile n into
-//              score buffer (n mod 2, n / 2 mod 2) of TMEM;
-//   warp 10    O_g += P V (N = head_dim) for tile n into group g = n mod 2's
-//              accumulator, P read from the tile's score buffer;
+//              runs, and issues S = Q K^T (M = 128, N = 128) for tile n into
+//              one of two 128-column score buffers in TMEM;
+//   warp 10    O_g += P_g V_g (K = 64 keys, N = head_dim) for each group g:
+//              its half of the tile's keys into its own accumulator, P read
+//              from the group's half of the score buffer;
 //   warps 0-7  two groups of four warps, one query row per thread: group g
-//              takes the tiles n = g mod 2: mask keys at or past the row's
-//              bound, online softmax (base 2, running max raised only past
-//              2^8), P written over the tile's scores;
+//              takes keys 64 g ... 64 g + 63 of every tile: mask keys at or
+//              past the row's bound, online softmax (base 2, running max
+//              raised only past 2^8), P written over those scores;
 //   warps 11-14 epilogue: combine the two groups' (m, l, O) by log-sum-exp,
 //              normalise and write the item while the groups run the next.
 // Per-request values sit in shared memory (when they fit), so moving from one
@@ -38,7 +41,8 @@
 namespace pkv {
 namespace ext {
 
-constexpr int kRows = 128, kTile = 64;
+constexpr int kRows = 128, kTile = 128;   // query rows per block, keys per tile
+constexpr int kChunkUnit = 64;             // a caller's kv_chunk is a multiple of this
 constexpr int kThreads = 480;              // warps 0-7 softmax (two groups), 8 producer, 9 q.k, 10 P.V, 11-14 epilogue
 constexpr int kProducerWarp = 8, kQkWarp = 9, kPvWarp = 10, kEpiWarp0 = 11;
 constexpr float kLn2 = 0.69314718055994531f;
@@ -49,22 +53,21 @@ constexpr int kItemReaders = 15;           // warps that read every queued item
 
 template <int D>
 struct Cfg {
-    static constexpr int kStages = D == 128 ? 4 : 8;           // K/V ring depth (128 KB either way)
+    static constexpr int kStages = D == 128 ? 2 : 4;           // depth of the K ring and of the V ring (128 KB in all)
     static constexpr int kSl = D / 64;                         // 64-dim slabs
     static constexpr int kQBytes = kSl * kRows * 128;          // one q block, SW128 K-major
     static constexpr int kKBytes = kSl * kTile * 128;          // one K (or V) tile
-    static constexpr int kStageBytes = 2 * kKBytes;
     static constexpr int kOffQ = 0;                            // two q blocks: this item's and the next
-    static constexpr int kOffKV = kOffQ + 2 * kQBytes;
-    static constexpr int kOffBar = kOffKV + kStages * kStageBytes;
+    static constexpr int kOffKV = kOffQ + 2 * kQBytes;         // K ring, then V ring
+    static constexpr int kOffBar = kOffKV + 2 * kStages * kKBytes;
     static constexpr int kNumBars = 56;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;    // tmem slot, abort flag, scan scratch
     static constexpr int kOffStats = kOffMisc + 128;           // [2 items][2 groups][128 rows] of (m, l) for the epilogue
     static constexpr int kOffRing = kOffStats + 4 * kRows * 8; // the CTA's next items, as the producer claims them
     static constexpr int kOffTable = kOffRing + kRing * 64;
     static constexpr int kFixedSmem = kOffTable + 1024;        // + request tables + alignment slack
-    static constexpr uint32_t kColS = 0;                       // four 64-column score buffers (two per group), P over S
-    static constexpr uint32_t kColO = 256;                     // the two groups' D-column accumulators
+    static constexpr uint32_t kColS = 0;                       // two 128-column score buffers (a 64-column half per group), P over S
+    static constexpr uint32_t kColO = 2 * kTile;               // the two groups' D-column accumulators
     static constexpr uint32_t kTmemCols = 512;
     static_assert(kColO + 2 * D <= kTmemCols, "tensor memory");
 };
@@ -335,17 +338,18 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 }
 
 enum Bar {
-    kQFull0 = 0, kQEmpty0 = 2, kKvFull0 = 4, kKvEmpty0 = kKvFull0 + 8, kSFull0 = kKvEmpty0 + 8,
-    kSFree0 = kSFull0 + 4, kPFull0 = kSFree0 + 4, kODone0 = kPFull0 + 4, kOFree0 = kODone0 + 2,
+    kQFull0 = 0, kQEmpty0 = 2, kKFull0 = 4, kKEmpty0 = kKFull0 + 4, kVFull0 = kKEmpty0 + 4, kVEmpty0 = kVFull0 + 4,
+    kSFull0 = kVEmpty0 + 4, kSFree0 = kSFull0 + 2, kPFull0 = kSFree0 + 2, kODone0 = kPFull0 + 4, kOFree0 = kODone0 + 2,
     kStatFull0 = kOFree0 + 2, kItemFull0 = kStatFull0 + 2, kItemEmpty0 = kItemFull0 + kRing,
     kFinalQk = kItemEmpty0 + kRing, kFinalPv, kBarCount
 };
 
-// Tile ti of an item goes to group ti mod 2 (by its place in the item, so an item's
-// result does not depend on which CTA runs it), and the group's c-th tile in the
-// CTA's sequence uses its score buffer c mod 2, so the group's Q K^T for its next
-// tile never waits for its softmax of this one; that buffer's use is c / 2.
-__device__ __forceinline__ int sbuf(int grp, uint32_t c) { return grp * 2 + static_cast<int>(c & 1); }
+// Keys 64 g ... 64 g + 63 of every 128-key tile go to softmax group g, by their place
+// in the item, so an item's result does not depend on which CTA runs it.  Tile n of
+// the CTA's sequence uses score buffer n mod 2 (its use n / 2), and group g hands
+// its P over to P V through barrier kPFull0 + 2 g + n mod 2: a group runs at most
+// two tiles ahead of P V (it needs the score buffer), so a barrier never completes
+// a second phase before its waiter has seen the first.
 
 // Item k of this CTA's sequence from the queue (w < 0: no more items, or an
 // abort).  Every reader warp takes every item once, in order, and frees its slot.
@@ -372,7 +376,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
            const __grid_constant__ CUtensorMap tmv) {
     using C = Cfg<D>;
     constexpr int kStages = C::kStages;
-    static_assert(kBarCount <= C::kNumBars && kStages <= 8, "barrier slots");
+    static_assert(kBarCount <= C::kNumBars && kStages <= 4, "barrier slots");
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     unsigned char *sQ = smem + C::kOffQ;
@@ -403,14 +407,16 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             mbar_init(&bars[kOFree0 + i], 4);
             mbar_init(&bars[kStatFull0 + i], 8);
         }
-        for (int i = 0; i < 4; ++i) {
-            mbar_init(&bars[kSFull0 + i], 1);   // q.k done
-            mbar_init(&bars[kSFree0 + i], 1);   // the P V that read P over these scores done
-            mbar_init(&bars[kPFull0 + i], 4);   // the group's four warps stored P
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[kSFull0 + i], 1);   // score buffer i: q.k done
+            mbar_init(&bars[kSFree0 + i], 1);   // score buffer i: both groups' P V that read P over it done
         }
+        for (int i = 0; i < 4; ++i) mbar_init(&bars[kPFull0 + i], 4);   // group i / 2's four warps stored P in buffer i % 2
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bars[kKvFull0 + s], 1);
-            mbar_init(&bars[kKvEmpty0 + s], 1);
+            mbar_init(&bars[kKFull0 + s], 1);
+            mbar_init(&bars[kKEmpty0 + s], 1);
+            mbar_init(&bars[kVFull0 + s], 1);
+            mbar_init(&bars[kVEmpty0 + s], 1);
         }
         for (int s = 0; s < kRing; ++s) {
             mbar_init(&bars[kItemFull0 + s], 1);
@@ -441,23 +447,24 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer: K/V tiles
-        // A box is `box` keys of one page; a tile is `nbox` boxes.  The pool rows of
-        // an item's boxes are looked up 32 at a time, one window ahead (lane j holds
-        // box 32 win + j), so no page-table load sits between two tile issues; the
-        // producer waits only for ring stages and runs ahead across items.  The TMA
-        // unit's time per box bounds this loop, so nothing is prefetched into L2.
+        // A box is `box` keys of one page; a tile is `nbox` boxes.  K and V go to
+        // rings of their own, so a K stage is refilled once its q.k is done, well
+        // before the tile's P V frees the V stage.  The pool rows of an item's boxes
+        // are looked up 32 at a time, one window ahead (lane j holds box 32 win + j),
+        // so no page-table load sits between two tile issues; the producer waits only
+        // for ring stages and runs ahead across items.  The TMA unit's time per box
+        // bounds this loop, so nothing is prefetched into L2.
         const int box = p.box_rows;
         const int nbox = kTile / box;
         const int32_t *tab = p.layout == PKV_LAYOUT_CSR ? p.kv_indices : p.block_table;
-        // one copy per lane: lane = (box j, slab, K or V), at most 32 per tile
-        const int nops = nbox * C::kSl * 2;
-        const int j_box = (lane / (C::kSl * 2)) & (nbox - 1), sl_op = (lane >> 1) % C::kSl;
-        const bool is_v = (lane & 1) != 0;
-        uint32_t n = 0, kpub = 0;
+        // one copy per lane and ring: lane = (box j, slab), at most 32 per tile
+        const int nops = nbox * C::kSl;
+        const int j_box = (lane / C::kSl) & (nbox - 1), sl_op = lane % C::kSl;
+        uint32_t n = 0, kpub = 0, nk = 0, nv = 0;   // tiles; K and V tiles issued
         bool ok = true;
         // Pages under 8 keys: the producer gathers a tile's rows itself with 16-byte
         // cp.async copies (one commit group per tile), written in the same swizzled
-        // layout the TMA boxes produce.  A tile's full barrier is arrived once its
+        // layout the TMA boxes produce.  A tile's full barriers are arrived once its
         // group has completed and the warp has fenced its writes for the tensor
         // cores' async proxy; up to two tiles stay in flight (`pend`).
         const bool gather = box < 8;
@@ -468,7 +475,10 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             else cp_async_wait<0>();
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[kKvFull0 + n_arr % kStages]);
+            if (lane == 0) {
+                mbar_arrive(&bars[kKFull0 + n_arr % kStages]);
+                mbar_arrive(&bars[kVFull0 + n_arr % kStages]);
+            }
             ++n_arr;
             --pend;
         };
@@ -503,6 +513,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             more = w1 < total;
             publish(more ? w1 : -1);
         }
+        unsigned char *sK = sKV, *sV = sKV + kStages * C::kKBytes;
         for (uint32_t k = 0; ok; ++k) {
             const Item it = ring_read(ring, bars, k, ok, abort_flag, p.err, p.wait_ns);
             if (it.w < 0) break;
@@ -518,6 +529,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                     return static_cast<int>((static_cast<int64_t>(page) << p.ps_shift) + (kb & p.ps_mask));
                 };
                 if (gather) {
+                    constexpr int kRowsPerLane = kTile / 32;
                     for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
                         const int kt0 = it.k0 + ti * kTile;
                         // pool row of key j of the tile: -1 past the item's keys, -2 outside the pool
@@ -528,21 +540,37 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                             if (page < 0 || page >= p.num_pages) return -2;
                             return static_cast<int>((static_cast<int64_t>(page) << p.ps_shift) + (kk & p.ps_mask));
                         };
-                        const int r0 = key_row(lane), r1 = key_row(lane + 32);
-                        if (r0 == -2 || r1 == -2) raise_flag(p.err, PKV_DEVERR_RANGE);
+                        int rr[kRowsPerLane];
+                        bool bad = false;
+#pragma unroll
+                        for (int q = 0; q < kRowsPerLane; ++q) {
+                            rr[q] = key_row(lane + 32 * q);
+                            bad |= rr[q] == -2;
+                        }
+                        if (bad) raise_flag(p.err, PKV_DEVERR_RANGE);
                         const int s = n % kStages;
-                        if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
+                        // the stage frees once the Q K^T / P V of tile n - kStages ran, which
+                        // waits for that tile's full barriers: settle it first
+                        while (pend > static_cast<uint32_t>(kStages - 1)) settle_one();
+                        if (lane == 0) {
+                            ok = wait_bar(&bars[kKEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err, p.wait_ns) &&
+                                 wait_bar(&bars[kVEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
+                        }
                         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                         if (!ok) break;
                         constexpr int CPR = D / 8;       // 16-byte chunks per row
                         constexpr int KPI = 32 / CPR;    // rows per warp instruction
                         const int c = lane % CPR, sl = c >> 3, cc = c & 7;
-                        unsigned char *kst = sKV + s * C::kStageBytes, *vst = kst + C::kKBytes;
+                        unsigned char *kst = sK + s * C::kKBytes, *vst = sV + s * C::kKBytes;
 #pragma unroll 4
                         for (int j0 = 0; j0 < kTile; j0 += KPI) {
                             const int j = j0 + lane / CPR;
-                            const int a0 = __shfl_sync(0xffffffffu, r0, j & 31), a1 = __shfl_sync(0xffffffffu, r1, j & 31);
-                            const int row = j < 32 ? a0 : a1;
+                            int row = -1;
+#pragma unroll
+                            for (int q = 0; q < kRowsPerLane; ++q) {
+                                const int a = __shfl_sync(0xffffffffu, rr[q], j & 31);
+                                if ((j >> 5) == q) row = a;
+                            }
                             const bool live = row >= 0;
                             const int off = sl * kTile * 128 + j * 128 + ((cc ^ (j & 7)) << 4);
                             const int64_t col = static_cast<int64_t>(it.kh) * D + c * 8;
@@ -550,6 +578,8 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                             cp_async_16(vst + off, live ? p.v_pool + row * p.v_stride + col : p.v_pool, live ? 16 : 0);
                         }
                         cp_async_commit();
+                        ++nk;
+                        ++nv;
                         ++pend;
                         if (pend > 2) settle_one();
                     }
@@ -566,26 +596,28 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                         const int bx0 = ti * nbox;
                         int row = __shfl_sync(0xffffffffu, (bx0 >> 5) == win ? cur : nxt, (bx0 & 31) + j_box);
                         if (lane >= nops) row = -1;
-                        if (row == -2 && lane % (2 * C::kSl) == 0) raise_flag(p.err, PKV_DEVERR_RANGE);
+                        if (row == -2 && sl_op == 0) raise_flag(p.err, PKV_DEVERR_RANGE);
                         const int s = n % kStages;
-                        if (lane == 0) ok = wait_bar(&bars[kKvEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
-                        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                        if (!ok) break;
-                        if (row == -2) {   // a page outside the pool reads as zeros
-                            unsigned char *dz = sKV + s * C::kStageBytes + (is_v ? C::kKBytes : 0) + sl_op * kTile * 128 +
-                                                j_box * box * 128;
-                            for (int o = 0; o < box * 128; o += 16) *reinterpret_cast<uint4 *>(dz + o) = make_uint4(0, 0, 0, 0);
-                            fence_proxy_async_smem();   // for the tensor cores and later TMA writes
-                        }
                         const uint32_t valid = __ballot_sync(0xffffffffu, row >= 0);
-                        __syncwarp();
-                        if (lane == 0)
-                            mbar_arrive_expect_tx(&bars[kKvFull0 + s], __popc(valid) * static_cast<uint32_t>(box) * 128u);
-                        __syncwarp();
-                        if (row >= 0)
-                            tma_load_3d(sKV + s * C::kStageBytes + (is_v ? C::kKBytes : 0) + sl_op * kTile * 128 +
-                                            j_box * box * 128,
-                                        is_v ? &tmv : &tmk, sl_op * 64, it.kh, row, &bars[kKvFull0 + s]);
+                        const uint32_t bytes = __popc(valid) * static_cast<uint32_t>(box) * 128u;
+                        // K, then V: each into its ring once its stage is free
+                        for (int kv = 0; kv < 2; ++kv) {
+                            uint64_t *emp = &bars[(kv ? kVEmpty0 : kKEmpty0) + s], *ful = &bars[(kv ? kVFull0 : kKFull0) + s];
+                            unsigned char *dst = (kv ? sV : sK) + s * C::kKBytes + sl_op * kTile * 128 + j_box * box * 128;
+                            if (lane == 0) ok = wait_bar(emp, ((n / kStages) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
+                            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                            if (!ok) break;
+                            if (row == -2) {   // a page outside the pool reads as zeros
+                                for (int o = 0; o < box * 128; o += 16) *reinterpret_cast<uint4 *>(dst + o) = make_uint4(0, 0, 0, 0);
+                                fence_proxy_async_smem();   // for the tensor cores and later TMA writes
+                            }
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive_expect_tx(ful, bytes);
+                            __syncwarp();
+                            if (row >= 0) tma_load_3d(dst, kv ? &tmv : &tmk, sl_op * 64, it.kh, row, ful);
+                            if (kv) ++nv; else ++nk;
+                        }
+                        if (!ok) break;
                     }
                 }
             }
@@ -596,9 +628,12 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             }
         }
         settle_all();
-        if (lane == 0)   // drain: the copies this warp issued have landed
-            for (uint32_t k = n > kStages ? n - kStages : 0; k < n; ++k)
-                drain_wait(&bars[kKvFull0 + k % kStages], (k / kStages) & 1);
+        if (lane == 0) {   // drain: the copies this warp issued have landed
+            for (uint32_t k = nk > kStages ? nk - kStages : 0; k < nk; ++k)
+                drain_wait(&bars[kKFull0 + k % kStages], (k / kStages) & 1);
+            for (uint32_t k = nv > kStages ? nv - kStages : 0; k < nv; ++k)
+                drain_wait(&bars[kVFull0 + k % kStages], (k / kStages) & 1);
+        }
         __syncwarp();
     } else if (warp == kQkWarp) {
         // ------------------------------------------------------------ S = Q K^T
@@ -621,7 +656,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             __syncwarp();
             if (ok) ++q_issued;
         };
-        uint32_t kr = 0, c0 = 0, c1 = 0;   // tiles issued per group
+        uint32_t kr = 0;
         Item it = ring_read(ring, bars, kr++, ok, abort_flag, p.err, p.wait_ns);
         bool q_req = false;   // it's q block already requested
         while (it.w >= 0 && ok) {
@@ -632,25 +667,25 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                 const int sl = iq & 1;
                 ok = warp_wait(ok, &bars[kQFull0 + sl], (iq >> 1) & 1, abort_flag, p.err, p.wait_ns);
                 for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
-                    const int g = ti & 1;
-                    const uint32_t c = g ? c1++ : c0++;
-                    const int s = n % kStages, sb = sbuf(g, c);
-                    ok = warp_wait(ok, &bars[kKvFull0 + s], (n / kStages) & 1, abort_flag, p.err, p.wait_ns);
-                    ok = warp_wait(ok, &bars[kSFree0 + sb], ((c >> 1) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
+                    // score buffer n mod 2 is free once both groups' P V of tile n - 2 are done
+                    const int s = n % kStages, b = n & 1;
+                    ok = warp_wait(ok, &bars[kKFull0 + s], (n / kStages) & 1, abort_flag, p.err, p.wait_ns);
+                    ok = warp_wait(ok, &bars[kSFree0 + b], ((n >> 1) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
                     if (!ok) break;
                     tc05::fence_after_sync();
                     if (lane == 0) {
-                        const uint64_t kd = tc05::smem_desc(sKV + s * C::kStageBytes, 16, 1024);
+                        const uint64_t kd = tc05::smem_desc(sKV + s * C::kKBytes, 16, 1024);
                         const uint64_t qd = tc05::smem_desc(sQ + sl * C::kQBytes, 16, 1024);
     #pragma unroll
                         for (int k2 = 0; k2 < C::kSl; ++k2)
     #pragma unroll
-                            for (int k = 0; k < 4; ++k)   // slab: q +16 KB, K +8 KB; k-step +32 bytes
-                                tc05::mma_ss(tbase + C::kColS + sb * kTile,
+                            for (int k = 0; k < 4; ++k)   // slab: q +16 KB, K +16 KB; k-step +32 bytes
+                                tc05::mma_ss(tbase + C::kColS + b * kTile,
                                              qd + static_cast<uint64_t>((k2 * kRows * 128 + k * 32) >> 4),
                                              kd + static_cast<uint64_t>((k2 * kTile * 128 + k * 32) >> 4), idesc,
                                              (k2 | k) ? 1u : 0u);
-                        tc05::commit(&bars[kSFull0 + sb]);
+                        tc05::commit(&bars[kSFull0 + b]);
+                        tc05::commit(&bars[kKEmpty0 + s]);
                         if (ti == it.n_tiles - 1) tc05::commit(&bars[kQEmpty0 + sl]);
                     }
                     __syncwarp();
@@ -672,24 +707,22 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
         }
         __syncwarp();
     } else if (warp == kPvWarp) {
-        // ------------------------------------------------------------ O_g += P V
-        // Tile ti goes to group ti mod 2's accumulator.  An item's first two tiles (one
-        // per group) start their accumulators afresh, once the epilogue has read the
-        // previous item's.
+        // ------------------------------------------------------------ O_g += P_g V_g
+        // Group g's half of tile n (keys 64 g ... 64 g + 63) into its accumulator.  An
+        // item's first tile starts both accumulators afresh, once the epilogue has read
+        // the previous item's.
         const uint32_t idesc = tc05::idesc_bf16_f32(kRows, D, false, true);
-        uint32_t n = 0, io = 0, c0 = 0, c1 = 0;   // tiles per group
+        uint32_t n = 0, io = 0;
         bool ok = true;
         for (uint32_t k = 0; ok; ++k) {
             const Item it = ring_read(ring, bars, k, ok, abort_flag, p.err, p.wait_ns);
             if (it.w < 0) break;
             if (it.n_tiles == 0) continue;
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
-                const int g = ti & 1;
-                const uint32_t c = g ? c1++ : c0++;
-                const int sb = sbuf(g, c);
-                ok = warp_wait(ok, &bars[kPFull0 + sb], (c >> 1) & 1, abort_flag, p.err, p.wait_ns);
+                const int s = n % kStages, b = n & 1;
+                ok = warp_wait(ok, &bars[kVFull0 + s], (n / kStages) & 1, abort_flag, p.err, p.wait_ns);
                 if (!ok) break;
-                unsigned char *v = sKV + (n % kStages) * C::kStageBytes + C::kKBytes;
+                unsigned char *v = sKV + (kStages + s) * C::kKBytes;
                 const int n_valid = it.k1 - (it.k0 + ti * kTile);
                 if (n_valid < kTile) {   // key rows past the chunk hold stale data: zero them
                     for (int i = lane; i < (kTile - n_valid) * C::kSl * 8; i += 32) {
@@ -702,17 +735,24 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                 }
                 if (ti == 0 && io > 0)
                     ok = warp_wait(ok, &bars[kOFree0 + ((io - 1) & 1)], ((io - 1) >> 1) & 1, abort_flag, p.err, p.wait_ns);
-                if (!ok) break;
-                tc05::fence_after_sync();
-                if (lane == 0) {
-                    const uint64_t vd = tc05::smem_desc(v, kTile * 128, 1024);
+                for (int g = 0; g < 2 && ok; ++g) {
+                    ok = warp_wait(ok, &bars[kPFull0 + 2 * g + b], (n >> 1) & 1, abort_flag, p.err, p.wait_ns);
+                    if (!ok) break;
+                    tc05::fence_after_sync();
+                    if (lane == 0) {
+                        const uint64_t vd = tc05::smem_desc(v + g * 64 * 128, kTile * 128, 1024);
 #pragma unroll
-                    for (int k = 0; k < kTile / 16; ++k)   // 16 keys: +2048 bytes of V, +8 columns of P
-                        tc05::mma_ts(tbase + C::kColO + g * D, tbase + C::kColS + sb * kTile + k * 8,
-                                     vd + static_cast<uint64_t>((k * 2048) >> 4), idesc,
-                                     (ti < 2 && k == 0) ? 0u : 1u);
-                    tc05::commit(&bars[kSFree0 + sb]);
-                    tc05::commit(&bars[kKvEmpty0 + n % kStages]);
+                        for (int k = 0; k < 4; ++k)   // 16 keys: +2048 bytes of V, +8 columns of P
+                            tc05::mma_ts(tbase + C::kColO + g * D, tbase + C::kColS + b * kTile + g * 64 + k * 8,
+                                         vd + static_cast<uint64_t>((k * 2048) >> 4), idesc,
+                                         (ti == 0 && k == 0) ? 0u : 1u);
+                    }
+                    __syncwarp();
+                }
+                if (!ok) break;
+                if (lane == 0) {
+                    tc05::commit(&bars[kSFree0 + b]);
+                    tc05::commit(&bars[kVEmpty0 + s]);
                     if (ti == it.n_tiles - 1) tc05::commit(&bars[kODone0 + (io & 1)]);
                 }
                 __syncwarp();
@@ -812,13 +852,13 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
         }
     } else {
         // ------------------------------------------------------------ softmax (one row per thread)
-        // Group grp = warp / 4 takes the tiles ti of each item with ti mod 2 = grp,
-        // keeping its own (m, l) and accumulator; warp w reads TMEM lanes 32 (w mod 4) ...
+        // Group grp = warp / 4 takes keys 64 grp ... 64 grp + 63 of every tile, keeping
+        // its own (m, l) and accumulator; warp w reads TMEM lanes 32 (w mod 4) ...
         const int grp = warp >> 2, quarter = warp & 3;
         const int r = quarter * 32 + lane;
         const uint32_t trow = tc05::taddr(tbase, quarter * 32, 0);
         const int tok = r >> p.g_shift, hh = r & (p.g - 1);
-        uint32_t io = 0, c = 0;   // items, and this group's tiles so far
+        uint32_t io = 0, n = 0;   // items and tiles so far
         bool ok = true;
         // the row's key bound; its load for the next item is issued an item early
         auto row_bound = [&](const Item &qi) -> int {
@@ -853,24 +893,25 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                 continue;
             }
             const int ko = io & 1;
-            for (int ti = grp; ti < it.n_tiles; ti += 2, ++c) {   // this group's tiles
-                const int sb = sbuf(grp, c);
-                const int key0 = it.k0 + ti * kTile;
+            for (int ti = 0; ti < it.n_tiles; ++ti, ++n) {
+                const int b = n & 1;
+                const int key0 = it.k0 + ti * kTile + grp * 64;   // this group's half of the tile
                 // rows past the block's tokens are never written: they only mask the
-                // keys past the chunk (stale data), which keeps full tiles select-free
-                const int vis = max(0, min(min(valid ? kend : it.k1, it.k1) - key0, kTile));
-                ok = warp_wait(ok, &bars[kSFull0 + sb], (c >> 1) & 1, abort_flag, p.err, p.wait_ns);
+                // keys past the chunk (stale data), which keeps full halves select-free
+                const int vis = max(0, min(min(valid ? kend : it.k1, it.k1) - key0, 64));
+                const uint32_t sc = trow + C::kColS + b * kTile + grp * 64;
+                ok = warp_wait(ok, &bars[kSFull0 + b], (n >> 1) & 1, abort_flag, p.err, p.wait_ns);
                 float x[64];
                 if (ok) {
                     tc05::fence_after_sync();
-                    tc05::ld_x64(trow + C::kColS + sb * kTile, x);
+                    tc05::ld_x64(sc, x);
                 } else {
 #pragma unroll
                     for (int j = 0; j < 64; ++j) x[j] = 0.f;
                 }
                 // keys at or past the row's bound read as -inf (no selects when the
-                // whole tile is inside every row's bound); max over a tree of pairs
-                if (!__all_sync(0xffffffffu, vis == kTile)) {
+                // whole half is inside every row's bound); max over a tree
+                if (!__all_sync(0xffffffffu, vis == 64)) {
 #pragma unroll
                     for (int j = 0; j < 64; ++j) x[j] = j < vis ? x[j] : -INFINITY;
                 }
@@ -890,10 +931,10 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                 const bool raise = mx > m + kLazy || (m == -INFINITY && mx != -INFINITY);
                 const float corr = raise ? ex2(m - mx) : 1.f;
                 if (__any_sync(0xffffffffu, raise && m != -INFINITY) && ok) {
-                    // the group's accumulator is final for its previous tile (of this item:
-                    // m is finite) once that tile's P V completed; rescale the row
-                    const uint32_t cp = c - 1;
-                    ok = warp_wait(ok, &bars[kSFree0 + sbuf(grp, cp)], (cp >> 1) & 1, abort_flag, p.err, p.wait_ns);
+                    // the group's accumulator is final for tile n - 1 (of this item: m is
+                    // finite) once that tile's P V completed; rescale the row
+                    const uint32_t np = n - 1;
+                    ok = warp_wait(ok, &bars[kSFree0 + (np & 1)], (np >> 1) & 1, abort_flag, p.err, p.wait_ns);
                     tc05::fence_after_sync();
 #pragma unroll 1
                     for (int cc = 0; cc < D / 16 && ok; ++cc) {
@@ -910,32 +951,29 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                     l *= corr;
                     m = mx;
                 }
-                uint32_t h[32];
+                uint32_t h0[16], h1[16];
                 float lsum = 0.f;
                 // a row with no keys yet (m = -inf) has only -inf scores: offset 0 gives p = 0
                 const float nm = m == -INFINITY ? 0.f : -m;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {   // p = 2^(scale log2(e) s - m)
-                    const float p0 = ex2(fmaf(x[2 * j], p.scale_log2, nm));
-                    const float p1 = ex2(fmaf(x[2 * j + 1], p.scale_log2, nm));
-                    lsum += p0 + p1;
-                    h[j] = pack_bf16x2(p0, p1);
+                for (int j = 0; j < 16; ++j) {   // p = 2^(scale log2(e) s - m)
+                    const float a0 = ex2(fmaf(x[2 * j], p.scale_log2, nm));
+                    const float a1 = ex2(fmaf(x[2 * j + 1], p.scale_log2, nm));
+                    const float b0 = ex2(fmaf(x[32 + 2 * j], p.scale_log2, nm));
+                    const float b1 = ex2(fmaf(x[32 + 2 * j + 1], p.scale_log2, nm));
+                    lsum += (a0 + a1) + (b0 + b1);
+                    h0[j] = pack_bf16x2(a0, a1);
+                    h1[j] = pack_bf16x2(b0, b1);
                 }
                 l += lsum;
                 if (ok) {   // P (bf16 pairs) over the first 32 columns of the scores just read
-                    uint32_t h0[16], h1[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        h0[j] = h[j];
-                        h1[j] = h[16 + j];
-                    }
-                    tc05::st_x16_u32(trow + C::kColS + sb * kTile, h0);
-                    tc05::st_x16_u32(trow + C::kColS + sb * kTile + 16, h1);
+                    tc05::st_x16_u32(sc, h0);
+                    tc05::st_x16_u32(sc + 16, h1);
                     tc05::wait_st();
                 }
                 tc05::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars[kPFull0 + sb]);
+                if (lane == 0) mbar_arrive(&bars[kPFull0 + 2 * grp + b]);
             }
             // hand (m, l) to the epilogue warps; the buffer is free once they are done
             // with the item two back
@@ -1074,7 +1112,8 @@ static bool make_plan(const pkv_extend_args *a, Plan &pl) {
     pl.groups_max = static_cast<int64_t>(a->num_kv_heads) * blocks_max;
     const int64_t L = std::max(1, a->max_seq_len);
     if (a->kv_chunk > 0) {
-        pl.chunk = a->kv_chunk;
+        // whole tiles: a block's pieces are then never empty ((pieces - 1) x piece < keys)
+        pl.chunk = (a->kv_chunk + kTile - 1) / kTile * kTile;
     } else {   // split the keys only when the query blocks alone leave SMs idle
         const int64_t target = 2 * static_cast<int64_t>(sm_count());
         const int64_t groups = std::max<int64_t>(1, static_cast<int64_t>(a->num_kv_heads) *
@@ -1113,7 +1152,7 @@ static pkv_status validate(const pkv_extend_args *a, bool check_ptrs) {
         return fail(PKV_ERR_UNSUPPORTED, "pkv_extend: page_size must be a power of two in [1, 1024]");
     if (a->layout != PKV_LAYOUT_CSR && a->layout != PKV_LAYOUT_BLOCK_TABLE)
         return fail(PKV_ERR_INVALID_ARG, "pkv_extend: layout must be CSR or BLOCK_TABLE");
-    if (a->kv_chunk < 0 || a->kv_chunk % kTile) return fail(PKV_ERR_INVALID_ARG, "pkv_extend: kv_chunk multiple of 64");
+    if (a->kv_chunk < 0 || a->kv_chunk % kChunkUnit) return fail(PKV_ERR_INVALID_ARG, "pkv_extend: kv_chunk multiple of 64");
     const int64_t rowq = static_cast<int64_t>(a->num_kv_heads) * a->head_dim;
     if (a->k_row_stride < rowq || a->v_row_stride < rowq || a->k_row_stride % 8 || a->v_row_stride % 8)
         return fail(PKV_ERR_INVALID_ARG, "pkv_extend: pool row strides must hold Hkv x head_dim and be 16-byte aligned");
