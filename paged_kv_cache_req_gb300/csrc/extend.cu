@@ -11,11 +11,12 @@
 // online-softmax state and accumulator: one Q K^T of N = 128 serves both, and
 // the tensor cores run the next tile's Q K^T and the groups' P V while the
 // groups compute their exponentials.  Per CTA:
-//   warp 8     producer: K and V tiles through rings of their own (2 stages each,
-//              4 at head_dim 64), so a K stage is refilled once its Q K^T is
-//              done: one TMA box per page per slab, one copy per lane and ring,
-//              pool rows looked up 32 boxes at a time; pages under 8 keys are
-//              gathered row by row with cp.async instead;
+//   warps 8, 15  producers of K and of V tiles, each through a ring of its own
+//              (2 stages, 4 at head_dim 64), so K runs ahead as soon as a Q K^T
+//              has run while V waits for P V: one TMA box per page per slab, one
+//              copy per lane, pool rows looked up 32 boxes at a time; pages under
+//              8 keys are gathered row by row with cp.async instead.  Warp 8 also
+//              claims the CTA's items and publishes them to every warp;
 //   warp 9     loads the q blocks (one 3-D box per 64-dim slab, rows
 //              token-major) into two buffers, the next item's while this one
 //              runs, and issues S = Q K^T (M = 128, N = 128) for tile n into
@@ -43,13 +44,14 @@ namespace ext {
 
 constexpr int kRows = 128, kTile = 128;   // query rows per block, keys per tile
 constexpr int kChunkUnit = 64;             // a caller's kv_chunk is a multiple of this
-constexpr int kThreads = 480;              // warps 0-7 softmax (two groups), 8 producer, 9 q.k, 10 P.V, 11-14 epilogue
-constexpr int kProducerWarp = 8, kQkWarp = 9, kPvWarp = 10, kEpiWarp0 = 11;
+constexpr int kThreads = 512;              // warps 0-7 softmax (two groups), 8 K producer, 9 q.k, 10 P.V,
+                                           // 11-14 epilogue, 15 V producer
+constexpr int kProducerWarp = 8, kQkWarp = 9, kPvWarp = 10, kEpiWarp0 = 11, kVProducerWarp = 15;
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kLog2e = 1.44269504088896341f;
 constexpr float kLazy = 8.f;
 constexpr int kRing = 8;                   // slots of the item queue
-constexpr int kItemReaders = 15;           // warps that read every queued item
+constexpr int kItemReaders = 16;           // warps that read every queued item
 
 template <int D>
 struct Cfg {
@@ -368,7 +370,7 @@ __device__ __forceinline__ Item ring_read(const Item *ring, uint64_t *bars, uint
     return it;
 }
 
-// Fifteen warps: four of them on one SM sub-partition share its 16K registers, so
+// Sixteen warps: four of them on one SM sub-partition share its 16K registers, so
 // at most 128 registers a thread.
 template <int D>
 __global__ void __maxnreg__(128)
@@ -445,26 +447,30 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
     const int64_t total = tb.off[p.batch];
     Item *ring = reinterpret_cast<Item *>(smem + C::kOffRing);
 
-    if (warp == kProducerWarp) {
-        // ------------------------------------------------------------ producer: K/V tiles
-        // A box is `box` keys of one page; a tile is `nbox` boxes.  K and V go to
-        // rings of their own, so a K stage is refilled once its q.k is done, well
-        // before the tile's P V frees the V stage.  The pool rows of an item's boxes
-        // are looked up 32 at a time, one window ahead (lane j holds box 32 win + j),
-        // so no page-table load sits between two tile issues; the producer waits only
-        // for ring stages and runs ahead across items.  The TMA unit's time per box
+    if (warp == kProducerWarp || warp == kVProducerWarp) {
+        // ------------------------------------------------------------ producers: K (warp 8), V (warp 15)
+        // A box is `box` keys of one page; a tile is `nbox` boxes.  Each warp fills
+        // its own ring, in tile order: K runs ahead as soon as a Q K^T has freed a
+        // stage, while V waits for P V.  The pool rows of an item's boxes are looked
+        // up 32 at a time, one window ahead (lane j holds box 32 win + j), so no
+        // page-table load sits between two tile issues.  The TMA unit's time per box
         // bounds this loop, so nothing is prefetched into L2.
+        const bool is_v = warp == kVProducerWarp;
         const int box = p.box_rows;
         const int nbox = kTile / box;
         const int32_t *tab = p.layout == PKV_LAYOUT_CSR ? p.kv_indices : p.block_table;
-        // one copy per lane and ring: lane = (box j, slab), at most 32 per tile
+        // one copy per lane: lane = (box j, slab), at most 32 per tile
         const int nops = nbox * C::kSl;
         const int j_box = (lane / C::kSl) & (nbox - 1), sl_op = lane % C::kSl;
-        uint32_t n = 0, kpub = 0, nk = 0, nv = 0;   // tiles; K and V tiles issued
+        uint64_t *fulls = &bars[is_v ? kVFull0 : kKFull0], *empties = &bars[is_v ? kVEmpty0 : kKEmpty0];
+        unsigned char *ring_base = sKV + (is_v ? kStages * C::kKBytes : 0);
+        const uint16_t *pool = is_v ? p.v_pool : p.k_pool;
+        const int64_t pool_stride = is_v ? p.v_stride : p.k_stride;
+        uint32_t n = 0, kpub = 0, issued = 0;   // tiles; tiles whose copies were issued
         bool ok = true;
-        // Pages under 8 keys: the producer gathers a tile's rows itself with 16-byte
+        // Pages under 8 keys: the warp gathers a tile's rows itself with 16-byte
         // cp.async copies (one commit group per tile), written in the same swizzled
-        // layout the TMA boxes produce.  A tile's full barriers are arrived once its
+        // layout the TMA boxes produce.  A tile's full barrier is arrived once its
         // group has completed and the warp has fenced its writes for the tensor
         // cores' async proxy; up to two tiles stay in flight (`pend`).
         const bool gather = box < 8;
@@ -475,17 +481,15 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             else cp_async_wait<0>();
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&bars[kKFull0 + n_arr % kStages]);
-                mbar_arrive(&bars[kVFull0 + n_arr % kStages]);
-            }
+            if (lane == 0) mbar_arrive(&fulls[n_arr % kStages]);
             ++n_arr;
             --pend;
         };
         auto settle_all = [&]() { while (pend > 0) settle_one(); };
-        // The queue: the CTA's first item is blockIdx.x; later ones are claimed from a
-        // global counter (dynamic balance), two items ahead of the one being issued,
-        // decoded here and published to every reader warp.  A negative w ends it.
+        // The queue (warp 8): the CTA's first item is blockIdx.x; later ones are
+        // claimed from a global counter (dynamic balance), two items ahead of the one
+        // being issued, decoded here and published to every reader warp.  A negative
+        // w ends it.
         auto publish = [&](int64_t w) {
             settle_all();   // the readers of the queue may be waiting for these tiles
             const uint32_t slot = kpub % kRing;
@@ -504,17 +508,20 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             __syncwarp();
             ++kpub;
         };
-        bool more = blockIdx.x < total;
-        publish(more ? static_cast<int64_t>(blockIdx.x) : -1);
-        if (more) {
-            int got = 0;
-            if (lane == 0) got = atomicAdd(p.counter, 1);
-            const int64_t w1 = static_cast<int64_t>(gridDim.x) + __shfl_sync(0xffffffffu, got, 0);
-            more = w1 < total;
-            publish(more ? w1 : -1);
+        bool more = false;
+        if (!is_v) {
+            more = blockIdx.x < total;
+            publish(more ? static_cast<int64_t>(blockIdx.x) : -1);
+            if (more) {
+                int got = 0;
+                if (lane == 0) got = atomicAdd(p.counter, 1);
+                const int64_t w1 = static_cast<int64_t>(gridDim.x) + __shfl_sync(0xffffffffu, got, 0);
+                more = w1 < total;
+                publish(more ? w1 : -1);
+            }
         }
-        unsigned char *sK = sKV, *sV = sKV + kStages * C::kKBytes;
         for (uint32_t k = 0; ok; ++k) {
+            if (is_v) settle_all();   // this warp may wait below for an item not yet published
             const Item it = ring_read(ring, bars, k, ok, abort_flag, p.err, p.wait_ns);
             if (it.w < 0) break;
             int got = 0;   // the claim's latency hides behind this item's tiles
@@ -547,21 +554,18 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                             rr[q] = key_row(lane + 32 * q);
                             bad |= rr[q] == -2;
                         }
-                        if (bad) raise_flag(p.err, PKV_DEVERR_RANGE);
+                        if (bad && !is_v) raise_flag(p.err, PKV_DEVERR_RANGE);
                         const int s = n % kStages;
                         // the stage frees once the Q K^T / P V of tile n - kStages ran, which
-                        // waits for that tile's full barriers: settle it first
+                        // waits for that tile's full barrier: settle it first
                         while (pend > static_cast<uint32_t>(kStages - 1)) settle_one();
-                        if (lane == 0) {
-                            ok = wait_bar(&bars[kKEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err, p.wait_ns) &&
-                                 wait_bar(&bars[kVEmpty0 + s], ((n / kStages) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
-                        }
+                        if (lane == 0) ok = wait_bar(&empties[s], ((n / kStages) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
                         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                         if (!ok) break;
                         constexpr int CPR = D / 8;       // 16-byte chunks per row
                         constexpr int KPI = 32 / CPR;    // rows per warp instruction
                         const int c = lane % CPR, sl = c >> 3, cc = c & 7;
-                        unsigned char *kst = sK + s * C::kKBytes, *vst = sV + s * C::kKBytes;
+                        unsigned char *st = ring_base + s * C::kKBytes;
 #pragma unroll 4
                         for (int j0 = 0; j0 < kTile; j0 += KPI) {
                             const int j = j0 + lane / CPR;
@@ -574,12 +578,10 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                             const bool live = row >= 0;
                             const int off = sl * kTile * 128 + j * 128 + ((cc ^ (j & 7)) << 4);
                             const int64_t col = static_cast<int64_t>(it.kh) * D + c * 8;
-                            cp_async_16(kst + off, live ? p.k_pool + row * p.k_stride + col : p.k_pool, live ? 16 : 0);
-                            cp_async_16(vst + off, live ? p.v_pool + row * p.v_stride + col : p.v_pool, live ? 16 : 0);
+                            cp_async_16(st + off, live ? pool + row * pool_stride + col : pool, live ? 16 : 0);
                         }
                         cp_async_commit();
-                        ++nk;
-                        ++nv;
+                        ++issued;
                         ++pend;
                         if (pend > 2) settle_one();
                     }
@@ -596,28 +598,22 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                         const int bx0 = ti * nbox;
                         int row = __shfl_sync(0xffffffffu, (bx0 >> 5) == win ? cur : nxt, (bx0 & 31) + j_box);
                         if (lane >= nops) row = -1;
-                        if (row == -2 && sl_op == 0) raise_flag(p.err, PKV_DEVERR_RANGE);
+                        if (row == -2 && sl_op == 0 && !is_v) raise_flag(p.err, PKV_DEVERR_RANGE);
                         const int s = n % kStages;
                         const uint32_t valid = __ballot_sync(0xffffffffu, row >= 0);
-                        const uint32_t bytes = __popc(valid) * static_cast<uint32_t>(box) * 128u;
-                        // K, then V: each into its ring once its stage is free
-                        for (int kv = 0; kv < 2; ++kv) {
-                            uint64_t *emp = &bars[(kv ? kVEmpty0 : kKEmpty0) + s], *ful = &bars[(kv ? kVFull0 : kKFull0) + s];
-                            unsigned char *dst = (kv ? sV : sK) + s * C::kKBytes + sl_op * kTile * 128 + j_box * box * 128;
-                            if (lane == 0) ok = wait_bar(emp, ((n / kStages) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
-                            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                            if (!ok) break;
-                            if (row == -2) {   // a page outside the pool reads as zeros
-                                for (int o = 0; o < box * 128; o += 16) *reinterpret_cast<uint4 *>(dst + o) = make_uint4(0, 0, 0, 0);
-                                fence_proxy_async_smem();   // for the tensor cores and later TMA writes
-                            }
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive_expect_tx(ful, bytes);
-                            __syncwarp();
-                            if (row >= 0) tma_load_3d(dst, kv ? &tmv : &tmk, sl_op * 64, it.kh, row, ful);
-                            if (kv) ++nv; else ++nk;
-                        }
+                        unsigned char *dst = ring_base + s * C::kKBytes + sl_op * kTile * 128 + j_box * box * 128;
+                        if (lane == 0) ok = wait_bar(&empties[s], ((n / kStages) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
+                        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                         if (!ok) break;
+                        if (row == -2) {   // a page outside the pool reads as zeros
+                            for (int o = 0; o < box * 128; o += 16) *reinterpret_cast<uint4 *>(dst + o) = make_uint4(0, 0, 0, 0);
+                            fence_proxy_async_smem();   // for the tensor cores and later TMA writes
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_expect_tx(&fulls[s], __popc(valid) * static_cast<uint32_t>(box) * 128u);
+                        __syncwarp();
+                        if (row >= 0) tma_load_3d(dst, is_v ? &tmv : &tmk, sl_op * 64, it.kh, row, &fulls[s]);
+                        ++issued;
                     }
                 }
             }
@@ -628,12 +624,9 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             }
         }
         settle_all();
-        if (lane == 0) {   // drain: the copies this warp issued have landed
-            for (uint32_t k = nk > kStages ? nk - kStages : 0; k < nk; ++k)
-                drain_wait(&bars[kKFull0 + k % kStages], (k / kStages) & 1);
-            for (uint32_t k = nv > kStages ? nv - kStages : 0; k < nv; ++k)
-                drain_wait(&bars[kVFull0 + k % kStages], (k / kStages) & 1);
-        }
+        if (lane == 0)   // drain: the copies this warp issued have landed
+            for (uint32_t k = issued > kStages ? issued - kStages : 0; k < issued; ++k)
+                drain_wait(&fulls[k % kStages], (k / kStages) & 1);
         __syncwarp();
     } else if (warp == kQkWarp) {
         // ------------------------------------------------------------ S = Q K^T
