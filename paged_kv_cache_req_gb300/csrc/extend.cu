@@ -332,6 +332,29 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// Two fp32 lanes in one 64-bit register, and the paired FMA / add on them (one
+// instruction for two values on this architecture).
+__device__ __forceinline__ uint64_t pair(float a, float b) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(a), "f"(b));
+    return d;
+}
+__device__ __forceinline__ float2 unpair(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // Three-input maximum (one instruction on this architecture).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
@@ -945,20 +968,24 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                     m = mx;
                 }
                 uint32_t h0[16], h1[16];
-                float lsum = 0.f;
                 // a row with no keys yet (m = -inf) has only -inf scores: offset 0 gives p = 0
                 const float nm = m == -INFINITY ? 0.f : -m;
+                // scaling and the row sum two keys per instruction (the softmax groups
+                // are bound by instruction issue)
+                const uint64_t sc2 = pair(p.scale_log2, p.scale_log2), nm2 = pair(nm, nm);
+                uint64_t acc = pair(0.f, 0.f);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {   // p = 2^(scale log2(e) s - m)
-                    const float a0 = ex2(fmaf(x[2 * j], p.scale_log2, nm));
-                    const float a1 = ex2(fmaf(x[2 * j + 1], p.scale_log2, nm));
-                    const float b0 = ex2(fmaf(x[32 + 2 * j], p.scale_log2, nm));
-                    const float b1 = ex2(fmaf(x[32 + 2 * j + 1], p.scale_log2, nm));
-                    lsum += (a0 + a1) + (b0 + b1);
+                    const float2 ya = unpair(fma2(pair(x[2 * j], x[2 * j + 1]), sc2, nm2));
+                    const float2 yb = unpair(fma2(pair(x[32 + 2 * j], x[32 + 2 * j + 1]), sc2, nm2));
+                    const float a0 = ex2(ya.x), a1 = ex2(ya.y), b0 = ex2(yb.x), b1 = ex2(yb.y);
+                    acc = add2(acc, pair(a0, a1));
+                    acc = add2(acc, pair(b0, b1));
                     h0[j] = pack_bf16x2(a0, a1);
                     h1[j] = pack_bf16x2(b0, b1);
                 }
-                l += lsum;
+                const float2 ls = unpair(acc);
+                l += ls.x + ls.y;
                 if (ok) {   // P (bf16 pairs) over the first 32 columns of the scores just read
                     tc05::st_x16_u32(sc, h0);
                     tc05::st_x16_u32(sc + 16, h1);
