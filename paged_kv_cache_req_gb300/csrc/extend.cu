@@ -635,7 +635,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                         __syncwarp();
                         if (lane == 0) mbar_arrive_expect_tx(&fulls[s], __popc(valid) * static_cast<uint32_t>(box) * 128u);
                         __syncwarp();
-                        if (row >= 0) tma_load_3d(dst, is_v ? &tmv : &tmk, sl_op * 64, it.kh, row, &fulls[s]);
+                        if (row >= 0) tma_load_2d(dst, is_v ? &tmv : &tmk, it.kh * D + sl_op * 64, row, &fulls[s]);
                         ++issued;
                     }
                 }
@@ -1241,12 +1241,13 @@ static pkv_status launch_t(const pkv_extend_args *a, const Plan &pl, void *ws, i
         const uint32_t bq[3] = {64, static_cast<uint32_t>(pl.g), static_cast<uint32_t>(pl.T)};
         if (!encode_tmap_bf16(&tmq, a->q, 3, dq, sq, bq))
             return fail(PKV_ERR_CUDA, "pkv_extend: cuTensorMapEncodeTiled rejected q");
-        const uint64_t dk[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a->num_kv_heads),
-                                static_cast<uint64_t>(a->num_slots)};
-        const uint64_t sk[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(a->k_row_stride) * 2};
-        const uint64_t sv[2] = {static_cast<uint64_t>(D) * 2, static_cast<uint64_t>(a->v_row_stride) * 2};
-        const uint32_t bk[3] = {64, 1, static_cast<uint32_t>(p.box_rows)};
-        if (!encode_tmap_bf16(&tmk, a->k_pool, 3, dk, sk, bk) || !encode_tmap_bf16(&tmv, a->v_pool, 3, dk, sv, bk))
+        // pool rows as a 2-D tensor (kv heads x head_dim wide): a box is 64 dims of one
+        // kv head over a page's rows
+        const uint64_t dk[2] = {static_cast<uint64_t>(a->num_kv_heads) * D, static_cast<uint64_t>(a->num_slots)};
+        const uint64_t sk[1] = {static_cast<uint64_t>(a->k_row_stride) * 2};
+        const uint64_t sv[1] = {static_cast<uint64_t>(a->v_row_stride) * 2};
+        const uint32_t bk[2] = {64, static_cast<uint32_t>(p.box_rows)};
+        if (!encode_tmap_bf16(&tmk, a->k_pool, 2, dk, sk, bk) || !encode_tmap_bf16(&tmv, a->v_pool, 2, dk, sv, bk))
             return fail(PKV_ERR_CUDA, "pkv_extend: cuTensorMapEncodeTiled rejected the pools");
     }
     std::atomic<int64_t> *m_lim = device_memo(reinterpret_cast<const void *>(ext_kernel<D>));
