@@ -207,20 +207,22 @@ __device__ __forceinline__ Item locate(const Params &p, const Tables &t, int64_t
     int rem = static_cast<int>(w - t.off[it.b]);
     it.kh = rem / per;
     rem -= it.kh * per;
-    int q = 0;
+    // a request's query blocks in decreasing order (causal blocks shrink towards the first
+    // token), so the items handed out last are the smallest and the CTAs finish together
+    int q = 0;   // place of the block in that order
     if (one) {
         q = rem;
         rem = 0;
     } else {
         for (;; ++q) {
-            const int c = chunks_of(p, block_keys(p, it.L, it.n, q));
+            const int c = chunks_of(p, block_keys(p, it.L, it.n, nq - 1 - q));
             if (rem < c) break;
             rem -= c;
         }
     }
-    it.qblk = q;
+    it.qblk = nq - 1 - q;
     it.c = rem;
-    const int kmax = block_keys(p, it.L, it.n, q);
+    const int kmax = block_keys(p, it.L, it.n, it.qblk);
     it.nch = chunks_of(p, kmax);
     // the block's nch pieces are made equal (a multiple of 64 keys, at most p.chunk)
     const int span = ((kmax + it.nch - 1) / it.nch + kTile - 1) / kTile * kTile;
@@ -1040,7 +1042,7 @@ __global__ void __launch_bounds__(256) ext_merge_kernel(const Params p, int64_t 
     const int nch = chunks_of(p, block_keys(p, L, n, qblk));
     if (nch <= 1) return;
     int64_t w0 = p.ioff[b] + static_cast<int64_t>(kh) * per_head_items(p, L, n);
-    for (int q = 0; q < qblk; ++q) w0 += chunks_of(p, block_keys(p, L, n, q));
+    for (int q = qblk + 1; q < nq; ++q) w0 += chunks_of(p, block_keys(p, L, n, q));   // blocks before it in item order
     for (int i = threadIdx.x; i < kRows * (D / 4); i += blockDim.x) {
         const int r = i / (D / 4), d4 = i % (D / 4);
         const int tok = r >> p.g_shift, hh = r & (p.g - 1);
