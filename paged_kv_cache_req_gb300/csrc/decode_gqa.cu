@@ -180,7 +180,8 @@ struct Tile {
 // (U units), span s = j * U + u, and CTA c takes spans c, c + grid, ...; an item
 // is the real tiles of one row inside one span.  With two or three items per
 // CTA, dealing whole pieces leaves some CTAs with half again the average work;
-// equal spans leave them within one stand-in tile of each other.  Cutting every
+// equal spans leave them within a few tiles of each other.  (Three stand-in tiles:
+// a traced item start and finish cost about what 2-3 tiles take.)  Cutting every
 // unit's sequence at the same places keeps U neighbouring CTAs on the same keys of
 // different kv heads at the same time, so the DRAM rows of a key (all kv heads side
 // by side) are read together, as in the piece order.  A row that a span
@@ -188,7 +189,7 @@ struct Tile {
 // the span's first item (its row began at or before the span's first tile), else
 // to slot 1 (only the span's last item can be cut there); merge_spans_kernel
 // combines them.
-constexpr int kSegCost = 1;
+constexpr int kSegCost = 3;
 
 // Work units of request b with L keys: items (pieces, all units) or tiles of one
 // unit's row (spans).
