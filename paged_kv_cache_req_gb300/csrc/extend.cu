@@ -12,14 +12,14 @@
 // the tensor cores run the next tile's Q K^T and the groups' P V while the
 // groups compute their exponentials.  Per CTA:
 //   warps 8, 15  producers of K and of V tiles, each through a ring of its own
-//              (2 stages, 4 at head_dim 64), so K runs ahead as soon as a Q K^T
+//              (2 and 3 stages, 4 each at head_dim 64), so K runs ahead as soon as a Q K^T
 //              has run while V waits for P V: one TMA box per page per slab, one
 //              copy per lane, pool rows looked up 32 boxes at a time; pages under
 //              8 keys are gathered row by row with cp.async instead.  Warp 8 also
 //              claims the CTA's items and publishes them to every warp;
 //   warp 9     loads the q blocks (one 3-D box per 64-dim slab, rows
-//              token-major) into two buffers, the next item's while this one
-//              runs, and issues S = Q K^T (M = 128, N = 128) for tile n into
+//              token-major; at head_dim 64 into two buffers, the next item's
+//              while this one runs), and issues S = Q K^T (M = 128, N = 128) for tile n into
 //              one of two 128-column score buffers in TMEM;
 //   warp 10    O_g += P_g V_g (K = 64 keys, N = head_dim) for each group g:
 //              its half of the tile's keys into its own accumulator, P read
@@ -55,13 +55,20 @@ constexpr int kItemReaders = 16;           // warps that read every queued item
 
 template <int D>
 struct Cfg {
-    static constexpr int kStages = D == 128 ? 2 : 4;           // depth of the K ring and of the V ring (128 KB in all)
+    // Shared memory at head_dim 128 (192 KB of 227): one q block (the next item's
+    // is requested when this one's last Q K^T has completed), a 2-stage K ring and
+    // a 3-stage V ring.  V is consumed a softmax later than K, so its deeper ring
+    // lets its copies run further ahead; this split timed 1-3 % faster than two q
+    // blocks with two stages each.
+    static constexpr int kQBufs = D == 128 ? 1 : 2;            // q blocks: this item's (and the next)
+    static constexpr int kKStages = D == 128 ? 2 : 4;          // depth of the K ring
+    static constexpr int kVStages = D == 128 ? 3 : 4;          // depth of the V ring
     static constexpr int kSl = D / 64;                         // 64-dim slabs
     static constexpr int kQBytes = kSl * kRows * 128;          // one q block, SW128 K-major
     static constexpr int kKBytes = kSl * kTile * 128;          // one K (or V) tile
-    static constexpr int kOffQ = 0;                            // two q blocks: this item's and the next
-    static constexpr int kOffKV = kOffQ + 2 * kQBytes;         // K ring, then V ring
-    static constexpr int kOffBar = kOffKV + 2 * kStages * kKBytes;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffKV = kOffQ + kQBufs * kQBytes;    // K ring, then V ring
+    static constexpr int kOffBar = kOffKV + (kKStages + kVStages) * kKBytes;
     static constexpr int kNumBars = 56;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;    // tmem slot, abort flag, scan scratch
     static constexpr int kOffStats = kOffMisc + 128;           // [2 items][2 groups][128 rows] of (m, l) for the epilogue
@@ -402,8 +409,8 @@ __global__ void __maxnreg__(128)
 ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
            const __grid_constant__ CUtensorMap tmv) {
     using C = Cfg<D>;
-    constexpr int kStages = C::kStages;
-    static_assert(kBarCount <= C::kNumBars && kStages <= 4, "barrier slots");
+    constexpr int kKStages = C::kKStages, kVStages = C::kVStages, kQBufs = C::kQBufs;
+    static_assert(kBarCount <= C::kNumBars && kKStages <= 4 && kVStages <= 4 && kQBufs <= 2, "barrier slots");
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     unsigned char *sQ = smem + C::kOffQ;
@@ -439,9 +446,11 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             mbar_init(&bars[kSFree0 + i], 1);   // score buffer i: both groups' P V that read P over it done
         }
         for (int i = 0; i < 4; ++i) mbar_init(&bars[kPFull0 + i], 4);   // group i / 2's four warps stored P in buffer i % 2
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kKStages; ++s) {
             mbar_init(&bars[kKFull0 + s], 1);
             mbar_init(&bars[kKEmpty0 + s], 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
             mbar_init(&bars[kVFull0 + s], 1);
             mbar_init(&bars[kVEmpty0 + s], 1);
         }
@@ -488,7 +497,8 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
         const int nops = nbox * C::kSl;
         const int j_box = (lane / C::kSl) & (nbox - 1), sl_op = lane % C::kSl;
         uint64_t *fulls = &bars[is_v ? kVFull0 : kKFull0], *empties = &bars[is_v ? kVEmpty0 : kKEmpty0];
-        unsigned char *ring_base = sKV + (is_v ? kStages * C::kKBytes : 0);
+        unsigned char *ring_base = sKV + (is_v ? kKStages * C::kKBytes : 0);
+        const uint32_t stages = is_v ? kVStages : kKStages;   // depth of this warp's ring
         const uint16_t *pool = is_v ? p.v_pool : p.k_pool;
         const int64_t pool_stride = is_v ? p.v_stride : p.k_stride;
         uint32_t n = 0, kpub = 0, issued = 0;   // tiles; tiles whose copies were issued
@@ -506,7 +516,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             else cp_async_wait<0>();
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&fulls[n_arr % kStages]);
+            if (lane == 0) mbar_arrive(&fulls[n_arr % stages]);
             ++n_arr;
             --pend;
         };
@@ -580,11 +590,11 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                             bad |= rr[q] == -2;
                         }
                         if (bad && !is_v) raise_flag(p.err, PKV_DEVERR_RANGE);
-                        const int s = n % kStages;
-                        // the stage frees once the Q K^T / P V of tile n - kStages ran, which
+                        const int s = static_cast<int>(n % stages);
+                        // the stage frees once the Q K^T / P V of tile n - stages ran, which
                         // waits for that tile's full barrier: settle it first
-                        while (pend > static_cast<uint32_t>(kStages - 1)) settle_one();
-                        if (lane == 0) ok = wait_bar(&empties[s], ((n / kStages) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
+                        while (pend > stages - 1) settle_one();
+                        if (lane == 0) ok = wait_bar(&empties[s], ((n / stages) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
                         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                         if (!ok) break;
                         constexpr int CPR = D / 8;       // 16-byte chunks per row
@@ -624,10 +634,10 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                         int row = __shfl_sync(0xffffffffu, (bx0 >> 5) == win ? cur : nxt, (bx0 & 31) + j_box);
                         if (lane >= nops) row = -1;
                         if (row == -2 && sl_op == 0 && !is_v) raise_flag(p.err, PKV_DEVERR_RANGE);
-                        const int s = n % kStages;
+                        const int s = static_cast<int>(n % stages);
                         const uint32_t valid = __ballot_sync(0xffffffffu, row >= 0);
                         unsigned char *dst = ring_base + s * C::kKBytes + sl_op * kTile * 128 + j_box * box * 128;
-                        if (lane == 0) ok = wait_bar(&empties[s], ((n / kStages) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
+                        if (lane == 0) ok = wait_bar(&empties[s], ((n / stages) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
                         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                         if (!ok) break;
                         if (row == -2) {   // a page outside the pool reads as zeros
@@ -650,20 +660,21 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
         }
         settle_all();
         if (lane == 0)   // drain: the copies this warp issued have landed
-            for (uint32_t k = issued > kStages ? issued - kStages : 0; k < issued; ++k)
-                drain_wait(&fulls[k % kStages], (k / kStages) & 1);
+            for (uint32_t k = issued > stages ? issued - stages : 0; k < issued; ++k)
+                drain_wait(&fulls[k % stages], (k / stages) & 1);
         __syncwarp();
     } else if (warp == kQkWarp) {
         // ------------------------------------------------------------ S = Q K^T
-        // This warp also loads the q blocks, into two buffers: item i + 1's block is
+        // This warp also loads the q blocks.  With two buffers, item i + 1's block is
         // requested once item i's first tile is issued (its buffer was freed by the
-        // completion of item i - 1's last q.k), so q never waits at an item boundary.
+        // completion of item i - 1's last q.k), so q never waits at an item boundary;
+        // with one, it is requested once item i's last q.k has completed.
         const uint32_t idesc = tc05::idesc_bf16_f32(kRows, kTile, false, false);
         uint32_t n = 0, iq = 0, q_issued = 0;
         bool ok = true;
         auto load_q = [&](const Item &qi, uint32_t slot_use) {   // slot_use: how many q loads came before
-            const int sl = slot_use & 1;
-            ok = warp_wait(ok, &bars[kQEmpty0 + sl], ((slot_use >> 1) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
+            const int sl = slot_use % kQBufs;
+            ok = warp_wait(ok, &bars[kQEmpty0 + sl], ((slot_use / kQBufs) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
             if (ok && lane == 0) {
                 mbar_arrive_expect_tx(&bars[kQFull0 + sl], C::kQBytes);
                 const int tok = qi.qo0 + qi.qblk * p.T;
@@ -682,12 +693,12 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             bool nx_req = false;
             if (it.n_tiles > 0) {
                 if (!q_req) load_q(it, iq);
-                const int sl = iq & 1;
-                ok = warp_wait(ok, &bars[kQFull0 + sl], (iq >> 1) & 1, abort_flag, p.err, p.wait_ns);
+                const int sl = iq % kQBufs;
+                ok = warp_wait(ok, &bars[kQFull0 + sl], (iq / kQBufs) & 1, abort_flag, p.err, p.wait_ns);
                 for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
                     // score buffer n mod 2 is free once both groups' P V of tile n - 2 are done
-                    const int s = n % kStages, b = n & 1;
-                    ok = warp_wait(ok, &bars[kKFull0 + s], (n / kStages) & 1, abort_flag, p.err, p.wait_ns);
+                    const int s = n % kKStages, b = n & 1;
+                    ok = warp_wait(ok, &bars[kKFull0 + s], (n / kKStages) & 1, abort_flag, p.err, p.wait_ns);
                     ok = warp_wait(ok, &bars[kSFree0 + b], ((n >> 1) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
                     if (!ok) break;
                     tc05::fence_after_sync();
@@ -707,7 +718,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                         if (ti == it.n_tiles - 1) tc05::commit(&bars[kQEmpty0 + sl]);
                     }
                     __syncwarp();
-                    if (ti == 0 && nx.w >= 0 && nx.n_tiles > 0) {
+                    if (ti == (kQBufs == 2 ? 0 : it.n_tiles - 1) && nx.w >= 0 && nx.n_tiles > 0) {
                         load_q(nx, iq + 1);
                         nx_req = true;
                     }
@@ -719,7 +730,7 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
         }
         if (lane == 0) {
             // q loads issued but not waited for have landed before shared memory is released
-            for (uint32_t k = iq; k < q_issued; ++k) drain_wait(&bars[kQFull0 + (k & 1)], (k >> 1) & 1);
+            for (uint32_t k = iq; k < q_issued; ++k) drain_wait(&bars[kQFull0 + k % kQBufs], (k / kQBufs) & 1);
             tc05::commit(&bars[kFinalQk]);
             drain_wait(&bars[kFinalQk], 0);
         }
@@ -737,10 +748,10 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             if (it.w < 0) break;
             if (it.n_tiles == 0) continue;
             for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
-                const int s = n % kStages, b = n & 1;
-                ok = warp_wait(ok, &bars[kVFull0 + s], (n / kStages) & 1, abort_flag, p.err, p.wait_ns);
+                const int s = n % kVStages, b = n & 1;
+                ok = warp_wait(ok, &bars[kVFull0 + s], (n / kVStages) & 1, abort_flag, p.err, p.wait_ns);
                 if (!ok) break;
-                unsigned char *v = sKV + (kStages + s) * C::kKBytes;
+                unsigned char *v = sKV + (kKStages + s) * C::kKBytes;
                 const int n_valid = it.k1 - (it.k0 + ti * kTile);
                 if (n_valid < kTile) {   // key rows past the chunk hold stale data: zero them
                     for (int i = lane; i < (kTile - n_valid) * C::kSl * 8; i += 32) {
