@@ -310,10 +310,11 @@ def decode_config(wl, cross_mode, alloc, world, fused=False):
             "l2": l2_note(total_bytes), "parallelism": parallelism(world)}
 
 
-def extend_config(ew, world):
+def extend_config(ew, world, token_table=False):
     flops, step_bytes_, _ = extend_amounts(ew)
     return {"workload": WORKLOAD_TEXT[ew.name], "name": ew.name, "batch": ew.batch,
             "query_rows": int(ew.qo_lens.sum()), "keys": int(ew.seq_lens.sum()),
+            "pages": "read from req_to_token (no pkv_build_indices)" if token_table else "kv_indptr / kv_indices",
             "attention_flops_per_step": flops, "algorithmic_bytes_per_step": step_bytes_,
             "l2": l2_note(step_bytes_), "parallelism": parallelism(world)}
 
@@ -588,7 +589,7 @@ def reference_extend(args, world):
     return {"impl": "reference", "metric": metric, "value": round(value, 6), "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": extend_config(ew, world),
+            "config": extend_config(ew, world, token_table=args.fused),
             "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": threads, "kind": "oracle",
                              "sample": "each step: " + desc},
             "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -601,7 +602,7 @@ def measure_extend(opts, world, rank, local, dist):
     oracle.build()
     ew = make_extend_workload(opts.workload, seed=opts.seed, batch=opts.batch)
     metric, unit, bound = EXTEND_METRIC[opts.workload]
-    step = ExtendStep(ew, device="cuda", kv_chunk=opts.kv_chunk, seed=opts.seed)
+    step = ExtendStep(ew, device="cuda", kv_chunk=opts.kv_chunk, seed=opts.seed, token_table=opts.fused)
     flops, step_bytes_, launch_bytes = extend_amounts(ew)
     amount = flops / 1e12 if unit == "TFLOP/s" else step_bytes_ / 1e9
     launch_amount = flops / 1e12 if unit == "TFLOP/s" else launch_bytes / 1e9
@@ -691,7 +692,7 @@ def measure_extend(opts, world, rank, local, dist):
         "metric": metric, "value": round(value, 3), "unit": unit, "n_gpus": world, "steps": opts.steps,
         "warmup": opts.warmup, "ms_per_step": round(tot_ms / opts.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "accumulate": "fp32", "data": "synthetic",
-        "config": extend_config(ew, world),
+        "config": extend_config(ew, world, token_table=opts.fused),
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": round(world * amount * opts.steps / (e_ms / 1e3), 3), "unit": unit,
@@ -883,8 +884,11 @@ PER_CONFIG = (
     ("llama3_8b", "paged", 100, True),
     ("deepseek_v3_mla", "paged", 100, False),
     ("llama3_8b_verify", "paged", 100, False),
+    ("llama3_8b_verify", "paged", 100, True),
     ("qwen3_0p6b_prefill", "paged", 100, False),
+    ("qwen3_0p6b_prefill", "paged", 100, True),
     ("hunyuan_image_spans", "paged", 50, False),
+    ("hunyuan_image_spans", "paged", 50, True),
     ("encoder_merge", "paged", 200, False),
 )
 ONE_THREAD_BASELINE = ("tiny_gqa", "qwen3_0p6b")
@@ -984,7 +988,8 @@ def main(argv=None):
                     help="headline workload only (no per_config entries for the other recipes)")
     ap.add_argument("--fused", action="store_true",
                     help="GQA decode reads its pages from req_to_token and stores the new rows itself "
-                         "(one launch per attention problem, no pkv_build_indices / pkv_store)")
+                         "(one launch per attention problem, no pkv_build_indices / pkv_store); "
+                         "the multi-query steps read their pages from req_to_token (no pkv_build_indices)")
     ap.add_argument("--alloc", action="store_true",
                     help="allocate each step's new slots on the device (pkv_alloc_extend + pkv_write_req_to_token)")
     ap.add_argument("--profile-run", action="store_true",

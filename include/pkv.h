@@ -312,7 +312,7 @@ pkv_status pkv_ragged_gather(const void *k_pool, const void *v_pool, int64_t num
  * of two in [1, 1024]; pages under 8 keys are gathered row by row).
  */
 typedef struct pkv_extend_args {
-    int32_t layout;            /* PKV_LAYOUT_CSR or PKV_LAYOUT_BLOCK_TABLE */
+    int32_t layout;            /* PKV_LAYOUT_CSR, PKV_LAYOUT_BLOCK_TABLE or PKV_LAYOUT_REQ_TO_TOKEN */
     int32_t batch;             /* B >= 0 */
     int32_t num_q_heads;       /* Hq */
     int32_t num_kv_heads;      /* Hkv; Hq / Hkv in {1, 2, 4, 8, 16} */
@@ -337,9 +337,16 @@ typedef struct pkv_extend_args {
     const int32_t *kv_indices;       /* CSR pages */
     const int32_t *kv_last_page_len; /* CSR [B] */
     const int32_t *block_table;      /* BLOCK_TABLE [B, block_table_width] */
-    const int32_t *seq_lens;         /* BLOCK_TABLE [B] */
+    const int32_t *seq_lens;         /* BLOCK_TABLE and REQ_TO_TOKEN [B] */
     void *out;                 /* bf16 [total_q, Hq, head_dim] */
     float *lse;                /* fp32 [total_q, Hq] natural-log softmax denominators; nullable */
+    /* REQ_TO_TOKEN (the same fields as pkv_decode_args) */
+    const int32_t *req_to_token;     /* int32 [r2t_rows, r2t_row_stride] */
+    int64_t r2t_rows;
+    int64_t r2t_row_stride;
+    int64_t r2t_width;               /* valid columns of a row */
+    const int32_t *req_pool_idx;     /* [B] row of request b */
+    const int32_t *kv_start;         /* [B] column of b's first key (a multiple of page_size), or NULL for 0 */
 } pkv_extend_args;
 
 /*
@@ -356,7 +363,11 @@ typedef struct pkv_extend_args {
  *     out[j,h,:] = softmax_{t < kv_end[j]}(sm_scale * q[j,h,:] . K[t, kh, :]) V[t, kh, :]
  * kv_end[j] = 0 gives out = 0, lse = -inf; kv_end outside [0, L_b] raises
  * PKV_DEVERR_RANGE and the row is treated as empty.  The new tokens' K/V must
- * already be in the pool (pkv_store first).  Arithmetic: bf16 inputs, fp32
+ * already be in the pool (pkv_store first).  PKV_LAYOUT_REQ_TO_TOKEN reads the
+ * pages straight from the token table as pkv_decode does (L_b = seq_lens[b], key
+ * t at slot req_to_token[row, s + t - t % ps] + t % ps with row =
+ * req_pool_idx[b] and s = kv_start[b] or 0; the same range and alignment
+ * checks), so no pkv_build_indices launch is needed.  Arithmetic: bf16 inputs, fp32
  * accumulation and softmax, bf16 output.  The key range of a block of rows may
  * be split into kv_chunk chunks whose partials are merged by log-sum-exp.
  * workspace: at least pkv_extend_workspace_size(args) bytes, 256-byte aligned,

@@ -73,6 +73,8 @@ class ExtendArgs(ctypes.Structure):
         ("kv_indptr", ctypes.c_void_p), ("kv_indices", ctypes.c_void_p), ("kv_last_page_len", ctypes.c_void_p),
         ("block_table", ctypes.c_void_p), ("seq_lens", ctypes.c_void_p),
         ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p),
+        ("req_to_token", ctypes.c_void_p), ("r2t_rows", ctypes.c_int64), ("r2t_row_stride", ctypes.c_int64),
+        ("r2t_width", ctypes.c_int64), ("req_pool_idx", ctypes.c_void_p), ("kv_start", ctypes.c_void_p),
     ]
 
 
@@ -283,8 +285,9 @@ def pkv_encoder_merge(buffer, block_ids, positions, hidden, err_flags, filled=No
 
 def make_extend_args(layout, q, k_pool, v_pool, out, qo_indptr, *, page_size, sm_scale, max_seq_len,
                      kv_end=None, kv_indptr=None, kv_indices=None, kv_last_page_len=None, block_table=None,
-                     seq_lens=None, lse=None, kv_chunk=0) -> ExtendArgs:
-    """q [total_q, Hq, D]; pools [slots, Hkv, D]."""
+                     seq_lens=None, lse=None, kv_chunk=0, req_to_token=None, req_pool_idx=None,
+                     kv_start=None) -> ExtendArgs:
+    """q [total_q, Hq, D]; pools [slots, Hkv, D]; req_to_token [rows, width] (token-table layout)."""
     T, hq, d = q.shape
     a = ExtendArgs()
     a.layout, a.batch = layout, qo_indptr.numel() - 1
@@ -294,9 +297,13 @@ def make_extend_args(layout, q, k_pool, v_pool, out, qo_indptr, *, page_size, sm
     a.total_q, a.num_slots = T, k_pool.shape[0]
     a.k_row_stride, a.v_row_stride = k_pool.stride(0), v_pool.stride(0)
     a.kv_indices_len = kv_indices.numel() if kv_indices is not None else 0
+    if req_to_token is not None:
+        a.r2t_rows, a.r2t_width = req_to_token.shape
+        a.r2t_row_stride = req_to_token.stride(0)
     tensors = (("q", q), ("k_pool", k_pool), ("v_pool", v_pool), ("qo_indptr", qo_indptr), ("kv_end", kv_end),
                ("kv_indptr", kv_indptr), ("kv_indices", kv_indices), ("kv_last_page_len", kv_last_page_len),
-               ("block_table", block_table), ("seq_lens", seq_lens), ("out", out), ("lse", lse))
+               ("block_table", block_table), ("seq_lens", seq_lens), ("out", out), ("lse", lse),
+               ("req_to_token", req_to_token), ("req_pool_idx", req_pool_idx), ("kv_start", kv_start))
     for name, t in tensors:
         setattr(a, name, None if t is None else _p(t).value)
     # the struct holds raw pointers: keep the tensors alive as long as it lives

@@ -97,6 +97,9 @@ struct Params {
                               // written by CTA 0 for the merge kernel
     const uint16_t *k_pool, *v_pool;   // pages under 8 keys: rows gathered with cp.async
     int64_t k_stride, v_stride;        // elements between pool rows
+    // PKV_LAYOUT_REQ_TO_TOKEN: the token table itself
+    const int32_t *r2t, *req_pool_idx, *kv_start;
+    int64_t r2t_rows, r2t_stride, r2t_width;
 };
 
 // Keys of request b (0 and a flag for malformed inputs).
@@ -112,6 +115,17 @@ __device__ __forceinline__ int key_count(const Params &p, int b, int64_t &base, 
             return 0;
         }
         L = n > 0 ? ((n - 1) << p.ps_shift) + last : 0;
+        cap = L;
+    } else if (p.layout == PKV_LAYOUT_REQ_TO_TOKEN) {
+        // the request's keys are columns s .. s + L - 1 of its row ("From slots to a page table")
+        const int64_t row = p.req_pool_idx[b], st = p.kv_start ? p.kv_start[b] : 0;
+        L = p.seq_lens[b];
+        if (row < 0 || row >= p.r2t_rows || st < 0 || (st & p.ps_mask) || L < 0 || st + L > p.r2t_width) {
+            if (report) raise_flag(p.err, PKV_DEVERR_RANGE);
+            base = 0;
+            return 0;
+        }
+        base = row * p.r2t_stride + st;
         cap = L;
     } else {
         base = static_cast<int64_t>(b) * p.bt_width;
@@ -185,7 +199,8 @@ __device__ __forceinline__ Req get_req(const Params &p, const Tables &t, int b) 
     r.L = t.keys[b];
     r.n = t.nq[b];
     r.qo0 = t.qo0[b];
-    r.base = p.layout == PKV_LAYOUT_CSR ? static_cast<int64_t>(t.base[b]) : static_cast<int64_t>(b) * p.bt_width;
+    // cached for the CSR and token-table layouts (the host caches only when it fits an int)
+    r.base = p.layout == PKV_LAYOUT_BLOCK_TABLE ? static_cast<int64_t>(b) * p.bt_width : static_cast<int64_t>(t.base[b]);
     return r;
 }
 
@@ -563,33 +578,43 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
             if (more && lane == 0) got = atomicAdd(p.counter, 1);
             if (it.n_tiles > 0) {
                 // pool row of box bx: -1 past the item's keys, -2 for a page outside the pool
+                // pool row of key k of the item: -2 for a page outside the pool, -3 for a
+                // token-table page start that is not a multiple of the page size
+                auto pool_row = [&](int k) -> int {
+                    if (p.layout == PKV_LAYOUT_REQ_TO_TOKEN) {   // the slot of the page's first key, + the offset
+                        const int first = __ldg(p.r2t + it.base + (k & ~p.ps_mask));
+                        if (first < 0 || first >= (p.num_pages << p.ps_shift)) return -2;
+                        if (first & p.ps_mask) return -3;
+                        return first + (k & p.ps_mask);
+                    }
+                    const int page = __ldg(tab + it.base + (k >> p.ps_shift));
+                    if (page < 0 || page >= p.num_pages) return -2;
+                    return static_cast<int>((static_cast<int64_t>(page) << p.ps_shift) + (k & p.ps_mask));
+                };
+                // pool row of box bx: -1 past the item's keys
                 auto box_row = [&](int bx) -> int {
                     const int kb = it.k0 + bx * box;
-                    if (kb >= it.k1) return -1;
-                    const int page = __ldg(tab + it.base + (kb >> p.ps_shift));
-                    if (page < 0 || page >= p.num_pages) return -2;
-                    return static_cast<int>((static_cast<int64_t>(page) << p.ps_shift) + (kb & p.ps_mask));
+                    return kb >= it.k1 ? -1 : pool_row(kb);
                 };
                 if (gather) {
                     constexpr int kRowsPerLane = kTile / 32;
                     for (int ti = 0; ti < it.n_tiles && ok; ++ti, ++n) {
                         const int kt0 = it.k0 + ti * kTile;
-                        // pool row of key j of the tile: -1 past the item's keys, -2 outside the pool
+                        // pool row of key j of the tile: -1 past the item's keys
                         auto key_row = [&](int j) -> int {
                             const int kk = kt0 + j;
-                            if (kk >= it.k1) return -1;
-                            const int page = __ldg(tab + it.base + (kk >> p.ps_shift));
-                            if (page < 0 || page >= p.num_pages) return -2;
-                            return static_cast<int>((static_cast<int64_t>(page) << p.ps_shift) + (kk & p.ps_mask));
+                            return kk >= it.k1 ? -1 : pool_row(kk);
                         };
                         int rr[kRowsPerLane];
-                        bool bad = false;
+                        bool bad_range = false, bad_start = false;
 #pragma unroll
                         for (int q = 0; q < kRowsPerLane; ++q) {
                             rr[q] = key_row(lane + 32 * q);
-                            bad |= rr[q] == -2;
+                            bad_range |= rr[q] == -2;
+                            bad_start |= rr[q] == -3;
                         }
-                        if (bad && !is_v) raise_flag(p.err, PKV_DEVERR_RANGE);
+                        if (bad_range && !is_v) raise_flag(p.err, PKV_DEVERR_RANGE);
+                        if (bad_start && !is_v) raise_flag(p.err, PKV_DEVERR_CONTIG);
                         const int s = static_cast<int>(n % stages);
                         // the stage frees once the Q K^T / P V of tile n - stages ran, which
                         // waits for that tile's full barrier: settle it first
@@ -633,14 +658,14 @@ ext_kernel(const Params p, const __grid_constant__ CUtensorMap tmq, const __grid
                         const int bx0 = ti * nbox;
                         int row = __shfl_sync(0xffffffffu, (bx0 >> 5) == win ? cur : nxt, (bx0 & 31) + j_box);
                         if (lane >= nops) row = -1;
-                        if (row == -2 && sl_op == 0 && !is_v) raise_flag(p.err, PKV_DEVERR_RANGE);
+                        if (row <= -2 && sl_op == 0 && !is_v) raise_flag(p.err, row == -2 ? PKV_DEVERR_RANGE : PKV_DEVERR_CONTIG);
                         const int s = static_cast<int>(n % stages);
                         const uint32_t valid = __ballot_sync(0xffffffffu, row >= 0);
                         unsigned char *dst = ring_base + s * C::kKBytes + sl_op * kTile * 128 + j_box * box * 128;
                         if (lane == 0) ok = wait_bar(&empties[s], ((n / stages) & 1) ^ 1, abort_flag, p.err, p.wait_ns);
                         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                         if (!ok) break;
-                        if (row == -2) {   // a page outside the pool reads as zeros
+                        if (row <= -2) {   // a bad page reads as zeros
                             for (int o = 0; o < box * 128; o += 16) *reinterpret_cast<uint4 *>(dst + o) = make_uint4(0, 0, 0, 0);
                             fence_proxy_async_smem();   // for the tensor cores and later TMA writes
                         }
@@ -1183,8 +1208,11 @@ static pkv_status validate(const pkv_extend_args *a, bool check_ptrs) {
     if (a->head_dim != 64 && a->head_dim != 128) return fail(PKV_ERR_UNSUPPORTED, "pkv_extend: head_dim 64 or 128");
     if (!is_pow2(a->page_size) || a->page_size > 1024)
         return fail(PKV_ERR_UNSUPPORTED, "pkv_extend: page_size must be a power of two in [1, 1024]");
-    if (a->layout != PKV_LAYOUT_CSR && a->layout != PKV_LAYOUT_BLOCK_TABLE)
-        return fail(PKV_ERR_INVALID_ARG, "pkv_extend: layout must be CSR or BLOCK_TABLE");
+    if (a->layout != PKV_LAYOUT_CSR && a->layout != PKV_LAYOUT_BLOCK_TABLE && a->layout != PKV_LAYOUT_REQ_TO_TOKEN)
+        return fail(PKV_ERR_INVALID_ARG, "pkv_extend: layout must be CSR, BLOCK_TABLE or REQ_TO_TOKEN");
+    if (a->layout == PKV_LAYOUT_REQ_TO_TOKEN &&
+        (a->r2t_rows < 0 || a->r2t_width < 0 || a->r2t_row_stride < a->r2t_width || a->r2t_width > INT32_MAX))
+        return fail(PKV_ERR_INVALID_ARG, "pkv_extend: bad req_to_token shape");
     if (a->kv_chunk < 0 || a->kv_chunk % kChunkUnit) return fail(PKV_ERR_INVALID_ARG, "pkv_extend: kv_chunk multiple of 64");
     const int64_t rowq = static_cast<int64_t>(a->num_kv_heads) * a->head_dim;
     if (a->k_row_stride < rowq || a->v_row_stride < rowq || a->k_row_stride % 8 || a->v_row_stride % 8)
@@ -1200,6 +1228,8 @@ static pkv_status validate(const pkv_extend_args *a, bool check_ptrs) {
         return fail(PKV_ERR_INVALID_ARG, "pkv_extend: CSR layout needs kv_indptr/kv_indices/kv_last_page_len");
     if (a->layout == PKV_LAYOUT_BLOCK_TABLE && (!a->block_table || !a->seq_lens || a->block_table_width < 0))
         return fail(PKV_ERR_INVALID_ARG, "pkv_extend: block-table layout needs block_table and seq_lens");
+    if (a->layout == PKV_LAYOUT_REQ_TO_TOKEN && (!a->req_to_token || !a->req_pool_idx || !a->seq_lens))
+        return fail(PKV_ERR_INVALID_ARG, "pkv_extend: token-table layout needs req_to_token, req_pool_idx, seq_lens");
     return PKV_OK;
 }
 
@@ -1245,6 +1275,12 @@ static pkv_status launch_t(const pkv_extend_args *a, const Plan &pl, void *ws, i
     p.v_pool = static_cast<const uint16_t *>(a->v_pool);
     p.k_stride = a->k_row_stride;
     p.v_stride = a->v_row_stride;
+    p.r2t = a->req_to_token;
+    p.req_pool_idx = a->req_pool_idx;
+    p.kv_start = a->kv_start;
+    p.r2t_rows = a->r2t_rows;
+    p.r2t_stride = a->r2t_row_stride;
+    p.r2t_width = a->r2t_width;
 
     CUtensorMap tmq, tmk, tmv;
     {   // q [total_q, Hq, D]: boxes of 64 dims x g heads x T tokens = 128 rows of 128 bytes
@@ -1283,7 +1319,9 @@ static pkv_status launch_t(const pkv_extend_args *a, const Plan &pl, void *ws, i
     size_t smem = C::kFixedSmem + (static_cast<size_t>(a->batch) + 1) * 4;
     if (smem > lim) return fail(PKV_ERR_UNSUPPORTED, "pkv_extend: batch too large for the on-chip item table");
     const size_t cached = smem + static_cast<size_t>(a->batch) * 16;
-    p.cache_requests = cached <= lim ? 1 : 0;
+    // a token-table base (row x stride + start) is cached as an int only when every one fits
+    const bool bases_fit = a->layout != PKV_LAYOUT_REQ_TO_TOKEN || a->r2t_rows * a->r2t_row_stride <= INT32_MAX;
+    p.cache_requests = cached <= lim && bases_fit ? 1 : 0;
     if (p.cache_requests) smem = cached;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(pl.items_max, sm_count()));
     if (cudaMemsetAsync(p.counter, 0, sizeof(int32_t), s) != cudaSuccess)

@@ -285,9 +285,13 @@ class ExtendStep:
         pkv_store           this step's new tokens' K/V -> their pool slots
         pkv_span_plan       (rows with segments) segment lists -> query rows and key bounds
         pkv_extend          attention of every query row over its visible keys
+
+    With ``token_table=True`` pkv_extend reads the pages straight from req_to_token
+    (PKV_LAYOUT_REQ_TO_TOKEN) and the step has no pkv_build_indices launch.
     """
 
-    def __init__(self, ew, device="cuda", kv_chunk: int = 0, seed: Optional[int] = None):
+    def __init__(self, ew, device="cuda", kv_chunk: int = 0, seed: Optional[int] = None, token_table: bool = False):
+        self.token_table = bool(token_table)
         self.ew = ew
         dev = self.device = torch.device(device)
         seed = ew.seed if seed is None else seed
@@ -345,14 +349,23 @@ class ExtendStep:
         self.in_buf = _pack(ins, dev)
         if self.kv_end is not None:
             self.seg = [getattr(self._seg_holder, "s%d" % i) for i in range(len(self.seg))]
-        self.args = B.make_extend_args(B.PKV_LAYOUT_CSR, self.q, self.k_pool, self.v_pool, self.out, self.qo_indptr,
-                                       page_size=ps, sm_scale=ew.sm_scale, max_seq_len=int(ew.seq_lens.max()),
-                                       kv_end=self.kv_end, kv_indptr=self.kv_indptr, kv_indices=self.kv_indices,
-                                       kv_last_page_len=self.kv_last, lse=self.lse, kv_chunk=kv_chunk)
+        if self.token_table:
+            self.args = B.make_extend_args(B.PKV_LAYOUT_REQ_TO_TOKEN, self.q, self.k_pool, self.v_pool, self.out,
+                                           self.qo_indptr, page_size=ps, sm_scale=ew.sm_scale,
+                                           max_seq_len=int(ew.seq_lens.max()), kv_end=self.kv_end,
+                                           seq_lens=self.seq_lens, req_to_token=self.r2t,
+                                           req_pool_idx=self.req_pool_idx, lse=self.lse, kv_chunk=kv_chunk)
+        else:
+            self.args = B.make_extend_args(B.PKV_LAYOUT_CSR, self.q, self.k_pool, self.v_pool, self.out, self.qo_indptr,
+                                           page_size=ps, sm_scale=ew.sm_scale, max_seq_len=int(ew.seq_lens.max()),
+                                           kv_end=self.kv_end, kv_indptr=self.kv_indptr, kv_indices=self.kv_indices,
+                                           kv_last_page_len=self.kv_last, lse=self.lse, kv_chunk=kv_chunk)
         self.ws_bytes = B.pkv_extend_workspace_size(self.args)
         self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8, device=dev)
 
     def build_indices(self):
+        if self.token_table:
+            return                                   # pkv_extend reads req_to_token itself
         ew = self.ew
         B.pkv_build_indices(self.r2t, self.req_pool_idx, self.seq_lens, ew.page_size, ew.num_pool_pages, self.err,
                             kv_indptr=self.kv_indptr, kv_indices=self.kv_indices, kv_last_page_len=self.kv_last)
@@ -374,7 +387,7 @@ class ExtendStep:
         self.attend()
 
     def launches_per_step(self) -> int:
-        return 3 + (1 if self.kv_end is not None else 0) + (1 if self.ws_bytes > 0 else 0)
+        return (2 if self.token_table else 3) + (1 if self.kv_end is not None else 0) + (1 if self.ws_bytes > 0 else 0)
 
     def check_errors(self) -> int:
         return int(self.err.item())

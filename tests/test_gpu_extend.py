@@ -54,6 +54,9 @@ def _run(B, r2t, rpi, num_pages, k, v, q, qo, lens, ps, kv_end=None, chunk=0, la
     if layout == "csr":
         args = B.make_extend_args(B.PKV_LAYOUT_CSR, qd, kd, vd, out, _dev(qo), kv_indptr=_dev(indptr),
                                   kv_indices=_dev(indices if len(indices) else [0]), kv_last_page_len=_dev(last), **kw)
+    elif layout == "token":
+        args = B.make_extend_args(B.PKV_LAYOUT_REQ_TO_TOKEN, qd, kd, vd, out, _dev(qo), seq_lens=_dev(lens),
+                                  req_to_token=_dev(r2t), req_pool_idx=_dev(rpi), **kw)
     else:
         args = B.make_extend_args(B.PKV_LAYOUT_BLOCK_TABLE, qd, kd, vd, out, _dev(qo), block_table=_dev(bt),
                                   seq_lens=_dev(lens), **kw)
@@ -67,16 +70,18 @@ def _run(B, r2t, rpi, num_pages, k, v, q, qo, lens, ps, kv_end=None, chunk=0, la
     return err.item(), bf16_to_f64(out), lse.double().cpu().numpy(), st, ref, ref_lse
 
 
+@pytest.mark.parametrize("layout", ["csr", "token"])
 @pytest.mark.parametrize("hq,hkv,d,ps", [(32, 8, 128, 64), (16, 16, 128, 16), (8, 1, 64, 8), (32, 4, 128, 32),
                                          (16, 1, 128, 64)])
-def test_extend_causal_mix(B, hq, hkv, d, ps):
-    # prefill (n = L), chunked prefill (n < L), one new token, 4 draft tokens, long prefix
+def test_extend_causal_mix(B, hq, hkv, d, ps, layout):
+    # prefill (n = L), chunked prefill (n < L), one new token, 4 draft tokens, long prefix;
+    # through the page list and straight through the token table
     lens = [300, 517, 129, 1000, 64, 3001]
     nq = [300, 200, 1, 4, 64, 37]
     case = _case(hq + d + ps, lens, nq, hq, hkv, d, ps)
-    e, gpu, g_lse, st, ref, ref_lse = _run(B, *case, lens, ps)
+    e, gpu, g_lse, st, ref, ref_lse = _run(B, *case, lens, ps, layout=layout)
     assert e == 0 and st == oracle.OK
-    assert_close(gpu, ref, "extend out hq=%d hkv=%d d=%d ps=%d" % (hq, hkv, d, ps))
+    assert_close(gpu, ref, "extend out hq=%d hkv=%d d=%d ps=%d %s" % (hq, hkv, d, ps, layout))
     assert_close(g_lse, ref_lse, "extend lse")
 
 
@@ -86,16 +91,16 @@ def test_extend_small_pages_gathered_by_rows(B, ps, hq, hkv, d):
     # pages under 8 keys: the producer gathers rows with cp.async instead of TMA boxes
     lens = [300, 77, 1000, 1, 129]
     nq = [300, 5, 64, 1, 16]
-    for chunk in (0, 64):
+    for chunk, layout in ((0, "csr"), (64, "csr"), (64, "token")):
         case = _case(ps * 10 + d + chunk, lens, nq, hq, hkv, d, ps)
-        e, gpu, g_lse, st, ref, ref_lse = _run(B, *case, lens, ps, chunk=chunk)
+        e, gpu, g_lse, st, ref, ref_lse = _run(B, *case, lens, ps, chunk=chunk, layout=layout)
         assert e == 0 and st == oracle.OK
-        assert_close(gpu, ref, "extend ps=%d d=%d chunk=%d" % (ps, d, chunk))
+        assert_close(gpu, ref, "extend ps=%d d=%d chunk=%d %s" % (ps, d, chunk, layout))
         assert_close(g_lse, ref_lse, "extend lse ps=%d" % ps)
 
 
 @pytest.mark.parametrize("chunk", [64, 192, 1024])
-@pytest.mark.parametrize("layout", ["csr", "block_table"])
+@pytest.mark.parametrize("layout", ["csr", "block_table", "token"])
 def test_extend_split_keys_and_layouts(B, chunk, layout):
     lens = [2000, 77, 900, 4100]
     nq = [4, 77, 16, 9]
@@ -228,3 +233,61 @@ def test_extend_flags_out_of_pool_pages(B, ps):
     st, refz, _ = oracle.extend(bits(q), bits(kz), bits(vz), r2t, rpi, lens, qo, kv_end, 1 / math.sqrt(128))
     assert st == oracle.OK
     assert_close(bf16_to_f64(out)[:qo[1]], refz[:qo[1]], "out-of-pool page reads as zeros, ps=%d" % ps)
+
+
+def test_extend_token_table_matches_the_page_list_bit_for_bit(B):
+    """The token-table layout reads the same pool rows in the same order as the page list, so
+    the two give the same bits (each is also checked against the oracle above)."""
+    lens = [700, 65, 2049, 300]
+    nq = [128, 65, 7, 300]
+    case = _case(77, lens, nq, 32, 8, 128, 16)
+    outs = [_run(B, *case, lens, 16, chunk=256, layout=lay) for lay in ("csr", "token")]
+    assert outs[0][0] == 0 and outs[1][0] == 0
+    assert np.array_equal(outs[0][1], outs[1][1]) and np.array_equal(outs[0][2], outs[1][2])
+
+
+@pytest.mark.parametrize("ps", [2, 16])
+def test_extend_token_table_flags_bad_rows_and_page_starts(B, ps):
+    """Token-table layout: a page start that is not a multiple of the page size raises
+    PKV_DEVERR_CONTIG and its keys read as zeros (both producers); a request row outside the
+    table raises PKV_DEVERR_RANGE and the request is empty; the other requests stay exact."""
+    dev = torch.device("cuda")
+    lens, nq = [40, 24, 30], [4, 3, 5]
+    r2t, rpi, num_pages, k, v, q, qo = _case(ps + 1, lens, nq, 16, 4, 128, ps)
+    scale = 1 / math.sqrt(128)
+    kv_end = np.concatenate([np.arange(L - n, L) + 1 for L, n in zip(lens, nq)]).astype(np.int32)
+    st, ref, _ = oracle.extend(bits(q), bits(k), bits(v), r2t, rpi, lens, qo, kv_end, scale)
+    assert st == oracle.OK
+
+    def call(r2t_d, rpi_d):
+        out = torch.zeros(tuple(q.shape), dtype=torch.bfloat16, device=dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        args = B.make_extend_args(B.PKV_LAYOUT_REQ_TO_TOKEN, q.to(dev), k.to(dev), v.to(dev), out, _dev(qo),
+                                  page_size=ps, sm_scale=scale, max_seq_len=max(lens), seq_lens=_dev(lens),
+                                  req_to_token=r2t_d, req_pool_idx=rpi_d)
+        ws = torch.empty(max(B.pkv_extend_workspace_size(args), 256), dtype=torch.uint8, device=dev)
+        B.pkv_extend(args, ws, err)
+        torch.cuda.synchronize()
+        return int(err.item()), bf16_to_f64(out)
+
+    # request 0's first page start moved off the page grid: its keys there read as zeros
+    bad = np.array(r2t, dtype=np.int32, copy=True)
+    row0 = int(rpi[0])
+    page = int(bad[row0, 0]) // ps
+    bad[row0, 0] += 1
+    e, gpu = call(_dev(bad), _dev(rpi))
+    assert e & B.PKV_DEVERR_CONTIG and not e & B.PKV_DEVERR_RANGE
+    assert_close(gpu[qo[1]:], ref[qo[1]:], "requests next to a misaligned page start, ps=%d" % ps)
+    kz, vz = k.clone(), v.clone()
+    kz[page * ps:(page + 1) * ps] = 0
+    vz[page * ps:(page + 1) * ps] = 0
+    st, refz, _ = oracle.extend(bits(q), bits(kz), bits(vz), r2t, rpi, lens, qo, kv_end, scale)
+    assert st == oracle.OK
+    assert_close(gpu[:qo[1]], refz[:qo[1]], "misaligned page start reads as zeros, ps=%d" % ps)
+    # request 1's row outside the table: a range error, the others exact
+    rpi_bad = np.array(rpi, dtype=np.int32, copy=True)
+    rpi_bad[1] = r2t.shape[0] + 3
+    e, gpu = call(_dev(r2t), _dev(rpi_bad))
+    assert e & B.PKV_DEVERR_RANGE
+    assert_close(gpu[:qo[1]], ref[:qo[1]], "request before a bad row, ps=%d" % ps)
+    assert_close(gpu[qo[2]:], ref[qo[2]:], "request after a bad row, ps=%d" % ps)

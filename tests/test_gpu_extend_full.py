@@ -69,12 +69,17 @@ def _spread(n, k, extra=()):
     return sorted(set(np.linspace(0, n - 1, num=min(n, k)).astype(np.int64).tolist() + [r for r in extra if r < n]))
 
 
-@pytest.mark.parametrize("name", ["llama3_8b_verify", "qwen3_0p6b_prefill", "hunyuan_image_spans"])
-def test_extend_recipe_at_full_size(B, name):
+@pytest.mark.parametrize("name,token_table", [("llama3_8b_verify", False), ("qwen3_0p6b_prefill", False),
+                                              ("hunyuan_image_spans", False), ("qwen3_0p6b_prefill", True)])
+def test_extend_recipe_at_full_size(B, name, token_table):
+    """The benchmarked steps at full size; prefill also with the pages read straight from
+    req_to_token (no pkv_build_indices launch)."""
     from paged_kv_cache_req_gb300.engine import ExtendStep
     from paged_kv_cache_req_gb300.workloads import make_extend_workload
     ew = make_extend_workload(name)
-    step = ExtendStep(ew, device="cuda")
+    step = ExtendStep(ew, device="cuda", token_table=token_table)
+    assert step.launches_per_step() == (2 if token_table else 3) + (1 if ew.segments is not None else 0) + \
+        (1 if step.ws_bytes > 0 else 0)
     step.run()
     torch.cuda.synchronize()
     assert step.check_errors() == 0
