@@ -204,7 +204,7 @@ typedef struct pkv_decode_args {
  * kv_chunk is 0); a request that a span boundary cuts is merged the same way.
  * For GQA with kv_chunk 0, pages of >= 8 keys (or VARLEN) and a batch so small
  * that even max_seq_len keys per request would give each of about two spans per
- * SM at most 128 tiles of 64 keys, the keys of each kv head's requests are cut
+ * SM (three at head_dim 64) at most 128 tiles of 64 keys, the keys of each kv head's requests are cut
  * the same way into equal spans (the same number for every kv head); the
  * workspace size then depends on the SM count, not on the batch.
  * Arithmetic: bf16 inputs, fp32 accumulation and softmax, bf16 output rounded

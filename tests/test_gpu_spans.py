@@ -1,7 +1,7 @@
 """GQA decode with equal spans of tiles (the split for small batches) against the oracle.
 
 When the library chooses the split (kv_chunk = 0) and even the longest requests
-would give each of about 2 x SMs spans only a few items, pkv_decode concatenates the
+would give each of about 2 x SMs spans (3 x SMs at head_dim 64) only a few items, pkv_decode concatenates the
 requests' rows of each kv head as tiles of 64 keys and cuts that sequence into equal
 spans;
 a row cut by a span boundary writes partials that a log-sum-exp merge combines,
@@ -37,11 +37,12 @@ def _r256(x):
 
 def _span_ws(hq, hkv, d):
     """Workspace of the span split: two partial slots per span, the same whole number of spans
-    per kv head (2 x SMs at most), and the span records."""
+    per kv head (2 x SMs at most, 3 x SMs at head_dim 64: one per CTA the SMs hold), and the
+    span records."""
     sm = torch.cuda.get_device_properties(0).multi_processor_count
     gc = min(hq // hkv, 16)
     units = hkv * (hq // hkv // gc)
-    spans = units * (2 * sm // units)
+    spans = units * ((3 if d == 64 else 2) * sm // units)
     return _r256(2 * spans * gc * d * 4) + _r256(2 * spans * gc * 4) + _r256((spans + 1) * 16)
 
 
