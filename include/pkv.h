@@ -66,7 +66,8 @@ typedef enum pkv_status {
 #define PKV_DEVERR_TIMEOUT 8  /* a device-side wait ran past its limit (pkv_set_wait_limit, ~2 s by
                                  default); outputs of the launch unspecified */
 
-#define PKV_ABI_VERSION 2
+/* 3: pkv_extend_args gained the token-table fields (req_to_token ... kv_start) at its end */
+#define PKV_ABI_VERSION 3
 
 /*
  * pkv_build_indices -- page lists from the token-granular table.

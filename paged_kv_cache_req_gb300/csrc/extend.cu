@@ -1173,10 +1173,11 @@ static bool make_plan(const pkv_extend_args *a, Plan &pl) {
         // whole tiles: a block's pieces are then never empty ((pieces - 1) x piece < keys)
         pl.chunk = (a->kv_chunk + kTile - 1) / kTile * kTile;
     } else {   // split the keys only when the query blocks alone leave SMs idle
-        const int64_t target = 2 * static_cast<int64_t>(sm_count());
+        // (an SM count of 0, when no device answers, plans as for one SM)
+        const int64_t target = 2 * std::max<int64_t>(1, sm_count());
         const int64_t groups = std::max<int64_t>(1, static_cast<int64_t>(a->num_kv_heads) *
                                                         std::max<int64_t>(a->batch, a->total_q / pl.T));
-        const int64_t want = (target + groups - 1) / groups;
+        const int64_t want = std::max<int64_t>(1, (target + groups - 1) / groups);
         int64_t c = (L + want - 1) / want;
         c = std::max<int64_t>(512, (c + kTile - 1) / kTile * kTile);
         // long rows of uneven length: cap an item at 4096 keys so no single item

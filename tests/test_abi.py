@@ -78,11 +78,26 @@ def test_extend_args_layout_matches_c(binding, tmp_path):
     a.head_dim, a.page_size = 128, 24                  # not a power of two
     assert binding._lib.pkv_extend(ctypes.byref(a), None, 0, ctypes.byref(flag), None) == binding.PKV_ERR_UNSUPPORTED
     assert binding._lib.pkv_extend_workspace_size(ctypes.byref(a)) == 0
+    # token-table layout: the table's shape and pointers are checked before any launch
+    dummy = ctypes.c_void_p(256).value
+    a.page_size, a.layout, a.total_q, a.num_slots = 16, binding.PKV_LAYOUT_REQ_TO_TOKEN, 4, 64
+    a.k_row_stride = a.v_row_stride = 4 * 128
+    a.q = a.k_pool = a.v_pool = a.out = a.qo_indptr = dummy
+    a.r2t_rows, a.r2t_width, a.r2t_row_stride = 2, 64, 32    # stride narrower than the rows
+    assert binding._lib.pkv_extend(ctypes.byref(a), None, 0, ctypes.byref(flag), None) == binding.PKV_ERR_INVALID_ARG
+    assert b"req_to_token" in binding._lib.pkv_last_error()
+    a.r2t_row_stride = 64
+    a.req_to_token = a.req_pool_idx = a.seq_lens = None       # the table itself missing
+    assert binding._lib.pkv_extend(ctypes.byref(a), None, 0, ctypes.byref(flag), None) == binding.PKV_ERR_INVALID_ARG
+    assert b"token-table" in binding._lib.pkv_last_error()
+    a.req_to_token = a.req_pool_idx = a.seq_lens = dummy      # valid: the plan has a size
+    a.max_seq_len = 64
+    assert binding._lib.pkv_extend_workspace_size(ctypes.byref(a)) >= 256
     assert flag.value == 0
 
 
 def test_status_strings_and_version(binding):
-    assert binding.pkv_abi_version() == 2
+    assert binding.pkv_abi_version() == 3
     assert binding.pkv_status_string(0) == "ok"
     assert binding.pkv_status_string(2) == "unsupported shape"
 
