@@ -341,7 +341,7 @@ typedef struct pkv_extend_args {
     const int32_t *seq_lens;         /* BLOCK_TABLE and REQ_TO_TOKEN [B] */
     void *out;                 /* bf16 [total_q, Hq, head_dim] */
     float *lse;                /* fp32 [total_q, Hq] natural-log softmax denominators; nullable */
-    /* REQ_TO_TOKEN (the same fields as pkv_decode_args) */
+    /* REQ_TO_TOKEN (added in ABI version 3; the same fields as pkv_decode_args) */
     const int32_t *req_to_token;     /* int32 [r2t_rows, r2t_row_stride] */
     int64_t r2t_rows;
     int64_t r2t_row_stride;
