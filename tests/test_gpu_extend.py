@@ -291,3 +291,50 @@ def test_extend_token_table_flags_bad_rows_and_page_starts(B, ps):
     assert e & B.PKV_DEVERR_RANGE
     assert_close(gpu[:qo[1]], ref[:qo[1]], "request before a bad row, ps=%d" % ps)
     assert_close(gpu[qo[2]:], ref[qo[2]:], "request after a bad row, ps=%d" % ps)
+
+
+def test_extend_token_table_with_start_columns(B):
+    """Token-table layout with kv_start: request b's keys are columns s_b .. s_b + L_b - 1 of its
+    row. The oracle runs on the same slots moved to column 0; a start that is not a multiple of
+    the page size raises PKV_DEVERR_RANGE and only that request is left out."""
+    dev = torch.device("cuda")
+    ps, lens, nq = 16, [200, 77, 130], [16, 5, 130]
+    starts = [32, 0, 160]
+    rng = np.random.default_rng(19)
+    num_pages = sum(-(-L // ps) for L in lens) + 8
+    r2t, rpi = paged_table(rng, lens, ps, num_pages, kv_start=starts)
+    shifted = np.zeros_like(r2t)
+    for b, (L, st_) in enumerate(zip(lens, starts)):
+        shifted[rpi[b], :L] = r2t[rpi[b], st_:st_ + L]
+    gen = torch.Generator().manual_seed(19)
+    k = torch.randn((num_pages * ps, 4, 128), generator=gen).to(torch.bfloat16)
+    v = torch.randn((num_pages * ps, 4, 128), generator=gen).to(torch.bfloat16)
+    qo = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    q = torch.randn((int(qo[-1]), 16, 128), generator=gen).to(torch.bfloat16)
+    scale = 1 / math.sqrt(128)
+    kv_end = np.concatenate([np.arange(L - n, L) + 1 for L, n in zip(lens, nq)]).astype(np.int32)
+    st, ref, ref_lse = oracle.extend(bits(q), bits(k), bits(v), shifted, rpi, lens, qo, kv_end, scale)
+    assert st == oracle.OK
+
+    def call(start_cols):
+        out = torch.zeros(tuple(q.shape), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((q.shape[0], 16), dtype=torch.float32, device=dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        args = B.make_extend_args(B.PKV_LAYOUT_REQ_TO_TOKEN, q.to(dev), k.to(dev), v.to(dev), out, _dev(qo),
+                                  page_size=ps, sm_scale=scale, max_seq_len=max(lens), seq_lens=_dev(lens),
+                                  req_to_token=_dev(r2t), req_pool_idx=_dev(rpi), kv_start=_dev(start_cols),
+                                  lse=lse, kv_chunk=64)
+        ws = torch.empty(max(B.pkv_extend_workspace_size(args), 256), dtype=torch.uint8, device=dev)
+        B.pkv_extend(args, ws, err)
+        torch.cuda.synchronize()
+        return int(err.item()), bf16_to_f64(out), lse.double().cpu().numpy()
+
+    e, gpu, g_lse = call(starts)
+    assert e == 0
+    assert_close(gpu, ref, "token table with start columns")
+    assert_close(g_lse, ref_lse, "token table with start columns lse")
+    bad = list(starts)
+    bad[0] = 33                                  # not a multiple of the page size
+    e, gpu, _ = call(bad)
+    assert e & B.PKV_DEVERR_RANGE
+    assert_close(gpu[qo[1]:], ref[qo[1]:], "requests next to a misaligned start")
