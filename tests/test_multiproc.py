@@ -79,20 +79,24 @@ def test_reference_arm_runs_on_rank0_only(rank):
         assert lines == []
 
 
-@pytest.mark.parametrize("workload", ["tiny_gqa", "qwen3_0p6b_prefill", "encoder_merge"])
-def test_reference_arm_prints_the_config_of_the_gpu_arm(workload):
-    """Both arms describe one workload with the same `config` object (built on the host)."""
+@pytest.mark.parametrize("workload,fused", [("tiny_gqa", False), ("qwen3_0p6b_prefill", False),
+                                            ("qwen3_0p6b_prefill", True), ("encoder_merge", False)])
+def test_reference_arm_prints_the_config_of_the_gpu_arm(workload, fused):
+    """Both arms describe one workload with the same `config` object (built on the host),
+    including how the multi-query step finds its pages (--fused: straight from req_to_token)."""
     import bench
     from paged_kv_cache_req_gb300.workloads import make_encoder_merge, make_extend_workload, make_workload
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
-                          workload, "--steps", "1", "--warmup", "3", "--ref-key-heads", "2000000"],
+                          workload, "--steps", "1", "--warmup", "3", "--ref-key-heads", "2000000"] +
+                         (["--fused"] if fused else []),
                          capture_output=True, text=True, timeout=600)
     assert out.returncode == 0, out.stderr[-2000:]
     d = json.loads([l for l in out.stdout.splitlines() if l.strip()][-1])
     if workload == "encoder_merge":
         want = bench.merge_config(make_encoder_merge(seed=0), 1)
     elif workload in bench.EXTEND_WORKLOADS:
-        want = bench.extend_config(make_extend_workload(workload, seed=0), 1)
+        want = bench.extend_config(make_extend_workload(workload, seed=0), 1, token_table=fused)
+        assert want["pages"].startswith("read from req_to_token" if fused else "kv_indptr")
     else:
         want = bench.decode_config(make_workload(workload, seed=0), "paged", False, 1)
     assert d["config"] == json.loads(json.dumps(want))
